@@ -1,0 +1,400 @@
+#!/usr/bin/env python
+"""Throughput of the KDA mixer on GB300: chunked prefill and decode tokens/s.
+
+One step = one pass of the whole mixer hot path on synthetic inputs:
+  * a fused-mixer prefill, B=1, T=65536, H=32, dk=dv=128, chunk 64: width-4
+    causal SiLU convs on q, k, v, in-kernel q/k L2 norm, chunked KDA with an
+    FP32 state, sigmoid output gate, bf16 activations in and out;
+  * one decode step for 256 independent sequences, H=32, d=128: conv window
+    update, L2 norm, FP32 state read-modify-write ([256,32,128,128] = 512 MiB),
+    gate.
+value = (prefill tokens + decode tokens) per step / step time, device-resident
+inputs; the "prefill" and "decode" objects give each part on its own with its
+roofline.  With --gpus N under torchrun every rank runs its own replica of the
+step (heads and sequences never interact, so there is no collective): weak
+scaling, max time over ranks.
+
+--impl reference times the CPU oracle (the reference arm for this method) on a
+bounded sample of the same workload on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "KDA prefill tokens/s & decode tokens/s at 1 GB300; % of tensor/HBM roofline"
+PREFILL = dict(T=65536, H=32, d=128, chunk=64, W=4)
+DECODE = dict(N=256, H=32, d=128, W=4)
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=3)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--e2e-steps", type=int, default=3)
+    p.add_argument("--cpu-sample-tokens", type=int, default=16384,
+                   help="prefill tokens (all heads) the CPU baseline runs; scaled to the full workload")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    return p.parse_args()
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            m = json.load(f)
+        return dict(hbm=float(m["hbm_gbs"]), bf16=float(m["bf16_tflops"]),
+                    bf16_sustained=float(m.get("bf16_tflops_sustained", m["bf16_tflops"])), src="measured")
+    except Exception:
+        return dict(hbm=6800.0, bf16=1900.0, bf16_sustained=1700.0, src="fallback")
+
+
+# ---- algorithmic work (bytes that must cross HBM, flops of the chunked form) ----
+
+def prefill_work(T, H, d, chunk, W, N=1):
+    dk = dv = d
+    per_tok_head = 2 * (2 * dk + dv) + 4 * dk + 4 + 2 * dv + 2 * dv    # q,k,v bf16; g; beta; gate; out bf16
+    D = 2 * H * dk + H * dv
+    bytes_ = T * H * per_tok_head + N * H * dk * dv * 4 + 2 * N * (W - 1) * D * 4 + D * W * 4
+    flops = T * H * (10 * chunk * d + 6 * d * d) + T * D * 2 * W
+    return bytes_, flops
+
+
+def decode_work(N, H, d, W):
+    dk = dv = d
+    D = 2 * H * dk + H * dv
+    per_nh = 2 * 4 * dk * dv + 2 * (2 * dk + dv) + 4 * dk + 4 + 2 * dv + 2 * dv
+    bytes_ = N * H * per_nh + 2 * N * (W - 1) * D * 4 + D * W * 4
+    flops = N * H * (7 * dk * dv + 2 * W * (2 * dk + dv))
+    return bytes_, flops
+
+
+# ---- clocks during the timed region ----
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu_id), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.t.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[4:8]):
+                if val.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": [], "samples": 0}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---- the GPU arm ----
+
+def make_inputs(torch, dev, seed):
+    """Seeded synthetic inputs drawn on the device with the workload recipe
+    (q,k,v,gate ~ N(0,1) bf16; g = -softplus(N(0,1)); beta = sigmoid(N(0,1));
+    conv weights ~ N(0, 0.5); decode state ~ N(0, 0.02); conv windows ~ N(0,1))."""
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(seed)
+    f32, bf16 = torch.float32, torch.bfloat16
+
+    def n(shape, std=1.0, dt=f32):
+        return (torch.randn(shape, generator=gen, device=dev, dtype=f32) * std).to(dt)
+
+    T, H, d, W = PREFILL["T"], PREFILL["H"], PREFILL["d"], PREFILL["W"]
+    D = 3 * H * d
+    P = dict(q=n((T, H, d), dt=bf16), k=n((T, H, d), dt=bf16), v=n((T, H, d), dt=bf16),
+             g=-torch.nn.functional.softplus(n((T, H, d))), beta=torch.sigmoid(n((T, H))),
+             gate=n((T, H, d), dt=bf16), conv_w=n((D, W), 0.5), conv_state=torch.zeros((1, W - 1, D), device=dev))
+    N, Hd, dd, Wd = DECODE["N"], DECODE["H"], DECODE["d"], DECODE["W"]
+    Dd = 3 * Hd * dd
+    Dc = dict(q=n((N, Hd, dd), dt=bf16), k=n((N, Hd, dd), dt=bf16), v=n((N, Hd, dd), dt=bf16),
+              g=-torch.nn.functional.softplus(n((N, Hd, dd))), beta=torch.sigmoid(n((N, Hd))),
+              gate=n((N, Hd, dd), dt=bf16), conv_w=n((Dd, Wd), 0.5),
+              conv_state=n((N, Wd - 1, Dd)).to(bf16).to(f32), state=n((N, Hd, dd, dd), 0.02))
+    return P, Dc
+
+
+def run_ours(args, rank, world, dev, torch):
+    import hybrid_linear_attention_rule_gb300 as K
+    K.load_library()
+    pk = peaks()
+    P, Dc = make_inputs(torch, dev, seed=1000 + rank)
+    T, H, d, C, W = PREFILL["T"], PREFILL["H"], PREFILL["d"], PREFILL["chunk"], PREFILL["W"]
+    N, Hd, dd, Wd = DECODE["N"], DECODE["H"], DECODE["d"], DECODE["W"]
+    cu_h = torch.tensor([0, T], dtype=torch.int32)
+    cu_d = cu_h.to(dev)
+    out_p = torch.empty((T, H, d), dtype=torch.bfloat16, device=dev)
+    fs = torch.empty((1, H, d, d), dtype=torch.float32, device=dev)
+    out_d = torch.empty((N, Hd, dd), dtype=torch.bfloat16, device=dev)
+    ws = torch.zeros(K.k3kda_prefill_workspace_size(1, T, H, d, d, C, K.BF16, True), dtype=torch.uint8, device=dev)
+    scale = d ** -0.5
+    stream = torch.cuda.current_stream()
+
+    def prefill_call(p, out, f):
+        K.k3kda_prefill(p["q"], p["k"], p["v"], p["g"], p["beta"], None, cu_d, cu_h, 1, T, H, d, d, C, scale, True,
+                        p["conv_w"], p["conv_state"], W, p["gate"], out, f, ws, stream)
+
+    def decode_call(c, out):
+        K.k3kda_decode_step(c["q"], c["k"], c["v"], c["g"], c["beta"], c["gate"], c["conv_w"], c["conv_state"],
+                            c["state"], N, Hd, dd, dd, Wd, scale, True, out, stream)
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    for _ in range(args.warmup):
+        prefill_call(P, out_p, fs)
+        decode_call(Dc, out_d)
+    torch.cuda.synchronize()
+    st = K.k3kda_workspace_status(ws)
+    if st != 0:
+        raise RuntimeError(f"prefill workspace status {st}")
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    barrier()
+    torch.cuda.synchronize()
+    n0 = K.k3kda_launch_count()
+    gpu_id = os.environ.get("LOCAL_RANK", "0")
+    with ClockSampler(gpu_id) as clk:
+        t_start = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        t_start.record(stream)
+        for s in range(args.steps):
+            ev[s][0].record(stream)
+            prefill_call(P, out_p, fs)
+            ev[s][1].record(stream)
+            decode_call(Dc, out_d)
+            ev[s][2].record(stream)
+        t_end.record(stream)
+        torch.cuda.synchronize()
+    launches = K.k3kda_launch_count() - n0
+    barrier()
+    total_ms = t_start.elapsed_time(t_end)
+    pre_ms = sum(e[0].elapsed_time(e[1]) for e in ev) / args.steps
+    dec_ms = sum(e[1].elapsed_time(e[2]) for e in ev) / args.steps
+    if world > 1:
+        t = torch.tensor([total_ms, pre_ms, dec_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms, pre_ms, dec_ms = (float(x) for x in t.tolist())
+    ms_per_step = total_ms / args.steps
+    tokens_per_step = T + N
+
+    pb, pf = prefill_work(T, H, d, C, W)
+    db, df = decode_work(N, Hd, dd, Wd)
+    pre_tok_s = T / (pre_ms / 1e3)
+    dec_tok_s = N / (dec_ms / 1e3)
+    roof_p = {"bound": "hbm", "achieved": pb / (pre_ms / 1e3) / 1e9, "peak": pk["hbm"], "unit": "GB/s",
+              "traffic": PREFILL_TRAFFIC_PER_LAUNCH}
+    roof_p["frac"] = roof_p["achieved"] / roof_p["peak"]
+    roof_p["tensor"] = {"achieved_tflops": pf / (pre_ms / 1e3) / 1e12, "peak": pk["bf16"],
+                        "frac": pf / (pre_ms / 1e3) / 1e12 / pk["bf16"]}
+    roof_d = {"bound": "hbm", "achieved": db / (dec_ms / 1e3) / 1e9, "peak": pk["hbm"], "unit": "GB/s",
+              "traffic": DECODE_TRAFFIC_PER_LAUNCH}
+    roof_d["frac"] = roof_d["achieved"] / roof_d["peak"]
+
+    res = {
+        "metric": METRIC, "value": world * tokens_per_step / (ms_per_step / 1e3), "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "io_dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "KDA mixer step: fused prefill T=65536 H=32 d=128 chunk64 conv4 gate + "
+                               "decode step N=256 H=32 d=128 conv4 gate",
+                   "prefill": dict(PREFILL, B=1, l2norm=True, gate=True, out="bf16"),
+                   "decode": dict(DECODE, l2norm=True, gate=True, state="fp32", out="bf16"),
+                   "l2_flush": "inputs larger than L2 (prefill 3.8 GB, decode 1.2 GB per step)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "prefill": {"tokens_per_s": world * pre_tok_s, "ms": pre_ms, "algorithmic_bytes": pb,
+                    "algorithmic_flops": pf, "roofline": roof_p},
+        "decode": {"tokens_per_s": world * dec_tok_s, "ms": dec_ms, "algorithmic_bytes": db,
+                   "algorithmic_flops": df, "roofline": roof_d},
+        "roofline": roof_p,
+        "peaks_source": pk["src"],
+        "gpu_launches": launches,
+        "clocks": clk.summary(),
+    }
+    if not args.no_e2e:
+        res["e2e"] = run_e2e(args, K, torch, dev, P, Dc, prefill_call, decode_call, out_p, fs, out_d, world, barrier)
+    return res
+
+
+def run_e2e(args, K, torch, dev, P, Dc, prefill_call, decode_call, out_p, fs, out_d, world, barrier):
+    """Same step through the C ABI, starting from pinned HOST buffers: every step copies
+    its inputs host->device and reads the outputs (prefill out, decode out, the updated
+    decode state) back to the host inside the timed region."""
+    hostP = {k: v.cpu().pin_memory() for k, v in P.items()}
+    hostD = {k: v.cpu().pin_memory() for k, v in Dc.items()}
+    devP = {k: torch.empty_like(v) for k, v in P.items()}
+    devD = {k: torch.empty_like(v) for k, v in Dc.items()}
+    res_p = torch.empty(out_p.shape, dtype=out_p.dtype).pin_memory()
+    res_d = torch.empty(out_d.shape, dtype=out_d.dtype).pin_memory()
+    res_s = torch.empty(Dc["state"].shape, dtype=torch.float32).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in list(hostP.values()) + list(hostD.values()))
+    d2h = sum(v.numel() * v.element_size() for v in (res_p, res_d, res_s))
+
+    def step():
+        for k, v in hostP.items():
+            devP[k].copy_(v, non_blocking=True)
+        for k, v in hostD.items():
+            devD[k].copy_(v, non_blocking=True)
+        prefill_call(devP, out_p, fs)
+        decode_call(devD, out_d)
+        res_p.copy_(out_p, non_blocking=True)
+        res_d.copy_(out_d, non_blocking=True)
+        res_s.copy_(devD["state"], non_blocking=True)
+
+    step()
+    torch.cuda.synchronize()
+    n = max(1, args.e2e_steps)
+    barrier()
+    t0 = time.perf_counter()
+    for _ in range(n):
+        step()
+    torch.cuda.synchronize()
+    dt = (time.perf_counter() - t0) / n
+    if world > 1:
+        t = torch.tensor([dt], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        dt = float(t.item())
+    return {"value": world * (PREFILL["T"] + DECODE["N"]) / dt, "unit": "tokens/s", "ms_per_step": dt * 1e3,
+            "steps": n, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+# Measured DRAM bytes per launch (ncu dram__bytes_read.sum + dram__bytes_write.sum)
+# of the current kernels, or None when not yet captured for this kernel version.
+PREFILL_TRAFFIC_PER_LAUNCH = None
+DECODE_TRAFFIC_PER_LAUNCH = None
+
+
+# ---- the CPU oracle (baseline leg and the reference arm) ----
+
+def cpu_oracle_sample(prefill_tokens, decode_seqs, seed=0):
+    """Time the oracle on the first `prefill_tokens` tokens of the fused-mixer workload
+    (all 32 heads) and on `decode_seqs` sequences of the decode workload; return the
+    seconds each took and the threads used."""
+    import kda_inputs as KI
+    import oracle as O
+    O.load()
+    c = KI.fused_mixer(seed=seed, T=prefill_tokens, H=PREFILL["H"], d=PREFILL["d"], W=PREFILL["W"])
+    t0 = time.perf_counter()
+    O.mixer(c.q, c.k, c.v, c.g, c.beta, gate=c.gate, conv_w=c.conv_w, use_qk_l2norm=True)
+    tp = time.perf_counter() - t0
+    dc = KI.decode_case(seed=seed, N=decode_seqs, H=DECODE["H"], d=DECODE["d"], W=DECODE["W"])
+    t0 = time.perf_counter()
+    O.decode_step(dc.q, dc.k, dc.v, dc.g, dc.beta, dc.state, gate=dc.gate, conv_w=dc.conv_w,
+                  conv_state=dc.conv_state)
+    td = time.perf_counter() - t0
+    return tp, td, O.num_threads()
+
+
+def cpu_value(tp, td, prefill_tokens, decode_seqs):
+    """Composite tokens/s of the oracle, scaled to the full step's token counts."""
+    t_step = tp * PREFILL["T"] / prefill_tokens + td * DECODE["N"] / decode_seqs
+    return (PREFILL["T"] + DECODE["N"]) / t_step, t_step
+
+
+def run_reference(args):
+    tok, seqs = max(256, args.cpu_sample_tokens // 4), 64
+    cpu_oracle_sample(64, 4)                                # load + warm the library
+    for _ in range(args.warmup):
+        cpu_oracle_sample(256, 8)
+    times = []
+    for s in range(args.steps):
+        tp, td, th = cpu_oracle_sample(tok, seqs, seed=s)
+        times.append(cpu_value(tp, td, tok, seqs)[1])
+    t_step = float(np.mean(times))
+    v = (PREFILL["T"] + DECODE["N"]) / t_step
+    sample = (f"each step: oracle fused mixer on the first {tok} of {PREFILL['T']} tokens (all 32 heads) and "
+              f"decode on {seqs} of {DECODE['N']} sequences, times scaled to the full step")
+    return {"impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_step * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "KDA mixer step: fused prefill T=65536 H=32 d=128 chunk64 conv4 gate + "
+                                   "decode step N=256 H=32 d=128 conv4 gate", "prefill": PREFILL, "decode": DECODE},
+            "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": th, "kind": "oracle", "sample": sample},
+            "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)))
+        return
+    import torch
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=dev)
+    # the CPU baseline runs before any CUDA work of the timed arm, on rank 0 at N=1 only
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        tok, seqs = args.cpu_sample_tokens, 64
+        tp, td, th = cpu_oracle_sample(tok, seqs)
+        v, _ = cpu_value(tp, td, tok, seqs)
+        cpu = {"value": v, "unit": "tokens/s", "cores": th, "kind": "oracle",
+               "sample": f"oracle fused mixer on the first {tok} of {PREFILL['T']} tokens (all 32 heads, "
+                         f"{tp:.1f} s) + decode on {seqs} of {DECODE['N']} sequences ({td:.1f} s), "
+                         f"scaled to the full step"}
+    res = run_ours(args, rank, world, dev, torch)
+    res["cpu_baseline"] = cpu
+    if rank == 0:
+        print(json.dumps(res))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

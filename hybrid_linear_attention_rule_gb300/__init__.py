@@ -1,0 +1,228 @@
+"""GB300 (sm_103a) KDA mixer: Python binding of libk3kda.
+
+The functions named ``k3kda_*`` are the C ABI of ``include/k3kda.h``, one for
+one, taking torch CUDA tensors (or None) and marshalling their device pointers
+and sizes; every step of the computation runs in the library's CUDA kernels.
+PyTorch only provides device memory and the current stream.  A nonzero status
+raises ``K3KDAError``.  If the CUDA library is missing and cannot be built,
+importing the binding's functions raises: there is no CPU fallback.
+
+Layouts (row-major, contiguous): q, k, g [T, H, dk]; v, gate, out [T, H, dv];
+beta [T, H]; states [N, H, dk, dv] fp32; cu_seqlens int32 [N+1]; conv weights
+[2*H*dk + H*dv, W] fp32; conv state [N, W-1, 2*H*dk + H*dv] fp32.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+__all__ = ["K3KDAError", "load_library", "library_path", "F32", "BF16", "L2_EPS",
+           "k3kda_version", "k3kda_status_string", "k3kda_launch_count", "k3kda_short_conv",
+           "k3kda_prefill_workspace_size", "k3kda_prefill", "k3kda_workspace_status",
+           "k3kda_decode_step", "prefill", "decode_step", "short_conv"]
+
+F32, BF16 = 0, 1
+L2_EPS = 1e-6
+_STATUS = {0: "OK", -1: "INVALID_ARG", -2: "UNSUPPORTED", -3: "ALIGNMENT", -4: "WORKSPACE",
+           -5: "CUDA", -6: "TIMEOUT"}
+
+_lib = None
+_lock = threading.Lock()
+
+
+class K3KDAError(RuntimeError):
+    def __init__(self, fn, status, detail=""):
+        self.status = status
+        super().__init__(f"{fn} failed: {_STATUS.get(status, status)} ({status}) {detail}".rstrip())
+
+
+def library_path() -> str:
+    from . import build as _b
+    return _b.LIB
+
+
+def load_library(build_if_missing: bool = True):
+    """Load libk3kda.so (building it with nvcc when missing or stale)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        from . import build as _b
+        if build_if_missing and not _b.up_to_date():
+            _b.build()
+        if not os.path.exists(_b.LIB):
+            raise RuntimeError(f"libk3kda.so not found at {_b.LIB}; build it with "
+                               "hybrid_linear_attention_rule_gb300.build.build()")
+        lib = ctypes.CDLL(_b.LIB)
+        P, I, F, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+        lib.k3kda_version.restype = I
+        lib.k3kda_status_string.restype = ctypes.c_char_p
+        lib.k3kda_status_string.argtypes = [I]
+        lib.k3kda_last_error.restype = ctypes.c_char_p
+        lib.k3kda_launch_count.restype = ctypes.c_longlong
+        lib.k3kda_short_conv.argtypes = [P, I, P, P, P, I, I, I, I, I, P, I, P]
+        lib.k3kda_short_conv.restype = I
+        lib.k3kda_prefill_workspace_size.argtypes = [I, I, I, I, I, I, I, I]
+        lib.k3kda_prefill_workspace_size.restype = Z
+        lib.k3kda_prefill.argtypes = [P, P, P, I, P, P, P, P, P, I, I, I, I, I, I, F, I, P, P, P, I, P,
+                                      P, Z, P]
+        lib.k3kda_prefill.restype = I
+        lib.k3kda_workspace_status.argtypes = [P, P]
+        lib.k3kda_workspace_status.restype = I
+        lib.k3kda_decode_step.argtypes = [P, P, P, I, P, P, P, P, P, P, I, I, I, I, I, F, I, P, I, P]
+        lib.k3kda_decode_step.restype = I
+        _lib = lib
+        return lib
+
+
+class _ConvArgs(ctypes.Structure):
+    _fields_ = [("weight", ctypes.c_void_p), ("conv_state", ctypes.c_void_p), ("W", ctypes.c_int)]
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("expected a torch.Tensor or None")
+    if not t.is_cuda:
+        raise ValueError("k3kda: tensors must live on a CUDA device (no CPU path exists)")
+    if not t.is_contiguous():
+        raise ValueError("k3kda: tensors must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _dtype(t):
+    if t.dtype == torch.bfloat16:
+        return BF16
+    if t.dtype == torch.float32:
+        return F32
+    raise TypeError(f"k3kda: unsupported element type {t.dtype}")
+
+
+def _stream(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(fn, st):
+    if st != 0:
+        lib = load_library()
+        raise K3KDAError(fn, st, lib.k3kda_last_error().decode() if st == -5 else "")
+
+
+# ---- the C ABI, one for one ------------------------------------------------
+
+def k3kda_version() -> int:
+    return int(load_library().k3kda_version())
+
+
+def k3kda_launch_count() -> int:
+    return int(load_library().k3kda_launch_count())
+
+
+def k3kda_status_string(status: int) -> str:
+    return load_library().k3kda_status_string(int(status)).decode()
+
+
+def k3kda_short_conv(x, weight, conv_state, cu_seqlens, N, T, D, W, apply_silu, out, stream=None):
+    lib = load_library()
+    st = lib.k3kda_short_conv(_ptr(x), _dtype(x), _ptr(weight), _ptr(conv_state), _ptr(cu_seqlens),
+                              int(N), int(T), int(D), int(W), int(bool(apply_silu)), _ptr(out),
+                              _dtype(out), _stream(stream))
+    _check("k3kda_short_conv", st)
+
+
+def k3kda_prefill_workspace_size(N, T, H, dk, dv, chunk, in_dtype, has_conv) -> int:
+    return int(load_library().k3kda_prefill_workspace_size(int(N), int(T), int(H), int(dk), int(dv),
+                                                           int(chunk), int(in_dtype), int(bool(has_conv))))
+
+
+def k3kda_prefill(q, k, v, g, beta, initial_state, cu_seqlens, cu_seqlens_host, N, T, H, dk, dv, chunk,
+                  scale, use_qk_l2norm, conv_weight, conv_state, conv_W, gate, out, final_state,
+                  workspace, stream=None):
+    """cu_seqlens_host: a CPU int32 tensor (or None), passed as the host copy."""
+    lib = load_library()
+    conv = None
+    if conv_weight is not None:
+        conv = ctypes.byref(_ConvArgs(_ptr(conv_weight), _ptr(conv_state), int(conv_W)))
+    hcu = None
+    if cu_seqlens_host is not None:
+        if cu_seqlens_host.is_cuda or cu_seqlens_host.dtype != torch.int32 or not cu_seqlens_host.is_contiguous():
+            raise ValueError("cu_seqlens_host must be a contiguous CPU int32 tensor")
+        hcu = ctypes.c_void_p(cu_seqlens_host.data_ptr())
+    st = lib.k3kda_prefill(_ptr(q), _ptr(k), _ptr(v), _dtype(q), _ptr(g), _ptr(beta), _ptr(initial_state),
+                           _ptr(cu_seqlens), hcu, int(N), int(T), int(H), int(dk), int(dv), int(chunk),
+                           float(scale), int(bool(use_qk_l2norm)), conv, _ptr(gate), _ptr(out), _dtype(out),
+                           _ptr(final_state), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                           _stream(stream))
+    _check("k3kda_prefill", st)
+
+
+def k3kda_workspace_status(workspace, stream=None) -> int:
+    return int(load_library().k3kda_workspace_status(_ptr(workspace), _stream(stream)))
+
+
+def k3kda_decode_step(q, k, v, g, beta, gate, conv_weight, conv_state, state, N, H, dk, dv, W, scale,
+                      use_qk_l2norm, out, stream=None):
+    lib = load_library()
+    st = lib.k3kda_decode_step(_ptr(q), _ptr(k), _ptr(v), _dtype(q), _ptr(g), _ptr(beta), _ptr(gate),
+                               _ptr(conv_weight), _ptr(conv_state), _ptr(state), int(N), int(H), int(dk),
+                               int(dv), int(W), float(scale), int(bool(use_qk_l2norm)), _ptr(out),
+                               _dtype(out), _stream(stream))
+    _check("k3kda_decode_step", st)
+
+
+# ---- conveniences: allocate outputs with torch, then call the ABI ----------
+
+def prefill(q, k, v, g, beta, initial_state=None, cu_seqlens=None, chunk=64, scale=None,
+            use_qk_l2norm=True, conv_weight=None, conv_state=None, gate=None, out_dtype=None,
+            return_final_state=True, workspace=None, stream=None):
+    """Allocate out / final_state / workspace and run k3kda_prefill.  cu_seqlens may be
+    a CPU or CUDA int32 tensor (both copies are passed).  Returns (out, final_state)."""
+    T, H, dk = q.shape
+    dv = v.shape[2]
+    dev = q.device
+    if cu_seqlens is None:
+        cu_h = torch.tensor([0, T], dtype=torch.int32)
+    else:
+        cu_h = cu_seqlens.to("cpu", torch.int32).contiguous()
+    cu_d = cu_h.to(dev)
+    N = cu_h.numel() - 1
+    out = torch.empty((T, H, dv), dtype=out_dtype or q.dtype, device=dev)
+    fs = torch.empty((N, H, dk, dv), dtype=torch.float32, device=dev) if return_final_state else None
+    W = 0 if conv_weight is None else conv_weight.shape[1]
+    if workspace is None:
+        nbytes = k3kda_prefill_workspace_size(N, T, H, dk, dv, chunk, _dtype(q), conv_weight is not None)
+        workspace = torch.zeros(nbytes, dtype=torch.uint8, device=dev)
+    k3kda_prefill(q, k, v, g, beta, initial_state, cu_d, cu_h, N, T, H, dk, dv, chunk,
+                  dk ** -0.5 if scale is None else scale, use_qk_l2norm, conv_weight, conv_state, W,
+                  gate, out, fs, workspace, stream)
+    return out, fs
+
+
+def decode_step(q, k, v, g, beta, state, gate=None, conv_weight=None, conv_state=None, scale=None,
+                use_qk_l2norm=True, out_dtype=None, stream=None):
+    """Run k3kda_decode_step; state and conv_state are updated in place.  Returns out."""
+    N, H, dk = q.shape
+    dv = v.shape[2]
+    out = torch.empty((N, H, dv), dtype=out_dtype or q.dtype, device=q.device)
+    W = 0 if conv_weight is None else conv_weight.shape[1]
+    k3kda_decode_step(q, k, v, g, beta, gate, conv_weight, conv_state, state, N, H, dk, dv, W,
+                      dk ** -0.5 if scale is None else scale, use_qk_l2norm, out, stream)
+    return out
+
+
+def short_conv(x, weight, conv_state=None, cu_seqlens=None, apply_silu=True, out_dtype=None, stream=None):
+    """Run k3kda_short_conv over x [T, D]; conv_state is updated in place.  Returns out."""
+    T, D = x.shape
+    W = weight.shape[1]
+    cu = None if cu_seqlens is None else cu_seqlens.to(x.device, torch.int32)
+    N = 1 if cu is None else cu.numel() - 1
+    out = torch.empty((T, D), dtype=out_dtype or x.dtype, device=x.device)
+    k3kda_short_conv(x, weight, conv_state, cu, N, T, D, W, apply_silu, out, stream)
+    return out

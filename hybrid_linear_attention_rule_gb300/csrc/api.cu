@@ -1,0 +1,213 @@
+// api.cu -- the C ABI of libk3kda (declared in include/k3kda.h): argument
+// validation on the host, workspace accounting and kernel launches on the
+// caller's stream.  No entry point allocates, synchronises (except
+// k3kda_workspace_status, whose job it is), throws or prints.
+#include <stdio.h>
+#include <atomic>
+#include <string.h>
+
+#include "common.cuh"
+
+namespace k3kda {
+size_t prefill_f32_smem_bytes(int chunk, int dk, int dv);
+bool tc_prefill_supported(int in_bf16, int dk, int dv, int chunk);
+size_t tc_prefill_workspace(int N, int H);
+cudaError_t launch_prefill_tc(const PrefillArgs &a, const int32_t *order, cudaStream_t s);
+}  // namespace k3kda
+
+using namespace k3kda;
+
+namespace {
+
+std::atomic<long long> g_launches{0};
+
+thread_local char g_last_error[256] = "";
+
+int cuda_status(cudaError_t e) {
+    if (e == cudaSuccess) return K3KDA_OK;
+    snprintf(g_last_error, sizeof(g_last_error), "%s: %s", cudaGetErrorName(e), cudaGetErrorString(e));
+    return K3KDA_ERR_CUDA;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool head_dim_ok(int d) { return d >= 16 && d <= 128 && d % 16 == 0; }
+bool dtype_ok(int t) { return t == K3KDA_F32 || t == K3KDA_BF16; }
+
+// Host-side check of a host copy of cu_seqlens.
+bool cu_ok(const int32_t *cu, int N, int T) {
+    if (cu[0] != 0 || cu[N] != T) return false;
+    for (int n = 0; n < N; ++n)
+        if (cu[n + 1] < cu[n]) return false;
+    return true;
+}
+
+constexpr size_t kStatusBytes = 256;
+
+size_t round256(size_t b) { return (b + 255) & ~size_t(255); }
+
+size_t conv_buffer_bytes(int T, int H, int dk, int dv) {
+    return round256((size_t)T * (2 * (size_t)H * dk + (size_t)H * dv) * sizeof(float));
+}
+
+}  // namespace
+
+void k3kda::count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+extern "C" {
+
+long long k3kda_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+
+const char *k3kda_status_string(int status) {
+    switch (status) {
+        case K3KDA_OK: return "K3KDA_OK";
+        case K3KDA_ERR_INVALID_ARG: return "K3KDA_ERR_INVALID_ARG";
+        case K3KDA_ERR_UNSUPPORTED: return "K3KDA_ERR_UNSUPPORTED";
+        case K3KDA_ERR_ALIGNMENT: return "K3KDA_ERR_ALIGNMENT";
+        case K3KDA_ERR_WORKSPACE: return "K3KDA_ERR_WORKSPACE";
+        case K3KDA_ERR_CUDA: return "K3KDA_ERR_CUDA";
+        case K3KDA_ERR_TIMEOUT: return "K3KDA_ERR_TIMEOUT";
+        default: return "K3KDA_UNKNOWN_STATUS";
+    }
+}
+
+int k3kda_version(void) { return K3KDA_VERSION; }
+
+const char *k3kda_last_error(void) { return g_last_error; }
+
+int k3kda_short_conv(const void *x, int x_dtype, const float *weight, float *conv_state,
+                     const int32_t *cu_seqlens, int N, int T, int D, int W, int apply_silu,
+                     void *out, int out_dtype, void *stream) {
+    if (N < 1 || T < 0 || D < 1 || W < 1 || W > 4) return K3KDA_ERR_INVALID_ARG;
+    if (!dtype_ok(x_dtype) || !dtype_ok(out_dtype)) return K3KDA_ERR_INVALID_ARG;
+    if ((T > 0 && (!x || !out)) || !weight) return K3KDA_ERR_INVALID_ARG;
+    if (cu_seqlens == nullptr && N != 1) return K3KDA_ERR_INVALID_ARG;
+    if (x == out && x != nullptr) return K3KDA_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(out) || !aligned16(weight) || !aligned16(conv_state))
+        return K3KDA_ERR_ALIGNMENT;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int st = cuda_status(launch_short_conv(x, x_dtype == K3KDA_BF16, weight, conv_state, cu_seqlens, N, T,
+                                           D, W, apply_silu, out, out_dtype == K3KDA_BF16, s));
+    if (st != K3KDA_OK || conv_state == nullptr) return st;
+    return cuda_status(launch_conv_state_update(x, x_dtype == K3KDA_BF16, conv_state, cu_seqlens, N, T, D,
+                                                W, s));
+}
+
+size_t k3kda_prefill_workspace_size(int N, int T, int H, int dk, int dv, int chunk, int in_dtype,
+                                    int has_conv) {
+    size_t b = kStatusBytes;
+    if (N < 0 || T < 0 || H < 0 || dk < 0 || dv < 0) return b;
+    if (has_conv) b += conv_buffer_bytes(T, H, dk, dv);
+    if (tc_prefill_supported(in_dtype == K3KDA_BF16 && !has_conv ? 1 : 0, dk, dv, chunk))
+        b += round256(tc_prefill_workspace(N, H));
+    return b;
+}
+
+int k3kda_prefill(const void *q, const void *k, const void *v, int in_dtype, const float *g,
+                  const float *beta, const float *initial_state, const int32_t *cu_seqlens,
+                  const int32_t *cu_seqlens_host, int N, int T, int H, int dk, int dv, int chunk,
+                  float scale, int use_qk_l2norm, const k3kda_conv_args *conv, const void *gate,
+                  void *out, int out_dtype, float *final_state, void *workspace,
+                  size_t workspace_bytes, void *stream) {
+    if (N < 1 || T < 0 || H < 1) return K3KDA_ERR_INVALID_ARG;
+    if (!dtype_ok(in_dtype) || !dtype_ok(out_dtype)) return K3KDA_ERR_INVALID_ARG;
+    if (!head_dim_ok(dk) || !head_dim_ok(dv)) return K3KDA_ERR_UNSUPPORTED;
+    if (chunk != 16 && chunk != 32 && chunk != 64) return K3KDA_ERR_UNSUPPORTED;
+    if (T > 0 && (!q || !k || !v || !g || !beta || !out)) return K3KDA_ERR_INVALID_ARG;
+    if (cu_seqlens == nullptr && N != 1) return K3KDA_ERR_INVALID_ARG;
+    if (cu_seqlens_host && !cu_ok(cu_seqlens_host, N, T)) return K3KDA_ERR_INVALID_ARG;
+    if (conv && (!conv->weight || conv->W < 1 || conv->W > 4)) return K3KDA_ERR_INVALID_ARG;
+    if ((long long)N * H * 4 > 0x7fffffffLL) return K3KDA_ERR_UNSUPPORTED;
+    for (const void *p : {q, k, v, (const void *)g, (const void *)beta, (const void *)initial_state, gate,
+                          (const void *)out, (const void *)final_state})
+        if (!aligned16(p)) return K3KDA_ERR_ALIGNMENT;
+    if (conv && (!aligned16(conv->weight) || !aligned16(conv->conv_state))) return K3KDA_ERR_ALIGNMENT;
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return K3KDA_ERR_WORKSPACE;
+    const size_t need = k3kda_prefill_workspace_size(N, T, H, dk, dv, chunk, in_dtype, conv != nullptr);
+    if (workspace_bytes < need) return K3KDA_ERR_WORKSPACE;
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    char *ws = static_cast<char *>(workspace);
+    unsigned int *status = reinterpret_cast<unsigned int *>(ws);
+    size_t off = kStatusBytes;
+
+    PrefillArgs a{};
+    a.q = q; a.k = k; a.v = v;
+    a.q_row = (int64_t)H * dk; a.k_row = (int64_t)H * dk; a.v_row = (int64_t)H * dv;
+    a.in_bf16 = in_dtype == K3KDA_BF16;
+    a.g = g; a.beta = beta; a.S0 = initial_state; a.cu = cu_seqlens;
+    a.N = N; a.T = T; a.H = H; a.dk = dk; a.dv = dv; a.chunk = chunk;
+    a.scale = scale; a.l2 = use_qk_l2norm != 0;
+    a.gate = gate; a.out = out; a.out_bf16 = out_dtype == K3KDA_BF16; a.Sfin = final_state;
+    a.status = status;
+
+    if (conv) {
+        // Conv stage: q, k, v channels convolved (+SiLU) into an fp32 [T, D] buffer in the
+        // workspace, then the conv state is advanced; the chunked kernel reads that buffer.
+        const int64_t Dq = (int64_t)H * dk, Dv = (int64_t)H * dv, D = 2 * Dq + Dv;
+        float *buf = reinterpret_cast<float *>(ws + off);
+        off += conv_buffer_bytes(T, H, dk, dv);
+        const int W = conv->W;
+        const void *src[3] = {q, k, v};
+        const int64_t width[3] = {Dq, Dq, Dv}, choff[3] = {0, Dq, 2 * Dq};
+        for (int i = 0; i < 3; ++i) {
+            int st = cuda_status(launch_short_conv_strided(
+                src[i], width[i], a.in_bf16, conv->weight + choff[i] * W,
+                conv->conv_state ? conv->conv_state + choff[i] : nullptr, D, cu_seqlens, N, T, (int)width[i],
+                W, 1, buf + choff[i], D, 0, s));
+            if (st != K3KDA_OK) return st;
+        }
+        if (conv->conv_state)
+            for (int i = 0; i < 3; ++i) {
+                int st = cuda_status(launch_conv_state_update_strided(src[i], width[i], a.in_bf16,
+                                                                      conv->conv_state + choff[i], D,
+                                                                      cu_seqlens, N, T, (int)width[i], W, s));
+                if (st != K3KDA_OK) return st;
+            }
+        a.q = buf; a.k = buf + Dq; a.v = buf + 2 * Dq;
+        a.q_row = a.k_row = a.v_row = D;
+        a.in_bf16 = 0;
+    }
+    if (T == 0 && final_state == nullptr) return K3KDA_OK;
+    if (tc_prefill_supported(a.in_bf16, dk, dv, chunk)) {
+        const int32_t *order = nullptr;   // longest-first schedule (host copy needed)
+        return cuda_status(launch_prefill_tc(a, order, s));
+    }
+    if (prefill_f32_smem_bytes(chunk, dk, dv) > 227 * 1024) return K3KDA_ERR_UNSUPPORTED;
+    return cuda_status(launch_prefill_f32(a, s));
+}
+
+int k3kda_workspace_status(void *workspace, void *stream) {
+    if (!workspace) return K3KDA_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    unsigned int word = 0;
+    int st = cuda_status(cudaMemcpyAsync(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost, s));
+    if (st != K3KDA_OK) return st;
+    st = cuda_status(cudaStreamSynchronize(s));
+    if (st != K3KDA_OK) return st;
+    if (word == 0) return K3KDA_OK;
+    st = cuda_status(cudaMemsetAsync(workspace, 0, sizeof(word), s));
+    if (st != K3KDA_OK) return st;
+    st = cuda_status(cudaStreamSynchronize(s));
+    return st != K3KDA_OK ? st : K3KDA_ERR_TIMEOUT;
+}
+
+int k3kda_decode_step(const void *q, const void *k, const void *v, int in_dtype, const float *g,
+                      const float *beta, const void *gate, const float *conv_weight, float *conv_state,
+                      float *state, int N, int H, int dk, int dv, int W, float scale, int use_qk_l2norm,
+                      void *out, int out_dtype, void *stream) {
+    if (N < 0 || H < 1) return K3KDA_ERR_INVALID_ARG;
+    if (!dtype_ok(in_dtype) || !dtype_ok(out_dtype)) return K3KDA_ERR_INVALID_ARG;
+    if (!head_dim_ok(dk) || !head_dim_ok(dv)) return K3KDA_ERR_UNSUPPORTED;
+    if (N > 0 && (!q || !k || !v || !g || !beta || !state || !out)) return K3KDA_ERR_INVALID_ARG;
+    if (conv_weight && (W < 1 || W > 4 || (W > 1 && !conv_state))) return K3KDA_ERR_INVALID_ARG;
+    if ((long long)N * H > 0x7fffffffLL) return K3KDA_ERR_UNSUPPORTED;
+    for (const void *p : {q, k, v, (const void *)g, (const void *)beta, gate, (const void *)conv_weight,
+                          (const void *)conv_state, (const void *)state, (const void *)out})
+        if (!aligned16(p)) return K3KDA_ERR_ALIGNMENT;
+    return cuda_status(launch_decode(q, k, v, in_dtype == K3KDA_BF16, g, beta, gate, conv_weight, conv_state,
+                                     state, N, H, dk, dv, conv_weight ? W : 0, scale, use_qk_l2norm != 0, out,
+                                     out_dtype == K3KDA_BF16, static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

@@ -1,0 +1,88 @@
+// common.cuh -- device helpers and internal launcher declarations shared by the
+// kernels of libk3kda (sm_103a).  Nothing here is part of the C ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+#include <stddef.h>
+
+#include "k3kda.h"
+
+namespace k3kda {
+
+// ---- element access ------------------------------------------------------
+
+__device__ __forceinline__ float load_elt(const void *p, size_t i, int bf16) {
+    if (bf16) return __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(p)[i]);
+    return reinterpret_cast<const float *>(p)[i];
+}
+
+__device__ __forceinline__ void store_elt(void *p, size_t i, float x, int bf16) {
+    if (bf16) reinterpret_cast<__nv_bfloat16 *>(p)[i] = __float2bfloat16_rn(x);
+    else reinterpret_cast<float *>(p)[i] = x;
+}
+
+__device__ __forceinline__ float sigmoidf_(float z) { return 1.0f / (1.0f + __expf(-z)); }
+__device__ __forceinline__ float siluf_(float z) { return z / (1.0f + __expf(-z)); }
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    return x;
+}
+
+// Sequence bounds for sequence n from a device cu_seqlens, clamped into
+// [0, T] and made non-decreasing so that a malformed array can never send a
+// kernel out of bounds (the host validates whenever it has a host copy).
+__device__ __forceinline__ void seq_bounds(const int32_t *cu, int n, int T, int &b, int &e) {
+    if (cu == nullptr) { b = 0; e = T; return; }
+    int lo = cu[n], hi = cu[n + 1];
+    lo = lo < 0 ? 0 : (lo > T ? T : lo);
+    hi = hi < lo ? lo : (hi > T ? T : hi);
+    b = lo; e = hi;
+}
+
+// Counts every kernel this library launches (reported by k3kda_launch_count).
+void count_launch();
+
+// ---- launchers (defined in the kernel files, called by the C ABI layer) ----
+
+cudaError_t launch_short_conv(const void *x, int x_bf16, const float *w, const float *cs_in,
+                              const int32_t *cu, int N, int T, int D, int W, int silu,
+                              void *out, int out_bf16, cudaStream_t s);
+cudaError_t launch_conv_state_update(const void *x, int x_bf16, float *cs, const int32_t *cu,
+                                     int N, int T, int D, int W, cudaStream_t s);
+
+cudaError_t launch_short_conv_strided(const void *x, int64_t x_stride, int x_bf16, const float *w,
+                                      const float *cs, int64_t cs_stride, const int32_t *cu, int N,
+                                      int T, int Dc, int W, int silu, void *out, int64_t out_stride,
+                                      int out_bf16, cudaStream_t s);
+cudaError_t launch_conv_state_update_strided(const void *x, int64_t x_stride, int x_bf16, float *cs,
+                                             int64_t cs_stride, const int32_t *cu, int N, int T,
+                                             int Dc, int W, cudaStream_t s);
+
+cudaError_t launch_decode(const void *q, const void *k, const void *v, int in_bf16, const float *g,
+                          const float *beta, const void *gate, const float *conv_w, float *conv_state,
+                          float *state, int N, int H, int dk, int dv, int W, float scale, int l2,
+                          void *out, int out_bf16, cudaStream_t s);
+
+struct PrefillArgs {
+    const void *q, *k, *v;   // [T,H,dk] x2, [T,H,dv]; element type by in_bf16
+    int64_t q_row, k_row, v_row;   // element stride between tokens (H*dk or D for fused-conv buffers)
+    int in_bf16;
+    const float *g, *beta, *S0;
+    const int32_t *cu;
+    int N, T, H, dk, dv, chunk;
+    float scale;
+    int l2;
+    const void *gate;
+    void *out;
+    int out_bf16;
+    float *Sfin;
+    unsigned int *status;    // device status word (workspace offset 0)
+};
+
+cudaError_t launch_prefill_f32(const PrefillArgs &a, cudaStream_t s);
+
+}  // namespace k3kda

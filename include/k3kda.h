@@ -1,0 +1,201 @@
+/*
+ * k3kda.h -- C ABI of the GB300 (sm_103a) KDA mixer library (libk3kda.so).
+ *
+ * KDA (Kimi Delta Attention) is the linear-attention mixer of the Kimi K3 /
+ * KimiLinear hybrid.  The pages this library follows name its pieces without
+ * writing the equations out:
+ *   - "Experimental Native Vulkan Backend for Kimi K3" (Hugging Face
+ *     discussion #187), feature list: independent Q/K/V short convolutions,
+ *     recurrent KDA state, KDA output gating;
+ *   - metrale_model_arch::kimi_k3 docs: Structs KdaConfig (head dim 128, conv
+ *     width 4 in production; tiny dims legal), KdaState (per-sequence state,
+ *     both buffers FP32, read-modify-write); Constants KDA_L2_EPS (eps of the
+ *     in-kernel q/k L2 norm); Functions kda_decode_token ("conv update then
+ *     recurrent step"); Re-exports launch_k3_kda_decode_token (the decode
+ *     launch over a caller-held device state);
+ *   - mlite-k3 README ("What this repository is"): unsupported inputs fail
+ *     explicitly rather than being approximated.
+ * The recurrence itself is the gated delta rule, per sequence and head:
+ *     S_t = (I - beta_t k_t k_t^T) Diag(exp(g_t)) S_{t-1} + beta_t k_t v_t^T
+ *     o_t = scale * S_t^T q_t          (then o_t * sigmoid(gate_t) if gated)
+ * with S in R^{dk x dv} kept in FP32.
+ *
+ * Conventions shared by every entry point
+ *   - All tensor pointers are DEVICE pointers unless a name ends in _host.
+ *     Every buffer is owned by the caller; the library allocates nothing and
+ *     keeps no per-call state.  Layouts are dense row-major, last index
+ *     fastest, with no padding.
+ *   - Work is enqueued on `stream` (a cudaStream_t passed as void*; NULL =
+ *     legacy default stream) and runs asynchronously; no entry point
+ *     synchronises.  Inputs must stay alive until the stream reaches the work.
+ *   - Every entry point returns a k3kda_status.  Arguments are checked on the
+ *     host before anything is launched; an invalid call launches nothing and
+ *     returns a negative status.  Nothing aborts, throws or prints.
+ *   - Supported head dims: dk, dv in {16, 32, ..., 128} (multiples of 16).
+ *     Conv width W in {1, 2, 3, 4}.  Chunk in {16, 32, 64}.
+ *   - Element types: q, k, v and gate share one type (k3kda_dtype); g, beta,
+ *     conv weights and all states are FP32.  Pointers must be 16-byte aligned.
+ *   - The L2 norm is x * (sum_c x_c^2 + eps)^(-1/2) over dk with eps =
+ *     K3KDA_L2_EPS; the pages name this constant but print no value (1e-6 is
+ *     used, the default of the flash-linear-attention norm it is taken from).
+ */
+#ifndef K3KDA_H
+#define K3KDA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define K3KDA_VERSION 1
+#define K3KDA_L2_EPS 1e-6f
+
+typedef enum {
+    K3KDA_OK = 0,
+    K3KDA_ERR_INVALID_ARG = -1,  /* null pointer, bad size, bad cu_seqlens        */
+    K3KDA_ERR_UNSUPPORTED = -2,  /* legal but not implemented (e.g. dk = 200)     */
+    K3KDA_ERR_ALIGNMENT = -3,    /* a pointer is not 16-byte aligned              */
+    K3KDA_ERR_WORKSPACE = -4,    /* workspace missing or smaller than required    */
+    K3KDA_ERR_CUDA = -5,         /* a CUDA launch or runtime call failed          */
+    K3KDA_ERR_TIMEOUT = -6       /* a bounded in-kernel wait gave up (see below)  */
+} k3kda_status;
+
+typedef enum { K3KDA_F32 = 0, K3KDA_BF16 = 1 } k3kda_dtype;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char *k3kda_status_string(int status);
+
+/* K3KDA_VERSION of the loaded library. */
+int k3kda_version(void);
+
+/* Number of CUDA kernels this library has launched in this process (all
+ * entry points, all threads).  A diagnostic for launch accounting. */
+long long k3kda_launch_count(void);
+
+/* Text of the last CUDA error seen by this thread inside the library ("" if
+ * none).  Valid until the next call from the same thread. */
+const char *k3kda_last_error(void);
+
+/*
+ * k3kda_short_conv -- causal depthwise short convolution with SiLU
+ * ("independent Q/K/V short convolutions", HF discussion #187 feature list;
+ * width 4 in production, metrale KdaConfig).  For every packed sequence n
+ * (tokens cu_seqlens[n] .. cu_seqlens[n+1]-1) and channel c:
+ *     y[t, c] = act( sum_{i=0}^{W-1} weight[c, i] * x[t - (W-1) + i, c] )
+ * where positions before the sequence start read conv_state[n, W-1+tau, c]
+ * (tau < 0; rows are oldest first) or zero when conv_state is NULL, and act is
+ * SiLU (z * sigmoid(z)) when apply_silu is nonzero, else the identity.  No bias.
+ *
+ *   x          [T, D]       x_dtype (F32 or BF16)
+ *   weight     [D, W]       FP32; weight[c, W-1] multiplies the current token
+ *   conv_state [N, W-1, D]  FP32, read-modify-write; NULL => zero history and
+ *                           no state written.  On return row r holds the
+ *                           pre-conv input at position L_n - (W-1) + r of
+ *                           sequence n (older rows shift in when L_n < W-1).
+ *   cu_seqlens [N+1]        int32 device; NULL allowed only when N == 1
+ *   out        [T, D]       out_dtype; may not alias x
+ * Errors: INVALID_ARG for N < 1, T < 0, D < 1, W outside 1..4, null x/weight/
+ * out; ALIGNMENT when x/out/weight/conv_state are not 16-byte aligned.
+ */
+int k3kda_short_conv(const void *x, int x_dtype, const float *weight, float *conv_state,
+                     const int32_t *cu_seqlens, int N, int T, int D, int W, int apply_silu,
+                     void *out, int out_dtype, void *stream);
+
+/* Optional fused short conv for k3kda_prefill: the q, k and v channels are
+ * convolved (+SiLU) as one tensor of D = 2*H*dk + H*dv channels ordered
+ * [q heads | k heads | v heads], with the k3kda_short_conv semantics above. */
+typedef struct k3kda_conv_args {
+    const float *weight;   /* [D, W] FP32, required                              */
+    float *conv_state;     /* [N, W-1, D] FP32 read-modify-write, or NULL (zero) */
+    int W;                 /* 1..4                                               */
+} k3kda_conv_args;
+
+/* Bytes of device workspace k3kda_prefill needs for these arguments (always a
+ * multiple of 256; at least 256, which holds the device status word). */
+size_t k3kda_prefill_workspace_size(int N, int T, int H, int dk, int dv, int chunk,
+                                    int in_dtype, int has_conv);
+
+/*
+ * k3kda_prefill -- chunked KDA prefill over packed variable-length sequences
+ * (the "recurrent KDA state" of HF discussion #187, computed chunk by chunk;
+ * the state is the FP32 KdaState of the metrale docs).  For each sequence n
+ * and head h the recurrence above runs over the sequence's tokens starting
+ * from initial_state[n, h] (zero if NULL), writing o for every token and the
+ * last state to final_state[n, h].  State, conv history and chunking restart
+ * at every cu_seqlens boundary; the last chunk of a sequence may be partial.
+ *
+ *   q, k           [T, H, dk]      in_dtype   (pre-conv when conv != NULL)
+ *   v              [T, H, dv]      in_dtype
+ *   g              [T, H, dk]      FP32 log-decay (alpha = exp(g); g <= 0 is
+ *                                  the supported range)
+ *   beta           [T, H]          FP32
+ *   initial_state  [N, H, dk, dv]  FP32 or NULL (zeros)
+ *   cu_seqlens     [N+1]           int32 device, cu[0] = 0, non-decreasing,
+ *                                  cu[N] = T; NULL allowed only when N == 1
+ *   cu_seqlens_host[N+1]           optional host copy; when given it is
+ *                                  validated (INVALID_ARG if malformed) and
+ *                                  used to schedule long sequences first
+ *   chunk          16, 32 or 64 (the chunk length of the chunked form)
+ *   scale          output scale (usually dk^-0.5)
+ *   use_qk_l2norm  nonzero: L2-normalise q and k per (token, head) in kernel,
+ *                  after the conv when there is one
+ *   conv           NULL, or the fused q/k/v short conv + SiLU
+ *   gate           [T, H, dv] in_dtype logits, or NULL (no output gate)
+ *   out            [T, H, dv] out_dtype
+ *   final_state    [N, H, dk, dv] FP32 or NULL; may alias initial_state
+ *   workspace      device scratch of k3kda_prefill_workspace_size() bytes,
+ *                  256-byte aligned, exclusively owned by this call until it
+ *                  completes on the stream
+ * The fast path (tensor cores, split-BF16 operands) runs for in_dtype BF16,
+ * dk = dv = 128, chunk 64; every other supported shape runs an FP32 CUDA-core
+ * chunked kernel.  Both compute the same chunked algebra.
+ * Errors: INVALID_ARG, UNSUPPORTED, ALIGNMENT, WORKSPACE, CUDA as above.
+ * A bounded in-kernel wait that gives up records K3KDA_ERR_TIMEOUT in the
+ * workspace status word (see k3kda_workspace_status) instead of hanging.
+ */
+int k3kda_prefill(const void *q, const void *k, const void *v, int in_dtype,
+                  const float *g, const float *beta, const float *initial_state,
+                  const int32_t *cu_seqlens, const int32_t *cu_seqlens_host,
+                  int N, int T, int H, int dk, int dv, int chunk, float scale,
+                  int use_qk_l2norm, const k3kda_conv_args *conv, const void *gate,
+                  void *out, int out_dtype, float *final_state,
+                  void *workspace, size_t workspace_bytes, void *stream);
+
+/* Synchronise `stream`, read and clear the status word at the start of a
+ * prefill workspace: K3KDA_OK, or K3KDA_ERR_TIMEOUT if a kernel that used this
+ * workspace gave up a bounded wait (its outputs are then invalid). */
+int k3kda_workspace_status(void *workspace, void *stream);
+
+/*
+ * k3kda_decode_step -- one new token for each of N independent sequences
+ * ("One decode token: conv update then recurrent step", metrale kda_decode_token;
+ * launch_k3_kda_decode_token over a KdaDeviceState).  Per sequence n and head h:
+ *   1. conv: the token's pre-conv q, k, v channels are shifted into the conv
+ *      window (conv_state rows are the previous W-1 inputs, oldest first),
+ *      convolved with conv_weight and passed through SiLU; conv_state is
+ *      updated in place to the newest W-1 inputs (skipped when conv_weight
+ *      is NULL: q, k, v are used as given);
+ *   2. q, k L2-normalised when use_qk_l2norm;
+ *   3. S <- (I - beta k k^T) Diag(exp(g)) S + beta k v^T  in place (FP32);
+ *   4. out = scale * S^T q, times sigmoid(gate) when gate != NULL.
+ *
+ *   q, k        [N, H, dk] in_dtype      v, gate [N, H, dv] in_dtype
+ *   g           [N, H, dk] FP32           beta   [N, H] FP32
+ *   conv_weight [2*H*dk + H*dv, W] FP32 or NULL;  conv_state [N, W-1, 2*H*dk + H*dv]
+ *   state       [N, H, dk, dv] FP32, read-modify-write in place
+ *   out         [N, H, dv] out_dtype
+ * Errors: INVALID_ARG, UNSUPPORTED, ALIGNMENT, CUDA.
+ */
+int k3kda_decode_step(const void *q, const void *k, const void *v, int in_dtype,
+                      const float *g, const float *beta, const void *gate,
+                      const float *conv_weight, float *conv_state, float *state,
+                      int N, int H, int dk, int dv, int W, float scale, int use_qk_l2norm,
+                      void *out, int out_dtype, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* K3KDA_H */

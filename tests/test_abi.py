@@ -1,0 +1,115 @@
+"""The C-ABI library loads, exports every symbol include/k3kda.h declares, and
+rejects bad arguments on the host before launching anything (no GPU needed:
+every call here returns from argument validation)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import hybrid_linear_attention_rule_gb300 as K
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "k3kda.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(k3kda_[a-z_0-9]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return K.load_library()
+
+
+def test_header_declares_the_three_calls():
+    names = declared_functions()
+    for n in ("k3kda_short_conv", "k3kda_prefill", "k3kda_decode_step"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, f"not exported: {missing}"
+
+
+def test_version_and_status_strings(lib):
+    assert K.k3kda_version() == 1
+    assert K.k3kda_status_string(0) == "K3KDA_OK"
+    assert K.k3kda_status_string(-6) == "K3KDA_ERR_TIMEOUT"
+    assert K.k3kda_status_string(123) == "K3KDA_UNKNOWN_STATUS"
+
+
+def test_workspace_size_is_aligned_and_grows_with_conv(lib):
+    a = K.k3kda_prefill_workspace_size(1, 1024, 4, 128, 128, 64, K.BF16, False)
+    b = K.k3kda_prefill_workspace_size(1, 1024, 4, 128, 128, 64, K.BF16, True)
+    assert a >= 256 and a % 256 == 0 and b % 256 == 0
+    assert b >= a + 1024 * (2 * 4 * 128 + 4 * 128) * 4
+
+
+# Fake, never-dereferenced device addresses: validation must reject before use.
+A16 = ctypes.c_void_p(0x10000)
+MIS = ctypes.c_void_p(0x10004)
+
+
+def _prefill(lib, **kw):
+    args = dict(q=A16, k=A16, v=A16, in_dtype=1, g=A16, beta=A16, S0=None, cu=None, cu_h=None, N=1, T=64,
+                H=2, dk=128, dv=128, chunk=64, scale=1.0, l2=1, conv=None, gate=None, out=A16, out_dtype=0,
+                fs=None, ws=None, ws_bytes=0, stream=None)
+    args.update(kw)
+    return lib.k3kda_prefill(*args.values())
+
+
+def test_prefill_rejects_bad_arguments(lib):
+    assert _prefill(lib, N=0) == -1
+    assert _prefill(lib, q=None) == -1
+    assert _prefill(lib, N=2) == -1                      # two sequences but no cu_seqlens
+    assert _prefill(lib, dk=200) == -2
+    assert _prefill(lib, dk=24) == -2
+    assert _prefill(lib, chunk=48) == -2
+    assert _prefill(lib, in_dtype=7) == -1
+    assert _prefill(lib, g=MIS) == -3
+    assert _prefill(lib, ws=None) == -4                  # no workspace
+    assert _prefill(lib, ws=A16, ws_bytes=16) == -4      # too small
+
+
+def test_prefill_validates_host_cu_seqlens(lib):
+    bad = (ctypes.c_int32 * 3)(0, 40, 30)                # decreasing
+    assert _prefill(lib, N=2, cu=A16, cu_h=ctypes.cast(bad, ctypes.c_void_p), T=30) == -1
+    bad_end = (ctypes.c_int32 * 3)(0, 10, 20)            # last != T
+    assert _prefill(lib, N=2, cu=A16, cu_h=ctypes.cast(bad_end, ctypes.c_void_p), T=30) == -1
+
+
+def test_decode_rejects_bad_arguments(lib):
+    def dec(**kw):
+        a = dict(q=A16, k=A16, v=A16, in_dtype=1, g=A16, beta=A16, gate=None, cw=None, cs=None, state=A16,
+                 N=4, H=2, dk=128, dv=128, W=4, scale=1.0, l2=1, out=A16, out_dtype=0, stream=None)
+        a.update(kw)
+        return lib.k3kda_decode_step(*a.values())
+    assert dec(state=None) == -1
+    assert dec(dv=130) == -2
+    assert dec(cw=A16, cs=None) == -1                    # conv weights without conv state
+    assert dec(cw=A16, cs=A16, W=5) == -1
+    assert dec(out=MIS) == -3
+
+
+def test_short_conv_rejects_bad_arguments(lib):
+    def conv(**kw):
+        a = dict(x=A16, xt=1, w=A16, cs=None, cu=None, N=1, T=10, D=64, W=4, silu=1, out=ctypes.c_void_p(0x20000),
+                 ot=1, stream=None)
+        a.update(kw)
+        return lib.k3kda_short_conv(*a.values())
+    assert conv(W=0) == -1
+    assert conv(W=5) == -1
+    assert conv(out=A16) == -1                           # out aliases x
+    assert conv(N=3) == -1                               # no cu_seqlens
+    assert conv(w=MIS) == -3
+
+
+def test_binding_refuses_cpu_tensors():
+    import torch
+    x = torch.zeros(4, 8)
+    with pytest.raises(ValueError):
+        K.k3kda_short_conv(x, torch.zeros(8, 4), None, None, 1, 4, 8, 4, True, torch.zeros(4, 8))

@@ -1,0 +1,170 @@
+"""Parity of k3kda_prefill (through the C ABI) with the oracle on the five workload
+families: fp32 core, chunked bf16 prefill, varlen with initial states, the fused
+mixer (conv + L2 + gate), plus edge cases.  Small cases are compared element by
+element; the full-size workloads run in the bench's launch configuration and are
+checked on seeded samples of heads (heads never interact)."""
+import numpy as np
+import pytest
+import torch
+
+import hybrid_linear_attention_rule_gb300 as K
+import kda_inputs as KI
+import oracle as O
+from parity_utils import (assert_close, case_to_device, head_subset, oracle_prefill, run_prefill,
+                          to_np)
+
+pytestmark = pytest.mark.gpu
+
+
+def _check(c, out_dtype=torch.float32, heads=None):
+    out, fs, d = run_prefill(c, out_dtype)
+    sub = c if heads is None else head_subset(c, heads)
+    ro, rs, rcs = oracle_prefill(sub)
+    o = to_np(out) if heads is None else to_np(out[:, heads])
+    s = to_np(fs) if heads is None else to_np(fs[:, heads])
+    fp32 = c.in_dtype == "f32"
+    eo = assert_close(o, ro, fp32, f"{c.name} out", store_bf16=out_dtype == torch.bfloat16)
+    es = assert_close(s, rs, fp32, f"{c.name} final state")
+    if c.conv_w is not None and heads is None:
+        assert np.array_equal(to_np(d["conv_state"]), rcs), "conv state must be the last inputs exactly"
+    print(f"{c.name}: max err out {eo:.3e} state {es:.3e}")
+    return out, fs, d
+
+
+# ---- fp32 core (the 1e-5 workload) ----
+
+def test_core_fp32_workload():
+    _check(KI.core_fp32(seed=0))
+
+
+@pytest.mark.parametrize("chunk", [16, 32, 64])
+def test_core_fp32_chunk_sizes_and_ragged_tail(chunk):
+    c = KI.prefill_case("fp32_ragged", [203], 2, 32, 48, chunk, "f32", seed=1, s0_std=0.02, gate=True)
+    _check(c)
+
+
+# ---- bf16 chunked prefill ----
+
+def test_prefill_bf16_small_ragged():
+    """15 full chunks plus a 40-token tail, 4 heads, d = 128, chunk 64."""
+    _check(KI.chunked_prefill(seed=1, T=1000, H=4))
+
+
+def test_prefill_bf16_output_store():
+    _check(KI.chunked_prefill(seed=2, T=300, H=2), out_dtype=torch.bfloat16)
+
+
+def test_prefill_without_l2norm():
+    c = KI.chunked_prefill(seed=3, T=200, H=2)
+    c.use_qk_l2norm = False
+    c.q = KI.round_bf16(c.q * 0.08)
+    c.k = KI.round_bf16(c.k * 0.08)
+    _check(c)
+
+
+# ---- varlen with initial states ----
+
+def test_varlen_small_with_edge_lengths():
+    """Empty, one-token, chunk-1, chunk, chunk+1 and multi-chunk sequences packed together."""
+    c = KI.prefill_case("varlen_edges", [0, 1, 63, 64, 65, 200, 0, 7], 3, 128, 128, 64, "bf16", seed=4,
+                        s0_std=0.02, gate=True)
+    _check(c)
+
+
+def test_varlen_mixed_head_dims_f32_path():
+    c = KI.prefill_case("varlen_dk64_dv128", [5, 90, 33], 2, 64, 128, 64, "bf16", seed=5, s0_std=0.02)
+    _check(c)
+
+
+def test_final_state_may_alias_initial_state():
+    c = KI.prefill_case("alias", [100, 30], 2, 128, 128, 64, "bf16", seed=6, s0_std=0.02)
+    d = case_to_device(c)
+    T, H, dk, dv, N = c.T, c.H, c.dk, c.dv, c.N
+    out = torch.empty((T, H, dv), device="cuda")
+    ws = torch.zeros(K.k3kda_prefill_workspace_size(N, T, H, dk, dv, 64, K.BF16, False), dtype=torch.uint8,
+                     device="cuda")
+    S = d["S0"].clone()
+    K.k3kda_prefill(d["q"], d["k"], d["v"], d["g"], d["beta"], S, d["cu"].cuda(), d["cu"], N, T, H, dk, dv, 64,
+                    c.scale, True, None, None, 0, None, out, S, ws)
+    torch.cuda.synchronize()
+    ro, rs, _ = oracle_prefill(c)
+    assert_close(to_np(out), ro, False, "alias out")
+    assert_close(to_np(S), rs, False, "alias state")
+
+
+# ---- fused mixer: conv + SiLU + L2 + chunked KDA + gate ----
+
+def test_fused_mixer_small():
+    _check(KI.fused_mixer(seed=1, T=777, H=2))
+
+
+def test_fused_mixer_varlen_with_conv_state():
+    c = KI.prefill_case("mixer_varlen", [2, 130, 1, 64], 2, 128, 128, 64, "bf16", seed=7, s0_std=0.02,
+                        gate=True, conv_width=4, conv_state=True)
+    _check(c)
+
+
+def test_state_and_conv_state_chaining():
+    """prefill(T) == prefill(T1) then prefill(T - T1) from the carried state and conv state."""
+    c = KI.fused_mixer(seed=8, T=300, H=2)
+    d = case_to_device(c)
+    out, fs = K.prefill(d["q"], d["k"], d["v"], d["g"], d["beta"], conv_weight=d["conv_w"],
+                        conv_state=d["conv_state"].clone(), gate=d["gate"], out_dtype=torch.float32)
+    T1 = 129
+    cs = d["conv_state"].clone()
+    sl = lambda x, a, b: x[a:b].contiguous()
+    o1, f1 = K.prefill(*(sl(d[n], 0, T1) for n in ("q", "k", "v", "g", "beta")), conv_weight=d["conv_w"],
+                       conv_state=cs, gate=sl(d["gate"], 0, T1), out_dtype=torch.float32)
+    o2, f2 = K.prefill(*(sl(d[n], T1, c.T) for n in ("q", "k", "v", "g", "beta")), initial_state=f1,
+                       conv_weight=d["conv_w"], conv_state=cs, gate=sl(d["gate"], T1, c.T), out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    ro, rs, _ = oracle_prefill(c)
+    assert_close(to_np(torch.cat([o1, o2])), ro, False, "chained out")
+    assert_close(to_np(f2), rs, False, "chained state")
+    assert_close(to_np(out), ro, False, "whole out")
+
+
+def test_prefill_then_decode_continues_the_sequence():
+    """A decode step after prefill(L-1) reproduces token L of the mixer."""
+    c = KI.fused_mixer(seed=9, T=70, H=2)
+    d = case_to_device(c)
+    L = c.T
+    cs = d["conv_state"].clone()
+    sl = lambda x: x[:L - 1].contiguous()
+    _, f1 = K.prefill(*(sl(d[n]) for n in ("q", "k", "v", "g", "beta")), conv_weight=d["conv_w"], conv_state=cs,
+                      gate=sl(d["gate"]), out_dtype=torch.float32)
+    last = lambda x: x[L - 1:].contiguous()
+    o = K.decode_step(*(last(d[n]) for n in ("q", "k", "v", "g", "beta")), f1, gate=last(d["gate"]),
+                      conv_weight=d["conv_w"], conv_state=cs, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    ro, rs, _ = oracle_prefill(c)
+    assert_close(to_np(o)[0], ro[-1], False, "decode after prefill")
+    assert_close(to_np(f1), rs, False, "state after decode")
+
+
+def test_empty_batch_copies_initial_state():
+    c = KI.prefill_case("empty", [0, 0], 2, 64, 64, 64, "bf16", seed=10, s0_std=0.02)
+    d = case_to_device(c)
+    out, fs = K.prefill(d["q"], d["k"], d["v"], d["g"], d["beta"], initial_state=d["S0"], cu_seqlens=d["cu"])
+    torch.cuda.synchronize()
+    assert np.array_equal(to_np(fs), c.S0)
+
+
+# ---- the full-size workloads (bench launch configuration), sampled heads ----
+
+@pytest.mark.slow
+def test_full_chunked_prefill_sampled_heads():
+    c = KI.chunked_prefill(seed=0)
+    _check(c, heads=[0, 13, 31])
+
+
+@pytest.mark.slow
+def test_full_varlen_prefill_sampled_heads():
+    c = KI.varlen_prefill(seed=0)
+    _check(c, heads=[7])
+
+
+@pytest.mark.slow
+def test_full_fused_mixer_sampled_heads():
+    c = KI.fused_mixer(seed=0)
+    _check(c, out_dtype=torch.bfloat16, heads=[5, 26])
