@@ -13,6 +13,8 @@ size_t prefill_f32_smem_bytes(int chunk, int dk, int dv);
 bool tc_prefill_supported(int in_bf16, int dk, int dv, int chunk);
 size_t tc_prefill_workspace(int N, int H);
 cudaError_t launch_prefill_tc(const PrefillArgs &a, const int32_t *order, cudaStream_t s);
+cudaError_t launch_prefill_tc_fused(const PrefillArgs &p, const float *conv_w, float *conv_state, int W,
+                                    cudaStream_t s);
 }  // namespace k3kda
 
 using namespace k3kda;
@@ -30,6 +32,7 @@ int cuda_status(cudaError_t e) {
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 bool head_dim_ok(int d) { return d >= 16 && d <= 128 && d % 16 == 0; }
 bool dtype_ok(int t) { return t == K3KDA_F32 || t == K3KDA_BF16; }
 
@@ -97,9 +100,9 @@ size_t k3kda_prefill_workspace_size(int N, int T, int H, int dk, int dv, int chu
                                     int has_conv) {
     size_t b = kStatusBytes;
     if (N < 0 || T < 0 || H < 0 || dk < 0 || dv < 0) return b;
+    if (tc_prefill_supported(in_dtype == K3KDA_BF16, dk, dv, chunk))
+        return b + round256(tc_prefill_workspace(N, H));   // conv, norm and gate are fused
     if (has_conv) b += conv_buffer_bytes(T, H, dk, dv);
-    if (tc_prefill_supported(in_dtype == K3KDA_BF16 && !has_conv ? 1 : 0, dk, dv, chunk))
-        b += round256(tc_prefill_workspace(N, H));
     return b;
 }
 
@@ -118,9 +121,10 @@ int k3kda_prefill(const void *q, const void *k, const void *v, int in_dtype, con
     if (cu_seqlens_host && !cu_ok(cu_seqlens_host, N, T)) return K3KDA_ERR_INVALID_ARG;
     if (conv && (!conv->weight || conv->W < 1 || conv->W > 4)) return K3KDA_ERR_INVALID_ARG;
     if ((long long)N * H * 4 > 0x7fffffffLL) return K3KDA_ERR_UNSUPPORTED;
-    for (const void *p : {q, k, v, (const void *)g, (const void *)beta, (const void *)initial_state, gate,
-                          (const void *)out, (const void *)final_state})
+    for (const void *p : {q, k, v, (const void *)g, (const void *)initial_state, gate, (const void *)out,
+                          (const void *)final_state})
         if (!aligned16(p)) return K3KDA_ERR_ALIGNMENT;
+    if (!aligned4(beta)) return K3KDA_ERR_ALIGNMENT;
     if (conv && (!aligned16(conv->weight) || !aligned16(conv->conv_state))) return K3KDA_ERR_ALIGNMENT;
     if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return K3KDA_ERR_WORKSPACE;
     const size_t need = k3kda_prefill_workspace_size(N, T, H, dk, dv, chunk, in_dtype, conv != nullptr);
@@ -138,9 +142,12 @@ int k3kda_prefill(const void *q, const void *k, const void *v, int in_dtype, con
     a.g = g; a.beta = beta; a.S0 = initial_state; a.cu = cu_seqlens;
     a.N = N; a.T = T; a.H = H; a.dk = dk; a.dv = dv; a.chunk = chunk;
     a.scale = scale; a.l2 = use_qk_l2norm != 0;
-    a.gate = gate; a.out = out; a.out_bf16 = out_dtype == K3KDA_BF16; a.Sfin = final_state;
+    a.gate = gate; a.gate_bf16 = in_dtype == K3KDA_BF16; a.out = out; a.out_bf16 = out_dtype == K3KDA_BF16; a.Sfin = final_state;
     a.status = status;
 
+    if (tc_prefill_supported(a.in_bf16, dk, dv, chunk))
+        return cuda_status(launch_prefill_tc_fused(a, conv ? conv->weight : nullptr,
+                                                   conv ? conv->conv_state : nullptr, conv ? conv->W : 0, s));
     if (conv) {
         // Conv stage: q, k, v channels convolved (+SiLU) into an fp32 [T, D] buffer in the
         // workspace, then the conv state is advanced; the chunked kernel reads that buffer.
@@ -169,10 +176,6 @@ int k3kda_prefill(const void *q, const void *k, const void *v, int in_dtype, con
         a.in_bf16 = 0;
     }
     if (T == 0 && final_state == nullptr) return K3KDA_OK;
-    if (tc_prefill_supported(a.in_bf16, dk, dv, chunk)) {
-        const int32_t *order = nullptr;   // longest-first schedule (host copy needed)
-        return cuda_status(launch_prefill_tc(a, order, s));
-    }
     if (prefill_f32_smem_bytes(chunk, dk, dv) > 227 * 1024) return K3KDA_ERR_UNSUPPORTED;
     return cuda_status(launch_prefill_f32(a, s));
 }
@@ -202,9 +205,10 @@ int k3kda_decode_step(const void *q, const void *k, const void *v, int in_dtype,
     if (N > 0 && (!q || !k || !v || !g || !beta || !state || !out)) return K3KDA_ERR_INVALID_ARG;
     if (conv_weight && (W < 1 || W > 4 || (W > 1 && !conv_state))) return K3KDA_ERR_INVALID_ARG;
     if ((long long)N * H > 0x7fffffffLL) return K3KDA_ERR_UNSUPPORTED;
-    for (const void *p : {q, k, v, (const void *)g, (const void *)beta, gate, (const void *)conv_weight,
-                          (const void *)conv_state, (const void *)state, (const void *)out})
+    for (const void *p : {q, k, v, (const void *)g, gate, (const void *)conv_weight, (const void *)conv_state,
+                          (const void *)state, (const void *)out})
         if (!aligned16(p)) return K3KDA_ERR_ALIGNMENT;
+    if (!aligned4(beta)) return K3KDA_ERR_ALIGNMENT;
     return cuda_status(launch_decode(q, k, v, in_dtype == K3KDA_BF16, g, beta, gate, conv_weight, conv_state,
                                      state, N, H, dk, dv, conv_weight ? W : 0, scale, use_qk_l2norm != 0, out,
                                      out_dtype == K3KDA_BF16, static_cast<cudaStream_t>(stream)));

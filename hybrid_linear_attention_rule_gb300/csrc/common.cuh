@@ -76,7 +76,8 @@ struct PrefillArgs {
     int N, T, H, dk, dv, chunk;
     float scale;
     int l2;
-    const void *gate;
+    const void *gate;        // [T,H,dv] logits or null
+    int gate_bf16;           // element type of gate (the q/k/v buffers may be fp32 after a conv stage)
     void *out;
     int out_bf16;
     float *Sfin;

@@ -170,7 +170,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_f32_kernel(PrefillArgs 
             for (int jj = 0; jj <= i; ++jj) acc = fmaf(Ai[jj], sU[jj * BVP + j], acc);
             float o = a.scale * acc;
             const size_t oi = ((size_t)(cs + i) * H + h) * dv + j0 + j;
-            if (a.gate) o = o * sigmoidf_(load_elt(a.gate, oi, a.in_bf16));
+            if (a.gate) o = o * sigmoidf_(load_elt(a.gate, oi, a.gate_bf16));
             store_elt(a.out, oi, o, a.out_bf16);
         }
         __syncthreads();

@@ -1,19 +1,714 @@
-// prefill_tc.cu -- tensor-core (tcgen05) chunked KDA prefill.  Placeholder:
-// no shape is routed here yet.
+// prefill_tc.cu -- chunked KDA prefill on the 5th-generation tensor cores
+// (tcgen05 MMA, TMEM accumulators), bf16 inputs, dk = dv = 128, chunk 64, with
+// the q/k/v short conv (+SiLU), q/k L2 norm and sigmoid output gate fused.
+//
+// The recurrence ("recurrent KDA state", HF discussion #187 feature list; FP32
+// KdaState, metrale kimi_k3 docs) in its chunked (WY/UT) form.  For a chunk of
+// 64 tokens with chunk-local cumulative log-decay G (per channel) and a
+// per-channel reference r = (G_first + G_last) / 2:
+//   Kh = k E, Qh = q E, Kb = k / E          with E = exp(G - r)
+//   Akk = diag(beta) tril(Kh Kb^T, -1),  Aqk = tril(Qh Kb^T)
+//   T  = (I + Akk)^-1,  Tb = T diag(beta)
+//   W' = Tb Kh,  U = Tb v
+//   S' = diag(exp(r)) S                        (state in the chunk's basis)
+//   V' = U - W' S'
+//   O  = scale (Qh S' + Aqk V')  [* sigmoid(gate)]
+//   S_next = diag(exp(G_last - r)) (S' + Kb^T V')
+// All exponents are of |G - r| <= half the chunk's total decay, so nothing
+// overflows for per-chunk decays below ~170 nats per channel.
+//
+// Precision: every MMA operand that is not exactly bf16 is split into a bf16
+// high part and a bf16 low part (x = hi + lo to ~2^-17 relative) and each
+// product is hi*hi + hi*lo + lo*hi with fp32 accumulation in TMEM; this keeps
+// the heavy-tailed state and outputs within ~1e-4 of the fp64 recurrence
+// relative to their RMS, where plain bf16 operands miss by ~10x.  Kh and Tb
+// are used in plain bf16 (their rounding stays below 2e-3 of RMS).
+//
+// Work layout: one CTA (8 warps) per (sequence, head); the CTA walks its
+// chunks in order.  CUDA cores build the operands in 128B-swizzled K-major
+// shared-memory tiles and invert the 64x64 unit-triangular matrix in fp32; a
+// single elected thread issues the tcgen05.mma chains; the fp32 state lives in
+// TMEM for the whole sequence.  TMEM columns: [0,64) Akk|Aqk then O^T,
+// [64,128) W'^T, [128,192) U^T then V'^T, [192,320) S'^T.
 #include "common.cuh"
+#include "tc_ptx.cuh"
 
 namespace k3kda {
+namespace {
+
+using namespace tc;
+
+constexpr int kC = 64;
+constexpr int kD = 128;
+constexpr int kThreads = 256;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColA = 0, kColW = 64, kColU = 128, kColS = 192;
+constexpr uint32_t kWaitLimit = 1u << 26;
+
+// shared-memory plan (byte offsets from a 1024-aligned base)
+constexpr uint32_t OFF_X = 0;                    // [128 rows][128 K] hi: Kh rows 0-63, Qh rows 64-127
+constexpr uint32_t OFF_XL = OFF_X + 32768;       // same, low parts
+constexpr uint32_t OFF_R = OFF_XL + 32768;       // 80 KB region reused across phases
+constexpr uint32_t OFF_KB_HI = OFF_R;            // [64 rows j][128 K c]
+constexpr uint32_t OFF_KB_LO = OFF_R + 16384;
+constexpr uint32_t OFF_KHT = OFF_R + 32768;      // [128 rows c][64 K j]
+constexpr uint32_t OFF_VT_HI = OFF_R + 49152;    // [128 rows j'][64 K j]
+constexpr uint32_t OFF_VT_LO = OFF_R + 65536;
+constexpr uint32_t OFF_SCR_A = OFF_R;            // fp32 64x64 (T solve), over Kb
+constexpr uint32_t OFF_SCR_T = OFF_R + 16384;
+constexpr uint32_t OFF_ST_HI = OFF_R;            // [128 rows j][128 K c], over Kb/KhT/vT
+constexpr uint32_t OFF_ST_LO = OFF_R + 32768;
+constexpr uint32_t OFF_WP = OFF_R + 65536;       // [64 rows i][128 K c]
+constexpr uint32_t OFF_VPT_HI = OFF_R;           // [128 rows j][64 K i], over S'^T
+constexpr uint32_t OFF_VPT_LO = OFF_R + 16384;
+constexpr uint32_t OFF_KBT_HI = OFF_R + 81920;   // [128 rows c][64 K i]
+constexpr uint32_t OFF_KBT_LO = OFF_KBT_HI + 16384;
+constexpr uint32_t OFF_AQK_HI = OFF_KBT_LO + 16384;   // [64 rows i][64 K i']
+constexpr uint32_t OFF_AQK_LO = OFF_AQK_HI + 8192;
+constexpr uint32_t OFF_TB = OFF_AQK_LO + 8192;        // [64 rows i][64 K j]
+constexpr uint32_t OFF_CONVW = OFF_TB + 8192;         // fp32 [384][4]
+constexpr uint32_t OFF_BETA = OFF_CONVW + 384 * 4 * 4;
+constexpr uint32_t OFF_REF = OFF_BETA + 256;          // r per channel
+constexpr uint32_t OFF_GL = OFF_REF + 512;            // G_last per channel
+constexpr uint32_t OFF_G0 = OFF_GL + 512;             // G_first per channel
+constexpr uint32_t OFF_FCOL = OFF_G0 + 512;           // state column factor for this chunk
+constexpr uint32_t OFF_LOGF = OFF_FCOL + 512;         // log of the basis factor carried in TMEM
+constexpr uint32_t OFF_SCAN = OFF_LOGF + 512;         // [8 warps][128] fp32 partial sums
+constexpr uint32_t OFF_MISC = OFF_SCAN + 4096;        // mbarrier (8 B), tmem slot, flag
+constexpr uint32_t kSmemUsed = OFF_MISC + 64;
+constexpr uint32_t kSmemBytes = kSmemUsed + 1024;     // + alignment slack
+
+struct TcArgs {
+    PrefillArgs p;
+    const float *conv_w;     // [2*H*128 + H*128, W] or null
+    float *conv_state;       // [N, W-1, 3*H*128] or null
+    int W;
+};
+
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+__device__ __forceinline__ void split_bf16(float x, float &hi, float &lo) {
+    hi = __bfloat162float(__float2bfloat16_rn(x));
+    lo = x - hi;
+}
+__device__ __forceinline__ int sidx(int r, int c) { return r * 64 + (c ^ (r & 31)); }   // fp32 64x64 scratch
+
+// Element (row, c) of a K-major tile whose K extent is 128 (two 64-wide atoms of rows*128 B each).
+__device__ __forceinline__ uint32_t kmaj128(uint32_t rows, uint32_t row, uint32_t c) {
+    return (c >> 6) * rows * 128u + sw128_offset(row, c & 63u);
+}
+
+__global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(TcArgs A) {
+    extern __shared__ uint8_t smraw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
+    const PrefillArgs &a = A.p;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int nh = blockIdx.x, n = nh / a.H, h = nh % a.H;
+    const int H = a.H;
+    const uint32_t sbase = smem_u32(sm);
+    float *sBeta = reinterpret_cast<float *>(sm + OFF_BETA);
+    float *sRef = reinterpret_cast<float *>(sm + OFF_REF);
+    float *sGL = reinterpret_cast<float *>(sm + OFF_GL);
+    float *sG0 = reinterpret_cast<float *>(sm + OFF_G0);
+    float *sFcol = reinterpret_cast<float *>(sm + OFF_FCOL);
+    float *sLogf = reinterpret_cast<float *>(sm + OFF_LOGF);
+    float *sScan = reinterpret_cast<float *>(sm + OFF_SCAN);
+    float *sConvW = reinterpret_cast<float *>(sm + OFF_CONVW);
+    float *scrA = reinterpret_cast<float *>(sm + OFF_SCR_A);
+    float *scrT = reinterpret_cast<float *>(sm + OFF_SCR_T);
+    uint64_t *mbar = reinterpret_cast<uint64_t *>(sm + OFF_MISC);
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + OFF_MISC + 8);
+    volatile uint32_t *sflag = reinterpret_cast<volatile uint32_t *>(sm + OFF_MISC + 16);
+    const uint32_t mbar_a = smem_u32(mbar);
+
+    int tb, te;
+    seq_bounds(a.cu, n, a.T, tb, te);
+    const int W = A.conv_w ? A.W : 0;
+    const int Dall = 3 * H * kD;
+
+    // ---- set-up: TMEM, barrier, conv weights, initial state ----
+    if (warp == 0) { tmem_alloc(smem_u32(tslot), kTmemCols); tmem_relinquish(); }
+    if (tid == 0) { mbar_init(mbar_a, 1); fence_mbar_init(); *sflag = 0; }
+    if (W > 0)
+        for (int e = tid; e < 384 * 4; e += kThreads) {
+            // taps right-aligned in a 4-wide window: tap t' multiplies token i - 3 + t'
+            const int ch = e >> 2, t = e & 3;
+            const int gch = (ch >> 7) * H * kD + h * kD + (ch & 127);
+            sConvW[e] = t >= 4 - W ? A.conv_w[(size_t)gch * W + (t - (4 - W))] : 0.f;
+        }
+    if (tid < kD) sLogf[tid] = 0.f;
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = *tslot;
+    const uint32_t lrow = 32u * (warp & 3);             // first TMEM lane of this warp
+    const uint32_t tl = tbase + (lrow << 16);
+    const int half = warp >> 2;                          // which column half this warp handles
+    {   // S'^T <- S0^T (true state; basis factor 1)
+        const int j = lrow + lane;
+        for (int cb = 0; cb < 64; cb += 16) {
+            uint32_t r[16];
+#pragma unroll
+            for (int u = 0; u < 16; ++u) {
+                const int c = half * 64 + cb + u;
+                r[u] = __float_as_uint(a.S0 ? a.S0[((size_t)nh * kD + c) * kD + j] : 0.f);
+            }
+            tmem_st16(tl + kColS + half * 64 + cb, r);
+        }
+        tmem_wait_st();
+    }
+    uint32_t phase = 0;
+    bool failed = false;
+
+    auto mma_wait = [&]() -> bool {
+        if (tid == 0) {
+            if (!mbar_wait_bounded(mbar_a, phase, kWaitLimit)) {
+                *sflag = 1;
+                atomicOr(a.status, 1u);
+            }
+        }
+        phase ^= 1u;
+        __syncthreads();
+        const bool bad = *sflag != 0;
+        tc_fence_after();
+        return !bad;
+    };
+
+    for (int cs = tb; cs < te; cs += kC) {
+        const int Lc = min(kC, te - cs);
+        // ================= prep: conv, norm, decay, operands =================
+        // thread owns tokens i0..i0+7 (i0 = 8*warp) and channels c0..c0+3 (c0 = 4*lane)
+        const int i0 = warp * 8, c0 = lane * 4;
+        float G[8][4];
+        {
+            float run[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int ii = 0; ii < 8; ++ii) {
+                const int i = i0 + ii;
+                float4 gv = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (i < Lc) gv = *reinterpret_cast<const float4 *>(a.g + ((size_t)(cs + i) * H + h) * kD + c0);
+                run[0] += gv.x; run[1] += gv.y; run[2] += gv.z; run[3] += gv.w;
+#pragma unroll
+                for (int m = 0; m < 4; ++m) G[ii][m] = run[m];
+            }
+#pragma unroll
+            for (int m = 0; m < 4; ++m) sScan[warp * kD + c0 + m] = run[m];
+        }
+        if (tid < kC) sBeta[tid] = tid < Lc ? a.beta[(size_t)(cs + tid) * H + h] : 0.f;
+        __syncthreads();
+        {
+            float off[4] = {0.f, 0.f, 0.f, 0.f};
+            for (int w2 = 0; w2 < warp; ++w2)
+#pragma unroll
+                for (int m = 0; m < 4; ++m) off[m] += sScan[w2 * kD + c0 + m];
+#pragma unroll
+            for (int ii = 0; ii < 8; ++ii)
+#pragma unroll
+                for (int m = 0; m < 4; ++m) G[ii][m] += off[m];
+            if (warp == 0)
+#pragma unroll
+                for (int m = 0; m < 4; ++m) sG0[c0 + m] = G[0][m];
+            if (warp == 7)
+#pragma unroll
+                for (int m = 0; m < 4; ++m) sGL[c0 + m] = G[7][m];
+        }
+        __syncthreads();
+        if (tid < kD) {
+            const float r = 0.5f * (sG0[tid] + sGL[tid]);
+            sRef[tid] = r;
+            sFcol[tid] = expf(sLogf[tid] + r);     // TMEM basis -> this chunk's S' = exp(r) S
+        }
+        __syncthreads();
+        float E[8][4], Eb[8][4];
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+            const float r = sRef[c0 + m];
+#pragma unroll
+            for (int ii = 0; ii < 8; ++ii) {
+                const float x = fminf(fmaxf(G[ii][m] - r, -87.f), 87.f);
+                E[ii][m] = __expf(x);
+                Eb[ii][m] = __expf(-x);
+            }
+        }
+        // --- q, k, v: load (+conv +SiLU) for 8 tokens x 4 channels, then norms ---
+        auto load_qkv = [&](int which, float (&y)[8][4]) {
+            const void *src = which == 0 ? a.q : (which == 1 ? a.k : a.v);
+            const int chbase = which * kD;        // channel index in this head's conv slice
+            const int gch0 = which * H * kD + h * kD + c0;   // global conv channel of c0
+            float x[11][4];
+#pragma unroll
+            for (int t = 0; t < 11; ++t) {
+                const int i = i0 - 3 + t;         // chunk-local token
+                const int pos = cs + i;           // absolute token
+#pragma unroll
+                for (int m = 0; m < 4; ++m) x[t][m] = 0.f;
+                if (t < 3 && W == 0) continue;
+                if (i >= Lc) continue;
+                if (pos >= tb) {
+                    const uint2 raw = *reinterpret_cast<const uint2 *>(
+                        reinterpret_cast<const __nv_bfloat16 *>(src) + ((size_t)pos * H + h) * kD + c0);
+                    const __nv_bfloat162 p0 = *reinterpret_cast<const __nv_bfloat162 *>(&raw.x);
+                    const __nv_bfloat162 p1 = *reinterpret_cast<const __nv_bfloat162 *>(&raw.y);
+                    x[t][0] = __low2float(p0); x[t][1] = __high2float(p0);
+                    x[t][2] = __low2float(p1); x[t][3] = __high2float(p1);
+                } else if (A.conv_state != nullptr && W > 1) {
+                    const int row = (W - 1) + (pos - tb);
+                    if (row >= 0) {
+                        const float4 cv = *reinterpret_cast<const float4 *>(
+                            A.conv_state + ((size_t)n * (W - 1) + row) * Dall + gch0);
+                        x[t][0] = cv.x; x[t][1] = cv.y; x[t][2] = cv.z; x[t][3] = cv.w;
+                    }
+                }
+            }
+#pragma unroll
+            for (int ii = 0; ii < 8; ++ii) {
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                    float acc;
+                    if (W > 0) {
+                        const float4 w = *reinterpret_cast<const float4 *>(sConvW + (chbase + c0 + m) * 4);
+                        acc = w.x * x[ii][m];
+                        acc = fmaf(w.y, x[ii + 1][m], acc);
+                        acc = fmaf(w.z, x[ii + 2][m], acc);
+                        acc = fmaf(w.w, x[ii + 3][m], acc);
+                        acc = acc / (1.0f + __expf(-acc));
+                    } else {
+                        acc = x[ii + 3][m];
+                    }
+                    y[ii][m] = (i0 + ii < Lc) ? acc : 0.f;
+                }
+            }
+        };
+        auto l2 = [&](float (&y)[8][4]) {
+            if (!a.l2) return;
+#pragma unroll
+            for (int ii = 0; ii < 8; ++ii) {
+                float ss = y[ii][0] * y[ii][0] + y[ii][1] * y[ii][1] + y[ii][2] * y[ii][2] + y[ii][3] * y[ii][3];
+                ss = warp_sum(ss);
+                const float inv = 1.0f / sqrtf(ss + K3KDA_L2_EPS);
+#pragma unroll
+                for (int m = 0; m < 4; ++m) y[ii][m] *= inv;
+            }
+        };
+        // row-major [token][c] writes (8 B per token) into a 128-row or 64-row K=128 tile
+        auto put_rows = [&](uint32_t off, uint32_t rows, int row0, const float (&v)[8][4]) {
+#pragma unroll
+            for (int ii = 0; ii < 8; ++ii) {
+                uint2 u;
+                u.x = pack_bf16(v[ii][0], v[ii][1]);
+                u.y = pack_bf16(v[ii][2], v[ii][3]);
+                *reinterpret_cast<uint2 *>(sm + off + kmaj128(rows, row0 + i0 + ii, c0)) = u;
+            }
+        };
+        // transposed [c][token] writes (16 B = 8 tokens per channel) into a 128-row K=64 tile;
+        // the channel order is rotated per lane pair so a warp store hits 8 distinct 16 B bank groups
+        auto put_cols = [&](uint32_t off, const float (&v)[8][4]) {
+#pragma unroll
+            for (int mm = 0; mm < 4; ++mm) {
+                const int m = (mm + (lane >> 1)) & 3;
+                float t0[8];
+#pragma unroll
+                for (int ii = 0; ii < 8; ++ii)
+                    t0[ii] = m == 0 ? v[ii][0] : (m == 1 ? v[ii][1] : (m == 2 ? v[ii][2] : v[ii][3]));
+                uint4 u;
+                u.x = pack_bf16(t0[0], t0[1]); u.y = pack_bf16(t0[2], t0[3]);
+                u.z = pack_bf16(t0[4], t0[5]); u.w = pack_bf16(t0[6], t0[7]);
+                *reinterpret_cast<uint4 *>(sm + off + sw128_offset(c0 + m, i0)) = u;
+            }
+        };
+        {
+            float y[8][4], hi[8][4], lo[8][4];
+            // q -> Qh = q E  (rows 64..127 of X / XL)
+            load_qkv(0, y);
+            l2(y);
+#pragma unroll
+            for (int ii = 0; ii < 8; ++ii)
+#pragma unroll
+                for (int m = 0; m < 4; ++m) split_bf16(y[ii][m] * E[ii][m], hi[ii][m], lo[ii][m]);
+            put_rows(OFF_X, 128, 64, hi);
+            put_rows(OFF_XL, 128, 64, lo);
+            // k -> Kh = k E (rows 0..63 of X / XL, and Kh^T plain), Kb = k / E (rows and transposed)
+            load_qkv(1, y);
+            l2(y);
+#pragma unroll
+            for (int ii = 0; ii < 8; ++ii)
+#pragma unroll
+                for (int m = 0; m < 4; ++m) split_bf16(y[ii][m] * E[ii][m], hi[ii][m], lo[ii][m]);
+            put_rows(OFF_X, 128, 0, hi);
+            put_rows(OFF_XL, 128, 0, lo);
+            put_cols(OFF_KHT, hi);
+#pragma unroll
+            for (int ii = 0; ii < 8; ++ii)
+#pragma unroll
+                for (int m = 0; m < 4; ++m) split_bf16(y[ii][m] * Eb[ii][m], hi[ii][m], lo[ii][m]);
+            put_rows(OFF_KB_HI, 64, 0, hi);
+            put_rows(OFF_KB_LO, 64, 0, lo);
+            put_cols(OFF_KBT_HI, hi);
+            put_cols(OFF_KBT_LO, lo);
+            // v -> v^T (hi/lo; lo is zero unless the conv made v inexact)
+            load_qkv(2, y);
+#pragma unroll
+            for (int ii = 0; ii < 8; ++ii)
+#pragma unroll
+                for (int m = 0; m < 4; ++m) split_bf16(y[ii][m], hi[ii][m], lo[ii][m]);
+            put_cols(OFF_VT_HI, hi);
+            put_cols(OFF_VT_LO, lo);
+        }
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        // ================= MMA: [Kh; Qh] Kb^T  -> Akk | Aqk =================
+        if (tid == 0) {
+            tc_fence_after();
+            const uint32_t id = idesc_bf16_f32(128, 64);
+            const uint32_t xa[3] = {sbase + OFF_X, sbase + OFF_X, sbase + OFF_XL};
+            const uint32_t kb[3] = {sbase + OFF_KB_HI, sbase + OFF_KB_LO, sbase + OFF_KB_HI};
+            int cnt = 0;
+            for (int sp = 0; sp < 3; ++sp)
+                for (int kk = 0; kk < 8; ++kk, ++cnt)
+                    mma_bf16(tbase + kColA, sdesc_kmajor_sw128(xa[sp] + (kk >> 2) * 16384 + (kk & 3) * 32),
+                             sdesc_kmajor_sw128(kb[sp] + (kk >> 2) * 8192 + (kk & 3) * 32), id, cnt > 0);
+            mma_commit(mbar_a);
+        }
+        if (!mma_wait()) { failed = true; break; }
+        // ================= Akk -> fp32 scratch, Aqk -> split tile =================
+        {
+            const int colbase = half * 32;
+            uint32_t r0[16], r1[16];
+            tmem_ld16(tl + kColA + colbase, r0);
+            tmem_ld16(tl + kColA + colbase + 16, r1);
+            tmem_wait_ld();
+            const int row = lrow + lane;
+            if (row < 64) {
+                const float b = sBeta[row];
+#pragma unroll
+                for (int u = 0; u < 32; ++u) {
+                    const int j = colbase + u;
+                    const float v = __uint_as_float(u < 16 ? r0[u] : r1[u - 16]);
+                    scrA[sidx(row, j)] = j < row ? b * v : 0.f;
+                }
+            } else {
+                const int i = row - 64;
+                uint32_t hw[16], lw[16];
+#pragma unroll
+                for (int u = 0; u < 32; u += 2) {
+                    float v0 = __uint_as_float(u < 16 ? r0[u] : r1[u - 16]);
+                    float v1 = __uint_as_float(u + 1 < 16 ? r0[u + 1] : r1[u + 1 - 16]);
+                    if (colbase + u > i) v0 = 0.f;
+                    if (colbase + u + 1 > i) v1 = 0.f;
+                    float h0, l0, h1, l1;
+                    split_bf16(v0, h0, l0);
+                    split_bf16(v1, h1, l1);
+                    hw[u >> 1] = pack_bf16(h0, h1);
+                    lw[u >> 1] = pack_bf16(l0, l1);
+                }
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    const uint32_t o = sw128_offset(i, colbase + q4 * 8);
+                    *reinterpret_cast<uint4 *>(sm + OFF_AQK_HI + o) = make_uint4(hw[4 * q4], hw[4 * q4 + 1], hw[4 * q4 + 2], hw[4 * q4 + 3]);
+                    *reinterpret_cast<uint4 *>(sm + OFF_AQK_LO + o) = make_uint4(lw[4 * q4], lw[4 * q4 + 1], lw[4 * q4 + 2], lw[4 * q4 + 3]);
+                }
+            }
+        }
+        __syncthreads();
+        // ================= T = (I + Akk)^-1 in fp32, Tb = T diag(beta) =================
+        if (tid < 64) {   // diagonal 16x16 blocks, one column per thread
+            const int b = tid >> 4, col = tid & 15, ib = b * 16;
+            float x[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) x[i] = (i == col) ? 1.f : 0.f;
+#pragma unroll
+            for (int i = 1; i < 16; ++i) {
+                float s = 0.f;
+#pragma unroll
+                for (int j = 0; j < i; ++j) s = fmaf(scrA[sidx(ib + i, ib + j)], x[j], s);
+                if (i > col) x[i] = -s;
+            }
+#pragma unroll
+            for (int i = 0; i < 16; ++i) scrT[sidx(ib + i, ib + col)] = x[i];
+        }
+        __syncthreads();
+        // off-diagonal block rows by distance d = 1, 2, 3:
+        //   P = sum_{m=b}^{b+d-1} A[b+d, m] T[m, b];   T[b+d, b] = -T[b+d, b+d] P
+        for (int d = 1; d <= 3; ++d) {
+            const int nblk = 4 - d;
+            for (int e = tid; e < nblk * 256; e += kThreads) {
+                const int b = e >> 8, r = (e >> 4) & 15, c = e & 15;
+                const int R = (b + d) * 16 + r, Cc = b * 16 + c;
+                float s = 0.f;
+                for (int m = b * 16; m < (b + d) * 16; ++m) s = fmaf(scrA[sidx(R, m)], scrT[sidx(m, Cc)], s);
+                scrT[sidx(b * 16 + r, (b + d) * 16 + c)] = s;          // P parked in the upper triangle
+            }
+            __syncthreads();
+            for (int e = tid; e < nblk * 256; e += kThreads) {
+                const int b = e >> 8, r = (e >> 4) & 15, c = e & 15;
+                const int R = (b + d) * 16 + r, Cc = b * 16 + c;
+                float s = 0.f;
+#pragma unroll
+                for (int m = 0; m < 16; ++m)
+                    s = fmaf(scrT[sidx(R, (b + d) * 16 + m)], scrT[sidx(b * 16 + m, (b + d) * 16 + c)], s);
+                scrT[sidx(R, Cc)] = -s;
+            }
+            __syncthreads();
+        }
+        {
+            const int i = tid >> 2, jq = (tid & 3) * 16;
+            uint32_t w[8];
+#pragma unroll
+            for (int u = 0; u < 16; u += 2) {
+                const int j = jq + u;
+                const float t0 = j <= i ? scrT[sidx(i, j)] * sBeta[j] : 0.f;
+                const float t1 = j + 1 <= i ? scrT[sidx(i, j + 1)] * sBeta[j + 1] : 0.f;
+                w[u >> 1] = pack_bf16(t0, t1);
+            }
+            *reinterpret_cast<uint4 *>(sm + OFF_TB + sw128_offset(i, jq)) = make_uint4(w[0], w[1], w[2], w[3]);
+            *reinterpret_cast<uint4 *>(sm + OFF_TB + sw128_offset(i, jq + 8)) = make_uint4(w[4], w[5], w[6], w[7]);
+        }
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        // ================= MMA: W'^T = Kh^T Tb^T,  U^T = v^T Tb^T =================
+        if (tid == 0) {
+            tc_fence_after();
+            const uint32_t id = idesc_bf16_f32(128, 64);
+            for (int kk = 0; kk < 4; ++kk) {
+                const uint64_t bd = sdesc_kmajor_sw128(sbase + OFF_TB + kk * 32);
+                mma_bf16(tbase + kColW, sdesc_kmajor_sw128(sbase + OFF_KHT + kk * 32), bd, id, kk > 0);
+            }
+            for (int kk = 0; kk < 4; ++kk) {
+                const uint64_t bd = sdesc_kmajor_sw128(sbase + OFF_TB + kk * 32);
+                mma_bf16(tbase + kColU, sdesc_kmajor_sw128(sbase + OFF_VT_HI + kk * 32), bd, id, kk > 0);
+            }
+            if (W > 0)
+                for (int kk = 0; kk < 4; ++kk) {
+                    const uint64_t bd = sdesc_kmajor_sw128(sbase + OFF_TB + kk * 32);
+                    mma_bf16(tbase + kColU, sdesc_kmajor_sw128(sbase + OFF_VT_LO + kk * 32), bd, id, 1);
+                }
+            mma_commit(mbar_a);
+        }
+        if (!mma_wait()) { failed = true; break; }
+        // ================= W' -> B tile; S'^T = S^T diag(fcol) -> TMEM and split A tile =================
+        {
+            const int c = lrow + lane;                 // W'^T row = channel c
+            uint32_t r0[16], r1[16];
+            tmem_ld16(tl + kColW + half * 32, r0);
+            tmem_ld16(tl + kColW + half * 32 + 16, r1);
+            tmem_wait_ld();
+#pragma unroll
+            for (int u = 0; u < 32; ++u) {
+                const int i = half * 32 + u;
+                const float v = __uint_as_float(u < 16 ? r0[u] : r1[u - 16]);
+                *reinterpret_cast<__nv_bfloat16 *>(sm + OFF_WP + kmaj128(64, i, c)) = __float2bfloat16_rn(v);
+            }
+        }
+        __syncthreads();   // every read of Kb/KhT/vT regions is done before S'^T overwrites them
+        {
+            const int j = lrow + lane;
+            for (int cb = 0; cb < 64; cb += 16) {
+                uint32_t r[16];
+                tmem_ld16(tl + kColS + half * 64 + cb, r);
+                tmem_wait_ld();
+                uint32_t hw[8], lw[8];
+#pragma unroll
+                for (int u = 0; u < 16; u += 2) {
+                    const int c = half * 64 + cb + u;
+                    const float v0 = __uint_as_float(r[u]) * sFcol[c];
+                    const float v1 = __uint_as_float(r[u + 1]) * sFcol[c + 1];
+                    r[u] = __float_as_uint(v0);
+                    r[u + 1] = __float_as_uint(v1);
+                    float h0, l0, h1, l1;
+                    split_bf16(v0, h0, l0);
+                    split_bf16(v1, h1, l1);
+                    hw[u >> 1] = pack_bf16(h0, h1);
+                    lw[u >> 1] = pack_bf16(l0, l1);
+                }
+                tmem_st16(tl + kColS + half * 64 + cb, r);
+                const uint32_t o0 = half * 16384 + sw128_offset(j, cb), o1 = half * 16384 + sw128_offset(j, cb + 8);
+                *reinterpret_cast<uint4 *>(sm + OFF_ST_HI + o0) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                *reinterpret_cast<uint4 *>(sm + OFF_ST_HI + o1) = make_uint4(hw[4], hw[5], hw[6], hw[7]);
+                *reinterpret_cast<uint4 *>(sm + OFF_ST_LO + o0) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+                *reinterpret_cast<uint4 *>(sm + OFF_ST_LO + o1) = make_uint4(lw[4], lw[5], lw[6], lw[7]);
+            }
+            tmem_wait_st();
+        }
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        // ================= MMA: V'^T = U^T - S'^T W'^T;  O^T = S'^T Qh^T =================
+        if (tid == 0) {
+            tc_fence_after();
+            const uint32_t idn = idesc_bf16_f32(128, 64, true);
+            const uint32_t id = idesc_bf16_f32(128, 64);
+            const uint32_t sa[2] = {sbase + OFF_ST_HI, sbase + OFF_ST_LO};
+            for (int sp = 0; sp < 2; ++sp)
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_bf16(tbase + kColU, sdesc_kmajor_sw128(sa[sp] + (kk >> 2) * 16384 + (kk & 3) * 32),
+                             sdesc_kmajor_sw128(sbase + OFF_WP + (kk >> 2) * 8192 + (kk & 3) * 32), idn, 1);
+            const uint32_t oa[3] = {sbase + OFF_ST_HI, sbase + OFF_ST_HI, sbase + OFF_ST_LO};
+            const uint32_t ob[3] = {sbase + OFF_X, sbase + OFF_XL, sbase + OFF_X};
+            int cnt = 0;
+            for (int sp = 0; sp < 3; ++sp)
+                for (int kk = 0; kk < 8; ++kk, ++cnt)
+                    mma_bf16(tbase + kColA, sdesc_kmajor_sw128(oa[sp] + (kk >> 2) * 16384 + (kk & 3) * 32),
+                             sdesc_kmajor_sw128(ob[sp] + (kk >> 2) * 16384 + 8192 + (kk & 3) * 32), id, cnt > 0);
+            mma_commit(mbar_a);
+        }
+        if (!mma_wait()) { failed = true; break; }
+        // ================= V'^T -> split A tile =================
+        {
+            const int j = lrow + lane;
+            uint32_t r0[16], r1[16];
+            tmem_ld16(tl + kColU + half * 32, r0);
+            tmem_ld16(tl + kColU + half * 32 + 16, r1);
+            tmem_wait_ld();
+            uint32_t hw[16], lw[16];
+#pragma unroll
+            for (int u = 0; u < 32; u += 2) {
+                const float v0 = __uint_as_float(u < 16 ? r0[u] : r1[u - 16]);
+                const float v1 = __uint_as_float(u + 1 < 16 ? r0[u + 1] : r1[u + 1 - 16]);
+                float h0, l0, h1, l1;
+                split_bf16(v0, h0, l0);
+                split_bf16(v1, h1, l1);
+                hw[u >> 1] = pack_bf16(h0, h1);
+                lw[u >> 1] = pack_bf16(l0, l1);
+            }
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+                const uint32_t o = sw128_offset(j, half * 32 + q4 * 8);
+                *reinterpret_cast<uint4 *>(sm + OFF_VPT_HI + o) = make_uint4(hw[4 * q4], hw[4 * q4 + 1], hw[4 * q4 + 2], hw[4 * q4 + 3]);
+                *reinterpret_cast<uint4 *>(sm + OFF_VPT_LO + o) = make_uint4(lw[4 * q4], lw[4 * q4 + 1], lw[4 * q4 + 2], lw[4 * q4 + 3]);
+            }
+        }
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        // ================= MMA: O^T += V'^T Aqk^T;  S'^T += V'^T Kb =================
+        if (tid == 0) {
+            tc_fence_after();
+            const uint32_t id64 = idesc_bf16_f32(128, 64);
+            const uint32_t id128 = idesc_bf16_f32(128, 128);
+            const uint32_t va[3] = {sbase + OFF_VPT_HI, sbase + OFF_VPT_HI, sbase + OFF_VPT_LO};
+            const uint32_t qb[3] = {sbase + OFF_AQK_HI, sbase + OFF_AQK_LO, sbase + OFF_AQK_HI};
+            const uint32_t kb[3] = {sbase + OFF_KBT_HI, sbase + OFF_KBT_LO, sbase + OFF_KBT_HI};
+            for (int sp = 0; sp < 3; ++sp)
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_bf16(tbase + kColA, sdesc_kmajor_sw128(va[sp] + kk * 32), sdesc_kmajor_sw128(qb[sp] + kk * 32),
+                             id64, 1);
+            for (int sp = 0; sp < 3; ++sp)
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_bf16(tbase + kColS, sdesc_kmajor_sw128(va[sp] + kk * 32), sdesc_kmajor_sw128(kb[sp] + kk * 32),
+                             id128, 1);
+            mma_commit(mbar_a);
+        }
+        if (!mma_wait()) { failed = true; break; }
+        // ================= epilogue: O^T -> gate -> out; carry the basis factor =================
+        {
+            const int j = lrow + lane;
+            uint32_t r0[16], r1[16];
+            tmem_ld16(tl + kColA + half * 32, r0);
+            tmem_ld16(tl + kColA + half * 32 + 16, r1);
+            tmem_wait_ld();
+#pragma unroll
+            for (int u = 0; u < 32; ++u) {
+                const int i = half * 32 + u;
+                if (i < Lc) {
+                    float o = a.scale * __uint_as_float(u < 16 ? r0[u] : r1[u - 16]);
+                    const size_t oi = ((size_t)(cs + i) * H + h) * kD + j;
+                    if (a.gate) o = o * sigmoidf_(__bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(a.gate)[oi]));
+                    store_elt(a.out, oi, o, a.out_bf16);
+                }
+            }
+        }
+        if (tid < kD) sLogf[tid] = sGL[tid] - sRef[tid];
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+    }
+
+    if (!failed) {
+        // ---- final state: S = S'^T diag(exp(logf)) ----
+        if (a.Sfin) {
+            const int j = lrow + lane;
+            for (int cb = 0; cb < 64; cb += 16) {
+                uint32_t r[16];
+                tmem_ld16(tl + kColS + half * 64 + cb, r);
+                tmem_wait_ld();
+#pragma unroll
+                for (int u = 0; u < 16; ++u) {
+                    const int c = half * 64 + cb + u;
+                    a.Sfin[((size_t)nh * kD + c) * kD + j] = __uint_as_float(r[u]) * expf(sLogf[c]);
+                }
+            }
+        }
+        // ---- conv state: the last W-1 pre-conv inputs of this head's q, k, v channels ----
+        if (A.conv_state != nullptr && W > 1) {
+            const int L = te - tb;
+            float keep[2][3];
+#pragma unroll
+            for (int s2 = 0; s2 < 2; ++s2) {
+                const int e = tid + s2 * kThreads;
+                const int which = e >> 7, c = e & 127;
+                const int gch = which * H * kD + h * kD + c;
+                const void *src = which == 0 ? a.q : (which == 1 ? a.k : a.v);
+#pragma unroll
+                for (int r = 0; r < 3; ++r) {
+                    keep[s2][r] = 0.f;
+                    if (e < 384 && r < W - 1) {
+                        const int p = L - (W - 1) + r;
+                        keep[s2][r] = p >= 0
+                            ? __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(src)[((size_t)(tb + p) * H + h) * kD + c])
+                            : A.conv_state[((size_t)n * (W - 1) + (L + r)) * Dall + gch];
+                    }
+                }
+            }
+            __syncthreads();
+#pragma unroll
+            for (int s2 = 0; s2 < 2; ++s2) {
+                const int e = tid + s2 * kThreads;
+                const int which = e >> 7, c = e & 127;
+                const int gch = which * H * kD + h * kD + c;
+#pragma unroll
+                for (int r = 0; r < 3; ++r)
+                    if (e < 384 && r < W - 1) A.conv_state[((size_t)n * (W - 1) + r) * Dall + gch] = keep[s2][r];
+            }
+        }
+    } else if (tid == 0) {
+        mbar_wait_bounded(mbar_a, phase ^ 1u, kWaitLimit);   // let an in-flight MMA drain before freeing TMEM
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tbase, kTmemCols);
+}
+
+}  // namespace
 
 bool tc_prefill_supported(int in_bf16, int dk, int dv, int chunk) {
-    (void)in_bf16; (void)dk; (void)dv; (void)chunk;
-    return false;
+    return in_bf16 && dk == kD && dv == kD && chunk == kC;
 }
 
 size_t tc_prefill_workspace(int N, int H) { (void)N; (void)H; return 0; }
 
+cudaError_t launch_prefill_tc_fused(const PrefillArgs &p, const float *conv_w, float *conv_state, int W,
+                                    cudaStream_t s) {
+    if ((long long)p.N * p.H == 0) return cudaSuccess;
+    static bool attr_done = false;
+    if (!attr_done) {
+        cudaError_t e = cudaFuncSetAttribute(kda_prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)kSmemBytes);
+        if (e != cudaSuccess) return e;
+        attr_done = true;
+    }
+    TcArgs A{p, conv_w, conv_state, conv_w ? W : 0};
+    kda_prefill_tc_kernel<<<(unsigned)(p.N * p.H), kThreads, kSmemBytes, s>>>(A);
+    count_launch();
+    return cudaGetLastError();
+}
+
 cudaError_t launch_prefill_tc(const PrefillArgs &a, const int32_t *order, cudaStream_t s) {
-    (void)a; (void)order; (void)s;
-    return cudaErrorNotSupported;
+    (void)order;
+    return launch_prefill_tc_fused(a, nullptr, nullptr, 0, s);
 }
 
 }  // namespace k3kda

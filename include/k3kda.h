@@ -34,7 +34,8 @@
  *   - Supported head dims: dk, dv in {16, 32, ..., 128} (multiples of 16).
  *     Conv width W in {1, 2, 3, 4}.  Chunk in {16, 32, 64}.
  *   - Element types: q, k, v and gate share one type (k3kda_dtype); g, beta,
- *     conv weights and all states are FP32.  Pointers must be 16-byte aligned.
+ *     conv weights and all states are FP32.  Pointers must be 16-byte aligned,
+ *     except beta, which needs 4-byte alignment (so token slices of it work).
  *   - The L2 norm is x * (sum_c x_c^2 + eps)^(-1/2) over dk with eps =
  *     K3KDA_L2_EPS; the pages name this constant but print no value (1e-6 is
  *     used, the default of the flash-linear-attention norm it is taken from).

@@ -78,8 +78,8 @@ def test_decode_conv_widths(W):
 def test_decode_without_l2norm():
     c = KI.decode_case(seed=6, N=3, H=2, d=64)
     c.use_qk_l2norm = False
-    c.q *= 0.1
-    c.k *= 0.1
+    c.q = KI.round_bf16(c.q * 0.1)
+    c.k = KI.round_bf16(c.k * 0.1)
     _check(c)
 
 
