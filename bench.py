@@ -48,6 +48,9 @@ def parse():
                    help="prefill tokens (all heads) the CPU baseline runs; scaled to the full workload")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--prefill-tokens", type=int, default=None,
+                   help="override the prefill length (profiling captures on a smaller case; "
+                        "the JSON config records the length used)")
     return p.parse_args()
 
 
@@ -247,7 +250,7 @@ def run_ours(args, rank, world, dev, torch):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "io_dtype": "bf16", "data": "synthetic",
-        "config": {"workload": "KDA mixer step: fused prefill T=65536 H=32 d=128 chunk64 conv4 gate + "
+        "config": {"workload": f"KDA mixer step: fused prefill T={T} H=32 d=128 chunk64 conv4 gate + "
                                "decode step N=256 H=32 d=128 conv4 gate",
                    "prefill": dict(PREFILL, B=1, l2norm=True, gate=True, out="bf16"),
                    "decode": dict(DECODE, l2norm=True, gate=True, state="fp32", out="bf16"),
@@ -366,6 +369,8 @@ def run_reference(args):
 
 def main():
     args = parse()
+    if args.prefill_tokens:
+        PREFILL["T"] = int(args.prefill_tokens)
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     if args.impl == "reference":

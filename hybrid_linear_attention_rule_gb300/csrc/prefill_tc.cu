@@ -9,27 +9,28 @@
 //   Kh = k E, Qh = q E, Kb = k / E          with E = exp(G - r)
 //   Akk = diag(beta) tril(Kh Kb^T, -1),  Aqk = tril(Qh Kb^T)
 //   T  = (I + Akk)^-1,  Tb = T diag(beta)
-//   W' = Tb Kh,  U = Tb v
 //   S' = diag(exp(r)) S                        (state in the chunk's basis)
-//   V' = U - W' S'
+//   U  = Tb v,  Y = Kh S',  V' = U - Tb Y
 //   O  = scale (Qh S' + Aqk V')  [* sigmoid(gate)]
 //   S_next = diag(exp(G_last - r)) (S' + Kb^T V')
-// All exponents are of |G - r| <= half the chunk's total decay, so nothing
-// overflows for per-chunk decays below ~170 nats per channel.
+// (V' = U - W S with W = Tb Kh written as U - Tb (Kh S') so that no transposed
+// copy of Kh or W is ever materialised.)  All exponents are of |G - r| <= half
+// the chunk's total decay, so nothing overflows for per-chunk decays below
+// ~170 nats per channel.
 //
 // Precision: every MMA operand that is not exactly bf16 is split into a bf16
 // high part and a bf16 low part (x = hi + lo to ~2^-17 relative) and each
-// product is hi*hi + hi*lo + lo*hi with fp32 accumulation in TMEM; this keeps
-// the heavy-tailed state and outputs within ~1e-4 of the fp64 recurrence
-// relative to their RMS, where plain bf16 operands miss by ~10x.  Kh and Tb
-// are used in plain bf16 (their rounding stays below 2e-3 of RMS).
+// product is hi*hi + hi*lo + lo*hi with fp32 accumulation in TMEM (only v,
+// exact in bf16 without a conv, stays single).  Plain bf16 operands miss a
+// 5e-3-of-RMS bar by 5-20x because the state and outputs are heavy tailed;
+// the split keeps them near 1e-4 of RMS.
 //
 // Work layout: one CTA (8 warps) per (sequence, head); the CTA walks its
 // chunks in order.  CUDA cores build the operands in 128B-swizzled K-major
 // shared-memory tiles and invert the 64x64 unit-triangular matrix in fp32; a
 // single elected thread issues the tcgen05.mma chains; the fp32 state lives in
 // TMEM for the whole sequence.  TMEM columns: [0,64) Akk|Aqk then O^T,
-// [64,128) W'^T, [128,192) U^T then V'^T, [192,320) S'^T.
+// [64,128) Y^T, [128,192) U^T then V'^T, [192,320) S'^T.
 #include "common.cuh"
 #include "tc_ptx.cuh"
 
@@ -42,31 +43,31 @@ constexpr int kC = 64;
 constexpr int kD = 128;
 constexpr int kThreads = 256;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColA = 0, kColW = 64, kColU = 128, kColS = 192;
+constexpr uint32_t kColA = 0, kColY = 64, kColU = 128, kColS = 192;
 constexpr uint32_t kWaitLimit = 1u << 26;
 
 // shared-memory plan (byte offsets from a 1024-aligned base)
 constexpr uint32_t OFF_X = 0;                    // [128 rows][128 K] hi: Kh rows 0-63, Qh rows 64-127
 constexpr uint32_t OFF_XL = OFF_X + 32768;       // same, low parts
-constexpr uint32_t OFF_R = OFF_XL + 32768;       // 80 KB region reused across phases
-constexpr uint32_t OFF_KB_HI = OFF_R;            // [64 rows j][128 K c]
-constexpr uint32_t OFF_KB_LO = OFF_R + 16384;
-constexpr uint32_t OFF_KHT = OFF_R + 32768;      // [128 rows c][64 K j]
-constexpr uint32_t OFF_VT_HI = OFF_R + 49152;    // [128 rows j'][64 K j]
-constexpr uint32_t OFF_VT_LO = OFF_R + 65536;
-constexpr uint32_t OFF_SCR_A = OFF_R;            // fp32 64x64 (T solve), over Kb
-constexpr uint32_t OFF_SCR_T = OFF_R + 16384;
-constexpr uint32_t OFF_ST_HI = OFF_R;            // [128 rows j][128 K c], over Kb/KhT/vT
-constexpr uint32_t OFF_ST_LO = OFF_R + 32768;
-constexpr uint32_t OFF_WP = OFF_R + 65536;       // [64 rows i][128 K c]
-constexpr uint32_t OFF_VPT_HI = OFF_R;           // [128 rows j][64 K i], over S'^T
-constexpr uint32_t OFF_VPT_LO = OFF_R + 16384;
-constexpr uint32_t OFF_KBT_HI = OFF_R + 81920;   // [128 rows c][64 K i]
-constexpr uint32_t OFF_KBT_LO = OFF_KBT_HI + 16384;
-constexpr uint32_t OFF_AQK_HI = OFF_KBT_LO + 16384;   // [64 rows i][64 K i']
-constexpr uint32_t OFF_AQK_LO = OFF_AQK_HI + 8192;
-constexpr uint32_t OFF_TB = OFF_AQK_LO + 8192;        // [64 rows i][64 K j]
-constexpr uint32_t OFF_CONVW = OFF_TB + 8192;         // fp32 [384][4]
+constexpr uint32_t OFF_KB_HI = 65536;            // [64 rows j][128 K c]      (prep .. MMA A)
+constexpr uint32_t OFF_KB_LO = 81920;
+constexpr uint32_t OFF_SCR_A = 65536;            // fp32 64x64, over Kb        (T solve)
+constexpr uint32_t OFF_SCR_T = 81920;
+constexpr uint32_t OFF_VT_HI = 98304;            // [128 rows j'][64 K j]     (prep .. MMA U)
+constexpr uint32_t OFF_VT_LO = 114688;
+constexpr uint32_t OFF_ST_HI = 65536;            // [128 rows j][128 K c], over Kb/vT (S' .. MMA Y/O)
+constexpr uint32_t OFF_ST_LO = 98304;
+constexpr uint32_t OFF_YT_HI = 65536;            // [128 rows j][64 K i], over S'^T (Y .. MMA V)
+constexpr uint32_t OFF_YT_LO = 81920;
+constexpr uint32_t OFF_VPT_HI = 98304;           // [128 rows j][64 K i], over S'^T (V' .. MMA O/S)
+constexpr uint32_t OFF_VPT_LO = 114688;
+constexpr uint32_t OFF_KBT_HI = 131072;          // [128 rows c][64 K i]      (prep .. MMA S)
+constexpr uint32_t OFF_KBT_LO = 147456;
+constexpr uint32_t OFF_AQK_HI = 163840;          // [64 rows i][64 K i']      (extract .. MMA O)
+constexpr uint32_t OFF_AQK_LO = 172032;
+constexpr uint32_t OFF_TB_HI = 180224;           // [64 rows i][64 K j]       (T solve .. MMA V)
+constexpr uint32_t OFF_TB_LO = 188416;
+constexpr uint32_t OFF_CONVW = 196608;           // fp32 [384][4]
 constexpr uint32_t OFF_BETA = OFF_CONVW + 384 * 4 * 4;
 constexpr uint32_t OFF_REF = OFF_BETA + 256;          // r per channel
 constexpr uint32_t OFF_GL = OFF_REF + 512;            // G_last per channel
@@ -338,7 +339,6 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(TcArgs A) {
                 for (int m = 0; m < 4; ++m) split_bf16(y[ii][m] * E[ii][m], hi[ii][m], lo[ii][m]);
             put_rows(OFF_X, 128, 0, hi);
             put_rows(OFF_XL, 128, 0, lo);
-            put_cols(OFF_KHT, hi);
 #pragma unroll
             for (int ii = 0; ii < 8; ++ii)
 #pragma unroll
@@ -413,7 +413,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(TcArgs A) {
             }
         }
         __syncthreads();
-        // ================= T = (I + Akk)^-1 in fp32, Tb = T diag(beta) =================
+        // ================= T = (I + Akk)^-1 in fp32, Tb = T diag(beta) (hi/lo) =================
         if (tid < 64) {   // diagonal 16x16 blocks, one column per thread
             const int b = tid >> 4, col = tid & 15, ib = b * 16;
             float x[16];
@@ -455,55 +455,43 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(TcArgs A) {
         }
         {
             const int i = tid >> 2, jq = (tid & 3) * 16;
-            uint32_t w[8];
+            uint32_t hw[8], lw[8];
 #pragma unroll
             for (int u = 0; u < 16; u += 2) {
                 const int j = jq + u;
                 const float t0 = j <= i ? scrT[sidx(i, j)] * sBeta[j] : 0.f;
                 const float t1 = j + 1 <= i ? scrT[sidx(i, j + 1)] * sBeta[j + 1] : 0.f;
-                w[u >> 1] = pack_bf16(t0, t1);
+                float h0, l0, h1, l1;
+                split_bf16(t0, h0, l0);
+                split_bf16(t1, h1, l1);
+                hw[u >> 1] = pack_bf16(h0, h1);
+                lw[u >> 1] = pack_bf16(l0, l1);
             }
-            *reinterpret_cast<uint4 *>(sm + OFF_TB + sw128_offset(i, jq)) = make_uint4(w[0], w[1], w[2], w[3]);
-            *reinterpret_cast<uint4 *>(sm + OFF_TB + sw128_offset(i, jq + 8)) = make_uint4(w[4], w[5], w[6], w[7]);
+            const uint32_t o0 = sw128_offset(i, jq), o1 = sw128_offset(i, jq + 8);
+            *reinterpret_cast<uint4 *>(sm + OFF_TB_HI + o0) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+            *reinterpret_cast<uint4 *>(sm + OFF_TB_HI + o1) = make_uint4(hw[4], hw[5], hw[6], hw[7]);
+            *reinterpret_cast<uint4 *>(sm + OFF_TB_LO + o0) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+            *reinterpret_cast<uint4 *>(sm + OFF_TB_LO + o1) = make_uint4(lw[4], lw[5], lw[6], lw[7]);
         }
         fence_async_smem();
         tc_fence_before();
         __syncthreads();
-        // ================= MMA: W'^T = Kh^T Tb^T,  U^T = v^T Tb^T =================
+        // ================= MMA: U^T = v^T Tb^T =================
         if (tid == 0) {
             tc_fence_after();
             const uint32_t id = idesc_bf16_f32(128, 64);
-            for (int kk = 0; kk < 4; ++kk) {
-                const uint64_t bd = sdesc_kmajor_sw128(sbase + OFF_TB + kk * 32);
-                mma_bf16(tbase + kColW, sdesc_kmajor_sw128(sbase + OFF_KHT + kk * 32), bd, id, kk > 0);
-            }
-            for (int kk = 0; kk < 4; ++kk) {
-                const uint64_t bd = sdesc_kmajor_sw128(sbase + OFF_TB + kk * 32);
-                mma_bf16(tbase + kColU, sdesc_kmajor_sw128(sbase + OFF_VT_HI + kk * 32), bd, id, kk > 0);
-            }
-            if (W > 0)
-                for (int kk = 0; kk < 4; ++kk) {
-                    const uint64_t bd = sdesc_kmajor_sw128(sbase + OFF_TB + kk * 32);
-                    mma_bf16(tbase + kColU, sdesc_kmajor_sw128(sbase + OFF_VT_LO + kk * 32), bd, id, 1);
-                }
+            const uint32_t va[3] = {sbase + OFF_VT_HI, sbase + OFF_VT_HI, sbase + OFF_VT_LO};
+            const uint32_t tb[3] = {sbase + OFF_TB_HI, sbase + OFF_TB_LO, sbase + OFF_TB_HI};
+            const int nsplit = W > 0 ? 3 : 2;           // v is exact bf16 without a conv
+            int cnt = 0;
+            for (int sp = 0; sp < nsplit; ++sp)
+                for (int kk = 0; kk < 4; ++kk, ++cnt)
+                    mma_bf16(tbase + kColU, sdesc_kmajor_sw128(va[sp] + kk * 32), sdesc_kmajor_sw128(tb[sp] + kk * 32),
+                             id, cnt > 0);
             mma_commit(mbar_a);
         }
         if (!mma_wait()) { failed = true; break; }
-        // ================= W' -> B tile; S'^T = S^T diag(fcol) -> TMEM and split A tile =================
-        {
-            const int c = lrow + lane;                 // W'^T row = channel c
-            uint32_t r0[16], r1[16];
-            tmem_ld16(tl + kColW + half * 32, r0);
-            tmem_ld16(tl + kColW + half * 32 + 16, r1);
-            tmem_wait_ld();
-#pragma unroll
-            for (int u = 0; u < 32; ++u) {
-                const int i = half * 32 + u;
-                const float v = __uint_as_float(u < 16 ? r0[u] : r1[u - 16]);
-                *reinterpret_cast<__nv_bfloat16 *>(sm + OFF_WP + kmaj128(64, i, c)) = __float2bfloat16_rn(v);
-            }
-        }
-        __syncthreads();   // every read of Kb/KhT/vT regions is done before S'^T overwrites them
+        // ================= S'^T = S^T diag(fcol) -> TMEM and split A tile =================
         {
             const int j = lrow + lane;
             for (int cb = 0; cb < 64; cb += 16) {
@@ -536,32 +524,30 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(TcArgs A) {
         fence_async_smem();
         tc_fence_before();
         __syncthreads();
-        // ================= MMA: V'^T = U^T - S'^T W'^T;  O^T = S'^T Qh^T =================
+        // ================= MMA: Y^T = S'^T Kh^T,  O^T = S'^T Qh^T =================
         if (tid == 0) {
             tc_fence_after();
-            const uint32_t idn = idesc_bf16_f32(128, 64, true);
             const uint32_t id = idesc_bf16_f32(128, 64);
-            const uint32_t sa[2] = {sbase + OFF_ST_HI, sbase + OFF_ST_LO};
-            for (int sp = 0; sp < 2; ++sp)
-                for (int kk = 0; kk < 8; ++kk)
-                    mma_bf16(tbase + kColU, sdesc_kmajor_sw128(sa[sp] + (kk >> 2) * 16384 + (kk & 3) * 32),
-                             sdesc_kmajor_sw128(sbase + OFF_WP + (kk >> 2) * 8192 + (kk & 3) * 32), idn, 1);
-            const uint32_t oa[3] = {sbase + OFF_ST_HI, sbase + OFF_ST_HI, sbase + OFF_ST_LO};
-            const uint32_t ob[3] = {sbase + OFF_X, sbase + OFF_XL, sbase + OFF_X};
-            int cnt = 0;
-            for (int sp = 0; sp < 3; ++sp)
-                for (int kk = 0; kk < 8; ++kk, ++cnt)
-                    mma_bf16(tbase + kColA, sdesc_kmajor_sw128(oa[sp] + (kk >> 2) * 16384 + (kk & 3) * 32),
-                             sdesc_kmajor_sw128(ob[sp] + (kk >> 2) * 16384 + 8192 + (kk & 3) * 32), id, cnt > 0);
+            const uint32_t sa[3] = {sbase + OFF_ST_HI, sbase + OFF_ST_HI, sbase + OFF_ST_LO};
+            const uint32_t xb[3] = {sbase + OFF_X, sbase + OFF_XL, sbase + OFF_X};
+            for (int rowoff = 0; rowoff < 2; ++rowoff) {        // 0: Kh rows -> Y^T, 1: Qh rows -> O^T
+                const uint32_t dcol = rowoff ? kColA : kColY;
+                int cnt = 0;
+                for (int sp = 0; sp < 3; ++sp)
+                    for (int kk = 0; kk < 8; ++kk, ++cnt)
+                        mma_bf16(tbase + dcol, sdesc_kmajor_sw128(sa[sp] + (kk >> 2) * 16384 + (kk & 3) * 32),
+                                 sdesc_kmajor_sw128(xb[sp] + (kk >> 2) * 16384 + rowoff * 8192 + (kk & 3) * 32), id,
+                                 cnt > 0);
+            }
             mma_commit(mbar_a);
         }
         if (!mma_wait()) { failed = true; break; }
-        // ================= V'^T -> split A tile =================
-        {
+        // ================= split-tile writer for a [128 rows][64 K] operand from 32 TMEM columns =================
+        auto tmem_to_tile64 = [&](uint32_t col, uint32_t off_hi, uint32_t off_lo) {
             const int j = lrow + lane;
             uint32_t r0[16], r1[16];
-            tmem_ld16(tl + kColU + half * 32, r0);
-            tmem_ld16(tl + kColU + half * 32 + 16, r1);
+            tmem_ld16(tl + col + half * 32, r0);
+            tmem_ld16(tl + col + half * 32 + 16, r1);
             tmem_wait_ld();
             uint32_t hw[16], lw[16];
 #pragma unroll
@@ -577,14 +563,32 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(TcArgs A) {
 #pragma unroll
             for (int q4 = 0; q4 < 4; ++q4) {
                 const uint32_t o = sw128_offset(j, half * 32 + q4 * 8);
-                *reinterpret_cast<uint4 *>(sm + OFF_VPT_HI + o) = make_uint4(hw[4 * q4], hw[4 * q4 + 1], hw[4 * q4 + 2], hw[4 * q4 + 3]);
-                *reinterpret_cast<uint4 *>(sm + OFF_VPT_LO + o) = make_uint4(lw[4 * q4], lw[4 * q4 + 1], lw[4 * q4 + 2], lw[4 * q4 + 3]);
+                *reinterpret_cast<uint4 *>(sm + off_hi + o) = make_uint4(hw[4 * q4], hw[4 * q4 + 1], hw[4 * q4 + 2], hw[4 * q4 + 3]);
+                *reinterpret_cast<uint4 *>(sm + off_lo + o) = make_uint4(lw[4 * q4], lw[4 * q4 + 1], lw[4 * q4 + 2], lw[4 * q4 + 3]);
             }
-        }
+        };
+        // ================= Y^T -> split tile;  MMA: V'^T = U^T - Y^T Tb^T =================
+        tmem_to_tile64(kColY, OFF_YT_HI, OFF_YT_LO);
         fence_async_smem();
         tc_fence_before();
         __syncthreads();
-        // ================= MMA: O^T += V'^T Aqk^T;  S'^T += V'^T Kb =================
+        if (tid == 0) {
+            tc_fence_after();
+            const uint32_t idn = idesc_bf16_f32(128, 64, true);
+            const uint32_t ya[3] = {sbase + OFF_YT_HI, sbase + OFF_YT_HI, sbase + OFF_YT_LO};
+            const uint32_t tb[3] = {sbase + OFF_TB_HI, sbase + OFF_TB_LO, sbase + OFF_TB_HI};
+            for (int sp = 0; sp < 3; ++sp)
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_bf16(tbase + kColU, sdesc_kmajor_sw128(ya[sp] + kk * 32), sdesc_kmajor_sw128(tb[sp] + kk * 32),
+                             idn, 1);
+            mma_commit(mbar_a);
+        }
+        if (!mma_wait()) { failed = true; break; }
+        // ================= V'^T -> split tile;  MMA: O^T += V'^T Aqk^T,  S'^T += V'^T Kb =================
+        tmem_to_tile64(kColU, OFF_VPT_HI, OFF_VPT_LO);
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
         if (tid == 0) {
             tc_fence_after();
             const uint32_t id64 = idesc_bf16_f32(128, 64);
