@@ -182,6 +182,33 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(TcArgs A) {
         // ================= prep: conv, norm, decay, operands =================
         // thread owns tokens i0..i0+7 (i0 = 8*warp) and channels c0..c0+3 (c0 = 4*lane)
         const int i0 = warp * 8, c0 = lane * 4;
+        // --- q, k, v: raw loads are issued one tensor ahead of the processing (conv + SiLU,
+        //     norm, scaling, split, shared-memory writes) so their latency overlaps work ---
+        struct Raw { uint2 r[11]; float4 hs[3]; };   // bf16 rows i0-3..i0+7; conv-state history rows
+        auto issue = [&](int which, Raw &R) {
+            const void *src = which == 0 ? a.q : (which == 1 ? a.k : a.v);
+            const int gch0 = which * H * kD + h * kD + c0;   // global conv channel of c0
+#pragma unroll
+            for (int t = 0; t < 11; ++t) {
+                const int i = i0 - 3 + t;         // chunk-local token
+                const int pos = cs + i;           // absolute token
+                R.r[t] = make_uint2(0u, 0u);
+                if (t < 3) R.hs[t] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (t < 3 && W == 0) continue;
+                if (i >= Lc) continue;
+                if (pos >= tb) {
+                    R.r[t] = __ldg(reinterpret_cast<const uint2 *>(
+                        reinterpret_cast<const __nv_bfloat16 *>(src) + ((size_t)pos * H + h) * kD + c0));
+                } else if (t < 3 && A.conv_state != nullptr && W > 1) {
+                    const int row = (W - 1) + (pos - tb);
+                    if (row >= 0)
+                        R.hs[t] = __ldg(reinterpret_cast<const float4 *>(
+                            A.conv_state + ((size_t)n * (W - 1) + row) * Dall + gch0));
+                }
+            }
+        };
+        Raw rq;
+        issue(0, rq);
         float G[8][4];
         {
             float run[4] = {0.f, 0.f, 0.f, 0.f};
@@ -233,34 +260,19 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(TcArgs A) {
                 Eb[ii][m] = __expf(-x);
             }
         }
-        // --- q, k, v: load (+conv +SiLU) for 8 tokens x 4 channels, then norms ---
-        auto load_qkv = [&](int which, float (&y)[8][4]) {
-            const void *src = which == 0 ? a.q : (which == 1 ? a.k : a.v);
+        auto finish = [&](int which, const Raw &R, float (&y)[8][4]) {
             const int chbase = which * kD;        // channel index in this head's conv slice
-            const int gch0 = which * H * kD + h * kD + c0;   // global conv channel of c0
             float x[11][4];
 #pragma unroll
             for (int t = 0; t < 11; ++t) {
-                const int i = i0 - 3 + t;         // chunk-local token
-                const int pos = cs + i;           // absolute token
-#pragma unroll
-                for (int m = 0; m < 4; ++m) x[t][m] = 0.f;
-                if (t < 3 && W == 0) continue;
-                if (i >= Lc) continue;
-                if (pos >= tb) {
-                    const uint2 raw = *reinterpret_cast<const uint2 *>(
-                        reinterpret_cast<const __nv_bfloat16 *>(src) + ((size_t)pos * H + h) * kD + c0);
-                    const __nv_bfloat162 p0 = *reinterpret_cast<const __nv_bfloat162 *>(&raw.x);
-                    const __nv_bfloat162 p1 = *reinterpret_cast<const __nv_bfloat162 *>(&raw.y);
+                const int pos = cs + i0 - 3 + t;
+                if (t < 3 && pos < tb) {
+                    x[t][0] = R.hs[t].x; x[t][1] = R.hs[t].y; x[t][2] = R.hs[t].z; x[t][3] = R.hs[t].w;
+                } else {
+                    const __nv_bfloat162 p0 = *reinterpret_cast<const __nv_bfloat162 *>(&R.r[t].x);
+                    const __nv_bfloat162 p1 = *reinterpret_cast<const __nv_bfloat162 *>(&R.r[t].y);
                     x[t][0] = __low2float(p0); x[t][1] = __high2float(p0);
                     x[t][2] = __low2float(p1); x[t][3] = __high2float(p1);
-                } else if (A.conv_state != nullptr && W > 1) {
-                    const int row = (W - 1) + (pos - tb);
-                    if (row >= 0) {
-                        const float4 cv = *reinterpret_cast<const float4 *>(
-                            A.conv_state + ((size_t)n * (W - 1) + row) * Dall + gch0);
-                        x[t][0] = cv.x; x[t][1] = cv.y; x[t][2] = cv.z; x[t][3] = cv.w;
-                    }
                 }
             }
 #pragma unroll
@@ -281,27 +293,25 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(TcArgs A) {
                     y[ii][m] = (i0 + ii < Lc) ? acc : 0.f;
                 }
             }
-        };
-        auto l2 = [&](float (&y)[8][4]) {
-            if (!a.l2) return;
+            if (a.l2 && which < 2) {
 #pragma unroll
-            for (int ii = 0; ii < 8; ++ii) {
-                float ss = y[ii][0] * y[ii][0] + y[ii][1] * y[ii][1] + y[ii][2] * y[ii][2] + y[ii][3] * y[ii][3];
-                ss = warp_sum(ss);
-                const float inv = 1.0f / sqrtf(ss + K3KDA_L2_EPS);
+                for (int ii = 0; ii < 8; ++ii) {
+                    float ss = y[ii][0] * y[ii][0] + y[ii][1] * y[ii][1] + y[ii][2] * y[ii][2] + y[ii][3] * y[ii][3];
+                    ss = warp_sum(ss);
+                    const float inv = 1.0f / sqrtf(ss + K3KDA_L2_EPS);
 #pragma unroll
-                for (int m = 0; m < 4; ++m) y[ii][m] *= inv;
+                    for (int m = 0; m < 4; ++m) y[ii][m] *= inv;
+                }
             }
         };
-        // row-major [token][c] writes (8 B per token) into a 128-row or 64-row K=128 tile
-        auto put_rows = [&](uint32_t off, uint32_t rows, int row0, const float (&v)[8][4]) {
+        // one token's 4 channels, split, into row `row` of a K=128 tile (hi and lo tiles)
+        auto put_row_split = [&](uint32_t off_hi, uint32_t off_lo, uint32_t rows, int row, const float (&v)[4]) {
+            float hv[4], lv[4];
 #pragma unroll
-            for (int ii = 0; ii < 8; ++ii) {
-                uint2 u;
-                u.x = pack_bf16(v[ii][0], v[ii][1]);
-                u.y = pack_bf16(v[ii][2], v[ii][3]);
-                *reinterpret_cast<uint2 *>(sm + off + kmaj128(rows, row0 + i0 + ii, c0)) = u;
-            }
+            for (int m = 0; m < 4; ++m) split_bf16(v[m], hv[m], lv[m]);
+            const uint32_t o = kmaj128(rows, row, c0);
+            *reinterpret_cast<uint2 *>(sm + off_hi + o) = make_uint2(pack_bf16(hv[0], hv[1]), pack_bf16(hv[2], hv[3]));
+            *reinterpret_cast<uint2 *>(sm + off_lo + o) = make_uint2(pack_bf16(lv[0], lv[1]), pack_bf16(lv[2], lv[3]));
         };
         // transposed [c][token] writes (16 B = 8 tokens per channel) into a 128-row K=64 tile;
         // the channel order is rotated per lane pair so a warp store hits 8 distinct 16 B bank groups
@@ -321,34 +331,34 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(TcArgs A) {
         };
         {
             float y[8][4], hi[8][4], lo[8][4];
+            Raw rk, rv;
+            issue(1, rk);
             // q -> Qh = q E  (rows 64..127 of X / XL)
-            load_qkv(0, y);
-            l2(y);
+            finish(0, rq, y);
+            issue(2, rv);
 #pragma unroll
-            for (int ii = 0; ii < 8; ++ii)
+            for (int ii = 0; ii < 8; ++ii) {
+                float t4[4];
 #pragma unroll
-                for (int m = 0; m < 4; ++m) split_bf16(y[ii][m] * E[ii][m], hi[ii][m], lo[ii][m]);
-            put_rows(OFF_X, 128, 64, hi);
-            put_rows(OFF_XL, 128, 64, lo);
-            // k -> Kh = k E (rows 0..63 of X / XL, and Kh^T plain), Kb = k / E (rows and transposed)
-            load_qkv(1, y);
-            l2(y);
+                for (int m = 0; m < 4; ++m) t4[m] = y[ii][m] * E[ii][m];
+                put_row_split(OFF_X, OFF_XL, 128, 64 + i0 + ii, t4);
+            }
+            // k -> Kh = k E (rows 0..63 of X / XL), Kb = k / E (rows, and transposed for the state update)
+            finish(1, rk, y);
 #pragma unroll
-            for (int ii = 0; ii < 8; ++ii)
+            for (int ii = 0; ii < 8; ++ii) {
+                float t4[4], u4[4];
 #pragma unroll
-                for (int m = 0; m < 4; ++m) split_bf16(y[ii][m] * E[ii][m], hi[ii][m], lo[ii][m]);
-            put_rows(OFF_X, 128, 0, hi);
-            put_rows(OFF_XL, 128, 0, lo);
+                for (int m = 0; m < 4; ++m) { t4[m] = y[ii][m] * E[ii][m]; u4[m] = y[ii][m] * Eb[ii][m]; }
+                put_row_split(OFF_X, OFF_XL, 128, i0 + ii, t4);
+                put_row_split(OFF_KB_HI, OFF_KB_LO, 64, i0 + ii, u4);
 #pragma unroll
-            for (int ii = 0; ii < 8; ++ii)
-#pragma unroll
-                for (int m = 0; m < 4; ++m) split_bf16(y[ii][m] * Eb[ii][m], hi[ii][m], lo[ii][m]);
-            put_rows(OFF_KB_HI, 64, 0, hi);
-            put_rows(OFF_KB_LO, 64, 0, lo);
+                for (int m = 0; m < 4; ++m) split_bf16(u4[m], hi[ii][m], lo[ii][m]);
+            }
             put_cols(OFF_KBT_HI, hi);
             put_cols(OFF_KBT_LO, lo);
             // v -> v^T (hi/lo; lo is zero unless the conv made v inexact)
-            load_qkv(2, y);
+            finish(2, rv, y);
 #pragma unroll
             for (int ii = 0; ii < 8; ++ii)
 #pragma unroll
@@ -432,13 +442,18 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(TcArgs A) {
         __syncthreads();
         // off-diagonal block rows by distance d = 1, 2, 3:
         //   P = sum_{m=b}^{b+d-1} A[b+d, m] T[m, b];   T[b+d, b] = -T[b+d, b+d] P
+#pragma unroll
         for (int d = 1; d <= 3; ++d) {
             const int nblk = 4 - d;
             for (int e = tid; e < nblk * 256; e += kThreads) {
                 const int b = e >> 8, r = (e >> 4) & 15, c = e & 15;
                 const int R = (b + d) * 16 + r, Cc = b * 16 + c;
                 float s = 0.f;
-                for (int m = b * 16; m < (b + d) * 16; ++m) s = fmaf(scrA[sidx(R, m)], scrT[sidx(m, Cc)], s);
+#pragma unroll
+                for (int mm = 0; mm < 16 * d; ++mm) {
+                    const int m = b * 16 + mm;
+                    s = fmaf(scrA[sidx(R, m)], scrT[sidx(m, Cc)], s);
+                }
                 scrT[sidx(b * 16 + r, (b + d) * 16 + c)] = s;          // P parked in the upper triangle
             }
             __syncthreads();
@@ -606,6 +621,19 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(TcArgs A) {
                              id128, 1);
             mma_commit(mbar_a);
         }
+        // gate logits for this thread's 32 outputs, fetched while the last MMAs run
+        float gv[32];
+        {
+            const int j = lrow + lane;
+#pragma unroll
+            for (int u = 0; u < 32; ++u) {
+                const int i = half * 32 + u;
+                gv[u] = 0.f;
+                if (a.gate && i < Lc)
+                    gv[u] = __bfloat162float(__ldg(reinterpret_cast<const __nv_bfloat16 *>(a.gate) +
+                                                   ((size_t)(cs + i) * H + h) * kD + j));
+            }
+        }
         if (!mma_wait()) { failed = true; break; }
         // ================= epilogue: O^T -> gate -> out; carry the basis factor =================
         {
@@ -620,7 +648,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(TcArgs A) {
                 if (i < Lc) {
                     float o = a.scale * __uint_as_float(u < 16 ? r0[u] : r1[u - 16]);
                     const size_t oi = ((size_t)(cs + i) * H + h) * kD + j;
-                    if (a.gate) o = o * sigmoidf_(__bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(a.gate)[oi]));
+                    if (a.gate) o = o * sigmoidf_(gv[u]);
                     store_elt(a.out, oi, o, a.out_bf16);
                 }
             }
