@@ -21,7 +21,7 @@ import torch
 
 __all__ = ["K3KDAError", "load_library", "library_path", "F32", "BF16", "L2_EPS",
            "k3kda_version", "k3kda_status_string", "k3kda_launch_count", "k3kda_short_conv",
-           "k3kda_prefill_workspace_size", "k3kda_prefill", "k3kda_workspace_status",
+           "k3kda_prefill_workspace_size", "k3kda_prefill", "k3kda_prefill_noalloc", "k3kda_workspace_status",
            "k3kda_decode_step", "prefill", "decode_step", "short_conv"]
 
 F32, BF16 = 0, 1
@@ -72,6 +72,8 @@ def load_library(build_if_missing: bool = True):
         lib.k3kda_prefill.argtypes = [P, P, P, I, P, P, P, P, P, I, I, I, I, I, I, F, I, P, P, P, I, P,
                                       P, Z, P]
         lib.k3kda_prefill.restype = I
+        lib.k3kda_prefill_noalloc.argtypes = [P, P, P, I, P, P, P, P, P, I, I, I, I, I, I, F, I, P, P, P, I, P, P]
+        lib.k3kda_prefill_noalloc.restype = I
         lib.k3kda_workspace_status.argtypes = [P, P]
         lib.k3kda_workspace_status.restype = I
         lib.k3kda_decode_step.argtypes = [P, P, P, I, P, P, P, P, P, P, I, I, I, I, I, F, I, P, I, P]
@@ -161,6 +163,29 @@ def k3kda_prefill(q, k, v, g, beta, initial_state, cu_seqlens, cu_seqlens_host, 
                            _ptr(final_state), _ptr(workspace), workspace.numel() * workspace.element_size(),
                            _stream(stream))
     _check("k3kda_prefill", st)
+
+
+def k3kda_prefill_noalloc(q, k, v, g, beta, initial_state, cu_seqlens, cu_seqlens_host, N, T, H, dk, dv,
+                          chunk, scale, use_qk_l2norm, conv_weight, conv_state, conv_W, gate, out, final_state,
+                          stream=None):
+    """k3kda_prefill without a workspace: for callers that cannot allocate device memory where
+    they run the mixer.  The scratch is a fixed 16 MiB array the library holds on each GPU; work
+    that needs more raises K3KDAError (WORKSPACE).  The first call on a device sets up the array's
+    address and should come before any stream capture; calls that overlap on the GPU race on it."""
+    lib = load_library()
+    conv = None
+    if conv_weight is not None:
+        conv = ctypes.byref(_ConvArgs(_ptr(conv_weight), _ptr(conv_state), int(conv_W)))
+    hcu = None
+    if cu_seqlens_host is not None:
+        if cu_seqlens_host.is_cuda or cu_seqlens_host.dtype != torch.int32 or not cu_seqlens_host.is_contiguous():
+            raise ValueError("cu_seqlens_host must be a contiguous CPU int32 tensor")
+        hcu = ctypes.c_void_p(cu_seqlens_host.data_ptr())
+    st = lib.k3kda_prefill_noalloc(_ptr(q), _ptr(k), _ptr(v), _dtype(q), _ptr(g), _ptr(beta), _ptr(initial_state),
+                                   _ptr(cu_seqlens), hcu, int(N), int(T), int(H), int(dk), int(dv), int(chunk),
+                                   float(scale), int(bool(use_qk_l2norm)), conv, _ptr(gate), _ptr(out), _dtype(out),
+                                   _ptr(final_state), _stream(stream))
+    _check("k3kda_prefill_noalloc", st)
 
 
 def k3kda_workspace_status(workspace, stream=None) -> int:

@@ -1,0 +1,65 @@
+// noalloc.cu -- k3kda_prefill_noalloc: the chunked prefill without a caller
+// workspace.
+//
+// Some callers cannot allocate device memory at the point where they run the
+// mixer: code inside a custom allocator or memory pool, runtimes that forbid
+// cudaMalloc after start-up, or plug-ins that only receive pre-allocated
+// input and output buffers.  This entry point serves them.  Its scratch (the
+// status word and, for the fp32 CUDA-core shapes with a fused conv, the fp32
+// conv staging buffer) lives in a fixed-size array that the library itself
+// reserves in device memory; every GPU that loads the library holds that
+// array until the process exits.
+#include <mutex>
+
+#include "common.cuh"
+
+namespace {
+
+// 16 MiB of library-held device scratch, shared by every call on a device.
+constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void *g_noalloc_ptr[kMaxDevices] = {};
+
+}  // namespace
+
+extern "C" {
+
+size_t k3kda_prefill_workspace_size(int N, int T, int H, int dk, int dv, int chunk, int in_dtype, int has_conv);
+int k3kda_prefill(const void *q, const void *k, const void *v, int in_dtype, const float *g, const float *beta,
+                  const float *initial_state, const int32_t *cu_seqlens, const int32_t *cu_seqlens_host, int N,
+                  int T, int H, int dk, int dv, int chunk, float scale, int use_qk_l2norm,
+                  const k3kda_conv_args *conv, const void *gate, void *out, int out_dtype, float *final_state,
+                  void *workspace, size_t workspace_bytes, void *stream);
+
+int k3kda_prefill_noalloc(const void *q, const void *k, const void *v, int in_dtype, const float *g,
+                          const float *beta, const float *initial_state, const int32_t *cu_seqlens,
+                          const int32_t *cu_seqlens_host, int N, int T, int H, int dk, int dv, int chunk,
+                          float scale, int use_qk_l2norm, const k3kda_conv_args *conv, const void *gate,
+                          void *out, int out_dtype, float *final_state, void *stream) {
+    // Reject work whose scratch would not fit before touching the device.
+    const size_t need = k3kda_prefill_workspace_size(N, T, H, dk, dv, chunk, in_dtype, conv != nullptr);
+    if (need > kNoAllocScratchBytes) return K3KDA_ERR_WORKSPACE;
+    // Once per device, with that device current: find the device address of the array.
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return K3KDA_ERR_CUDA;
+    void *scratch = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_noalloc_mu);
+        if (g_noalloc_ptr[dev] == nullptr) {
+            void *p = nullptr;
+            if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return K3KDA_ERR_CUDA;
+            g_noalloc_ptr[dev] = p;
+        }
+        scratch = g_noalloc_ptr[dev];
+    }
+    // The status word must start at zero; the rest is written before it is read.
+    if (cudaMemsetAsync(scratch, 0, 256, static_cast<cudaStream_t>(stream)) != cudaSuccess) return K3KDA_ERR_CUDA;
+    return k3kda_prefill(q, k, v, in_dtype, g, beta, initial_state, cu_seqlens, cu_seqlens_host, N, T, H, dk, dv,
+                         chunk, scale, use_qk_l2norm, conv, gate, out, out_dtype, final_state, scratch,
+                         kNoAllocScratchBytes, stream);
+}
+
+}  // extern "C"

@@ -170,6 +170,37 @@ int k3kda_prefill(const void *q, const void *k, const void *v, int in_dtype,
 int k3kda_workspace_status(void *workspace, void *stream);
 
 /*
+ * k3kda_prefill_noalloc -- k3kda_prefill for callers that cannot allocate
+ * device memory where they call the mixer (inside an allocator or memory
+ * pool, in runtimes that forbid cudaMalloc after start-up, in plug-ins that
+ * are handed only their input and output buffers).  The pages have no
+ * counterpart: this is a convenience of this library.
+ *
+ * Arguments and results are those of k3kda_prefill without the workspace:
+ * the scratch comes from a 16 MiB device array that the library reserves
+ * statically (K3KDA_NOALLOC_SCRATCH_BYTES); every GPU that loads the library
+ * holds it until the process exits.  The call itself allocates nothing.
+ *   - Work whose k3kda_prefill_workspace_size() exceeds the array (only the
+ *     fp32 CUDA-core shapes with a fused conv need more than 256 bytes: their
+ *     fp32 [T, 2*H*dk + H*dv] conv staging buffer) returns
+ *     K3KDA_ERR_WORKSPACE before anything is enqueued.
+ *   - The first call on each device looks up the array's device address with
+ *     that device current; make that first call before any stream capture.
+ *   - All calls on a device share the one array and it keeps the last call's
+ *     contents.  Each call clears the status word on `stream` before its
+ *     kernels; calls whose work overlaps on the GPU (different streams, no
+ *     ordering between them) race on the array.  A timed-out in-kernel wait is
+ *     recorded in the library's array and is not reported by this call.
+ */
+#define K3KDA_NOALLOC_SCRATCH_BYTES (16u << 20)
+int k3kda_prefill_noalloc(const void *q, const void *k, const void *v, int in_dtype,
+                          const float *g, const float *beta, const float *initial_state,
+                          const int32_t *cu_seqlens, const int32_t *cu_seqlens_host,
+                          int N, int T, int H, int dk, int dv, int chunk, float scale,
+                          int use_qk_l2norm, const k3kda_conv_args *conv, const void *gate,
+                          void *out, int out_dtype, float *final_state, void *stream);
+
+/*
  * k3kda_decode_step -- one new token for each of N independent sequences
  * ("One decode token: conv update then recurrent step", metrale kda_decode_token;
  * launch_k3_kda_decode_token over a KdaDeviceState).  Per sequence n and head h:

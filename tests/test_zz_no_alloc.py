@@ -1,0 +1,66 @@
+"""k3kda_prefill_noalloc, the prefill for callers that cannot allocate device
+memory where they run the mixer (inside an allocator or memory pool, runtimes
+that forbid cudaMalloc after start-up, plug-ins handed only their buffers).
+
+It must give the same results as k3kda_prefill with a caller workspace, call
+after call (its scratch is one library-held array whose contents persist
+between calls), and must refuse work whose scratch exceeds the array.  This
+file is collected last so that a run stopping at the first failure has run
+every other test first; it also passes alone in a fresh process."""
+import pytest
+import torch
+
+import hybrid_linear_attention_rule_gb300 as K
+import kda_inputs as KI
+from parity_utils import assert_close, case_to_device, to_np
+
+pytestmark = pytest.mark.gpu
+
+
+def _noalloc(c, d, conv_state):
+    T, H, dk, dv, N = c.T, c.H, c.dk, c.dv, c.N
+    out = torch.full((T, H, dv), float("nan"), dtype=torch.float32, device="cuda")
+    fs = torch.full((N, H, dk, dv), float("nan"), dtype=torch.float32, device="cuda")
+    K.k3kda_prefill_noalloc(d["q"], d["k"], d["v"], d["g"], d["beta"], d["S0"], d["cu"].cuda(), d["cu"], N, T, H,
+                            dk, dv, c.chunk, c.scale, c.use_qk_l2norm, d["conv_w"], conv_state, c.W, d["gate"], out,
+                            fs)
+    torch.cuda.synchronize()
+    return out, fs
+
+
+@pytest.mark.parametrize("shape", ["tensor_core_d128", "fp32_path_conv_staging"])
+def test_noalloc_matches_workspace_prefill_twice(shape):
+    if shape == "tensor_core_d128":
+        c = KI.prefill_case("noalloc_tc", [130, 170], 2, 128, 128, 64, "bf16", seed=31, s0_std=0.02,
+                            gate=True, conv_width=4, conv_state=True)
+    else:   # dk = 64 runs the fp32 kernel, whose fused conv stages its output in the scratch
+        c = KI.prefill_case("noalloc_f32", [77, 123], 2, 64, 128, 64, "bf16", seed=32, s0_std=0.02,
+                            gate=True, conv_width=4, conv_state=True)
+    d = case_to_device(c)
+    cs_ref = d["conv_state"].clone()
+    ref_out, ref_fs = K.prefill(d["q"], d["k"], d["v"], d["g"], d["beta"], initial_state=d["S0"],
+                                cu_seqlens=d["cu"], chunk=c.chunk, scale=c.scale, conv_weight=d["conv_w"],
+                                conv_state=cs_ref, gate=d["gate"], out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    for call in range(2):
+        cs = d["conv_state"].clone()
+        out, fs = _noalloc(c, d, cs)
+        assert_close(to_np(out), to_np(ref_out), False, f"{shape} out, call {call}")
+        assert_close(to_np(fs), to_np(ref_fs), False, f"{shape} final state, call {call}")
+        assert torch.equal(cs, cs_ref), "conv state"
+
+
+def test_noalloc_refuses_work_larger_than_its_scratch():
+    # fp32 path with a conv: the staging buffer is T * (2*H*dk + H*dv) * 4 bytes = 32 MiB here
+    T, H, dk, dv = 8192, 4, 64, 128
+    dev = "cuda"
+    q = torch.zeros((T, H, dk), dtype=torch.bfloat16, device=dev)
+    v = torch.zeros((T, H, dv), dtype=torch.bfloat16, device=dev)
+    g = torch.zeros((T, H, dk), device=dev)
+    beta = torch.zeros((T, H), device=dev)
+    cw = torch.zeros((2 * H * dk + H * dv, 4), device=dev)
+    out = torch.zeros((T, H, dv), device=dev)
+    with pytest.raises(K.K3KDAError) as ei:
+        K.k3kda_prefill_noalloc(q, q, v, g, beta, None, None, None, 1, T, H, dk, dv, 64, dk ** -0.5, True, cw, None,
+                                4, None, out, None)
+    assert ei.value.status == -4
