@@ -145,6 +145,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(DecodeArgs a) {
         const int s = kk & 1;
         uint8_t *P = sm + s * kStageBytes;
         const int n = it / H, h = it - (it / H) * H;
+        const float bval = tid < dv ? __ldg(a.beta + it) : 0.f;   // in flight while the stage lands
         if (tid == 0 && !mbar_wait_bounded(full0 + 8 * s, (kk >> 1) & 1, kWaitLimit)) {
             *sflag = 1;
             if (a.status) atomicOr(a.status, 2u);
@@ -246,7 +247,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(DecodeArgs a) {
                 av += red[w * kMaxD + tid];
                 bv += red[(kConsumerWarps + w) * kMaxD + tid];
             }
-            const float d = a.beta[it] * (sv[tid] - av);
+            const float d = bval * (sv[tid] - av);
             sd[tid] = d;
             float o = a.scale * fmaf(qk, d, bv);
             if (a.gate) o = o / (1.0f + expf(-sgate[tid]));

@@ -25,7 +25,7 @@
 // 5e-3-of-RMS bar by 5-20x because the state and outputs are heavy tailed;
 // the split keeps them near 1e-4 of RMS.
 //
-// Work layout: one CTA (8 warps) per (sequence, head); the CTA walks its
+// Work layout: one CTA (16 warps) per (sequence, head); the CTA walks its
 // chunks in order.  CUDA cores build the operands in 128B-swizzled K-major
 // shared-memory tiles and invert the 64x64 unit-triangular matrix in fp32; a
 // single elected thread issues the tcgen05.mma chains; the fp32 state lives in
@@ -41,7 +41,9 @@ using namespace tc;
 
 constexpr int kC = 64;
 constexpr int kD = 128;
-constexpr int kThreads = 256;
+constexpr int kWarps = 16;
+constexpr int kThreads = 32 * kWarps;
+constexpr int kTok = kC / kWarps;                // tokens per thread in the prep phase (4)
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColA = 0, kColY = 64, kColU = 128, kColS = 192;
 constexpr uint32_t kWaitLimit = 1u << 26;
@@ -67,15 +69,15 @@ constexpr uint32_t OFF_AQK_HI = 163840;          // [64 rows i][64 K i']      (e
 constexpr uint32_t OFF_AQK_LO = 172032;
 constexpr uint32_t OFF_TB_HI = 180224;           // [64 rows i][64 K j]       (T solve .. MMA V)
 constexpr uint32_t OFF_TB_LO = 188416;
-constexpr uint32_t OFF_CONVW = 196608;           // fp32 [384][4]
+constexpr uint32_t OFF_CONVW = 196608;           // fp32 [4 taps][384 channels]
 constexpr uint32_t OFF_BETA = OFF_CONVW + 384 * 4 * 4;
 constexpr uint32_t OFF_REF = OFF_BETA + 256;          // r per channel
 constexpr uint32_t OFF_GL = OFF_REF + 512;            // G_last per channel
 constexpr uint32_t OFF_G0 = OFF_GL + 512;             // G_first per channel
 constexpr uint32_t OFF_FCOL = OFF_G0 + 512;           // state column factor for this chunk
 constexpr uint32_t OFF_LOGF = OFF_FCOL + 512;         // log of the basis factor carried in TMEM
-constexpr uint32_t OFF_SCAN = OFF_LOGF + 512;         // [8 warps][128] fp32 partial sums
-constexpr uint32_t OFF_MISC = OFF_SCAN + 4096;        // mbarrier (8 B), tmem slot, flag
+constexpr uint32_t OFF_SCAN = OFF_LOGF + 512;         // [16 warps][128] fp32 partial sums
+constexpr uint32_t OFF_MISC = OFF_SCAN + kWarps * kD * 4;   // mbarrier (8 B), tmem slot, flag
 constexpr uint32_t kSmemUsed = OFF_MISC + 64;
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;     // + alignment slack
 
@@ -95,10 +97,32 @@ __device__ __forceinline__ void split_bf16(float x, float &hi, float &lo) {
     lo = x - hi;
 }
 __device__ __forceinline__ int sidx(int r, int c) { return r * 64 + (c ^ (r & 31)); }   // fp32 64x64 scratch
+// z * sigmoid(z) and sigmoid(z) with the fast (2 ulp) divide; the limits are exact (0 and 1)
+__device__ __forceinline__ float silu_fast(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
+__device__ __forceinline__ float sigmoid_fast(float z) { return __fdividef(1.0f, 1.0f + __expf(-z)); }
 
 // Element (row, c) of a K-major tile whose K extent is 128 (two 64-wide atoms of rows*128 B each).
 __device__ __forceinline__ uint32_t kmaj128(uint32_t rows, uint32_t row, uint32_t c) {
     return (c >> 6) * rows * 128u + sw128_offset(row, c & 63u);
+}
+
+// 16 TMEM columns of one lane -> split bf16 into row `row` of a K=64 tile at column col0
+__device__ __forceinline__ void tile64_put16(uint8_t *sm, uint32_t off_hi, uint32_t off_lo, int row, int col0,
+                                             const float (&v)[16]) {
+    uint32_t hw[8], lw[8];
+#pragma unroll
+    for (int u = 0; u < 16; u += 2) {
+        float h0, l0, h1, l1;
+        split_bf16(v[u], h0, l0);
+        split_bf16(v[u + 1], h1, l1);
+        hw[u >> 1] = pack_bf16(h0, h1);
+        lw[u >> 1] = pack_bf16(l0, l1);
+    }
+    const uint32_t o0 = sw128_offset(row, col0), o1 = sw128_offset(row, col0 + 8);
+    *reinterpret_cast<uint4 *>(sm + off_hi + o0) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+    *reinterpret_cast<uint4 *>(sm + off_hi + o1) = make_uint4(hw[4], hw[5], hw[6], hw[7]);
+    *reinterpret_cast<uint4 *>(sm + off_lo + o0) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+    *reinterpret_cast<uint4 *>(sm + off_lo + o1) = make_uint4(lw[4], lw[5], lw[6], lw[7]);
 }
 
 __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(TcArgs A) {
@@ -134,8 +158,8 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(TcArgs A) {
     if (tid == 0) { mbar_init(mbar_a, 1); fence_mbar_init(); *sflag = 0; }
     if (W > 0)
         for (int e = tid; e < 384 * 4; e += kThreads) {
-            // taps right-aligned in a 4-wide window: tap t' multiplies token i - 3 + t'
-            const int ch = e >> 2, t = e & 3;
+            // tap-major, taps right-aligned in a 4-wide window: tap t multiplies token i - 3 + t
+            const int t = e / 384, ch = e - t * 384;
             const int gch = (ch >> 7) * H * kD + h * kD + (ch & 127);
             sConvW[e] = t >= 4 - W ? A.conv_w[(size_t)gch * W + (t - (4 - W))] : 0.f;
         }
@@ -146,17 +170,17 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(TcArgs A) {
     const uint32_t tbase = *tslot;
     const uint32_t lrow = 32u * (warp & 3);             // first TMEM lane of this warp
     const uint32_t tl = tbase + (lrow << 16);
-    const int half = warp >> 2;                          // which column half this warp handles
+    const int quarter = warp >> 2;                       // which column quarter this warp handles
     {   // S'^T <- S0^T (true state; basis factor 1)
         const int j = lrow + lane;
-        for (int cb = 0; cb < 64; cb += 16) {
+        for (int cb = 0; cb < 32; cb += 16) {
             uint32_t r[16];
 #pragma unroll
             for (int u = 0; u < 16; ++u) {
-                const int c = half * 64 + cb + u;
+                const int c = quarter * 32 + cb + u;
                 r[u] = __float_as_uint(a.S0 ? a.S0[((size_t)nh * kD + c) * kD + j] : 0.f);
             }
-            tmem_st16(tl + kColS + half * 64 + cb, r);
+            tmem_st16(tl + kColS + quarter * 32 + cb, r);
         }
         tmem_wait_st();
     }
@@ -177,19 +201,31 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(TcArgs A) {
         return !bad;
     };
 
+#ifdef K3KDA_PHASE_TIMERS
+    // optional per-phase cycle counters (thread 0), written after the status word
+    unsigned long long ph[10] = {0, 0, 0, 0, 0, 0, 0, 0, 0, 0};
+    long long tlast = clock64();
+#define PHASE(i)                                                   \
+    if (tid == 0) {                                                \
+        const long long now = clock64();                           \
+        ph[i] += (unsigned long long)(now - tlast);                \
+        tlast = now;                                               \
+    }
+#else
+#define PHASE(i)
+#endif
     for (int cs = tb; cs < te; cs += kC) {
         const int Lc = min(kC, te - cs);
         // ================= prep: conv, norm, decay, operands =================
-        // thread owns tokens i0..i0+7 (i0 = 8*warp) and channels c0..c0+3 (c0 = 4*lane)
-        const int i0 = warp * 8, c0 = lane * 4;
-        // --- q, k, v: raw loads are issued one tensor ahead of the processing (conv + SiLU,
-        //     norm, scaling, split, shared-memory writes) so their latency overlaps work ---
-        struct Raw { uint2 r[11]; float4 hs[3]; };   // bf16 rows i0-3..i0+7; conv-state history rows
+        // thread owns tokens i0..i0+3 (i0 = 4*warp) and channels c0..c0+3 (c0 = 4*lane)
+        const int i0 = warp * kTok, c0 = lane * 4;
+        // raw loads are issued one tensor ahead of the processing so their latency overlaps work
+        struct Raw { uint2 r[kTok + 3]; float4 hs[3]; };   // bf16 rows i0-3..i0+3; conv-state history rows
         auto issue = [&](int which, Raw &R) {
             const void *src = which == 0 ? a.q : (which == 1 ? a.k : a.v);
             const int gch0 = which * H * kD + h * kD + c0;   // global conv channel of c0
 #pragma unroll
-            for (int t = 0; t < 11; ++t) {
+            for (int t = 0; t < kTok + 3; ++t) {
                 const int i = i0 - 3 + t;         // chunk-local token
                 const int pos = cs + i;           // absolute token
                 R.r[t] = make_uint2(0u, 0u);
@@ -209,38 +245,37 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(TcArgs A) {
         };
         Raw rq;
         issue(0, rq);
-        float G[8][4];
+        float G[kTok][4];
         {
             float run[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int ii = 0; ii < 8; ++ii) {
+            for (int ii = 0; ii < kTok; ++ii) {
                 const int i = i0 + ii;
                 float4 gv = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (i < Lc) gv = *reinterpret_cast<const float4 *>(a.g + ((size_t)(cs + i) * H + h) * kD + c0);
+                if (i < Lc) gv = __ldg(reinterpret_cast<const float4 *>(a.g + ((size_t)(cs + i) * H + h) * kD + c0));
                 run[0] += gv.x; run[1] += gv.y; run[2] += gv.z; run[3] += gv.w;
 #pragma unroll
                 for (int m = 0; m < 4; ++m) G[ii][m] = run[m];
             }
-#pragma unroll
-            for (int m = 0; m < 4; ++m) sScan[warp * kD + c0 + m] = run[m];
+            *reinterpret_cast<float4 *>(sScan + warp * kD + c0) = make_float4(run[0], run[1], run[2], run[3]);
         }
         if (tid < kC) sBeta[tid] = tid < Lc ? a.beta[(size_t)(cs + tid) * H + h] : 0.f;
         __syncthreads();
         {
             float off[4] = {0.f, 0.f, 0.f, 0.f};
-            for (int w2 = 0; w2 < warp; ++w2)
+            for (int w2 = 0; w2 < warp; ++w2) {
+                const float4 s4 = *reinterpret_cast<const float4 *>(sScan + w2 * kD + c0);
+                off[0] += s4.x; off[1] += s4.y; off[2] += s4.z; off[3] += s4.w;
+            }
 #pragma unroll
-                for (int m = 0; m < 4; ++m) off[m] += sScan[w2 * kD + c0 + m];
-#pragma unroll
-            for (int ii = 0; ii < 8; ++ii)
+            for (int ii = 0; ii < kTok; ++ii)
 #pragma unroll
                 for (int m = 0; m < 4; ++m) G[ii][m] += off[m];
             if (warp == 0)
-#pragma unroll
-                for (int m = 0; m < 4; ++m) sG0[c0 + m] = G[0][m];
-            if (warp == 7)
-#pragma unroll
-                for (int m = 0; m < 4; ++m) sGL[c0 + m] = G[7][m];
+                *reinterpret_cast<float4 *>(sG0 + c0) = make_float4(G[0][0], G[0][1], G[0][2], G[0][3]);
+            if (warp == kWarps - 1)
+                *reinterpret_cast<float4 *>(sGL + c0) =
+                    make_float4(G[kTok - 1][0], G[kTok - 1][1], G[kTok - 1][2], G[kTok - 1][3]);
         }
         __syncthreads();
         if (tid < kD) {
@@ -249,22 +284,23 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(TcArgs A) {
             sFcol[tid] = expf(sLogf[tid] + r);     // TMEM basis -> this chunk's S' = exp(r) S
         }
         __syncthreads();
-        float E[8][4], Eb[8][4];
+        float E[kTok][4], Eb[kTok][4];
+        {
+            const float4 r4 = *reinterpret_cast<const float4 *>(sRef + c0);
+            const float rr[4] = {r4.x, r4.y, r4.z, r4.w};
 #pragma unroll
-        for (int m = 0; m < 4; ++m) {
-            const float r = sRef[c0 + m];
+            for (int m = 0; m < 4; ++m)
 #pragma unroll
-            for (int ii = 0; ii < 8; ++ii) {
-                const float x = fminf(fmaxf(G[ii][m] - r, -87.f), 87.f);
-                E[ii][m] = __expf(x);
-                Eb[ii][m] = __expf(-x);
-            }
+                for (int ii = 0; ii < kTok; ++ii) {
+                    const float x = fminf(fmaxf(G[ii][m] - rr[m], -87.f), 87.f);
+                    E[ii][m] = __expf(x);
+                    Eb[ii][m] = __expf(-x);
+                }
         }
-        auto finish = [&](int which, const Raw &R, float (&y)[8][4]) {
-            const int chbase = which * kD;        // channel index in this head's conv slice
-            float x[11][4];
+        auto finish = [&](int which, const Raw &R, float (&y)[kTok][4]) {
+            float x[kTok + 3][4];
 #pragma unroll
-            for (int t = 0; t < 11; ++t) {
+            for (int t = 0; t < kTok + 3; ++t) {
                 const int pos = cs + i0 - 3 + t;
                 if (t < 3 && pos < tb) {
                     x[t][0] = R.hs[t].x; x[t][1] = R.hs[t].y; x[t][2] = R.hs[t].z; x[t][3] = R.hs[t].w;
@@ -275,30 +311,36 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(TcArgs A) {
                     x[t][2] = __low2float(p1); x[t][3] = __high2float(p1);
                 }
             }
+            if (W > 0) {
+                float4 w4[4];
 #pragma unroll
-            for (int ii = 0; ii < 8; ++ii) {
+                for (int t = 0; t < 4; ++t)
+                    w4[t] = *reinterpret_cast<const float4 *>(sConvW + t * 384 + which * kD + c0);
 #pragma unroll
-                for (int m = 0; m < 4; ++m) {
-                    float acc;
-                    if (W > 0) {
-                        const float4 w = *reinterpret_cast<const float4 *>(sConvW + (chbase + c0 + m) * 4);
-                        acc = w.x * x[ii][m];
-                        acc = fmaf(w.y, x[ii + 1][m], acc);
-                        acc = fmaf(w.z, x[ii + 2][m], acc);
-                        acc = fmaf(w.w, x[ii + 3][m], acc);
-                        acc = acc / (1.0f + __expf(-acc));
-                    } else {
-                        acc = x[ii + 3][m];
+                for (int ii = 0; ii < kTok; ++ii) {
+                    float acc[4];
+                    acc[0] = w4[0].x * x[ii][0]; acc[1] = w4[0].y * x[ii][1];
+                    acc[2] = w4[0].z * x[ii][2]; acc[3] = w4[0].w * x[ii][3];
+#pragma unroll
+                    for (int t = 1; t < 4; ++t) {
+                        acc[0] = fmaf(w4[t].x, x[ii + t][0], acc[0]); acc[1] = fmaf(w4[t].y, x[ii + t][1], acc[1]);
+                        acc[2] = fmaf(w4[t].z, x[ii + t][2], acc[2]); acc[3] = fmaf(w4[t].w, x[ii + t][3], acc[3]);
                     }
-                    y[ii][m] = (i0 + ii < Lc) ? acc : 0.f;
+#pragma unroll
+                    for (int m = 0; m < 4; ++m) y[ii][m] = (i0 + ii < Lc) ? silu_fast(acc[m]) : 0.f;
                 }
+            } else {
+#pragma unroll
+                for (int ii = 0; ii < kTok; ++ii)
+#pragma unroll
+                    for (int m = 0; m < 4; ++m) y[ii][m] = (i0 + ii < Lc) ? x[ii + 3][m] : 0.f;
             }
             if (a.l2 && which < 2) {
 #pragma unroll
-                for (int ii = 0; ii < 8; ++ii) {
+                for (int ii = 0; ii < kTok; ++ii) {
                     float ss = y[ii][0] * y[ii][0] + y[ii][1] * y[ii][1] + y[ii][2] * y[ii][2] + y[ii][3] * y[ii][3];
                     ss = warp_sum(ss);
-                    const float inv = 1.0f / sqrtf(ss + K3KDA_L2_EPS);
+                    const float inv = rsqrtf(ss + K3KDA_L2_EPS);
 #pragma unroll
                     for (int m = 0; m < 4; ++m) y[ii][m] *= inv;
                 }
@@ -313,31 +355,29 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(TcArgs A) {
             *reinterpret_cast<uint2 *>(sm + off_hi + o) = make_uint2(pack_bf16(hv[0], hv[1]), pack_bf16(hv[2], hv[3]));
             *reinterpret_cast<uint2 *>(sm + off_lo + o) = make_uint2(pack_bf16(lv[0], lv[1]), pack_bf16(lv[2], lv[3]));
         };
-        // transposed [c][token] writes (16 B = 8 tokens per channel) into a 128-row K=64 tile;
-        // the channel order is rotated per lane pair so a warp store hits 8 distinct 16 B bank groups
-        auto put_cols = [&](uint32_t off, const float (&v)[8][4]) {
+        // transposed [c][token] writes (8 B = 4 tokens per channel) into a 128-row K=64 tile;
+        // the channel order is rotated per lane pair so a warp store spreads over the bank groups
+        auto put_cols = [&](uint32_t off, const float (&v)[kTok][4]) {
 #pragma unroll
             for (int mm = 0; mm < 4; ++mm) {
                 const int m = (mm + (lane >> 1)) & 3;
-                float t0[8];
+                float t0[kTok];
 #pragma unroll
-                for (int ii = 0; ii < 8; ++ii)
+                for (int ii = 0; ii < kTok; ++ii)
                     t0[ii] = m == 0 ? v[ii][0] : (m == 1 ? v[ii][1] : (m == 2 ? v[ii][2] : v[ii][3]));
-                uint4 u;
-                u.x = pack_bf16(t0[0], t0[1]); u.y = pack_bf16(t0[2], t0[3]);
-                u.z = pack_bf16(t0[4], t0[5]); u.w = pack_bf16(t0[6], t0[7]);
-                *reinterpret_cast<uint4 *>(sm + off + sw128_offset(c0 + m, i0)) = u;
+                *reinterpret_cast<uint2 *>(sm + off + sw128_offset(c0 + m, i0)) =
+                    make_uint2(pack_bf16(t0[0], t0[1]), pack_bf16(t0[2], t0[3]));
             }
         };
         {
-            float y[8][4], hi[8][4], lo[8][4];
+            float y[kTok][4], hi[kTok][4], lo[kTok][4];
             Raw rk, rv;
             issue(1, rk);
             // q -> Qh = q E  (rows 64..127 of X / XL)
             finish(0, rq, y);
             issue(2, rv);
 #pragma unroll
-            for (int ii = 0; ii < 8; ++ii) {
+            for (int ii = 0; ii < kTok; ++ii) {
                 float t4[4];
 #pragma unroll
                 for (int m = 0; m < 4; ++m) t4[m] = y[ii][m] * E[ii][m];
@@ -346,7 +386,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(TcArgs A) {
             // k -> Kh = k E (rows 0..63 of X / XL), Kb = k / E (rows, and transposed for the state update)
             finish(1, rk, y);
 #pragma unroll
-            for (int ii = 0; ii < 8; ++ii) {
+            for (int ii = 0; ii < kTok; ++ii) {
                 float t4[4], u4[4];
 #pragma unroll
                 for (int m = 0; m < 4; ++m) { t4[m] = y[ii][m] * E[ii][m]; u4[m] = y[ii][m] * Eb[ii][m]; }
@@ -360,7 +400,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(TcArgs A) {
             // v -> v^T (hi/lo; lo is zero unless the conv made v inexact)
             finish(2, rv, y);
 #pragma unroll
-            for (int ii = 0; ii < 8; ++ii)
+            for (int ii = 0; ii < kTok; ++ii)
 #pragma unroll
                 for (int m = 0; m < 4; ++m) split_bf16(y[ii][m], hi[ii][m], lo[ii][m]);
             put_cols(OFF_VT_HI, hi);
@@ -369,6 +409,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(TcArgs A) {
         fence_async_smem();
         tc_fence_before();
         __syncthreads();
+        PHASE(0);
         // ================= MMA: [Kh; Qh] Kb^T  -> Akk | Aqk =================
         if (tid == 0) {
             tc_fence_after();
@@ -383,96 +424,126 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(TcArgs A) {
             mma_commit(mbar_a);
         }
         if (!mma_wait()) { failed = true; break; }
+        PHASE(1);
         // ================= Akk -> fp32 scratch, Aqk -> split tile =================
         {
-            const int colbase = half * 32;
-            uint32_t r0[16], r1[16];
+            const int colbase = quarter * 16;
+            uint32_t r0[16];
             tmem_ld16(tl + kColA + colbase, r0);
-            tmem_ld16(tl + kColA + colbase + 16, r1);
             tmem_wait_ld();
             const int row = lrow + lane;
             if (row < 64) {
                 const float b = sBeta[row];
 #pragma unroll
-                for (int u = 0; u < 32; ++u) {
+                for (int u = 0; u < 16; ++u) {
                     const int j = colbase + u;
-                    const float v = __uint_as_float(u < 16 ? r0[u] : r1[u - 16]);
-                    scrA[sidx(row, j)] = j < row ? b * v : 0.f;
+                    scrA[sidx(row, j)] = j < row ? b * __uint_as_float(r0[u]) : 0.f;
                 }
             } else {
                 const int i = row - 64;
-                uint32_t hw[16], lw[16];
+                float v[16];
 #pragma unroll
-                for (int u = 0; u < 32; u += 2) {
-                    float v0 = __uint_as_float(u < 16 ? r0[u] : r1[u - 16]);
-                    float v1 = __uint_as_float(u + 1 < 16 ? r0[u + 1] : r1[u + 1 - 16]);
-                    if (colbase + u > i) v0 = 0.f;
-                    if (colbase + u + 1 > i) v1 = 0.f;
-                    float h0, l0, h1, l1;
-                    split_bf16(v0, h0, l0);
-                    split_bf16(v1, h1, l1);
-                    hw[u >> 1] = pack_bf16(h0, h1);
-                    lw[u >> 1] = pack_bf16(l0, l1);
-                }
-#pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4) {
-                    const uint32_t o = sw128_offset(i, colbase + q4 * 8);
-                    *reinterpret_cast<uint4 *>(sm + OFF_AQK_HI + o) = make_uint4(hw[4 * q4], hw[4 * q4 + 1], hw[4 * q4 + 2], hw[4 * q4 + 3]);
-                    *reinterpret_cast<uint4 *>(sm + OFF_AQK_LO + o) = make_uint4(lw[4 * q4], lw[4 * q4 + 1], lw[4 * q4 + 2], lw[4 * q4 + 3]);
-                }
+                for (int u = 0; u < 16; ++u) v[u] = colbase + u > i ? 0.f : __uint_as_float(r0[u]);
+                tile64_put16(sm, OFF_AQK_HI, OFF_AQK_LO, i, colbase, v);
             }
         }
         __syncthreads();
+        PHASE(2);
         // ================= T = (I + Akk)^-1 in fp32, Tb = T diag(beta) (hi/lo) =================
-        if (tid < 64) {   // diagonal 16x16 blocks, one column per thread
+        // diagonal 16x16 blocks by substitution (one column per thread); the upper blocks
+        // (0,1) and (2,3) that the block products read are zeroed at the same time
+        if (tid < 64) {
             const int b = tid >> 4, col = tid & 15, ib = b * 16;
             float x[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) x[i] = (i == col) ? 1.f : 0.f;
 #pragma unroll
             for (int i = 1; i < 16; ++i) {
-                float s = 0.f;
+                float s0 = 0.f, s1 = 0.f;
 #pragma unroll
-                for (int j = 0; j < i; ++j) s = fmaf(scrA[sidx(ib + i, ib + j)], x[j], s);
-                if (i > col) x[i] = -s;
+                for (int j = 0; j < i; j += 2) {
+                    s0 = fmaf(scrA[sidx(ib + i, ib + j)], x[j], s0);
+                    if (j + 1 < i) s1 = fmaf(scrA[sidx(ib + i, ib + j + 1)], x[j + 1], s1);
+                }
+                if (i > col) x[i] = -(s0 + s1);
             }
 #pragma unroll
             for (int i = 0; i < 16; ++i) scrT[sidx(ib + i, ib + col)] = x[i];
+        } else {
+            for (int e = tid - 64; e < 512; e += kThreads - 64) {
+                const int blk = e >> 8, r = (e >> 4) & 15, c = e & 15;
+                scrT[sidx(blk * 32 + r, blk * 32 + 16 + c)] = 0.f;
+            }
         }
         __syncthreads();
-        // off-diagonal block rows by distance d = 1, 2, 3:
-        //   P = sum_{m=b}^{b+d-1} A[b+d, m] T[m, b];   T[b+d, b] = -T[b+d, b+d] P
+        // level 1: T[b+1,b] = -T[b+1,b+1] (A[b+1,b] T[b,b]) for b = 0, 2; P parked in block (0, 2 + b/2)
+        {
+            const int e = tid;                               // 512 elements, one per thread
+            const int pb = e >> 8, r = (e >> 4) & 15, c = e & 15, b = 2 * pb;
+            float s0 = 0.f, s1 = 0.f;
 #pragma unroll
-        for (int d = 1; d <= 3; ++d) {
-            const int nblk = 4 - d;
-            for (int e = tid; e < nblk * 256; e += kThreads) {
-                const int b = e >> 8, r = (e >> 4) & 15, c = e & 15;
-                const int R = (b + d) * 16 + r, Cc = b * 16 + c;
-                float s = 0.f;
-#pragma unroll
-                for (int mm = 0; mm < 16 * d; ++mm) {
-                    const int m = b * 16 + mm;
-                    s = fmaf(scrA[sidx(R, m)], scrT[sidx(m, Cc)], s);
-                }
-                scrT[sidx(b * 16 + r, (b + d) * 16 + c)] = s;          // P parked in the upper triangle
+            for (int m = 0; m < 16; m += 2) {
+                s0 = fmaf(scrA[sidx((b + 1) * 16 + r, b * 16 + m)], scrT[sidx(b * 16 + m, b * 16 + c)], s0);
+                s1 = fmaf(scrA[sidx((b + 1) * 16 + r, b * 16 + m + 1)], scrT[sidx(b * 16 + m + 1, b * 16 + c)], s1);
             }
+            scrT[sidx(r, (2 + pb) * 16 + c)] = s0 + s1;
             __syncthreads();
-            for (int e = tid; e < nblk * 256; e += kThreads) {
-                const int b = e >> 8, r = (e >> 4) & 15, c = e & 15;
-                const int R = (b + d) * 16 + r, Cc = b * 16 + c;
-                float s = 0.f;
+            s0 = 0.f; s1 = 0.f;
 #pragma unroll
-                for (int m = 0; m < 16; ++m)
-                    s = fmaf(scrT[sidx(R, (b + d) * 16 + m)], scrT[sidx(b * 16 + m, (b + d) * 16 + c)], s);
-                scrT[sidx(R, Cc)] = -s;
+            for (int m = 0; m < 16; m += 2) {
+                s0 = fmaf(scrT[sidx((b + 1) * 16 + r, (b + 1) * 16 + m)], scrT[sidx(m, (2 + pb) * 16 + c)], s0);
+                s1 = fmaf(scrT[sidx((b + 1) * 16 + r, (b + 1) * 16 + m + 1)], scrT[sidx(m + 1, (2 + pb) * 16 + c)], s1);
             }
+            scrT[sidx((b + 1) * 16 + r, b * 16 + c)] = -(s0 + s1);
             __syncthreads();
         }
+        // level 2: T[32:64, 0:32] = -T2 (A[32:64, 0:32] T1); P (32x32) parked in T[0:32, 32:64]
         {
-            const int i = tid >> 2, jq = (tid & 3) * 16;
-            uint32_t hw[8], lw[8];
+            float p[2];
 #pragma unroll
-            for (int u = 0; u < 16; u += 2) {
+            for (int k2 = 0; k2 < 2; ++k2) {
+                const int e = tid + k2 * kThreads;          // 1024 elements, two per thread
+                const int r = e >> 5, c = e & 31;
+                float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+                for (int m = 0; m < 32; m += 2) {
+                    s0 = fmaf(scrA[sidx(32 + r, m)], scrT[sidx(m, c)], s0);
+                    s1 = fmaf(scrA[sidx(32 + r, m + 1)], scrT[sidx(m + 1, c)], s1);
+                }
+                p[k2] = s0 + s1;
+            }
+            // (the reads above touch only T1 and A; the park area is written after every read)
+            __syncthreads();
+#pragma unroll
+            for (int k2 = 0; k2 < 2; ++k2) {
+                const int e = tid + k2 * kThreads;
+                scrT[sidx(e >> 5, 32 + (e & 31))] = p[k2];
+            }
+            __syncthreads();
+#pragma unroll
+            for (int k2 = 0; k2 < 2; ++k2) {
+                const int e = tid + k2 * kThreads;
+                const int r = e >> 5, c = e & 31;
+                float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+                for (int m = 0; m < 32; m += 2) {
+                    s0 = fmaf(scrT[sidx(32 + r, 32 + m)], scrT[sidx(m, 32 + c)], s0);
+                    s1 = fmaf(scrT[sidx(32 + r, 32 + m + 1)], scrT[sidx(m + 1, 32 + c)], s1);
+                }
+                p[k2] = -(s0 + s1);
+            }
+#pragma unroll
+            for (int k2 = 0; k2 < 2; ++k2) {
+                const int e = tid + k2 * kThreads;
+                scrT[sidx(32 + (e >> 5), e & 31)] = p[k2];
+            }
+        }
+        __syncthreads();
+        {
+            const int i = tid >> 3, jq = (tid & 7) * 8;
+            uint32_t hw[4], lw[4];
+#pragma unroll
+            for (int u = 0; u < 8; u += 2) {
                 const int j = jq + u;
                 const float t0 = j <= i ? scrT[sidx(i, j)] * sBeta[j] : 0.f;
                 const float t1 = j + 1 <= i ? scrT[sidx(i, j + 1)] * sBeta[j + 1] : 0.f;
@@ -482,63 +553,53 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(TcArgs A) {
                 hw[u >> 1] = pack_bf16(h0, h1);
                 lw[u >> 1] = pack_bf16(l0, l1);
             }
-            const uint32_t o0 = sw128_offset(i, jq), o1 = sw128_offset(i, jq + 8);
+            const uint32_t o0 = sw128_offset(i, jq);
             *reinterpret_cast<uint4 *>(sm + OFF_TB_HI + o0) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-            *reinterpret_cast<uint4 *>(sm + OFF_TB_HI + o1) = make_uint4(hw[4], hw[5], hw[6], hw[7]);
             *reinterpret_cast<uint4 *>(sm + OFF_TB_LO + o0) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
-            *reinterpret_cast<uint4 *>(sm + OFF_TB_LO + o1) = make_uint4(lw[4], lw[5], lw[6], lw[7]);
         }
         fence_async_smem();
         tc_fence_before();
         __syncthreads();
+        PHASE(3);
         // ================= MMA: U^T = v^T Tb^T =================
         if (tid == 0) {
             tc_fence_after();
             const uint32_t id = idesc_bf16_f32(128, 64);
             const uint32_t va[3] = {sbase + OFF_VT_HI, sbase + OFF_VT_HI, sbase + OFF_VT_LO};
-            const uint32_t tb[3] = {sbase + OFF_TB_HI, sbase + OFF_TB_LO, sbase + OFF_TB_HI};
+            const uint32_t tb3[3] = {sbase + OFF_TB_HI, sbase + OFF_TB_LO, sbase + OFF_TB_HI};
             const int nsplit = W > 0 ? 3 : 2;           // v is exact bf16 without a conv
             int cnt = 0;
             for (int sp = 0; sp < nsplit; ++sp)
                 for (int kk = 0; kk < 4; ++kk, ++cnt)
-                    mma_bf16(tbase + kColU, sdesc_kmajor_sw128(va[sp] + kk * 32), sdesc_kmajor_sw128(tb[sp] + kk * 32),
+                    mma_bf16(tbase + kColU, sdesc_kmajor_sw128(va[sp] + kk * 32), sdesc_kmajor_sw128(tb3[sp] + kk * 32),
                              id, cnt > 0);
             mma_commit(mbar_a);
         }
         if (!mma_wait()) { failed = true; break; }
+        PHASE(4);
         // ================= S'^T = S^T diag(fcol) -> TMEM and split A tile =================
         {
             const int j = lrow + lane;
-            for (int cb = 0; cb < 64; cb += 16) {
+            for (int cb = 0; cb < 32; cb += 16) {
+                const int col = quarter * 32 + cb;              // state column (channel c) of u = 0
                 uint32_t r[16];
-                tmem_ld16(tl + kColS + half * 64 + cb, r);
+                tmem_ld16(tl + kColS + col, r);
                 tmem_wait_ld();
-                uint32_t hw[8], lw[8];
+                float v[16];
 #pragma unroll
-                for (int u = 0; u < 16; u += 2) {
-                    const int c = half * 64 + cb + u;
-                    const float v0 = __uint_as_float(r[u]) * sFcol[c];
-                    const float v1 = __uint_as_float(r[u + 1]) * sFcol[c + 1];
-                    r[u] = __float_as_uint(v0);
-                    r[u + 1] = __float_as_uint(v1);
-                    float h0, l0, h1, l1;
-                    split_bf16(v0, h0, l0);
-                    split_bf16(v1, h1, l1);
-                    hw[u >> 1] = pack_bf16(h0, h1);
-                    lw[u >> 1] = pack_bf16(l0, l1);
+                for (int u = 0; u < 16; ++u) {
+                    v[u] = __uint_as_float(r[u]) * sFcol[col + u];
+                    r[u] = __float_as_uint(v[u]);
                 }
-                tmem_st16(tl + kColS + half * 64 + cb, r);
-                const uint32_t o0 = half * 16384 + sw128_offset(j, cb), o1 = half * 16384 + sw128_offset(j, cb + 8);
-                *reinterpret_cast<uint4 *>(sm + OFF_ST_HI + o0) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-                *reinterpret_cast<uint4 *>(sm + OFF_ST_HI + o1) = make_uint4(hw[4], hw[5], hw[6], hw[7]);
-                *reinterpret_cast<uint4 *>(sm + OFF_ST_LO + o0) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
-                *reinterpret_cast<uint4 *>(sm + OFF_ST_LO + o1) = make_uint4(lw[4], lw[5], lw[6], lw[7]);
+                tmem_st16(tl + kColS + col, r);
+                tile64_put16(sm, OFF_ST_HI + (col >> 6) * 16384, OFF_ST_LO + (col >> 6) * 16384, j, col & 63, v);
             }
             tmem_wait_st();
         }
         fence_async_smem();
         tc_fence_before();
         __syncthreads();
+        PHASE(5);
         // ================= MMA: Y^T = S'^T Kh^T,  O^T = S'^T Qh^T =================
         if (tid == 0) {
             tc_fence_after();
@@ -557,30 +618,16 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(TcArgs A) {
             mma_commit(mbar_a);
         }
         if (!mma_wait()) { failed = true; break; }
-        // ================= split-tile writer for a [128 rows][64 K] operand from 32 TMEM columns =================
+        PHASE(6);
+        // 16 TMEM columns of this warp -> split [128 rows][64 K] tile
         auto tmem_to_tile64 = [&](uint32_t col, uint32_t off_hi, uint32_t off_lo) {
-            const int j = lrow + lane;
-            uint32_t r0[16], r1[16];
-            tmem_ld16(tl + col + half * 32, r0);
-            tmem_ld16(tl + col + half * 32 + 16, r1);
+            uint32_t r0[16];
+            tmem_ld16(tl + col + quarter * 16, r0);
             tmem_wait_ld();
-            uint32_t hw[16], lw[16];
+            float v[16];
 #pragma unroll
-            for (int u = 0; u < 32; u += 2) {
-                const float v0 = __uint_as_float(u < 16 ? r0[u] : r1[u - 16]);
-                const float v1 = __uint_as_float(u + 1 < 16 ? r0[u + 1] : r1[u + 1 - 16]);
-                float h0, l0, h1, l1;
-                split_bf16(v0, h0, l0);
-                split_bf16(v1, h1, l1);
-                hw[u >> 1] = pack_bf16(h0, h1);
-                lw[u >> 1] = pack_bf16(l0, l1);
-            }
-#pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-                const uint32_t o = sw128_offset(j, half * 32 + q4 * 8);
-                *reinterpret_cast<uint4 *>(sm + off_hi + o) = make_uint4(hw[4 * q4], hw[4 * q4 + 1], hw[4 * q4 + 2], hw[4 * q4 + 3]);
-                *reinterpret_cast<uint4 *>(sm + off_lo + o) = make_uint4(lw[4 * q4], lw[4 * q4 + 1], lw[4 * q4 + 2], lw[4 * q4 + 3]);
-            }
+            for (int u = 0; u < 16; ++u) v[u] = __uint_as_float(r0[u]);
+            tile64_put16(sm, off_hi, off_lo, lrow + lane, quarter * 16, v);
         };
         // ================= Y^T -> split tile;  MMA: V'^T = U^T - Y^T Tb^T =================
         tmem_to_tile64(kColY, OFF_YT_HI, OFF_YT_LO);
@@ -591,14 +638,15 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(TcArgs A) {
             tc_fence_after();
             const uint32_t idn = idesc_bf16_f32(128, 64, true);
             const uint32_t ya[3] = {sbase + OFF_YT_HI, sbase + OFF_YT_HI, sbase + OFF_YT_LO};
-            const uint32_t tb[3] = {sbase + OFF_TB_HI, sbase + OFF_TB_LO, sbase + OFF_TB_HI};
+            const uint32_t tb3[3] = {sbase + OFF_TB_HI, sbase + OFF_TB_LO, sbase + OFF_TB_HI};
             for (int sp = 0; sp < 3; ++sp)
                 for (int kk = 0; kk < 4; ++kk)
-                    mma_bf16(tbase + kColU, sdesc_kmajor_sw128(ya[sp] + kk * 32), sdesc_kmajor_sw128(tb[sp] + kk * 32),
+                    mma_bf16(tbase + kColU, sdesc_kmajor_sw128(ya[sp] + kk * 32), sdesc_kmajor_sw128(tb3[sp] + kk * 32),
                              idn, 1);
             mma_commit(mbar_a);
         }
         if (!mma_wait()) { failed = true; break; }
+        PHASE(7);
         // ================= V'^T -> split tile;  MMA: O^T += V'^T Aqk^T,  S'^T += V'^T Kb =================
         tmem_to_tile64(kColU, OFF_VPT_HI, OFF_VPT_LO);
         fence_async_smem();
@@ -621,55 +669,61 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(TcArgs A) {
                              id128, 1);
             mma_commit(mbar_a);
         }
-        // gate logits for this thread's 32 outputs, fetched while the last MMAs run
-        float gv[32];
+        // gate logits (raw bf16 bits) for this thread's 16 outputs, fetched while the last MMAs run
+        uint32_t graw[16];
         {
             const int j = lrow + lane;
 #pragma unroll
-            for (int u = 0; u < 32; ++u) {
-                const int i = half * 32 + u;
-                gv[u] = 0.f;
+            for (int u = 0; u < 16; ++u) {
+                const int i = quarter * 16 + u;
+                graw[u] = 0u;
                 if (a.gate && i < Lc)
-                    gv[u] = __bfloat162float(__ldg(reinterpret_cast<const __nv_bfloat16 *>(a.gate) +
-                                                   ((size_t)(cs + i) * H + h) * kD + j));
+                    graw[u] = __ldg(reinterpret_cast<const unsigned short *>(a.gate) +
+                                    ((size_t)(cs + i) * H + h) * kD + j);
             }
         }
         if (!mma_wait()) { failed = true; break; }
+        PHASE(8);
         // ================= epilogue: O^T -> gate -> out; carry the basis factor =================
         {
             const int j = lrow + lane;
-            uint32_t r0[16], r1[16];
-            tmem_ld16(tl + kColA + half * 32, r0);
-            tmem_ld16(tl + kColA + half * 32 + 16, r1);
+            uint32_t r0[16];
+            tmem_ld16(tl + kColA + quarter * 16, r0);
             tmem_wait_ld();
 #pragma unroll
-            for (int u = 0; u < 32; ++u) {
-                const int i = half * 32 + u;
+            for (int u = 0; u < 16; ++u) {
+                const int i = quarter * 16 + u;
                 if (i < Lc) {
-                    float o = a.scale * __uint_as_float(u < 16 ? r0[u] : r1[u - 16]);
-                    const size_t oi = ((size_t)(cs + i) * H + h) * kD + j;
-                    if (a.gate) o = o * sigmoidf_(gv[u]);
-                    store_elt(a.out, oi, o, a.out_bf16);
+                    float o = a.scale * __uint_as_float(r0[u]);
+                    if (a.gate) o *= sigmoid_fast(__uint_as_float(graw[u] << 16));
+                    store_elt(a.out, ((size_t)(cs + i) * H + h) * kD + j, o, a.out_bf16);
                 }
             }
         }
+        PHASE(9);
         if (tid < kD) sLogf[tid] = sGL[tid] - sRef[tid];
         tc_fence_before();
         __syncthreads();
         tc_fence_after();
     }
-
+#ifdef K3KDA_PHASE_TIMERS
+    if (tid == 0 && blockIdx.x == 0) {
+        unsigned long long *dst = reinterpret_cast<unsigned long long *>(a.status) + 8;
+        for (int i = 0; i < 10; ++i) dst[i] = ph[i];
+    }
+#endif
+#undef PHASE
     if (!failed) {
         // ---- final state: S = S'^T diag(exp(logf)) ----
         if (a.Sfin) {
             const int j = lrow + lane;
-            for (int cb = 0; cb < 64; cb += 16) {
+            for (int cb = 0; cb < 32; cb += 16) {
                 uint32_t r[16];
-                tmem_ld16(tl + kColS + half * 64 + cb, r);
+                tmem_ld16(tl + kColS + quarter * 32 + cb, r);
                 tmem_wait_ld();
 #pragma unroll
                 for (int u = 0; u < 16; ++u) {
-                    const int c = half * 64 + cb + u;
+                    const int c = quarter * 32 + cb + u;
                     a.Sfin[((size_t)nh * kD + c) * kD + j] = __uint_as_float(r[u]) * expf(sLogf[c]);
                 }
             }
@@ -677,34 +731,26 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(TcArgs A) {
         // ---- conv state: the last W-1 pre-conv inputs of this head's q, k, v channels ----
         if (A.conv_state != nullptr && W > 1) {
             const int L = te - tb;
-            float keep[2][3];
-#pragma unroll
-            for (int s2 = 0; s2 < 2; ++s2) {
-                const int e = tid + s2 * kThreads;
-                const int which = e >> 7, c = e & 127;
-                const int gch = which * H * kD + h * kD + c;
+            float keep[3] = {0.f, 0.f, 0.f};
+            const int e = tid;
+            const int which = e >> 7, c = e & 127;
+            const int gch = which * H * kD + h * kD + c;
+            if (e < 384) {
                 const void *src = which == 0 ? a.q : (which == 1 ? a.k : a.v);
 #pragma unroll
-                for (int r = 0; r < 3; ++r) {
-                    keep[s2][r] = 0.f;
-                    if (e < 384 && r < W - 1) {
+                for (int r = 0; r < 3; ++r)
+                    if (r < W - 1) {
                         const int p = L - (W - 1) + r;
-                        keep[s2][r] = p >= 0
+                        keep[r] = p >= 0
                             ? __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(src)[((size_t)(tb + p) * H + h) * kD + c])
                             : A.conv_state[((size_t)n * (W - 1) + (L + r)) * Dall + gch];
                     }
-                }
             }
             __syncthreads();
-#pragma unroll
-            for (int s2 = 0; s2 < 2; ++s2) {
-                const int e = tid + s2 * kThreads;
-                const int which = e >> 7, c = e & 127;
-                const int gch = which * H * kD + h * kD + c;
+            if (e < 384)
 #pragma unroll
                 for (int r = 0; r < 3; ++r)
-                    if (e < 384 && r < W - 1) A.conv_state[((size_t)n * (W - 1) + r) * Dall + gch] = keep[s2][r];
-            }
+                    if (r < W - 1) A.conv_state[((size_t)n * (W - 1) + r) * Dall + gch] = keep[r];
         }
     } else if (tid == 0) {
         mbar_wait_bounded(mbar_a, phase ^ 1u, kWaitLimit);   // let an in-flight MMA drain before freeing TMEM
