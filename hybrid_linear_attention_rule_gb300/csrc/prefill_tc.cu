@@ -31,6 +31,9 @@
 // single elected thread issues the tcgen05.mma chains; the fp32 state lives in
 // TMEM for the whole sequence.  TMEM columns: [0,64) Akk|Aqk then O^T,
 // [64,128) Y^T, [128,192) U^T then V'^T, [192,320) S'^T.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include "common.cuh"
 #include "tc_ptx.cuh"
 
@@ -48,44 +51,52 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColA = 0, kColY = 64, kColU = 128, kColS = 192;
 constexpr uint32_t kWaitLimit = 1u << 26;
 
-// shared-memory plan (byte offsets from a 1024-aligned base)
+// shared-memory plan (byte offsets from a 1024-aligned base).  Regions A and B
+// are reused phase by phase within a chunk; the input rows of the next chunk are
+// staged into them by bulk copies while this chunk's last MMAs run.
 constexpr uint32_t OFF_X = 0;                    // [128 rows][128 K] hi: Kh rows 0-63, Qh rows 64-127
 constexpr uint32_t OFF_XL = OFF_X + 32768;       // same, low parts
-constexpr uint32_t OFF_KB_HI = 65536;            // [64 rows j][128 K c]      (prep .. MMA A)
-constexpr uint32_t OFF_KB_LO = 81920;
-constexpr uint32_t OFF_SCR_A = 65536;            // fp32 64x64, over Kb        (T solve)
-constexpr uint32_t OFF_SCR_T = 81920;
-constexpr uint32_t OFF_VT_HI = 98304;            // [128 rows j'][64 K j]     (prep .. MMA U)
-constexpr uint32_t OFF_VT_LO = 114688;
-constexpr uint32_t OFF_ST_HI = 65536;            // [128 rows j][128 K c], over Kb/vT (S' .. MMA Y/O)
-constexpr uint32_t OFF_ST_LO = 98304;
-constexpr uint32_t OFF_YT_HI = 65536;            // [128 rows j][64 K i], over S'^T (Y .. MMA V)
+constexpr uint32_t OFF_GST = 65536;              // A: g rows fp32 [64][128]       (staged .. prep)
+constexpr uint32_t OFF_V_HI = 65536;             // A: v rows [64 j][128 j']        (prep .. MMA U, MN-major A)
+constexpr uint32_t OFF_V_LO = 81920;
+constexpr uint32_t OFF_ST_HI = 65536;            // A: S'^T [128 rows j][128 K c]   (S' .. MMA Y/O)
+constexpr uint32_t OFF_YT_HI = 65536;            // A: Y^T [128 rows j][64 K i]     (Y .. MMA V)
 constexpr uint32_t OFF_YT_LO = 81920;
-constexpr uint32_t OFF_VPT_HI = 98304;           // [128 rows j][64 K i], over S'^T (V' .. MMA O/S)
+constexpr uint32_t OFF_QST = 98304;              // B: q rows bf16 [64][128]        (staged .. prep)
+constexpr uint32_t OFF_KST = 114688;             // B: k rows bf16 [64][128]
+constexpr uint32_t OFF_SCR_A = 98304;            // B: fp32 64x64                   (T solve)
+constexpr uint32_t OFF_SCR_T = 114688;
+constexpr uint32_t OFF_ST_LO = 98304;            // B: S'^T low parts
+constexpr uint32_t OFF_VPT_HI = 98304;           // B: V'^T [128 rows j][64 K i]    (V' .. MMA O/S)
 constexpr uint32_t OFF_VPT_LO = 114688;
-constexpr uint32_t OFF_KBT_HI = 131072;          // [128 rows c][64 K i]      (prep .. MMA S)
-constexpr uint32_t OFF_KBT_LO = 147456;
+constexpr uint32_t OFF_KB_HI = 131072;           // Kb [64 rows i][128 K c]: K-major B of MMA A, MN-major B of MMA S
+constexpr uint32_t OFF_KB_LO = 147456;
 constexpr uint32_t OFF_AQK_HI = 163840;          // [64 rows i][64 K i']      (extract .. MMA O)
 constexpr uint32_t OFF_AQK_LO = 172032;
+constexpr uint32_t OFF_SCAN = OFF_AQK_HI;        // fp32 [16 warps][128] partial sums, prep only
 constexpr uint32_t OFF_TB_HI = 180224;           // [64 rows i][64 K j]       (T solve .. MMA V)
 constexpr uint32_t OFF_TB_LO = 188416;
-constexpr uint32_t OFF_CONVW = 196608;           // fp32 [4 taps][384 channels]
-constexpr uint32_t OFF_BETA = OFF_CONVW + 384 * 4 * 4;
+constexpr uint32_t OFF_VST = 196608;             // v rows bf16 [64][128] (staged .. prep)
+constexpr uint32_t OFF_CONVW = 212992;           // fp32 [4 taps][384 channels]
+constexpr uint32_t OFF_HIST = OFF_CONVW + 384 * 4 * 4;   // fp32 [3 tensors][3 rows][128]: pre-conv rows before the chunk
+constexpr uint32_t OFF_BETA = OFF_HIST + 3 * 3 * 128 * 4;
 constexpr uint32_t OFF_REF = OFF_BETA + 256;          // r per channel
 constexpr uint32_t OFF_GL = OFF_REF + 512;            // G_last per channel
 constexpr uint32_t OFF_G0 = OFF_GL + 512;             // G_first per channel
 constexpr uint32_t OFF_FCOL = OFF_G0 + 512;           // state column factor for this chunk
 constexpr uint32_t OFF_LOGF = OFF_FCOL + 512;         // log of the basis factor carried in TMEM
-constexpr uint32_t OFF_SCAN = OFF_LOGF + 512;         // [16 warps][128] fp32 partial sums
-constexpr uint32_t OFF_MISC = OFF_SCAN + kWarps * kD * 4;   // mbarrier (8 B), tmem slot, flag
+constexpr uint32_t OFF_MISC = OFF_LOGF + 512;         // mbarriers (2 x 8 B), tmem slot, flag
 constexpr uint32_t kSmemUsed = OFF_MISC + 64;
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;     // + alignment slack
+static_assert(kSmemBytes <= 232448, "shared memory plan exceeds the per-CTA limit");
 
 struct TcArgs {
+    CUtensorMap tm_q, tm_k, tm_v, tm_g;   // [T, H, 128] bf16 (q, k, v) and fp32 (g); box 64 tokens x 1 head x 128
     PrefillArgs p;
     const float *conv_w;     // [2*H*128 + H*128, W] or null
     float *conv_state;       // [N, W-1, 3*H*128] or null
     int W;
+    int box_rows;            // tokens per staged tile: min(64, T)
 };
 
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
@@ -125,7 +136,7 @@ __device__ __forceinline__ void tile64_put16(uint8_t *sm, uint32_t off_hi, uint3
     *reinterpret_cast<uint4 *>(sm + off_lo + o1) = make_uint4(lw[4], lw[5], lw[6], lw[7]);
 }
 
-__global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(TcArgs A) {
+__global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __grid_constant__ TcArgs A) {
     extern __shared__ uint8_t smraw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
     const PrefillArgs &a = A.p;
@@ -143,10 +154,12 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(TcArgs A) {
     float *sConvW = reinterpret_cast<float *>(sm + OFF_CONVW);
     float *scrA = reinterpret_cast<float *>(sm + OFF_SCR_A);
     float *scrT = reinterpret_cast<float *>(sm + OFF_SCR_T);
+    float *sHist = reinterpret_cast<float *>(sm + OFF_HIST);
     uint64_t *mbar = reinterpret_cast<uint64_t *>(sm + OFF_MISC);
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + OFF_MISC + 8);
-    volatile uint32_t *sflag = reinterpret_cast<volatile uint32_t *>(sm + OFF_MISC + 16);
-    const uint32_t mbar_a = smem_u32(mbar);
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + OFF_MISC + 16);
+    volatile uint32_t *sflag = reinterpret_cast<volatile uint32_t *>(sm + OFF_MISC + 24);
+    const uint32_t mbar_a = smem_u32(mbar);          // MMA completion
+    const uint32_t mbar_s = smem_u32(mbar + 1);      // staged input rows landed
 
     int tb, te;
     seq_bounds(a.cu, n, a.T, tb, te);
@@ -155,7 +168,16 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(TcArgs A) {
 
     // ---- set-up: TMEM, barrier, conv weights, initial state ----
     if (warp == 0) { tmem_alloc(smem_u32(tslot), kTmemCols); tmem_relinquish(); }
-    if (tid == 0) { mbar_init(mbar_a, 1); fence_mbar_init(); *sflag = 0; }
+    if (tid == 0) { mbar_init(mbar_a, 1); mbar_init(mbar_s, 1); fence_mbar_init(); *sflag = 0; }
+    // conv history of the first chunk: the conv-state rows (right-aligned), else zeros
+    for (int e = tid; e < 3 * 3 * 128; e += kThreads) {
+        const int which = e / 384, r = (e / 128) % 3, c = e & 127;
+        const int row = W - 4 + r;                   // conv-state row holding token r - 3
+        float x = 0.f;
+        if (W > 1 && A.conv_state != nullptr && row >= 0)
+            x = A.conv_state[((size_t)n * (W - 1) + row) * Dall + which * H * kD + h * kD + c];
+        sHist[e] = x;
+    }
     if (W > 0)
         for (int e = tid; e < 384 * 4; e += kThreads) {
             // tap-major, taps right-aligned in a 4-wide window: tap t multiplies token i - 3 + t
@@ -184,8 +206,28 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(TcArgs A) {
         }
         tmem_wait_st();
     }
-    uint32_t phase = 0;
+    uint32_t phase = 0, sphase = 0;
     bool failed = false;
+
+    // A chunk's input rows are brought into shared memory by tiled TMA loads (one per
+    // tensor, issued by one thread): g and v first (their regions free up earlier), then q
+    // and k, all completing one phase of mbar_s.  Rows past T arrive as zeros; rows past the
+    // sequence end are loaded but never used.
+    const uint32_t kStageBytes = (uint32_t)A.box_rows * (kD * 4 + 3 * kD * 2);
+    auto stage_gv = [&](int cs2) {
+        if (tid != 0) return;
+        fence_async_smem();
+        mbar_arrive_expect_tx(mbar_s, kStageBytes);
+        tma_load_3d(sbase + OFF_GST, &A.tm_g, 0, h, cs2, mbar_s);
+        tma_load_3d(sbase + OFF_VST, &A.tm_v, 0, h, cs2, mbar_s);
+    };
+    auto stage_qk = [&](int cs2) {
+        if (tid != 0) return;
+        fence_async_smem();
+        tma_load_3d(sbase + OFF_QST, &A.tm_q, 0, h, cs2, mbar_s);
+        tma_load_3d(sbase + OFF_KST, &A.tm_k, 0, h, cs2, mbar_s);
+    };
+    if (tb < te) { stage_gv(tb); stage_qk(tb); }
 
     auto mma_wait = [&]() -> bool {
         if (tid == 0) {
@@ -217,34 +259,16 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(TcArgs A) {
     for (int cs = tb; cs < te; cs += kC) {
         const int Lc = min(kC, te - cs);
         // ================= prep: conv, norm, decay, operands =================
-        // thread owns tokens i0..i0+3 (i0 = 4*warp) and channels c0..c0+3 (c0 = 4*lane)
+        // thread owns tokens i0..i0+3 (i0 = 4*warp) and channels c0..c0+3 (c0 = 4*lane);
+        // the chunk's input rows were staged into shared memory by bulk copies
         const int i0 = warp * kTok, c0 = lane * 4;
-        // raw loads are issued one tensor ahead of the processing so their latency overlaps work
-        struct Raw { uint2 r[kTok + 3]; float4 hs[3]; };   // bf16 rows i0-3..i0+3; conv-state history rows
-        auto issue = [&](int which, Raw &R) {
-            const void *src = which == 0 ? a.q : (which == 1 ? a.k : a.v);
-            const int gch0 = which * H * kD + h * kD + c0;   // global conv channel of c0
-#pragma unroll
-            for (int t = 0; t < kTok + 3; ++t) {
-                const int i = i0 - 3 + t;         // chunk-local token
-                const int pos = cs + i;           // absolute token
-                R.r[t] = make_uint2(0u, 0u);
-                if (t < 3) R.hs[t] = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (t < 3 && W == 0) continue;
-                if (i >= Lc) continue;
-                if (pos >= tb) {
-                    R.r[t] = __ldg(reinterpret_cast<const uint2 *>(
-                        reinterpret_cast<const __nv_bfloat16 *>(src) + ((size_t)pos * H + h) * kD + c0));
-                } else if (t < 3 && A.conv_state != nullptr && W > 1) {
-                    const int row = (W - 1) + (pos - tb);
-                    if (row >= 0)
-                        R.hs[t] = __ldg(reinterpret_cast<const float4 *>(
-                            A.conv_state + ((size_t)n * (W - 1) + row) * Dall + gch0));
-                }
-            }
-        };
-        Raw rq;
-        issue(0, rq);
+        if (tid == 0 && !mbar_wait_bounded(mbar_s, sphase, kWaitLimit)) {
+            *sflag = 1;
+            atomicOr(a.status, 1u);
+        }
+        sphase ^= 1u;
+        __syncthreads();
+        if (*sflag) { failed = true; break; }
         float G[kTok][4];
         {
             float run[4] = {0.f, 0.f, 0.f, 0.f};
@@ -252,7 +276,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(TcArgs A) {
             for (int ii = 0; ii < kTok; ++ii) {
                 const int i = i0 + ii;
                 float4 gv = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (i < Lc) gv = __ldg(reinterpret_cast<const float4 *>(a.g + ((size_t)(cs + i) * H + h) * kD + c0));
+                if (i < Lc) gv = *reinterpret_cast<const float4 *>(sm + OFF_GST + i * (kD * 4) + c0 * 4);
                 run[0] += gv.x; run[1] += gv.y; run[2] += gv.z; run[3] += gv.w;
 #pragma unroll
                 for (int m = 0; m < 4; ++m) G[ii][m] = run[m];
@@ -297,18 +321,24 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(TcArgs A) {
                     Eb[ii][m] = __expf(-x);
                 }
         }
-        auto finish = [&](int which, const Raw &R, float (&y)[kTok][4]) {
+        // conv (+SiLU) and norm of q (which 0), k (1) or v (2) for this thread's 4 tokens x 4 channels
+        auto finish = [&](int which, float (&y)[kTok][4]) {
+            const uint32_t st = which == 0 ? OFF_QST : (which == 1 ? OFF_KST : OFF_VST);
             float x[kTok + 3][4];
 #pragma unroll
             for (int t = 0; t < kTok + 3; ++t) {
-                const int pos = cs + i0 - 3 + t;
-                if (t < 3 && pos < tb) {
-                    x[t][0] = R.hs[t].x; x[t][1] = R.hs[t].y; x[t][2] = R.hs[t].z; x[t][3] = R.hs[t].w;
-                } else {
-                    const __nv_bfloat162 p0 = *reinterpret_cast<const __nv_bfloat162 *>(&R.r[t].x);
-                    const __nv_bfloat162 p1 = *reinterpret_cast<const __nv_bfloat162 *>(&R.r[t].y);
+                const int i = i0 - 3 + t;               // chunk-local token
+                if (i < 0) {
+                    const float4 hv = *reinterpret_cast<const float4 *>(sHist + (which * 3 + 3 + i) * 128 + c0);
+                    x[t][0] = hv.x; x[t][1] = hv.y; x[t][2] = hv.z; x[t][3] = hv.w;
+                } else if (i < Lc) {
+                    const uint2 raw = *reinterpret_cast<const uint2 *>(sm + st + i * (kD * 2) + c0 * 2);
+                    const __nv_bfloat162 p0 = *reinterpret_cast<const __nv_bfloat162 *>(&raw.x);
+                    const __nv_bfloat162 p1 = *reinterpret_cast<const __nv_bfloat162 *>(&raw.y);
                     x[t][0] = __low2float(p0); x[t][1] = __high2float(p0);
                     x[t][2] = __low2float(p1); x[t][3] = __high2float(p1);
+                } else {
+                    x[t][0] = x[t][1] = x[t][2] = x[t][3] = 0.f;
                 }
             }
             if (W > 0) {
@@ -333,7 +363,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(TcArgs A) {
 #pragma unroll
                 for (int ii = 0; ii < kTok; ++ii)
 #pragma unroll
-                    for (int m = 0; m < 4; ++m) y[ii][m] = (i0 + ii < Lc) ? x[ii + 3][m] : 0.f;
+                    for (int m = 0; m < 4; ++m) y[ii][m] = x[ii + 3][m];
             }
             if (a.l2 && which < 2) {
 #pragma unroll
@@ -355,27 +385,10 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(TcArgs A) {
             *reinterpret_cast<uint2 *>(sm + off_hi + o) = make_uint2(pack_bf16(hv[0], hv[1]), pack_bf16(hv[2], hv[3]));
             *reinterpret_cast<uint2 *>(sm + off_lo + o) = make_uint2(pack_bf16(lv[0], lv[1]), pack_bf16(lv[2], lv[3]));
         };
-        // transposed [c][token] writes (8 B = 4 tokens per channel) into a 128-row K=64 tile;
-        // the channel order is rotated per lane pair so a warp store spreads over the bank groups
-        auto put_cols = [&](uint32_t off, const float (&v)[kTok][4]) {
-#pragma unroll
-            for (int mm = 0; mm < 4; ++mm) {
-                const int m = (mm + (lane >> 1)) & 3;
-                float t0[kTok];
-#pragma unroll
-                for (int ii = 0; ii < kTok; ++ii)
-                    t0[ii] = m == 0 ? v[ii][0] : (m == 1 ? v[ii][1] : (m == 2 ? v[ii][2] : v[ii][3]));
-                *reinterpret_cast<uint2 *>(sm + off + sw128_offset(c0 + m, i0)) =
-                    make_uint2(pack_bf16(t0[0], t0[1]), pack_bf16(t0[2], t0[3]));
-            }
-        };
         {
-            float y[kTok][4], hi[kTok][4], lo[kTok][4];
-            Raw rk, rv;
-            issue(1, rk);
+            float y[kTok][4];
             // q -> Qh = q E  (rows 64..127 of X / XL)
-            finish(0, rq, y);
-            issue(2, rv);
+            finish(0, y);
 #pragma unroll
             for (int ii = 0; ii < kTok; ++ii) {
                 float t4[4];
@@ -383,8 +396,8 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(TcArgs A) {
                 for (int m = 0; m < 4; ++m) t4[m] = y[ii][m] * E[ii][m];
                 put_row_split(OFF_X, OFF_XL, 128, 64 + i0 + ii, t4);
             }
-            // k -> Kh = k E (rows 0..63 of X / XL), Kb = k / E (rows, and transposed for the state update)
-            finish(1, rk, y);
+            // k -> Kh = k E (rows 0..63 of X / XL), Kb = k / E (rows; the state update reads them MN-major)
+            finish(1, y);
 #pragma unroll
             for (int ii = 0; ii < kTok; ++ii) {
                 float t4[4], u4[4];
@@ -392,24 +405,23 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(TcArgs A) {
                 for (int m = 0; m < 4; ++m) { t4[m] = y[ii][m] * E[ii][m]; u4[m] = y[ii][m] * Eb[ii][m]; }
                 put_row_split(OFF_X, OFF_XL, 128, i0 + ii, t4);
                 put_row_split(OFF_KB_HI, OFF_KB_LO, 64, i0 + ii, u4);
-#pragma unroll
-                for (int m = 0; m < 4; ++m) split_bf16(u4[m], hi[ii][m], lo[ii][m]);
             }
-            put_cols(OFF_KBT_HI, hi);
-            put_cols(OFF_KBT_LO, lo);
-            // v -> v^T (hi/lo; lo is zero unless the conv made v inexact)
-            finish(2, rv, y);
+            // v -> v rows (hi/lo; lo is zero unless the conv made v inexact), read MN-major by MMA U
+            finish(2, y);
 #pragma unroll
-            for (int ii = 0; ii < kTok; ++ii)
-#pragma unroll
-                for (int m = 0; m < 4; ++m) split_bf16(y[ii][m], hi[ii][m], lo[ii][m]);
-            put_cols(OFF_VT_HI, hi);
-            put_cols(OFF_VT_LO, lo);
+            for (int ii = 0; ii < kTok; ++ii) put_row_split(OFF_V_HI, OFF_V_LO, 64, i0 + ii, y[ii]);
         }
         fence_async_smem();
         tc_fence_before();
         __syncthreads();
         PHASE(0);
+        // pre-conv rows 61..63 of this chunk are the conv history of the next one
+        if (W > 0 && cs + kC < te)
+            for (int e = tid; e < 3 * 3 * 128; e += kThreads) {
+                const int which = e / 384, r = (e / 128) % 3, c = e & 127;
+                const uint32_t st = which == 0 ? OFF_QST : (which == 1 ? OFF_KST : OFF_VST);
+                sHist[e] = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(sm + st + (kC - 3 + r) * (kD * 2) + c * 2));
+            }
         // ================= MMA: [Kh; Qh] Kb^T  -> Akk | Aqk =================
         if (tid == 0) {
             tc_fence_after();
@@ -564,15 +576,15 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(TcArgs A) {
         // ================= MMA: U^T = v^T Tb^T =================
         if (tid == 0) {
             tc_fence_after();
-            const uint32_t id = idesc_bf16_f32(128, 64);
-            const uint32_t va[3] = {sbase + OFF_VT_HI, sbase + OFF_VT_HI, sbase + OFF_VT_LO};
+            const uint32_t id = idesc_bf16_f32(128, 64, false, /*a_mn=*/true);
+            const uint32_t va[3] = {sbase + OFF_V_HI, sbase + OFF_V_HI, sbase + OFF_V_LO};
             const uint32_t tb3[3] = {sbase + OFF_TB_HI, sbase + OFF_TB_LO, sbase + OFF_TB_HI};
             const int nsplit = W > 0 ? 3 : 2;           // v is exact bf16 without a conv
             int cnt = 0;
             for (int sp = 0; sp < nsplit; ++sp)
                 for (int kk = 0; kk < 4; ++kk, ++cnt)
-                    mma_bf16(tbase + kColU, sdesc_kmajor_sw128(va[sp] + kk * 32), sdesc_kmajor_sw128(tb3[sp] + kk * 32),
-                             id, cnt > 0);
+                    mma_bf16(tbase + kColU, sdesc_mnmajor_sw128(va[sp] + kk * 2048, 8192),
+                             sdesc_kmajor_sw128(tb3[sp] + kk * 32), id, cnt > 0);
             mma_commit(mbar_a);
         }
         if (!mma_wait()) { failed = true; break; }
@@ -646,6 +658,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(TcArgs A) {
             mma_commit(mbar_a);
         }
         if (!mma_wait()) { failed = true; break; }
+        if (cs + kC < te) stage_gv(cs + kC);          // Y^T region and the v staging rows are free now
         PHASE(7);
         // ================= V'^T -> split tile;  MMA: O^T += V'^T Aqk^T,  S'^T += V'^T Kb =================
         tmem_to_tile64(kColU, OFF_VPT_HI, OFF_VPT_LO);
@@ -655,18 +668,18 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(TcArgs A) {
         if (tid == 0) {
             tc_fence_after();
             const uint32_t id64 = idesc_bf16_f32(128, 64);
-            const uint32_t id128 = idesc_bf16_f32(128, 128);
+            const uint32_t id128 = idesc_bf16_f32(128, 128, false, false, /*b_mn=*/true);
             const uint32_t va[3] = {sbase + OFF_VPT_HI, sbase + OFF_VPT_HI, sbase + OFF_VPT_LO};
             const uint32_t qb[3] = {sbase + OFF_AQK_HI, sbase + OFF_AQK_LO, sbase + OFF_AQK_HI};
-            const uint32_t kb[3] = {sbase + OFF_KBT_HI, sbase + OFF_KBT_LO, sbase + OFF_KBT_HI};
+            const uint32_t kb[3] = {sbase + OFF_KB_HI, sbase + OFF_KB_LO, sbase + OFF_KB_HI};
             for (int sp = 0; sp < 3; ++sp)
                 for (int kk = 0; kk < 4; ++kk)
                     mma_bf16(tbase + kColA, sdesc_kmajor_sw128(va[sp] + kk * 32), sdesc_kmajor_sw128(qb[sp] + kk * 32),
                              id64, 1);
             for (int sp = 0; sp < 3; ++sp)
                 for (int kk = 0; kk < 4; ++kk)
-                    mma_bf16(tbase + kColS, sdesc_kmajor_sw128(va[sp] + kk * 32), sdesc_kmajor_sw128(kb[sp] + kk * 32),
-                             id128, 1);
+                    mma_bf16(tbase + kColS, sdesc_kmajor_sw128(va[sp] + kk * 32),
+                             sdesc_mnmajor_sw128(kb[sp] + kk * 2048, 8192), id128, 1);
             mma_commit(mbar_a);
         }
         // gate logits (raw bf16 bits) for this thread's 16 outputs, fetched while the last MMAs run
@@ -683,6 +696,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(TcArgs A) {
             }
         }
         if (!mma_wait()) { failed = true; break; }
+        if (cs + kC < te) stage_qk(cs + kC);          // V'^T region is free now
         PHASE(8);
         // ================= epilogue: O^T -> gate -> out; carry the basis factor =================
         {
@@ -768,9 +782,45 @@ bool tc_prefill_supported(int in_bf16, int dk, int dv, int chunk) {
 
 size_t tc_prefill_workspace(int N, int H) { (void)N; (void)H; return 0; }
 
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+// [T, H, 128] row-major tensor as a 3-D map (128 channels, H heads, T tokens); box = one
+// head's 128 channels for 64 consecutive tokens, no swizzle (plain row-major staging).
+cudaError_t make_map(CUtensorMap *m, const void *base, CUtensorMapDataType dt, int esz, int T, int H) {
+    const cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)H, (cuuint64_t)T};
+    const cuuint64_t strides[2] = {(cuuint64_t)kD * esz, (cuuint64_t)H * kD * esz};
+    const cuuint32_t box[3] = {(cuuint32_t)kD, 1u, (cuuint32_t)(T < kC ? T : kC)};
+    const cuuint32_t estr[3] = {1u, 1u, 1u};
+    const CUresult r = g_encode(m, dt, 3, const_cast<void *>(base), dims, strides, box, estr,
+                                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+}  // namespace
+
 cudaError_t launch_prefill_tc_fused(const PrefillArgs &p, const float *conv_w, float *conv_state, int W,
                                     cudaStream_t s) {
     if ((long long)p.N * p.H == 0) return cudaSuccess;
+    if (g_encode == nullptr) {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+        if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || fn == nullptr)
+            return e != cudaSuccess ? e : cudaErrorSymbolNotFound;
+        g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    TcArgs A{};
+    if (p.T > 0) {
+        cudaError_t e;
+        if ((e = make_map(&A.tm_q, p.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.T, p.H)) != cudaSuccess ||
+            (e = make_map(&A.tm_k, p.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.T, p.H)) != cudaSuccess ||
+            (e = make_map(&A.tm_v, p.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.T, p.H)) != cudaSuccess ||
+            (e = make_map(&A.tm_g, p.g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, p.T, p.H)) != cudaSuccess)
+            return e;
+    }
     static bool attr_done = false;
     if (!attr_done) {
         cudaError_t e = cudaFuncSetAttribute(kda_prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -778,7 +828,11 @@ cudaError_t launch_prefill_tc_fused(const PrefillArgs &p, const float *conv_w, f
         if (e != cudaSuccess) return e;
         attr_done = true;
     }
-    TcArgs A{p, conv_w, conv_state, conv_w ? W : 0};
+    A.p = p;
+    A.conv_w = conv_w;
+    A.conv_state = conv_state;
+    A.W = conv_w ? W : 0;
+    A.box_rows = p.T < kC ? p.T : kC;
     kda_prefill_tc_kernel<<<(unsigned)(p.N * p.H), kThreads, kSmemBytes, s>>>(A);
     count_launch();
     return cudaGetLastError();

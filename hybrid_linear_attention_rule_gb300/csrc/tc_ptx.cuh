@@ -71,12 +71,29 @@ __device__ __forceinline__ uint64_t sdesc_kmajor_sw128(uint32_t saddr) {
     return d;
 }
 
-// Instruction descriptor, kind::f16 with bf16 A and B, fp32 accumulator, both K-major.
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool negate_a = false) {
+// MN-major operand tile with the 128-byte swizzle: K rows of 64 contiguous MN
+// elements (128 B), 8-row K groups of 1024 B; successive 64-element MN blocks
+// lie mn_block_bytes apart.  Advancing K by 16 rows is a +2048 B start address.
+__device__ __forceinline__ uint64_t sdesc_mnmajor_sw128(uint32_t saddr, uint32_t mn_block_bytes) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);             // start address (16 B units)
+    d |= (uint64_t)((mn_block_bytes >> 4) & 0x3FFFu) << 16; // leading byte offset: MN block pitch
+    d |= (uint64_t)(1024u >> 4) << 32;                      // stride byte offset: 8-row K group pitch
+    d |= (uint64_t)1 << 46;                                 // descriptor version for tcgen05
+    d |= (uint64_t)2 << 61;                                 // swizzle mode: 128 B
+    return d;
+}
+
+// Instruction descriptor, kind::f16 with bf16 A and B, fp32 accumulator, both K-major
+// unless a_mn / b_mn select the MN-major layout for that operand.
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool negate_a = false, bool a_mn = false,
+                                                      bool b_mn = false) {
     return (1u << 4)                                  // D format: f32
            | (1u << 7)                                // A format: bf16
            | (1u << 10)                               // B format: bf16
            | ((negate_a ? 1u : 0u) << 13)             // negate A
+           | ((a_mn ? 1u : 0u) << 15)                 // A major: MN
+           | ((b_mn ? 1u : 0u) << 16)                 // B major: MN
            | ((uint32_t)(N >> 3) << 17)               // N / 8
            | ((uint32_t)(M >> 4) << 24);              // M / 16
 }
@@ -141,6 +158,15 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst_smem, const void *src, uin
     asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
                  ::"r"(dst_smem), "l"(src), "r"(bytes), "r"(mbar)
                  : "memory");
+}
+// Tiled TMA load of a 3-D box (coordinates innermost first) into shared memory,
+// completing on an mbarrier.  tmap is the generic address of a CUtensorMap held in
+// kernel-parameter (grid-constant) memory.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst_smem, const void *tmap, int x, int y, int z, uint32_t mbar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];"
+        ::"r"(dst_smem), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(z), "r"(mbar)
+        : "memory");
 }
 // Named barrier over `count` threads (a multiple of 32).
 __device__ __forceinline__ void named_bar(uint32_t id, uint32_t count) {

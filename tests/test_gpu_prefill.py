@@ -50,6 +50,11 @@ def test_prefill_bf16_small_ragged():
     _check(KI.chunked_prefill(seed=1, T=1000, H=4))
 
 
+def test_prefill_shorter_than_one_chunk():
+    """T < 64: the staged token tile is shorter than a chunk."""
+    _check(KI.fused_mixer(seed=12, T=37, H=2))
+
+
 def test_prefill_bf16_output_store():
     _check(KI.chunked_prefill(seed=2, T=300, H=2), out_dtype=torch.bfloat16)
 
