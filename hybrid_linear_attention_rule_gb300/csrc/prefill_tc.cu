@@ -92,6 +92,7 @@ static_assert(kSmemBytes <= 232448, "shared memory plan exceeds the per-CTA limi
 
 struct TcArgs {
     CUtensorMap tm_q, tm_k, tm_v, tm_g;   // [T, H, 128] bf16 (q, k, v) and fp32 (g); box 64 tokens x 1 head x 128
+    CUtensorMap tm_gate;                  // [T, H, 128] bf16 gate logits (when gated)
     PrefillArgs p;
     const float *conv_w;     // [2*H*128 + H*128, W] or null
     float *conv_state;       // [N, W-1, 3*H*128] or null
@@ -111,6 +112,10 @@ __device__ __forceinline__ int sidx(int r, int c) { return r * 64 + (c ^ (r & 31
 // z * sigmoid(z) and sigmoid(z) with the fast (2 ulp) divide; the limits are exact (0 and 1)
 __device__ __forceinline__ float silu_fast(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
 __device__ __forceinline__ float sigmoid_fast(float z) { return __fdividef(1.0f, 1.0f + __expf(-z)); }
+
+// Advance a shared-memory descriptor's start address by `bytes` (a multiple of 16, no carry
+// out of the 14-bit field for addresses below 256 KB).
+__device__ __forceinline__ uint64_t dadd(uint64_t desc, uint32_t bytes) { return desc + (bytes >> 4); }
 
 // Element (row, c) of a K-major tile whose K extent is 128 (two 64-wide atoms of rows*128 B each).
 __device__ __forceinline__ uint32_t kmaj128(uint32_t rows, uint32_t row, uint32_t c) {
@@ -156,10 +161,11 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
     float *scrT = reinterpret_cast<float *>(sm + OFF_SCR_T);
     float *sHist = reinterpret_cast<float *>(sm + OFF_HIST);
     uint64_t *mbar = reinterpret_cast<uint64_t *>(sm + OFF_MISC);
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + OFF_MISC + 16);
-    volatile uint32_t *sflag = reinterpret_cast<volatile uint32_t *>(sm + OFF_MISC + 24);
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + OFF_MISC + 24);
+    volatile uint32_t *sflag = reinterpret_cast<volatile uint32_t *>(sm + OFF_MISC + 28);
     const uint32_t mbar_a = smem_u32(mbar);          // MMA completion
     const uint32_t mbar_s = smem_u32(mbar + 1);      // staged input rows landed
+    const uint32_t mbar_g = smem_u32(mbar + 2);      // staged gate tile landed
 
     int tb, te;
     seq_bounds(a.cu, n, a.T, tb, te);
@@ -168,7 +174,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
 
     // ---- set-up: TMEM, barrier, conv weights, initial state ----
     if (warp == 0) { tmem_alloc(smem_u32(tslot), kTmemCols); tmem_relinquish(); }
-    if (tid == 0) { mbar_init(mbar_a, 1); mbar_init(mbar_s, 1); fence_mbar_init(); *sflag = 0; }
+    if (tid == 0) { mbar_init(mbar_a, 1); mbar_init(mbar_s, 1); mbar_init(mbar_g, 1); fence_mbar_init(); *sflag = 0; }
     // conv history of the first chunk: the conv-state rows (right-aligned), else zeros
     for (int e = tid; e < 3 * 3 * 128; e += kThreads) {
         const int which = e / 384, r = (e / 128) % 3, c = e & 127;
@@ -206,7 +212,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
         }
         tmem_wait_st();
     }
-    uint32_t phase = 0, sphase = 0;
+    uint32_t phase = 0, sphase = 0, gphase = 0;
     bool failed = false;
 
     // A chunk's input rows are brought into shared memory by tiled TMA loads (one per
@@ -426,13 +432,14 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
         if (tid == 0) {
             tc_fence_after();
             const uint32_t id = idesc_bf16_f32(128, 64);
-            const uint32_t xa[3] = {sbase + OFF_X, sbase + OFF_X, sbase + OFF_XL};
-            const uint32_t kb[3] = {sbase + OFF_KB_HI, sbase + OFF_KB_LO, sbase + OFF_KB_HI};
-            int cnt = 0;
+            const uint64_t dX = sdesc_kmajor_sw128(sbase + OFF_X), dXL = sdesc_kmajor_sw128(sbase + OFF_XL);
+            const uint64_t dKh = sdesc_kmajor_sw128(sbase + OFF_KB_HI), dKl = sdesc_kmajor_sw128(sbase + OFF_KB_LO);
+#pragma unroll
             for (int sp = 0; sp < 3; ++sp)
-                for (int kk = 0; kk < 8; ++kk, ++cnt)
-                    mma_bf16(tbase + kColA, sdesc_kmajor_sw128(xa[sp] + (kk >> 2) * 16384 + (kk & 3) * 32),
-                             sdesc_kmajor_sw128(kb[sp] + (kk >> 2) * 8192 + (kk & 3) * 32), id, cnt > 0);
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_bf16(tbase + kColA, dadd(sp == 2 ? dXL : dX, (kk >> 2) * 16384 + (kk & 3) * 32),
+                             dadd(sp == 1 ? dKl : dKh, (kk >> 2) * 8192 + (kk & 3) * 32), id, (sp | kk) != 0);
             mma_commit(mbar_a);
         }
         if (!mma_wait()) { failed = true; break; }
@@ -464,8 +471,8 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
         // ================= T = (I + Akk)^-1 in fp32, Tb = T diag(beta) (hi/lo) =================
         // diagonal 16x16 blocks by substitution (one column per thread); the upper blocks
         // (0,1) and (2,3) that the block products read are zeroed at the same time
-        if (tid < 64) {
-            const int b = tid >> 4, col = tid & 15, ib = b * 16;
+        if (warp < 4 && lane < 16) {
+            const int b = warp, col = lane, ib = b * 16;
             float x[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) x[i] = (i == col) ? 1.f : 0.f;
@@ -481,8 +488,8 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
             }
 #pragma unroll
             for (int i = 0; i < 16; ++i) scrT[sidx(ib + i, ib + col)] = x[i];
-        } else {
-            for (int e = tid - 64; e < 512; e += kThreads - 64) {
+        } else if (warp >= 4) {
+            for (int e = tid - 128; e < 512; e += kThreads - 128) {
                 const int blk = e >> 8, r = (e >> 4) & 15, c = e & 15;
                 scrT[sidx(blk * 32 + r, blk * 32 + 16 + c)] = 0.f;
             }
@@ -509,45 +516,40 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
             scrT[sidx((b + 1) * 16 + r, b * 16 + c)] = -(s0 + s1);
             __syncthreads();
         }
-        // level 2: T[32:64, 0:32] = -T2 (A[32:64, 0:32] T1); P (32x32) parked in T[0:32, 32:64]
+        // level 2: T[32:64, 0:32] = -T2 (A[32:64, 0:32] T1); P (32x32) parked in T[0:32, 32:64].
+        // 256 threads, each a 2x2 output tile (rows r0, r0+1; columns cc, cc+1; r0, cc even).  With
+        // the XOR swizzle, (row even, columns 2k, 2k+1) and (row m, columns cc, cc+1) are adjacent
+        // words, so every operand pair is one 8-byte load (for odd m the pair is stored swapped).
         {
-            float p[2];
-#pragma unroll
-            for (int k2 = 0; k2 < 2; ++k2) {
-                const int e = tid + k2 * kThreads;          // 1024 elements, two per thread
-                const int r = e >> 5, c = e & 31;
-                float s0 = 0.f, s1 = 0.f;
+            const int r0 = ((tid >> 4) & 15) * 2, cc = (tid & 15) * 2;
+            auto block_prod = [&](const float *Lm, int lrow, int lcol, int rcol, float (&p)[4]) {
+                p[0] = p[1] = p[2] = p[3] = 0.f;
 #pragma unroll
                 for (int m = 0; m < 32; m += 2) {
-                    s0 = fmaf(scrA[sidx(32 + r, m)], scrT[sidx(m, c)], s0);
-                    s1 = fmaf(scrA[sidx(32 + r, m + 1)], scrT[sidx(m + 1, c)], s1);
+                    const float2 a0 = *reinterpret_cast<const float2 *>(Lm + sidx(lrow + r0, lcol + m));
+                    const float2 a1 = *reinterpret_cast<const float2 *>(Lm + sidx(lrow + r0 + 1, lcol + m) - 1);
+                    const float2 be = *reinterpret_cast<const float2 *>(scrT + sidx(m, rcol + cc));
+                    const float2 bo = *reinterpret_cast<const float2 *>(scrT + sidx(m + 1, rcol + cc) - 1);
+                    // row r0 + 1 is odd: its pair (m, m+1) sits swapped, like the odd-m row of the right factor
+                    p[0] = fmaf(a0.x, be.x, p[0]); p[1] = fmaf(a0.x, be.y, p[1]);
+                    p[2] = fmaf(a1.y, be.x, p[2]); p[3] = fmaf(a1.y, be.y, p[3]);
+                    p[0] = fmaf(a0.y, bo.y, p[0]); p[1] = fmaf(a0.y, bo.x, p[1]);
+                    p[2] = fmaf(a1.x, bo.y, p[2]); p[3] = fmaf(a1.x, bo.x, p[3]);
                 }
-                p[k2] = s0 + s1;
+            };
+            float p[4];
+            if (tid < 256) {
+                block_prod(scrA, 32, 0, 0, p);
+                // the park area is read by nobody in this pass
+                *reinterpret_cast<float2 *>(scrT + sidx(r0, 32 + cc)) = make_float2(p[0], p[1]);
+                *reinterpret_cast<float2 *>(scrT + sidx(r0 + 1, 32 + cc) - 1) = make_float2(p[3], p[2]);
             }
-            // (the reads above touch only T1 and A; the park area is written after every read)
             __syncthreads();
-#pragma unroll
-            for (int k2 = 0; k2 < 2; ++k2) {
-                const int e = tid + k2 * kThreads;
-                scrT[sidx(e >> 5, 32 + (e & 31))] = p[k2];
-            }
-            __syncthreads();
-#pragma unroll
-            for (int k2 = 0; k2 < 2; ++k2) {
-                const int e = tid + k2 * kThreads;
-                const int r = e >> 5, c = e & 31;
-                float s0 = 0.f, s1 = 0.f;
-#pragma unroll
-                for (int m = 0; m < 32; m += 2) {
-                    s0 = fmaf(scrT[sidx(32 + r, 32 + m)], scrT[sidx(m, 32 + c)], s0);
-                    s1 = fmaf(scrT[sidx(32 + r, 32 + m + 1)], scrT[sidx(m + 1, 32 + c)], s1);
-                }
-                p[k2] = -(s0 + s1);
-            }
-#pragma unroll
-            for (int k2 = 0; k2 < 2; ++k2) {
-                const int e = tid + k2 * kThreads;
-                scrT[sidx(32 + (e >> 5), e & 31)] = p[k2];
+            if (tid < 256) {
+                block_prod(scrT, 32, 32, 32, p);
+                // T21 lives in rows 32..63, columns 0..31: not read by this pass
+                *reinterpret_cast<float2 *>(scrT + sidx(32 + r0, cc)) = make_float2(-p[0], -p[1]);
+                *reinterpret_cast<float2 *>(scrT + sidx(33 + r0, cc) - 1) = make_float2(-p[3], -p[2]);
             }
         }
         __syncthreads();
@@ -577,14 +579,16 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
         if (tid == 0) {
             tc_fence_after();
             const uint32_t id = idesc_bf16_f32(128, 64, false, /*a_mn=*/true);
-            const uint32_t va[3] = {sbase + OFF_V_HI, sbase + OFF_V_HI, sbase + OFF_V_LO};
-            const uint32_t tb3[3] = {sbase + OFF_TB_HI, sbase + OFF_TB_LO, sbase + OFF_TB_HI};
+            const uint64_t dVh = sdesc_mnmajor_sw128(sbase + OFF_V_HI, 8192), dVl = sdesc_mnmajor_sw128(sbase + OFF_V_LO, 8192);
+            const uint64_t dTh = sdesc_kmajor_sw128(sbase + OFF_TB_HI), dTl = sdesc_kmajor_sw128(sbase + OFF_TB_LO);
             const int nsplit = W > 0 ? 3 : 2;           // v is exact bf16 without a conv
-            int cnt = 0;
-            for (int sp = 0; sp < nsplit; ++sp)
-                for (int kk = 0; kk < 4; ++kk, ++cnt)
-                    mma_bf16(tbase + kColU, sdesc_mnmajor_sw128(va[sp] + kk * 2048, 8192),
-                             sdesc_kmajor_sw128(tb3[sp] + kk * 32), id, cnt > 0);
+#pragma unroll
+            for (int sp = 0; sp < 3; ++sp)
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    if (sp < nsplit)
+                        mma_bf16(tbase + kColU, dadd(sp == 2 ? dVl : dVh, kk * 2048), dadd(sp == 1 ? dTl : dTh, kk * 32),
+                                 id, (sp | kk) != 0);
             mma_commit(mbar_a);
         }
         if (!mma_wait()) { failed = true; break; }
@@ -616,16 +620,18 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
         if (tid == 0) {
             tc_fence_after();
             const uint32_t id = idesc_bf16_f32(128, 64);
-            const uint32_t sa[3] = {sbase + OFF_ST_HI, sbase + OFF_ST_HI, sbase + OFF_ST_LO};
-            const uint32_t xb[3] = {sbase + OFF_X, sbase + OFF_XL, sbase + OFF_X};
+            const uint64_t dSh = sdesc_kmajor_sw128(sbase + OFF_ST_HI), dSl = sdesc_kmajor_sw128(sbase + OFF_ST_LO);
+            const uint64_t dX = sdesc_kmajor_sw128(sbase + OFF_X), dXL = sdesc_kmajor_sw128(sbase + OFF_XL);
+#pragma unroll
             for (int rowoff = 0; rowoff < 2; ++rowoff) {        // 0: Kh rows -> Y^T, 1: Qh rows -> O^T
                 const uint32_t dcol = rowoff ? kColA : kColY;
-                int cnt = 0;
+#pragma unroll
                 for (int sp = 0; sp < 3; ++sp)
-                    for (int kk = 0; kk < 8; ++kk, ++cnt)
-                        mma_bf16(tbase + dcol, sdesc_kmajor_sw128(sa[sp] + (kk >> 2) * 16384 + (kk & 3) * 32),
-                                 sdesc_kmajor_sw128(xb[sp] + (kk >> 2) * 16384 + rowoff * 8192 + (kk & 3) * 32), id,
-                                 cnt > 0);
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk)
+                        mma_bf16(tbase + dcol, dadd(sp == 2 ? dSl : dSh, (kk >> 2) * 16384 + (kk & 3) * 32),
+                                 dadd(sp == 1 ? dXL : dX, (kk >> 2) * 16384 + rowoff * 8192 + (kk & 3) * 32), id,
+                                 (sp | kk) != 0);
             }
             mma_commit(mbar_a);
         }
@@ -649,16 +655,22 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
         if (tid == 0) {
             tc_fence_after();
             const uint32_t idn = idesc_bf16_f32(128, 64, true);
-            const uint32_t ya[3] = {sbase + OFF_YT_HI, sbase + OFF_YT_HI, sbase + OFF_YT_LO};
-            const uint32_t tb3[3] = {sbase + OFF_TB_HI, sbase + OFF_TB_LO, sbase + OFF_TB_HI};
+            const uint64_t dYh = sdesc_kmajor_sw128(sbase + OFF_YT_HI), dYl = sdesc_kmajor_sw128(sbase + OFF_YT_LO);
+            const uint64_t dTh = sdesc_kmajor_sw128(sbase + OFF_TB_HI), dTl = sdesc_kmajor_sw128(sbase + OFF_TB_LO);
+#pragma unroll
             for (int sp = 0; sp < 3; ++sp)
+#pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
-                    mma_bf16(tbase + kColU, sdesc_kmajor_sw128(ya[sp] + kk * 32), sdesc_kmajor_sw128(tb3[sp] + kk * 32),
-                             idn, 1);
+                    mma_bf16(tbase + kColU, dadd(sp == 2 ? dYl : dYh, kk * 32), dadd(sp == 1 ? dTl : dTh, kk * 32), idn, 1);
             mma_commit(mbar_a);
         }
         if (!mma_wait()) { failed = true; break; }
         if (cs + kC < te) stage_gv(cs + kC);          // Y^T region and the v staging rows are free now
+        if (a.gate && tid == 0) {                     // this chunk's gate tile into the (now dead) Tb region
+            fence_async_smem();
+            mbar_arrive_expect_tx(mbar_g, (uint32_t)A.box_rows * kD * 2);
+            tma_load_3d(sbase + OFF_TB_HI, &A.tm_gate, 0, h, cs, mbar_g);
+        }
         PHASE(7);
         // ================= V'^T -> split tile;  MMA: O^T += V'^T Aqk^T,  S'^T += V'^T Kb =================
         tmem_to_tile64(kColU, OFF_VPT_HI, OFF_VPT_LO);
@@ -669,33 +681,27 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
             tc_fence_after();
             const uint32_t id64 = idesc_bf16_f32(128, 64);
             const uint32_t id128 = idesc_bf16_f32(128, 128, false, false, /*b_mn=*/true);
-            const uint32_t va[3] = {sbase + OFF_VPT_HI, sbase + OFF_VPT_HI, sbase + OFF_VPT_LO};
-            const uint32_t qb[3] = {sbase + OFF_AQK_HI, sbase + OFF_AQK_LO, sbase + OFF_AQK_HI};
-            const uint32_t kb[3] = {sbase + OFF_KB_HI, sbase + OFF_KB_LO, sbase + OFF_KB_HI};
+            const uint64_t dVh = sdesc_kmajor_sw128(sbase + OFF_VPT_HI), dVl = sdesc_kmajor_sw128(sbase + OFF_VPT_LO);
+            const uint64_t dAh = sdesc_kmajor_sw128(sbase + OFF_AQK_HI), dAl = sdesc_kmajor_sw128(sbase + OFF_AQK_LO);
+            const uint64_t dKh = sdesc_mnmajor_sw128(sbase + OFF_KB_HI, 8192), dKl = sdesc_mnmajor_sw128(sbase + OFF_KB_LO, 8192);
+#pragma unroll
             for (int sp = 0; sp < 3; ++sp)
+#pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
-                    mma_bf16(tbase + kColA, sdesc_kmajor_sw128(va[sp] + kk * 32), sdesc_kmajor_sw128(qb[sp] + kk * 32),
-                             id64, 1);
+                    mma_bf16(tbase + kColA, dadd(sp == 2 ? dVl : dVh, kk * 32), dadd(sp == 1 ? dAl : dAh, kk * 32), id64, 1);
+#pragma unroll
             for (int sp = 0; sp < 3; ++sp)
+#pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
-                    mma_bf16(tbase + kColS, sdesc_kmajor_sw128(va[sp] + kk * 32),
-                             sdesc_mnmajor_sw128(kb[sp] + kk * 2048, 8192), id128, 1);
+                    mma_bf16(tbase + kColS, dadd(sp == 2 ? dVl : dVh, kk * 32), dadd(sp == 1 ? dKl : dKh, kk * 2048), id128, 1);
             mma_commit(mbar_a);
         }
-        // gate logits (raw bf16 bits) for this thread's 16 outputs, fetched while the last MMAs run
-        uint32_t graw[16];
-        {
-            const int j = lrow + lane;
-#pragma unroll
-            for (int u = 0; u < 16; ++u) {
-                const int i = quarter * 16 + u;
-                graw[u] = 0u;
-                if (a.gate && i < Lc)
-                    graw[u] = __ldg(reinterpret_cast<const unsigned short *>(a.gate) +
-                                    ((size_t)(cs + i) * H + h) * kD + j);
-            }
+        if (a.gate && tid == 0 && !mbar_wait_bounded(mbar_g, gphase, kWaitLimit)) {
+            *sflag = 1;
+            atomicOr(a.status, 1u);
         }
-        if (!mma_wait()) { failed = true; break; }
+        gphase ^= 1u;
+        if (!mma_wait()) { failed = true; break; }   // its barrier also publishes the gate tile
         if (cs + kC < te) stage_qk(cs + kC);          // V'^T region is free now
         PHASE(8);
         // ================= epilogue: O^T -> gate -> out; carry the basis factor =================
@@ -709,7 +715,9 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
                 const int i = quarter * 16 + u;
                 if (i < Lc) {
                     float o = a.scale * __uint_as_float(r0[u]);
-                    if (a.gate) o *= sigmoid_fast(__uint_as_float(graw[u] << 16));
+                    if (a.gate)
+                        o *= sigmoid_fast(__bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(
+                            sm + OFF_TB_HI + i * (kD * 2) + j * 2)));
                     store_elt(a.out, ((size_t)(cs + i) * H + h) * kD + j, o, a.out_bf16);
                 }
             }
@@ -818,7 +826,8 @@ cudaError_t launch_prefill_tc_fused(const PrefillArgs &p, const float *conv_w, f
         if ((e = make_map(&A.tm_q, p.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.T, p.H)) != cudaSuccess ||
             (e = make_map(&A.tm_k, p.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.T, p.H)) != cudaSuccess ||
             (e = make_map(&A.tm_v, p.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.T, p.H)) != cudaSuccess ||
-            (e = make_map(&A.tm_g, p.g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, p.T, p.H)) != cudaSuccess)
+            (e = make_map(&A.tm_g, p.g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, p.T, p.H)) != cudaSuccess ||
+            (p.gate && (e = make_map(&A.tm_gate, p.gate, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.T, p.H)) != cudaSuccess))
             return e;
     }
     static bool attr_done = false;
