@@ -21,7 +21,7 @@ import torch
 
 __all__ = ["K3KDAError", "load_library", "library_path", "F32", "BF16", "L2_EPS",
            "k3kda_version", "k3kda_status_string", "k3kda_launch_count", "k3kda_short_conv",
-           "k3kda_prefill_workspace_size", "k3kda_prefill", "k3kda_prefill_noalloc", "k3kda_workspace_status",
+           "k3kda_prefill_workspace_size", "k3kda_prefill_workspace_min", "k3kda_prefill", "k3kda_prefill_noalloc", "k3kda_workspace_status",
            "k3kda_decode_step", "prefill", "decode_step", "short_conv"]
 
 F32, BF16 = 0, 1
@@ -69,6 +69,8 @@ def load_library(build_if_missing: bool = True):
         lib.k3kda_short_conv.restype = I
         lib.k3kda_prefill_workspace_size.argtypes = [I, I, I, I, I, I, I, I]
         lib.k3kda_prefill_workspace_size.restype = Z
+        lib.k3kda_prefill_workspace_min.argtypes = [I, I, I, I, I, I, I, I]
+        lib.k3kda_prefill_workspace_min.restype = Z
         lib.k3kda_prefill.argtypes = [P, P, P, I, P, P, P, P, P, I, I, I, I, I, I, F, I, P, P, P, I, P,
                                       P, Z, P]
         lib.k3kda_prefill.restype = I
@@ -144,6 +146,11 @@ def k3kda_prefill_workspace_size(N, T, H, dk, dv, chunk, in_dtype, has_conv) -> 
                                                            int(chunk), int(in_dtype), int(bool(has_conv))))
 
 
+def k3kda_prefill_workspace_min(N, T, H, dk, dv, chunk, in_dtype, has_conv) -> int:
+    return int(load_library().k3kda_prefill_workspace_min(int(N), int(T), int(H), int(dk), int(dv),
+                                                          int(chunk), int(in_dtype), int(bool(has_conv))))
+
+
 def k3kda_prefill(q, k, v, g, beta, initial_state, cu_seqlens, cu_seqlens_host, N, T, H, dk, dv, chunk,
                   scale, use_qk_l2norm, conv_weight, conv_state, conv_W, gate, out, final_state,
                   workspace, stream=None):
@@ -206,9 +213,11 @@ def k3kda_decode_step(q, k, v, g, beta, gate, conv_weight, conv_state, state, N,
 
 def prefill(q, k, v, g, beta, initial_state=None, cu_seqlens=None, chunk=64, scale=None,
             use_qk_l2norm=True, conv_weight=None, conv_state=None, gate=None, out_dtype=None,
-            return_final_state=True, workspace=None, stream=None):
+            return_final_state=True, workspace=None, min_workspace=False, stream=None):
     """Allocate out / final_state / workspace and run k3kda_prefill.  cu_seqlens may be
-    a CPU or CUDA int32 tensor (both copies are passed).  Returns (out, final_state)."""
+    a CPU or CUDA int32 tensor (both copies are passed).  The workspace is the size of
+    k3kda_prefill_workspace_size (the fastest path), or of k3kda_prefill_workspace_min
+    with min_workspace=True.  Returns (out, final_state)."""
     T, H, dk = q.shape
     dv = v.shape[2]
     dev = q.device
@@ -222,8 +231,10 @@ def prefill(q, k, v, g, beta, initial_state=None, cu_seqlens=None, chunk=64, sca
     fs = torch.empty((N, H, dk, dv), dtype=torch.float32, device=dev) if return_final_state else None
     W = 0 if conv_weight is None else conv_weight.shape[1]
     if workspace is None:
-        nbytes = k3kda_prefill_workspace_size(N, T, H, dk, dv, chunk, _dtype(q), conv_weight is not None)
-        workspace = torch.zeros(nbytes, dtype=torch.uint8, device=dev)
+        size_fn = k3kda_prefill_workspace_min if min_workspace else k3kda_prefill_workspace_size
+        nbytes = size_fn(N, T, H, dk, dv, chunk, _dtype(q), conv_weight is not None)
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+        workspace[:256].zero_()                     # the status word; the rest is written before it is read
     k3kda_prefill(q, k, v, g, beta, initial_state, cu_d, cu_h, N, T, H, dk, dv, chunk,
                   dk ** -0.5 if scale is None else scale, use_qk_l2norm, conv_weight, conv_state, W,
                   gate, out, fs, workspace, stream)

@@ -15,6 +15,9 @@ size_t tc_prefill_workspace(int N, int H);
 cudaError_t launch_prefill_tc(const PrefillArgs &a, const int32_t *order, cudaStream_t s);
 cudaError_t launch_prefill_tc_fused(const PrefillArgs &p, const float *conv_w, float *conv_state, int W,
                                     cudaStream_t s);
+size_t tc_split_workspace(int N, int T, int H);
+cudaError_t launch_prefill_tc_split(const PrefillArgs &p, const float *conv_w, float *conv_state, int W,
+                                    void *ws, cudaStream_t s);
 }  // namespace k3kda
 
 using namespace k3kda;
@@ -101,9 +104,17 @@ size_t k3kda_prefill_workspace_size(int N, int T, int H, int dk, int dv, int chu
     size_t b = kStatusBytes;
     if (N < 0 || T < 0 || H < 0 || dk < 0 || dv < 0) return b;
     if (tc_prefill_supported(in_dtype == K3KDA_BF16, dk, dv, chunk))
-        return b + round256(tc_prefill_workspace(N, H));   // conv, norm and gate are fused
+        return b + round256(tc_split_workspace(N, T, H));   // chunk records of the two-pass path
     if (has_conv) b += conv_buffer_bytes(T, H, dk, dv);
     return b;
+}
+
+size_t k3kda_prefill_workspace_min(int N, int T, int H, int dk, int dv, int chunk, int in_dtype,
+                                   int has_conv) {
+    if (N >= 0 && T >= 0 && H >= 0 && dk >= 0 && dv >= 0 &&
+        tc_prefill_supported(in_dtype == K3KDA_BF16, dk, dv, chunk))
+        return kStatusBytes + round256(tc_prefill_workspace(N, H));   // single-pass kernel
+    return k3kda_prefill_workspace_size(N, T, H, dk, dv, chunk, in_dtype, has_conv);
 }
 
 int k3kda_prefill(const void *q, const void *k, const void *v, int in_dtype, const float *g,
@@ -127,7 +138,7 @@ int k3kda_prefill(const void *q, const void *k, const void *v, int in_dtype, con
     if (!aligned4(beta)) return K3KDA_ERR_ALIGNMENT;
     if (conv && (!aligned16(conv->weight) || !aligned16(conv->conv_state))) return K3KDA_ERR_ALIGNMENT;
     if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return K3KDA_ERR_WORKSPACE;
-    const size_t need = k3kda_prefill_workspace_size(N, T, H, dk, dv, chunk, in_dtype, conv != nullptr);
+    const size_t need = k3kda_prefill_workspace_min(N, T, H, dk, dv, chunk, in_dtype, conv != nullptr);
     if (workspace_bytes < need) return K3KDA_ERR_WORKSPACE;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -145,9 +156,15 @@ int k3kda_prefill(const void *q, const void *k, const void *v, int in_dtype, con
     a.gate = gate; a.gate_bf16 = in_dtype == K3KDA_BF16; a.out = out; a.out_bf16 = out_dtype == K3KDA_BF16; a.Sfin = final_state;
     a.status = status;
 
-    if (tc_prefill_supported(a.in_bf16, dk, dv, chunk))
-        return cuda_status(launch_prefill_tc_fused(a, conv ? conv->weight : nullptr,
-                                                   conv ? conv->conv_state : nullptr, conv ? conv->W : 0, s));
+    if (tc_prefill_supported(a.in_bf16, dk, dv, chunk)) {
+        const float *cw = conv ? conv->weight : nullptr;
+        float *cst = conv ? conv->conv_state : nullptr;
+        const int W = conv ? conv->W : 0;
+        // two-pass path when the workspace holds the chunk records, else the single-pass kernel
+        if (T > 0 && workspace_bytes - off >= tc_split_workspace(N, T, H))
+            return cuda_status(launch_prefill_tc_split(a, cw, cst, W, ws + off, s));
+        return cuda_status(launch_prefill_tc_fused(a, cw, cst, W, s));
+    }
     if (conv) {
         // Conv stage: q, k, v channels convolved (+SiLU) into an fp32 [T, D] buffer in the
         // workspace, then the conv state is advanced; the chunked kernel reads that buffer.

@@ -27,7 +27,7 @@ void *g_noalloc_ptr[kMaxDevices] = {};
 
 extern "C" {
 
-size_t k3kda_prefill_workspace_size(int N, int T, int H, int dk, int dv, int chunk, int in_dtype, int has_conv);
+size_t k3kda_prefill_workspace_min(int N, int T, int H, int dk, int dv, int chunk, int in_dtype, int has_conv);
 int k3kda_prefill(const void *q, const void *k, const void *v, int in_dtype, const float *g, const float *beta,
                   const float *initial_state, const int32_t *cu_seqlens, const int32_t *cu_seqlens_host, int N,
                   int T, int H, int dk, int dv, int chunk, float scale, int use_qk_l2norm,
@@ -40,7 +40,7 @@ int k3kda_prefill_noalloc(const void *q, const void *k, const void *v, int in_dt
                           float scale, int use_qk_l2norm, const k3kda_conv_args *conv, const void *gate,
                           void *out, int out_dtype, float *final_state, void *stream) {
     // Reject work whose scratch would not fit before touching the device.
-    const size_t need = k3kda_prefill_workspace_size(N, T, H, dk, dv, chunk, in_dtype, conv != nullptr);
+    const size_t need = k3kda_prefill_workspace_min(N, T, H, dk, dv, chunk, in_dtype, conv != nullptr);
     if (need > kNoAllocScratchBytes) return K3KDA_ERR_WORKSPACE;
     // Once per device, with that device current: find the device address of the array.
     int dev = 0;

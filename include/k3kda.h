@@ -113,10 +113,20 @@ typedef struct k3kda_conv_args {
     int W;                 /* 1..4                                               */
 } k3kda_conv_args;
 
-/* Bytes of device workspace k3kda_prefill needs for these arguments (always a
- * multiple of 256; at least 256, which holds the device status word). */
+/* Bytes of device workspace with which k3kda_prefill runs its fastest path for
+ * these arguments (always a multiple of 256; at least 256, which holds the
+ * device status word).  For the tensor-core shape (BF16, dk = dv = 128, chunk
+ * 64) this is the two-pass path's chunk-record buffer: 148,480 bytes per
+ * (64-token chunk, head), about 2.3 KB per token and head, plus N*4 bytes. */
 size_t k3kda_prefill_workspace_size(int N, int T, int H, int dk, int dv, int chunk,
                                     int in_dtype, int has_conv);
+
+/* The smallest workspace k3kda_prefill accepts for these arguments.  For the
+ * tensor-core shape it is 256 bytes and selects the single-pass kernel (one
+ * CTA per sequence and head); other shapes need what
+ * k3kda_prefill_workspace_size returns. */
+size_t k3kda_prefill_workspace_min(int N, int T, int H, int dk, int dv, int chunk,
+                                   int in_dtype, int has_conv);
 
 /*
  * k3kda_prefill -- chunked KDA prefill over packed variable-length sequences
@@ -136,8 +146,7 @@ size_t k3kda_prefill_workspace_size(int N, int T, int H, int dk, int dv, int chu
  *   cu_seqlens     [N+1]           int32 device, cu[0] = 0, non-decreasing,
  *                                  cu[N] = T; NULL allowed only when N == 1
  *   cu_seqlens_host[N+1]           optional host copy; when given it is
- *                                  validated (INVALID_ARG if malformed) and
- *                                  used to schedule long sequences first
+ *                                  validated (INVALID_ARG if malformed)
  *   chunk          16, 32 or 64 (the chunk length of the chunked form)
  *   scale          output scale (usually dk^-0.5)
  *   use_qk_l2norm  nonzero: L2-normalise q and k per (token, head) in kernel,
@@ -146,12 +155,17 @@ size_t k3kda_prefill_workspace_size(int N, int T, int H, int dk, int dv, int chu
  *   gate           [T, H, dv] in_dtype logits, or NULL (no output gate)
  *   out            [T, H, dv] out_dtype
  *   final_state    [N, H, dk, dv] FP32 or NULL; may alias initial_state
- *   workspace      device scratch of k3kda_prefill_workspace_size() bytes,
- *                  256-byte aligned, exclusively owned by this call until it
- *                  completes on the stream
- * The fast path (tensor cores, split-BF16 operands) runs for in_dtype BF16,
- * dk = dv = 128, chunk 64; every other supported shape runs an FP32 CUDA-core
- * chunked kernel.  Both compute the same chunked algebra.
+ *   workspace      device scratch of at least k3kda_prefill_workspace_min()
+ *                  bytes (k3kda_prefill_workspace_size() for the fastest path),
+ *                  256-byte aligned, its first 256 bytes zero on the first
+ *                  use, exclusively owned by this call until it completes on
+ *                  the stream
+ * The fast paths (tensor cores, split-BF16 operands) run for in_dtype BF16,
+ * dk = dv = 128, chunk 64: with the full workspace a two-pass scheme (a
+ * chunk-prep kernel over every (chunk, head) on all SMs, then a scan kernel per
+ * sequence and head that carries the state); with less, one single-pass kernel
+ * per sequence and head.  Every other supported shape runs an FP32 CUDA-core
+ * chunked kernel.  All compute the same chunked algebra.
  * Errors: INVALID_ARG, UNSUPPORTED, ALIGNMENT, WORKSPACE, CUDA as above.
  * A bounded in-kernel wait that gives up records K3KDA_ERR_TIMEOUT in the
  * workspace status word (see k3kda_workspace_status) instead of hanging.
@@ -180,10 +194,12 @@ int k3kda_workspace_status(void *workspace, void *stream);
  * the scratch comes from a 16 MiB device array that the library reserves
  * statically (K3KDA_NOALLOC_SCRATCH_BYTES); every GPU that loads the library
  * holds it until the process exits.  The call itself allocates nothing.
- *   - Work whose k3kda_prefill_workspace_size() exceeds the array (only the
+ *   - Work whose k3kda_prefill_workspace_min() exceeds the array (only the
  *     fp32 CUDA-core shapes with a fused conv need more than 256 bytes: their
  *     fp32 [T, 2*H*dk + H*dv] conv staging buffer) returns
- *     K3KDA_ERR_WORKSPACE before anything is enqueued.
+ *     K3KDA_ERR_WORKSPACE before anything is enqueued.  Tensor-core shapes
+ *     whose chunk records fit in the array run the two-pass path, larger ones
+ *     the single-pass kernel.
  *   - The first call on each device looks up the array's device address with
  *     that device current; make that first call before any stream capture.
  *   - All calls on a device share the one array and it keeps the last call's

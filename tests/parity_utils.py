@@ -48,11 +48,14 @@ def case_to_device(c: KI.KdaCase):
     return d
 
 
-def run_prefill(c: KI.KdaCase, out_dtype=torch.float32, d=None):
+def run_prefill(c: KI.KdaCase, out_dtype=torch.float32, d=None, min_workspace=False):
+    """min_workspace=True gives the prefill the smallest workspace it accepts, which selects
+    the single-pass tensor-core kernel instead of the two-pass one for bf16 d = 128 shapes."""
     d = d or case_to_device(c)
     out, fs = K.prefill(d["q"], d["k"], d["v"], d["g"], d["beta"], initial_state=d["S0"], cu_seqlens=d["cu"],
                         chunk=c.chunk, scale=c.scale, use_qk_l2norm=c.use_qk_l2norm, conv_weight=d["conv_w"],
-                        conv_state=d["conv_state"], gate=d["gate"], out_dtype=out_dtype)
+                        conv_state=d["conv_state"], gate=d["gate"], out_dtype=out_dtype,
+                        min_workspace=min_workspace)
     torch.cuda.synchronize()
     return out, fs, d
 

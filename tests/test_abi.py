@@ -43,15 +43,22 @@ def test_version_and_status_strings(lib):
 
 
 def test_workspace_size_is_aligned_and_grows_with_conv(lib):
-    # tensor-core shape (bf16, d = 128, chunk 64): the conv is fused, only the status word is needed
+    # tensor-core shape (bf16, d = 128, chunk 64): the conv is fused; the full workspace holds one
+    # 148,480-byte record per (chunk, head) for the two-pass path, the minimum only the status word
     a = K.k3kda_prefill_workspace_size(1, 1024, 4, 128, 128, 64, K.BF16, False)
     b = K.k3kda_prefill_workspace_size(1, 1024, 4, 128, 128, 64, K.BF16, True)
-    assert a == b == 256
+    assert a == b and a % 256 == 0
+    assert a == 256 + 256 + 16 * 4 * 148480          # status, chunk offsets, 16 chunks x 4 heads
+    assert K.k3kda_prefill_workspace_min(1, 1024, 4, 128, 128, 64, K.BF16, True) == 256
+    # packed sequences: at most (T + 63 N) / 64 chunks in all
+    e = K.k3kda_prefill_workspace_size(3, 1000, 2, 128, 128, 64, K.BF16, True)
+    assert e == 256 + 256 + ((1000 + 63 * 3) // 64) * 2 * 148480
     # fp32 CUDA-core shapes stage the conv output in an fp32 [T, D] buffer
     c = K.k3kda_prefill_workspace_size(1, 1024, 4, 64, 128, 64, K.BF16, False)
     d = K.k3kda_prefill_workspace_size(1, 1024, 4, 64, 128, 64, K.BF16, True)
     assert c >= 256 and c % 256 == 0 and d % 256 == 0
     assert d >= c + 1024 * (2 * 4 * 64 + 4 * 128) * 4
+    assert K.k3kda_prefill_workspace_min(1, 1024, 4, 64, 128, 64, K.BF16, True) == d
 
 
 # Fake, never-dereferenced device addresses: validation must reject before use.

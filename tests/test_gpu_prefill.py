@@ -16,8 +16,14 @@ from parity_utils import (assert_close, case_to_device, head_subset, oracle_pref
 pytestmark = pytest.mark.gpu
 
 
-def _check(c, out_dtype=torch.float32, heads=None):
-    out, fs, d = run_prefill(c, out_dtype)
+# The tensor-core shapes (bf16, d = 128, chunk 64) have two paths: the two-pass one (chunk-prep
+# kernel over all (chunk, head) items, then a scan kernel per sequence and head), selected by the
+# full workspace, and the single-pass kernel, selected by the minimum workspace.
+PATHS = pytest.mark.parametrize("path", ["two_pass", "single_pass"])
+
+
+def _check(c, out_dtype=torch.float32, heads=None, path="two_pass"):
+    out, fs, d = run_prefill(c, out_dtype, min_workspace=path == "single_pass")
     sub = c if heads is None else head_subset(c, heads)
     ro, rs, rcs = oracle_prefill(sub)
     o = to_np(out) if heads is None else to_np(out[:, heads])
@@ -45,35 +51,39 @@ def test_core_fp32_chunk_sizes_and_ragged_tail(chunk):
 
 # ---- bf16 chunked prefill ----
 
-def test_prefill_bf16_small_ragged():
+@PATHS
+def test_prefill_bf16_small_ragged(path):
     """15 full chunks plus a 40-token tail, 4 heads, d = 128, chunk 64."""
-    _check(KI.chunked_prefill(seed=1, T=1000, H=4))
+    _check(KI.chunked_prefill(seed=1, T=1000, H=4), path=path)
 
 
-def test_prefill_shorter_than_one_chunk():
+@PATHS
+def test_prefill_shorter_than_one_chunk(path):
     """T < 64: the staged token tile is shorter than a chunk."""
-    _check(KI.fused_mixer(seed=12, T=37, H=2))
+    _check(KI.fused_mixer(seed=12, T=37, H=2), path=path)
 
 
 def test_prefill_bf16_output_store():
     _check(KI.chunked_prefill(seed=2, T=300, H=2), out_dtype=torch.bfloat16)
 
 
-def test_prefill_without_l2norm():
+@PATHS
+def test_prefill_without_l2norm(path):
     c = KI.chunked_prefill(seed=3, T=200, H=2)
     c.use_qk_l2norm = False
     c.q = KI.round_bf16(c.q * 0.08)
     c.k = KI.round_bf16(c.k * 0.08)
-    _check(c)
+    _check(c, path=path)
 
 
 # ---- varlen with initial states ----
 
-def test_varlen_small_with_edge_lengths():
+@PATHS
+def test_varlen_small_with_edge_lengths(path):
     """Empty, one-token, chunk-1, chunk, chunk+1 and multi-chunk sequences packed together."""
     c = KI.prefill_case("varlen_edges", [0, 1, 63, 64, 65, 200, 0, 7], 3, 128, 128, 64, "bf16", seed=4,
                         s0_std=0.02, gate=True)
-    _check(c)
+    _check(c, path=path)
 
 
 def test_varlen_mixed_head_dims_f32_path():
@@ -99,13 +109,24 @@ def test_final_state_may_alias_initial_state():
 
 # ---- fused mixer: conv + SiLU + L2 + chunked KDA + gate ----
 
-def test_fused_mixer_small():
-    _check(KI.fused_mixer(seed=1, T=777, H=2))
+@PATHS
+def test_fused_mixer_small(path):
+    _check(KI.fused_mixer(seed=1, T=777, H=2), path=path)
 
 
-def test_fused_mixer_varlen_with_conv_state():
+@PATHS
+def test_fused_mixer_varlen_with_conv_state(path):
     c = KI.prefill_case("mixer_varlen", [2, 130, 1, 64], 2, 128, 128, 64, "bf16", seed=7, s0_std=0.02,
                         gate=True, conv_width=4, conv_state=True)
+    _check(c, path=path)
+
+
+@pytest.mark.parametrize("W", [1, 2, 3])
+def test_fused_mixer_narrow_conv_two_pass(W):
+    """Conv widths below 4: the conv history before each chunk comes from the inputs (or, before
+    the sequence start, from the right-aligned conv state) with taps right-aligned."""
+    c = KI.prefill_case(f"mixer_w{W}", [70, 3, 190], 2, 128, 128, 64, "bf16", seed=20 + W, s0_std=0.02,
+                        gate=True, conv_width=W, conv_state=True)
     _check(c)
 
 
@@ -170,6 +191,7 @@ def test_full_varlen_prefill_sampled_heads():
 
 
 @pytest.mark.slow
-def test_full_fused_mixer_sampled_heads():
+@PATHS
+def test_full_fused_mixer_sampled_heads(path):
     c = KI.fused_mixer(seed=0)
-    _check(c, out_dtype=torch.bfloat16, heads=[5, 26])
+    _check(c, out_dtype=torch.bfloat16, heads=[5, 26], path=path)
