@@ -16,12 +16,15 @@
 //       S_next = diag(exp(G_last - r)) (S' + Kb^T V')
 //
 // The record of an item (148,480 bytes, in the caller's workspace) holds the
-// split-bf16 tiles [W; Qh], Kb and Aqk in the exact 128B-swizzled shared-memory
+// split-bf16 tiles [W; Qh], Kb and Aqk^T in the exact 128B-swizzled shared-memory
 // layout in which the scan kernel's MMAs read them, U^T in fp32 and the
-// per-channel r and G_last, so the scan kernel fetches it with three plain bulk
-// copies that overlap its own MMAs.  The scan keeps the fp32 state in TMEM for
-// the whole sequence, like the single-pass kernel; per chunk it runs two MMA
-// chains (N = 128 against [W; Qh], then O += V'^T Aqk^T and S += V'^T Kb).
+// per-channel r and G_last; the scan kernel fetches the tiles with bulk copies
+// that overlap its own MMAs.  It keeps the fp32 state in TMEM for the whole
+// sequence, like the single-pass kernel; per chunk it runs two MMA chains, both
+// with the A operand in TMEM: N = 128 against [W; Qh], then N = 192 against
+// [Aqk^T | Kb] (O += V'^T Aqk^T beside S += V'^T Kb in adjacent TMEM columns).
+// The time of a tcgen05 MMA here is set by the instruction count far more than
+// by N, hence the wide chains.
 #include <cuda.h>
 
 #include "tc_chunk.cuh"
@@ -34,19 +37,17 @@ using namespace tcc;
 
 // ---- one chunk record (byte offsets; identical to the scan kernel's smem layout) ----
 constexpr uint32_t REC_X = 0;            // [W rows 0-63; Qh rows 64-127] x 128 K, split: hi 32 KB, lo 32 KB
-constexpr uint32_t REC_KB = 65536;       // Kb rows [64][128 K], split: hi 16 KB, lo 16 KB
-constexpr uint32_t REC_AQK = 98304;      // Aqk [64][64 K], split: hi 8 KB, lo 8 KB
-constexpr uint32_t REC_U = 114688;       // U^T fp32 [128 dv][64 tok]; 16-byte units XOR-swizzled by (dv & 15)
+constexpr uint32_t REC_B = 65536;        // MN-major B of MMA O/S, per split half [Aqk^T 8 KB | Kb rows 16 KB]: hi, lo
+constexpr uint32_t REC_U = 114688;       // U^T fp32 as 16 blocks of 4 tokens: [tok / 4][128 dv][4 tok]
 constexpr uint32_t REC_VEC = 147456;     // r[128], G_last[128] fp32
 constexpr uint32_t REC_BYTES = 148480;
 static_assert(OFF_XL == OFF_X + 32768, "the [Kh; Qh] tile pair must be contiguous (one bulk store)");
-static_assert(OFF_KB_LO == OFF_KB_HI + 16384 && OFF_AQK_HI == OFF_KB_HI + 32768 && OFF_AQK_LO == OFF_AQK_HI + 8192,
-              "Kb and Aqk tiles must be contiguous in the prep kernel's layout (one bulk store)");
 static_assert(OFF_GL == OFF_REF + 512, "r and G_last must be adjacent (one bulk store)");
 
-// byte offset of U^T element (dv j, token i) inside the U block
+// byte offset of U^T element (dv j, token i) inside the U block: a warp's 32 consecutive dv
+// channels with the same 4 tokens fill 512 contiguous bytes (coalesced stores, conflict-free loads)
 __device__ __forceinline__ uint32_t u_off(uint32_t j, uint32_t i) {
-    return j * 256u + ((((i >> 2) ^ (j & 15u)) << 4) | ((i & 3u) << 2));
+    return (i >> 2) * 2048u + j * 16u + (i & 3u) * 4u;
 }
 
 // ============================ chunk offsets ============================
@@ -158,66 +159,99 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_prep_kernel(const __gri
         return !bad;
     };
 
-    int cur_h = -1;
-    for (int it = blockIdx.x; it < total; it += gridDim.x) {
-        const int qc = it / H, h = it - qc * H;
+    // work item -> (head, sequence, chunk start)
+    struct Item { int h, n, tb, te, cs; };
+    auto locate = [&](int it) {
+        Item x;
+        const int qc = it / H;
+        x.h = it - qc * H;
         int lo = 0, hi = N;                              // sequence n with off[n] <= qc < off[n + 1]
         while (hi - lo > 1) {
             const int mid = (lo + hi) >> 1;
             if (A.chunk_off[mid] <= qc) lo = mid; else hi = mid;
         }
-        const int n = lo;
-        int tb, te;
-        seq_bounds(a.cu, n, a.T, tb, te);
-        const int cs = tb + (qc - A.chunk_off[n]) * kC;
-        const int Lc = min(kC, te - cs);
+        x.n = lo;
+        seq_bounds(a.cu, x.n, a.T, x.tb, x.te);
+        x.cs = x.tb + (qc - A.chunk_off[x.n]) * kC;
+        return x;
+    };
+    // conv weights of the item's head and its conv history (pre-conv q, k, v rows of tokens
+    // cs-3 .. cs-1 from the inputs, or from the right-aligned initial conv state before the
+    // sequence start), by all threads; prep_chunk is their only reader
+    int cur_h = -1;
+    auto load_history = [&](const Item &x) {
+        if (W == 0) return;
+        if (x.h != cur_h) {
+            for (int e = tid; e < 384 * 4; e += kThreads) {
+                // tap-major, taps right-aligned in a 4-wide window: tap t multiplies token i - 3 + t
+                const int t = e / 384, ch = e - t * 384;
+                const int gch = (ch >> 7) * H * kD + x.h * kD + (ch & 127);
+                sConvW[e] = t >= 4 - W ? A.conv_w[(size_t)gch * W + (t - (4 - W))] : 0.f;
+            }
+            cur_h = x.h;
+        }
+        for (int e = tid; e < 3 * 3 * 128; e += kThreads) {
+            const int which = e / 384, r = (e / 128) % 3, c = e & 127;
+            const int t = x.cs - 3 + r;
+            float v = 0.f;
+            if (t >= x.tb) {
+                const void *src = which == 0 ? a.q : (which == 1 ? a.k : a.v);
+                v = __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(src)[((size_t)t * H + x.h) * kD + c]);
+            } else {
+                const int row = W - 1 + (t - x.tb);
+                if (W > 1 && A.conv_state != nullptr && row >= 0)
+                    v = A.conv_state[((size_t)x.n * (W - 1) + row) * Dall + which * H * kD + x.h * kD + c];
+            }
+            sHist[e] = v;
+        }
+    };
+    // An item's rows land in three pieces on one phase of mbar_s, each as soon as its region is
+    // free: v (after prep), q and k (after the triangular solve), g (after MMA U).  Thread 0.
+    auto stage_v = [&](const Item &x) {
+        mbar_arrive_expect_tx(mbar_s, kStageBytes);
+        tma_load_3d(sbase + OFF_VST, &A.tm_v, 0, x.h, x.cs, mbar_s);
+        pend_s = true;
+    };
+    auto stage_qk = [&](const Item &x) {
+        tma_load_3d(sbase + OFF_QST, &A.tm_q, 0, x.h, x.cs, mbar_s);
+        tma_load_3d(sbase + OFF_KST, &A.tm_k, 0, x.h, x.cs, mbar_s);
+    };
+    auto stage_g = [&](const Item &x) { tma_load_3d(sbase + OFF_GST, &A.tm_g, 0, x.h, x.cs, mbar_s); };
 
-        // stage this chunk's rows once the previous record has been read out of shared memory
+    PhaseClock clk;   // phases: 0 staging wait, 1 prep, 2 MMA A (+ next history), 3 extract, 4 solve, 5 MMA U/W, 6 records out
+    if ((int)blockIdx.x < total) {
+        const Item x0 = locate(blockIdx.x);
+        if (tid == 0) { stage_v(x0); stage_qk(x0); stage_g(x0); }
+        load_history(x0);
+    }
+    for (int it = blockIdx.x; it < total; it += gridDim.x) {
+        const Item x = locate(it);
+        const bool has_next = it + (int)gridDim.x < total;
+        const Item y = has_next ? locate(it + gridDim.x) : x;
+        const int Lc = min(kC, x.te - x.cs);
         if (tid == 0) {
-            bulk_wait_read_all();
-            mbar_arrive_expect_tx(mbar_s, kStageBytes);
-            tma_load_3d(sbase + OFF_GST, &A.tm_g, 0, h, cs, mbar_s);
-            tma_load_3d(sbase + OFF_VST, &A.tm_v, 0, h, cs, mbar_s);
-            tma_load_3d(sbase + OFF_QST, &A.tm_q, 0, h, cs, mbar_s);
-            tma_load_3d(sbase + OFF_KST, &A.tm_k, 0, h, cs, mbar_s);
-            pend_s = true;
+            bulk_wait_read_all();                        // the previous records have left shared memory
+            wait_on(mbar_s, sph, pend_s);
         }
-        if (W > 0) {
-            if (h != cur_h) {
-                for (int e = tid; e < 384 * 4; e += kThreads) {
-                    // tap-major, taps right-aligned in a 4-wide window: tap t multiplies token i - 3 + t
-                    const int t = e / 384, ch = e - t * 384;
-                    const int gch = (ch >> 7) * H * kD + h * kD + (ch & 127);
-                    sConvW[e] = t >= 4 - W ? A.conv_w[(size_t)gch * W + (t - (4 - W))] : 0.f;
-                }
-                cur_h = h;
-            }
-            // conv history: pre-conv q, k, v rows of tokens cs-3 .. cs-1 of this sequence, from the
-            // inputs, or from the initial conv state (right-aligned) before the sequence start
-            for (int e = tid; e < 3 * 3 * 128; e += kThreads) {
-                const int which = e / 384, r = (e / 128) % 3, c = e & 127;
-                const int t = cs - 3 + r;
-                float x = 0.f;
-                if (t >= tb) {
-                    const void *src = which == 0 ? a.q : (which == 1 ? a.k : a.v);
-                    x = __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(src)[((size_t)t * H + h) * kD + c]);
-                } else {
-                    const int row = W - 1 + (t - tb);
-                    if (W > 1 && A.conv_state != nullptr && row >= 0)
-                        x = A.conv_state[((size_t)n * (W - 1) + row) * Dall + which * H * kD + h * kD + c];
-                }
-                sHist[e] = x;
-            }
-        }
-        if (tid == 0) wait_on(mbar_s, sph, pend_s);
         __syncthreads();
         if (*sflag) break;
+        clk.tick(0);
 
-        prep_chunk(sm, a, cs, Lc, h, W, nullptr, nullptr);
-        if (tid == 0) { issue_mma_a(sbase, tbase + kColA, mbar_a); pend_a = true; }
+        prep_chunk(sm, a, x.cs, Lc, x.h, W, nullptr, nullptr);
+        clk.tick(1);
+        if (tid == 0) {
+            issue_mma_a(sbase, tbase + kColA, mbar_a);
+            pend_a = true;
+            if (has_next) stage_v(y);
+        }
+        if (has_next) load_history(y);                   // overlaps MMA A
         if (!mma_wait()) break;
+        clk.tick(2);
         extract_a(sm, tl, kColA);
+        clk.tick(3);
         solve_tb(sm);
+        if (tid == 0 && has_next) stage_qk(y);           // the solve's scratch region is free
+        clk.tick(4);
 
         // ---- MMA: U^T = v^T Tb^T and W^T = Kh^T Tb^T (Kh rows 0-63 of X read MN-major) ----
         if (tid == 0) {
@@ -244,8 +278,11 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_prep_kernel(const __gri
             pend_a = true;
         }
         if (!mma_wait()) break;
+        if (tid == 0 && has_next) stage_g(y);            // the v rows (region A) have been consumed
+        clk.tick(5);
 
-        // ---- U^T -> fp32 block (region A: the v rows are dead), W -> X/XL rows 0-63 ----
+        // ---- U^T -> the record (straight from registers), W -> X/XL rows 0-63 ----
+        uint8_t *rec = A.rec + (size_t)it * REC_BYTES;
         {
             const int j = lrow + lane;                  // dv channel for U^T, dk channel for W^T
             uint32_t r[16];
@@ -253,7 +290,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_prep_kernel(const __gri
             tmem_wait_ld();
 #pragma unroll
             for (int t = 0; t < 4; ++t)
-                *reinterpret_cast<uint4 *>(sm + OFF_GST + u_off(j, quarter * 16 + 4 * t)) =
+                *reinterpret_cast<uint4 *>(rec + REC_U + u_off(j, quarter * 16 + 4 * t)) =
                     make_uint4(r[4 * t], r[4 * t + 1], r[4 * t + 2], r[4 * t + 3]);
             tmem_ld16(tl + kColWp + quarter * 16, r);
             tmem_wait_ld();
@@ -270,15 +307,18 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_prep_kernel(const __gri
         tc_fence_before();
         __syncthreads();
         if (tid == 0) {
-            uint8_t *rec = A.rec + (size_t)it * REC_BYTES;
             bulk_s2g(rec + REC_X, sbase + OFF_X, 65536);
-            bulk_s2g(rec + REC_KB, sbase + OFF_KB_HI, 49152);   // Kb hi, Kb lo, Aqk hi, Aqk lo
-            bulk_s2g(rec + REC_U, sbase + OFF_GST, 32768);
+            bulk_s2g(rec + REC_B, sbase + OFF_AQK_HI, 8192);
+            bulk_s2g(rec + REC_B + 8192, sbase + OFF_KB_HI, 16384);
+            bulk_s2g(rec + REC_B + 24576, sbase + OFF_AQK_LO, 8192);
+            bulk_s2g(rec + REC_B + 32768, sbase + OFF_KB_LO, 16384);
             bulk_s2g(rec + REC_VEC, sbase + OFF_REF, 1024);     // r, G_last
             bulk_commit();
         }
         tc_fence_after();
+        clk.tick(6);
     }
+    clk.flush(reinterpret_cast<unsigned long long *>(a.status) + 16);
     if (tid == 0) {
         bulk_wait_all();
         // after a timed-out wait, let what is still in flight land before the CTA exits
@@ -292,32 +332,58 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_prep_kernel(const __gri
 
 // ============================ pass 2: chunk scan ============================
 struct ScanArgs {
-    CUtensorMap tm_gate;      // [T, H, 128] bf16 gate logits (when gated)
+    CUtensorMap tm_gate;      // [T, H, 128] bf16 gate logits (when gated), box min(64, T) tokens of one head
     PrefillArgs p;
+    int box_rows;
     float *conv_state;        // [N, W-1, 3*H*128] advanced at the end, or null
     int W;
-    int box_rows;
     const int32_t *chunk_off;
     const uint8_t *rec;
 };
 
-// scan kernel shared memory: the record image [0, REC_BYTES), then
-constexpr uint32_t Q_ST_HI = REC_BYTES;             // S'^T [128 rows j][128 K c] hi   (S' .. MMA W/O)
-constexpr uint32_t Q_ST_LO = Q_ST_HI + 32768;       //                           lo
-constexpr uint32_t Q_VPT_HI = Q_ST_HI;              // V'^T [128 rows j][64 K i] hi   (V' .. MMA O/S)
-constexpr uint32_t Q_VPT_LO = Q_ST_HI + 16384;      //                           lo
-constexpr uint32_t Q_GATE = Q_ST_LO;                // gate logits bf16 [64 tok][128] (MMA W/O .. epilogue)
-constexpr uint32_t Q_LOGF = Q_ST_LO + 32768;        // log of the basis factor carried in TMEM
-constexpr uint32_t Q_FCOL = Q_LOGF + 512;           // state column factor of this chunk
-constexpr uint32_t Q_MISC = Q_FCOL + 512;           // 5 mbarriers, tmem slot, flag
+// scan kernel shared memory: [W; Qh] of even chunks and [Aqk^T | Kb] at their record offsets, then
+// [W; Qh] of odd chunks (the next chunk's tile lands while this chunk's MMAs read the other)
+constexpr uint32_t Q_X1 = REC_U;                    // [W; Qh] tile of odd chunks (64 KB)
+constexpr uint32_t Q_G0 = Q_X1 + 65536;             // gate logits bf16 [64 tok][128] of even / odd chunks
+constexpr uint32_t Q_G1 = Q_G0 + 16384;
+constexpr uint32_t Q_LOGF = Q_G1 + 16384;           // log of the basis factor carried in TMEM
+constexpr uint32_t Q_FCOL = Q_LOGF + 512;           // state column factors, two chunks (double buffer)
+constexpr uint32_t Q_MISC = Q_FCOL + 1024;          // 6 mbarriers, tmem slot, flag
 constexpr uint32_t kScanSmemBytes = Q_MISC + 64 + 1024;
-static_assert(Q_ST_HI % 1024 == 0 && Q_ST_LO % 1024 == 0 && Q_VPT_LO % 1024 == 0, "tile alignment");
+static_assert(Q_X1 % 1024 == 0, "tile alignment");
 static_assert(kScanSmemBytes <= 232448, "scan kernel shared memory exceeds the per-CTA limit");
 
-constexpr uint32_t kScanTmemCols = 256;
-constexpr uint32_t kColD = 0;      // [0, 64): (W S')^T, then [64, 128): O^T
-constexpr uint32_t kColSs = 128;   // S'^T, 128 columns
+// Tensor memory: the MMA A operands S'^T and V'^T live here as split bf16 (two values per
+// 32-bit column, the even K index in the low half), so shared memory only feeds the B operands.
+constexpr uint32_t kScanTmemCols = 512;
+constexpr uint32_t kColD = 0;       // [0, 64): (W S')^T, [64, 128): O^T (fp32)
+constexpr uint32_t kColSs = 128;    // S'^T fp32, 128 columns
+static_assert(kColD + 128 == kColSs, "O^T and S'^T must be adjacent: one N = 192 chain accumulates into both");
+constexpr uint32_t kColSh = 256;    // S'^T hi / lo, bf16 pairs: 64 columns each
+constexpr uint32_t kColSl = 320;
+constexpr uint32_t kColVh = 384;    // V'^T hi / lo, bf16 pairs: 32 columns each
+constexpr uint32_t kColVl = 416;
 
+// 16 consecutive K values of one TMEM lane -> split bf16 pairs at columns col_hi, col_lo (8 each)
+__device__ __forceinline__ void tmem_put_split16(uint32_t col_hi, uint32_t col_lo, const float (&v)[16]) {
+    uint32_t hw[8], lw[8];
+#pragma unroll
+    for (int u = 0; u < 16; u += 2) {
+        float h0, l0, h1, l1;
+        split_bf16(v[u], h0, l0);
+        split_bf16(v[u + 1], h1, l1);
+        hw[u >> 1] = pack_bf16(h0, h1);
+        lw[u >> 1] = pack_bf16(l0, l1);
+    }
+    tmem_st8(col_hi, hw);
+    tmem_st8(col_lo, lw);
+}
+
+// Per chunk: MMA [(W S')^T | (Qh S')^T]; V'^T = U^T - (W S')^T; MMA [O^T | S'^T] += V'^T [Aqk^T | Kb]
+// while the gate's sigmoid is taken; then one phase writes this chunk's outputs and moves the
+// state into the next chunk's basis.  [W; Qh] and the gate rows (both double-buffered, two chunks
+// ahead) and [Aqk^T | Kb] arrive by bulk copies issued as soon as their buffers are free; U^T, r
+// and G_last are read by the threads that use them, one chunk ahead, into registers.
 __global__ void __launch_bounds__(kThreads, 1) kda_chunk_scan_kernel(const __grid_constant__ ScanArgs A) {
     extern __shared__ uint8_t smraw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
@@ -328,12 +394,11 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_scan_kernel(const __gri
     const uint32_t sbase = smem_u32(sm);
     float *sLogf = reinterpret_cast<float *>(sm + Q_LOGF);
     float *sFcol = reinterpret_cast<float *>(sm + Q_FCOL);
-    const float *sVec = reinterpret_cast<const float *>(sm + REC_VEC);
     uint64_t *mbar = reinterpret_cast<uint64_t *>(sm + Q_MISC);
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + Q_MISC + 40);
-    volatile uint32_t *sflag = reinterpret_cast<volatile uint32_t *>(sm + Q_MISC + 44);
-    const uint32_t mb_a = smem_u32(mbar), mb_x = smem_u32(mbar + 1), mb_k = smem_u32(mbar + 2),
-                   mb_u = smem_u32(mbar + 3), mb_g = smem_u32(mbar + 4);
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + Q_MISC + 48);
+    volatile uint32_t *sflag = reinterpret_cast<volatile uint32_t *>(sm + Q_MISC + 52);
+    const uint32_t mb_a = smem_u32(mbar), mb_x0 = smem_u32(mbar + 1), mb_x1 = smem_u32(mbar + 2),
+                   mb_k = smem_u32(mbar + 3), mb_g0 = smem_u32(mbar + 4), mb_g1 = smem_u32(mbar + 5);
 
     int tb, te;
     seq_bounds(a.cu, n, a.T, tb, te);
@@ -341,10 +406,12 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_scan_kernel(const __gri
     const int nq = A.chunk_off[n + 1] - q0;
     const int W = A.W;
     const int Dall = 3 * H * kD;
+    const bool gated = a.gate != nullptr;
 
     if (warp == 0) { tmem_alloc(smem_u32(tslot), kScanTmemCols); tmem_relinquish(); }
     if (tid == 0) {
-        mbar_init(mb_a, 1); mbar_init(mb_x, 1); mbar_init(mb_k, 1); mbar_init(mb_u, 1); mbar_init(mb_g, 1);
+        mbar_init(mb_a, 1); mbar_init(mb_x0, 1); mbar_init(mb_x1, 1); mbar_init(mb_k, 1);
+        mbar_init(mb_g0, 1); mbar_init(mb_g1, 1);
         fence_mbar_init();
         *sflag = 0;
     }
@@ -356,8 +423,8 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_scan_kernel(const __gri
     const uint32_t lrow = 32u * (warp & 3);
     const uint32_t tl = tbase + (lrow << 16);
     const int quarter = warp >> 2;
+    const int j = lrow + lane;                          // this thread's TMEM lane: dv channel
     {   // S'^T <- S0^T (true state; basis factor 1)
-        const int j = lrow + lane;
         for (int cb = 0; cb < 32; cb += 16) {
             uint32_t r[16];
 #pragma unroll
@@ -372,8 +439,8 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_scan_kernel(const __gri
 
     auto rec_of = [&](int c) { return A.rec + ((size_t)(q0 + c) * H + h) * REC_BYTES; };
     // thread 0's view of the outstanding asynchronous operations
-    uint32_t aph = 0, xph = 0, kph = 0, uph = 0, gph = 0;
-    bool pend_a = false, pend_x = false, pend_k = false, pend_u = false, pend_g = false;
+    uint32_t aph = 0, kph = 0, xph0 = 0, xph1 = 0, gph0 = 0, gph1 = 0;
+    bool pend_a = false, pend_k = false, pend_x0 = false, pend_x1 = false, pend_g0 = false, pend_g1 = false;
     auto wait_on = [&](uint32_t bar, uint32_t &ph, bool &pend) -> bool {
         if (!pend) return true;
         if (!mbar_wait_bounded(bar, ph, kWaitLimit)) {
@@ -385,11 +452,23 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_scan_kernel(const __gri
         pend = false;
         return true;
     };
-    auto load = [&](uint32_t bar, uint32_t off, int c, uint32_t bytes, bool &pend) {
+    auto load = [&](uint32_t bar, uint32_t dst, uint32_t off, int c, uint32_t bytes, bool &pend) {
         mbar_arrive_expect_tx(bar, bytes);
-        bulk_g2s(sbase + off, rec_of(c) + off, bytes, bar);
+        bulk_g2s(sbase + dst, rec_of(c) + off, bytes, bar);
         pend = true;
     };
+    auto load_x = [&](int c) {
+        if (c & 1) load(mb_x1, Q_X1, REC_X, c, 65536, pend_x1);
+        else load(mb_x0, REC_X, REC_X, c, 65536, pend_x0);
+    };
+    auto wait_x = [&](int c) { return (c & 1) ? wait_on(mb_x1, xph1, pend_x1) : wait_on(mb_x0, xph0, pend_x0); };
+    auto load_gate = [&](int c) {                    // chunk c's gate rows -> buffer c & 1 (thread 0)
+        const uint32_t bar = (c & 1) ? mb_g1 : mb_g0;
+        mbar_arrive_expect_tx(bar, (uint32_t)A.box_rows * kD * 2);
+        tma_load_3d(sbase + ((c & 1) ? Q_G1 : Q_G0), &A.tm_gate, 0, h, tb + c * kC, bar);
+        if (c & 1) pend_g1 = true; else pend_g0 = true;
+    };
+    auto wait_gate = [&](int c) { return (c & 1) ? wait_on(mb_g1, gph1, pend_g1) : wait_on(mb_g0, gph0, pend_g0); };
     auto mma_wait = [&]() -> bool {
         if (tid == 0 && !*sflag) wait_on(mb_a, aph, pend_a);
         __syncthreads();
@@ -397,147 +476,169 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_scan_kernel(const __gri
         tc_fence_after();
         return !bad;
     };
-    if (tid == 0 && nq > 0) {
-        load(mb_x, REC_X, 0, 65536, pend_x);
-        load(mb_k, REC_KB, 0, 49152, pend_k);
-        load(mb_u, REC_U, 0, 33792, pend_u);             // U^T, r, G_last
-    }
+
+    // register-resident operands, one chunk ahead
+    float uR[16];                 // U^T row j, tokens 16*quarter .. +15
+    float rN = 0.f, glN = 0.f;    // tid < 128: r and G_last of the chunk after the current one
+    float logf_cur = 0.f;         // tid < 128: log of the basis factor of the current chunk
+    auto load_u = [&](int c) {
+        const uint8_t *p = rec_of(c) + REC_U;
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            const float4 v = __ldg(reinterpret_cast<const float4 *>(p + u_off(j, quarter * 16 + 4 * t)));
+            uR[4 * t] = v.x; uR[4 * t + 1] = v.y; uR[4 * t + 2] = v.z; uR[4 * t + 3] = v.w;
+        }
+    };
+    auto load_vec = [&](int c) {
+        const float *p = reinterpret_cast<const float *>(rec_of(c) + REC_VEC);
+        rN = __ldg(p + tid);
+        glN = __ldg(p + kD + tid);
+    };
+    // S'^T = S^T diag(fcol) -> TMEM, fp32 and split bf16 (the A operand of MMA W/Qh)
+    auto to_basis = [&](const float *fcol) {
+        for (int cb = 0; cb < 32; cb += 16) {
+            const int col = quarter * 32 + cb;
+            uint32_t r[16];
+            tmem_ld16(tl + kColSs + col, r);
+            tmem_wait_ld();
+            float v[16];
+#pragma unroll
+            for (int u = 0; u < 16; ++u) {
+                v[u] = __uint_as_float(r[u]) * fcol[col + u];
+                r[u] = __float_as_uint(v[u]);
+            }
+            tmem_st16(tl + kColSs + col, r);
+            tmem_put_split16(tl + kColSh + col / 2, tl + kColSl + col / 2, v);
+        }
+        tmem_wait_st();
+    };
 
     bool failed = false;
+    PhaseClock clk;   // phases: 0 MMA W, 1 V' tile, 2 MMA O/S, 3 epilogue + next basis
+    if (nq > 0) {
+        if (tid == 0) {
+            load_x(0);
+            load(mb_k, REC_B, REC_B, 0, 49152, pend_k);     // [Aqk^T | Kb] hi, lo
+            if (gated) load_gate(0);
+            if (nq > 1) {
+                load_x(1);
+                if (gated) load_gate(1);
+            }
+        }
+        load_u(0);
+        if (tid < kD) {
+            load_vec(0);
+            sFcol[tid] = expf(rN);                       // the initial basis factor is 1
+            logf_cur = glN - rN;
+            sLogf[tid] = logf_cur;
+            if (nq > 1) load_vec(1);
+        }
+        __syncthreads();
+        to_basis(sFcol);
+        tc_fence_before();
+        __syncthreads();
+    }
     for (int c = 0; c < nq; ++c) {
         const int cs = tb + c * kC;
         const int Lc = min(kC, te - cs);
         const bool more = c + 1 < nq;
-        // ---- basis change: fcol = exp(logf_prev + r), logf = G_last - r ----
-        if (tid == 0) wait_on(mb_u, uph, pend_u);
-        __syncthreads();
-        if (*sflag) { failed = true; break; }
-        if (tid < kD) {
-            const float r = sVec[tid];
-            sFcol[tid] = expf(sLogf[tid] + r);
-            sLogf[tid] = sVec[kD + tid] - r;
-        }
-        __syncthreads();
-        // ---- S'^T = S^T diag(fcol) -> TMEM and split A tile ----
-        {
-            const int j = lrow + lane;
-            for (int cb = 0; cb < 32; cb += 16) {
-                const int col = quarter * 32 + cb;
-                uint32_t r[16];
-                tmem_ld16(tl + kColSs + col, r);
-                tmem_wait_ld();
-                float v[16];
-#pragma unroll
-                for (int u = 0; u < 16; ++u) {
-                    v[u] = __uint_as_float(r[u]) * sFcol[col + u];
-                    r[u] = __float_as_uint(v[u]);
-                }
-                tmem_st16(tl + kColSs + col, r);
-                tile64_put16(sm, Q_ST_HI + (col >> 6) * 16384, Q_ST_LO + (col >> 6) * 16384, j, col & 63, v);
-            }
-            tmem_wait_st();
-        }
-        fence_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        // ---- MMA: D^T = S'^T [W; Qh]^T  ((W S')^T in columns 0-63, (Qh S')^T in 64-127) ----
-        if (tid == 0 && wait_on(mb_x, xph, pend_x)) {
+        float *fnext = sFcol + ((c + 1) & 1) * kD;
+        // ---- MMA: D^T = S'^T [W; Qh]^T ((W S')^T in D[0, 64), (Qh S')^T in D[64, 128)) ----
+        if (tid == 0 && wait_x(c)) {
             tc_fence_after();
             const uint32_t id = idesc_bf16_f32(128, 128);
-            const uint64_t dSh = sdesc_kmajor_sw128(sbase + Q_ST_HI), dSl = sdesc_kmajor_sw128(sbase + Q_ST_LO);
-            const uint64_t dX = sdesc_kmajor_sw128(sbase + REC_X), dXL = sdesc_kmajor_sw128(sbase + REC_X + 32768);
+            const uint32_t xoff = (c & 1) ? Q_X1 : REC_X;
+            const uint64_t dX = sdesc_kmajor_sw128(sbase + xoff), dXL = sdesc_kmajor_sw128(sbase + xoff + 32768);
 #pragma unroll
             for (int sp = 0; sp < 3; ++sp)
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
-                    mma_bf16(tbase + kColD, dadd(sp == 2 ? dSl : dSh, (kk >> 2) * 16384 + (kk & 3) * 32),
-                             dadd(sp == 1 ? dXL : dX, (kk >> 2) * 16384 + (kk & 3) * 32), id, (sp | kk) != 0);
+                    mma_bf16_ta(tbase + kColD, tbase + (sp == 2 ? kColSl : kColSh) + kk * 8,
+                                dadd(sp == 1 ? dXL : dX, (kk >> 2) * 16384 + (kk & 3) * 32), id, (sp | kk) != 0);
             mma_commit(mb_a);
             pend_a = true;
         }
-        if (!mma_wait()) { failed = true; break; }
-        if (tid == 0) {
-            if (more) load(mb_x, REC_X, c + 1, 65536, pend_x);    // [W; Qh] of the next chunk
-            if (a.gate) {                                          // this chunk's gate rows (S' tile is dead)
-                mbar_arrive_expect_tx(mb_g, (uint32_t)A.box_rows * kD * 2);
-                tma_load_3d(sbase + Q_GATE, &A.tm_gate, 0, h, cs, mb_g);
-                pend_g = true;
-            }
+        // the next chunk's basis factor, while the MMAs run
+        if (tid < kD && more) {
+            fnext[tid] = expf(logf_cur + rN);
+            logf_cur = glN - rN;
+            sLogf[tid] = logf_cur;
+            if (c + 2 < nq) load_vec(c + 2);
         }
+        if (!mma_wait()) { failed = true; break; }
+        clk.tick(0);
         // ---- V'^T = U^T - (W S')^T -> split tile ----
         {
-            const int j = lrow + lane;
             uint32_t r[16];
             tmem_ld16(tl + kColD + quarter * 16, r);
             tmem_wait_ld();
             float v[16];
 #pragma unroll
-            for (int t = 0; t < 4; ++t) {
-                const float4 u4 = *reinterpret_cast<const float4 *>(sm + REC_U + u_off(j, quarter * 16 + 4 * t));
-                v[4 * t + 0] = u4.x - __uint_as_float(r[4 * t + 0]);
-                v[4 * t + 1] = u4.y - __uint_as_float(r[4 * t + 1]);
-                v[4 * t + 2] = u4.z - __uint_as_float(r[4 * t + 2]);
-                v[4 * t + 3] = u4.w - __uint_as_float(r[4 * t + 3]);
-            }
-            tile64_put16(sm, Q_VPT_HI, Q_VPT_LO, j, quarter * 16, v);
+            for (int u = 0; u < 16; ++u) v[u] = uR[u] - __uint_as_float(r[u]);
+            tmem_put_split16(tl + kColVh + quarter * 8, tl + kColVl + quarter * 8, v);
+            tmem_wait_st();
         }
-        fence_async_smem();
+        if (more) load_u(c + 1);
         tc_fence_before();
         __syncthreads();
-        // ---- MMA: O^T += V'^T Aqk^T,  S'^T += V'^T Kb ----
-        if (tid == 0) {
-            if (more) load(mb_u, REC_U, c + 1, 33792, pend_u);    // U^T, r, G_last of the next chunk
-            if (wait_on(mb_k, kph, pend_k)) {
-                tc_fence_after();
-                const uint32_t id64 = idesc_bf16_f32(128, 64);
-                const uint32_t id128 = idesc_bf16_f32(128, 128, false, false, /*b_mn=*/true);
-                const uint64_t dVh = sdesc_kmajor_sw128(sbase + Q_VPT_HI), dVl = sdesc_kmajor_sw128(sbase + Q_VPT_LO);
-                const uint64_t dAh = sdesc_kmajor_sw128(sbase + REC_AQK), dAl = sdesc_kmajor_sw128(sbase + REC_AQK + 8192);
-                const uint64_t dKh = sdesc_mnmajor_sw128(sbase + REC_KB, 8192),
-                               dKl = sdesc_mnmajor_sw128(sbase + REC_KB + 16384, 8192);
+        clk.tick(1);
+        // ---- MMA: [O^T | S'^T] += V'^T [Aqk^T | Kb]  (N = 192: D columns 64 .. 255) ----
+        if (tid == 0 && wait_on(mb_k, kph, pend_k)) {
+            tc_fence_after();
+            const uint32_t id = idesc_bf16_f32(128, 192, false, false, /*b_mn=*/true);
+            const uint64_t dBh = sdesc_mnmajor_sw128(sbase + REC_B, 8192),
+                           dBl = sdesc_mnmajor_sw128(sbase + REC_B + 24576, 8192);
 #pragma unroll
-                for (int sp = 0; sp < 3; ++sp)
+            for (int sp = 0; sp < 3; ++sp)
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        mma_bf16(tbase + kColD + 64, dadd(sp == 2 ? dVl : dVh, kk * 32), dadd(sp == 1 ? dAl : dAh, kk * 32),
-                                 id64, 1);
-#pragma unroll
-                for (int sp = 0; sp < 3; ++sp)
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        mma_bf16(tbase + kColSs, dadd(sp == 2 ? dVl : dVh, kk * 32), dadd(sp == 1 ? dKl : dKh, kk * 2048),
-                                 id128, 1);
-                mma_commit(mb_a);
-                pend_a = true;
-            }
-            if (!*sflag) wait_on(mb_g, gph, pend_g);
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_bf16_ta(tbase + kColD + 64, tbase + (sp == 2 ? kColVl : kColVh) + kk * 8,
+                                dadd(sp == 1 ? dBl : dBh, kk * 2048), id, 1);
+            mma_commit(mb_a);
+            pend_a = true;
         }
-        if (!mma_wait()) { failed = true; break; }       // its barrier also publishes the gate rows
-        if (tid == 0 && more) load(mb_k, REC_KB, c + 1, 49152, pend_k);   // Kb, Aqk of the next chunk
-        // ---- epilogue: O^T -> scale, gate -> out ----
+        float sg[16];                                    // sigmoid of the gate logits, while the MMAs run
+        if (gated) {
+            if (tid == 0 && !*sflag) wait_gate(c);
+            __syncthreads();
+            const uint8_t *gt = sm + ((c & 1) ? Q_G1 : Q_G0);
+#pragma unroll
+            for (int u = 0; u < 16; ++u)
+                sg[u] = sigmoid_fast(__bfloat162float(
+                    *reinterpret_cast<const __nv_bfloat16 *>(gt + (quarter * 16 + u) * (kD * 2) + j * 2)));
+        } else {
+#pragma unroll
+            for (int u = 0; u < 16; ++u) sg[u] = 1.f;
+        }
+        if (!mma_wait()) { failed = true; break; }
+        if (tid == 0 && more) load(mb_k, REC_B, REC_B, c + 1, 49152, pend_k);   // [Aqk^T | Kb] of the next chunk
+        if (tid == 0 && c + 2 < nq) {                    // this chunk's [W; Qh] and gate buffers are free
+            load_x(c + 2);
+            if (gated) load_gate(c + 2);
+        }
+        clk.tick(2);
+        // ---- this chunk's outputs, then the state into the next chunk's basis ----
         {
-            const int j = lrow + lane;
             uint32_t r0[16];
             tmem_ld16(tl + kColD + 64 + quarter * 16, r0);
             tmem_wait_ld();
 #pragma unroll
             for (int u = 0; u < 16; ++u) {
                 const int i = quarter * 16 + u;
-                if (i < Lc) {
-                    float o = a.scale * __uint_as_float(r0[u]);
-                    if (a.gate)
-                        o *= sigmoid_fast(__bfloat162float(
-                            *reinterpret_cast<const __nv_bfloat16 *>(sm + Q_GATE + i * (kD * 2) + j * 2)));
-                    store_elt(a.out, ((size_t)(cs + i) * H + h) * kD + j, o, a.out_bf16);
-                }
+                if (i < Lc) store_elt(a.out, ((size_t)(cs + i) * H + h) * kD + j, a.scale * __uint_as_float(r0[u]) * sg[u],
+                                      a.out_bf16);
             }
         }
+        if (more) to_basis(fnext);
         tc_fence_before();
+        __syncthreads();
+        clk.tick(3);
     }
+    clk.flush(reinterpret_cast<unsigned long long *>(a.status) + 8);
     if (!failed) {
+        tc_fence_after();
         // ---- final state: S = S'^T diag(exp(logf)) ----
         if (a.Sfin) {
-            const int j = lrow + lane;
             for (int cb = 0; cb < 32; cb += 16) {
                 uint32_t r[16];
                 tmem_ld16(tl + kColSs + quarter * 32 + cb, r);
@@ -577,10 +678,11 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_scan_kernel(const __gri
     if (tid == 0) {
         // after a failure, let what is still in flight land before the CTA exits
         if (pend_a) mbar_wait_bounded(mb_a, aph, kWaitLimit);
-        if (pend_x) mbar_wait_bounded(mb_x, xph, kWaitLimit);
+        if (pend_x0) mbar_wait_bounded(mb_x0, xph0, kWaitLimit);
+        if (pend_x1) mbar_wait_bounded(mb_x1, xph1, kWaitLimit);
         if (pend_k) mbar_wait_bounded(mb_k, kph, kWaitLimit);
-        if (pend_u) mbar_wait_bounded(mb_u, uph, kWaitLimit);
-        if (pend_g) mbar_wait_bounded(mb_g, gph, kWaitLimit);
+        if (pend_g0) mbar_wait_bounded(mb_g0, gph0, kWaitLimit);
+        if (pend_g1) mbar_wait_bounded(mb_g1, gph1, kWaitLimit);
     }
     tc_fence_before();
     __syncthreads();
@@ -647,10 +749,10 @@ cudaError_t launch_prefill_tc_split(const PrefillArgs &p, const float *conv_w, f
     if (p.gate && p.T > 0 &&
         (e = make_row_map(&S.tm_gate, p.gate, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.T, p.H)) != cudaSuccess)
         return e;
+    S.box_rows = box_rows;
     S.p = p;
     S.conv_state = conv_w ? conv_state : nullptr;
     S.W = conv_w ? W : 0;
-    S.box_rows = box_rows;
     S.chunk_off = chunk_off;
     S.rec = rec;
     kda_chunk_scan_kernel<<<(unsigned)(p.N * p.H), kThreads, kScanSmemBytes, s>>>(S);

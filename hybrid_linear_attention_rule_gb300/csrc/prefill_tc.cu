@@ -301,16 +301,16 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
         __syncthreads();
         if (tid == 0) {
             tc_fence_after();
-            const uint32_t id64 = idesc_bf16_f32(128, 64);
+            const uint32_t id64b = idesc_bf16_f32(128, 64, false, false, /*b_mn=*/true);
             const uint32_t id128 = idesc_bf16_f32(128, 128, false, false, /*b_mn=*/true);
             const uint64_t dVh = sdesc_kmajor_sw128(sbase + OFF_VPT_HI), dVl = sdesc_kmajor_sw128(sbase + OFF_VPT_LO);
-            const uint64_t dAh = sdesc_kmajor_sw128(sbase + OFF_AQK_HI), dAl = sdesc_kmajor_sw128(sbase + OFF_AQK_LO);
+            const uint64_t dAh = sdesc_mnmajor_sw128(sbase + OFF_AQK_HI, 8192), dAl = sdesc_mnmajor_sw128(sbase + OFF_AQK_LO, 8192);
             const uint64_t dKh = sdesc_mnmajor_sw128(sbase + OFF_KB_HI, 8192), dKl = sdesc_mnmajor_sw128(sbase + OFF_KB_LO, 8192);
 #pragma unroll
             for (int sp = 0; sp < 3; ++sp)
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
-                    mma_bf16(tbase + kColA, dadd(sp == 2 ? dVl : dVh, kk * 32), dadd(sp == 1 ? dAl : dAh, kk * 32), id64, 1);
+                    mma_bf16(tbase + kColA, dadd(sp == 2 ? dVl : dVh, kk * 32), dadd(sp == 1 ? dAl : dAh, kk * 2048), id64b, 1);
 #pragma unroll
             for (int sp = 0; sp < 3; ++sp)
 #pragma unroll

@@ -53,7 +53,7 @@ constexpr uint32_t OFF_VPT_HI = 98304;           // B: V'^T [128 rows j][64 K i]
 constexpr uint32_t OFF_VPT_LO = 114688;
 constexpr uint32_t OFF_KB_HI = 131072;           // Kb [64 rows i][128 K c]: K-major B of MMA A, MN-major B of MMA S
 constexpr uint32_t OFF_KB_LO = 147456;
-constexpr uint32_t OFF_AQK_HI = 163840;          // [64 rows i][64 K i']      (extract .. MMA O)
+constexpr uint32_t OFF_AQK_HI = 163840;          // Aqk^T [64 rows i'][64 i]  (extract .. MMA O; MN-major B)
 constexpr uint32_t OFF_AQK_LO = 172032;
 constexpr uint32_t OFF_SCAN = OFF_AQK_HI;        // fp32 [16 warps][128] partial sums, prep only
 constexpr uint32_t OFF_TB_HI = 180224;           // [64 rows i][64 K j]       (T solve .. MMA V)
@@ -292,7 +292,7 @@ __device__ __forceinline__ void issue_mma_a(uint32_t sbase, uint32_t tmem_col_ad
     mma_commit(mbar);
 }
 
-// ---- stage 3: Akk (times beta, strictly lower) -> fp32 scratch A, Aqk (lower) -> split tile ----
+// ---- stage 3: Akk (times beta, strictly lower) -> fp32 scratch A, Aqk (lower) -> split tile (transposed) ----
 // tl is this warp's TMEM lane base, col the first column of the MMA A result.
 __device__ __forceinline__ void extract_a(uint8_t *sm, uint32_t tl, uint32_t col) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -314,11 +314,19 @@ __device__ __forceinline__ void extract_a(uint8_t *sm, uint32_t tl, uint32_t col
                 scrA[sidx(row, j)] = j < row ? b * __uint_as_float(r0[u]) : 0.f;
             }
         } else {
+            // Aqk stored transposed, [i'][i]: the MMAs read it as an MN-major B operand, so that
+            // it can sit beside the Kb rows in one N = 192 operand; a warp's 32 lanes (32
+            // consecutive i) fill 64 contiguous bytes of one row i'
             const int i = row - 64;
-            float v[16];
 #pragma unroll
-            for (int u = 0; u < 16; ++u) v[u] = colbase + u > i ? 0.f : __uint_as_float(r0[u]);
-            tile64_put16(sm, OFF_AQK_HI, OFF_AQK_LO, i, colbase, v);
+            for (int u = 0; u < 16; ++u) {
+                const int ip = colbase + u;
+                float hv, lv;
+                split_bf16(ip > i ? 0.f : __uint_as_float(r0[u]), hv, lv);
+                const uint32_t o = sw128_offset(ip, i);
+                *reinterpret_cast<__nv_bfloat16 *>(sm + OFF_AQK_HI + o) = __float2bfloat16_rn(hv);
+                *reinterpret_cast<__nv_bfloat16 *>(sm + OFF_AQK_LO + o) = __float2bfloat16_rn(lv);
+            }
         }
     }
     __syncthreads();
@@ -437,6 +445,33 @@ __device__ __forceinline__ void solve_tb(uint8_t *sm) {
     tc_fence_before();
     __syncthreads();
 }
+
+// ---- optional per-phase cycle counters (compile with -DK3KDA_PHASE_TIMERS) ----
+// Thread 0 accumulates clock64() deltas per phase; flush() adds them to a device array.
+struct PhaseClock {
+#ifdef K3KDA_PHASE_TIMERS
+    unsigned long long ph[8];
+    long long last;
+    __device__ PhaseClock() {
+        for (int i = 0; i < 8; ++i) ph[i] = 0;
+        last = clock64();
+    }
+    __device__ __forceinline__ void tick(int i) {
+        if (threadIdx.x == 0) {
+            const long long now = clock64();
+            ph[i] += (unsigned long long)(now - last);
+            last = now;
+        }
+    }
+    __device__ __forceinline__ void flush(unsigned long long *dst) {
+        if (threadIdx.x == 0 && blockIdx.x == 0)
+            for (int i = 0; i < 8; ++i) dst[i] = ph[i];
+    }
+#else
+    __device__ __forceinline__ void tick(int) {}
+    __device__ __forceinline__ void flush(unsigned long long *) {}
+#endif
+};
 
 // ---- host side ----
 // [T, H, 128] row-major tensor as a 3-D TMA map (128 channels, H heads, T tokens); box =
