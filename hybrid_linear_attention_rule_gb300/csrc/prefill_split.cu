@@ -27,6 +27,9 @@
 // by N, hence the wide chains.
 #include <cuda.h>
 
+#include <algorithm>
+#include <mutex>
+
 #include "tc_chunk.cuh"
 
 namespace k3kda {
@@ -104,6 +107,7 @@ struct PrepArgs {
     int box_rows;
     const int32_t *chunk_off; // [N + 1]
     uint8_t *rec;             // [total chunks * H] records
+    int q_lo, q_hi;           // global chunk range of this launch (items q * H + h)
 };
 
 constexpr uint32_t kPrepTmemCols = 256;
@@ -135,7 +139,8 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_prep_kernel(const __gri
     const uint32_t lrow = 32u * (warp & 3);
     const uint32_t tl = tbase + (lrow << 16);
     const int quarter = warp >> 2;
-    const int total = A.chunk_off[N] * H;
+    const int item_lo = A.q_lo * H;
+    const int total = min(A.chunk_off[N], A.q_hi) * H;   // one past the last item of this launch
     const uint32_t kStageBytes = (uint32_t)A.box_rows * (kD * 4 + 3 * kD * 2);
 
     // thread 0's view of the outstanding asynchronous operations
@@ -219,12 +224,12 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_prep_kernel(const __gri
     auto stage_g = [&](const Item &x) { tma_load_3d(sbase + OFF_GST, &A.tm_g, 0, x.h, x.cs, mbar_s); };
 
     PhaseClock clk;   // phases: 0 staging wait, 1 prep, 2 MMA A (+ next history), 3 extract, 4 solve, 5 MMA U/W, 6 records out
-    if ((int)blockIdx.x < total) {
-        const Item x0 = locate(blockIdx.x);
+    if (item_lo + (int)blockIdx.x < total) {
+        const Item x0 = locate(item_lo + blockIdx.x);
         if (tid == 0) { stage_v(x0); stage_qk(x0); stage_g(x0); }
         load_history(x0);
     }
-    for (int it = blockIdx.x; it < total; it += gridDim.x) {
+    for (int it = item_lo + blockIdx.x; it < total; it += gridDim.x) {
         const Item x = locate(it);
         const bool has_next = it + (int)gridDim.x < total;
         const Item y = has_next ? locate(it + gridDim.x) : x;
@@ -339,6 +344,9 @@ struct ScanArgs {
     int W;
     const int32_t *chunk_off;
     const uint8_t *rec;
+    int q_lo, q_hi;           // global chunk range of this launch
+    float *carry_S;           // [N*H][128 dv][128 dk] state in the last chunk's basis between launches
+    float *carry_logf;        // [N*H][128] log of that basis factor
 };
 
 // scan kernel shared memory: [W; Qh] of even chunks and [Aqk^T | Kb] at their record offsets, then
@@ -404,6 +412,10 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_scan_kernel(const __gri
     seq_bounds(a.cu, n, a.T, tb, te);
     const int q0 = A.chunk_off[n];
     const int nq = A.chunk_off[n + 1] - q0;
+    // this launch's chunks of the sequence: [c_begin, c_end); an empty sequence belongs to the first launch
+    const int c_begin = max(0, A.q_lo - q0), c_end = min(nq, A.q_hi - q0);
+    if (c_begin >= c_end && !(nq == 0 && A.q_lo == 0)) return;
+    const bool first = c_begin == 0, last = c_end == nq;
     const int W = A.W;
     const int Dall = 3 * H * kD;
     const bool gated = a.gate != nullptr;
@@ -424,17 +436,32 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_scan_kernel(const __gri
     const uint32_t tl = tbase + (lrow << 16);
     const int quarter = warp >> 2;
     const int j = lrow + lane;                          // this thread's TMEM lane: dv channel
-    {   // S'^T <- S0^T (true state; basis factor 1)
+    // S'^T <- S0^T (true state, basis factor 1) at the sequence start, else the carried state
+    float logf_cur = 0.f;         // tid < 128: log of the basis factor of the current chunk
+    {
         for (int cb = 0; cb < 32; cb += 16) {
             uint32_t r[16];
+            if (first) {
 #pragma unroll
-            for (int u = 0; u < 16; ++u) {
-                const int c = quarter * 32 + cb + u;
-                r[u] = __float_as_uint(a.S0 ? a.S0[((size_t)nh * kD + c) * kD + j] : 0.f);
+                for (int u = 0; u < 16; ++u) {
+                    const int c = quarter * 32 + cb + u;
+                    r[u] = __float_as_uint(a.S0 ? a.S0[((size_t)nh * kD + c) * kD + j] : 0.f);
+                }
+            } else {
+                const float *carry = A.carry_S + ((size_t)nh * kD + j) * kD + quarter * 32 + cb;
+#pragma unroll
+                for (int u = 0; u < 16; u += 4) {
+                    const uint4 v = *reinterpret_cast<const uint4 *>(carry + u);
+                    r[u] = v.x; r[u + 1] = v.y; r[u + 2] = v.z; r[u + 3] = v.w;
+                }
             }
             tmem_st16(tl + kColSs + quarter * 32 + cb, r);
         }
         tmem_wait_st();
+        if (!first && tid < kD) {
+            logf_cur = A.carry_logf[(size_t)nh * kD + tid];
+            sLogf[tid] = logf_cur;
+        }
     }
 
     auto rec_of = [&](int c) { return A.rec + ((size_t)(q0 + c) * H + h) * REC_BYTES; };
@@ -480,7 +507,6 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_scan_kernel(const __gri
     // register-resident operands, one chunk ahead
     float uR[16];                 // U^T row j, tokens 16*quarter .. +15
     float rN = 0.f, glN = 0.f;    // tid < 128: r and G_last of the chunk after the current one
-    float logf_cur = 0.f;         // tid < 128: log of the basis factor of the current chunk
     auto load_u = [&](int c) {
         const uint8_t *p = rec_of(c) + REC_U;
 #pragma unroll
@@ -515,33 +541,34 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_scan_kernel(const __gri
 
     bool failed = false;
     PhaseClock clk;   // phases: 0 MMA W, 1 V' tile, 2 MMA O/S, 3 epilogue + next basis
-    if (nq > 0) {
+    if (c_begin < c_end) {
+        const int c = c_begin;
         if (tid == 0) {
-            load_x(0);
-            load(mb_k, REC_B, REC_B, 0, 49152, pend_k);     // [Aqk^T | Kb] hi, lo
-            if (gated) load_gate(0);
-            if (nq > 1) {
-                load_x(1);
-                if (gated) load_gate(1);
+            load_x(c);
+            load(mb_k, REC_B, REC_B, c, 49152, pend_k);     // [Aqk^T | Kb] hi, lo
+            if (gated) load_gate(c);
+            if (c + 1 < c_end) {
+                load_x(c + 1);
+                if (gated) load_gate(c + 1);
             }
         }
-        load_u(0);
+        load_u(c);
         if (tid < kD) {
-            load_vec(0);
-            sFcol[tid] = expf(rN);                       // the initial basis factor is 1
+            load_vec(c);
+            sFcol[(c & 1) * kD + tid] = expf(logf_cur + rN);
             logf_cur = glN - rN;
             sLogf[tid] = logf_cur;
-            if (nq > 1) load_vec(1);
+            if (c + 1 < c_end) load_vec(c + 1);
         }
         __syncthreads();
-        to_basis(sFcol);
+        to_basis(sFcol + (c & 1) * kD);
         tc_fence_before();
         __syncthreads();
     }
-    for (int c = 0; c < nq; ++c) {
+    for (int c = c_begin; c < c_end; ++c) {
         const int cs = tb + c * kC;
         const int Lc = min(kC, te - cs);
-        const bool more = c + 1 < nq;
+        const bool more = c + 1 < c_end;
         float *fnext = sFcol + ((c + 1) & 1) * kD;
         // ---- MMA: D^T = S'^T [W; Qh]^T ((W S')^T in D[0, 64), (Qh S')^T in D[64, 128)) ----
         if (tid == 0 && wait_x(c)) {
@@ -563,7 +590,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_scan_kernel(const __gri
             fnext[tid] = expf(logf_cur + rN);
             logf_cur = glN - rN;
             sLogf[tid] = logf_cur;
-            if (c + 2 < nq) load_vec(c + 2);
+            if (c + 2 < c_end) load_vec(c + 2);
         }
         if (!mma_wait()) { failed = true; break; }
         clk.tick(0);
@@ -612,7 +639,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_scan_kernel(const __gri
         }
         if (!mma_wait()) { failed = true; break; }
         if (tid == 0 && more) load(mb_k, REC_B, REC_B, c + 1, 49152, pend_k);   // [Aqk^T | Kb] of the next chunk
-        if (tid == 0 && c + 2 < nq) {                    // this chunk's [W; Qh] and gate buffers are free
+        if (tid == 0 && c + 2 < c_end) {                 // this chunk's [W; Qh] and gate buffers are free
             load_x(c + 2);
             if (gated) load_gate(c + 2);
         }
@@ -635,7 +662,21 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_scan_kernel(const __gri
         clk.tick(3);
     }
     clk.flush(reinterpret_cast<unsigned long long *>(a.status) + 8);
-    if (!failed) {
+    if (!failed && !last) {
+        tc_fence_after();
+        // ---- hand the state (and its basis) to the launch that continues the sequence ----
+        float *carry = A.carry_S + ((size_t)nh * kD + j) * kD;
+        for (int cb = 0; cb < 32; cb += 16) {
+            uint32_t r[16];
+            tmem_ld16(tl + kColSs + quarter * 32 + cb, r);
+            tmem_wait_ld();
+#pragma unroll
+            for (int u = 0; u < 16; u += 4)
+                *reinterpret_cast<uint4 *>(carry + quarter * 32 + cb + u) = make_uint4(r[u], r[u + 1], r[u + 2], r[u + 3]);
+        }
+        if (tid < kD) A.carry_logf[(size_t)nh * kD + tid] = sLogf[tid];
+    }
+    if (!failed && last) {
         tc_fence_after();
         // ---- final state: S = S'^T diag(exp(logf)) ----
         if (a.Sfin) {
@@ -692,19 +733,69 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_scan_kernel(const __gri
 size_t max_chunks(int N, int T) { return ((size_t)T + 63u * (size_t)N) / kC; }
 size_t round256_(size_t b) { return (b + 255) & ~size_t(255); }
 
+// Segmented pipeline: the prep pass of chunk segment s + 1 (caller's stream) overlaps the scan of
+// segment s (a high-priority side stream of the library), ordered by events only; the scan hands
+// its state from one segment's launch to the next through the carry buffer.  Used when the
+// (sequence, head) pairs are few (the scan then leaves most SMs to the prep pass) and long.
+constexpr int kSegChunks = 64;
+constexpr int kMaxSegs = 64;
+constexpr int kMaxDevices = 64;
+bool use_segments(int N, int T, int H) { return (long long)N * H <= 64 && max_chunks(N, T) >= 2 * kSegChunks; }
+size_t carry_bytes(int N, int H) { return (size_t)N * H * (kD * kD + kD) * sizeof(float); }
+
+struct SideStream {
+    cudaStream_t stream = nullptr;
+    cudaEvent_t ev[kMaxSegs + 1] = {};
+    bool ready = false;
+};
+std::mutex g_side_mu;
+SideStream g_side[kMaxDevices];
+
+cudaError_t side_stream(SideStream **out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_side_mu);
+    SideStream &ss = g_side[dev];
+    if (!ss.ready) {
+        int lo = 0, hi = 0;
+        if ((e = cudaDeviceGetStreamPriorityRange(&lo, &hi)) != cudaSuccess ||
+            (e = cudaStreamCreateWithPriority(&ss.stream, cudaStreamNonBlocking, hi)) != cudaSuccess)
+            return e;
+        for (int i = 0; i <= kMaxSegs; ++i)
+            if ((e = cudaEventCreateWithFlags(&ss.ev[i], cudaEventDisableTiming)) != cudaSuccess) return e;
+        ss.ready = true;
+    }
+    *out = &ss;
+    return cudaSuccess;
+}
+
 }  // namespace
 
-// Workspace of the two-pass path (after the status word): chunk offsets, then the records.
+// Workspace of the two-pass path (after the status word): chunk offsets, the scan's state carry
+// (segmented pipeline only), then the records.
 size_t tc_split_workspace(int N, int T, int H) {
-    return round256_((size_t)(N + 1) * sizeof(int32_t)) + max_chunks(N, T) * (size_t)H * REC_BYTES;
+    return round256_((size_t)(N + 1) * sizeof(int32_t)) + (use_segments(N, T, H) ? round256_(carry_bytes(N, H)) : 0) +
+           max_chunks(N, T) * (size_t)H * REC_BYTES;
 }
 
 cudaError_t launch_prefill_tc_split(const PrefillArgs &p, const float *conv_w, float *conv_state, int W,
                                     void *ws, cudaStream_t s) {
     if ((long long)p.N * p.H == 0) return cudaSuccess;
-    int32_t *chunk_off = static_cast<int32_t *>(ws);
-    uint8_t *rec = static_cast<uint8_t *>(ws) + round256_((size_t)(p.N + 1) * sizeof(int32_t));
+    uint8_t *w = static_cast<uint8_t *>(ws);
+    int32_t *chunk_off = reinterpret_cast<int32_t *>(w);
+    w += round256_((size_t)(p.N + 1) * sizeof(int32_t));
+    const bool seg = use_segments(p.N, p.T, p.H);
+    float *carry_S = nullptr, *carry_logf = nullptr;
+    if (seg) {
+        carry_S = reinterpret_cast<float *>(w);
+        carry_logf = carry_S + (size_t)p.N * p.H * kD * kD;
+        w += round256_(carry_bytes(p.N, p.H));
+    }
+    uint8_t *rec = w;
     const int box_rows = p.T < kC ? p.T : kC;
+    const int qmax = (int)max_chunks(p.N, p.T);
     cudaError_t e;
     static bool attr_done = false;
     if (!attr_done) {
@@ -720,30 +811,24 @@ cudaError_t launch_prefill_tc_split(const PrefillArgs &p, const float *conv_w, f
         (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
         return e;
 
-    kda_chunk_offsets_kernel<<<1, 1024, 0, s>>>(p.cu, p.N, p.T, (int)max_chunks(p.N, p.T), chunk_off);
+    kda_chunk_offsets_kernel<<<1, 1024, 0, s>>>(p.cu, p.N, p.T, qmax, chunk_off);
     count_launch();
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
-    const size_t items = max_chunks(p.N, p.T) * (size_t)p.H;
-    if (items > 0) {
-        PrepArgs P{};
-        if ((e = make_row_map(&P.tm_q, p.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.T, p.H)) != cudaSuccess ||
-            (e = make_row_map(&P.tm_k, p.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.T, p.H)) != cudaSuccess ||
-            (e = make_row_map(&P.tm_v, p.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.T, p.H)) != cudaSuccess ||
-            (e = make_row_map(&P.tm_g, p.g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, p.T, p.H)) != cudaSuccess)
-            return e;
-        P.p = p;
-        P.conv_w = conv_w;
-        P.conv_state = conv_state;
-        P.W = conv_w ? W : 0;
-        P.box_rows = box_rows;
-        P.chunk_off = chunk_off;
-        P.rec = rec;
-        const unsigned grid = (unsigned)(items < (size_t)sms ? items : (size_t)sms);
-        kda_chunk_prep_kernel<<<grid, kThreads, kSmemBytes, s>>>(P);
-        count_launch();
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    }
+    PrepArgs P{};
+    if (qmax > 0 &&
+        ((e = make_row_map(&P.tm_q, p.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.T, p.H)) != cudaSuccess ||
+         (e = make_row_map(&P.tm_k, p.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.T, p.H)) != cudaSuccess ||
+         (e = make_row_map(&P.tm_v, p.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.T, p.H)) != cudaSuccess ||
+         (e = make_row_map(&P.tm_g, p.g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, p.T, p.H)) != cudaSuccess))
+        return e;
+    P.p = p;
+    P.conv_w = conv_w;
+    P.conv_state = conv_state;
+    P.W = conv_w ? W : 0;
+    P.box_rows = box_rows;
+    P.chunk_off = chunk_off;
+    P.rec = rec;
 
     ScanArgs S{};
     if (p.gate && p.T > 0 &&
@@ -755,9 +840,46 @@ cudaError_t launch_prefill_tc_split(const PrefillArgs &p, const float *conv_w, f
     S.W = conv_w ? W : 0;
     S.chunk_off = chunk_off;
     S.rec = rec;
-    kda_chunk_scan_kernel<<<(unsigned)(p.N * p.H), kThreads, kScanSmemBytes, s>>>(S);
-    count_launch();
-    return cudaGetLastError();
+    S.carry_S = carry_S;
+    S.carry_logf = carry_logf;
+    const unsigned scan_grid = (unsigned)(p.N * p.H);
+
+    auto prep = [&](int q_lo, int q_hi, int max_ctas, cudaStream_t st) -> cudaError_t {
+        const size_t items = (size_t)(q_hi - q_lo) * p.H;
+        if (items == 0) return cudaSuccess;
+        P.q_lo = q_lo;
+        P.q_hi = q_hi;
+        const unsigned grid = (unsigned)(items < (size_t)max_ctas ? items : (size_t)max_ctas);
+        kda_chunk_prep_kernel<<<grid, kThreads, kSmemBytes, st>>>(P);
+        count_launch();
+        return cudaGetLastError();
+    };
+    auto scan = [&](int q_lo, int q_hi, cudaStream_t st) -> cudaError_t {
+        S.q_lo = q_lo;
+        S.q_hi = q_hi;
+        kda_chunk_scan_kernel<<<scan_grid, kThreads, kScanSmemBytes, st>>>(S);
+        count_launch();
+        return cudaGetLastError();
+    };
+    if (!seg) {
+        if ((e = prep(0, qmax, sms, s)) != cudaSuccess) return e;
+        return scan(0, qmax, s);
+    }
+    SideStream *side = nullptr;
+    if ((e = side_stream(&side)) != cudaSuccess) return e;
+    const int nseg = std::min(kMaxSegs, (qmax + kSegChunks - 1) / kSegChunks);
+    const int per = (qmax + nseg - 1) / nseg;
+    const int reserve = (int)scan_grid;                    // SMs left to the concurrent scan
+    for (int k = 0; k < nseg; ++k) {
+        const int q_lo = k * per, q_hi = std::min(qmax, q_lo + per);
+        if ((e = prep(q_lo, q_hi, k == 0 ? sms : std::max(1, sms - reserve), s)) != cudaSuccess ||
+            (e = cudaEventRecord(side->ev[k], s)) != cudaSuccess ||
+            (e = cudaStreamWaitEvent(side->stream, side->ev[k], 0)) != cudaSuccess ||
+            (e = scan(q_lo, q_hi, side->stream)) != cudaSuccess)
+            return e;
+    }
+    if ((e = cudaEventRecord(side->ev[nseg], side->stream)) != cudaSuccess) return e;
+    return cudaStreamWaitEvent(s, side->ev[nseg], 0);
 }
 
 }  // namespace k3kda

@@ -121,6 +121,19 @@ def test_fused_mixer_varlen_with_conv_state(path):
     _check(c, path=path)
 
 
+def test_two_pass_segmented_varlen_with_states():
+    """Few (sequence, head) pairs and >= 128 chunks: the two passes run as a pipeline of chunk
+    segments, the scan handing its state between segment launches; the middle sequence (chunks
+    65 .. 130) crosses the segment boundary at chunk 67."""
+    c = KI.prefill_case("segmented_varlen", [4100, 4200, 70], 2, 128, 128, 64, "bf16", seed=40, s0_std=0.02,
+                        gate=True, conv_width=4, conv_state=True)
+    _check(c)
+
+
+def test_two_pass_segmented_single_long_sequence():
+    _check(KI.fused_mixer(seed=41, T=8300, H=1))
+
+
 @pytest.mark.parametrize("W", [1, 2, 3])
 def test_fused_mixer_narrow_conv_two_pass(W):
     """Conv widths below 4: the conv history before each chunk comes from the inputs (or, before
