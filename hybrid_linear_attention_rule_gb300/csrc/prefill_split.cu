@@ -28,6 +28,7 @@
 #include <cuda.h>
 
 #include <algorithm>
+#include <cstdlib>
 #include <mutex>
 
 #include "tc_chunk.cuh"
@@ -867,12 +868,24 @@ cudaError_t launch_prefill_tc_split(const PrefillArgs &p, const float *conv_w, f
     }
     SideStream *side = nullptr;
     if ((e = side_stream(&side)) != cudaSuccess) return e;
-    const int nseg = std::min(kMaxSegs, (qmax + kSegChunks - 1) / kSegChunks);
-    const int per = (qmax + nseg - 1) / nseg;
     const int reserve = (int)scan_grid;                    // SMs left to the concurrent scan
+    const int prep_ctas = std::max(1, sms - reserve);
+    // segment length near kSegChunks whose (chunk, head) items fill whole waves of the prep grid
+    int per = kSegChunks;
+    double best = 0.0;
+    for (int c = kSegChunks * 3 / 4; c <= kSegChunks * 5 / 4; ++c) {
+        const long long items = (long long)c * p.H, waves = (items + prep_ctas - 1) / prep_ctas;
+        const double eff = (double)items / (double)(waves * prep_ctas);
+        if (eff > best + 1e-9 || (eff > best - 1e-9 && std::abs(c - kSegChunks) < std::abs(per - kSegChunks))) {
+            best = eff;
+            per = c;
+        }
+    }
+    if ((qmax + per - 1) / per > kMaxSegs) per = (qmax + kMaxSegs - 1) / kMaxSegs;
+    const int nseg = (qmax + per - 1) / per;
     for (int k = 0; k < nseg; ++k) {
         const int q_lo = k * per, q_hi = std::min(qmax, q_lo + per);
-        if ((e = prep(q_lo, q_hi, k == 0 ? sms : std::max(1, sms - reserve), s)) != cudaSuccess ||
+        if ((e = prep(q_lo, q_hi, k == 0 ? sms : prep_ctas, s)) != cudaSuccess ||
             (e = cudaEventRecord(side->ev[k], s)) != cudaSuccess ||
             (e = cudaStreamWaitEvent(side->stream, side->ev[k], 0)) != cudaSuccess ||
             (e = scan(q_lo, q_hi, side->stream)) != cudaSuccess)
