@@ -140,6 +140,23 @@ class ClockSampler:
         return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
 
 
+# ---- replicas: the slowest rank's time is the job's time ----
+
+def max_over_ranks(values, world, device):
+    """Elementwise max of a list of floats over all ranks (identity at world == 1)."""
+    if world <= 1:
+        return [float(x) for x in values]
+    import torch
+    t = torch.tensor([float(x) for x in values], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return [float(x) for x in t.tolist()]
+
+
+def job_value(units_per_rank, world, seconds):
+    """Whole-job throughput of `world` replicas that each process `units_per_rank` units."""
+    return world * units_per_rank / seconds
+
+
 # ---- the GPU arm ----
 
 def make_inputs(torch, dev, seed):
@@ -225,10 +242,7 @@ def run_ours(args, rank, world, dev, torch):
     total_ms = t_start.elapsed_time(t_end)
     pre_ms = sum(e[0].elapsed_time(e[1]) for e in ev) / args.steps
     dec_ms = sum(e[1].elapsed_time(e[2]) for e in ev) / args.steps
-    if world > 1:
-        t = torch.tensor([total_ms, pre_ms, dec_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms, pre_ms, dec_ms = (float(x) for x in t.tolist())
+    total_ms, pre_ms, dec_ms = max_over_ranks([total_ms, pre_ms, dec_ms], world, dev)
     ms_per_step = total_ms / args.steps
     tokens_per_step = T + N
 
@@ -246,7 +260,7 @@ def run_ours(args, rank, world, dev, torch):
     roof_d["frac"] = roof_d["achieved"] / roof_d["peak"]
 
     res = {
-        "metric": METRIC, "value": world * tokens_per_step / (ms_per_step / 1e3), "unit": "tokens/s",
+        "metric": METRIC, "value": job_value(tokens_per_step, world, ms_per_step / 1e3), "unit": "tokens/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "io_dtype": "bf16", "data": "synthetic",
@@ -304,11 +318,8 @@ def run_e2e(args, K, torch, dev, P, Dc, prefill_call, decode_call, out_p, fs, ou
         step()
     torch.cuda.synchronize()
     dt = (time.perf_counter() - t0) / n
-    if world > 1:
-        t = torch.tensor([dt], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        dt = float(t.item())
-    return {"value": world * (PREFILL["T"] + DECODE["N"]) / dt, "unit": "tokens/s", "ms_per_step": dt * 1e3,
+    dt = max_over_ranks([dt], world, dev)[0]
+    return {"value": job_value(PREFILL["T"] + DECODE["N"], world, dt), "unit": "tokens/s", "ms_per_step": dt * 1e3,
             "steps": n, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
 
