@@ -21,7 +21,8 @@ import torch
 
 __all__ = ["K3KDAError", "load_library", "library_path", "F32", "BF16", "L2_EPS",
            "k3kda_version", "k3kda_status_string", "k3kda_launch_count", "k3kda_short_conv",
-           "k3kda_prefill_workspace_size", "k3kda_prefill_workspace_min", "k3kda_prefill", "k3kda_prefill_noalloc", "k3kda_workspace_status",
+           "k3kda_prefill_workspace_size", "k3kda_prefill_workspace_min", "k3kda_prefill", "k3kda_prefill_slots",
+           "k3kda_decode_step_slots", "k3kda_prefill_noalloc", "k3kda_workspace_status",
            "k3kda_decode_step", "prefill", "decode_step", "short_conv"]
 
 F32, BF16 = 0, 1
@@ -80,6 +81,12 @@ def load_library(build_if_missing: bool = True):
         lib.k3kda_workspace_status.restype = I
         lib.k3kda_decode_step.argtypes = [P, P, P, I, P, P, P, P, P, P, I, I, I, I, I, F, I, P, I, P]
         lib.k3kda_decode_step.restype = I
+        lib.k3kda_prefill_slots.argtypes = [P, P, P, I, P, P, P, P, P, I, P, P, I, I, I, I, I, I, F, I, P, P,
+                                            P, I, P, Z, P]
+        lib.k3kda_prefill_slots.restype = I
+        lib.k3kda_decode_step_slots.argtypes = [P, P, P, I, P, P, P, P, P, P, P, P, I, I, I, I, I, I, F, I, P, I,
+                                                P]
+        lib.k3kda_decode_step_slots.restype = I
         _lib = lib
         return lib
 
@@ -170,6 +177,43 @@ def k3kda_prefill(q, k, v, g, beta, initial_state, cu_seqlens, cu_seqlens_host, 
                            _ptr(final_state), _ptr(workspace), workspace.numel() * workspace.element_size(),
                            _stream(stream))
     _check("k3kda_prefill", st)
+
+
+def _host_i32(t, what):
+    if t is None:
+        return None
+    if t.is_cuda or t.dtype != torch.int32 or not t.is_contiguous():
+        raise ValueError(f"{what} must be a contiguous CPU int32 tensor")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def k3kda_prefill_slots(q, k, v, g, beta, state_pool, state_idx, state_idx_host, num_slots, cu_seqlens,
+                        cu_seqlens_host, N, T, H, dk, dv, chunk, scale, use_qk_l2norm, conv_weight,
+                        conv_state_pool, conv_W, gate, out, workspace, stream=None):
+    """k3kda_prefill on slot-indexed state pools: sequence n reads and updates slot state_idx[n]."""
+    lib = load_library()
+    conv = None
+    if conv_weight is not None:
+        conv = ctypes.byref(_ConvArgs(_ptr(conv_weight), _ptr(conv_state_pool), int(conv_W)))
+    st = lib.k3kda_prefill_slots(_ptr(q), _ptr(k), _ptr(v), _dtype(q), _ptr(g), _ptr(beta), _ptr(state_pool),
+                                 _ptr(state_idx), _host_i32(state_idx_host, "state_idx_host"), int(num_slots),
+                                 _ptr(cu_seqlens), _host_i32(cu_seqlens_host, "cu_seqlens_host"), int(N), int(T),
+                                 int(H), int(dk), int(dv), int(chunk), float(scale), int(bool(use_qk_l2norm)), conv,
+                                 _ptr(gate), _ptr(out), _dtype(out), _ptr(workspace),
+                                 workspace.numel() * workspace.element_size(), _stream(stream))
+    _check("k3kda_prefill_slots", st)
+
+
+def k3kda_decode_step_slots(q, k, v, g, beta, gate, conv_weight, conv_state_pool, state_pool, state_idx,
+                            state_idx_host, num_slots, N, H, dk, dv, W, scale, use_qk_l2norm, out, stream=None):
+    """k3kda_decode_step on slot-indexed state pools: sequence n reads and updates slot state_idx[n]."""
+    lib = load_library()
+    st = lib.k3kda_decode_step_slots(_ptr(q), _ptr(k), _ptr(v), _dtype(q), _ptr(g), _ptr(beta), _ptr(gate),
+                                     _ptr(conv_weight), _ptr(conv_state_pool), _ptr(state_pool), _ptr(state_idx),
+                                     _host_i32(state_idx_host, "state_idx_host"), int(num_slots), int(N), int(H),
+                                     int(dk), int(dv), int(W), float(scale), int(bool(use_qk_l2norm)), _ptr(out),
+                                     _dtype(out), _stream(stream))
+    _check("k3kda_decode_step_slots", st)
 
 
 def k3kda_prefill_noalloc(q, k, v, g, beta, initial_state, cu_seqlens, cu_seqlens_host, N, T, H, dk, dv,

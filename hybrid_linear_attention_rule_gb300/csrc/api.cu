@@ -5,6 +5,7 @@
 #include <stdio.h>
 #include <atomic>
 #include <string.h>
+#include <vector>
 
 #include "common.cuh"
 
@@ -47,6 +48,18 @@ bool cu_ok(const int32_t *cu, int N, int T) {
     return true;
 }
 
+// Host-side check of a host copy of a slot map: every entry in [0, num_slots), none repeated
+// (two sequences updating one slot in the same call would race).
+bool slots_ok(const int32_t *slot, int N, int num_slots) {
+    if (num_slots < 1) return false;
+    std::vector<unsigned char> seen((size_t)num_slots, 0);
+    for (int n = 0; n < N; ++n) {
+        const int32_t x = slot[n];
+        if (x < 0 || x >= num_slots || seen[(size_t)x]) return false;
+        seen[(size_t)x] = 1;
+    }
+    return true;
+}
 constexpr size_t kStatusBytes = 256;
 
 size_t round256(size_t b) { return (b + 255) & ~size_t(255); }
@@ -117,12 +130,12 @@ size_t k3kda_prefill_workspace_min(int N, int T, int H, int dk, int dv, int chun
     return k3kda_prefill_workspace_size(N, T, H, dk, dv, chunk, in_dtype, has_conv);
 }
 
-int k3kda_prefill(const void *q, const void *k, const void *v, int in_dtype, const float *g,
-                  const float *beta, const float *initial_state, const int32_t *cu_seqlens,
-                  const int32_t *cu_seqlens_host, int N, int T, int H, int dk, int dv, int chunk,
-                  float scale, int use_qk_l2norm, const k3kda_conv_args *conv, const void *gate,
-                  void *out, int out_dtype, float *final_state, void *workspace,
-                  size_t workspace_bytes, void *stream) {
+static int prefill_impl(const void *q, const void *k, const void *v, int in_dtype, const float *g,
+                        const float *beta, const float *initial_state, const int32_t *cu_seqlens,
+                        const int32_t *cu_seqlens_host, int N, int T, int H, int dk, int dv, int chunk,
+                        float scale, int use_qk_l2norm, const k3kda_conv_args *conv, const void *gate,
+                        void *out, int out_dtype, float *final_state, void *workspace,
+                        size_t workspace_bytes, void *stream, const int32_t *slot, int num_slots) {
     if (N < 1 || T < 0 || H < 1) return K3KDA_ERR_INVALID_ARG;
     if (!dtype_ok(in_dtype) || !dtype_ok(out_dtype)) return K3KDA_ERR_INVALID_ARG;
     if (!head_dim_ok(dk) || !head_dim_ok(dv)) return K3KDA_ERR_UNSUPPORTED;
@@ -155,6 +168,8 @@ int k3kda_prefill(const void *q, const void *k, const void *v, int in_dtype, con
     a.scale = scale; a.l2 = use_qk_l2norm != 0;
     a.gate = gate; a.gate_bf16 = in_dtype == K3KDA_BF16; a.out = out; a.out_bf16 = out_dtype == K3KDA_BF16; a.Sfin = final_state;
     a.status = status;
+    a.slot = slot;
+    a.num_slots = num_slots;
 
     if (tc_prefill_supported(a.in_bf16, dk, dv, chunk)) {
         const float *cw = conv ? conv->weight : nullptr;
@@ -178,14 +193,15 @@ int k3kda_prefill(const void *q, const void *k, const void *v, int in_dtype, con
             int st = cuda_status(launch_short_conv_strided(
                 src[i], width[i], a.in_bf16, conv->weight + choff[i] * W,
                 conv->conv_state ? conv->conv_state + choff[i] : nullptr, D, cu_seqlens, N, T, (int)width[i],
-                W, 1, buf + choff[i], D, 0, s));
+                W, 1, buf + choff[i], D, 0, s, slot, num_slots));
             if (st != K3KDA_OK) return st;
         }
         if (conv->conv_state)
             for (int i = 0; i < 3; ++i) {
                 int st = cuda_status(launch_conv_state_update_strided(src[i], width[i], a.in_bf16,
                                                                       conv->conv_state + choff[i], D,
-                                                                      cu_seqlens, N, T, (int)width[i], W, s));
+                                                                      cu_seqlens, N, T, (int)width[i], W, s,
+                                                                      slot, num_slots));
                 if (st != K3KDA_OK) return st;
             }
         a.q = buf; a.k = buf + Dq; a.v = buf + 2 * Dq;
@@ -195,6 +211,32 @@ int k3kda_prefill(const void *q, const void *k, const void *v, int in_dtype, con
     if (T == 0 && final_state == nullptr) return K3KDA_OK;
     if (prefill_f32_smem_bytes(chunk, dk, dv) > 227 * 1024) return K3KDA_ERR_UNSUPPORTED;
     return cuda_status(launch_prefill_f32(a, s));
+}
+
+int k3kda_prefill(const void *q, const void *k, const void *v, int in_dtype, const float *g,
+                  const float *beta, const float *initial_state, const int32_t *cu_seqlens,
+                  const int32_t *cu_seqlens_host, int N, int T, int H, int dk, int dv, int chunk,
+                  float scale, int use_qk_l2norm, const k3kda_conv_args *conv, const void *gate,
+                  void *out, int out_dtype, float *final_state, void *workspace,
+                  size_t workspace_bytes, void *stream) {
+    return prefill_impl(q, k, v, in_dtype, g, beta, initial_state, cu_seqlens, cu_seqlens_host, N, T, H, dk, dv,
+                        chunk, scale, use_qk_l2norm, conv, gate, out, out_dtype, final_state, workspace,
+                        workspace_bytes, stream, nullptr, 0);
+}
+
+int k3kda_prefill_slots(const void *q, const void *k, const void *v, int in_dtype, const float *g,
+                        const float *beta, float *state_pool, const int32_t *state_idx,
+                        const int32_t *state_idx_host, int num_slots, const int32_t *cu_seqlens,
+                        const int32_t *cu_seqlens_host, int N, int T, int H, int dk, int dv, int chunk,
+                        float scale, int use_qk_l2norm, const k3kda_conv_args *conv, const void *gate,
+                        void *out, int out_dtype, void *workspace, size_t workspace_bytes, void *stream) {
+    if (N < 1 || num_slots < 1 || !state_pool || !state_idx) return K3KDA_ERR_INVALID_ARG;
+    if ((long long)num_slots * H * 4 > 0x7fffffffLL) return K3KDA_ERR_UNSUPPORTED;
+    if (!aligned4(state_idx)) return K3KDA_ERR_ALIGNMENT;
+    if (state_idx_host && !slots_ok(state_idx_host, N, num_slots)) return K3KDA_ERR_INVALID_ARG;
+    return prefill_impl(q, k, v, in_dtype, g, beta, state_pool, cu_seqlens, cu_seqlens_host, N, T, H, dk, dv,
+                        chunk, scale, use_qk_l2norm, conv, gate, out, out_dtype, state_pool, workspace,
+                        workspace_bytes, stream, state_idx, num_slots);
 }
 
 int k3kda_workspace_status(void *workspace, void *stream) {
@@ -212,10 +254,10 @@ int k3kda_workspace_status(void *workspace, void *stream) {
     return st != K3KDA_OK ? st : K3KDA_ERR_TIMEOUT;
 }
 
-int k3kda_decode_step(const void *q, const void *k, const void *v, int in_dtype, const float *g,
-                      const float *beta, const void *gate, const float *conv_weight, float *conv_state,
-                      float *state, int N, int H, int dk, int dv, int W, float scale, int use_qk_l2norm,
-                      void *out, int out_dtype, void *stream) {
+static int decode_impl(const void *q, const void *k, const void *v, int in_dtype, const float *g,
+                       const float *beta, const void *gate, const float *conv_weight, float *conv_state,
+                       float *state, int N, int H, int dk, int dv, int W, float scale, int use_qk_l2norm,
+                       void *out, int out_dtype, void *stream, const int32_t *slot, int num_slots) {
     if (N < 0 || H < 1) return K3KDA_ERR_INVALID_ARG;
     if (!dtype_ok(in_dtype) || !dtype_ok(out_dtype)) return K3KDA_ERR_INVALID_ARG;
     if (!head_dim_ok(dk) || !head_dim_ok(dv)) return K3KDA_ERR_UNSUPPORTED;
@@ -228,7 +270,28 @@ int k3kda_decode_step(const void *q, const void *k, const void *v, int in_dtype,
     if (!aligned4(beta)) return K3KDA_ERR_ALIGNMENT;
     return cuda_status(launch_decode(q, k, v, in_dtype == K3KDA_BF16, g, beta, gate, conv_weight, conv_state,
                                      state, N, H, dk, dv, conv_weight ? W : 0, scale, use_qk_l2norm != 0, out,
-                                     out_dtype == K3KDA_BF16, static_cast<cudaStream_t>(stream)));
+                                     out_dtype == K3KDA_BF16, static_cast<cudaStream_t>(stream), slot, num_slots));
+}
+
+int k3kda_decode_step(const void *q, const void *k, const void *v, int in_dtype, const float *g,
+                      const float *beta, const void *gate, const float *conv_weight, float *conv_state,
+                      float *state, int N, int H, int dk, int dv, int W, float scale, int use_qk_l2norm,
+                      void *out, int out_dtype, void *stream) {
+    return decode_impl(q, k, v, in_dtype, g, beta, gate, conv_weight, conv_state, state, N, H, dk, dv, W, scale,
+                       use_qk_l2norm, out, out_dtype, stream, nullptr, 0);
+}
+
+int k3kda_decode_step_slots(const void *q, const void *k, const void *v, int in_dtype, const float *g,
+                            const float *beta, const void *gate, const float *conv_weight, float *conv_state_pool,
+                            float *state_pool, const int32_t *state_idx, const int32_t *state_idx_host,
+                            int num_slots, int N, int H, int dk, int dv, int W, float scale, int use_qk_l2norm,
+                            void *out, int out_dtype, void *stream) {
+    if (N < 0 || num_slots < 1 || (N > 0 && !state_idx)) return K3KDA_ERR_INVALID_ARG;
+    if ((long long)num_slots * H > 0x7fffffffLL) return K3KDA_ERR_UNSUPPORTED;
+    if (!aligned4(state_idx)) return K3KDA_ERR_ALIGNMENT;
+    if (state_idx_host && !slots_ok(state_idx_host, N, num_slots)) return K3KDA_ERR_INVALID_ARG;
+    return decode_impl(q, k, v, in_dtype, g, beta, gate, conv_weight, conv_state_pool, state_pool, N, H, dk, dv, W,
+                       scale, use_qk_l2norm, out, out_dtype, stream, state_idx, num_slots);
 }
 
 }  // extern "C"

@@ -43,6 +43,15 @@ __device__ __forceinline__ void seq_bounds(const int32_t *cu, int n, int T, int 
     b = lo; e = hi;
 }
 
+// Pool slot of sequence n when a call maps its sequences onto a slot-indexed state pool
+// (continuous batching), n itself otherwise; -1 when the map's entry is outside [0, num_slots):
+// such a sequence starts from zero state and conv history and writes neither back.
+__device__ __forceinline__ int seq_slot(const int32_t *slot, int num_slots, int n) {
+    if (slot == nullptr) return n;
+    const int s = slot[n];
+    return (s >= 0 && s < num_slots) ? s : -1;
+}
+
 // Counts every kernel this library launches (reported by k3kda_launch_count).
 void count_launch();
 
@@ -57,15 +66,18 @@ cudaError_t launch_conv_state_update(const void *x, int x_bf16, float *cs, const
 cudaError_t launch_short_conv_strided(const void *x, int64_t x_stride, int x_bf16, const float *w,
                                       const float *cs, int64_t cs_stride, const int32_t *cu, int N,
                                       int T, int Dc, int W, int silu, void *out, int64_t out_stride,
-                                      int out_bf16, cudaStream_t s);
+                                      int out_bf16, cudaStream_t s, const int32_t *slot = nullptr,
+                                      int num_slots = 0);
 cudaError_t launch_conv_state_update_strided(const void *x, int64_t x_stride, int x_bf16, float *cs,
                                              int64_t cs_stride, const int32_t *cu, int N, int T,
-                                             int Dc, int W, cudaStream_t s);
+                                             int Dc, int W, cudaStream_t s, const int32_t *slot = nullptr,
+                                             int num_slots = 0);
 
 cudaError_t launch_decode(const void *q, const void *k, const void *v, int in_bf16, const float *g,
                           const float *beta, const void *gate, const float *conv_w, float *conv_state,
                           float *state, int N, int H, int dk, int dv, int W, float scale, int l2,
-                          void *out, int out_bf16, cudaStream_t s);
+                          void *out, int out_bf16, cudaStream_t s, const int32_t *slot = nullptr,
+                          int num_slots = 0);
 
 struct PrefillArgs {
     const void *q, *k, *v;   // [T,H,dk] x2, [T,H,dv]; element type by in_bf16
@@ -82,6 +94,8 @@ struct PrefillArgs {
     int out_bf16;
     float *Sfin;
     unsigned int *status;    // device status word (workspace offset 0)
+    const int32_t *slot;     // [N] pool slot of each sequence for S0 / Sfin / conv state, or null (slot n)
+    int num_slots;
 };
 
 cudaError_t launch_prefill_f32(const PrefillArgs &a, cudaStream_t s);

@@ -67,6 +67,8 @@ struct DecodeArgs {
     void *out;
     int out_bf16;
     unsigned int *status;   // may be null
+    const int32_t *slot;    // [N] state / conv-state row of each sequence, or null (row n)
+    int num_slots;
 };
 
 __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(DecodeArgs a) {
@@ -99,22 +101,28 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(DecodeArgs a) {
     if (warp == kConsumerWarps) {
         // ---------------- producer ----------------
         if (lane == 0) {
-            for (int kk = 0;; ++kk) {
+            // m counts the items actually staged: an item whose slot is out of range is skipped by
+            // the producer and the consumers alike, so both sides agree on stages and parities
+            for (int kk = 0, m = 0;; ++kk) {
                 const int it = blockIdx.x + kk * gridDim.x;
                 if (it >= NH) break;
-                const int s = kk & 1;
+                const int n = it / H, h = it - (it / H) * H;
+                const int sn = seq_slot(a.slot, a.num_slots, n);
+                if (sn < 0) continue;
+                const int s = m & 1;
                 const uint32_t P = smem_u32(sm + s * kStageBytes);
-                if (kk >= kStages && !mbar_wait_bounded(empty0 + 8 * s, ((kk - kStages) >> 1) & 1, kWaitLimit)) {
+                if (m >= kStages && !mbar_wait_bounded(empty0 + 8 * s, ((m - kStages) >> 1) & 1, kWaitLimit)) {
                     if (a.status) atomicOr(a.status, 2u);
                     break;
                 }
-                const int n = it / H, h = it - (it / H) * H;
+                ++m;
+                const size_t sit = (size_t)sn * H + h;      // the state this item reads and writes
                 uint32_t bytes = (uint32_t)(dk * dv * 4 + 2 * dk * esz + dv * esz + dk * 4);
                 if (a.gate) bytes += dv * esz;
                 if (a.conv_w) bytes += (uint32_t)(nch * 4 * (W - 1) + nch * 4 * W);
                 mbar_arrive_expect_tx(full0 + 8 * s, bytes);
                 const uint32_t fb = full0 + 8 * s;
-                bulk_g2s(P + ST_S, a.state + (size_t)it * dk * dv, dk * dv * 4, fb);
+                bulk_g2s(P + ST_S, a.state + sit * dk * dv, dk * dv * 4, fb);
                 bulk_g2s(P + ST_Q, (const char *)a.q + (size_t)it * dk * esz, dk * esz, fb);
                 bulk_g2s(P + ST_K, (const char *)a.k + (size_t)it * dk * esz, dk * esz, fb);
                 bulk_g2s(P + ST_V, (const char *)a.v + (size_t)it * dv * esz, dv * esz, fb);
@@ -128,7 +136,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(DecodeArgs a) {
                     for (int r = 0; r < W - 1; ++r)
                         for (int u = 0; u < 3; ++u)
                             bulk_g2s(P + ST_CS + (r * nch + loc[u]) * 4,
-                                     a.conv_state + ((size_t)n * (W - 1) + r) * D + seg[u], len[u] * 4, fb);
+                                     a.conv_state + ((size_t)sn * (W - 1) + r) * D + seg[u], len[u] * 4, fb);
                     for (int u = 0; u < 3; ++u)
                         bulk_g2s(P + ST_CW + loc[u] * W * 4, a.conv_w + seg[u] * W, len[u] * W * 4, fb);
                 }
@@ -139,17 +147,24 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(DecodeArgs a) {
 
     // ---------------- consumers (256 threads, named barrier 1) ----------------
     const bool colok = 4 * lane < dv;
-    for (int kk = 0;; ++kk) {
+    for (int kk = 0, m = 0;; ++kk) {
         const int it = blockIdx.x + kk * gridDim.x;
         if (it >= NH) break;
-        const int s = kk & 1;
-        uint8_t *P = sm + s * kStageBytes;
         const int n = it / H, h = it - (it / H) * H;
+        const int sn = seq_slot(a.slot, a.num_slots, n);
+        if (sn < 0) {                                  // no state to update: the output row is zero
+            if (tid < dv) store_elt(a.out, (size_t)it * dv + tid, 0.f, a.out_bf16);
+            continue;
+        }
+        const int s = m & 1;
+        uint8_t *P = sm + s * kStageBytes;
+        const size_t sit = (size_t)sn * H + h;
         const float bval = tid < dv ? __ldg(a.beta + it) : 0.f;   // in flight while the stage lands
-        if (tid == 0 && !mbar_wait_bounded(full0 + 8 * s, (kk >> 1) & 1, kWaitLimit)) {
+        if (tid == 0 && !mbar_wait_bounded(full0 + 8 * s, (m >> 1) & 1, kWaitLimit)) {
             *sflag = 1;
             if (a.status) atomicOr(a.status, 2u);
         }
+        ++m;
         named_bar(1, kConsumers);
         if (*sflag) break;
 
@@ -171,7 +186,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(DecodeArgs a) {
                 for (int r = 0; r < 3; ++r)
                     if (r < W - 1) { prev[r] = cs[r * nch + i]; acc = fmaf(w[r], prev[r], acc); }
                 const int ch = which == 0 ? h * dk + li : (which == 1 ? H * dk + h * dk + li : 2 * H * dk + h * dv + li);
-                float *gcs = a.conv_state + (size_t)n * (W - 1) * D + ch;
+                float *gcs = a.conv_state + (size_t)sn * (W - 1) * D + ch;
 #pragma unroll
                 for (int r = 0; r < 2; ++r)
                     if (r < W - 2) gcs[(size_t)r * D] = prev[r + 1];
@@ -257,7 +272,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(DecodeArgs a) {
 
         // 6. rank-1 update, streamed straight to HBM
         if (colok) {
-            float *Sg = a.state + (size_t)it * dk * dv;
+            float *Sg = a.state + sit * dk * dv;
             const float4 dd = *reinterpret_cast<const float4 *>(&sd[4 * lane]);
 #pragma unroll
             for (int r = 0; r < kRowsPerWarp; ++r) {
@@ -282,7 +297,7 @@ int g_num_sms = 0;
 cudaError_t launch_decode(const void *q, const void *k, const void *v, int in_bf16, const float *g,
                           const float *beta, const void *gate, const float *conv_w, float *conv_state,
                           float *state, int N, int H, int dk, int dv, int W, float scale, int l2,
-                          void *out, int out_bf16, cudaStream_t s) {
+                          void *out, int out_bf16, cudaStream_t s, const int32_t *slot, int num_slots) {
     if (N == 0) return cudaSuccess;
     if (g_num_sms == 0) {
         int dev = 0, sms = 0;
@@ -294,7 +309,7 @@ cudaError_t launch_decode(const void *q, const void *k, const void *v, int in_bf
         g_num_sms = sms;
     }
     DecodeArgs a{q, k, v, in_bf16, g, beta, gate, conv_w, conv_state, state, N, H, dk, dv, conv_w ? W : 0, scale,
-                 l2, out, out_bf16, nullptr};
+                 l2, out, out_bf16, nullptr, slot, num_slots};
     const long long items = (long long)N * H;
     const int grid = (int)(items < g_num_sms ? items : g_num_sms);
     decode_kernel<<<grid, kDecThreads, kSmemBytes, s>>>(a);

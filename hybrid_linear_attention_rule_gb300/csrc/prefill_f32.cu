@@ -56,6 +56,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_f32_kernel(PrefillArgs 
     const int vb = blockIdx.x % nvb;
     const int nh = blockIdx.x / nvb;
     const int h = nh % a.H, n = nh / a.H;
+    const int sn = seq_slot(a.slot, a.num_slots, n);           // state row of this sequence (-1: none)
+    const size_t snh = (size_t)(sn < 0 ? 0 : sn) * a.H + h;
     const int dk = a.dk, dv = a.dv, H = a.H;
     const Smem P = smem_plan(C, dk, BV);
     float *sQ = sm + P.q, *sK = sm + P.k, *sG = sm + P.G, *sW = sm + P.W, *sU = sm + P.U;
@@ -69,7 +71,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_f32_kernel(PrefillArgs 
     // state block S[:, j0:j0+BV]
     for (int e = tid; e < dk * BV; e += kPfThreads) {
         const int c = e / BV, j = e % BV;
-        sS[c * BVP + j] = a.S0 ? a.S0[((size_t)nh * dk + c) * dv + j0 + j] : 0.f;
+        sS[c * BVP + j] = (a.S0 && sn >= 0) ? a.S0[(snh * dk + c) * dv + j0 + j] : 0.f;
     }
 
     for (int cs = tb; cs < te; cs += C) {
@@ -183,10 +185,10 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_f32_kernel(PrefillArgs 
         }
     }
     __syncthreads();
-    if (a.Sfin)
+    if (a.Sfin && sn >= 0)
         for (int e = tid; e < dk * BV; e += kPfThreads) {
             const int c = e / BV, j = e % BV;
-            a.Sfin[((size_t)nh * dk + c) * dv + j0 + j] = sS[c * BVP + j];
+            a.Sfin[(snh * dk + c) * dv + j0 + j] = sS[c * BVP + j];
         }
 }
 

@@ -205,8 +205,9 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_prep_kernel(const __gri
                 v = __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(src)[((size_t)t * H + x.h) * kD + c]);
             } else {
                 const int row = W - 1 + (t - x.tb);
-                if (W > 1 && A.conv_state != nullptr && row >= 0)
-                    v = A.conv_state[((size_t)x.n * (W - 1) + row) * Dall + which * H * kD + x.h * kD + c];
+                const int sn = seq_slot(a.slot, a.num_slots, x.n);
+                if (W > 1 && A.conv_state != nullptr && row >= 0 && sn >= 0)
+                    v = A.conv_state[((size_t)sn * (W - 1) + row) * Dall + which * H * kD + x.h * kD + c];
             }
             sHist[e] = v;
         }
@@ -417,6 +418,8 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_scan_kernel(const __gri
     const int c_begin = max(0, A.q_lo - q0), c_end = min(nq, A.q_hi - q0);
     if (c_begin >= c_end && !(nq == 0 && A.q_lo == 0)) return;
     const bool first = c_begin == 0, last = c_end == nq;
+    const int sn = seq_slot(a.slot, a.num_slots, n);           // state / conv-state row (-1: none)
+    const size_t snh = (size_t)(sn < 0 ? 0 : sn) * a.H + h;
     const int W = A.W;
     const int Dall = 3 * H * kD;
     const bool gated = a.gate != nullptr;
@@ -446,7 +449,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_scan_kernel(const __gri
 #pragma unroll
                 for (int u = 0; u < 16; ++u) {
                     const int c = quarter * 32 + cb + u;
-                    r[u] = __float_as_uint(a.S0 ? a.S0[((size_t)nh * kD + c) * kD + j] : 0.f);
+                    r[u] = __float_as_uint((a.S0 && sn >= 0) ? a.S0[(snh * kD + c) * kD + j] : 0.f);
                 }
             } else {
                 const float *carry = A.carry_S + ((size_t)nh * kD + j) * kD + quarter * 32 + cb;
@@ -680,7 +683,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_scan_kernel(const __gri
     if (!failed && last) {
         tc_fence_after();
         // ---- final state: S = S'^T diag(exp(logf)) ----
-        if (a.Sfin) {
+        if (a.Sfin && sn >= 0) {
             for (int cb = 0; cb < 32; cb += 16) {
                 uint32_t r[16];
                 tmem_ld16(tl + kColSs + quarter * 32 + cb, r);
@@ -688,12 +691,12 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_scan_kernel(const __gri
 #pragma unroll
                 for (int u = 0; u < 16; ++u) {
                     const int c = quarter * 32 + cb + u;
-                    a.Sfin[((size_t)nh * kD + c) * kD + j] = __uint_as_float(r[u]) * expf(sLogf[c]);
+                    a.Sfin[(snh * kD + c) * kD + j] = __uint_as_float(r[u]) * expf(sLogf[c]);
                 }
             }
         }
         // ---- conv state: the last W-1 pre-conv inputs of this head's q, k, v channels ----
-        if (A.conv_state != nullptr && W > 1) {
+        if (A.conv_state != nullptr && W > 1 && sn >= 0) {
             const int L = te - tb;
             float keep[3] = {0.f, 0.f, 0.f};
             const int e = tid;
@@ -707,14 +710,14 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_scan_kernel(const __gri
                         const int p = L - (W - 1) + r;
                         keep[r] = p >= 0
                             ? __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(src)[((size_t)(tb + p) * H + h) * kD + c])
-                            : A.conv_state[((size_t)n * (W - 1) + (L + r)) * Dall + gch];
+                            : A.conv_state[((size_t)sn * (W - 1) + (L + r)) * Dall + gch];
                     }
             }
             __syncthreads();
             if (e < 384)
 #pragma unroll
                 for (int r = 0; r < 3; ++r)
-                    if (r < W - 1) A.conv_state[((size_t)n * (W - 1) + r) * Dall + gch] = keep[r];
+                    if (r < W - 1) A.conv_state[((size_t)sn * (W - 1) + r) * Dall + gch] = keep[r];
         }
     }
     if (tid == 0) {

@@ -60,6 +60,8 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
     const PrefillArgs &a = A.p;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int nh = blockIdx.x, n = nh / a.H, h = nh % a.H;
+    const int sn = seq_slot(a.slot, a.num_slots, n);           // state / conv-state row (-1: none)
+    const size_t snh = (size_t)(sn < 0 ? 0 : sn) * a.H + h;
     const int H = a.H;
     const uint32_t sbase = smem_u32(sm);
     float *sRef = reinterpret_cast<float *>(sm + OFF_REF);
@@ -88,8 +90,8 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
         const int which = e / 384, r = (e / 128) % 3, c = e & 127;
         const int row = W - 4 + r;                   // conv-state row holding token r - 3
         float x = 0.f;
-        if (W > 1 && A.conv_state != nullptr && row >= 0)
-            x = A.conv_state[((size_t)n * (W - 1) + row) * Dall + which * H * kD + h * kD + c];
+        if (W > 1 && A.conv_state != nullptr && row >= 0 && sn >= 0)
+            x = A.conv_state[((size_t)sn * (W - 1) + row) * Dall + which * H * kD + h * kD + c];
         sHist[e] = x;
     }
     if (W > 0)
@@ -114,7 +116,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
 #pragma unroll
             for (int u = 0; u < 16; ++u) {
                 const int c = quarter * 32 + cb + u;
-                r[u] = __float_as_uint(a.S0 ? a.S0[((size_t)nh * kD + c) * kD + j] : 0.f);
+                r[u] = __float_as_uint((a.S0 && sn >= 0) ? a.S0[(snh * kD + c) * kD + j] : 0.f);
             }
             tmem_st16(tl + kColS + quarter * 32 + cb, r);
         }
@@ -359,7 +361,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
 #undef PHASE
     if (!failed) {
         // ---- final state: S = S'^T diag(exp(logf)) ----
-        if (a.Sfin) {
+        if (a.Sfin && sn >= 0) {
             const int j = lrow + lane;
             for (int cb = 0; cb < 32; cb += 16) {
                 uint32_t r[16];
@@ -368,12 +370,12 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
 #pragma unroll
                 for (int u = 0; u < 16; ++u) {
                     const int c = quarter * 32 + cb + u;
-                    a.Sfin[((size_t)nh * kD + c) * kD + j] = __uint_as_float(r[u]) * expf(sLogf[c]);
+                    a.Sfin[(snh * kD + c) * kD + j] = __uint_as_float(r[u]) * expf(sLogf[c]);
                 }
             }
         }
         // ---- conv state: the last W-1 pre-conv inputs of this head's q, k, v channels ----
-        if (A.conv_state != nullptr && W > 1) {
+        if (A.conv_state != nullptr && W > 1 && sn >= 0) {
             const int L = te - tb;
             float keep[3] = {0.f, 0.f, 0.f};
             const int e = tid;
@@ -387,14 +389,14 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
                         const int p = L - (W - 1) + r;
                         keep[r] = p >= 0
                             ? __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(src)[((size_t)(tb + p) * H + h) * kD + c])
-                            : A.conv_state[((size_t)n * (W - 1) + (L + r)) * Dall + gch];
+                            : A.conv_state[((size_t)sn * (W - 1) + (L + r)) * Dall + gch];
                     }
             }
             __syncthreads();
             if (e < 384)
 #pragma unroll
                 for (int r = 0; r < 3; ++r)
-                    if (r < W - 1) A.conv_state[((size_t)n * (W - 1) + r) * Dall + gch] = keep[r];
+                    if (r < W - 1) A.conv_state[((size_t)sn * (W - 1) + r) * Dall + gch] = keep[r];
         }
     } else if (tid == 0) {
         mbar_wait_bounded(mbar_a, phase ^ 1u, kWaitLimit);   // let an in-flight MMA drain before freeing TMEM

@@ -37,6 +37,7 @@ struct ConvIO {
     const float *w;                     // [Dc, W] rows of the channels handled
     const float *cs; int64_t cs_stride; // conv state base (channel offset applied), row stride
     void *out; int64_t out_stride; int out_bf16;
+    const int32_t *slot; int num_slots;  // conv-state row of each sequence (null: its index)
 };
 
 template <int W>
@@ -59,8 +60,9 @@ short_conv_kernel(ConvIO io, const int32_t *cu, int N, int T, int Dc, int silu) 
         if (p >= b) return load_elt(io.x, (size_t)p * io.x_stride + c, io.x_bf16);
         if (io.cs == nullptr || W == 1) return 0.0f;
         const int row = (W - 1) + (p - b);      // 0 .. W-2 for a well-formed cu_seqlens
-        if (row < 0) return 0.0f;
-        return io.cs[((size_t)n * (W - 1) + row) * io.cs_stride + c];
+        const int sn = seq_slot(io.slot, io.num_slots, n);
+        if (row < 0 || sn < 0) return 0.0f;
+        return io.cs[((size_t)sn * (W - 1) + row) * io.cs_stride + c];
     };
     float win[W];
 #pragma unroll
@@ -85,10 +87,13 @@ short_conv_kernel(ConvIO io, const int32_t *cu, int N, int T, int Dc, int silu) 
 // the old row L + r when that position is before the start.  Rows are visited
 // in increasing r, and row r only reads old rows > r, so the update is in place.
 __global__ void conv_state_kernel(const void *x, int64_t x_stride, int x_bf16, float *cs,
-                                  int64_t cs_stride, const int32_t *cu, int N, int T, int Dc, int W) {
+                                  int64_t cs_stride, const int32_t *cu, int N, int T, int Dc, int W,
+                                  const int32_t *slot, int num_slots) {
     const int c = blockIdx.x * blockDim.x + threadIdx.x;
     const int n = blockIdx.y;
     if (c >= Dc || n >= N) return;
+    const int sn = seq_slot(slot, num_slots, n);
+    if (sn < 0) return;
     int b, e;
     seq_bounds(cu, n, T, b, e);
     const int L = e - b;
@@ -96,8 +101,8 @@ __global__ void conv_state_kernel(const void *x, int64_t x_stride, int x_bf16, f
         const int p = L - (W - 1) + r;
         float val;
         if (p >= 0) val = load_elt(x, (size_t)(b + p) * x_stride + c, x_bf16);
-        else val = cs[((size_t)n * (W - 1) + (L + r)) * cs_stride + c];
-        cs[((size_t)n * (W - 1) + r) * cs_stride + c] = val;
+        else val = cs[((size_t)sn * (W - 1) + (L + r)) * cs_stride + c];
+        cs[((size_t)sn * (W - 1) + r) * cs_stride + c] = val;
     }
 }
 
@@ -106,9 +111,9 @@ __global__ void conv_state_kernel(const void *x, int64_t x_stride, int x_bf16, f
 cudaError_t launch_short_conv_strided(const void *x, int64_t x_stride, int x_bf16, const float *w,
                                       const float *cs, int64_t cs_stride, const int32_t *cu, int N,
                                       int T, int Dc, int W, int silu, void *out, int64_t out_stride,
-                                      int out_bf16, cudaStream_t s) {
+                                      int out_bf16, cudaStream_t s, const int32_t *slot, int num_slots) {
     if (T == 0 || Dc == 0) return cudaSuccess;
-    ConvIO io{x, x_stride, x_bf16, w, cs, cs_stride, out, out_stride, out_bf16};
+    ConvIO io{x, x_stride, x_bf16, w, cs, cs_stride, out, out_stride, out_bf16, slot, num_slots};
     dim3 grid((Dc + kConvThreads - 1) / kConvThreads, (T + kConvTokens - 1) / kConvTokens);
     switch (W) {
         case 1: short_conv_kernel<1><<<grid, kConvThreads, 0, s>>>(io, cu, N, T, Dc, silu); count_launch(); break;
@@ -122,10 +127,11 @@ cudaError_t launch_short_conv_strided(const void *x, int64_t x_stride, int x_bf1
 
 cudaError_t launch_conv_state_update_strided(const void *x, int64_t x_stride, int x_bf16, float *cs,
                                              int64_t cs_stride, const int32_t *cu, int N, int T,
-                                             int Dc, int W, cudaStream_t s) {
+                                             int Dc, int W, cudaStream_t s, const int32_t *slot,
+                                             int num_slots) {
     if (W <= 1 || N == 0 || Dc == 0) return cudaSuccess;
     dim3 grid((Dc + 255) / 256, N);
-    conv_state_kernel<<<grid, 256, 0, s>>>(x, x_stride, x_bf16, cs, cs_stride, cu, N, T, Dc, W);
+    conv_state_kernel<<<grid, 256, 0, s>>>(x, x_stride, x_bf16, cs, cs_stride, cu, N, T, Dc, W, slot, num_slots);
     count_launch();
     return cudaGetLastError();
 }

@@ -184,6 +184,41 @@ int k3kda_prefill(const void *q, const void *k, const void *v, int in_dtype,
 int k3kda_workspace_status(void *workspace, void *stream);
 
 /*
+ * Slot-indexed state pools (continuous batching).  A serving runtime keeps the
+ * recurrent state of every live request in one FP32 pool and, per call, maps
+ * the call's sequences onto pool slots ("HybridCache" slot identity; state
+ * buffers FP32 and read-modify-write per the KdaState docs).  These two calls
+ * are k3kda_prefill / k3kda_decode_step with that indirection:
+ *   state_pool       [num_slots, H, dk, dv] FP32; sequence n starts from
+ *                    state_pool[state_idx[n]] and its final state is written
+ *                    back there (zero a slot before a new request's prefill)
+ *   conv_state_pool  [num_slots, W-1, 2*H*dk + H*dv] FP32, likewise per slot
+ *                    (for prefill: conv->conv_state is the pool)
+ *   state_idx        [N] int32, device, 4-byte aligned
+ *   state_idx_host   optional host copy: validated, INVALID_ARG when an entry
+ *                    is outside [0, num_slots) or repeated
+ * A device entry outside [0, num_slots) is never dereferenced: that sequence
+ * runs from zero state and conv history, writes nothing to the pools, and a
+ * decode writes a zero output row.  Repeated entries race (undefined result).
+ * Other arguments, layouts, errors: as k3kda_prefill / k3kda_decode_step.
+ */
+int k3kda_prefill_slots(const void *q, const void *k, const void *v, int in_dtype,
+                        const float *g, const float *beta, float *state_pool,
+                        const int32_t *state_idx, const int32_t *state_idx_host, int num_slots,
+                        const int32_t *cu_seqlens, const int32_t *cu_seqlens_host,
+                        int N, int T, int H, int dk, int dv, int chunk, float scale,
+                        int use_qk_l2norm, const k3kda_conv_args *conv, const void *gate,
+                        void *out, int out_dtype, void *workspace, size_t workspace_bytes,
+                        void *stream);
+
+int k3kda_decode_step_slots(const void *q, const void *k, const void *v, int in_dtype,
+                            const float *g, const float *beta, const void *gate,
+                            const float *conv_weight, float *conv_state_pool, float *state_pool,
+                            const int32_t *state_idx, const int32_t *state_idx_host, int num_slots,
+                            int N, int H, int dk, int dv, int W, float scale, int use_qk_l2norm,
+                            void *out, int out_dtype, void *stream);
+
+/*
  * k3kda_prefill_noalloc -- k3kda_prefill for callers that cannot allocate
  * device memory where they call the mixer (inside an allocator or memory
  * pool, in runtimes that forbid cudaMalloc after start-up, in plug-ins that

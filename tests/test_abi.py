@@ -107,6 +107,41 @@ def test_decode_rejects_bad_arguments(lib):
     assert dec(out=MIS) == -3
 
 
+def _i32(*vals):
+    arr = (ctypes.c_int32 * len(vals))(*vals)
+    return arr, ctypes.cast(arr, ctypes.c_void_p)
+
+
+def test_slot_pool_calls_validate_the_slot_map(lib):
+    def pre(**kw):
+        a = dict(q=A16, k=A16, v=A16, in_dtype=1, g=A16, beta=A16, pool=A16, idx=A16, idx_h=None, slots=8,
+                 cu=A16, cu_h=None, N=3, T=96, H=2, dk=128, dv=128, chunk=64, scale=1.0, l2=1, conv=None, gate=None,
+                 out=A16, out_dtype=0, ws=None, ws_bytes=0, stream=None)
+        a.update(kw)
+        return lib.k3kda_prefill_slots(*a.values())
+
+    def dec(**kw):
+        a = dict(q=A16, k=A16, v=A16, in_dtype=1, g=A16, beta=A16, gate=None, cw=None, cs=None, pool=A16,
+                 idx=A16, idx_h=None, slots=8, N=3, H=2, dk=128, dv=128, W=4, scale=1.0, l2=1, out=A16,
+                 out_dtype=0, stream=None)
+        a.update(kw)
+        return lib.k3kda_decode_step_slots(*a.values())
+
+    ok_keep, ok = _i32(5, 0, 7)
+    oob_keep, oob = _i32(5, 8, 1)                        # 8 is past the pool
+    neg_keep, neg = _i32(-1, 2, 3)
+    dup_keep, dup = _i32(2, 4, 2)                        # two sequences on one slot would race
+    for call in (pre, dec):
+        assert call(slots=0) == -1
+        assert call(idx=None) == -1
+        assert call(idx=ctypes.c_void_p(0x10002)) == -3     # state_idx must be 4-byte aligned
+        for bad in (oob, neg, dup):
+            assert call(idx_h=bad) == -1
+    assert pre(pool=None) == -1
+    assert pre(idx_h=ok, ws=None) == -4                  # a good map reaches the workspace check
+    assert dec(idx_h=ok, dv=130) == -2                   # ... and the shape checks
+
+
 def test_short_conv_rejects_bad_arguments(lib):
     def conv(**kw):
         a = dict(x=A16, xt=1, w=A16, cs=None, cu=None, N=1, T=10, D=64, W=4, silu=1, out=ctypes.c_void_p(0x20000),
