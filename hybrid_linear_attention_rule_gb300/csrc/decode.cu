@@ -16,8 +16,8 @@
 // SM) walk the (n, h) items with a two-stage shared-memory ring: a producer
 // warp streams each item's state and its small inputs (q, k, v, g, gate, the
 // conv window and weights) with cp.async.bulk copies that complete on an
-// mbarrier, while 8 consumer warps work on the previous item.  Consumers pull
-// the state into registers (warp w: rows w, w+8, ...; lane l: columns
+// mbarrier, while 16 consumer warps work on the previous item.  Consumers pull
+// the state into registers (warp w: rows w, w+16, ...; lane l: columns
 // 4l..4l+3), hand the stage back at once, reduce the column sums across warps
 // through shared memory, and write the new state straight to HBM with
 // streaming 128-bit stores, so loads of the next items overlap compute and
@@ -30,11 +30,11 @@ namespace {
 
 using namespace tc;
 
-constexpr int kConsumerWarps = 8;
+constexpr int kConsumerWarps = 16;
 constexpr int kConsumers = 32 * kConsumerWarps;
 constexpr int kDecThreads = kConsumers + 32;      // + one producer warp
 constexpr int kMaxD = 128;
-constexpr int kRowsPerWarp = kMaxD / kConsumerWarps;   // 16
+constexpr int kRowsPerWarp = kMaxD / kConsumerWarps;   // 8
 constexpr int kStages = 2;
 constexpr uint32_t kWaitLimit = 1u << 26;
 
