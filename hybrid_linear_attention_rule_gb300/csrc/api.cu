@@ -13,7 +13,6 @@ namespace k3kda {
 size_t prefill_f32_smem_bytes(int chunk, int dk, int dv);
 bool tc_prefill_supported(int in_bf16, int dk, int dv, int chunk);
 size_t tc_prefill_workspace(int N, int H);
-cudaError_t launch_prefill_tc(const PrefillArgs &a, const int32_t *order, cudaStream_t s);
 cudaError_t launch_prefill_tc_fused(const PrefillArgs &p, const float *conv_w, float *conv_state, int W,
                                     cudaStream_t s);
 size_t tc_split_workspace(int N, int T, int H);

@@ -473,9 +473,4 @@ cudaError_t launch_prefill_tc_fused(const PrefillArgs &p, const float *conv_w, f
     return cudaGetLastError();
 }
 
-cudaError_t launch_prefill_tc(const PrefillArgs &a, const int32_t *order, cudaStream_t s) {
-    (void)order;
-    return launch_prefill_tc_fused(a, nullptr, nullptr, 0, s);
-}
-
 }  // namespace k3kda
