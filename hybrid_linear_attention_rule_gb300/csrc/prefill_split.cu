@@ -107,7 +107,7 @@ struct PrepArgs {
     int W;
     int box_rows;
     const int32_t *chunk_off; // [N + 1]
-    uint8_t *rec;             // [total chunks * H] records
+    uint8_t *rec;             // records of this launch's chunks: [(q - q_lo) * H + h]
     int q_lo, q_hi;           // global chunk range of this launch (items q * H + h)
 };
 
@@ -289,7 +289,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_prep_kernel(const __gri
         clk.tick(5);
 
         // ---- U^T -> the record (straight from registers), W -> X/XL rows 0-63 ----
-        uint8_t *rec = A.rec + (size_t)it * REC_BYTES;
+        uint8_t *rec = A.rec + (size_t)(it - item_lo) * REC_BYTES;
         {
             const int j = lrow + lane;                  // dv channel for U^T, dk channel for W^T
             uint32_t r[16];
@@ -345,7 +345,7 @@ struct ScanArgs {
     float *conv_state;        // [N, W-1, 3*H*128] advanced at the end, or null
     int W;
     const int32_t *chunk_off;
-    const uint8_t *rec;
+    const uint8_t *rec;       // records of this launch's chunks: [(q - q_lo) * H + h]
     int q_lo, q_hi;           // global chunk range of this launch
     float *carry_S;           // [N*H][128 dv][128 dk] state in the last chunk's basis between launches
     float *carry_logf;        // [N*H][128] log of that basis factor
@@ -468,7 +468,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_scan_kernel(const __gri
         }
     }
 
-    auto rec_of = [&](int c) { return A.rec + ((size_t)(q0 + c) * H + h) * REC_BYTES; };
+    auto rec_of = [&](int c) { return A.rec + ((size_t)(q0 + c - A.q_lo) * H + h) * REC_BYTES; };
     // thread 0's view of the outstanding asynchronous operations
     uint32_t aph = 0, kph = 0, xph0 = 0, xph1 = 0, gph0 = 0, gph1 = 0;
     bool pend_a = false, pend_k = false, pend_x0 = false, pend_x1 = false, pend_g0 = false, pend_g1 = false;
@@ -741,15 +741,26 @@ size_t round256_(size_t b) { return (b + 255) & ~size_t(255); }
 // segment s (a high-priority side stream of the library), ordered by events only; the scan hands
 // its state from one segment's launch to the next through the carry buffer.  Used when the
 // (sequence, head) pairs are few (the scan then leaves most SMs to the prep pass) and long.
+// Segments write their records into a ring of kRing buffers, so the workspace does not grow with
+// T: segment k's prep waits for the scan of segment k - kRing, the last reader of its buffer.
 constexpr int kSegChunks = 64;
 constexpr int kMaxSegs = 64;
+constexpr int kRing = 3;
 constexpr int kMaxDevices = 64;
 bool use_segments(int N, int T, int H) { return (long long)N * H <= 64 && max_chunks(N, T) >= 2 * kSegChunks; }
 size_t carry_bytes(int N, int H) { return (size_t)N * H * (kD * kD + kD) * sizeof(float); }
+// chunks one ring buffer holds: the longest segment the launcher may choose
+int ring_chunks(int N, int T) {
+    const int qmax = (int)max_chunks(N, T);
+    return std::max(kSegChunks * 5 / 4, (qmax + kMaxSegs - 1) / kMaxSegs);
+}
+// whether the records go through the ring (else every chunk's record has its own place)
+bool use_ring(int N, int T) { return max_chunks(N, T) > (size_t)kRing * ring_chunks(N, T); }
 
 struct SideStream {
     cudaStream_t stream = nullptr;
-    cudaEvent_t ev[kMaxSegs + 1] = {};
+    cudaEvent_t ev[kMaxSegs + 1] = {};   // prep of segment k done (scan k may start); [nseg]: all scans done
+    cudaEvent_t ev_scan[kMaxSegs] = {};  // scan of segment k done (its ring buffer may be rewritten)
     bool ready = false;
 };
 std::mutex g_side_mu;
@@ -769,6 +780,8 @@ cudaError_t side_stream(SideStream **out) {
             return e;
         for (int i = 0; i <= kMaxSegs; ++i)
             if ((e = cudaEventCreateWithFlags(&ss.ev[i], cudaEventDisableTiming)) != cudaSuccess) return e;
+        for (int i = 0; i < kMaxSegs; ++i)
+            if ((e = cudaEventCreateWithFlags(&ss.ev_scan[i], cudaEventDisableTiming)) != cudaSuccess) return e;
         ss.ready = true;
     }
     *out = &ss;
@@ -777,11 +790,13 @@ cudaError_t side_stream(SideStream **out) {
 
 }  // namespace
 
-// Workspace of the two-pass path (after the status word): chunk offsets, the scan's state carry
-// (segmented pipeline only), then the records.
+// Workspace of the two-pass path (after the status word): chunk offsets, then for the segmented
+// pipeline the scan's state carry and kRing record buffers, otherwise one record per (chunk, head).
 size_t tc_split_workspace(int N, int T, int H) {
-    return round256_((size_t)(N + 1) * sizeof(int32_t)) + (use_segments(N, T, H) ? round256_(carry_bytes(N, H)) : 0) +
-           max_chunks(N, T) * (size_t)H * REC_BYTES;
+    const size_t off = round256_((size_t)(N + 1) * sizeof(int32_t));
+    const size_t chunks = use_segments(N, T, H) && use_ring(N, T) ? (size_t)kRing * ring_chunks(N, T)
+                                                                   : max_chunks(N, T);
+    return off + (use_segments(N, T, H) ? round256_(carry_bytes(N, H)) : 0) + chunks * H * REC_BYTES;
 }
 
 cudaError_t launch_prefill_tc_split(const PrefillArgs &p, const float *conv_w, float *conv_state, int W,
@@ -886,12 +901,18 @@ cudaError_t launch_prefill_tc_split(const PrefillArgs &p, const float *conv_w, f
     }
     if ((qmax + per - 1) / per > kMaxSegs) per = (qmax + kMaxSegs - 1) / kMaxSegs;
     const int nseg = (qmax + per - 1) / per;
+    const bool ring = use_ring(p.N, p.T);
+    const int slot_chunks = ring_chunks(p.N, p.T);        // >= per by construction
     for (int k = 0; k < nseg; ++k) {
         const int q_lo = k * per, q_hi = std::min(qmax, q_lo + per);
-        if ((e = prep(q_lo, q_hi, k == 0 ? sms : prep_ctas, s)) != cudaSuccess ||
+        P.rec = rec + (ring ? (size_t)(k % kRing) * slot_chunks : (size_t)q_lo) * p.H * REC_BYTES;
+        S.rec = P.rec;
+        if ((ring && k >= kRing && (e = cudaStreamWaitEvent(s, side->ev_scan[k - kRing], 0)) != cudaSuccess) ||
+            (e = prep(q_lo, q_hi, k == 0 ? sms : prep_ctas, s)) != cudaSuccess ||
             (e = cudaEventRecord(side->ev[k], s)) != cudaSuccess ||
             (e = cudaStreamWaitEvent(side->stream, side->ev[k], 0)) != cudaSuccess ||
-            (e = scan(q_lo, q_hi, side->stream)) != cudaSuccess)
+            (e = scan(q_lo, q_hi, side->stream)) != cudaSuccess ||
+            (e = cudaEventRecord(side->ev_scan[k], side->stream)) != cudaSuccess)
             return e;
     }
     if ((e = cudaEventRecord(side->ev[nseg], side->stream)) != cudaSuccess) return e;

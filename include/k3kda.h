@@ -116,8 +116,11 @@ typedef struct k3kda_conv_args {
 /* Bytes of device workspace with which k3kda_prefill runs its fastest path for
  * these arguments (always a multiple of 256; at least 256, which holds the
  * device status word).  For the tensor-core shape (BF16, dk = dv = 128, chunk
- * 64) this is the two-pass path's chunk-record buffer: 148,480 bytes per
- * (64-token chunk, head), about 2.3 KB per token and head, plus N*4 bytes. */
+ * 64) this is the two-pass path's chunk-record buffer, 148,480 bytes per
+ * (64-token chunk, head) held at once: every chunk's record (about 2.3 KB per
+ * token and head) when N*H > 64 or the sequences are short; with N*H <= 64 and
+ * at least 128 chunks, at most three pipeline segments' worth (max(80,
+ * chunks/64) chunks each), independent of T, plus 66 KB per sequence and head. */
 size_t k3kda_prefill_workspace_size(int N, int T, int H, int dk, int dv, int chunk,
                                     int in_dtype, int has_conv);
 

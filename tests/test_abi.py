@@ -54,6 +54,14 @@ def test_workspace_size_is_aligned_and_grows_with_conv(lib):
     e = K.k3kda_prefill_workspace_size(3, 1000, 2, 128, 128, 64, K.BF16, True)
     assert e == 256 + 256 + ((1000 + 63 * 3) // 64) * 2 * 148480
     # fp32 CUDA-core shapes stage the conv output in an fp32 [T, D] buffer
+    # long sequences with few (sequence, head) pairs: a ring of three segments' records plus the
+    # scan's state carry (66,048 B per sequence and head), independent of T up to 64 segments
+    carry = -(-32 * 66048 // 256) * 256
+    ring = lambda chunks: min(chunks, 3 * max(80, -(-chunks // 64))) * 32 * 148480
+    for T in (8192, 65536, 1 << 18):
+        assert K.k3kda_prefill_workspace_size(1, T, 32, 128, 128, 64, K.BF16, True) == 256 + 256 + carry + ring(T // 64)
+    assert K.k3kda_prefill_workspace_size(1, 1 << 21, 32, 128, 128, 64, K.BF16, True) == \
+        256 + 256 + carry + ring((1 << 21) // 64)
     c = K.k3kda_prefill_workspace_size(1, 1024, 4, 64, 128, 64, K.BF16, False)
     d = K.k3kda_prefill_workspace_size(1, 1024, 4, 64, 128, 64, K.BF16, True)
     assert c >= 256 and c % 256 == 0 and d % 256 == 0

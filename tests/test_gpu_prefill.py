@@ -134,6 +134,12 @@ def test_two_pass_segmented_single_long_sequence():
     _check(KI.fused_mixer(seed=41, T=8300, H=1))
 
 
+def test_two_pass_segment_ring_wraps():
+    """300 chunks of one head: four segments through a ring of three record buffers, so a
+    prep launch rewrites the buffer of a segment whose scan has finished."""
+    _check(KI.fused_mixer(seed=42, T=19200, H=1))
+
+
 @pytest.mark.parametrize("W", [1, 2, 3])
 def test_fused_mixer_narrow_conv_two_pass(W):
     """Conv widths below 4: the conv history before each chunk comes from the inputs (or, before
