@@ -758,6 +758,7 @@ int ring_chunks(int N, int T) {
 bool use_ring(int N, int T) { return max_chunks(N, T) > (size_t)kRing * ring_chunks(N, T); }
 
 struct SideStream {
+    std::mutex enqueue;                  // one call's launches and event records at a time
     cudaStream_t stream = nullptr;
     cudaEvent_t ev[kMaxSegs + 1] = {};   // prep of segment k done (scan k may start); [nseg]: all scans done
     cudaEvent_t ev_scan[kMaxSegs] = {};  // scan of segment k done (its ring buffer may be rewritten)
@@ -886,6 +887,9 @@ cudaError_t launch_prefill_tc_split(const PrefillArgs &p, const float *conv_w, f
     }
     SideStream *side = nullptr;
     if ((e = side_stream(&side)) != cudaSuccess) return e;
+    // The events are shared by every call on this device: a concurrent call recording them between
+    // this call's record and wait would order this call's scans after the wrong prep launches.
+    std::lock_guard<std::mutex> enqueue_lock(side->enqueue);
     const int reserve = (int)scan_grid;                    // SMs left to the concurrent scan
     const int prep_ctas = std::max(1, sms - reserve);
     // segment length near kSegChunks whose (chunk, head) items fill whole waves of the prep grid

@@ -169,6 +169,11 @@ size_t k3kda_prefill_workspace_min(int N, int T, int H, int dk, int dv, int chun
  * sequence and head that carries the state); with less, one single-pass kernel
  * per sequence and head.  Every other supported shape runs an FP32 CUDA-core
  * chunked kernel.  All compute the same chunked algebra.
+ * With few (sequence, head) pairs (N*H <= 64) and at least 128 chunks the two
+ * passes run as a pipeline of chunk segments: the scan launches go to one
+ * high-priority stream per device that the library creates on first use and
+ * joins back to `stream` with events (so stream capture sees one fork/join);
+ * calls from several host threads are enqueued one after another there.
  * Errors: INVALID_ARG, UNSUPPORTED, ALIGNMENT, WORKSPACE, CUDA as above.
  * A bounded in-kernel wait that gives up records K3KDA_ERR_TIMEOUT in the
  * workspace status word (see k3kda_workspace_status) instead of hanging.

@@ -134,6 +134,43 @@ def test_two_pass_segmented_single_long_sequence():
     _check(KI.fused_mixer(seed=41, T=8300, H=1))
 
 
+def test_two_pass_pipeline_from_two_host_threads():
+    """Two host threads, each on its own stream, run the segmented pipeline (which shares the
+    library's side stream and events per device) repeatedly; every result must equal a run made
+    alone, bit for bit."""
+    import threading
+    cases = [KI.fused_mixer(seed=50 + i, T=8300, H=1) for i in range(2)]
+    devs = [case_to_device(c) for c in cases]
+
+    def once(i):
+        d = dict(devs[i])
+        d["conv_state"] = devs[i]["conv_state"].clone()
+        out, fs, _ = run_prefill(cases[i], d=d)
+        return out, fs
+
+    refs = [once(i) for i in range(2)]
+    results, errors = [[], []], []
+
+    def work(i):
+        try:
+            st = torch.cuda.Stream()
+            with torch.cuda.stream(st):
+                for _ in range(4):
+                    results[i].append(once(i))
+        except Exception as exc:          # surfaced below
+            errors.append(exc)
+
+    threads = [threading.Thread(target=work, args=(i,)) for i in range(2)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors, errors
+    for i in range(2):
+        for out, fs in results[i]:
+            assert torch.equal(out, refs[i][0]) and torch.equal(fs, refs[i][1])
+
+
 def test_two_pass_segment_ring_wraps():
     """300 chunks of one head: four segments through a ring of three record buffers, so a
     prep launch rewrites the buffer of a segment whose scan has finished."""
