@@ -7,6 +7,8 @@
 #include <stdint.h>
 #include <stddef.h>
 
+#include <atomic>
+
 #include "k3kda.h"
 
 namespace k3kda {
@@ -50,6 +52,19 @@ __device__ __forceinline__ int seq_slot(const int32_t *slot, int num_slots, int 
     if (slot == nullptr) return n;
     const int s = slot[n];
     return (s >= 0 && s < num_slots) ? s : -1;
+}
+
+// Raise a kernel's dynamic shared-memory limit on the current device, once per device (the
+// attribute belongs to the device's context); safe to call from several host threads.
+inline cudaError_t smem_attr_once(const void *func, int bytes, std::atomic<uint64_t> &done) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint64_t bit = dev >= 0 && dev < 64 ? uint64_t(1) << dev : 0;
+    if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+    e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_release);
+    return e;
 }
 
 // Counts every kernel this library launches (reported by k3kda_launch_count).

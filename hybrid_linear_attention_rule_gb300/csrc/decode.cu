@@ -290,7 +290,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(DecodeArgs a) {
     }
 }
 
-int g_num_sms = 0;
+std::atomic<uint64_t> g_decode_attr{0};
 
 }  // namespace
 
@@ -299,19 +299,15 @@ cudaError_t launch_decode(const void *q, const void *k, const void *v, int in_bf
                           float *state, int N, int H, int dk, int dv, int W, float scale, int l2,
                           void *out, int out_bf16, cudaStream_t s, const int32_t *slot, int num_slots) {
     if (N == 0) return cudaSuccess;
-    if (g_num_sms == 0) {
-        int dev = 0, sms = 0;
-        cudaError_t e = cudaGetDevice(&dev);
-        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
-        if (e != cudaSuccess) return e;
-        g_num_sms = sms;
-    }
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess) e = smem_attr_once((const void *)decode_kernel, (int)kSmemBytes, g_decode_attr);
+    if (e != cudaSuccess) return e;
     DecodeArgs a{q, k, v, in_bf16, g, beta, gate, conv_w, conv_state, state, N, H, dk, dv, conv_w ? W : 0, scale,
                  l2, out, out_bf16, nullptr, slot, num_slots};
     const long long items = (long long)N * H;
-    const int grid = (int)(items < g_num_sms ? items : g_num_sms);
+    const int grid = (int)(items < sms ? items : sms);
     decode_kernel<<<grid, kDecThreads, kSmemBytes, s>>>(a);
     count_launch();
     return cudaGetLastError();

@@ -817,15 +817,10 @@ cudaError_t launch_prefill_tc_split(const PrefillArgs &p, const float *conv_w, f
     const int box_rows = p.T < kC ? p.T : kC;
     const int qmax = (int)max_chunks(p.N, p.T);
     cudaError_t e;
-    static bool attr_done = false;
-    if (!attr_done) {
-        if ((e = cudaFuncSetAttribute(kda_chunk_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      (int)kSmemBytes)) != cudaSuccess ||
-            (e = cudaFuncSetAttribute(kda_chunk_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      (int)kScanSmemBytes)) != cudaSuccess)
-            return e;
-        attr_done = true;
-    }
+    static std::atomic<uint64_t> prep_attr{0}, scan_attr{0};
+    if ((e = smem_attr_once((const void *)kda_chunk_prep_kernel, (int)kSmemBytes, prep_attr)) != cudaSuccess ||
+        (e = smem_attr_once((const void *)kda_chunk_scan_kernel, (int)kScanSmemBytes, scan_attr)) != cudaSuccess)
+        return e;
     int dev = 0, sms = 0;
     if ((e = cudaGetDevice(&dev)) != cudaSuccess ||
         (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)

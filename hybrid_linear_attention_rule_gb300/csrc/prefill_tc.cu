@@ -456,13 +456,9 @@ cudaError_t launch_prefill_tc_fused(const PrefillArgs &p, const float *conv_w, f
             (p.gate && (e = make_row_map(&A.tm_gate, p.gate, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.T, p.H)) != cudaSuccess))
             return e;
     }
-    static bool attr_done = false;
-    if (!attr_done) {
-        cudaError_t e = cudaFuncSetAttribute(kda_prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)kSmemBytes);
-        if (e != cudaSuccess) return e;
-        attr_done = true;
-    }
+    static std::atomic<uint64_t> attr_done{0};
+    if (cudaError_t e = smem_attr_once((const void *)kda_prefill_tc_kernel, (int)kSmemBytes, attr_done))
+        return e;
     A.p = p;
     A.conv_w = conv_w;
     A.conv_state = conv_state;
