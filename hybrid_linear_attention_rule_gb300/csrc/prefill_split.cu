@@ -140,8 +140,6 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_prep_kernel(const __gri
     const uint32_t lrow = 32u * (warp & 3);
     const uint32_t tl = tbase + (lrow << 16);
     const int quarter = warp >> 2;
-    const int item_lo = A.q_lo * H;
-    const int total = min(A.chunk_off[N], A.q_hi) * H;   // one past the last item of this launch
     const uint32_t kStageBytes = (uint32_t)A.box_rows * (kD * 4 + 3 * kD * 2);
 
     // thread 0's view of the outstanding asynchronous operations
@@ -165,25 +163,32 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_prep_kernel(const __gri
         return !bad;
     };
 
-    // work item -> (head, sequence, chunk start)
-    struct Item { int h, n, tb, te, cs; };
-    auto locate = [&](int it) {
+    // Items in head-major order (head, chunk), each CTA taking a contiguous run of them: a CTA's
+    // consecutive items are then mostly consecutive chunks of one head, whose conv history is the
+    // previous chunk's last staged rows and whose conv weights are already loaded.
+    const int nq = max(0, min(A.chunk_off[N], A.q_hi) - A.q_lo);   // chunks of this launch
+    const long long total = (long long)nq * H;
+    const int m_lo = (int)(total * blockIdx.x / gridDim.x);
+    const int m_hi = (int)(total * (blockIdx.x + 1) / gridDim.x);
+    struct Item { int h, qc, n, tb, te, cs; };
+    auto locate = [&](int m) {
         Item x;
-        const int qc = it / H;
-        x.h = it - qc * H;
+        x.h = m / nq;
+        x.qc = A.q_lo + (m - x.h * nq);
         int lo = 0, hi = N;                              // sequence n with off[n] <= qc < off[n + 1]
         while (hi - lo > 1) {
             const int mid = (lo + hi) >> 1;
-            if (A.chunk_off[mid] <= qc) lo = mid; else hi = mid;
+            if (A.chunk_off[mid] <= x.qc) lo = mid; else hi = mid;
         }
         x.n = lo;
         seq_bounds(a.cu, x.n, a.T, x.tb, x.te);
-        x.cs = x.tb + (qc - A.chunk_off[x.n]) * kC;
+        x.cs = x.tb + (x.qc - A.chunk_off[x.n]) * kC;
         return x;
     };
+    auto rec_of = [&](const Item &x) { return A.rec + ((size_t)(x.qc - A.q_lo) * H + x.h) * REC_BYTES; };
     // conv weights of the item's head and its conv history (pre-conv q, k, v rows of tokens
     // cs-3 .. cs-1 from the inputs, or from the right-aligned initial conv state before the
-    // sequence start), by all threads; prep_chunk is their only reader
+    // sequence start), by all threads; the prep stages are their only readers
     int cur_h = -1;
     auto load_history = [&](const Item &x) {
         if (W == 0) return;
@@ -212,31 +217,51 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_prep_kernel(const __gri
             sHist[e] = v;
         }
     };
-    // An item's rows land in three pieces on one phase of mbar_s, each as soon as its region is
-    // free: v (after prep), q and k (after the triangular solve), g (after MMA U).  Thread 0.
-    auto stage_v = [&](const Item &x) {
+    // the conv history of the chunk after a whole chunk: its last three staged rows
+    auto copy_history = [&]() {
+        if (W == 0) return;
+        for (int e = tid; e < 3 * 3 * 128; e += kThreads) {
+            const int which = e / 384, r = (e / 128) % 3, c = e & 127;
+            const uint32_t st = which == 0 ? PlanPrep::QST : (which == 1 ? PlanPrep::KST : PlanPrep::VST);
+            sHist[e] = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(sm + st + (kC - 3 + r) * (kD * 2) + c * 2));
+        }
+    };
+    // An item's rows land on one phase of mbar_s in two pieces (thread 0): q, k, v while the
+    // previous item's MMA A runs, g once the previous item's triangular solve has freed region R.
+    auto stage_qkv = [&](const Item &x) {
         mbar_arrive_expect_tx(mbar_s, kStageBytes);
-        tma_load_3d(sbase + OFF_VST, &A.tm_v, 0, x.h, x.cs, mbar_s);
+        tma_load_3d(sbase + PlanPrep::QST, &A.tm_q, 0, x.h, x.cs, mbar_s);
+        tma_load_3d(sbase + PlanPrep::KST, &A.tm_k, 0, x.h, x.cs, mbar_s);
+        tma_load_3d(sbase + PlanPrep::VST, &A.tm_v, 0, x.h, x.cs, mbar_s);
         pend_s = true;
     };
-    auto stage_qk = [&](const Item &x) {
-        tma_load_3d(sbase + OFF_QST, &A.tm_q, 0, x.h, x.cs, mbar_s);
-        tma_load_3d(sbase + OFF_KST, &A.tm_k, 0, x.h, x.cs, mbar_s);
+    auto stage_g = [&](const Item &x) { tma_load_3d(sbase + PlanPrep::GST, &A.tm_g, 0, x.h, x.cs, mbar_s); };
+    auto prefetch_rows = [&](const Item &x) {        // into L2, an item ahead of the staging copies
+        tma_prefetch_3d(&A.tm_q, 0, x.h, x.cs);
+        tma_prefetch_3d(&A.tm_k, 0, x.h, x.cs);
+        tma_prefetch_3d(&A.tm_v, 0, x.h, x.cs);
+        tma_prefetch_3d(&A.tm_g, 0, x.h, x.cs);
     };
-    auto stage_g = [&](const Item &x) { tma_load_3d(sbase + OFF_GST, &A.tm_g, 0, x.h, x.cs, mbar_s); };
 
-    PhaseClock clk;   // phases: 0 staging wait, 1 prep, 2 MMA A (+ next history), 3 extract, 4 solve, 5 MMA U/W, 6 records out
-    if (item_lo + (int)blockIdx.x < total) {
-        const Item x0 = locate(item_lo + blockIdx.x);
-        if (tid == 0) { stage_v(x0); stage_qk(x0); stage_g(x0); }
+    PhaseClock clk;   // phases: 0 staging wait, 1 prep q/k, 2 prep v (MMA A), 3 history + MMA A wait, 4 extract, 5 solve, 6 MMA U/W, 7 records out
+    if (m_lo < m_hi) {
+        const Item x0 = locate(m_lo);
+        if (tid == 0) {
+            stage_qkv(x0);
+            stage_g(x0);
+            if (m_lo + 1 < m_hi) prefetch_rows(locate(m_lo + 1));
+        }
         load_history(x0);
     }
-    for (int it = item_lo + blockIdx.x; it < total; it += gridDim.x) {
-        const Item x = locate(it);
-        const bool has_next = it + (int)gridDim.x < total;
-        const Item y = has_next ? locate(it + gridDim.x) : x;
+    for (int m = m_lo; m < m_hi; ++m) {
+        const Item x = locate(m);
+        const bool has_next = m + 1 < m_hi;
+        const Item y = has_next ? locate(m + 1) : x;
+        const bool cont = has_next && y.h == x.h && y.qc == x.qc + 1 && y.cs > y.tb;
         const int Lc = min(kC, x.te - x.cs);
+        uint8_t *rec = rec_of(x);
         if (tid == 0) {
+            if (m + 2 < m_hi) prefetch_rows(locate(m + 2));
             bulk_wait_read_all();                        // the previous records have left shared memory
             wait_on(mbar_s, sph, pend_s);
         }
@@ -244,29 +269,51 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_prep_kernel(const __gri
         if (*sflag) break;
         clk.tick(0);
 
-        prep_chunk(sm, a, x.cs, Lc, x.h, W, nullptr, nullptr);
+        prep_qk<PlanPrep>(sm, a, x.cs, Lc, x.h, W, nullptr, nullptr);
         clk.tick(1);
         if (tid == 0) {
-            issue_mma_a(sbase, tbase + kColA, mbar_a);
+            issue_mma_a<PlanPrep>(sbase, tbase + kColA, mbar_a);
             pend_a = true;
-            if (has_next) stage_v(y);
+            // Qh (rows 64..127 of each K atom, hi and lo), Kb and r, G_last are final: out now
+#pragma unroll
+            for (int p = 0; p < 4; ++p)
+                bulk_s2g(rec + REC_X + p * 16384 + 8192, sbase + OFF_X + p * 16384 + 8192, 8192);
+            bulk_s2g(rec + REC_B + 8192, sbase + PlanPrep::KB_HI, 16384);
+            bulk_s2g(rec + REC_B + 32768, sbase + PlanPrep::KB_LO, 16384);
+            bulk_s2g(rec + REC_VEC, sbase + OFF_REF, 1024);     // r, G_last
+            bulk_commit();
         }
-        if (has_next) load_history(y);                   // overlaps MMA A
-        if (!mma_wait()) break;
+        prep_v<PlanPrep>(sm, a, Lc, W);                  // overlaps MMA A
         clk.tick(2);
-        extract_a(sm, tl, kColA);
+        if (has_next) {
+            if (cont) copy_history(); else load_history(y);
+        }
+        __syncthreads();                                 // this item's staged rows are consumed
+        if (tid == 0) {
+            if (has_next) stage_qkv(y);
+            bulk_wait_read_all();                        // Kb has left region R, which the extract reuses
+        }
+        if (!mma_wait()) break;
         clk.tick(3);
-        solve_tb(sm);
-        if (tid == 0 && has_next) stage_qk(y);           // the solve's scratch region is free
+        extract_a<PlanPrep>(sm, tl, kColA);
         clk.tick(4);
+        solve_tb<PlanPrep>(sm);
+        if (tid == 0) {
+            bulk_s2g(rec + REC_B, sbase + PlanPrep::AQK_HI, 8192);
+            bulk_s2g(rec + REC_B + 24576, sbase + PlanPrep::AQK_LO, 8192);
+            bulk_commit();
+            if (has_next) stage_g(y);                    // region R is free
+        }
+        clk.tick(5);
 
         // ---- MMA: U^T = v^T Tb^T and W^T = Kh^T Tb^T (Kh rows 0-63 of X read MN-major) ----
         if (tid == 0) {
             tc_fence_after();
             const uint32_t id = idesc_bf16_f32(128, 64, false, /*a_mn=*/true);
-            const uint64_t dVh = sdesc_mnmajor_sw128(sbase + OFF_V_HI, 8192), dVl = sdesc_mnmajor_sw128(sbase + OFF_V_LO, 8192);
+            const uint64_t dVh = sdesc_mnmajor_sw128(sbase + PlanPrep::V_HI, 8192),
+                           dVl = sdesc_mnmajor_sw128(sbase + PlanPrep::V_LO, 8192);
             const uint64_t dKh = sdesc_mnmajor_sw128(sbase + OFF_X, 16384), dKl = sdesc_mnmajor_sw128(sbase + OFF_XL, 16384);
-            const uint64_t dTh = sdesc_kmajor_sw128(sbase + OFF_TB_HI), dTl = sdesc_kmajor_sw128(sbase + OFF_TB_LO);
+            const uint64_t dTh = sdesc_kmajor_sw128(sbase + PlanPrep::TB_HI), dTl = sdesc_kmajor_sw128(sbase + PlanPrep::TB_LO);
             const int nsplit = W > 0 ? 3 : 2;           // v is exact bf16 without a conv
 #pragma unroll
             for (int sp = 0; sp < 3; ++sp)
@@ -285,11 +332,9 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_prep_kernel(const __gri
             pend_a = true;
         }
         if (!mma_wait()) break;
-        if (tid == 0 && has_next) stage_g(y);            // the v rows (region A) have been consumed
-        clk.tick(5);
+        clk.tick(6);
 
-        // ---- U^T -> the record (straight from registers), W -> X/XL rows 0-63 ----
-        uint8_t *rec = A.rec + (size_t)(it - item_lo) * REC_BYTES;
+        // ---- U^T -> the record (straight from registers), W -> X/XL rows 0-63 -> the record ----
         {
             const int j = lrow + lane;                  // dv channel for U^T, dk channel for W^T
             uint32_t r[16];
@@ -314,16 +359,12 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_prep_kernel(const __gri
         tc_fence_before();
         __syncthreads();
         if (tid == 0) {
-            bulk_s2g(rec + REC_X, sbase + OFF_X, 65536);
-            bulk_s2g(rec + REC_B, sbase + OFF_AQK_HI, 8192);
-            bulk_s2g(rec + REC_B + 8192, sbase + OFF_KB_HI, 16384);
-            bulk_s2g(rec + REC_B + 24576, sbase + OFF_AQK_LO, 8192);
-            bulk_s2g(rec + REC_B + 32768, sbase + OFF_KB_LO, 16384);
-            bulk_s2g(rec + REC_VEC, sbase + OFF_REF, 1024);     // r, G_last
+#pragma unroll
+            for (int p = 0; p < 4; ++p) bulk_s2g(rec + REC_X + p * 16384, sbase + OFF_X + p * 16384, 8192);
             bulk_commit();
         }
         tc_fence_after();
-        clk.tick(6);
+        clk.tick(7);
     }
     clk.flush(reinterpret_cast<unsigned long long *>(a.status) + 16);
     if (tid == 0) {
@@ -340,6 +381,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_prep_kernel(const __gri
 // ============================ pass 2: chunk scan ============================
 struct ScanArgs {
     CUtensorMap tm_gate;      // [T, H, 128] bf16 gate logits (when gated), box min(64, T) tokens of one head
+    CUtensorMap tm_out;       // [T, H, 128] bf16 outputs (when stored as bf16), same box
     PrefillArgs p;
     int box_rows;
     float *conv_state;        // [N, W-1, 3*H*128] advanced at the end, or null
@@ -356,7 +398,8 @@ struct ScanArgs {
 constexpr uint32_t Q_X1 = REC_U;                    // [W; Qh] tile of odd chunks (64 KB)
 constexpr uint32_t Q_G0 = Q_X1 + 65536;             // gate logits bf16 [64 tok][128] of even / odd chunks
 constexpr uint32_t Q_G1 = Q_G0 + 16384;
-constexpr uint32_t Q_LOGF = Q_G1 + 16384;           // log of the basis factor carried in TMEM
+constexpr uint32_t Q_OST = Q_G1 + 16384;            // bf16 outputs [64 tok][128] of one chunk, stored by TMA
+constexpr uint32_t Q_LOGF = Q_OST + 16384;          // log of the basis factor carried in TMEM
 constexpr uint32_t Q_FCOL = Q_LOGF + 512;           // state column factors, two chunks (double buffer)
 constexpr uint32_t Q_MISC = Q_FCOL + 1024;          // 6 mbarriers, tmem slot, flag
 constexpr uint32_t kScanSmemBytes = Q_MISC + 64 + 1024;
@@ -526,21 +569,29 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_scan_kernel(const __gri
     };
     // S'^T = S^T diag(fcol) -> TMEM, fp32 and split bf16 (the A operand of MMA W/Qh)
     auto to_basis = [&](const float *fcol) {
-        for (int cb = 0; cb < 32; cb += 16) {
-            const int col = quarter * 32 + cb;
-            uint32_t r[16];
-            tmem_ld16(tl + kColSs + col, r);
-            tmem_wait_ld();
+        uint32_t r[2][16];
+        tmem_ld16(tl + kColSs + quarter * 32, r[0]);
+        tmem_ld16(tl + kColSs + quarter * 32 + 16, r[1]);
+        tmem_wait_ld();
+#pragma unroll
+        for (int b = 0; b < 2; ++b) {
+            const int col = quarter * 32 + 16 * b;
             float v[16];
 #pragma unroll
             for (int u = 0; u < 16; ++u) {
-                v[u] = __uint_as_float(r[u]) * fcol[col + u];
-                r[u] = __float_as_uint(v[u]);
+                v[u] = __uint_as_float(r[b][u]) * fcol[col + u];
+                r[b][u] = __float_as_uint(v[u]);
             }
-            tmem_st16(tl + kColSs + col, r);
+            tmem_st16(tl + kColSs + col, r[b]);
             tmem_put_split16(tl + kColSh + col / 2, tl + kColSl + col / 2, v);
         }
         tmem_wait_st();
+    };
+
+    // a chunk's record and gate rows into L2 ahead of their copies into shared memory (thread 0)
+    auto prefetch_chunk = [&](int c) {
+        prefetch_l2(rec_of(c), REC_BYTES);
+        if (gated) tma_prefetch_3d(&A.tm_gate, 0, h, tb + c * kC);
     };
 
     bool failed = false;
@@ -550,6 +601,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_scan_kernel(const __gri
         if (tid == 0) {
             load_x(c);
             load(mb_k, REC_B, REC_B, c, 49152, pend_k);     // [Aqk^T | Kb] hi, lo
+            for (int d = 1; d <= 2 && c + d < c_end; ++d) prefetch_chunk(c + d);
             if (gated) load_gate(c);
             if (c + 1 < c_end) {
                 load_x(c + 1);
@@ -589,6 +641,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_scan_kernel(const __gri
             mma_commit(mb_a);
             pend_a = true;
         }
+        if (tid == 0 && c + 3 < c_end) prefetch_chunk(c + 3);
         // the next chunk's basis factor, while the MMAs run
         if (tid < kD && more) {
             fnext[tid] = expf(logf_cur + rN);
@@ -610,6 +663,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_scan_kernel(const __gri
             tmem_wait_st();
         }
         if (more) load_u(c + 1);
+        if (tid == 0) bulk_wait_read_all();              // the previous chunk's output tile has been read
         tc_fence_before();
         __syncthreads();
         clk.tick(1);
@@ -649,20 +703,36 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_scan_kernel(const __gri
         }
         clk.tick(2);
         // ---- this chunk's outputs, then the state into the next chunk's basis ----
+        // bf16 outputs go through a shared tile and one TMA store that runs behind the next chunk,
+        // unless the chunk is a ragged sequence end inside the tensor (the box would cross into
+        // the next sequence's rows; TMA clips only at the tensor's end)
+        const bool tma_out = a.out_bf16 && (Lc == kC || te == a.T);
         {
             uint32_t r0[16];
             tmem_ld16(tl + kColD + 64 + quarter * 16, r0);
             tmem_wait_ld();
+            if (tma_out) {
+                __nv_bfloat16 *ot = reinterpret_cast<__nv_bfloat16 *>(sm + Q_OST);
 #pragma unroll
-            for (int u = 0; u < 16; ++u) {
-                const int i = quarter * 16 + u;
-                if (i < Lc) store_elt(a.out, ((size_t)(cs + i) * H + h) * kD + j, a.scale * __uint_as_float(r0[u]) * sg[u],
-                                      a.out_bf16);
+                for (int u = 0; u < 16; ++u)
+                    ot[(quarter * 16 + u) * kD + j] = __float2bfloat16_rn(a.scale * __uint_as_float(r0[u]) * sg[u]);
+            } else {
+#pragma unroll
+                for (int u = 0; u < 16; ++u) {
+                    const int i = quarter * 16 + u;
+                    if (i < Lc) store_elt(a.out, ((size_t)(cs + i) * H + h) * kD + j, a.scale * __uint_as_float(r0[u]) * sg[u],
+                                          a.out_bf16);
+                }
             }
         }
         if (more) to_basis(fnext);
+        if (tma_out) fence_async_smem();
         tc_fence_before();
         __syncthreads();
+        if (tid == 0 && tma_out) {
+            tma_store_3d(&A.tm_out, sbase + Q_OST, 0, h, cs);
+            bulk_commit();
+        }
         clk.tick(3);
     }
     clk.flush(reinterpret_cast<unsigned long long *>(a.status) + 8);
@@ -721,6 +791,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_scan_kernel(const __gri
         }
     }
     if (tid == 0) {
+        bulk_wait_all();                                 // output tiles written
         // after a failure, let what is still in flight land before the CTA exits
         if (pend_a) mbar_wait_bounded(mb_a, aph, kWaitLimit);
         if (pend_x0) mbar_wait_bounded(mb_x0, xph0, kWaitLimit);
@@ -848,6 +919,9 @@ cudaError_t launch_prefill_tc_split(const PrefillArgs &p, const float *conv_w, f
     ScanArgs S{};
     if (p.gate && p.T > 0 &&
         (e = make_row_map(&S.tm_gate, p.gate, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.T, p.H)) != cudaSuccess)
+        return e;
+    if (p.out_bf16 && p.T > 0 &&
+        (e = make_row_map(&S.tm_out, p.out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.T, p.H)) != cudaSuccess)
         return e;
     S.box_rows = box_rows;
     S.p = p;

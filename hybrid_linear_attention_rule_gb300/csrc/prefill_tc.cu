@@ -182,7 +182,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
         sphase ^= 1u;
         __syncthreads();
         if (*sflag) { failed = true; break; }
-        prep_chunk(sm, a, cs, Lc, h, W, sLogf, sFcol);
+        prep_chunk<PlanFused>(sm, a, cs, Lc, h, W, sLogf, sFcol);
         PHASE(0);
         // pre-conv rows 61..63 of this chunk are the conv history of the next one
         if (W > 0 && cs + kC < te)
@@ -192,12 +192,12 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
                 sHist[e] = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(sm + st + (kC - 3 + r) * (kD * 2) + c * 2));
             }
         // ================= MMA: [Kh; Qh] Kb^T  -> Akk | Aqk =================
-        if (tid == 0) issue_mma_a(sbase, tbase + kColA, mbar_a);
+        if (tid == 0) issue_mma_a<PlanFused>(sbase, tbase + kColA, mbar_a);
         if (!mma_wait()) { failed = true; break; }
         PHASE(1);
-        extract_a(sm, tl, kColA);
+        extract_a<PlanFused>(sm, tl, kColA);
         PHASE(2);
-        solve_tb(sm);
+        solve_tb<PlanFused>(sm);
         PHASE(3);
         // ================= MMA: U^T = v^T Tb^T =================
         if (tid == 0) {

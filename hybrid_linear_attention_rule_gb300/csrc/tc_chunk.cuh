@@ -72,6 +72,29 @@ constexpr uint32_t kSmemUsed = OFF_MISC + 64;
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;     // + alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory plan exceeds the per-CTA limit");
 
+// The stage functions take the offsets of their tiles from a plan.  The single-pass kernel uses
+// the plan above (regions A and B reused by its state chain).  The chunk-prep kernel of the
+// two-pass path uses one in which the next chunk's q, k, v rows land during this chunk's MMA A
+// and its g rows during MMA U/W: region R holds the staged g rows, then Kb (until MMA A), then
+// the solve's scratch.
+struct PlanFused {
+    static constexpr uint32_t GST = OFF_GST, QST = OFF_QST, KST = OFF_KST, VST = OFF_VST;
+    static constexpr uint32_t V_HI = OFF_V_HI, V_LO = OFF_V_LO, KB_HI = OFF_KB_HI, KB_LO = OFF_KB_LO;
+    static constexpr uint32_t SCR_A = OFF_SCR_A, SCR_T = OFF_SCR_T, AQK_HI = OFF_AQK_HI, AQK_LO = OFF_AQK_LO;
+    static constexpr uint32_t TB_HI = OFF_TB_HI, TB_LO = OFF_TB_LO, SCAN = OFF_SCAN;
+};
+struct PlanPrep {
+    static constexpr uint32_t V_HI = 65536, V_LO = 81920;                  // v rows      (prep_v .. MMA U)
+    static constexpr uint32_t QST = 98304, KST = 114688, VST = 131072;     // staged rows (MMA A .. next prep)
+    static constexpr uint32_t GST = 147456;                                // R: staged g (solve .. next prep_qk)
+    static constexpr uint32_t KB_HI = 147456, KB_LO = 163840;              // R: Kb       (prep_qk .. MMA A)
+    static constexpr uint32_t SCR_A = 147456, SCR_T = 163840;              // R: scratch  (extract .. solve)
+    static constexpr uint32_t AQK_HI = 180224, AQK_LO = 188416;            // Aqk^T       (extract .. its store)
+    static constexpr uint32_t SCAN = AQK_HI;                               // g partial sums (prep_qk)
+    static constexpr uint32_t TB_HI = 196608, TB_LO = 204800;              // Tb          (solve .. MMA U/W)
+};
+static_assert(PlanPrep::TB_LO + 8192 <= OFF_CONVW, "prep plan runs into the small arrays");
+
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
     __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
     return *reinterpret_cast<uint32_t *>(&v);
@@ -114,12 +137,86 @@ __device__ __forceinline__ void tile64_put16(uint8_t *sm, uint32_t off_hi, uint3
 }
 
 // ---- stage 1: staged rows + conv history -> operand tiles ----
-// Reads GST, QST, KST, VST (the chunk's g, q, k, v rows) and HIST (the three
-// pre-conv q, k, v rows before the chunk); writes X/XL ([Kh; Qh] rows), KB, V_HI/LO,
-// BETA, G0, GL, REF, and FCOL = exp(LOGF + r) when fcol is given.  Thread (warp, lane)
-// owns tokens 4*warp .. +3 and channels 4*lane .. +3.
-__device__ __forceinline__ void prep_chunk(uint8_t *sm, const PrefillArgs &a, int cs, int Lc, int h, int W,
-                                           const float *logf, float *fcol) {
+// Thread (warp, lane) owns tokens 4*warp .. +3 and channels 4*lane .. +3 of the chunk.
+
+// Conv (+SiLU) and, for q and k with the L2 norm on, the norm of tensor `which` (0 q, 1 k, 2 v)
+// for this thread's 4 tokens x 4 channels: reads the staged rows at `st` and the pre-conv rows
+// before the chunk in HIST (tensor-major, three rows each).
+__device__ __forceinline__ void conv_rows(const uint8_t *sm, const PrefillArgs &a, int which, uint32_t st,
+                                          int Lc, int W, float (&y)[kTok][4]) {
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int i0 = warp * kTok, c0 = lane * 4;
+    const float *sConvW = reinterpret_cast<const float *>(sm + OFF_CONVW);
+    const float *sHist = reinterpret_cast<const float *>(sm + OFF_HIST);
+    float x[kTok + 3][4];
+#pragma unroll
+    for (int t = 0; t < kTok + 3; ++t) {
+        const int i = i0 - 3 + t;               // chunk-local token
+        if (i < 0) {
+            const float4 hv = *reinterpret_cast<const float4 *>(sHist + (which * 3 + 3 + i) * 128 + c0);
+            x[t][0] = hv.x; x[t][1] = hv.y; x[t][2] = hv.z; x[t][3] = hv.w;
+        } else if (i < Lc) {
+            const uint2 raw = *reinterpret_cast<const uint2 *>(sm + st + i * (kD * 2) + c0 * 2);
+            const __nv_bfloat162 p0 = *reinterpret_cast<const __nv_bfloat162 *>(&raw.x);
+            const __nv_bfloat162 p1 = *reinterpret_cast<const __nv_bfloat162 *>(&raw.y);
+            x[t][0] = __low2float(p0); x[t][1] = __high2float(p0);
+            x[t][2] = __low2float(p1); x[t][3] = __high2float(p1);
+        } else {
+            x[t][0] = x[t][1] = x[t][2] = x[t][3] = 0.f;
+        }
+    }
+    if (W > 0) {
+        float4 w4[4];
+#pragma unroll
+        for (int t = 0; t < 4; ++t) w4[t] = *reinterpret_cast<const float4 *>(sConvW + t * 384 + which * kD + c0);
+#pragma unroll
+        for (int ii = 0; ii < kTok; ++ii) {
+            float acc[4];
+            acc[0] = w4[0].x * x[ii][0]; acc[1] = w4[0].y * x[ii][1];
+            acc[2] = w4[0].z * x[ii][2]; acc[3] = w4[0].w * x[ii][3];
+#pragma unroll
+            for (int t = 1; t < 4; ++t) {
+                acc[0] = fmaf(w4[t].x, x[ii + t][0], acc[0]); acc[1] = fmaf(w4[t].y, x[ii + t][1], acc[1]);
+                acc[2] = fmaf(w4[t].z, x[ii + t][2], acc[2]); acc[3] = fmaf(w4[t].w, x[ii + t][3], acc[3]);
+            }
+#pragma unroll
+            for (int m = 0; m < 4; ++m) y[ii][m] = (i0 + ii < Lc) ? silu_fast(acc[m]) : 0.f;
+        }
+    } else {
+#pragma unroll
+        for (int ii = 0; ii < kTok; ++ii)
+#pragma unroll
+            for (int m = 0; m < 4; ++m) y[ii][m] = x[ii + 3][m];
+    }
+    if (a.l2 && which < 2) {
+#pragma unroll
+        for (int ii = 0; ii < kTok; ++ii) {
+            float ss = y[ii][0] * y[ii][0] + y[ii][1] * y[ii][1] + y[ii][2] * y[ii][2] + y[ii][3] * y[ii][3];
+            ss = warp_sum(ss);
+            const float inv = rsqrtf(ss + K3KDA_L2_EPS);
+#pragma unroll
+            for (int m = 0; m < 4; ++m) y[ii][m] *= inv;
+        }
+    }
+}
+
+// One token's 4 channels, split, into row `row` of a K=128 tile (hi and lo tiles).
+__device__ __forceinline__ void put_row_split(uint8_t *sm, uint32_t off_hi, uint32_t off_lo, uint32_t rows, int row,
+                                              int c0, const float (&v)[4]) {
+    float hv[4], lv[4];
+#pragma unroll
+    for (int m = 0; m < 4; ++m) split_bf16(v[m], hv[m], lv[m]);
+    const uint32_t o = kmaj128(rows, row, c0);
+    *reinterpret_cast<uint2 *>(sm + off_hi + o) = make_uint2(pack_bf16(hv[0], hv[1]), pack_bf16(hv[2], hv[3]));
+    *reinterpret_cast<uint2 *>(sm + off_lo + o) = make_uint2(pack_bf16(lv[0], lv[1]), pack_bf16(lv[2], lv[3]));
+}
+
+// q and k: reads GST, QST, KST and the q, k rows of HIST; writes X/XL ([Kh; Qh] rows), KB, BETA,
+// G0, GL, REF, and FCOL = exp(LOGF + r) when fcol is given.  Reads of GST all precede the first
+// barrier, so GST may share its region with KB.
+template <class P>
+__device__ __forceinline__ void prep_qk(uint8_t *sm, const PrefillArgs &a, int cs, int Lc, int h, int W,
+                                        const float *logf, float *fcol) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int H = a.H;
     const int i0 = warp * kTok, c0 = lane * 4;
@@ -127,9 +224,7 @@ __device__ __forceinline__ void prep_chunk(uint8_t *sm, const PrefillArgs &a, in
     float *sRef = reinterpret_cast<float *>(sm + OFF_REF);
     float *sGL = reinterpret_cast<float *>(sm + OFF_GL);
     float *sG0 = reinterpret_cast<float *>(sm + OFF_G0);
-    float *sScan = reinterpret_cast<float *>(sm + OFF_SCAN);
-    const float *sConvW = reinterpret_cast<const float *>(sm + OFF_CONVW);
-    const float *sHist = reinterpret_cast<const float *>(sm + OFF_HIST);
+    float *sScan = reinterpret_cast<float *>(sm + P::SCAN);
     float G[kTok][4];
     {
         float run[4] = {0.f, 0.f, 0.f, 0.f};
@@ -137,7 +232,7 @@ __device__ __forceinline__ void prep_chunk(uint8_t *sm, const PrefillArgs &a, in
         for (int ii = 0; ii < kTok; ++ii) {
             const int i = i0 + ii;
             float4 gv = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (i < Lc) gv = *reinterpret_cast<const float4 *>(sm + OFF_GST + i * (kD * 4) + c0 * 4);
+            if (i < Lc) gv = *reinterpret_cast<const float4 *>(sm + P::GST + i * (kD * 4) + c0 * 4);
             run[0] += gv.x; run[1] += gv.y; run[2] += gv.z; run[3] += gv.w;
 #pragma unroll
             for (int m = 0; m < 4; ++m) G[ii][m] = run[m];
@@ -182,107 +277,60 @@ __device__ __forceinline__ void prep_chunk(uint8_t *sm, const PrefillArgs &a, in
                 Eb[ii][m] = __expf(-x);
             }
     }
-    // conv (+SiLU) and norm of q (which 0), k (1) or v (2) for this thread's 4 tokens x 4 channels
-    auto finish = [&](int which, float (&y)[kTok][4]) {
-        const uint32_t st = which == 0 ? OFF_QST : (which == 1 ? OFF_KST : OFF_VST);
-        float x[kTok + 3][4];
+    float y[kTok][4];
+    // q -> Qh = q E  (rows 64..127 of X / XL)
+    conv_rows(sm, a, 0, P::QST, Lc, W, y);
 #pragma unroll
-        for (int t = 0; t < kTok + 3; ++t) {
-            const int i = i0 - 3 + t;               // chunk-local token
-            if (i < 0) {
-                const float4 hv = *reinterpret_cast<const float4 *>(sHist + (which * 3 + 3 + i) * 128 + c0);
-                x[t][0] = hv.x; x[t][1] = hv.y; x[t][2] = hv.z; x[t][3] = hv.w;
-            } else if (i < Lc) {
-                const uint2 raw = *reinterpret_cast<const uint2 *>(sm + st + i * (kD * 2) + c0 * 2);
-                const __nv_bfloat162 p0 = *reinterpret_cast<const __nv_bfloat162 *>(&raw.x);
-                const __nv_bfloat162 p1 = *reinterpret_cast<const __nv_bfloat162 *>(&raw.y);
-                x[t][0] = __low2float(p0); x[t][1] = __high2float(p0);
-                x[t][2] = __low2float(p1); x[t][3] = __high2float(p1);
-            } else {
-                x[t][0] = x[t][1] = x[t][2] = x[t][3] = 0.f;
-            }
-        }
-        if (W > 0) {
-            float4 w4[4];
+    for (int ii = 0; ii < kTok; ++ii) {
+        float t4[4];
 #pragma unroll
-            for (int t = 0; t < 4; ++t)
-                w4[t] = *reinterpret_cast<const float4 *>(sConvW + t * 384 + which * kD + c0);
+        for (int m = 0; m < 4; ++m) t4[m] = y[ii][m] * E[ii][m];
+        put_row_split(sm, OFF_X, OFF_XL, 128, 64 + i0 + ii, c0, t4);
+    }
+    // k -> Kh = k E (rows 0..63 of X / XL), Kb = k / E (rows; the state update reads them MN-major)
+    conv_rows(sm, a, 1, P::KST, Lc, W, y);
 #pragma unroll
-            for (int ii = 0; ii < kTok; ++ii) {
-                float acc[4];
-                acc[0] = w4[0].x * x[ii][0]; acc[1] = w4[0].y * x[ii][1];
-                acc[2] = w4[0].z * x[ii][2]; acc[3] = w4[0].w * x[ii][3];
+    for (int ii = 0; ii < kTok; ++ii) {
+        float t4[4], u4[4];
 #pragma unroll
-                for (int t = 1; t < 4; ++t) {
-                    acc[0] = fmaf(w4[t].x, x[ii + t][0], acc[0]); acc[1] = fmaf(w4[t].y, x[ii + t][1], acc[1]);
-                    acc[2] = fmaf(w4[t].z, x[ii + t][2], acc[2]); acc[3] = fmaf(w4[t].w, x[ii + t][3], acc[3]);
-                }
-#pragma unroll
-                for (int m = 0; m < 4; ++m) y[ii][m] = (i0 + ii < Lc) ? silu_fast(acc[m]) : 0.f;
-            }
-        } else {
-#pragma unroll
-            for (int ii = 0; ii < kTok; ++ii)
-#pragma unroll
-                for (int m = 0; m < 4; ++m) y[ii][m] = x[ii + 3][m];
-        }
-        if (a.l2 && which < 2) {
-#pragma unroll
-            for (int ii = 0; ii < kTok; ++ii) {
-                float ss = y[ii][0] * y[ii][0] + y[ii][1] * y[ii][1] + y[ii][2] * y[ii][2] + y[ii][3] * y[ii][3];
-                ss = warp_sum(ss);
-                const float inv = rsqrtf(ss + K3KDA_L2_EPS);
-#pragma unroll
-                for (int m = 0; m < 4; ++m) y[ii][m] *= inv;
-            }
-        }
-    };
-    // one token's 4 channels, split, into row `row` of a K=128 tile (hi and lo tiles)
-    auto put_row_split = [&](uint32_t off_hi, uint32_t off_lo, uint32_t rows, int row, const float (&v)[4]) {
-        float hv[4], lv[4];
-#pragma unroll
-        for (int m = 0; m < 4; ++m) split_bf16(v[m], hv[m], lv[m]);
-        const uint32_t o = kmaj128(rows, row, c0);
-        *reinterpret_cast<uint2 *>(sm + off_hi + o) = make_uint2(pack_bf16(hv[0], hv[1]), pack_bf16(hv[2], hv[3]));
-        *reinterpret_cast<uint2 *>(sm + off_lo + o) = make_uint2(pack_bf16(lv[0], lv[1]), pack_bf16(lv[2], lv[3]));
-    };
-    {
-        float y[kTok][4];
-        // q -> Qh = q E  (rows 64..127 of X / XL)
-        finish(0, y);
-#pragma unroll
-        for (int ii = 0; ii < kTok; ++ii) {
-            float t4[4];
-#pragma unroll
-            for (int m = 0; m < 4; ++m) t4[m] = y[ii][m] * E[ii][m];
-            put_row_split(OFF_X, OFF_XL, 128, 64 + i0 + ii, t4);
-        }
-        // k -> Kh = k E (rows 0..63 of X / XL), Kb = k / E (rows; the state update reads them MN-major)
-        finish(1, y);
-#pragma unroll
-        for (int ii = 0; ii < kTok; ++ii) {
-            float t4[4], u4[4];
-#pragma unroll
-            for (int m = 0; m < 4; ++m) { t4[m] = y[ii][m] * E[ii][m]; u4[m] = y[ii][m] * Eb[ii][m]; }
-            put_row_split(OFF_X, OFF_XL, 128, i0 + ii, t4);
-            put_row_split(OFF_KB_HI, OFF_KB_LO, 64, i0 + ii, u4);
-        }
-        // v -> v rows (hi/lo; lo is zero unless the conv made v inexact), read MN-major by MMA U
-        finish(2, y);
-#pragma unroll
-        for (int ii = 0; ii < kTok; ++ii) put_row_split(OFF_V_HI, OFF_V_LO, 64, i0 + ii, y[ii]);
+        for (int m = 0; m < 4; ++m) { t4[m] = y[ii][m] * E[ii][m]; u4[m] = y[ii][m] * Eb[ii][m]; }
+        put_row_split(sm, OFF_X, OFF_XL, 128, i0 + ii, c0, t4);
+        put_row_split(sm, P::KB_HI, P::KB_LO, 64, i0 + ii, c0, u4);
     }
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
 }
 
+// v: reads VST and the v rows of HIST; writes V_HI/LO (v rows, hi/lo; lo is zero unless the conv
+// made v inexact), read MN-major by MMA U.
+template <class P>
+__device__ __forceinline__ void prep_v(uint8_t *sm, const PrefillArgs &a, int Lc, int W) {
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int i0 = warp * kTok, c0 = lane * 4;
+    float y[kTok][4];
+    conv_rows(sm, a, 2, P::VST, Lc, W, y);
+#pragma unroll
+    for (int ii = 0; ii < kTok; ++ii) put_row_split(sm, P::V_HI, P::V_LO, 64, i0 + ii, c0, y[ii]);
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+}
+
+template <class P>
+__device__ __forceinline__ void prep_chunk(uint8_t *sm, const PrefillArgs &a, int cs, int Lc, int h, int W,
+                                           const float *logf, float *fcol) {
+    prep_qk<P>(sm, a, cs, Lc, h, W, logf, fcol);
+    prep_v<P>(sm, a, Lc, W);
+}
+
 // ---- stage 2 (one thread): [Kh; Qh] Kb^T -> TMEM columns [col, col + 64), commit to mbar ----
+template <class P>
 __device__ __forceinline__ void issue_mma_a(uint32_t sbase, uint32_t tmem_col_addr, uint32_t mbar) {
     tc_fence_after();
     const uint32_t id = idesc_bf16_f32(128, 64);
     const uint64_t dX = sdesc_kmajor_sw128(sbase + OFF_X), dXL = sdesc_kmajor_sw128(sbase + OFF_XL);
-    const uint64_t dKh = sdesc_kmajor_sw128(sbase + OFF_KB_HI), dKl = sdesc_kmajor_sw128(sbase + OFF_KB_LO);
+    const uint64_t dKh = sdesc_kmajor_sw128(sbase + P::KB_HI), dKl = sdesc_kmajor_sw128(sbase + P::KB_LO);
 #pragma unroll
     for (int sp = 0; sp < 3; ++sp)
 #pragma unroll
@@ -294,11 +342,12 @@ __device__ __forceinline__ void issue_mma_a(uint32_t sbase, uint32_t tmem_col_ad
 
 // ---- stage 3: Akk (times beta, strictly lower) -> fp32 scratch A, Aqk (lower) -> split tile (transposed) ----
 // tl is this warp's TMEM lane base, col the first column of the MMA A result.
+template <class P>
 __device__ __forceinline__ void extract_a(uint8_t *sm, uint32_t tl, uint32_t col) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int quarter = warp >> 2, lrow = 32 * (warp & 3);
     const float *sBeta = reinterpret_cast<const float *>(sm + OFF_BETA);
-    float *scrA = reinterpret_cast<float *>(sm + OFF_SCR_A);
+    float *scrA = reinterpret_cast<float *>(sm + P::SCR_A);
     // ================= Akk -> fp32 scratch, Aqk -> split tile =================
     {
         const int colbase = quarter * 16;
@@ -324,8 +373,8 @@ __device__ __forceinline__ void extract_a(uint8_t *sm, uint32_t tl, uint32_t col
                 float hv, lv;
                 split_bf16(ip > i ? 0.f : __uint_as_float(r0[u]), hv, lv);
                 const uint32_t o = sw128_offset(ip, i);
-                *reinterpret_cast<__nv_bfloat16 *>(sm + OFF_AQK_HI + o) = __float2bfloat16_rn(hv);
-                *reinterpret_cast<__nv_bfloat16 *>(sm + OFF_AQK_LO + o) = __float2bfloat16_rn(lv);
+                *reinterpret_cast<__nv_bfloat16 *>(sm + P::AQK_HI + o) = __float2bfloat16_rn(hv);
+                *reinterpret_cast<__nv_bfloat16 *>(sm + P::AQK_LO + o) = __float2bfloat16_rn(lv);
             }
         }
     }
@@ -333,11 +382,12 @@ __device__ __forceinline__ void extract_a(uint8_t *sm, uint32_t tl, uint32_t col
 }
 
 // ---- stage 4: T = (I + Akk)^-1 (fp32, block recursive), Tb = T diag(beta) -> split tile ----
+template <class P>
 __device__ __forceinline__ void solve_tb(uint8_t *sm) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const float *sBeta = reinterpret_cast<const float *>(sm + OFF_BETA);
-    const float *scrA = reinterpret_cast<const float *>(sm + OFF_SCR_A);
-    float *scrT = reinterpret_cast<float *>(sm + OFF_SCR_T);
+    const float *scrA = reinterpret_cast<const float *>(sm + P::SCR_A);
+    float *scrT = reinterpret_cast<float *>(sm + P::SCR_T);
     // ================= T = (I + Akk)^-1 in fp32, Tb = T diag(beta) (hi/lo) =================
     // diagonal 16x16 blocks by substitution (one column per thread); the upper blocks
     // (0,1) and (2,3) that the block products read are zeroed at the same time
@@ -438,8 +488,8 @@ __device__ __forceinline__ void solve_tb(uint8_t *sm) {
             lw[u >> 1] = pack_bf16(l0, l1);
         }
         const uint32_t o0 = sw128_offset(i, jq);
-        *reinterpret_cast<uint4 *>(sm + OFF_TB_HI + o0) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-        *reinterpret_cast<uint4 *>(sm + OFF_TB_LO + o0) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+        *reinterpret_cast<uint4 *>(sm + P::TB_HI + o0) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+        *reinterpret_cast<uint4 *>(sm + P::TB_LO + o0) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
     }
     fence_async_smem();
     tc_fence_before();

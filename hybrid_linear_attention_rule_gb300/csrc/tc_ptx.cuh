@@ -194,6 +194,25 @@ __device__ __forceinline__ void bulk_s2g(void *dst, uint32_t src_smem, uint32_t 
                  : "memory");
 }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Prefetch [src, src + bytes) from global memory into L2 (src 16-byte aligned, bytes a multiple
+// of 16); nothing signals completion, a later copy of the same bytes just finds them in L2.
+__device__ __forceinline__ void prefetch_l2(const void *src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+// Prefetch the 3-D map's box at {x, y, z} into L2.
+__device__ __forceinline__ void tma_prefetch_3d(const void *tmap, int x, int y, int z) {
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];"
+                 ::"l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(z)
+                 : "memory");
+}
+// TMA tensor store shared -> global of the 3-D map's box at {x, y, z}, in the issuing thread's
+// bulk-async group; box rows outside the tensor are not written.  The writers of the source
+// must have fenced it to the async proxy (fence.proxy.async) first.
+__device__ __forceinline__ void tma_store_3d(const void *tmap, uint32_t src_smem, int x, int y, int z) {
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];"
+                 ::"l"(reinterpret_cast<uint64_t>(tmap)), "r"(src_smem), "r"(x), "r"(y), "r"(z)
+                 : "memory");
+}
 // Wait until every committed bulk group of this thread has finished reading shared memory.
 __device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 // Wait until every committed bulk group of this thread has completed (writes performed).

@@ -68,6 +68,22 @@ def test_prefill_bf16_output_store():
 
 
 @PATHS
+def test_prefill_bf16_output_varlen_ragged(path):
+    """bf16 outputs of whole chunks leave through a TMA tile store; a ragged chunk at a sequence
+    end inside the batch is stored row by row (a tile would cross into the next sequence), a
+    ragged chunk at the end of the batch by a tile clipped at the tensor's end."""
+    c = KI.prefill_case("bf16_out_varlen", [70, 3, 190, 64, 1, 129], 2, 128, 128, 64, "bf16", seed=30,
+                        s0_std=0.02, gate=True, conv_width=4, conv_state=True)
+    _check(c, out_dtype=torch.bfloat16, path=path)
+
+
+def test_prefill_bf16_output_shorter_than_one_chunk_varlen():
+    """T < 64: the tile box is T rows; the second sequence's tile starts inside it and is clipped."""
+    c = KI.prefill_case("bf16_out_short", [10, 27], 2, 128, 128, 64, "bf16", seed=31, s0_std=0.02, gate=True)
+    _check(c, out_dtype=torch.bfloat16)
+
+
+@PATHS
 def test_prefill_without_l2norm(path):
     c = KI.chunked_prefill(seed=3, T=200, H=2)
     c.use_qk_l2norm = False
@@ -121,13 +137,14 @@ def test_fused_mixer_varlen_with_conv_state(path):
     _check(c, path=path)
 
 
-def test_two_pass_segmented_varlen_with_states():
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
+def test_two_pass_segmented_varlen_with_states(out_dtype):
     """Few (sequence, head) pairs and >= 128 chunks: the two passes run as a pipeline of chunk
     segments, the scan handing its state between segment launches; the middle sequence (chunks
     65 .. 130) crosses the segment boundary at chunk 67."""
     c = KI.prefill_case("segmented_varlen", [4100, 4200, 70], 2, 128, 128, 64, "bf16", seed=40, s0_std=0.02,
                         gate=True, conv_width=4, conv_state=True)
-    _check(c)
+    _check(c, out_dtype=out_dtype)
 
 
 def test_two_pass_segmented_single_long_sequence():
