@@ -41,7 +41,7 @@ using namespace tcc;
 
 // ---- one chunk record (byte offsets; identical to the scan kernel's smem layout) ----
 constexpr uint32_t REC_X = 0;            // [W rows 0-63; Qh rows 64-127] x 128 K, split: hi 32 KB, lo 32 KB
-constexpr uint32_t REC_B = 65536;        // MN-major B of MMA O/S, per split half [Aqk^T 8 KB | Kb rows 16 KB]: hi, lo
+constexpr uint32_t REC_B = 65536;        // MN-major B of MMA O/S: 8 KB N-blocks Aqk^T hi, lo, then Kb hi, lo per K atom
 constexpr uint32_t REC_U = 114688;       // U^T fp32 as 16 blocks of 4 tokens: [tok / 4][128 dv][4 tok]
 constexpr uint32_t REC_VEC = 147456;     // r[128], G_last[128] fp32
 constexpr uint32_t REC_BYTES = 148480;
@@ -111,8 +111,9 @@ struct PrepArgs {
     int q_lo, q_hi;           // global chunk range of this launch (items q * H + h)
 };
 
-constexpr uint32_t kPrepTmemCols = 256;
-constexpr uint32_t kColWp = 64, kColUp = 128;    // W^T and U^T results ([0, 64): Akk | Aqk)
+constexpr uint32_t kPrepTmemCols = 512;
+// MMA A result in [0, 128) (two halves summed: hi*hi + lo*hi | hi*lo), U^T and W^T likewise
+constexpr uint32_t kColUp = 128, kColWp = 256;
 
 __global__ void __launch_bounds__(kThreads, 1) kda_chunk_prep_kernel(const __grid_constant__ PrepArgs A) {
     extern __shared__ uint8_t smraw[];
@@ -123,6 +124,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_prep_kernel(const __gri
     const uint32_t sbase = smem_u32(sm);
     float *sConvW = reinterpret_cast<float *>(sm + OFF_CONVW);
     float *sHist = reinterpret_cast<float *>(sm + OFF_HIST);
+    float *sBeta = reinterpret_cast<float *>(sm + OFF_BETA);
     uint64_t *mbar = reinterpret_cast<uint64_t *>(sm + OFF_MISC);
     uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + OFF_MISC + 24);
     volatile uint32_t *sflag = reinterpret_cast<volatile uint32_t *>(sm + OFF_MISC + 28);
@@ -170,7 +172,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_prep_kernel(const __gri
     const long long total = (long long)nq * H;
     const int m_lo = (int)(total * blockIdx.x / gridDim.x);
     const int m_hi = (int)(total * (blockIdx.x + 1) / gridDim.x);
-    struct Item { int h, qc, n, tb, te, cs; };
+    struct Item { int h, qc, n, tb, te, cs, qend; };   // qend: one past the sequence's last chunk
     auto locate = [&](int m) {
         Item x;
         x.h = m / nq;
@@ -183,7 +185,19 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_prep_kernel(const __gri
         x.n = lo;
         seq_bounds(a.cu, x.n, a.T, x.tb, x.te);
         x.cs = x.tb + (x.qc - A.chunk_off[x.n]) * kC;
+        x.qend = A.chunk_off[x.n + 1];
         return x;
+    };
+    // item m + 1 after item x = item m: the next chunk of the same sequence and head without
+    // touching global memory, else a fresh lookup
+    auto advance = [&](const Item &x, int m) {
+        if ((m + 1) % nq != 0 && x.qc + 1 < x.qend) {
+            Item y = x;
+            y.qc += 1;
+            y.cs += kC;
+            return y;
+        }
+        return locate(m + 1);
     };
     auto rec_of = [&](const Item &x) { return A.rec + ((size_t)(x.qc - A.q_lo) * H + x.h) * REC_BYTES; };
     // conv weights of the item's head and its conv history (pre-conv q, k, v rows of tokens
@@ -244,25 +258,26 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_prep_kernel(const __gri
     };
 
     PhaseClock clk;   // phases: 0 staging wait, 1 prep q/k, 2 prep v (MMA A), 3 history + MMA A wait, 4 extract, 5 solve, 6 MMA U/W, 7 records out
+    Item x, y;                                           // this item and the next
     if (m_lo < m_hi) {
-        const Item x0 = locate(m_lo);
+        x = locate(m_lo);
+        y = m_lo + 1 < m_hi ? advance(x, m_lo) : x;
         if (tid == 0) {
-            stage_qkv(x0);
-            stage_g(x0);
-            if (m_lo + 1 < m_hi) prefetch_rows(locate(m_lo + 1));
+            stage_qkv(x);
+            stage_g(x);
+            if (m_lo + 1 < m_hi) prefetch_rows(y);
         }
-        load_history(x0);
+        load_history(x);
+        if (tid < kC) sBeta[tid] = tid < x.te - x.cs ? a.beta[(size_t)(x.cs + tid) * H + x.h] : 0.f;
     }
-    for (int m = m_lo; m < m_hi; ++m) {
-        const Item x = locate(m);
+    for (int m = m_lo; m < m_hi; ++m, x = y, y = m + 1 < m_hi ? advance(y, m) : y) {
         const bool has_next = m + 1 < m_hi;
-        const Item y = has_next ? locate(m + 1) : x;
         const bool cont = has_next && y.h == x.h && y.qc == x.qc + 1 && y.cs > y.tb;
         const int Lc = min(kC, x.te - x.cs);
         uint8_t *rec = rec_of(x);
         if (tid == 0) {
-            if (m + 2 < m_hi) prefetch_rows(locate(m + 2));
-            bulk_wait_read_all();                        // the previous records have left shared memory
+            if (m + 2 < m_hi) prefetch_rows(advance(y, m + 1));
+            bulk_wait_read_but_last();                   // all but W have left shared memory (prep_qk waits for W)
             wait_on(mbar_s, sph, pend_s);
         }
         __syncthreads();
@@ -274,14 +289,17 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_prep_kernel(const __gri
         if (tid == 0) {
             issue_mma_a<PlanPrep>(sbase, tbase + kColA, mbar_a);
             pend_a = true;
-            // Qh (rows 64..127 of each K atom, hi and lo), Kb and r, G_last are final: out now
+            // Qh (rows 64..127 of each K atom, hi and lo) and Kb are final: out now.  The stacked Kb
+            // tile (per K atom the hi rows, then the lo rows) is the record's layout as it stands
 #pragma unroll
             for (int p = 0; p < 4; ++p)
                 bulk_s2g(rec + REC_X + p * 16384 + 8192, sbase + OFF_X + p * 16384 + 8192, 8192);
-            bulk_s2g(rec + REC_B + 8192, sbase + PlanPrep::KB_HI, 16384);
-            bulk_s2g(rec + REC_B + 32768, sbase + PlanPrep::KB_LO, 16384);
-            bulk_s2g(rec + REC_VEC, sbase + OFF_REF, 1024);     // r, G_last
+            bulk_s2g(rec + REC_B + 16384, sbase + PlanPrep::KB_HI, 32768);
             bulk_commit();
+        }
+        if (tid < kD) {                                  // r, G_last
+            reinterpret_cast<float *>(rec + REC_VEC)[tid] = reinterpret_cast<const float *>(sm + OFF_REF)[tid];
+            reinterpret_cast<float *>(rec + REC_VEC)[kD + tid] = reinterpret_cast<const float *>(sm + OFF_GL)[tid];
         }
         prep_v<PlanPrep>(sm, a, Lc, W);                  // overlaps MMA A
         clk.tick(2);
@@ -298,36 +316,41 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_prep_kernel(const __gri
         extract_a<PlanPrep>(sm, tl, kColA);
         clk.tick(4);
         solve_tb<PlanPrep>(sm);
+        float beta_next = 0.f;                           // the next item's beta, written after MMA U/W
+        if (has_next && tid < kC && tid < y.te - y.cs) beta_next = a.beta[(size_t)(y.cs + tid) * H + y.h];
         if (tid == 0) {
-            bulk_s2g(rec + REC_B, sbase + PlanPrep::AQK_HI, 8192);
-            bulk_s2g(rec + REC_B + 24576, sbase + PlanPrep::AQK_LO, 8192);
+            static_assert(PlanPrep::AQK_LO == PlanPrep::AQK_HI + 8192, "Aqk^T hi and lo must be adjacent");
+            bulk_s2g(rec + REC_B, sbase + PlanPrep::AQK_HI, 16384);
             bulk_commit();
             if (has_next) stage_g(y);                    // region R is free
         }
         clk.tick(5);
 
-        // ---- MMA: U^T = v^T Tb^T and W^T = Kh^T Tb^T (Kh rows 0-63 of X read MN-major) ----
+        // ---- MMA: U^T = v^T Tb^T and W^T = Kh^T Tb^T (Kh rows 0-63 of X read MN-major).  Tb_hi and
+        // Tb_lo are adjacent 64-row tiles, one N = 128 operand: x_hi [Tb_hi; Tb_lo]^T, then x_lo Tb_hi^T
+        // into the first 64 columns; the result is the sum of the two halves ----
         if (tid == 0) {
             tc_fence_after();
-            const uint32_t id = idesc_bf16_f32(128, 64, false, /*a_mn=*/true);
+            const uint32_t id128 = idesc_bf16_f32(128, 128, false, /*a_mn=*/true),
+                           id64 = idesc_bf16_f32(128, 64, false, /*a_mn=*/true);
             const uint64_t dVh = sdesc_mnmajor_sw128(sbase + PlanPrep::V_HI, 8192),
                            dVl = sdesc_mnmajor_sw128(sbase + PlanPrep::V_LO, 8192);
             const uint64_t dKh = sdesc_mnmajor_sw128(sbase + OFF_X, 16384), dKl = sdesc_mnmajor_sw128(sbase + OFF_XL, 16384);
-            const uint64_t dTh = sdesc_kmajor_sw128(sbase + PlanPrep::TB_HI), dTl = sdesc_kmajor_sw128(sbase + PlanPrep::TB_LO);
-            const int nsplit = W > 0 ? 3 : 2;           // v is exact bf16 without a conv
+            const uint64_t dT = sdesc_kmajor_sw128(sbase + PlanPrep::TB_HI);
+            static_assert(PlanPrep::TB_LO == PlanPrep::TB_HI + 8192, "Tb hi and lo must form one 128-row tile");
 #pragma unroll
-            for (int sp = 0; sp < 3; ++sp)
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    if (sp < nsplit)
-                        mma_bf16(tbase + kColUp, dadd(sp == 2 ? dVl : dVh, kk * 2048), dadd(sp == 1 ? dTl : dTh, kk * 32),
-                                 id, (sp | kk) != 0);
-#pragma unroll
-            for (int sp = 0; sp < 3; ++sp)
+            for (int kk = 0; kk < 4; ++kk)
+                mma_bf16(tbase + kColUp, dadd(dVh, kk * 2048), dadd(dT, kk * 32), id128, kk != 0);
+            if (W > 0)                                   // v is exact bf16 without a conv
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
-                    mma_bf16(tbase + kColWp, dadd(sp == 2 ? dKl : dKh, kk * 2048), dadd(sp == 1 ? dTl : dTh, kk * 32),
-                             id, (sp | kk) != 0);
+                    mma_bf16(tbase + kColUp, dadd(dVl, kk * 2048), dadd(dT, kk * 32), id64, 1);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+                mma_bf16(tbase + kColWp, dadd(dKh, kk * 2048), dadd(dT, kk * 32), id128, kk != 0);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+                mma_bf16(tbase + kColWp, dadd(dKl, kk * 2048), dadd(dT, kk * 32), id64, 1);
             mma_commit(mbar_a);
             pend_a = true;
         }
@@ -337,15 +360,20 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_prep_kernel(const __gri
         // ---- U^T -> the record (straight from registers), W -> X/XL rows 0-63 -> the record ----
         {
             const int j = lrow + lane;                  // dv channel for U^T, dk channel for W^T
-            uint32_t r[16];
-            tmem_ld16(tl + kColUp + quarter * 16, r);
-            tmem_wait_ld();
+            uint32_t r[16], r2[16];
+            auto ld_sum = [&](uint32_t col) {
+                tmem_ld16(tl + col + quarter * 16, r);
+                tmem_ld16(tl + col + 64 + quarter * 16, r2);
+                tmem_wait_ld();
+#pragma unroll
+                for (int u = 0; u < 16; ++u) r[u] = __float_as_uint(__uint_as_float(r[u]) + __uint_as_float(r2[u]));
+            };
+            ld_sum(kColUp);
 #pragma unroll
             for (int t = 0; t < 4; ++t)
                 *reinterpret_cast<uint4 *>(rec + REC_U + u_off(j, quarter * 16 + 4 * t)) =
                     make_uint4(r[4 * t], r[4 * t + 1], r[4 * t + 2], r[4 * t + 3]);
-            tmem_ld16(tl + kColWp + quarter * 16, r);
-            tmem_wait_ld();
+            ld_sum(kColWp);
 #pragma unroll
             for (int u = 0; u < 16; ++u) {
                 float hv, lv;
@@ -355,6 +383,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_prep_kernel(const __gri
                 *reinterpret_cast<__nv_bfloat16 *>(sm + OFF_XL + o) = __float2bfloat16_rn(lv);
             }
         }
+        if (has_next && tid < kC) sBeta[tid] = beta_next;
         fence_async_smem();
         tc_fence_before();
         __syncthreads();
@@ -671,8 +700,9 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_scan_kernel(const __gri
         if (tid == 0 && wait_on(mb_k, kph, pend_k)) {
             tc_fence_after();
             const uint32_t id = idesc_bf16_f32(128, 192, false, false, /*b_mn=*/true);
-            const uint64_t dBh = sdesc_mnmajor_sw128(sbase + REC_B, 8192),
-                           dBl = sdesc_mnmajor_sw128(sbase + REC_B + 24576, 8192);
+            // N-blocks (Aqk^T, Kb atom 0, Kb atom 1) 16 KB apart, the lo blocks 8 KB after the hi ones
+            const uint64_t dBh = sdesc_mnmajor_sw128(sbase + REC_B, 16384),
+                           dBl = sdesc_mnmajor_sw128(sbase + REC_B + 8192, 16384);
 #pragma unroll
             for (int sp = 0; sp < 3; ++sp)
 #pragma unroll

@@ -82,6 +82,8 @@ struct PlanFused {
     static constexpr uint32_t V_HI = OFF_V_HI, V_LO = OFF_V_LO, KB_HI = OFF_KB_HI, KB_LO = OFF_KB_LO;
     static constexpr uint32_t SCR_A = OFF_SCR_A, SCR_T = OFF_SCR_T, AQK_HI = OFF_AQK_HI, AQK_LO = OFF_AQK_LO;
     static constexpr uint32_t TB_HI = OFF_TB_HI, TB_LO = OFF_TB_LO, SCAN = OFF_SCAN;
+    static constexpr bool KB_STACKED = false;    // Kb hi and lo as two 64-row tiles
+    static constexpr bool CALLER_STAGES = false; // prep_qk loads beta and owns every tile it writes
 };
 struct PlanPrep {
     static constexpr uint32_t V_HI = 65536, V_LO = 81920;                  // v rows      (prep_v .. MMA U)
@@ -92,6 +94,12 @@ struct PlanPrep {
     static constexpr uint32_t AQK_HI = 180224, AQK_LO = 188416;            // Aqk^T       (extract .. its store)
     static constexpr uint32_t SCAN = AQK_HI;                               // g partial sums (prep_qk)
     static constexpr uint32_t TB_HI = 196608, TB_LO = 204800;              // Tb          (solve .. MMA U/W)
+    // Kb hi in rows 0-63 and lo in rows 64-127 of one 128-row tile: MMA A then reads [Kb_hi; Kb_lo]
+    // as one N = 128 operand (hi*hi and hi*lo in one chain) and adds lo*hi with N = 64
+    static constexpr bool KB_STACKED = true;
+    // the caller writes BETA before prep_qk, and the bulk stores still reading X rows 0-63 (issued
+    // by thread 0) are waited for inside prep_qk, before those rows are rewritten
+    static constexpr bool CALLER_STAGES = true;
 };
 static_assert(PlanPrep::TB_LO + 8192 <= OFF_CONVW, "prep plan runs into the small arrays");
 
@@ -239,7 +247,7 @@ __device__ __forceinline__ void prep_qk(uint8_t *sm, const PrefillArgs &a, int c
         }
         *reinterpret_cast<float4 *>(sScan + warp * kD + c0) = make_float4(run[0], run[1], run[2], run[3]);
     }
-    if (tid < kC) sBeta[tid] = tid < Lc ? a.beta[(size_t)(cs + tid) * H + h] : 0.f;
+    if (!P::CALLER_STAGES && tid < kC) sBeta[tid] = tid < Lc ? a.beta[(size_t)(cs + tid) * H + h] : 0.f;
     __syncthreads();
     {
         float off[4] = {0.f, 0.f, 0.f, 0.f};
@@ -263,6 +271,7 @@ __device__ __forceinline__ void prep_qk(uint8_t *sm, const PrefillArgs &a, int c
         sRef[tid] = r;
         if (fcol) fcol[tid] = expf(logf[tid] + r);     // TMEM basis -> this chunk's S' = exp(r) S
     }
+    if (P::CALLER_STAGES && tid == 0) bulk_wait_read_all();   // X rows are rewritten below
     __syncthreads();
     float E[kTok][4], Eb[kTok][4];
     {
@@ -295,7 +304,8 @@ __device__ __forceinline__ void prep_qk(uint8_t *sm, const PrefillArgs &a, int c
 #pragma unroll
         for (int m = 0; m < 4; ++m) { t4[m] = y[ii][m] * E[ii][m]; u4[m] = y[ii][m] * Eb[ii][m]; }
         put_row_split(sm, OFF_X, OFF_XL, 128, i0 + ii, c0, t4);
-        put_row_split(sm, P::KB_HI, P::KB_LO, 64, i0 + ii, c0, u4);
+        if (P::KB_STACKED) put_row_split(sm, P::KB_HI, P::KB_HI + 8192, 128, i0 + ii, c0, u4);
+        else put_row_split(sm, P::KB_HI, P::KB_LO, 64, i0 + ii, c0, u4);
     }
     fence_async_smem();
     tc_fence_before();
@@ -324,19 +334,34 @@ __device__ __forceinline__ void prep_chunk(uint8_t *sm, const PrefillArgs &a, in
     prep_v<P>(sm, a, Lc, W);
 }
 
-// ---- stage 2 (one thread): [Kh; Qh] Kb^T -> TMEM columns [col, col + 64), commit to mbar ----
+// ---- stage 2 (one thread): [Kh; Qh] Kb^T -> TMEM columns [col, col + 64) (with a stacked Kb tile:
+// [col, col + 128), the sum of the two halves), commit to mbar ----
 template <class P>
 __device__ __forceinline__ void issue_mma_a(uint32_t sbase, uint32_t tmem_col_addr, uint32_t mbar) {
     tc_fence_after();
-    const uint32_t id = idesc_bf16_f32(128, 64);
     const uint64_t dX = sdesc_kmajor_sw128(sbase + OFF_X), dXL = sdesc_kmajor_sw128(sbase + OFF_XL);
-    const uint64_t dKh = sdesc_kmajor_sw128(sbase + P::KB_HI), dKl = sdesc_kmajor_sw128(sbase + P::KB_LO);
-#pragma unroll
-    for (int sp = 0; sp < 3; ++sp)
+    if (P::KB_STACKED) {
+        // X_hi [Kb_hi; Kb_lo]^T (N = 128), then X_lo Kb_hi^T into the first 64 columns
+        const uint64_t dK = sdesc_kmajor_sw128(sbase + P::KB_HI);
+        const uint32_t id128 = idesc_bf16_f32(128, 128), id64 = idesc_bf16_f32(128, 64);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-            mma_bf16(tmem_col_addr, dadd(sp == 2 ? dXL : dX, (kk >> 2) * 16384 + (kk & 3) * 32),
-                     dadd(sp == 1 ? dKl : dKh, (kk >> 2) * 8192 + (kk & 3) * 32), id, (sp | kk) != 0);
+            mma_bf16(tmem_col_addr, dadd(dX, (kk >> 2) * 16384 + (kk & 3) * 32), dadd(dK, (kk >> 2) * 16384 + (kk & 3) * 32),
+                     id128, kk != 0);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+            mma_bf16(tmem_col_addr, dadd(dXL, (kk >> 2) * 16384 + (kk & 3) * 32), dadd(dK, (kk >> 2) * 16384 + (kk & 3) * 32),
+                     id64, 1);
+    } else {
+        const uint32_t id = idesc_bf16_f32(128, 64);
+        const uint64_t dKh = sdesc_kmajor_sw128(sbase + P::KB_HI), dKl = sdesc_kmajor_sw128(sbase + P::KB_LO);
+#pragma unroll
+        for (int sp = 0; sp < 3; ++sp)
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+                mma_bf16(tmem_col_addr, dadd(sp == 2 ? dXL : dX, (kk >> 2) * 16384 + (kk & 3) * 32),
+                         dadd(sp == 1 ? dKl : dKh, (kk >> 2) * 8192 + (kk & 3) * 32), id, (sp | kk) != 0);
+    }
     mma_commit(mbar);
 }
 
@@ -353,7 +378,15 @@ __device__ __forceinline__ void extract_a(uint8_t *sm, uint32_t tl, uint32_t col
         const int colbase = quarter * 16;
         uint32_t r0[16];
         tmem_ld16(tl + col + colbase, r0);
-        tmem_wait_ld();
+        if (P::KB_STACKED) {
+            uint32_t r1[16];
+            tmem_ld16(tl + col + 64 + colbase, r1);
+            tmem_wait_ld();
+#pragma unroll
+            for (int u = 0; u < 16; ++u) r0[u] = __float_as_uint(__uint_as_float(r0[u]) + __uint_as_float(r1[u]));
+        } else {
+            tmem_wait_ld();
+        }
         const int row = lrow + lane;
         if (row < 64) {
             const float b = sBeta[row];

@@ -199,6 +199,10 @@ __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.comm
 __device__ __forceinline__ void prefetch_l2(const void *src, uint32_t bytes) {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
+// Prefetch the 128-byte line holding p into L2 (an ordinary load-path prefetch, no TMA).
+__device__ __forceinline__ void prefetch_line_l2(const void *p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
 // Prefetch the 3-D map's box at {x, y, z} into L2.
 __device__ __forceinline__ void tma_prefetch_3d(const void *tmap, int x, int y, int z) {
     asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];"
@@ -215,6 +219,8 @@ __device__ __forceinline__ void tma_store_3d(const void *tmap, uint32_t src_smem
 }
 // Wait until every committed bulk group of this thread has finished reading shared memory.
 __device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// Same, except that the most recently committed group may still be reading.
+__device__ __forceinline__ void bulk_wait_read_but_last() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
 // Wait until every committed bulk group of this thread has completed (writes performed).
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 // Named barrier over `count` threads (a multiple of 32).
