@@ -250,12 +250,9 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_prep_kernel(const __gri
         pend_s = true;
     };
     auto stage_g = [&](const Item &x) { tma_load_3d(sbase + PlanPrep::GST, &A.tm_g, 0, x.h, x.cs, mbar_s); };
-    auto prefetch_rows = [&](const Item &x) {        // into L2, an item ahead of the staging copies
-        tma_prefetch_3d(&A.tm_q, 0, x.h, x.cs);
-        tma_prefetch_3d(&A.tm_k, 0, x.h, x.cs);
-        tma_prefetch_3d(&A.tm_v, 0, x.h, x.cs);
-        tma_prefetch_3d(&A.tm_g, 0, x.h, x.cs);
-    };
+    // the g rows into L2 ahead of their staging copy, which is issued late (after the previous
+    // item's solve); q, k and v are staged a whole item ahead and need no prefetch
+    auto prefetch_rows = [&](const Item &x) { tma_prefetch_3d(&A.tm_g, 0, x.h, x.cs); };
 
     PhaseClock clk;   // phases: 0 staging wait, 1 prep q/k, 2 prep v (MMA A), 3 history + MMA A wait, 4 extract, 5 solve, 6 MMA U/W, 7 records out
     Item x, y;                                           // this item and the next
@@ -276,7 +273,6 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_prep_kernel(const __gri
         const int Lc = min(kC, x.te - x.cs);
         uint8_t *rec = rec_of(x);
         if (tid == 0) {
-            if (m + 2 < m_hi) prefetch_rows(advance(y, m + 1));
             bulk_wait_read_but_last();                   // all but W have left shared memory (prep_qk waits for W)
             wait_on(mbar_s, sph, pend_s);
         }
@@ -353,6 +349,9 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_prep_kernel(const __gri
                 mma_bf16(tbase + kColWp, dadd(dKl, kk * 2048), dadd(dT, kk * 32), id64, 1);
             mma_commit(mbar_a);
             pend_a = true;
+            // the g rows of the item after next into L2, while the MMAs run (the issue may wait
+            // on the copy engine)
+            if (m + 2 < m_hi) prefetch_rows(advance(y, m + 1));
         }
         if (!mma_wait()) break;
         clk.tick(6);

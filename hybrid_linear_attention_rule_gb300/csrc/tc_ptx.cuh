@@ -199,10 +199,6 @@ __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.comm
 __device__ __forceinline__ void prefetch_l2(const void *src, uint32_t bytes) {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
-// Prefetch the 128-byte line holding p into L2 (an ordinary load-path prefetch, no TMA).
-__device__ __forceinline__ void prefetch_line_l2(const void *p) {
-    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
-}
 // Prefetch the 3-D map's box at {x, y, z} into L2.
 __device__ __forceinline__ void tma_prefetch_3d(const void *tmap, int x, int y, int z) {
     asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];"
