@@ -73,7 +73,7 @@ struct DecodeArgs {
 
 __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(DecodeArgs a) {
     extern __shared__ uint8_t smraw[];
-    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
+    uint8_t *sm = smem_align1024(smraw);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int dk = a.dk, dv = a.dv, H = a.H, W = a.W;
     const int NH = a.N * a.H;

@@ -40,12 +40,13 @@ using namespace tc;
 using namespace tcc;
 
 // ---- one chunk record (byte offsets; identical to the scan kernel's smem layout) ----
-constexpr uint32_t REC_X = 0;            // [W rows 0-63; Qh rows 64-127] x 128 K, split: hi 32 KB, lo 32 KB
+constexpr uint32_t REC_X = 0;            // [W rows 0-63; Qh rows 64-127] x 128 K, per 64-wide K atom hi then lo (16 KB each)
 constexpr uint32_t REC_B = 65536;        // MN-major B of MMA O/S: 8 KB N-blocks Aqk^T hi, lo, then Kb hi, lo per K atom
 constexpr uint32_t REC_U = 114688;       // U^T fp32 as 16 blocks of 4 tokens: [tok / 4][128 dv][4 tok]
 constexpr uint32_t REC_VEC = 147456;     // r[128], G_last[128] fp32
 constexpr uint32_t REC_BYTES = 148480;
-static_assert(OFF_XL == OFF_X + 32768, "the [Kh; Qh] tile pair must be contiguous (one bulk store)");
+static_assert(PlanPrep::X_LO == PlanPrep::X_HI + 16384 && PlanPrep::X_ATOM == 32768,
+              "the record's [W; Qh] part is the prep plan's X tile: [hi 0 | lo 0 | hi 1 | lo 1]");
 static_assert(OFF_GL == OFF_REF + 512, "r and G_last must be adjacent (one bulk store)");
 
 // byte offset of U^T element (dv j, token i) inside the U block: a warp's 32 consecutive dv
@@ -117,7 +118,7 @@ constexpr uint32_t kColUp = 128, kColWp = 256;
 
 __global__ void __launch_bounds__(kThreads, 1) kda_chunk_prep_kernel(const __grid_constant__ PrepArgs A) {
     extern __shared__ uint8_t smraw[];
-    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
+    uint8_t *sm = smem_align1024(smraw);
     const PrefillArgs &a = A.p;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int H = a.H, N = a.N;
@@ -289,7 +290,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_prep_kernel(const __gri
             // tile (per K atom the hi rows, then the lo rows) is the record's layout as it stands
 #pragma unroll
             for (int p = 0; p < 4; ++p)
-                bulk_s2g(rec + REC_X + p * 16384 + 8192, sbase + OFF_X + p * 16384 + 8192, 8192);
+                bulk_s2g(rec + REC_X + p * 16384 + 8192, sbase + PlanPrep::X_HI + p * 16384 + 8192, 8192);
             bulk_s2g(rec + REC_B + 16384, sbase + PlanPrep::KB_HI, 32768);
             bulk_commit();
         }
@@ -331,7 +332,8 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_prep_kernel(const __gri
                            id64 = idesc_bf16_f32(128, 64, false, /*a_mn=*/true);
             const uint64_t dVh = sdesc_mnmajor_sw128(sbase + PlanPrep::V_HI, 8192),
                            dVl = sdesc_mnmajor_sw128(sbase + PlanPrep::V_LO, 8192);
-            const uint64_t dKh = sdesc_mnmajor_sw128(sbase + OFF_X, 16384), dKl = sdesc_mnmajor_sw128(sbase + OFF_XL, 16384);
+            const uint64_t dKh = sdesc_mnmajor_sw128(sbase + PlanPrep::X_HI, PlanPrep::X_ATOM),
+                           dKl = sdesc_mnmajor_sw128(sbase + PlanPrep::X_LO, PlanPrep::X_ATOM);
             const uint64_t dT = sdesc_kmajor_sw128(sbase + PlanPrep::TB_HI);
             static_assert(PlanPrep::TB_LO == PlanPrep::TB_HI + 8192, "Tb hi and lo must form one 128-row tile");
 #pragma unroll
@@ -377,9 +379,9 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_prep_kernel(const __gri
             for (int u = 0; u < 16; ++u) {
                 float hv, lv;
                 split_bf16(__uint_as_float(r[u]), hv, lv);
-                const uint32_t o = kmaj128(128, quarter * 16 + u, j);
-                *reinterpret_cast<__nv_bfloat16 *>(sm + OFF_X + o) = __float2bfloat16_rn(hv);
-                *reinterpret_cast<__nv_bfloat16 *>(sm + OFF_XL + o) = __float2bfloat16_rn(lv);
+                const uint32_t o = (j >> 6) * PlanPrep::X_ATOM + sw128_offset(quarter * 16 + u, j & 63);
+                *reinterpret_cast<__nv_bfloat16 *>(sm + PlanPrep::X_HI + o) = __float2bfloat16_rn(hv);
+                *reinterpret_cast<__nv_bfloat16 *>(sm + PlanPrep::X_LO + o) = __float2bfloat16_rn(lv);
             }
         }
         if (has_next && tid < kC) sBeta[tid] = beta_next;
@@ -388,7 +390,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_prep_kernel(const __gri
         __syncthreads();
         if (tid == 0) {
 #pragma unroll
-            for (int p = 0; p < 4; ++p) bulk_s2g(rec + REC_X + p * 16384, sbase + OFF_X + p * 16384, 8192);
+            for (int p = 0; p < 4; ++p) bulk_s2g(rec + REC_X + p * 16384, sbase + PlanPrep::X_HI + p * 16384, 8192);
             bulk_commit();
         }
         tc_fence_after();
@@ -436,14 +438,17 @@ static_assert(kScanSmemBytes <= 232448, "scan kernel shared memory exceeds the p
 
 // Tensor memory: the MMA A operands S'^T and V'^T live here as split bf16 (two values per
 // 32-bit column, the even K index in the low half), so shared memory only feeds the B operands.
+// MMA W writes D = S'^T [W_hi; Qh_hi; W_lo; Qh_lo]^T into columns [0, 256) (S'_lo adds into the
+// first 128): (W S')^T = D[0, 64) + D[128, 192), (Qh S')^T = D[64, 128) + D[192, 256).  The V'
+// phase then puts each thread's V'^T K-step (hi 8 | lo 8) over the columns of D[0, 64) it has
+// read, and O^T = (Qh S')^T into D[192, 256), next to the state.
 constexpr uint32_t kScanTmemCols = 512;
-constexpr uint32_t kColD = 0;       // [0, 64): (W S')^T, [64, 128): O^T (fp32)
-constexpr uint32_t kColSs = 128;    // S'^T fp32, 128 columns
-static_assert(kColD + 128 == kColSs, "O^T and S'^T must be adjacent: one N = 192 chain accumulates into both");
-constexpr uint32_t kColSh = 256;    // S'^T hi / lo, bf16 pairs: 64 columns each
-constexpr uint32_t kColSl = 320;
-constexpr uint32_t kColVh = 384;    // V'^T hi / lo, bf16 pairs: 32 columns each
-constexpr uint32_t kColVl = 416;
+constexpr uint32_t kColD = 0;       // D, 256 columns; V'^T split in [0, 64)
+constexpr uint32_t kColO = 192;     // O^T (fp32)
+constexpr uint32_t kColSs = 256;    // S'^T fp32, 128 columns
+static_assert(kColO + 64 == kColSs, "O^T and S'^T must be adjacent: one N = 192 chain accumulates into both");
+constexpr uint32_t kColSh = 384;    // S'^T hi / lo, bf16 pairs: 64 columns each
+constexpr uint32_t kColSl = 448;
 
 // 16 consecutive K values of one TMEM lane -> split bf16 pairs at columns col_hi, col_lo (8 each)
 __device__ __forceinline__ void tmem_put_split16(uint32_t col_hi, uint32_t col_lo, const float (&v)[16]) {
@@ -467,7 +472,7 @@ __device__ __forceinline__ void tmem_put_split16(uint32_t col_hi, uint32_t col_l
 // and G_last are read by the threads that use them, one chunk ahead, into registers.
 __global__ void __launch_bounds__(kThreads, 1) kda_chunk_scan_kernel(const __grid_constant__ ScanArgs A) {
     extern __shared__ uint8_t smraw[];
-    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
+    uint8_t *sm = smem_align1024(smraw);
     const PrefillArgs &a = A.p;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int nh = blockIdx.x, n = nh / a.H, h = nh % a.H;
@@ -654,18 +659,21 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_scan_kernel(const __gri
         const int Lc = min(kC, te - cs);
         const bool more = c + 1 < c_end;
         float *fnext = sFcol + ((c + 1) & 1) * kD;
-        // ---- MMA: D^T = S'^T [W; Qh]^T ((W S')^T in D[0, 64), (Qh S')^T in D[64, 128)) ----
+        // ---- MMA: D = S'^T [W; Qh]^T, hi and lo parts in separate columns ----
         if (tid == 0 && wait_x(c)) {
             tc_fence_after();
-            const uint32_t id = idesc_bf16_f32(128, 128);
+            // per K atom the tile's 256 rows are [W_hi; Qh_hi; W_lo; Qh_lo]: S'_hi against all of
+            // them (N = 256), then S'_lo against the hi rows (N = 128)
+            const uint32_t id256 = idesc_bf16_f32(128, 256), id128 = idesc_bf16_f32(128, 128);
             const uint32_t xoff = (c & 1) ? Q_X1 : REC_X;
-            const uint64_t dX = sdesc_kmajor_sw128(sbase + xoff), dXL = sdesc_kmajor_sw128(sbase + xoff + 32768);
+            const uint64_t dX = sdesc_kmajor_sw128(sbase + xoff);
 #pragma unroll
-            for (int sp = 0; sp < 3; ++sp)
+            for (int kk = 0; kk < 8; ++kk)
+                mma_bf16_ta(tbase + kColD, tbase + kColSh + kk * 8, dadd(dX, (kk >> 2) * 32768 + (kk & 3) * 32), id256,
+                            kk != 0);
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
-                    mma_bf16_ta(tbase + kColD, tbase + (sp == 2 ? kColSl : kColSh) + kk * 8,
-                                dadd(sp == 1 ? dXL : dX, (kk >> 2) * 16384 + (kk & 3) * 32), id, (sp | kk) != 0);
+            for (int kk = 0; kk < 8; ++kk)
+                mma_bf16_ta(tbase + kColD, tbase + kColSl + kk * 8, dadd(dX, (kk >> 2) * 32768 + (kk & 3) * 32), id128, 1);
             mma_commit(mb_a);
             pend_a = true;
         }
@@ -679,15 +687,22 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_scan_kernel(const __gri
         }
         if (!mma_wait()) { failed = true; break; }
         clk.tick(0);
-        // ---- V'^T = U^T - (W S')^T -> split tile ----
+        // ---- V'^T = U^T - (W S')^T -> split, over the columns just read; O^T = (Qh S')^T ----
         {
-            uint32_t r[16];
+            uint32_t r[16], r2[16];
             tmem_ld16(tl + kColD + quarter * 16, r);
+            tmem_ld16(tl + kColD + 128 + quarter * 16, r2);
             tmem_wait_ld();
             float v[16];
 #pragma unroll
-            for (int u = 0; u < 16; ++u) v[u] = uR[u] - __uint_as_float(r[u]);
-            tmem_put_split16(tl + kColVh + quarter * 8, tl + kColVl + quarter * 8, v);
+            for (int u = 0; u < 16; ++u) v[u] = uR[u] - (__uint_as_float(r[u]) + __uint_as_float(r2[u]));
+            tmem_put_split16(tl + kColD + quarter * 16, tl + kColD + quarter * 16 + 8, v);
+            tmem_ld16(tl + kColD + 64 + quarter * 16, r);
+            tmem_ld16(tl + kColO + quarter * 16, r2);
+            tmem_wait_ld();
+#pragma unroll
+            for (int u = 0; u < 16; ++u) r[u] = __float_as_uint(__uint_as_float(r[u]) + __uint_as_float(r2[u]));
+            tmem_st16(tl + kColO + quarter * 16, r);
             tmem_wait_st();
         }
         if (more) load_u(c + 1);
@@ -695,7 +710,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_scan_kernel(const __gri
         tc_fence_before();
         __syncthreads();
         clk.tick(1);
-        // ---- MMA: [O^T | S'^T] += V'^T [Aqk^T | Kb]  (N = 192: D columns 64 .. 255) ----
+        // ---- MMA: [O^T | S'^T] += V'^T [Aqk^T | Kb]  (N = 192: columns kColO .. kColSs + 127) ----
         if (tid == 0 && wait_on(mb_k, kph, pend_k)) {
             tc_fence_after();
             const uint32_t id = idesc_bf16_f32(128, 192, false, false, /*b_mn=*/true);
@@ -706,7 +721,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_scan_kernel(const __gri
             for (int sp = 0; sp < 3; ++sp)
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
-                    mma_bf16_ta(tbase + kColD + 64, tbase + (sp == 2 ? kColVl : kColVh) + kk * 8,
+                    mma_bf16_ta(tbase + kColO, tbase + kColD + kk * 16 + (sp == 2 ? 8 : 0),
                                 dadd(sp == 1 ? dBl : dBh, kk * 2048), id, 1);
             mma_commit(mb_a);
             pend_a = true;
@@ -738,7 +753,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_scan_kernel(const __gri
         const bool tma_out = a.out_bf16 && (Lc == kC || te == a.T);
         {
             uint32_t r0[16];
-            tmem_ld16(tl + kColD + 64 + quarter * 16, r0);
+            tmem_ld16(tl + kColO + quarter * 16, r0);
             tmem_wait_ld();
             if (tma_out) {
                 __nv_bfloat16 *ot = reinterpret_cast<__nv_bfloat16 *>(sm + Q_OST);

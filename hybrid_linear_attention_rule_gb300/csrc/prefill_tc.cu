@@ -56,7 +56,7 @@ struct TcArgs {
 
 __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __grid_constant__ TcArgs A) {
     extern __shared__ uint8_t smraw[];
-    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
+    uint8_t *sm = smem_align1024(smraw);
     const PrefillArgs &a = A.p;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int nh = blockIdx.x, n = nh / a.H, h = nh % a.H;

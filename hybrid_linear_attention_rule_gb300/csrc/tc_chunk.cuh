@@ -82,6 +82,7 @@ struct PlanFused {
     static constexpr uint32_t V_HI = OFF_V_HI, V_LO = OFF_V_LO, KB_HI = OFF_KB_HI, KB_LO = OFF_KB_LO;
     static constexpr uint32_t SCR_A = OFF_SCR_A, SCR_T = OFF_SCR_T, AQK_HI = OFF_AQK_HI, AQK_LO = OFF_AQK_LO;
     static constexpr uint32_t TB_HI = OFF_TB_HI, TB_LO = OFF_TB_LO, SCAN = OFF_SCAN;
+    static constexpr uint32_t X_HI = OFF_X, X_LO = OFF_XL, X_ATOM = 16384;   // [Kh; Qh]: hi atoms, then lo atoms
     static constexpr bool KB_STACKED = false;    // Kb hi and lo as two 64-row tiles
     static constexpr bool CALLER_STAGES = false; // prep_qk loads beta and owns every tile it writes
 };
@@ -94,6 +95,9 @@ struct PlanPrep {
     static constexpr uint32_t AQK_HI = 180224, AQK_LO = 188416;            // Aqk^T       (extract .. its store)
     static constexpr uint32_t SCAN = AQK_HI;                               // g partial sums (prep_qk)
     static constexpr uint32_t TB_HI = 196608, TB_LO = 204800;              // Tb          (solve .. MMA U/W)
+    // [Kh; Qh] with the hi and lo tiles of each K atom adjacent ([hi 0 | lo 0 | hi 1 | lo 1], 16 KB
+    // each): per K atom the 256 rows [Kh_hi; Qh_hi; Kh_lo; Qh_lo] are then one N = 256 operand
+    static constexpr uint32_t X_HI = 0, X_LO = 16384, X_ATOM = 32768;
     // Kb hi in rows 0-63 and lo in rows 64-127 of one 128-row tile: MMA A then reads [Kb_hi; Kb_lo]
     // as one N = 128 operand (hi*hi and hi*lo in one chain) and adds lo*hi with N = 64
     static constexpr bool KB_STACKED = true;
@@ -208,13 +212,14 @@ __device__ __forceinline__ void conv_rows(const uint8_t *sm, const PrefillArgs &
     }
 }
 
-// One token's 4 channels, split, into row `row` of a K=128 tile (hi and lo tiles).
-__device__ __forceinline__ void put_row_split(uint8_t *sm, uint32_t off_hi, uint32_t off_lo, uint32_t rows, int row,
+// One token's 4 channels, split, into row `row` of a K=128 tile (hi and lo tiles) whose two
+// 64-wide K atoms lie `atom` bytes apart.
+__device__ __forceinline__ void put_row_split(uint8_t *sm, uint32_t off_hi, uint32_t off_lo, uint32_t atom, int row,
                                               int c0, const float (&v)[4]) {
     float hv[4], lv[4];
 #pragma unroll
     for (int m = 0; m < 4; ++m) split_bf16(v[m], hv[m], lv[m]);
-    const uint32_t o = kmaj128(rows, row, c0);
+    const uint32_t o = (c0 >> 6) * atom + sw128_offset(row, c0 & 63);
     *reinterpret_cast<uint2 *>(sm + off_hi + o) = make_uint2(pack_bf16(hv[0], hv[1]), pack_bf16(hv[2], hv[3]));
     *reinterpret_cast<uint2 *>(sm + off_lo + o) = make_uint2(pack_bf16(lv[0], lv[1]), pack_bf16(lv[2], lv[3]));
 }
@@ -294,7 +299,7 @@ __device__ __forceinline__ void prep_qk(uint8_t *sm, const PrefillArgs &a, int c
         float t4[4];
 #pragma unroll
         for (int m = 0; m < 4; ++m) t4[m] = y[ii][m] * E[ii][m];
-        put_row_split(sm, OFF_X, OFF_XL, 128, 64 + i0 + ii, c0, t4);
+        put_row_split(sm, P::X_HI, P::X_LO, P::X_ATOM, 64 + i0 + ii, c0, t4);
     }
     // k -> Kh = k E (rows 0..63 of X / XL), Kb = k / E (rows; the state update reads them MN-major)
     conv_rows(sm, a, 1, P::KST, Lc, W, y);
@@ -303,9 +308,9 @@ __device__ __forceinline__ void prep_qk(uint8_t *sm, const PrefillArgs &a, int c
         float t4[4], u4[4];
 #pragma unroll
         for (int m = 0; m < 4; ++m) { t4[m] = y[ii][m] * E[ii][m]; u4[m] = y[ii][m] * Eb[ii][m]; }
-        put_row_split(sm, OFF_X, OFF_XL, 128, i0 + ii, c0, t4);
-        if (P::KB_STACKED) put_row_split(sm, P::KB_HI, P::KB_HI + 8192, 128, i0 + ii, c0, u4);
-        else put_row_split(sm, P::KB_HI, P::KB_LO, 64, i0 + ii, c0, u4);
+        put_row_split(sm, P::X_HI, P::X_LO, P::X_ATOM, i0 + ii, c0, t4);
+        if (P::KB_STACKED) put_row_split(sm, P::KB_HI, P::KB_HI + 8192, 16384, i0 + ii, c0, u4);
+        else put_row_split(sm, P::KB_HI, P::KB_LO, 8192, i0 + ii, c0, u4);
     }
     fence_async_smem();
     tc_fence_before();
@@ -321,7 +326,7 @@ __device__ __forceinline__ void prep_v(uint8_t *sm, const PrefillArgs &a, int Lc
     float y[kTok][4];
     conv_rows(sm, a, 2, P::VST, Lc, W, y);
 #pragma unroll
-    for (int ii = 0; ii < kTok; ++ii) put_row_split(sm, P::V_HI, P::V_LO, 64, i0 + ii, c0, y[ii]);
+    for (int ii = 0; ii < kTok; ++ii) put_row_split(sm, P::V_HI, P::V_LO, 8192, i0 + ii, c0, y[ii]);
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
@@ -339,19 +344,19 @@ __device__ __forceinline__ void prep_chunk(uint8_t *sm, const PrefillArgs &a, in
 template <class P>
 __device__ __forceinline__ void issue_mma_a(uint32_t sbase, uint32_t tmem_col_addr, uint32_t mbar) {
     tc_fence_after();
-    const uint64_t dX = sdesc_kmajor_sw128(sbase + OFF_X), dXL = sdesc_kmajor_sw128(sbase + OFF_XL);
+    const uint64_t dX = sdesc_kmajor_sw128(sbase + P::X_HI), dXL = sdesc_kmajor_sw128(sbase + P::X_LO);
     if (P::KB_STACKED) {
         // X_hi [Kb_hi; Kb_lo]^T (N = 128), then X_lo Kb_hi^T into the first 64 columns
         const uint64_t dK = sdesc_kmajor_sw128(sbase + P::KB_HI);
         const uint32_t id128 = idesc_bf16_f32(128, 128), id64 = idesc_bf16_f32(128, 64);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-            mma_bf16(tmem_col_addr, dadd(dX, (kk >> 2) * 16384 + (kk & 3) * 32), dadd(dK, (kk >> 2) * 16384 + (kk & 3) * 32),
-                     id128, kk != 0);
+            mma_bf16(tmem_col_addr, dadd(dX, (kk >> 2) * P::X_ATOM + (kk & 3) * 32),
+                     dadd(dK, (kk >> 2) * 16384 + (kk & 3) * 32), id128, kk != 0);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-            mma_bf16(tmem_col_addr, dadd(dXL, (kk >> 2) * 16384 + (kk & 3) * 32), dadd(dK, (kk >> 2) * 16384 + (kk & 3) * 32),
-                     id64, 1);
+            mma_bf16(tmem_col_addr, dadd(dXL, (kk >> 2) * P::X_ATOM + (kk & 3) * 32),
+                     dadd(dK, (kk >> 2) * 16384 + (kk & 3) * 32), id64, 1);
     } else {
         const uint32_t id = idesc_bf16_f32(128, 64);
         const uint64_t dKh = sdesc_kmajor_sw128(sbase + P::KB_HI), dKl = sdesc_kmajor_sw128(sbase + P::KB_LO);
@@ -359,7 +364,7 @@ __device__ __forceinline__ void issue_mma_a(uint32_t sbase, uint32_t tmem_col_ad
         for (int sp = 0; sp < 3; ++sp)
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)
-                mma_bf16(tmem_col_addr, dadd(sp == 2 ? dXL : dX, (kk >> 2) * 16384 + (kk & 3) * 32),
+                mma_bf16(tmem_col_addr, dadd(sp == 2 ? dXL : dX, (kk >> 2) * P::X_ATOM + (kk & 3) * 32),
                          dadd(sp == 1 ? dKl : dKh, (kk >> 2) * 8192 + (kk & 3) * 32), id, (sp | kk) != 0);
     }
     mma_commit(mbar);

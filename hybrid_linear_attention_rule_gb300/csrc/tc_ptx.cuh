@@ -12,6 +12,12 @@ namespace tc {
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
+// The dynamic shared-memory window rounded up to a 1024-byte boundary, derived from the shared
+// array by pointer arithmetic so that the compiler still knows every access through it to be a
+// shared one (a round trip through an integer would leave it a generic pointer).
+__device__ __forceinline__ uint8_t *smem_align1024(uint8_t *base) {
+    return base + ((1024u - (smem_u32(base) & 1023u)) & 1023u);
+}
 
 // ---- mbarrier ----
 __device__ __forceinline__ void mbar_init(uint32_t addr, uint32_t count) {
