@@ -677,7 +677,6 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_scan_kernel(const __gri
             mma_commit(mb_a);
             pend_a = true;
         }
-        if (tid == 0 && c + 3 < c_end) prefetch_chunk(c + 3);
         // the next chunk's basis factor, while the MMAs run
         if (tid < kD && more) {
             fnext[tid] = expf(logf_cur + rN);
@@ -745,6 +744,8 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_scan_kernel(const __gri
             load_x(c + 2);
             if (gated) load_gate(c + 2);
         }
+        // the record three chunks ahead into L2, queued behind the copies above
+        if (tid == 0 && c + 3 < c_end) prefetch_chunk(c + 3);
         clk.tick(2);
         // ---- this chunk's outputs, then the state into the next chunk's basis ----
         // bf16 outputs go through a shared tile and one TMA store that runs behind the next chunk,
