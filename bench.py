@@ -326,8 +326,8 @@ def run_e2e(args, K, torch, dev, P, Dc, prefill_call, decode_call, out_p, fs, ou
 # Measured DRAM bytes per call (ncu dram__bytes_read.sum + dram__bytes_write.sum, summed over the
 # call's kernels) of the current kernel versions, or None when not yet captured for a kernel
 # version.  The prefill figure is a T=8192 capture scaled by the tokens processed to T=65536.
-PREFILL_TRAFFIC_PER_LAUNCH = 12.05e9     # two-pass call: prep + scan + offsets, 1.5063 GB at T=8192 x 8
-DECODE_TRAFFIC_PER_LAUNCH = 1.0999e9
+PREFILL_TRAFFIC_PER_LAUNCH = 12.13e9     # two-pass call: prep + scan + offsets, 1.517 GB at T=8192 x 8
+DECODE_TRAFFIC_PER_LAUNCH = 1.0997e9
 
 
 # ---- the CPU oracle (baseline leg and the reference arm) ----
