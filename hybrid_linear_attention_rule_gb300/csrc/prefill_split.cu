@@ -517,7 +517,10 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_scan_kernel(const __gri
     const int quarter = warp >> 2;
     const int j = lrow + lane;                          // this thread's TMEM lane: dv channel
     // S'^T <- S0^T (true state, basis factor 1) at the sequence start, else the carried state
-    float logf_cur = 0.f;         // tid < 128: log of the basis factor of the current chunk
+    // the per-channel basis factors are kept by the last four warps (vt >= 0), which have no
+    // copies or MMAs to issue, so that the issuing warp does not trail the others
+    const int vt = tid - (kThreads - kD);
+    float logf_cur = 0.f;         // vt >= 0: log of the basis factor of the current chunk
     {
         for (int cb = 0; cb < 32; cb += 16) {
             uint32_t r[16];
@@ -538,9 +541,9 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_scan_kernel(const __gri
             tmem_st16(tl + kColSs + quarter * 32 + cb, r);
         }
         tmem_wait_st();
-        if (!first && tid < kD) {
-            logf_cur = A.carry_logf[(size_t)nh * kD + tid];
-            sLogf[tid] = logf_cur;
+        if (!first && vt >= 0) {
+            logf_cur = A.carry_logf[(size_t)nh * kD + vt];
+            sLogf[vt] = logf_cur;
         }
     }
 
@@ -576,6 +579,13 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_scan_kernel(const __gri
         if (c & 1) pend_g1 = true; else pend_g0 = true;
     };
     auto wait_gate = [&](int c) { return (c & 1) ? wait_on(mb_g1, gph1, pend_g1) : wait_on(mb_g0, gph0, pend_g0); };
+    // the other threads wait for chunk c's gate rows themselves (no CTA barrier): the phase of
+    // buffer c & 1 is the number of earlier loads into it, mod 2
+    auto gate_ready = [&](int c) {
+        const int b = c & 1;
+        const int first_b = c_begin + ((b - c_begin) & 1);
+        mbar_wait_bounded(b ? mb_g1 : mb_g0, (uint32_t)(((c - first_b) >> 1) & 1), kWaitLimit);
+    };
     auto mma_wait = [&]() -> bool {
         if (tid == 0 && !*sflag) wait_on(mb_a, aph, pend_a);
         __syncthreads();
@@ -586,7 +596,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_scan_kernel(const __gri
 
     // register-resident operands, one chunk ahead
     float uR[16];                 // U^T row j, tokens 16*quarter .. +15
-    float rN = 0.f, glN = 0.f;    // tid < 128: r and G_last of the chunk after the current one
+    float rN = 0.f, glN = 0.f;    // vt >= 0: r and G_last of the chunk after the current one
     auto load_u = [&](int c) {
         const uint8_t *p = rec_of(c) + REC_U;
 #pragma unroll
@@ -597,8 +607,8 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_scan_kernel(const __gri
     };
     auto load_vec = [&](int c) {
         const float *p = reinterpret_cast<const float *>(rec_of(c) + REC_VEC);
-        rN = __ldg(p + tid);
-        glN = __ldg(p + kD + tid);
+        rN = __ldg(p + vt);
+        glN = __ldg(p + kD + vt);
     };
     // S'^T = S^T diag(fcol) -> TMEM, fp32 and split bf16 (the A operand of MMA W/Qh)
     auto to_basis = [&](const float *fcol) {
@@ -621,7 +631,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_scan_kernel(const __gri
         tmem_wait_st();
     };
 
-    // a chunk's record and gate rows into L2 ahead of their copies into shared memory (thread 0)
+    // a chunk's record and gate rows into L2 ahead of their copies into shared memory (one thread)
     auto prefetch_chunk = [&](int c) {
         prefetch_l2(rec_of(c), REC_BYTES);
         if (gated) tma_prefetch_3d(&A.tm_gate, 0, h, tb + c * kC);
@@ -642,11 +652,11 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_scan_kernel(const __gri
             }
         }
         load_u(c);
-        if (tid < kD) {
+        if (vt >= 0) {
             load_vec(c);
-            sFcol[(c & 1) * kD + tid] = expf(logf_cur + rN);
+            sFcol[(c & 1) * kD + vt] = expf(logf_cur + rN);
             logf_cur = glN - rN;
-            sLogf[tid] = logf_cur;
+            sLogf[vt] = logf_cur;
             if (c + 1 < c_end) load_vec(c + 1);
         }
         __syncthreads();
@@ -678,10 +688,10 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_scan_kernel(const __gri
             pend_a = true;
         }
         // the next chunk's basis factor, while the MMAs run
-        if (tid < kD && more) {
-            fnext[tid] = expf(logf_cur + rN);
+        if (vt >= 0 && more) {
+            fnext[vt] = expf(logf_cur + rN);
             logf_cur = glN - rN;
-            sLogf[tid] = logf_cur;
+            sLogf[vt] = logf_cur;
             if (c + 2 < c_end) load_vec(c + 2);
         }
         if (!mma_wait()) { failed = true; break; }
@@ -727,8 +737,11 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_scan_kernel(const __gri
         }
         float sg[16];                                    // sigmoid of the gate logits, while the MMAs run
         if (gated) {
-            if (tid == 0 && !*sflag) wait_gate(c);
-            __syncthreads();
+            if (tid == 0) {
+                if (!*sflag) wait_gate(c);
+            } else {
+                gate_ready(c);
+            }
             const uint8_t *gt = sm + ((c & 1) ? Q_G1 : Q_G0);
 #pragma unroll
             for (int u = 0; u < 16; ++u)
