@@ -72,6 +72,7 @@ def load(path: str | None = None):
         lib.kda_oracle_chunked.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, D, I, P, P]
         lib.kda_oracle_mixer.argtypes = [P, P, P, P, P, P, P, P, I, P, P, P, I, I, I, I, I, D, I, D, P, P]
         lib.kda_oracle_decode_step.argtypes = [P, P, P, P, P, P, P, I, P, P, I, I, I, I, D, I, D, P]
+        lib.kda_oracle_recurrent_backward.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, I, D, P, P, P, P, P, P]
         for f in ("kda_oracle_short_conv", "kda_oracle_l2norm", "kda_oracle_recurrent",
                   "kda_oracle_bruteforce", "kda_oracle_chunked", "kda_oracle_mixer",
                   "kda_oracle_decode_step"):
@@ -162,6 +163,35 @@ def recurrent(q, k, v, g, beta, initial_state=None, gate=None, cu_seqlens=None, 
     """Per-token KDA recurrence (the definition). Returns (o [T,H,dv], final_state [N,H,dk,dv])."""
     lib = lib or load()
     return _core(lib.kda_oracle_recurrent, q, k, v, g, beta, initial_state, gate, cu_seqlens, scale)
+
+
+def recurrent_backward(q, k, v, g, beta, dO, initial_state=None, dS_final=None, cu_seqlens=None, scale=None,
+                       lib=None):
+    """Gradients of the ungated recurrence (reverse-mode, token by token) for the loss whose
+    gradients with respect to o and to the final states are dO [T,H,dv] and dS_final
+    [N,H,dk,dv] (optional).  Returns a dict with dq, dk, dv, dg [T,H,*], dbeta [T,H] and
+    dS0 [N,H,dk,dv]."""
+    lib = lib or load()
+    q = _f64(q, name="q")
+    T, H, dk = q.shape
+    v = _f64(v, name="v")
+    dv = v.shape[2]
+    k = _f64(k, (T, H, dk), "k")
+    g = _f64(g, (T, H, dk), "g")
+    beta = _f64(beta, (T, H), "beta")
+    dO = _f64(dO, (T, H, dv), "dO")
+    cu, N = _cu(cu_seqlens, T)
+    S0 = _f64(initial_state, (N, H, dk, dv), "initial_state")
+    dSf = _f64(dS_final, (N, H, dk, dv), "dS_final")
+    scale = float(dk) ** -0.5 if scale is None else float(scale)
+    out = dict(dq=np.zeros((T, H, dk)), dk=np.zeros((T, H, dk)), dv=np.zeros((T, H, dv)), dg=np.zeros((T, H, dk)),
+               dbeta=np.zeros((T, H)), dS0=np.zeros((N, H, dk, dv)))
+    rc = lib.kda_oracle_recurrent_backward(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(S0), _ptr(dO),
+                                           _ptr(dSf), _ptr(cu), N, T, H, dk, dv, scale, _ptr(out["dq"]),
+                                           _ptr(out["dk"]), _ptr(out["dv"]), _ptr(out["dg"]), _ptr(out["dbeta"]),
+                                           _ptr(out["dS0"]))
+    _check(rc, "recurrent_backward")
+    return out
 
 
 def bruteforce(q, k, v, g, beta, initial_state=None, gate=None, cu_seqlens=None, scale=None, lib=None):

@@ -190,6 +190,121 @@ int kda_oracle_recurrent(const double *q, const double *k, const double *v,
     return bad ? -1 : 0;
 }
 
+/* Reverse-mode derivative of the recurrence above, without the gate ("native forward +
+ * backward" in the feature list of "Experimental Native Vulkan Backend for Kimi K3", Hugging
+ * Face discussion #187, names the backward; none of the pages writes it out, so this is the
+ * derivative of the definition, by the chain rule, token by token).  Given dO (the gradient
+ * of a loss with respect to o = scale S_t^T q_t) and dSfin (with respect to each sequence's
+ * final state; may be null), it returns the gradients with respect to q, k, v, g, beta and
+ * the initial state.  The forward states S_0 .. S_L of a sequence are kept for the reverse
+ * sweep.  For t = L .. 1, with P = Diag(alpha_t) S_{t-1}, u = v_t - P^T k_t and G the gradient
+ * reaching S_t (dSfin before the last token):
+ *   G  += scale q_t dO_t^T              (o_t reads S_t)
+ *   gq  = scale S_t dO_t
+ *   h   = G^T k_t;   gv = beta_t h;   gbeta = h . u
+ *   gk  = beta_t (G u - P h)            (S_t = P + beta k u^T with u depending on k)
+ *   dP  = G - beta_t k_t h^T;   gg[c] = sum_j P[c][j] dP[c][j]   (dP/dg = P row-wise)
+ *   G   = Diag(alpha_t) dP              (the gradient reaching S_{t-1})
+ * and after the sweep G is the initial-state gradient.  Tiny inputs only. */
+int kda_oracle_recurrent_backward(const double *q, const double *k, const double *v, const double *g,
+                                  const double *beta, const double *S0, const double *dO, const double *dSfin,
+                                  const int *cu, int N, int T, int H, int dk, int dv, double scale,
+                                  double *gq, double *gk, double *gv, double *gg, double *gbeta, double *gS0)
+{
+    if (check_cu(cu, N, T) || H <= 0 || dk <= 0 || dv <= 0) return -1;
+    if (!q || !k || !v || !g || !beta || !dO || !gq || !gk || !gv || !gg || !gbeta || !gS0) return -1;
+    const size_t M = (size_t)dk * dv;
+    int bad = 0;
+#pragma omp parallel for collapse(2) schedule(dynamic)
+    for (int n = 0; n < N; ++n) {
+        for (int h = 0; h < H; ++h) {
+            const long L = cu[n + 1] - cu[n];
+            double *S = (double *)malloc(sizeof(double) * M * (size_t)(L + 1));
+            double *G = (double *)malloc(sizeof(double) * M);
+            double *P = (double *)malloc(sizeof(double) * M);
+            double *u = (double *)malloc(sizeof(double) * dv);
+            double *hv = (double *)malloc(sizeof(double) * dv);
+            if (!S || !G || !P || !u || !hv) {
+                free(S); free(G); free(P); free(u); free(hv);
+#pragma omp atomic write
+                bad = 1;
+                continue;
+            }
+            const size_t so = ((size_t)n * H + h) * M;
+            for (size_t e = 0; e < M; ++e) S[e] = S0 ? S0[so + e] : 0.0;
+            /* forward, keeping every state */
+            for (long i = 0; i < L; ++i) {
+                const long t = cu[n] + i;
+                const double *kt = k + ((size_t)t * H + h) * dk, *gt = g + ((size_t)t * H + h) * dk;
+                const double *vt = v + ((size_t)t * H + h) * dv;
+                const double bt = beta[(size_t)t * H + h];
+                const double *Sp = S + (size_t)i * M;
+                double *Sn = S + (size_t)(i + 1) * M;
+                for (int c = 0; c < dk; ++c)
+                    for (int j = 0; j < dv; ++j) P[(size_t)c * dv + j] = exp(gt[c]) * Sp[(size_t)c * dv + j];
+                for (int j = 0; j < dv; ++j) {
+                    double w = 0.0;
+                    for (int c = 0; c < dk; ++c) w += P[(size_t)c * dv + j] * kt[c];
+                    u[j] = vt[j] - w;
+                }
+                for (int c = 0; c < dk; ++c)
+                    for (int j = 0; j < dv; ++j) Sn[(size_t)c * dv + j] = P[(size_t)c * dv + j] + bt * kt[c] * u[j];
+            }
+            /* reverse sweep */
+            for (size_t e = 0; e < M; ++e) G[e] = dSfin ? dSfin[so + e] : 0.0;
+            for (long i = L - 1; i >= 0; --i) {
+                const long t = cu[n] + i;
+                const size_t tk = ((size_t)t * H + h) * dk, tv = ((size_t)t * H + h) * dv;
+                const double *qt = q + tk, *kt = k + tk, *gt = g + tk, *vt = v + tv, *dOt = dO + tv;
+                const double bt = beta[(size_t)t * H + h];
+                const double *Sp = S + (size_t)i * M, *St = S + (size_t)(i + 1) * M;
+                for (int c = 0; c < dk; ++c)
+                    for (int j = 0; j < dv; ++j) G[(size_t)c * dv + j] += scale * qt[c] * dOt[j];
+                for (int c = 0; c < dk; ++c) {
+                    double a = 0.0;
+                    for (int j = 0; j < dv; ++j) a += St[(size_t)c * dv + j] * dOt[j];
+                    gq[tk + c] = scale * a;
+                }
+                for (int c = 0; c < dk; ++c)
+                    for (int j = 0; j < dv; ++j) P[(size_t)c * dv + j] = exp(gt[c]) * Sp[(size_t)c * dv + j];
+                for (int j = 0; j < dv; ++j) {
+                    double w = 0.0, x = 0.0;
+                    for (int c = 0; c < dk; ++c) {
+                        w += P[(size_t)c * dv + j] * kt[c];
+                        x += G[(size_t)c * dv + j] * kt[c];
+                    }
+                    u[j] = vt[j] - w;
+                    hv[j] = x;
+                }
+                double db = 0.0;
+                for (int j = 0; j < dv; ++j) {
+                    gv[tv + j] = bt * hv[j];
+                    db += hv[j] * u[j];
+                }
+                gbeta[(size_t)t * H + h] = db;
+                for (int c = 0; c < dk; ++c) {
+                    double gu = 0.0, ph = 0.0, pd = 0.0;
+                    for (int j = 0; j < dv; ++j) {
+                        gu += G[(size_t)c * dv + j] * u[j];
+                        ph += P[(size_t)c * dv + j] * hv[j];
+                    }
+                    gk[tk + c] = bt * (gu - ph);
+                    const double al = exp(gt[c]);
+                    for (int j = 0; j < dv; ++j) {
+                        const double dP = G[(size_t)c * dv + j] - bt * kt[c] * hv[j];
+                        pd += P[(size_t)c * dv + j] * dP;
+                        G[(size_t)c * dv + j] = al * dP;
+                    }
+                    gg[tk + c] = pd;
+                }
+            }
+            for (size_t e = 0; e < M; ++e) gS0[so + e] = G[e];
+            free(S); free(G); free(P); free(u); free(hv);
+        }
+    }
+    return bad ? -1 : 0;
+}
+
 /* Brute force: build the dense dk x dk transition M_t = (I - beta k k^T) Diag(alpha)
  * and form S_t = M_t S_{t-1} + beta k v^T with plain matrix products.  Tiny
  * inputs only (O(dk^2 dv) per token). */

@@ -326,11 +326,68 @@ def pin_mixer_composition(lib):
     return max(np.abs(o - o2).max(), np.abs(S - S2).max()), 1e-13
 
 
+def pin_backward_finite_differences(lib):
+    """The reverse-mode gradients equal central differences of the forward oracle's loss
+    sum(dO * o) + sum(dS_final * S_final), for every element of q, k, v, g, beta and S_0
+    (varlen, two heads, decaying, non-unit keys)."""
+    rng = np.random.default_rng(31)
+    cu = np.array([0, 3, 3, 7], dtype=np.int32)
+    T, H, dk, dv = 7, 2, 3, 4
+    args = dict(q=_rand(rng, T, H, dk), k=0.5 * _rand(rng, T, H, dk), v=_rand(rng, T, H, dv),
+                g=-0.3 * np.abs(_rand(rng, T, H, dk)), beta=rng.uniform(0.1, 0.9, (T, H)),
+                S0=0.3 * _rand(rng, 3, H, dk, dv))
+    dO, dSf, scale = _rand(rng, T, H, dv), _rand(rng, 3, H, dk, dv), 0.7
+
+    def loss(a):
+        o, S = O.recurrent(a["q"], a["k"], a["v"], a["g"], a["beta"], initial_state=a["S0"], cu_seqlens=cu,
+                           scale=scale, lib=lib)
+        return float((o * dO).sum() + (S * dSf).sum())
+
+    gr = O.recurrent_backward(args["q"], args["k"], args["v"], args["g"], args["beta"], dO, initial_state=args["S0"],
+                              dS_final=dSf, cu_seqlens=cu, scale=scale, lib=lib)
+    names = dict(q="dq", k="dk", v="dv", g="dg", beta="dbeta", S0="dS0")
+    err, eps = 0.0, 1e-6
+    for nm, arr in args.items():
+        for idx in np.ndindex(arr.shape):
+            a1 = {kk: vv.copy() for kk, vv in args.items()}
+            a2 = {kk: vv.copy() for kk, vv in args.items()}
+            a1[nm][idx] += eps
+            a2[nm][idx] -= eps
+            fd = (loss(a1) - loss(a2)) / (2 * eps)
+            err = max(err, abs(fd - gr[names[nm]][idx]) / max(1.0, abs(fd)))
+    return err, 1e-7
+
+
+def pin_backward_single_token_closed_form(lib):
+    """T=1 from a zero state (S_1 = beta k v^T, o = scale beta (k.q) v), by hand: with
+    G = dS_final + scale q dO^T and h = G^T k: dq = scale beta k (v.dO), dv = beta h,
+    dbeta = h.v, dk = beta G v, dg = 0, dS0 = Diag(alpha) (G - beta k h^T)."""
+    rng = np.random.default_rng(32)
+    H, dk, dv = 2, 5, 3
+    q, k, v = _rand(rng, 1, H, dk), _rand(rng, 1, H, dk), _rand(rng, 1, H, dv)
+    g, beta = -np.abs(_rand(rng, 1, H, dk)), rng.uniform(0.1, 0.9, (1, H))
+    dO, dSf, scale = _rand(rng, 1, H, dv), _rand(rng, 1, H, dk, dv), 0.45
+    gr = O.recurrent_backward(q, k, v, g, beta, dO, dS_final=dSf, scale=scale, lib=lib)
+    err = 0.0
+    for h in range(H):
+        qh, kh, vh, dOh, b = q[0, h], k[0, h], v[0, h], dO[0, h], beta[0, h]
+        G = dSf[0, h] + scale * np.outer(qh, dOh)
+        hv = G.T @ kh
+        want = dict(dq=scale * b * kh * (vh @ dOh), dv=b * hv, dbeta=hv @ vh, dk=b * G @ vh, dg=np.zeros(dk),
+                    dS0=np.exp(g[0, h])[:, None] * (G - b * np.outer(kh, hv)))
+        got = dict(dq=gr["dq"][0, h], dv=gr["dv"][0, h], dbeta=gr["dbeta"][0, h], dk=gr["dk"][0, h],
+                   dg=gr["dg"][0, h], dS0=gr["dS0"][0, h])
+        for key in want:
+            err = max(err, float(np.abs(np.asarray(want[key]) - np.asarray(got[key])).max()))
+    return err, 1e-13
+
+
 ALL_PINS = [pin_single_token_closed_form, pin_pure_decay, pin_orthonormal_delta_rule,
             pin_repeated_key_overwrites, pin_linearity, pin_exact_rational, pin_bruteforce_agrees,
             pin_gate_is_sigmoid, pin_state_chaining, pin_varlen_is_independent,
             pin_chunked_equals_recurrent, pin_conv_matches_numpy, pin_conv_chaining, pin_l2norm,
-            pin_decode_is_one_more_token, pin_mixer_composition]
+            pin_decode_is_one_more_token, pin_mixer_composition, pin_backward_finite_differences,
+            pin_backward_single_token_closed_form]
 
 
 def failing_pins(lib):

@@ -46,6 +46,11 @@ MUTANTS = {
                              "cs_out[((size_t)n * R + (R - 1 - r)) * D + c] = xv;")],
     "l2_eps_outside_root": [("double inv = 1.0 / sqrt(ss + eps);", "double inv = 1.0 / (sqrt(ss) + eps);")],
     "l2_missing_root": [("double inv = 1.0 / sqrt(ss + eps);", "double inv = 1.0 / (ss + eps);")],
+    "backward_drops_key_path_through_u": [("gk[tk + c] = bt * (gu - ph);", "gk[tk + c] = bt * gu;")],
+    "backward_skips_decay": [("G[(size_t)c * dv + j] = al * dP;", "G[(size_t)c * dv + j] = dP;")],
+    "backward_misses_output_term": [("G[(size_t)c * dv + j] += scale * qt[c] * dOt[j];",
+                                     "G[(size_t)c * dv + j] += 0.0 * qt[c] * dOt[j];")],
+    "backward_reads_old_state_for_q": [("a += St[(size_t)c * dv + j] * dOt[j];", "a += Sp[(size_t)c * dv + j] * dOt[j];")],
     "state_not_reset_between_sequences": [
         ("for (long t = cu[n]; t < cu[n + 1]; ++t) {\n                const double *qt = q + ((size_t)t * H + h) * dk;\n                const double *kt = k + ((size_t)t * H + h) * dk;\n                const double *gt = g + ((size_t)t * H + h) * dk;\n                const double *vt = v + ((size_t)t * H + h) * dv;\n                const double bt = beta[(size_t)t * H + h];\n                for (int c = 0; c < dk; ++c) {\n                    const double a",
          "for (long t = (cu[n] > 0 ? cu[n] - 1 : 0); t < cu[n + 1]; ++t) {\n                const double *qt = q + ((size_t)t * H + h) * dk;\n                const double *kt = k + ((size_t)t * H + h) * dk;\n                const double *gt = g + ((size_t)t * H + h) * dk;\n                const double *vt = v + ((size_t)t * H + h) * dv;\n                const double bt = beta[(size_t)t * H + h];\n                for (int c = 0; c < dk; ++c) {\n                    const double a")],
