@@ -23,6 +23,7 @@ __all__ = ["K3KDAError", "load_library", "library_path", "F32", "BF16", "L2_EPS"
            "k3kda_version", "k3kda_status_string", "k3kda_launch_count", "k3kda_short_conv",
            "k3kda_prefill_workspace_size", "k3kda_prefill_workspace_min", "k3kda_prefill", "k3kda_prefill_slots",
            "k3kda_decode_step_slots", "k3kda_prefill_noalloc", "k3kda_workspace_status",
+           "k3kda_backward_workspace_size", "k3kda_backward", "backward",
            "k3kda_decode_step", "prefill", "decode_step", "short_conv"]
 
 F32, BF16 = 0, 1
@@ -87,6 +88,11 @@ def load_library(build_if_missing: bool = True):
         lib.k3kda_decode_step_slots.argtypes = [P, P, P, I, P, P, P, P, P, P, P, P, I, I, I, I, I, I, F, I, P, I,
                                                 P]
         lib.k3kda_decode_step_slots.restype = I
+        lib.k3kda_backward_workspace_size.argtypes = [I, I, I, I, I]
+        lib.k3kda_backward_workspace_size.restype = ctypes.c_size_t
+        lib.k3kda_backward.argtypes = [P, P, P, I, P, P, P, P, P, I, I, I, I, I, F, P, P, P, P, P, P, P, P, P,
+                                       ctypes.c_size_t, P]
+        lib.k3kda_backward.restype = I
         _lib = lib
         return lib
 
@@ -214,6 +220,44 @@ def k3kda_decode_step_slots(q, k, v, g, beta, gate, conv_weight, conv_state_pool
                                      int(dk), int(dv), int(W), float(scale), int(bool(use_qk_l2norm)), _ptr(out),
                                      _dtype(out), _stream(stream))
     _check("k3kda_decode_step_slots", st)
+
+
+def k3kda_backward_workspace_size(N, T, H, dk, dv):
+    return int(load_library().k3kda_backward_workspace_size(int(N), int(T), int(H), int(dk), int(dv)))
+
+
+def k3kda_backward(q, k, v, g, beta, initial_state, cu_seqlens, cu_seqlens_host, N, T, H, dk, dv, scale, dO,
+                   dS_final, dq, dk_out, dv_out, dg, dbeta, dS0, workspace, stream=None):
+    """Reverse-mode gradients of the ungated recurrence (see include/k3kda.h)."""
+    lib = load_library()
+    st = lib.k3kda_backward(_ptr(q), _ptr(k), _ptr(v), _dtype(q), _ptr(g), _ptr(beta), _ptr(initial_state),
+                            _ptr(cu_seqlens), _host_i32(cu_seqlens_host, "cu_seqlens_host"), int(N), int(T), int(H),
+                            int(dk), int(dv), float(scale), _ptr(dO), _ptr(dS_final), _ptr(dq), _ptr(dk_out),
+                            _ptr(dv_out), _ptr(dg), _ptr(dbeta), _ptr(dS0), _ptr(workspace),
+                            int(workspace.numel() * workspace.element_size()), _stream(stream))
+    _check("k3kda_backward", st)
+
+
+def backward(q, k, v, g, beta, dO, initial_state=None, dS_final=None, cu_seqlens=None, scale=None, stream=None):
+    """Gradients (dict of fp32 tensors dq, dk, dv, dg, dbeta, dS0) of the ungated recurrence for the
+    loss gradients dO [T, H, dv] (fp32) and dS_final [N, H, dk, dv] (optional); allocates its outputs
+    and workspace with torch."""
+    T, H, dk = q.shape
+    dv = v.shape[-1]
+    if cu_seqlens is None:
+        cu_host = torch.tensor([0, T], dtype=torch.int32)
+    else:
+        cu_host = cu_seqlens.to("cpu", torch.int32)
+    N = int(cu_host.numel()) - 1
+    cu_dev = cu_host.to(q.device)
+    scale = float(dk) ** -0.5 if scale is None else float(scale)
+    f32 = dict(dtype=torch.float32, device=q.device)
+    out = dict(dq=torch.empty(T, H, dk, **f32), dk=torch.empty(T, H, dk, **f32), dv=torch.empty(T, H, dv, **f32),
+               dg=torch.empty(T, H, dk, **f32), dbeta=torch.empty(T, H, **f32), dS0=torch.empty(N, H, dk, dv, **f32))
+    ws = torch.empty(k3kda_backward_workspace_size(N, T, H, dk, dv), dtype=torch.uint8, device=q.device)
+    k3kda_backward(q, k, v, g, beta, initial_state, cu_dev, cu_host, N, T, H, dk, dv, scale, dO, dS_final,
+                   out["dq"], out["dk"], out["dv"], out["dg"], out["dbeta"], out["dS0"], ws, stream)
+    return out
 
 
 def k3kda_prefill_noalloc(q, k, v, g, beta, initial_state, cu_seqlens, cu_seqlens_host, N, T, H, dk, dv,

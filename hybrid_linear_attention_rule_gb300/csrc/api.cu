@@ -238,6 +238,39 @@ int k3kda_prefill_slots(const void *q, const void *k, const void *v, int in_dtyp
                         workspace_bytes, stream, state_idx, num_slots);
 }
 
+size_t k3kda_backward_workspace_size(int N, int T, int H, int dk, int dv) {
+    if (N < 0 || T < 0 || H < 0 || dk != 128 || dv != 128) return kStatusBytes;
+    return kStatusBytes + backward_workspace(N, T, H);
+}
+
+int k3kda_backward(const void *q, const void *k, const void *v, int in_dtype, const float *g, const float *beta,
+                   const float *initial_state, const int32_t *cu_seqlens, const int32_t *cu_seqlens_host, int N,
+                   int T, int H, int dk, int dv, float scale, const float *dO, const float *dS_final, float *dq,
+                   float *dk_out, float *dv_out, float *dg, float *dbeta, float *dS0, void *workspace,
+                   size_t workspace_bytes, void *stream) {
+    if (N < 1 || T < 0 || H < 1) return K3KDA_ERR_INVALID_ARG;
+    if (!dtype_ok(in_dtype)) return K3KDA_ERR_INVALID_ARG;
+    if (dk != 128 || dv != 128) return K3KDA_ERR_UNSUPPORTED;
+    if (T > 0 && (!q || !k || !v || !g || !beta || !dO || !dq || !dk_out || !dv_out || !dg || !dbeta))
+        return K3KDA_ERR_INVALID_ARG;
+    if (!dS0) return K3KDA_ERR_INVALID_ARG;
+    if (cu_seqlens == nullptr && N != 1) return K3KDA_ERR_INVALID_ARG;
+    if (cu_seqlens_host && !cu_ok(cu_seqlens_host, N, T)) return K3KDA_ERR_INVALID_ARG;
+    if ((long long)N * H * 4 > 0x7fffffffLL) return K3KDA_ERR_UNSUPPORTED;
+    for (const void *p : {q, k, v, (const void *)g, (const void *)initial_state, (const void *)dO,
+                          (const void *)dS_final, (const void *)dq, (const void *)dk_out, (const void *)dv_out,
+                          (const void *)dg, (const void *)dS0})
+        if (!aligned16(p)) return K3KDA_ERR_ALIGNMENT;
+    if (!aligned4(beta) || !aligned4(dbeta)) return K3KDA_ERR_ALIGNMENT;
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return K3KDA_ERR_WORKSPACE;
+    if (workspace_bytes < k3kda_backward_workspace_size(N, T, H, dk, dv)) return K3KDA_ERR_WORKSPACE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    char *ws = static_cast<char *>(workspace);
+    return cuda_status(launch_backward(q, k, v, in_dtype == K3KDA_BF16, g, beta, initial_state, cu_seqlens, N, T, H,
+                                       scale, dO, dS_final, dq, dk_out, dv_out, dg, dbeta, dS0, ws + kStatusBytes,
+                                       s));
+}
+
 int k3kda_workspace_status(void *workspace, void *stream) {
     if (!workspace) return K3KDA_ERR_INVALID_ARG;
     cudaStream_t s = static_cast<cudaStream_t>(stream);

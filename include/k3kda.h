@@ -285,6 +285,35 @@ int k3kda_decode_step(const void *q, const void *k, const void *v, int in_dtype,
                       int N, int H, int dk, int dv, int W, float scale, int use_qk_l2norm,
                       void *out, int out_dtype, void *stream);
 
+/* ---- backward of the recurrence ----
+ * Reverse-mode gradients of the ungated KDA recurrence (the one k3kda_prefill runs, without
+ * the conv, norm and gate around it; "native forward + backward" in the feature list of
+ * "Experimental Native Vulkan Backend for Kimi K3", Hugging Face discussion #187):
+ *     S_t = (I - beta_t k_t k_t^T) Diag(exp g_t) S_{t-1} + beta_t k_t v_t^T,   o_t = scale S_t^T q_t,
+ * with S_0 = initial_state (zero when NULL) and state, chunking and everything else
+ * restarting at every cu_seqlens boundary.  Given dO = dL/do [T, H, dv] and dS_final =
+ * dL/dS_final [N, H, dk, dv] (zero when NULL) it writes dq, dk, dg [T, H, dk], dv [T, H, dv],
+ * dbeta [T, H] and dS0 [N, H, dk, dv], all FP32.  q, k are used as given (apply the L2 norm's
+ * and the conv's own derivatives around this call when they precede it).
+ *
+ *   q, k [T, H, dk], v [T, H, dv]  in_dtype;  g [T, H, dk], beta [T, H], dO [T, H, dv] FP32
+ *   cu_seqlens: int32 [N+1] device, cu_seqlens_host: optional host copy (validated when given)
+ * Only dk = dv = 128 (UNSUPPORTED otherwise).  FP32 arithmetic on CUDA cores: a forward pass
+ * keeps the state before every 64-token chunk in the workspace, a reverse pass recomputes each
+ * chunk's states from its checkpoint and sweeps its tokens backwards; every (sequence, head)
+ * is split over 4 CTAs by 32-column blocks of dv.  Asynchronous on `stream`; the workspace
+ * (k3kda_backward_workspace_size bytes, 256-byte aligned, caller-owned) is scratch only.
+ * Errors: INVALID_ARG, UNSUPPORTED, ALIGNMENT (16 bytes for every array but beta, dbeta: 4),
+ * WORKSPACE, CUDA. */
+size_t k3kda_backward_workspace_size(int N, int T, int H, int dk, int dv);
+int k3kda_backward(const void *q, const void *k, const void *v, int in_dtype,
+                   const float *g, const float *beta, const float *initial_state,
+                   const int32_t *cu_seqlens, const int32_t *cu_seqlens_host,
+                   int N, int T, int H, int dk, int dv, float scale,
+                   const float *dO, const float *dS_final,
+                   float *dq, float *dk_out, float *dv_out, float *dg, float *dbeta, float *dS0,
+                   void *workspace, size_t workspace_bytes, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

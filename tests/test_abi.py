@@ -95,6 +95,36 @@ def test_prefill_rejects_bad_arguments(lib):
     assert _prefill(lib, ws=A16, ws_bytes=16) == -4      # too small
 
 
+def _backward(lib, **kw):
+    args = dict(q=A16, k=A16, v=A16, in_dtype=1, g=A16, beta=A16, S0=None, cu=None, cu_h=None, N=1, T=64, H=2,
+                dk=128, dv=128, scale=1.0, dO=A16, dSf=None, dq=A16, dk_out=A16, dv_out=A16, dg=A16, dbeta=A16,
+                dS0=A16, ws=None, ws_bytes=0, stream=None)
+    args.update(kw)
+    return lib.k3kda_backward(*args.values())
+
+
+def test_backward_rejects_bad_arguments(lib):
+    assert _backward(lib, N=0) == -1
+    assert _backward(lib, dO=None) == -1
+    assert _backward(lib, dS0=None) == -1
+    assert _backward(lib, N=2) == -1                     # two sequences but no cu_seqlens
+    assert _backward(lib, dk=64, dv=64) == -2            # only dk = dv = 128
+    assert _backward(lib, in_dtype=5) == -1
+    assert _backward(lib, dq=MIS) == -3
+    assert _backward(lib, ws=None) == -4
+    assert _backward(lib, ws=A16, ws_bytes=16) == -4
+    bad = (ctypes.c_int32 * 3)(0, 40, 30)
+    assert _backward(lib, N=2, cu=A16, cu_h=ctypes.cast(bad, ctypes.c_void_p), T=30) == -1
+
+
+def test_backward_workspace_size(lib):
+    per_chunk = 32 * 4 * 128 * 32 * 4                    # H * 4 column blocks * one block's state
+    T, H = 8192, 32
+    want = 256 + 256 + (T // 64) * per_chunk + 1 * H * 4 * 64 * 128 * 32 * 4
+    assert K.k3kda_backward_workspace_size(1, T, H, 128, 128) == want
+    assert K.k3kda_backward_workspace_size(1, T, H, 64, 64) == 256
+
+
 def test_prefill_validates_host_cu_seqlens(lib):
     bad = (ctypes.c_int32 * 3)(0, 40, 30)                # decreasing
     assert _prefill(lib, N=2, cu=A16, cu_h=ctypes.cast(bad, ctypes.c_void_p), T=30) == -1
