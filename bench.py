@@ -35,6 +35,7 @@ sys.path.insert(0, ROOT)
 METRIC = "KDA prefill tokens/s & decode tokens/s at 1 GB300; % of tensor/HBM roofline"
 PREFILL = dict(T=65536, H=32, d=128, chunk=64, W=4)
 DECODE = dict(N=256, H=32, d=128, W=4)
+BACKWARD = dict(T=8192, H=32, d=128)      # gradients of the recurrence: the chunked-prefill shape
 
 
 def parse():
@@ -48,6 +49,7 @@ def parse():
                    help="prefill tokens (all heads) the CPU baseline runs; scaled to the full workload")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-backward", action="store_true")
     p.add_argument("--prefill-tokens", type=int, default=None,
                    help="override the prefill length (profiling captures on a smaller case; "
                         "the JSON config records the length used)")
@@ -73,6 +75,14 @@ def prefill_work(T, H, d, chunk, W, N=1):
     bytes_ = T * H * per_tok_head + N * H * dk * dv * 4 + 2 * N * (W - 1) * D * 4 + D * W * 4
     flops = T * H * (10 * chunk * d + 6 * d * d) + T * D * 2 * W
     return bytes_, flops
+
+
+def backward_work(T, H, d):
+    """Bytes: q, k, v (bf16), g, dO (fp32), beta in; dq, dk, dg, dv (fp32), dbeta out.
+    Flops: one forward pass of the recurrence (5 d^2 per token and head) plus the reverse
+    sweep (18 d^2); the kernels also recompute the forward once more (5 d^2)."""
+    per_tok_head = 3 * 2 * d + 4 * d + 4 * d + 4 + 4 * (3 * d + d) + 4
+    return T * H * per_tok_head, T * H * 23 * d * d
 
 
 def decode_work(N, H, d, W):
@@ -281,7 +291,53 @@ def run_ours(args, rank, world, dev, torch):
     }
     if not args.no_e2e:
         res["e2e"] = run_e2e(args, K, torch, dev, P, Dc, prefill_call, decode_call, out_p, fs, out_d, world, barrier)
+    if not args.no_backward:
+        res["backward"] = run_backward(args, K, torch, dev, rank, world, clk_mhz=res["clocks"].get("sm_mhz"))
     return res
+
+
+def run_backward(args, K, torch, dev, rank, world, clk_mhz=None):
+    """Gradients of the recurrence (k3kda_backward) on the chunked-prefill shape, timed with CUDA
+    events over the same steps and warm-up as the main step; reported beside it, not in value."""
+    T, H, d = BACKWARD["T"], BACKWARD["H"], BACKWARD["d"]
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(2000 + rank)
+    n = lambda *s: torch.randn(s, generator=gen, device=dev)
+    unit = lambda x: (x / x.norm(dim=-1, keepdim=True)).to(torch.bfloat16)
+    q, k, v = unit(n(T, H, d)), unit(n(T, H, d)), n(T, H, d).to(torch.bfloat16)
+    g, beta, dO = -torch.nn.functional.softplus(n(T, H, d)), torch.sigmoid(n(T, H)), n(T, H, d)
+    cu_h = torch.tensor([0, T], dtype=torch.int32)
+    cu_d = cu_h.to(dev)
+    f32 = dict(dtype=torch.float32, device=dev)
+    outs = [torch.empty(T, H, d, **f32) for _ in range(4)] + [torch.empty(T, H, **f32), torch.empty(1, H, d, d, **f32)]
+    ws = torch.empty(K.k3kda_backward_workspace_size(1, T, H, d, d), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def call():
+        K.k3kda_backward(q, k, v, g, beta, None, cu_d, cu_h, 1, T, H, d, d, d ** -0.5, dO, None, outs[0], outs[1],
+                         outs[2], outs[3], outs[4], outs[5], ws, stream)
+
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    steps = max(1, args.steps)
+    e0.record(stream)
+    for _ in range(steps):
+        call()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    ms = max_over_ranks([ms], world, dev)[0]
+    by, fl = backward_work(T, H, d)
+    pk = peaks()
+    mhz = clk_mhz or 2070.0
+    fp32_peak = 152 * 128 * 2 * mhz * 1e6 / 1e12          # FP32 FMA lanes x 2 flop x SM clock, TFLOP/s
+    ach = fl / (ms / 1e3) / 1e12
+    return {"workload": f"gradients of the recurrence, T={T} H={H} d={d}, bf16 q/k/v, fp32 dO", "ms": ms,
+            "tokens_per_s": world * T / (ms / 1e3), "algorithmic_bytes": by, "algorithmic_flops": fl,
+            "roofline": {"bound": "alu", "achieved": ach, "peak": fp32_peak, "unit": "TFLOP/s", "frac": ach / fp32_peak,
+                         "hbm_achieved_gbs": by / (ms / 1e3) / 1e9, "hbm_peak_gbs": pk["hbm"]}}
 
 
 def run_e2e(args, K, torch, dev, P, Dc, prefill_call, decode_call, out_p, fs, out_d, world, barrier):
