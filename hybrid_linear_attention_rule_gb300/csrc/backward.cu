@@ -110,10 +110,19 @@ __device__ __forceinline__ void warp_rows_reduce(float (&x)[kCols], float &out) 
     // the kept index is 8*b4 + 4*b3 + 2*b2 + b1 of the lane, i.e. lane >> 1
 }
 
-struct Shared {
+struct __align__(16) Shared {
     float red[2][kWarps][kBV];    // warp partial column sums of two vectors
     float u[2][kBV], h[2][kBV];   // the column vectors of a token (alternating buffers)
 };
+
+// this thread's 16 columns of a 32-float shared vector (16-byte loads)
+__device__ __forceinline__ void ld16(const float *v, int c0, float (&x)[16]) {
+#pragma unroll
+    for (int u = 0; u < 16; u += 4) {
+        const float4 f = *reinterpret_cast<const float4 *>(v + c0 + u);
+        x[u] = f.x; x[u + 1] = f.y; x[u + 2] = f.z; x[u + 3] = f.w;
+    }
+}
 
 // A 16-token block's inputs in shared memory, raw (q, k, v in the input dtype; g, beta, dO
 // fp32), copied in by every thread with 16-byte cp.async while the previous block is worked
@@ -238,8 +247,11 @@ __device__ __forceinline__ void forward_step(Shared &sh, float (&S)[kCols], cons
     }
     __syncthreads();
     const int c0 = (tid & 1) * kCols;
+    float uv[kCols];
+    ld16(sh.u[buf], c0, uv);
+    const float bk = x.beta * x.k;
 #pragma unroll
-    for (int u = 0; u < kCols; ++u) S[u] = p[u] + x.beta * x.k * sh.u[buf][c0 + u];
+    for (int u = 0; u < kCols; ++u) S[u] = fmaf(bk, uv[u], p[u]);
 }
 
 // the forward over the block's first L tokens from S; when store is given, the state after
@@ -331,12 +343,13 @@ __global__ void __launch_bounds__(kThreads) kda_bwd_sweep_kernel(const __grid_co
             if (i > 0) ld_block(i > 1 ? scr + (size_t)(i - 2) * kBlockFloats : ck, r, c0, Spn);
             const int buf = i & 1;
             // G += scale q dO^T;  dq = scale S_t dO (this CTA's columns)
-            float sdo = 0.f;
+            float sdo = 0.f, dO[kCols];
+            ld16(bi.dO[i], c0, dO);
+            const float sq = A.scale * x.q;
 #pragma unroll
             for (int u = 0; u < kCols; ++u) {
-                const float d = bi.dO[i][c0 + u];
-                G[u] = fmaf(A.scale * x.q, d, G[u]);
-                sdo = fmaf(S[u], d, sdo);
+                G[u] = fmaf(sq, dO[u], G[u]);
+                sdo = fmaf(S[u], dO[u], sdo);
             }
             sdo += __shfl_xor_sync(0xffffffffu, sdo, 1);
             add_rows(A.dq + ((size_t)t * H + h) * kD + 16 * warp, A.scale * sdo);
@@ -371,13 +384,15 @@ __global__ void __launch_bounds__(kThreads) kda_bwd_sweep_kernel(const __grid_co
             }
             __syncthreads();
             // dk = beta (G u - P h);  dP = G - beta k h^T;  dg = rowsum(P o dP);  G <- alpha dP
-            float gu = 0.f, phh = 0.f, pdp = 0.f;
+            float gu = 0.f, phh = 0.f, pdp = 0.f, uv[kCols], hv[kCols];
+            ld16(sh.u[buf], c0, uv);
+            ld16(sh.h[buf], c0, hv);
+            const float bk = x.beta * x.k;
 #pragma unroll
             for (int u = 0; u < kCols; ++u) {
-                const float uu = sh.u[buf][c0 + u], hh = sh.h[buf][c0 + u];
-                gu = fmaf(G[u], uu, gu);
-                phh = fmaf(p[u], hh, phh);
-                const float dP = G[u] - x.beta * x.k * hh;
+                gu = fmaf(G[u], uv[u], gu);
+                phh = fmaf(p[u], hv[u], phh);
+                const float dP = fmaf(-bk, hv[u], G[u]);
                 pdp = fmaf(p[u], dP, pdp);
                 G[u] = x.a * dP;
             }
