@@ -1,4 +1,4 @@
-"""Seeded synthetic inputs for the KDA mixer workloads.
+"""Seeded synthetic inputs for the KDA mixer workloads and the attention layers' decode token.
 
 This module only draws random numbers and shapes them; it holds none of the
 mixer's arithmetic, so the CPU oracle and the CUDA path can both take their
@@ -25,7 +25,8 @@ from dataclasses import dataclass, field
 import numpy as np
 
 STREAMS = {"q": 1, "k": 2, "v": 3, "g": 4, "beta": 5, "gate": 6, "conv_w": 7, "S0": 8,
-           "lengths": 9, "conv_state": 10}
+           "lengths": 9, "conv_state": 10, "mla_q": 11, "mla_k": 12, "mla_v": 13, "mla_gate": 14,
+           "mla_k_cache": 15, "mla_v_cache": 16, "mla_lengths": 17}
 
 
 def _rng(seed: int, name: str) -> np.random.Generator:
@@ -191,3 +192,48 @@ def fused_mixer(seed=0, T=65536, H=32, d=128, chunk=64, W=4) -> KdaCase:
     chunked KDA, output * sigmoid(gate); bf16 activations, fp32 state from zero."""
     return prefill_case("mixer_T%d_H%d_d%d_W%d" % (T, H, d, W), [T], H, d, d, chunk, "bf16",
                         seed, gate=True, conv_width=W)
+
+
+# ---- the gated attention (MLA) layers' decode token ----
+
+@dataclass
+class MlaDecodeCase:
+    """One decode token of the hybrid's attention layers for N sequences: projected q, k, v of the
+    new token, the per-head key/value caches [N, H, L_max, d] (every row filled, so that a read past
+    a sequence's length shows), and the cached lengths."""
+    name: str
+    N: int
+    H: int
+    d: int
+    L_max: int
+    in_dtype: str                      # storage type of q, k_new, v_new, gate
+    cache_dtype: str                   # storage type of the caches
+    q: np.ndarray                      # float32 [N, H, d]
+    k_new: np.ndarray
+    v_new: np.ndarray
+    k_cache: np.ndarray                # float32 [N, H, L_max, d]
+    v_cache: np.ndarray
+    cache_len: np.ndarray              # int32 [N]
+    scale: float
+    rope_dim: int = 0
+    theta: float = 10000.0
+    gate: np.ndarray | None = None
+
+
+def mla_decode_case(name, N, H, d, L_max, lengths, seed=0, in_dtype="bf16", cache_dtype="bf16",
+                    rope_dim=0, theta=10000.0, gate=True) -> MlaDecodeCase:
+    """q, k_new, v_new, gate and the cached rows ~ N(0, 1) (bf16-exact for bf16 storage); lengths
+    given explicitly, or as (lo, hi) for uniform integers in [lo, hi]; scale = d^-1/2."""
+    bi, bc = in_dtype == "bf16", cache_dtype == "bf16"
+    if isinstance(lengths, tuple):
+        lens = _rng(seed, "mla_lengths").integers(lengths[0], lengths[1] + 1, size=N)
+    else:
+        lens = np.asarray(lengths)
+    return MlaDecodeCase(
+        name=name, N=N, H=H, d=d, L_max=L_max, in_dtype=in_dtype, cache_dtype=cache_dtype,
+        q=normal((N, H, d), 1.0, seed, "mla_q", bi), k_new=normal((N, H, d), 1.0, seed, "mla_k", bi),
+        v_new=normal((N, H, d), 1.0, seed, "mla_v", bi),
+        k_cache=normal((N, H, L_max, d), 1.0, seed, "mla_k_cache", bc),
+        v_cache=normal((N, H, L_max, d), 1.0, seed, "mla_v_cache", bc),
+        cache_len=lens.astype(np.int32), scale=float(d) ** -0.5, rope_dim=rope_dim, theta=theta,
+        gate=normal((N, H, d), 1.0, seed, "mla_gate", bi) if gate else None)
