@@ -16,7 +16,7 @@ HEADER = os.path.join(ROOT, "include", "k3kda.h")
 def declared_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(k3kda_[a-z_0-9]+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(k3(?:kda|mla)_[a-z_0-9]+)\s*\(", text)))
 
 
 @pytest.fixture(scope="module")
@@ -26,7 +26,7 @@ def lib():
 
 def test_header_declares_the_three_calls():
     names = declared_functions()
-    for n in ("k3kda_short_conv", "k3kda_prefill", "k3kda_decode_step"):
+    for n in ("k3kda_short_conv", "k3kda_prefill", "k3kda_decode_step", "k3mla_decode_step"):
         assert n in names
 
 
@@ -118,9 +118,10 @@ def test_backward_rejects_bad_arguments(lib):
 
 
 def test_backward_workspace_size(lib):
-    per_chunk = 32 * 4 * 128 * 32 * 4                    # H * 4 column blocks * one block's state
+    per_block = 32 * 4 * 128 * 32 * 4                    # H * 4 column blocks * one block's state
     T, H = 8192, 32
-    want = 256 + 256 + (T // 64) * per_chunk + 1 * H * 4 * 64 * 128 * 32 * 4
+    # a checkpoint before every 16-token block, plus one block of 16 per-token states per CTA
+    want = 256 + 256 + (T // 16) * per_block + 1 * H * 4 * 16 * 128 * 32 * 4
     assert K.k3kda_backward_workspace_size(1, T, H, 128, 128) == want
     assert K.k3kda_backward_workspace_size(1, T, H, 64, 64) == 256
 
@@ -198,3 +199,36 @@ def test_binding_refuses_cpu_tensors():
     x = torch.zeros(4, 8)
     with pytest.raises(ValueError):
         K.k3kda_short_conv(x, torch.zeros(8, 4), None, None, 1, 4, 8, 4, True, torch.zeros(4, 8))
+
+
+def _mla(lib, **kw):
+    a = dict(q=A16, k=A16, v=A16, in_dtype=1, gate=None, kc=A16, vc=A16, cache_dtype=1, lens=A16, N=4, H=2, d=128,
+             L_max=1024, rope_dim=0, theta=10000.0, scale=1.0, out=A16, out_dtype=1, ws=None, ws_bytes=0, stream=None)
+    a.update(kw)
+    return lib.k3mla_decode_step(*a.values())
+
+
+def test_mla_decode_rejects_bad_arguments(lib):
+    big = 1 << 30
+    assert _mla(lib, N=0) == 0                           # nothing to do: no launch, no workspace needed
+    assert _mla(lib, N=-1) == -1
+    assert _mla(lib, L_max=0) == -1
+    assert _mla(lib, kc=None) == -1
+    assert _mla(lib, lens=None) == -1
+    assert _mla(lib, rope_dim=3) == -1                   # odd
+    assert _mla(lib, rope_dim=130) == -1                 # above d
+    assert _mla(lib, rope_dim=64, theta=0.0) == -1
+    assert _mla(lib, cache_dtype=7) == -1
+    assert _mla(lib, d=96) == -2
+    assert _mla(lib, N=4096, H=64, L_max=big) == -2      # grid above 2^31 - 1 blocks
+    assert _mla(lib, vc=MIS) == -3
+    assert _mla(lib, ws=None) == -4
+    assert _mla(lib, ws=A16, ws_bytes=16) == -4
+
+
+def test_mla_workspace_size(lib):
+    r = lambda b: (b + 255) // 256 * 256
+    N, H, d, L = 256, 32, 128, 8192
+    S = L // 512
+    assert K.k3mla_decode_workspace_size(N, H, d, L) == r(N * 4) + r(N * H * d * 4) + r(N * H * S * 8) + r(N * H * S * d * 4)
+    assert K.k3mla_decode_workspace_size(3, 2, 64, 513) == r(12) + r(3 * 2 * 64 * 4) + r(3 * 2 * 2 * 8) + r(3 * 2 * 2 * 64 * 4)
