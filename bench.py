@@ -36,6 +36,7 @@ METRIC = "KDA prefill tokens/s & decode tokens/s at 1 GB300; % of tensor/HBM roo
 PREFILL = dict(T=65536, H=32, d=128, chunk=64, W=4)
 DECODE = dict(N=256, H=32, d=128, W=4)
 BACKWARD = dict(T=8192, H=32, d=128)      # gradients of the recurrence: the chunked-prefill shape
+MLA = dict(N=256, H=32, d=128, L_max=8192)   # the attention layers' decode token: the decode batch
 
 
 def parse():
@@ -50,6 +51,9 @@ def parse():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-backward", action="store_true")
+    p.add_argument("--no-mla", action="store_true")
+    p.add_argument("--mla-seqs", type=int, default=None,
+                   help="override the attention decode batch (profiling captures on a smaller case)")
     p.add_argument("--prefill-tokens", type=int, default=None,
                    help="override the prefill length (profiling captures on a smaller case; "
                         "the JSON config records the length used)")
@@ -83,6 +87,17 @@ def backward_work(T, H, d):
     sweep (18 d^2); the kernels also recompute the forward once more (5 d^2)."""
     per_tok_head = 3 * 2 * d + 4 * d + 4 * d + 4 + 4 * (3 * d + d) + 4
     return T * H * per_tok_head, T * H * 23 * d * d
+
+
+def mla_work(lens, H, d):
+    """Bytes of one attention decode token with bf16 caches: every cached key and value row read
+    once (the appended one included), the new rows written, q, k, v, gate read and the bf16
+    output written, the lengths read and written.  Flops: 4 d per attended key (score and
+    weighted value)."""
+    keys = int(np.sum(np.asarray(lens, dtype=np.int64) + 1))
+    N = len(lens)
+    bytes_ = keys * H * d * 2 * 2 + N * H * d * 2 * 2 + N * H * d * 2 * 5 + N * 8
+    return bytes_, keys * H * 4 * d
 
 
 def decode_work(N, H, d, W):
@@ -293,7 +308,56 @@ def run_ours(args, rank, world, dev, torch):
         res["e2e"] = run_e2e(args, K, torch, dev, P, Dc, prefill_call, decode_call, out_p, fs, out_d, world, barrier)
     if not args.no_backward:
         res["backward"] = run_backward(args, K, torch, dev, rank, world, clk_mhz=res["clocks"].get("sm_mhz"))
+    if not args.no_mla:
+        res["mla_decode"] = run_mla(args, K, torch, dev, rank, world)
     return res
+
+
+def run_mla(args, K, torch, dev, rank, world):
+    """One decode token of the attention layers (k3mla_decode_step): 256 sequences x 32 heads,
+    d = 128, bf16 key/value caches of 8192 rows per (sequence, head), cached lengths uniform in
+    [1, 8191], no RoPE, sigmoid gate, bf16 output.  The lengths are reset before every step (outside
+    the events), so each timed step attends over the same keys; reported beside the main step."""
+    N, H, d, L = args.mla_seqs or MLA["N"], MLA["H"], MLA["d"], MLA["L_max"]
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(3000 + rank)
+    bf = dict(device=dev, dtype=torch.bfloat16)
+    kc = torch.randn(N, H, L, d, generator=gen, **bf)
+    vc = torch.randn(N, H, L, d, generator=gen, **bf)
+    q, k, v, g = (torch.randn(N, H, d, generator=gen, **bf) for _ in range(4))
+    lens_np = np.random.default_rng(99 + rank).integers(1, L, size=N).astype(np.int32)
+    lens0 = torch.from_numpy(lens_np).to(dev)
+    lens = lens0.clone()
+    out = torch.empty(N, H, d, **bf)
+    ws = torch.empty(K.k3mla_decode_workspace_size(N, H, d, L), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def call():
+        K.k3mla_decode_step(q, k, v, g, kc, vc, lens, N, H, d, L, 0, 10000.0, d ** -0.5, out, ws, stream)
+
+    for _ in range(args.warmup):
+        lens.copy_(lens0)
+        call()
+    torch.cuda.synchronize()
+    steps = max(1, args.steps)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for e0, e1 in ev:
+        lens.copy_(lens0)
+        e0.record(stream)
+        call()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    ms = sum(e0.elapsed_time(e1) for e0, e1 in ev) / steps
+    ms = max_over_ranks([ms], world, dev)[0]
+    by, fl = mla_work(lens_np, H, d)
+    pk = peaks()
+    ach = by / (ms / 1e3) / 1e9
+    del kc, vc
+    return {"workload": f"attention decode token, N={N} H={H} d={d}, bf16 caches L_max={L}, lengths uniform in "
+                        f"[1, {L - 1}] ({int(lens_np.sum())} cached keys per head), NoPE, gate",
+            "ms": ms, "tokens_per_s": world * N / (ms / 1e3), "algorithmic_bytes": by, "algorithmic_flops": fl,
+            "roofline": {"bound": "hbm", "achieved": ach, "peak": pk["hbm"], "unit": "GB/s", "frac": ach / pk["hbm"],
+                         "traffic": None}}
 
 
 def run_backward(args, K, torch, dev, rank, world, clk_mhz=None):
