@@ -37,6 +37,7 @@ PREFILL = dict(T=65536, H=32, d=128, chunk=64, W=4)
 DECODE = dict(N=256, H=32, d=128, W=4)
 BACKWARD = dict(T=8192, H=32, d=128)      # gradients of the recurrence: the chunked-prefill shape
 MLA = dict(N=256, H=32, d=128, L_max=8192)   # the attention layers' decode token: the decode batch
+MLA_TRAFFIC_PER_KEY_HEAD = 1.388246e9 / ((84420 + 16) * 32)   # DRAM bytes per attended (key, head), measured
 
 
 def parse():
@@ -352,12 +353,15 @@ def run_mla(args, K, torch, dev, rank, world):
     by, fl = mla_work(lens_np, H, d)
     pk = peaks()
     ach = by / (ms / 1e3) / 1e9
+    # DRAM bytes of the attention kernel from one ncu capture of the 16-sequence case (1.3882 GB for
+    # 84420 cached keys per head), scaled by the keys attended: traffic grows in proportion to them
+    traffic = MLA_TRAFFIC_PER_KEY_HEAD * float(np.sum(lens_np.astype(np.int64) + 1)) * H
     del kc, vc
     return {"workload": f"attention decode token, N={N} H={H} d={d}, bf16 caches L_max={L}, lengths uniform in "
                         f"[1, {L - 1}] ({int(lens_np.sum())} cached keys per head), NoPE, gate",
             "ms": ms, "tokens_per_s": world * N / (ms / 1e3), "algorithmic_bytes": by, "algorithmic_flops": fl,
             "roofline": {"bound": "hbm", "achieved": ach, "peak": pk["hbm"], "unit": "GB/s", "frac": ach / pk["hbm"],
-                         "traffic": None}}
+                         "traffic": traffic}}
 
 
 def run_backward(args, K, torch, dev, rank, world, clk_mhz=None):
