@@ -4,7 +4,7 @@
 // The recurrence S_t = (I - beta_t k_t k_t^T) Diag(exp g_t) S_{t-1} + beta_t k_t v_t^T is
 // separable in the dv columns of S, and so is its reverse sweep, except for the quantities
 // that sum over dv (dq, dk, dg, dbeta), which each CTA adds into the outputs with atomics.
-// So a CTA owns one (sequence, head, 32-column block): 4 CTAs per head at dv = 128.
+// So a CTA owns one (sequence, head, 16-column block): 8 CTAs per head at dv = 128.
 //
 // Pass 1 runs the recurrence forward and stores the state before every 16-token block.
 // Pass 2 walks the blocks backwards: it recomputes the block's states from its checkpoint
@@ -28,10 +28,11 @@ namespace k3kda {
 namespace {
 
 constexpr int kD = 128;           // dk = dv
-constexpr int kBV = 32;           // dv columns per CTA
+constexpr int kBV = 16;           // dv columns per CTA
 constexpr int kNV = kD / kBV;     // CTAs per (sequence, head)
-constexpr int kThreads = 256;     // thread (row r = tid / 2, half) owns 16 columns of row r
-constexpr int kCols = 16;
+constexpr int kThreads = 256;     // thread (row r = tid / 2, half) owns kCols columns of row r
+constexpr int kCols = kBV / 2;
+constexpr int kColShift = kCols == 16 ? 1 : kCols == 8 ? 2 : 3;   // lane >> kColShift = kept column
 constexpr int kChunk = 16;        // tokens per checkpoint
 constexpr int kWarps = kThreads / 32;
 constexpr size_t kBlockFloats = (size_t)kD * kBV;   // one CTA's share of a state
@@ -63,62 +64,43 @@ __global__ void __launch_bounds__(1024) chunk_offsets_kernel(const int32_t *cu, 
     }
 }
 
-// Sum over the block's 128 rows of this thread's 16 column values (x), for two vectors at once:
-// a reduce-scatter over the 16 rows of the warp (lane bits 1-4) leaves lane (i, half) with
-// column half*16 + i, then the warps' partials meet in shared memory.  The 32 column sums of
-// vector a are returned in red[0][0][...] .. (read after the barrier inside) -- see below.
-__device__ __forceinline__ void warp_rows_reduce(float (&x)[kCols], float &out) {
+// Sum over the warp's 16 rows of this thread's kCols column values: a reduce-scatter over the
+// row bits of the lane (bits 4, 3, ... : each step keeps half of the remaining columns, chosen
+// by the lane's bit) leaves one column per lane, finished by all-reduce steps over the row bits
+// that remain; lane L then holds column (L & 1) * kCols + (L >> kColShift) summed over the warp's
+// rows, and the warps' partials meet in shared memory.
+__device__ __forceinline__ float warp_rows_reduce(const float (&x)[kCols]) {
     const int lane = threadIdx.x & 31;
-    // step over lane bit 4 (rows i and i^8): keep columns 8..15 when the bit is set
-    float y8[8];
-    {
-        const bool hi = (lane >> 4) & 1;
+    float y[kCols];
 #pragma unroll
-        for (int m = 0; m < 8; ++m) {
-            const float send = hi ? x[m] : x[m + 8];
-            const float keep = hi ? x[m + 8] : x[m];
-            y8[m] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+    for (int m = 0; m < kCols; ++m) y[m] = x[m];
+#pragma unroll
+    for (int st = 0; (kCols >> (st + 1)) >= 1; ++st) {
+        const int off = 16 >> st, cnt = kCols >> (st + 1);
+        const bool hi = (lane & off) != 0;
+#pragma unroll
+        for (int m = 0; m < cnt; ++m) {
+            const float send = hi ? y[m] : y[m + cnt];
+            const float keep = hi ? y[m + cnt] : y[m];
+            y[m] = keep + __shfl_xor_sync(0xffffffffu, send, off);
         }
     }
-    float y4[4];
-    {
-        const bool hi = (lane >> 3) & 1;
 #pragma unroll
-        for (int m = 0; m < 4; ++m) {
-            const float send = hi ? y8[m] : y8[m + 4];
-            const float keep = hi ? y8[m + 4] : y8[m];
-            y4[m] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
-        }
-    }
-    float y2[2];
-    {
-        const bool hi = (lane >> 2) & 1;
-#pragma unroll
-        for (int m = 0; m < 2; ++m) {
-            const float send = hi ? y4[m] : y4[m + 2];
-            const float keep = hi ? y4[m + 2] : y4[m];
-            y2[m] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
-        }
-    }
-    {
-        const bool hi = (lane >> 1) & 1;
-        const float send = hi ? y2[0] : y2[1];
-        const float keep = hi ? y2[1] : y2[0];
-        out = keep + __shfl_xor_sync(0xffffffffu, send, 2);
-    }
-    // lane (i = lane >> 1, half = lane & 1) now holds column half*16 + (bit-reversed... ) :
-    // the kept index is 8*b4 + 4*b3 + 2*b2 + b1 of the lane, i.e. lane >> 1
+    for (int off = 16 / kCols; off >= 2; off >>= 1) y[0] += __shfl_xor_sync(0xffffffffu, y[0], off);
+    return y[0];
 }
+
+__device__ __forceinline__ int kept_column(int lane) { return (lane & 1) * kCols + (lane >> kColShift); }
 
 struct __align__(16) Shared {
     float red[2][kWarps][kBV];    // warp partial column sums of two vectors
     float u[2][kBV], h[2][kBV];   // the column vectors of a token (alternating buffers)
 };
 
-// this thread's 16 columns of a 32-float shared vector (16-byte loads)
-__device__ __forceinline__ void ld16(const float *v, int c0, float (&x)[16]) {
+// this thread's kCols columns of a kBV-float shared vector (16-byte loads)
+__device__ __forceinline__ void ldc(const float *v, int c0, float (&x)[kCols]) {
 #pragma unroll
-    for (int u = 0; u < 16; u += 4) {
+    for (int u = 0; u < kCols; u += 4) {
         const float4 f = *reinterpret_cast<const float4 *>(v + c0 + u);
         x[u] = f.x; x[u + 1] = f.y; x[u + 2] = f.z; x[u + 3] = f.w;
     }
@@ -235,9 +217,7 @@ __device__ __forceinline__ void forward_step(Shared &sh, float (&S)[kCols], cons
         p[u] = x.a * S[u];
         kp[u] = x.k * p[u];
     }
-    float part;
-    warp_rows_reduce(kp, part);
-    sh.red[0][warp][(lane & 1) * kCols + (lane >> 1)] = part;
+    sh.red[0][warp][kept_column(lane)] = warp_rows_reduce(kp);
     __syncthreads();
     if (tid < kBV) {
         float w = 0.f;
@@ -248,7 +228,7 @@ __device__ __forceinline__ void forward_step(Shared &sh, float (&S)[kCols], cons
     __syncthreads();
     const int c0 = (tid & 1) * kCols;
     float uv[kCols];
-    ld16(sh.u[buf], c0, uv);
+    ldc(sh.u[buf], c0, uv);
     const float bk = x.beta * x.k;
 #pragma unroll
     for (int u = 0; u < kCols; ++u) S[u] = fmaf(bk, uv[u], p[u]);
@@ -344,7 +324,7 @@ __global__ void __launch_bounds__(kThreads) kda_bwd_sweep_kernel(const __grid_co
             const int buf = i & 1;
             // G += scale q dO^T;  dq = scale S_t dO (this CTA's columns)
             float sdo = 0.f, dO[kCols];
-            ld16(bi.dO[i], c0, dO);
+            ldc(bi.dO[i], c0, dO);
             const float sq = A.scale * x.q;
 #pragma unroll
             for (int u = 0; u < kCols; ++u) {
@@ -361,32 +341,33 @@ __global__ void __launch_bounds__(kThreads) kda_bwd_sweep_kernel(const __grid_co
                 kp[u] = x.k * p[u];
                 kg[u] = x.k * G[u];
             }
-            float pw, ph;
-            warp_rows_reduce(kp, pw);
-            warp_rows_reduce(kg, ph);
-            const int col = (lane & 1) * kCols + (lane >> 1);
-            sh.red[0][warp][col] = pw;
-            sh.red[1][warp][col] = ph;
+            const int col = kept_column(lane);
+            sh.red[0][warp][col] = warp_rows_reduce(kp);
+            sh.red[1][warp][col] = warp_rows_reduce(kg);
             __syncthreads();
-            if (tid < kBV) {
-                float w = 0.f, hh = 0.f;
+            if (warp == 0) {
+                float db = 0.f;
+                if (lane < kBV) {
+                    float w = 0.f, hh = 0.f;
 #pragma unroll
-                for (int wi = 0; wi < kWarps; ++wi) {
-                    w += sh.red[0][wi][tid];
-                    hh += sh.red[1][wi][tid];
+                    for (int wi = 0; wi < kWarps; ++wi) {
+                        w += sh.red[0][wi][lane];
+                        hh += sh.red[1][wi][lane];
+                    }
+                    const float uu = ld_in(bi.v[i], lane, A.bf16) - w;
+                    sh.u[buf][lane] = uu;
+                    sh.h[buf][lane] = hh;
+                    A.dv[((size_t)t * H + h) * kD + cb + lane] = x.beta * hh;
+                    db = hh * uu;
                 }
-                const float uu = ld_in(bi.v[i], tid, A.bf16) - w;
-                sh.u[buf][tid] = uu;
-                sh.h[buf][tid] = hh;
-                A.dv[((size_t)t * H + h) * kD + cb + tid] = x.beta * hh;
-                const float db = warp_sum(hh * uu);
-                if (tid == 0) atomicAdd(A.dbeta + (size_t)t * H + h, db);
+                db = warp_sum(db);
+                if (lane == 0) atomicAdd(A.dbeta + (size_t)t * H + h, db);
             }
             __syncthreads();
             // dk = beta (G u - P h);  dP = G - beta k h^T;  dg = rowsum(P o dP);  G <- alpha dP
             float gu = 0.f, phh = 0.f, pdp = 0.f, uv[kCols], hv[kCols];
-            ld16(sh.u[buf], c0, uv);
-            ld16(sh.h[buf], c0, hv);
+            ldc(sh.u[buf], c0, uv);
+            ldc(sh.h[buf], c0, hv);
             const float bk = x.beta * x.k;
 #pragma unroll
             for (int u = 0; u < kCols; ++u) {

@@ -299,9 +299,9 @@ int k3kda_decode_step(const void *q, const void *k, const void *v, int in_dtype,
  *   q, k [T, H, dk], v [T, H, dv]  in_dtype;  g [T, H, dk], beta [T, H], dO [T, H, dv] FP32
  *   cu_seqlens: int32 [N+1] device, cu_seqlens_host: optional host copy (validated when given)
  * Only dk = dv = 128 (UNSUPPORTED otherwise).  FP32 arithmetic on CUDA cores: a forward pass
- * keeps the state before every 64-token chunk in the workspace, a reverse pass recomputes each
- * chunk's states from its checkpoint and sweeps its tokens backwards; every (sequence, head)
- * is split over 4 CTAs by 32-column blocks of dv.  Asynchronous on `stream`; the workspace
+ * keeps the state before every 16-token block in the workspace, a reverse pass recomputes each
+ * block's states from its checkpoint and sweeps its tokens backwards; every (sequence, head)
+ * is split over 8 CTAs by 16-column blocks of dv.  Asynchronous on `stream`; the workspace
  * (k3kda_backward_workspace_size bytes, 256-byte aligned, caller-owned) is scratch only.
  * Errors: INVALID_ARG, UNSUPPORTED, ALIGNMENT (16 bytes for every array but beta, dbeta: 4),
  * WORKSPACE, CUDA. */

@@ -118,10 +118,10 @@ def test_backward_rejects_bad_arguments(lib):
 
 
 def test_backward_workspace_size(lib):
-    per_block = 32 * 4 * 128 * 32 * 4                    # H * 4 column blocks * one block's state
+    per_block = 32 * 128 * 128 * 4                       # H full fp32 states (the column-block CTAs tile each)
     T, H = 8192, 32
-    # a checkpoint before every 16-token block, plus one block of 16 per-token states per CTA
-    want = 256 + 256 + (T // 16) * per_block + 1 * H * 4 * 16 * 128 * 32 * 4
+    # a checkpoint before every 16-token block, plus 16 per-token states of every CTA's columns
+    want = 256 + 256 + (T // 16) * per_block + 1 * H * 16 * 128 * 128 * 4
     assert K.k3kda_backward_workspace_size(1, T, H, 128, 128) == want
     assert K.k3kda_backward_workspace_size(1, T, H, 64, 64) == 256
 
