@@ -240,7 +240,7 @@ int k3kda_prefill_slots(const void *q, const void *k, const void *v, int in_dtyp
 
 size_t k3kda_backward_workspace_size(int N, int T, int H, int dk, int dv) {
     if (N < 0 || T < 0 || H < 0 || dk != 128 || dv != 128) return kStatusBytes;
-    return kStatusBytes + backward_workspace(N, T, H);
+    return kStatusBytes + backward_chunked_workspace(N, T, H);
 }
 
 int k3kda_backward(const void *q, const void *k, const void *v, int in_dtype, const float *g, const float *beta,
@@ -256,7 +256,9 @@ int k3kda_backward(const void *q, const void *k, const void *v, int in_dtype, co
     if (!dS0) return K3KDA_ERR_INVALID_ARG;
     if (cu_seqlens == nullptr && N != 1) return K3KDA_ERR_INVALID_ARG;
     if (cu_seqlens_host && !cu_ok(cu_seqlens_host, N, T)) return K3KDA_ERR_INVALID_ARG;
-    if ((long long)N * H * 4 > 0x7fffffffLL) return K3KDA_ERR_UNSUPPORTED;
+    // grids: (chunks of 16 tokens) x H items and N x H x 8 column blocks
+    if ((long long)N * H * 8 > 0x7fffffffLL || ((long long)T / 16 + N + 1) * H > 0x7fffffffLL)
+        return K3KDA_ERR_UNSUPPORTED;
     for (const void *p : {q, k, v, (const void *)g, (const void *)initial_state, (const void *)dO,
                           (const void *)dS_final, (const void *)dq, (const void *)dk_out, (const void *)dv_out,
                           (const void *)dg, (const void *)dS0})
@@ -266,7 +268,7 @@ int k3kda_backward(const void *q, const void *k, const void *v, int in_dtype, co
     if (workspace_bytes < k3kda_backward_workspace_size(N, T, H, dk, dv)) return K3KDA_ERR_WORKSPACE;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     char *ws = static_cast<char *>(workspace);
-    return cuda_status(launch_backward(q, k, v, in_dtype == K3KDA_BF16, g, beta, initial_state, cu_seqlens, N, T, H,
+    return cuda_status(launch_backward_chunked(q, k, v, in_dtype == K3KDA_BF16, g, beta, initial_state, cu_seqlens, N, T, H,
                                        scale, dO, dS_final, dq, dk_out, dv_out, dg, dbeta, dS0, ws + kStatusBytes,
                                        s));
 }

@@ -1,0 +1,690 @@
+// backward_chunked.cu -- reverse-mode gradients of the KDA recurrence in chunked form.
+//
+// The recurrence S_t = (I - beta_t k_t k_t^T) Diag(exp g_t) S_{t-1} + beta_t k_t v_t^T,
+// o_t = scale S_t^T q_t (the ungated core of the mixer, "Experimental Native Vulkan Backend for
+// Kimi K3", Hugging Face discussion #187, feature list) is written per chunk of kC tokens in the
+// WY form the forward uses: with Gamma the in-chunk cumulative log decay, r a per-channel centre
+// (half the chunk's first and last Gamma) and G' = Gamma - r,
+//   Qt = q e^{G'},  Kt = k e^{G'},  Kh = k e^{-G'},  B = strict_lower(Kt Kh^T),
+//   Aqk = lower(Qt Kh^T),  Tm = (I + diag(beta) B)^-1,  W = Tm diag(beta) Kt,  U = Tm diag(beta) V,
+//   S' = e^{r} S,  Delta = U - W S',  O = scale (Qt S' + Aqk Delta),
+//   S_next = e^{Gamma_L - r} (S' + Kh^T Delta).
+// Differentiating these products (the chain rule on the chunk algebra) gives, for the gradient
+// Dout reaching S_next and dO of the chunk's outputs (dOs = scale dO):
+//   dX = e^{Gamma_L - r} Dout,  dDelta = Kh dX + Aqk^T dOs,  dR = Tm^T dDelta,
+//   Din = e^{r} (dX + Qt^T dOs - Kt^T diag(beta) dR)        (the gradient reaching S),
+//   dA = -strict_lower(dR Delta^T),  dAqk = lower(dOs Delta^T),
+//   dQt = dOs S'^T + dAqk Kh,  dKt = diag(beta) (dA Kh - dR S'^T),
+//   dKh = Delta dX^T + dAqk^T Qt + dA^T diag(beta) Kt,  dv = diag(beta) dR,
+//   dbeta = rowsum((V - Kt S') o dR) + rowsum(dA o B),
+//   dq = dQt e^{G'},  dk = dKt e^{G'} + dKh e^{-G'},
+//   dGamma = dQt o Qt + dKt o Kt - dKh o Kh  (+ rowsum(S_next o Dout) on the chunk's last row),
+//   dg = the in-chunk suffix sum of dGamma.
+// (r cancels from every output, so it is held constant.)  Four launches:
+//   1. prep    one CTA per (chunk, head): the tiles above, Tm by forward substitution;
+//   2. forward one CTA per (sequence, head, 16-column block of dv): the states at chunk starts;
+//   3. chain   same grid, chunks in reverse: dX, dR and Din, with dS0 at the sequence start;
+//   4. grads   one CTA per (chunk, head): dq, dk, dv, dg, dbeta.
+// Everything runs in fp32 on CUDA cores.  Chunks of 16 tokens keep e^{+-G'} small, so the
+// cancellations in dGamma stay at fp32 rounding level.
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+
+#include <atomic>
+
+#include "common.cuh"
+
+namespace k3kda {
+namespace {
+
+constexpr int kD = 128;
+constexpr int kC = 16;             // tokens per chunk
+constexpr int kBV = 16;            // dv columns of a chain CTA
+constexpr int kNV = kD / kBV;      // chain CTAs per (sequence, head)
+constexpr int kThreads = 256;
+constexpr int LD = kD + 1;         // padded row of a 128-wide tile in shared memory
+constexpr int LC = kC + 1;         // padded row of a 16-wide tile
+constexpr int LB = kBV + 1;
+
+struct CbArgs {
+    const void *q, *k, *v;
+    int bf16;
+    const float *g, *beta, *S0, *dO, *dSfin;
+    const int32_t *cu;
+    int N, T, H, Q;                // Q: chunks over all sequences
+    float scale;
+    int32_t *chunk_off;            // [N + 1]
+    int32_t *ck_t0, *ck_len;       // [Q]
+    // per (chunk, head) item, fp32
+    float *Qt, *Kt, *Kh, *E, *W, *U;   // [item][kC][kD]
+    float *Tm, *Aqk, *Bm;              // [item][kC][kC]
+    float *rr, *glr;                   // [item][kD]
+    float *Dl, *dR;                    // [item][kC][kD]
+    float *dX;                         // [item][kD][kD]
+    float *dgl;                        // [item][kNV][kD]
+    float *St;                         // [(Q + N) * H][kD][kD]: state at each chunk start, then the final
+    float *dq, *dk, *dv, *dg, *dbeta, *dS0;
+};
+
+__device__ __forceinline__ float ld_x(const void *p, size_t i, int bf16) {
+    return bf16 ? __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(p)[i]) : reinterpret_cast<const float *>(p)[i];
+}
+
+__global__ void __launch_bounds__(32) cb_offsets_kernel(CbArgs A) {
+    if (threadIdx.x != 0) return;
+    int acc = 0;
+    A.chunk_off[0] = 0;
+    for (int n = 0; n < A.N; ++n) {
+        int b, e;
+        seq_bounds(A.cu, n, A.T, b, e);
+        for (int t = b; t < e; t += kC) {
+            A.ck_t0[acc] = t;
+            A.ck_len[acc] = min(kC, e - t);
+            ++acc;
+        }
+        A.chunk_off[n + 1] = acc;
+    }
+}
+
+// C[m][n] over an M x N tile, thread tile TM x TN with rows m = tm + (M / TM) v and columns
+// n = tn + (N / TN) u; A(m, kk) = a[m * sam + kk * sak], B(kk, n) = b[kk * sbk + n * sbn].
+template <int M, int N, int TM, int TN>
+__device__ __forceinline__ void mm(float (&acc)[TM][TN], const float *a, int sam, int sak, const float *b, int sbk,
+                                   int sbn, int K) {
+    static_assert((M / TM) * (N / TN) == kThreads, "tile shape");
+    const int tn = threadIdx.x % (N / TN), tm = threadIdx.x / (N / TN);
+    for (int kk = 0; kk < K; ++kk) {
+        float av[TM], bv[TN];
+#pragma unroll
+        for (int v = 0; v < TM; ++v) av[v] = a[(tm + (M / TM) * v) * sam + kk * sak];
+#pragma unroll
+        for (int u = 0; u < TN; ++u) bv[u] = b[kk * sbk + (tn + (N / TN) * u) * sbn];
+#pragma unroll
+        for (int v = 0; v < TM; ++v)
+#pragma unroll
+            for (int u = 0; u < TN; ++u) acc[v][u] = fmaf(av[v], bv[u], acc[v][u]);
+    }
+}
+
+template <int TM, int TN>
+__device__ __forceinline__ void zero(float (&acc)[TM][TN]) {
+#pragma unroll
+    for (int v = 0; v < TM; ++v)
+#pragma unroll
+        for (int u = 0; u < TN; ++u) acc[v][u] = 0.f;
+}
+
+// ---- 1. prep: one CTA per (chunk, head) ---------------------------------------------------------
+
+__global__ void __launch_bounds__(kThreads) cb_prep_kernel(const __grid_constant__ CbArgs A) {
+    __shared__ float sG[kC][LD], sQt[kC][LD], sKt[kC][LD], sKh[kC][LD];
+    __shared__ float sB[kC][LC], sT[kC][LC];
+    __shared__ float sBeta[kC], sR[kD];
+    const int tid = threadIdx.x;
+    const int item = blockIdx.x, qc = item / A.H, h = item % A.H, H = A.H;
+    if (qc >= A.chunk_off[A.N]) return;                // the grid covers an upper bound of the chunks
+    const int t0 = A.ck_t0[qc], L = A.ck_len[qc];
+    for (int e = tid; e < kC * kD; e += kThreads) {
+        const int i = e / kD, c = e % kD;
+        sG[i][c] = i < L ? A.g[((size_t)(t0 + i) * H + h) * kD + c] : 0.f;
+    }
+    if (tid < kC) sBeta[tid] = tid < L ? A.beta[(size_t)(t0 + tid) * H + h] : 0.f;
+    __syncthreads();
+    if (tid < kD) {
+        float run = 0.f;
+        for (int i = 0; i < kC; ++i) { run += sG[i][tid]; sG[i][tid] = run; }
+        const float r = 0.5f * (sG[0][tid] + sG[L - 1][tid]);
+        sR[tid] = r;
+        A.rr[(size_t)item * kD + tid] = r;
+        A.glr[(size_t)item * kD + tid] = sG[L - 1][tid] - r;
+    }
+    __syncthreads();
+    const size_t tile = (size_t)item * kC * kD;
+    for (int e = tid; e < kC * kD; e += kThreads) {
+        const int i = e / kD, c = e % kD;
+        const float gp = fminf(fmaxf(sG[i][c] - sR[c], -87.f), 87.f);
+        const float ex = expf(gp), exi = expf(-gp);
+        const size_t src = ((size_t)(t0 + i) * H + h) * kD + c;
+        const float qv = i < L ? ld_x(A.q, src, A.bf16) : 0.f, kv = i < L ? ld_x(A.k, src, A.bf16) : 0.f;
+        const float qt = qv * ex, kt = kv * ex, kh = kv * exi;
+        sQt[i][c] = qt; sKt[i][c] = kt; sKh[i][c] = kh;
+        A.Qt[tile + e] = qt; A.Kt[tile + e] = kt; A.Kh[tile + e] = kh; A.E[tile + e] = ex;
+    }
+    __syncthreads();
+    {
+        // B = strict_lower(Kt Kh^T), Aqk = lower(Qt Kh^T): one element per thread
+        float b1[1][1], b2[1][1];
+        zero(b1); zero(b2);
+        mm<kC, kC, 1, 1>(b1, &sKt[0][0], LD, 1, &sKh[0][0], 1, LD, kD);
+        mm<kC, kC, 1, 1>(b2, &sQt[0][0], LD, 1, &sKh[0][0], 1, LD, kD);
+        const int i = tid / kC, j = tid % kC;
+        const float bv = j < i ? b1[0][0] : 0.f, av = j <= i ? b2[0][0] : 0.f;
+        sB[i][j] = bv;
+        A.Bm[(size_t)item * kC * kC + tid] = bv;
+        A.Aqk[(size_t)item * kC * kC + tid] = av;
+    }
+    __syncthreads();
+    if (tid < kC) {
+        // column tid of Tm = (I + diag(beta) B)^-1 by forward substitution
+        float x[kC];
+#pragma unroll
+        for (int i = 0; i < kC; ++i) {
+            float s = 0.f;
+#pragma unroll
+            for (int j = 0; j < i; ++j) s = fmaf(sB[i][j], x[j], s);
+            x[i] = (i == tid) ? 1.f : (i < tid ? 0.f : -sBeta[i] * s);
+        }
+#pragma unroll
+        for (int i = 0; i < kC; ++i) sT[i][tid] = x[i];
+    }
+    __syncthreads();
+    A.Tm[(size_t)item * kC * kC + tid] = sT[tid / kC][tid % kC];
+    // W = Tm diag(beta) Kt, U = Tm diag(beta) V (V into sG, Kt scaled by beta in place)
+    for (int e = tid; e < kC * kD; e += kThreads) {
+        const int i = e / kD, c = e % kD;
+        sG[i][c] = i < L ? sBeta[i] * ld_x(A.v, ((size_t)(t0 + i) * H + h) * kD + c, A.bf16) : 0.f;
+        sKt[i][c] *= sBeta[i];
+    }
+    __syncthreads();
+    {
+        float w[1][8], u[1][8];
+        zero(w); zero(u);
+        mm<kC, kD, 1, 8>(w, &sT[0][0], LC, 1, &sKt[0][0], LD, 1, kC);
+        mm<kC, kD, 1, 8>(u, &sT[0][0], LC, 1, &sG[0][0], LD, 1, kC);
+        const int i = tid / (kD / 8), tn = tid % (kD / 8);
+#pragma unroll
+        for (int x = 0; x < 8; ++x) {
+            const int c = tn + (kD / 8) * x;
+            A.W[tile + i * kD + c] = w[0][x];
+            A.U[tile + i * kD + c] = u[0][x];
+        }
+    }
+}
+
+// ---- staging: 16-byte cp.async pieces, one commit group per chunk ------------------------------------
+
+__device__ __forceinline__ void cp16(void *dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)), "l"(src)
+                 : "memory");
+}
+// copies `bytes` (0 or 16) and zero-fills the rest of the 16 bytes
+__device__ __forceinline__ void cp16z(void *dst, const void *src, int bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)), "l"(src),
+                 "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+// a [kC][kD] fp32 tile (rows of 512 B) into a [kC][ld] shared tile
+__device__ __forceinline__ void stage_tile(float *dst, int ld, const float *src) {
+    for (int e = threadIdx.x; e < kC * (kD / 4); e += kThreads) {
+        const int i = e / (kD / 4), p = e % (kD / 4);
+        cp16(dst + i * ld + p * 4, src + (size_t)i * kD + p * 4);
+    }
+}
+__device__ __forceinline__ void stage_vec(float *dst, const float *src, int n) {
+    for (int e = threadIdx.x; e < n / 4; e += kThreads) cp16(dst + e * 4, src + e * 4);
+}
+
+// ---- 2. forward: the states at chunk starts -------------------------------------------------------
+
+struct FwdStage {
+    float W[kC][kD], Kh[kC][kD], U[kC][kBV], rr[kD], glr[kD];
+};
+constexpr size_t kFwdSmem = 2 * sizeof(FwdStage);
+
+__device__ __forceinline__ void stage_fwd(const CbArgs &A, FwdStage &st, size_t item, int cb) {
+    const size_t tile = item * kC * kD;
+    stage_tile(&st.W[0][0], kD, A.W + tile);
+    stage_tile(&st.Kh[0][0], kD, A.Kh + tile);
+    for (int e = threadIdx.x; e < kC * (kBV / 4); e += kThreads) {
+        const int i = e / (kBV / 4), p = e % (kBV / 4);
+        cp16(&st.U[i][p * 4], A.U + tile + (size_t)i * kD + cb + p * 4);
+    }
+    stage_vec(st.rr, A.rr + item * kD, kD);
+    stage_vec(st.glr, A.glr + item * kD, kD);
+    cp_commit();
+}
+
+__global__ void __launch_bounds__(kThreads) cb_forward_kernel(const __grid_constant__ CbArgs A) {
+    extern __shared__ __align__(16) uint8_t dyn[];
+    FwdStage *stg = reinterpret_cast<FwdStage *>(dyn);
+    __shared__ float sSp[kD][LB], sDl[kC][LB];
+    const int tid = threadIdx.x, r = tid >> 1, c0 = (tid & 1) * 8;
+    const int blk = blockIdx.x % kNV, nh = blockIdx.x / kNV, n = nh / A.H, h = nh % A.H, H = A.H;
+    const int cb = blk * kBV;
+    float S[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) S[u] = A.S0 ? A.S0[((size_t)nh * kD + r) * kD + cb + c0 + u] : 0.f;
+    const int q0 = A.chunk_off[n], nq = A.chunk_off[n + 1] - q0;
+    const int di = tid / kBV, dj = tid % kBV;          // Delta element of this thread
+    if (nq > 0) stage_fwd(A, stg[0], (size_t)q0 * H + h, cb);
+    for (int c = 0; c <= nq; ++c) {
+        float *stp = A.St + ((size_t)(q0 + c + n) * H + h) * kD * kD + (size_t)r * kD + cb + c0;
+#pragma unroll
+        for (int u = 0; u < 8; u += 4) *reinterpret_cast<float4 *>(stp + u) = make_float4(S[u], S[u + 1], S[u + 2], S[u + 3]);
+        if (c == nq) break;
+        const size_t item = (size_t)(q0 + c) * H + h;
+        if (c + 1 < nq) {
+            stage_fwd(A, stg[(c + 1) & 1], item + H, cb);
+            cp_wait<1>();
+        } else {
+            cp_wait<0>();
+        }
+        const FwdStage &st = stg[c & 1];
+        __syncthreads();                               // chunk c's tiles are in
+        const float er = expf(st.rr[r]);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            S[u] *= er;
+            sSp[r][c0 + u] = S[u];
+        }
+        __syncthreads();
+        {
+            const float *w = st.W[di];
+            float acc = 0.f;
+            for (int cc = 0; cc < kD; cc += 4) {
+                const float4 w4 = *reinterpret_cast<const float4 *>(w + cc);
+                acc = fmaf(w4.x, sSp[cc][dj], acc);
+                acc = fmaf(w4.y, sSp[cc + 1][dj], acc);
+                acc = fmaf(w4.z, sSp[cc + 2][dj], acc);
+                acc = fmaf(w4.w, sSp[cc + 3][dj], acc);
+            }
+            const float d = st.U[di][dj] - acc;
+            sDl[di][dj] = d;
+            A.Dl[item * kC * kD + (size_t)di * kD + cb + dj] = d;
+        }
+        __syncthreads();
+        float acc[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) acc[u] = S[u];
+#pragma unroll
+        for (int i = 0; i < kC; ++i) {
+            const float khv = st.Kh[i][r];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) acc[u] = fmaf(khv, sDl[i][c0 + u], acc[u]);
+        }
+        const float eg = expf(st.glr[r]);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) S[u] = eg * acc[u];
+        __syncthreads();                               // buffer c & 1 is refilled for chunk c + 2
+    }
+}
+
+// ---- 3. chain: gradients at chunk boundaries, chunks in reverse ----------------------------------
+
+struct ChainStage {
+    float Kh[kC][kD], Qt[kC][kD], Kt[kC][kD], Sn[kD][kBV];
+    float Aqk[kC][kC], Tm[kC][kC], dO[kC][kBV];
+    float rr[kD], glr[kD], beta[kC];
+};
+constexpr size_t kChainSmem = 2 * sizeof(ChainStage);
+
+__device__ __forceinline__ void stage_chain(const CbArgs &A, ChainStage &st, size_t item, int qc, int slot_next, int h,
+                                            int cb) {
+    const size_t tile = item * kC * kD, small = item * kC * kC;
+    const int t0 = A.ck_t0[qc], L = A.ck_len[qc], H = A.H;
+    stage_tile(&st.Kh[0][0], kD, A.Kh + tile);
+    stage_tile(&st.Qt[0][0], kD, A.Qt + tile);
+    stage_tile(&st.Kt[0][0], kD, A.Kt + tile);
+    const float *sn = A.St + ((size_t)slot_next * H + h) * kD * kD + cb;
+    for (int e = threadIdx.x; e < kD * (kBV / 4); e += kThreads) {
+        const int rw = e / (kBV / 4), p = e % (kBV / 4);
+        cp16(&st.Sn[rw][p * 4], sn + (size_t)rw * kD + p * 4);
+    }
+    stage_vec(&st.Aqk[0][0], A.Aqk + small, kC * kC);
+    stage_vec(&st.Tm[0][0], A.Tm + small, kC * kC);
+    for (int e = threadIdx.x; e < kC * (kBV / 4); e += kThreads) {
+        const int i = e / (kBV / 4), p = e % (kBV / 4);
+        const int ti = i < L ? t0 + i : t0;            // rows past the chunk's end are zero-filled
+        cp16z(&st.dO[i][p * 4], A.dO + ((size_t)ti * H + h) * kD + cb + p * 4, i < L ? 16 : 0);
+    }
+    stage_vec(st.rr, A.rr + item * kD, kD);
+    stage_vec(st.glr, A.glr + item * kD, kD);
+    if (threadIdx.x < kC) {
+        // beta is strided by H: 4-byte pieces
+        const int i = threadIdx.x;
+        const int ti = i < L ? t0 + i : t0;
+        asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"((uint32_t)__cvta_generic_to_shared(&st.beta[i])),
+                     "l"(A.beta + (size_t)ti * H + h), "r"(i < L ? 4 : 0)
+                     : "memory");
+    }
+    cp_commit();
+}
+
+__global__ void __launch_bounds__(kThreads) cb_chain_kernel(const __grid_constant__ CbArgs A) {
+    extern __shared__ __align__(16) uint8_t dyn[];
+    ChainStage *stg = reinterpret_cast<ChainStage *>(dyn);
+    __shared__ float sdX[kD][LB], sdD[kC][LB], sbR[kC][LB];
+    const int tid = threadIdx.x, r = tid >> 1, c0 = (tid & 1) * 8;
+    const int blk = blockIdx.x % kNV, nh = blockIdx.x / kNV, n = nh / A.H, h = nh % A.H, H = A.H;
+    const int cb = blk * kBV;
+    const float scale = A.scale;
+    float Dout[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) Dout[u] = A.dSfin ? A.dSfin[((size_t)nh * kD + r) * kD + cb + c0 + u] : 0.f;
+    const int q0 = A.chunk_off[n], nq = A.chunk_off[n + 1] - q0;
+    const int di = tid / kBV, dj = tid % kBV;
+    if (nq > 0) stage_chain(A, stg[(nq - 1) & 1], (size_t)(q0 + nq - 1) * H + h, q0 + nq - 1, q0 + nq + n, h, cb);
+    for (int c = nq - 1; c >= 0; --c) {
+        const size_t item = (size_t)(q0 + c) * H + h, tile = item * kC * kD;
+        if (c > 0) {
+            stage_chain(A, stg[(c - 1) & 1], item - H, q0 + c - 1, q0 + c + n, h, cb);
+            cp_wait<1>();
+        } else {
+            cp_wait<0>();
+        }
+        const ChainStage &st = stg[c & 1];
+        __syncthreads();                               // chunk c's tiles are in
+        // rowsum(S_next o Dout) over this CTA's columns, for dGamma of the chunk's last row
+        {
+            float p = 0.f;
+#pragma unroll
+            for (int u = 0; u < 8; ++u) p = fmaf(st.Sn[r][c0 + u], Dout[u], p);
+            p += __shfl_xor_sync(0xffffffffu, p, 1);
+            if ((tid & 1) == 0) A.dgl[(item * kNV + blk) * kD + r] = p;
+        }
+        const float eg = expf(st.glr[r]);
+        float dX[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            dX[u] = eg * Dout[u];
+            sdX[r][c0 + u] = dX[u];
+        }
+        {
+            float *dxg = A.dX + item * kD * kD + (size_t)r * kD + cb + c0;
+#pragma unroll
+            for (int u = 0; u < 8; u += 4) *reinterpret_cast<float4 *>(dxg + u) = make_float4(dX[u], dX[u + 1], dX[u + 2], dX[u + 3]);
+        }
+        __syncthreads();
+        // dDelta = Kh dX + Aqk^T dOs
+        {
+            const float *kh = st.Kh[di];
+            float acc = 0.f;
+            for (int rr = 0; rr < kD; rr += 4) {
+                const float4 k4 = *reinterpret_cast<const float4 *>(kh + rr);
+                acc = fmaf(k4.x, sdX[rr][dj], acc);
+                acc = fmaf(k4.y, sdX[rr + 1][dj], acc);
+                acc = fmaf(k4.z, sdX[rr + 2][dj], acc);
+                acc = fmaf(k4.w, sdX[rr + 3][dj], acc);
+            }
+            float a2 = 0.f;
+            for (int m = di; m < kC; ++m) a2 = fmaf(st.Aqk[m][di], st.dO[m][dj], a2);
+            sdD[di][dj] = fmaf(scale, a2, acc);
+        }
+        __syncthreads();
+        // dR = Tm^T dDelta
+        {
+            float acc = 0.f;
+            for (int m = di; m < kC; ++m) acc = fmaf(st.Tm[m][di], sdD[m][dj], acc);
+            A.dR[tile + (size_t)di * kD + cb + dj] = acc;
+            sbR[di][dj] = st.beta[di] * acc;
+        }
+        __syncthreads();
+        // Din = e^{r} (dX + Qt^T dOs - Kt^T diag(beta) dR)
+        float acc[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) acc[u] = dX[u];
+#pragma unroll
+        for (int i = 0; i < kC; ++i) {
+            const float qv = scale * st.Qt[i][r], kv = st.Kt[i][r];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) acc[u] = fmaf(qv, st.dO[i][c0 + u], fmaf(-kv, sbR[i][c0 + u], acc[u]));
+        }
+        const float er = expf(st.rr[r]);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) Dout[u] = er * acc[u];
+        __syncthreads();                               // buffer c & 1 is refilled for chunk c - 2
+    }
+    float *d0 = A.dS0 + ((size_t)nh * kD + r) * kD + cb + c0;
+#pragma unroll
+    for (int u = 0; u < 8; u += 4) *reinterpret_cast<float4 *>(d0 + u) = make_float4(Dout[u], Dout[u + 1], Dout[u + 2], Dout[u + 3]);
+}
+
+// ---- 4. grads: one CTA per (chunk, head) ------------------------------------------------------------
+
+constexpr int L4 = kD + 4;         // 16-byte aligned padded rows for float4 reads
+
+struct GradSmem {
+    float S[kD][L4], dX[kD][L4];
+    float Dl[kC][L4], dR[kC][L4], dO[kC][L4], Qt[kC][L4], Kt[kC][L4], Kh[kC][L4];
+    float dA[kC][LC], dAq[kC][LC], Bm[kC][kC];
+    float beta[kC], er[kD];
+};
+constexpr size_t kGradSmem = sizeof(GradSmem);
+
+// acc[x] += sum_k a[k] b_x[k] over k < kD, b_x = rows tn + 16 x of b (float4 reads)
+__device__ __forceinline__ void dot_rows(float (&acc)[8], const float *a, const float (*b)[L4], int tn) {
+#pragma unroll 4
+    for (int k = 0; k < kD; k += 4) {
+        const float4 a4 = *reinterpret_cast<const float4 *>(a + k);
+#pragma unroll
+        for (int x = 0; x < 8; ++x) {
+            const float4 b4 = *reinterpret_cast<const float4 *>(&b[tn + (kD / 8) * x][k]);
+            acc[x] = fmaf(a4.x, b4.x, fmaf(a4.y, b4.y, fmaf(a4.z, b4.z, fmaf(a4.w, b4.w, acc[x]))));
+        }
+    }
+}
+__device__ __forceinline__ void dot_rows2(float (&acc1)[8], float (&acc2)[8], const float *a1, const float *a2,
+                                          const float (*b)[L4], int tn) {
+#pragma unroll 2
+    for (int k = 0; k < kD; k += 4) {
+        const float4 p = *reinterpret_cast<const float4 *>(a1 + k), q = *reinterpret_cast<const float4 *>(a2 + k);
+#pragma unroll
+        for (int x = 0; x < 8; ++x) {
+            const float4 b4 = *reinterpret_cast<const float4 *>(&b[tn + (kD / 8) * x][k]);
+            acc1[x] = fmaf(p.x, b4.x, fmaf(p.y, b4.y, fmaf(p.z, b4.z, fmaf(p.w, b4.w, acc1[x]))));
+            acc2[x] = fmaf(q.x, b4.x, fmaf(q.y, b4.y, fmaf(q.z, b4.z, fmaf(q.w, b4.w, acc2[x]))));
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kThreads) cb_grad_kernel(const __grid_constant__ CbArgs A) {
+    extern __shared__ __align__(16) uint8_t dyn[];
+    GradSmem &s = *reinterpret_cast<GradSmem *>(dyn);
+    const int tid = threadIdx.x;
+    const int item = blockIdx.x, qc = item / A.H, h = item % A.H, H = A.H;
+    if (qc >= A.chunk_off[A.N]) return;
+    const int t0 = A.ck_t0[qc], L = A.ck_len[qc];
+    // the sequence of this chunk: its chunk-start state slot is qc + n
+    int n = 0;
+    while (A.chunk_off[n + 1] <= qc) ++n;
+    const size_t tile = (size_t)item * kC * kD, small = (size_t)item * kC * kC;
+    const float *St = A.St + ((size_t)(qc + n) * H + h) * kD * kD;
+    const float *dXg = A.dX + (size_t)item * kD * kD;
+    for (int e = tid; e < kD * (kD / 4); e += kThreads) {
+        const int a = e / (kD / 4), p = e % (kD / 4);
+        cp16(&s.S[a][p * 4], St + (size_t)a * kD + p * 4);
+        cp16(&s.dX[a][p * 4], dXg + (size_t)a * kD + p * 4);
+    }
+    stage_tile(&s.Dl[0][0], L4, A.Dl + tile);
+    stage_tile(&s.dR[0][0], L4, A.dR + tile);
+    stage_tile(&s.Qt[0][0], L4, A.Qt + tile);
+    stage_tile(&s.Kt[0][0], L4, A.Kt + tile);
+    stage_tile(&s.Kh[0][0], L4, A.Kh + tile);
+    for (int e = tid; e < kC * (kD / 4); e += kThreads) {
+        const int i = e / (kD / 4), p = e % (kD / 4);
+        const int ti = i < L ? t0 + i : t0;
+        cp16z(&s.dO[i][p * 4], A.dO + ((size_t)ti * H + h) * kD + p * 4, i < L ? 16 : 0);
+    }
+    stage_vec(&s.Bm[0][0], A.Bm + small, kC * kC);
+    cp_commit();
+    if (tid < kC) s.beta[tid] = tid < L ? A.beta[(size_t)(t0 + tid) * H + h] : 0.f;
+    if (tid < kD) s.er[tid] = expf(A.rr[(size_t)item * kD + tid]);
+    cp_wait<0>();
+    __syncthreads();
+    const float scale = A.scale;
+    {
+        // dA = -strict_lower(dR Delta^T), dAqk = lower(dOs Delta^T): one element per thread
+        const int i = tid / kC, j = tid % kC;
+        float a1 = 0.f, a2 = 0.f;
+#pragma unroll 4
+        for (int k = 0; k < kD; k += 4) {
+            const float4 d4 = *reinterpret_cast<const float4 *>(&s.Dl[j][k]);
+            const float4 r4 = *reinterpret_cast<const float4 *>(&s.dR[i][k]);
+            const float4 o4 = *reinterpret_cast<const float4 *>(&s.dO[i][k]);
+            a1 = fmaf(r4.x, d4.x, fmaf(r4.y, d4.y, fmaf(r4.z, d4.z, fmaf(r4.w, d4.w, a1))));
+            a2 = fmaf(o4.x, d4.x, fmaf(o4.y, d4.y, fmaf(o4.z, d4.z, fmaf(o4.w, d4.w, a2))));
+        }
+        s.dA[i][j] = j < i ? -a1 : 0.f;
+        s.dAq[i][j] = j <= i ? scale * a2 : 0.f;
+    }
+    __syncthreads();
+    const int i = tid / (kD / 8), tn = tid % (kD / 8);    // row i, columns tn + 16 x
+    const float bi = s.beta[i];
+    float y[8], dqt[8], dkt[8], dkh[8];
+#pragma unroll
+    for (int x = 0; x < 8; ++x) y[x] = dqt[x] = dkt[x] = dkh[x] = 0.f;
+    // Y = dR S'^T and dO S'^T (S' = e^{r} S: the column factor is applied after the sums)
+    dot_rows2(y, dqt, s.dR[i], s.dO[i], s.S, tn);
+    // dKh = Delta dX^T + ...
+    dot_rows(dkh, s.Dl[i], s.dX, tn);
+#pragma unroll
+    for (int x = 0; x < 8; ++x) {
+        const float f = s.er[tn + (kD / 8) * x];
+        y[x] *= f;
+        dqt[x] *= scale * f;
+    }
+    // + dAqk Kh, dA Kh, dAqk^T Qt, dA^T diag(beta) Kt  (K = kC)
+#pragma unroll
+    for (int m = 0; m < kC; ++m) {
+        const float aq = s.dAq[i][m], ad = s.dA[i][m], aqt = s.dAq[m][i], adt = s.dA[m][i] * s.beta[m];
+#pragma unroll
+        for (int x = 0; x < 8; ++x) {
+            const int c = tn + (kD / 8) * x;
+            const float kh = s.Kh[m][c];
+            dqt[x] = fmaf(aq, kh, dqt[x]);
+            dkt[x] = fmaf(ad, kh, dkt[x]);
+            dkh[x] = fmaf(aqt, s.Qt[m][c], fmaf(adt, s.Kt[m][c], dkh[x]));
+        }
+    }
+    // dbeta: rowsum(v o dR) - rowsum(Kt o Y) + rowsum(dA o B); dv = beta dR
+    float pb = 0.f;
+    const size_t row = ((size_t)(t0 + i) * H + h) * kD;
+    float dgm[8];
+#pragma unroll
+    for (int x = 0; x < 8; ++x) {
+        const int c = tn + (kD / 8) * x;
+        const float dr = s.dR[i][c], kt = s.Kt[i][c];
+        const float vv = i < L ? ld_x(A.v, row + c, A.bf16) : 0.f;
+        pb += vv * dr - kt * y[x];
+        dkt[x] = bi * (dkt[x] - y[x]);
+        const float ex = A.E[tile + (size_t)i * kD + c];
+        if (i < L) {
+            A.dv[row + c] = bi * dr;
+            A.dq[row + c] = dqt[x] * ex;
+            A.dk[row + c] = dkt[x] * ex + dkh[x] / ex;
+        }
+        dgm[x] = dqt[x] * s.Qt[i][c] + dkt[x] * kt - dkh[x] * s.Kh[i][c];
+    }
+    // sum pb over the row's 16 threads (consecutive lanes of one half-warp)
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) pb += __shfl_xor_sync(0xffffffffu, pb, o);
+    __syncthreads();                                   // S free: dGamma goes there
+    float (*dG)[L4] = s.S;
+#pragma unroll
+    for (int x = 0; x < 8; ++x) dG[i][tn + (kD / 8) * x] = dgm[x];
+    if (tn == 0) {
+        float ab = 0.f;
+        for (int j = 0; j < i; ++j) ab = fmaf(s.dA[i][j], s.Bm[i][j], ab);
+        if (i < L) A.dbeta[(size_t)(t0 + i) * H + h] = pb + ab;
+    }
+    __syncthreads();
+    if (tid < kD) {
+        float gl = 0.f;
+        for (int b = 0; b < kNV; ++b) gl += A.dgl[((size_t)item * kNV + b) * kD + tid];
+        dG[L - 1][tid] += gl;
+        float run = 0.f;
+        for (int ii = L - 1; ii >= 0; --ii) {
+            run += dG[ii][tid];
+            A.dg[((size_t)(t0 + ii) * H + h) * kD + tid] = run;
+        }
+    }
+}
+
+size_t r256(size_t b) { return (b + 255) & ~size_t(255); }
+
+struct Layout {
+    size_t off_chunk, ck_t0, ck_len, Qt, Kt, Kh, E, W, U, Tm, Aqk, Bm, rr, glr, Dl, dR, dX, dgl, St, total;
+};
+
+Layout layout(int N, int T, int H) {
+    const size_t Q = ((size_t)T + (size_t)(kC - 1) * (size_t)N) / kC + 1;
+    const size_t NI = Q * (size_t)H;
+    Layout l;
+    size_t o = 0;
+    auto take = [&](size_t bytes) { const size_t at = o; o += r256(bytes); return at; };
+    l.off_chunk = take((size_t)(N + 1) * 4);
+    l.ck_t0 = take(Q * 4);
+    l.ck_len = take(Q * 4);
+    const size_t tb = NI * kC * kD * 4, sb = NI * kC * kC * 4, vb = NI * kD * 4;
+    l.Qt = take(tb); l.Kt = take(tb); l.Kh = take(tb); l.E = take(tb); l.W = take(tb); l.U = take(tb);
+    l.Tm = take(sb); l.Aqk = take(sb); l.Bm = take(sb);
+    l.rr = take(vb); l.glr = take(vb);
+    l.Dl = take(tb); l.dR = take(tb);
+    l.dX = take(NI * kD * kD * 4);
+    l.dgl = take(NI * kNV * kD * 4);
+    l.St = take((Q + N) * (size_t)H * kD * kD * 4);
+    l.total = o;
+    return l;
+}
+
+std::atomic<uint64_t> g_grad_attr{0}, g_fwd_attr{0}, g_chain_attr{0};
+
+}  // namespace
+
+size_t backward_chunked_workspace(int N, int T, int H) { return layout(N, T, H).total; }
+
+cudaError_t launch_backward_chunked(const void *q, const void *k, const void *v, int bf16, const float *g,
+                                    const float *beta, const float *S0, const int32_t *cu, int N, int T, int H,
+                                    float scale, const float *dO, const float *dSfin, float *dq, float *dk, float *dv,
+                                    float *dg, float *dbeta, float *dS0, void *ws, cudaStream_t s) {
+    cudaError_t e;
+    if (T == 0) {
+        // no tokens: dS0 = dS_final (or zero)
+        const size_t sb = (size_t)N * H * kD * kD * sizeof(float);
+        if (dSfin) return cudaMemcpyAsync(dS0, dSfin, sb, cudaMemcpyDeviceToDevice, s);
+        return cudaMemsetAsync(dS0, 0, sb, s);
+    }
+    const Layout l = layout(N, T, H);
+    char *w = static_cast<char *>(ws);
+    CbArgs A;
+    A.q = q; A.k = k; A.v = v; A.bf16 = bf16; A.g = g; A.beta = beta; A.S0 = S0; A.dO = dO; A.dSfin = dSfin;
+    A.cu = cu; A.N = N; A.T = T; A.H = H; A.scale = scale;
+    A.Q = (int)(((size_t)T + (size_t)(kC - 1) * (size_t)N) / kC);
+    A.chunk_off = reinterpret_cast<int32_t *>(w + l.off_chunk);
+    A.ck_t0 = reinterpret_cast<int32_t *>(w + l.ck_t0);
+    A.ck_len = reinterpret_cast<int32_t *>(w + l.ck_len);
+    auto f = [&](size_t off) { return reinterpret_cast<float *>(w + off); };
+    A.Qt = f(l.Qt); A.Kt = f(l.Kt); A.Kh = f(l.Kh); A.E = f(l.E); A.W = f(l.W); A.U = f(l.U);
+    A.Tm = f(l.Tm); A.Aqk = f(l.Aqk); A.Bm = f(l.Bm); A.rr = f(l.rr); A.glr = f(l.glr);
+    A.Dl = f(l.Dl); A.dR = f(l.dR); A.dX = f(l.dX); A.dgl = f(l.dgl); A.St = f(l.St);
+    A.dq = dq; A.dk = dk; A.dv = dv; A.dg = dg; A.dbeta = dbeta; A.dS0 = dS0;
+    // chunk enumeration from the device cu_seqlens; the item grids cover the upper bound A.Q of
+    // the chunk count and CTAs past the real chunks return at once
+    cb_offsets_kernel<<<1, 32, 0, s>>>(A);
+    count_launch();
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    const unsigned items = (unsigned)((size_t)A.Q * H), chains = (unsigned)((size_t)N * H * kNV);
+    cb_prep_kernel<<<items, kThreads, 0, s>>>(A);
+    count_launch();
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (chains) {
+        if ((e = smem_attr_once((const void *)cb_forward_kernel, (int)kFwdSmem, g_fwd_attr)) != cudaSuccess) return e;
+        if ((e = smem_attr_once((const void *)cb_chain_kernel, (int)kChainSmem, g_chain_attr)) != cudaSuccess) return e;
+        cb_forward_kernel<<<chains, kThreads, kFwdSmem, s>>>(A);
+        count_launch();
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        cb_chain_kernel<<<chains, kThreads, kChainSmem, s>>>(A);
+        count_launch();
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    if ((e = smem_attr_once((const void *)cb_grad_kernel, (int)kGradSmem, g_grad_attr)) != cudaSuccess) return e;
+    cb_grad_kernel<<<items, kThreads, kGradSmem, s>>>(A);
+    count_launch();
+    return cudaGetLastError();
+}
+
+}  // namespace k3kda

@@ -121,6 +121,13 @@ cudaError_t launch_backward(const void *q, const void *k, const void *v, int bf1
                             const float *dSfin, float *dq, float *dk, float *dv, float *dg, float *dbeta, float *dS0,
                             void *ws, cudaStream_t s);
 
+// the same gradients in chunked form (csrc/backward_chunked.cu); dk = dv = 128
+size_t backward_chunked_workspace(int N, int T, int H);
+cudaError_t launch_backward_chunked(const void *q, const void *k, const void *v, int bf16, const float *g,
+                                    const float *beta, const float *S0, const int32_t *cu, int N, int T, int H,
+                                    float scale, const float *dO, const float *dSfin, float *dq, float *dk, float *dv,
+                                    float *dg, float *dbeta, float *dS0, void *ws, cudaStream_t s);
+
 // one decode token of the gated attention layers (csrc/mla_decode.cu); d in {64, 128, 256}
 size_t mla_splits(int L_max);
 size_t mla_workspace(int N, int H, int d, int L_max);
