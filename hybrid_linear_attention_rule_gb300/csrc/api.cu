@@ -256,8 +256,8 @@ int k3kda_backward(const void *q, const void *k, const void *v, int in_dtype, co
     if (!dS0) return K3KDA_ERR_INVALID_ARG;
     if (cu_seqlens == nullptr && N != 1) return K3KDA_ERR_INVALID_ARG;
     if (cu_seqlens_host && !cu_ok(cu_seqlens_host, N, T)) return K3KDA_ERR_INVALID_ARG;
-    // grids: (chunks of 16 tokens) x H items and N x H x 8 column blocks
-    if ((long long)N * H * 8 > 0x7fffffffLL || ((long long)T / 16 + N + 1) * H > 0x7fffffffLL)
+    // grids: 2 x (chunks of 16 tokens) x H items and N x H x 8 column blocks
+    if ((long long)N * H * 8 > 0x7fffffffLL || 2 * ((long long)T / 16 + N + 1) * H > 0x7fffffffLL)
         return K3KDA_ERR_UNSUPPORTED;
     for (const void *p : {q, k, v, (const void *)g, (const void *)initial_state, (const void *)dO,
                           (const void *)dS_final, (const void *)dq, (const void *)dk_out, (const void *)dv_out,

@@ -22,8 +22,10 @@
 //   dg = the in-chunk suffix sum of dGamma.
 // (r cancels from every output, so it is held constant.)  Four launches:
 //   1. prep    one CTA per (chunk, head): the tiles above, Tm by forward substitution;
-//   2. forward one CTA per (sequence, head, 16-column block of dv): the states at chunk starts;
-//   3. chain   same grid, chunks in reverse: dX, dR and Din, with dS0 at the sequence start;
+//   2. forward one CTA per (sequence, head, 32-column block of dv): the states at chunk starts;
+//   3. chain   one CTA per (sequence, head, 16-column block), chunks in reverse: dX, dR and Din,
+//              with dS0 at the sequence start; it needs no forward state, so 2 and 3 are one
+//              launch whose CTAs run side by side;
 //   4. grads   one CTA per (chunk, head): dq, dk, dv, dg, dbeta.
 // Everything runs in fp32 on CUDA cores.  Chunks of 16 tokens keep e^{+-G'} small, so the
 // cancellations in dGamma stay at fp32 rounding level.
@@ -61,7 +63,6 @@ struct CbArgs {
     float *rr, *glr;                   // [item][kD]
     float *Dl, *dR;                    // [item][kC][kD]
     float *dX;                         // [item][kD][kD]
-    float *dgl;                        // [item][kNV][kD]
     float *St;                         // [(Q + N) * H][kD][kD]: state at each chunk start, then the final
     float *dq, *dk, *dv, *dg, *dbeta, *dS0;
 };
@@ -230,17 +231,19 @@ __device__ __forceinline__ void stage_vec(float *dst, const float *src, int n) {
 
 // ---- 2. forward: the states at chunk starts -------------------------------------------------------
 
+constexpr int kFV = 32;                                // dv columns of a forward-chain CTA
+constexpr int kFN = kD / kFV;
 struct FwdStage {
-    float W[kC][kD], Kh[kC][kD], U[kC][kBV], rr[kD], glr[kD];
+    float W[kC][kD], Kh[kC][kD], U[kC][kFV], rr[kD], glr[kD];
 };
-constexpr size_t kFwdSmem = 2 * sizeof(FwdStage);
+constexpr int kFS = 2;                                 // forward chain: stages in the ring
 
 __device__ __forceinline__ void stage_fwd(const CbArgs &A, FwdStage &st, size_t item, int cb) {
     const size_t tile = item * kC * kD;
     stage_tile(&st.W[0][0], kD, A.W + tile);
     stage_tile(&st.Kh[0][0], kD, A.Kh + tile);
-    for (int e = threadIdx.x; e < kC * (kBV / 4); e += kThreads) {
-        const int i = e / (kBV / 4), p = e % (kBV / 4);
+    for (int e = threadIdx.x; e < kC * (kFV / 4); e += kThreads) {
+        const int i = e / (kFV / 4), p = e % (kFV / 4);
         cp16(&st.U[i][p * 4], A.U + tile + (size_t)i * kD + cb + p * 4);
     }
     stage_vec(st.rr, A.rr + item * kD, kD);
@@ -248,92 +251,95 @@ __device__ __forceinline__ void stage_fwd(const CbArgs &A, FwdStage &st, size_t 
     cp_commit();
 }
 
-__global__ void __launch_bounds__(kThreads) cb_forward_kernel(const __grid_constant__ CbArgs A) {
-    extern __shared__ __align__(16) uint8_t dyn[];
-    FwdStage *stg = reinterpret_cast<FwdStage *>(dyn);
-    __shared__ float sSp[kD][LB], sDl[kC][LB];
-    const int tid = threadIdx.x, r = tid >> 1, c0 = (tid & 1) * 8;
-    const int blk = blockIdx.x % kNV, nh = blockIdx.x / kNV, n = nh / A.H, h = nh % A.H, H = A.H;
-    const int cb = blk * kBV;
-    float S[8];
+struct FwdSmem {
+    FwdStage stg[kFS];
+    float sSp[kD][kFV + 1], sDl[kC][kFV + 1];
+};
+
+__device__ __forceinline__ void forward_chain(const CbArgs &A, uint8_t *dyn, int bid) {
+    FwdSmem &fs = *reinterpret_cast<FwdSmem *>(dyn);
+    FwdStage *stg = fs.stg;
+    float (*sSp)[kFV + 1] = fs.sSp;
+    float (*sDl)[kFV + 1] = fs.sDl;
+    // thread: row r, 16 columns; Delta elements (di, dj) and (di, dj + 1)
+    const int tid = threadIdx.x, r = tid >> 1, c0 = (tid & 1) * 16;
+    const int blk = bid % kFN, nh = bid / kFN, n = nh / A.H, h = nh % A.H, H = A.H;
+    const int cb = blk * kFV;
+    float S[16];
 #pragma unroll
-    for (int u = 0; u < 8; ++u) S[u] = A.S0 ? A.S0[((size_t)nh * kD + r) * kD + cb + c0 + u] : 0.f;
+    for (int u = 0; u < 16; ++u) S[u] = A.S0 ? A.S0[((size_t)nh * kD + r) * kD + cb + c0 + u] : 0.f;
     const int q0 = A.chunk_off[n], nq = A.chunk_off[n + 1] - q0;
-    const int di = tid / kBV, dj = tid % kBV;          // Delta element of this thread
-    if (nq > 0) stage_fwd(A, stg[0], (size_t)q0 * H + h, cb);
+    const int di = tid / 16, dj = (tid % 16) * 2;
+    // one commit group per chunk (empty past the end), kFS - 1 chunks ahead
+    for (int d = 0; d < kFS - 1; ++d) {
+        if (d < nq) stage_fwd(A, stg[d], (size_t)(q0 + d) * H + h, cb);
+        else cp_commit();
+    }
     for (int c = 0; c <= nq; ++c) {
         float *stp = A.St + ((size_t)(q0 + c + n) * H + h) * kD * kD + (size_t)r * kD + cb + c0;
 #pragma unroll
-        for (int u = 0; u < 8; u += 4) *reinterpret_cast<float4 *>(stp + u) = make_float4(S[u], S[u + 1], S[u + 2], S[u + 3]);
+        for (int u = 0; u < 16; u += 4) *reinterpret_cast<float4 *>(stp + u) = make_float4(S[u], S[u + 1], S[u + 2], S[u + 3]);
         if (c == nq) break;
         const size_t item = (size_t)(q0 + c) * H + h;
-        if (c + 1 < nq) {
-            stage_fwd(A, stg[(c + 1) & 1], item + H, cb);
-            cp_wait<1>();
-        } else {
-            cp_wait<0>();
-        }
-        const FwdStage &st = stg[c & 1];
+        if (c + kFS - 1 < nq) stage_fwd(A, stg[(c + kFS - 1) % kFS], item + (size_t)(kFS - 1) * H, cb);
+        else cp_commit();
+        cp_wait<kFS - 1>();
+        const FwdStage &st = stg[c % kFS];
         __syncthreads();                               // chunk c's tiles are in
         const float er = expf(st.rr[r]);
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
+        for (int u = 0; u < 16; ++u) {
             S[u] *= er;
             sSp[r][c0 + u] = S[u];
         }
         __syncthreads();
         {
             const float *w = st.W[di];
-            float acc = 0.f;
+            float a0 = 0.f, a1 = 0.f;
             for (int cc = 0; cc < kD; cc += 4) {
                 const float4 w4 = *reinterpret_cast<const float4 *>(w + cc);
-                acc = fmaf(w4.x, sSp[cc][dj], acc);
-                acc = fmaf(w4.y, sSp[cc + 1][dj], acc);
-                acc = fmaf(w4.z, sSp[cc + 2][dj], acc);
-                acc = fmaf(w4.w, sSp[cc + 3][dj], acc);
+                a0 = fmaf(w4.x, sSp[cc][dj], a0);         a1 = fmaf(w4.x, sSp[cc][dj + 1], a1);
+                a0 = fmaf(w4.y, sSp[cc + 1][dj], a0);     a1 = fmaf(w4.y, sSp[cc + 1][dj + 1], a1);
+                a0 = fmaf(w4.z, sSp[cc + 2][dj], a0);     a1 = fmaf(w4.z, sSp[cc + 2][dj + 1], a1);
+                a0 = fmaf(w4.w, sSp[cc + 3][dj], a0);     a1 = fmaf(w4.w, sSp[cc + 3][dj + 1], a1);
             }
-            const float d = st.U[di][dj] - acc;
-            sDl[di][dj] = d;
-            A.Dl[item * kC * kD + (size_t)di * kD + cb + dj] = d;
+            const float d0 = st.U[di][dj] - a0, d1 = st.U[di][dj + 1] - a1;
+            sDl[di][dj] = d0;
+            sDl[di][dj + 1] = d1;
+            *reinterpret_cast<float2 *>(A.Dl + item * kC * kD + (size_t)di * kD + cb + dj) = make_float2(d0, d1);
         }
         __syncthreads();
-        float acc[8];
+        float acc[16];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) acc[u] = S[u];
+        for (int u = 0; u < 16; ++u) acc[u] = S[u];
 #pragma unroll
         for (int i = 0; i < kC; ++i) {
             const float khv = st.Kh[i][r];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) acc[u] = fmaf(khv, sDl[i][c0 + u], acc[u]);
+            for (int u = 0; u < 16; ++u) acc[u] = fmaf(khv, sDl[i][c0 + u], acc[u]);
         }
         const float eg = expf(st.glr[r]);
 #pragma unroll
-        for (int u = 0; u < 8; ++u) S[u] = eg * acc[u];
-        __syncthreads();                               // buffer c & 1 is refilled for chunk c + 2
+        for (int u = 0; u < 16; ++u) S[u] = eg * acc[u];
+        __syncthreads();                               // buffer c % kFS is refilled for chunk c + kFS
     }
 }
 
 // ---- 3. chain: gradients at chunk boundaries, chunks in reverse ----------------------------------
 
 struct ChainStage {
-    float Kh[kC][kD], Qt[kC][kD], Kt[kC][kD], Sn[kD][kBV];
+    float Kh[kC][kD], Qt[kC][kD], Kt[kC][kD];
     float Aqk[kC][kC], Tm[kC][kC], dO[kC][kBV];
     float rr[kD], glr[kD], beta[kC];
 };
-constexpr size_t kChainSmem = 2 * sizeof(ChainStage);
+constexpr int kCS = 2;                                 // backward chain: stages in the ring
 
-__device__ __forceinline__ void stage_chain(const CbArgs &A, ChainStage &st, size_t item, int qc, int slot_next, int h,
-                                            int cb) {
+__device__ __forceinline__ void stage_chain(const CbArgs &A, ChainStage &st, size_t item, int qc, int h, int cb) {
     const size_t tile = item * kC * kD, small = item * kC * kC;
     const int t0 = A.ck_t0[qc], L = A.ck_len[qc], H = A.H;
     stage_tile(&st.Kh[0][0], kD, A.Kh + tile);
     stage_tile(&st.Qt[0][0], kD, A.Qt + tile);
     stage_tile(&st.Kt[0][0], kD, A.Kt + tile);
-    const float *sn = A.St + ((size_t)slot_next * H + h) * kD * kD + cb;
-    for (int e = threadIdx.x; e < kD * (kBV / 4); e += kThreads) {
-        const int rw = e / (kBV / 4), p = e % (kBV / 4);
-        cp16(&st.Sn[rw][p * 4], sn + (size_t)rw * kD + p * 4);
-    }
     stage_vec(&st.Aqk[0][0], A.Aqk + small, kC * kC);
     stage_vec(&st.Tm[0][0], A.Tm + small, kC * kC);
     for (int e = threadIdx.x; e < kC * (kBV / 4); e += kThreads) {
@@ -354,12 +360,19 @@ __device__ __forceinline__ void stage_chain(const CbArgs &A, ChainStage &st, siz
     cp_commit();
 }
 
-__global__ void __launch_bounds__(kThreads) cb_chain_kernel(const __grid_constant__ CbArgs A) {
-    extern __shared__ __align__(16) uint8_t dyn[];
-    ChainStage *stg = reinterpret_cast<ChainStage *>(dyn);
-    __shared__ float sdX[kD][LB], sdD[kC][LB], sbR[kC][LB];
+struct ChainSmem {
+    ChainStage stg[kCS];
+    float sdX[kD][LB], sdD[kC][LB], sbR[kC][LB];
+};
+
+__device__ __forceinline__ void backward_chain(const CbArgs &A, uint8_t *dyn, int bid) {
+    ChainSmem &cs = *reinterpret_cast<ChainSmem *>(dyn);
+    ChainStage *stg = cs.stg;
+    float (*sdX)[LB] = cs.sdX;
+    float (*sdD)[LB] = cs.sdD;
+    float (*sbR)[LB] = cs.sbR;
     const int tid = threadIdx.x, r = tid >> 1, c0 = (tid & 1) * 8;
-    const int blk = blockIdx.x % kNV, nh = blockIdx.x / kNV, n = nh / A.H, h = nh % A.H, H = A.H;
+    const int blk = bid % kNV, nh = bid / kNV, n = nh / A.H, h = nh % A.H, H = A.H;
     const int cb = blk * kBV;
     const float scale = A.scale;
     float Dout[8];
@@ -367,25 +380,23 @@ __global__ void __launch_bounds__(kThreads) cb_chain_kernel(const __grid_constan
     for (int u = 0; u < 8; ++u) Dout[u] = A.dSfin ? A.dSfin[((size_t)nh * kD + r) * kD + cb + c0 + u] : 0.f;
     const int q0 = A.chunk_off[n], nq = A.chunk_off[n + 1] - q0;
     const int di = tid / kBV, dj = tid % kBV;
-    if (nq > 0) stage_chain(A, stg[(nq - 1) & 1], (size_t)(q0 + nq - 1) * H + h, q0 + nq - 1, q0 + nq + n, h, cb);
-    for (int c = nq - 1; c >= 0; --c) {
+    // chunk j of the sweep is c = nq - 1 - j; one commit group per chunk (empty past the end)
+    for (int d = 0; d < kCS - 1; ++d) {
+        const int cc = nq - 1 - d;
+        if (cc >= 0) stage_chain(A, stg[d], (size_t)(q0 + cc) * H + h, q0 + cc, h, cb);
+        else cp_commit();
+    }
+    for (int j = 0; j < nq; ++j) {
+        const int c = nq - 1 - j;
         const size_t item = (size_t)(q0 + c) * H + h, tile = item * kC * kD;
-        if (c > 0) {
-            stage_chain(A, stg[(c - 1) & 1], item - H, q0 + c - 1, q0 + c + n, h, cb);
-            cp_wait<1>();
-        } else {
-            cp_wait<0>();
-        }
-        const ChainStage &st = stg[c & 1];
-        __syncthreads();                               // chunk c's tiles are in
-        // rowsum(S_next o Dout) over this CTA's columns, for dGamma of the chunk's last row
         {
-            float p = 0.f;
-#pragma unroll
-            for (int u = 0; u < 8; ++u) p = fmaf(st.Sn[r][c0 + u], Dout[u], p);
-            p += __shfl_xor_sync(0xffffffffu, p, 1);
-            if ((tid & 1) == 0) A.dgl[(item * kNV + blk) * kD + r] = p;
+            const int cc = c - (kCS - 1);
+            if (cc >= 0) stage_chain(A, stg[(j + kCS - 1) % kCS], (size_t)(q0 + cc) * H + h, q0 + cc, h, cb);
+            else cp_commit();
         }
+        cp_wait<kCS - 1>();
+        const ChainStage &st = stg[j % kCS];
+        __syncthreads();                               // chunk c's tiles are in
         const float eg = expf(st.glr[r]);
         float dX[8];
 #pragma unroll
@@ -436,74 +447,95 @@ __global__ void __launch_bounds__(kThreads) cb_chain_kernel(const __grid_constan
         const float er = expf(st.rr[r]);
 #pragma unroll
         for (int u = 0; u < 8; ++u) Dout[u] = er * acc[u];
-        __syncthreads();                               // buffer c & 1 is refilled for chunk c - 2
+        __syncthreads();                               // buffer j % kCS is refilled for chunk c - kCS
     }
     float *d0 = A.dS0 + ((size_t)nh * kD + r) * kD + cb + c0;
 #pragma unroll
     for (int u = 0; u < 8; u += 4) *reinterpret_cast<float4 *>(d0 + u) = make_float4(Dout[u], Dout[u + 1], Dout[u + 2], Dout[u + 3]);
 }
 
-// ---- 4. grads: one CTA per (chunk, head) ------------------------------------------------------------
+// Both chains in one launch: CTAs [0, N H kFN) run the forward chain, the rest the backward
+// chain.  The two share no data, and one grid lets them run side by side (three CTAs fit on an SM).
+constexpr size_t kChainsSmem = sizeof(FwdSmem) > sizeof(ChainSmem) ? sizeof(FwdSmem) : sizeof(ChainSmem);
 
+__global__ void __launch_bounds__(kThreads) cb_chains_kernel(const __grid_constant__ CbArgs A, int fchains) {
+    extern __shared__ __align__(16) uint8_t dyn[];
+    if ((int)blockIdx.x < fchains) forward_chain(A, dyn, blockIdx.x);
+    else backward_chain(A, dyn, blockIdx.x - fchains);
+}
+
+// ---- 4. grads: two CTAs per (chunk, head), one per half of the dk columns --------------------------
+// Every product below that runs over dk (dQt, dKt, dKh and so dq, dk, dg) needs, for output
+// column c, only row c of S and of dX, so a CTA holds half of each and two CTAs share an SM.
+// dbeta sums over dk: each half adds its share into the zeroed output.
+
+constexpr int kHC = kD / 2;        // dk columns of one grads CTA
 constexpr int L4 = kD + 4;         // 16-byte aligned padded rows for float4 reads
+constexpr int LH = kHC + 4;
 
 struct GradSmem {
-    float S[kD][L4], dX[kD][L4];
-    float Dl[kC][L4], dR[kC][L4], dO[kC][L4], Qt[kC][L4], Kt[kC][L4], Kh[kC][L4];
+    float S[kHC][L4], dX[kHC][L4];                 // rows c of this half
+    float Dl[kC][L4], dR[kC][L4], dO[kC][L4];
+    float Qt[kC][LH], Kt[kC][LH], Kh[kC][LH];      // this half's columns
     float dA[kC][LC], dAq[kC][LC], Bm[kC][kC];
-    float beta[kC], er[kD];
+    float beta[kC], er[kHC];
 };
 constexpr size_t kGradSmem = sizeof(GradSmem);
 
-// acc[x] += sum_k a[k] b_x[k] over k < kD, b_x = rows tn + 16 x of b (float4 reads)
-__device__ __forceinline__ void dot_rows(float (&acc)[8], const float *a, const float (*b)[L4], int tn) {
+// acc[x] += sum_k a1[k] b_x[k] (and a2), k < kD, b_x = row tn + 16 x of b (float4 reads)
+__device__ __forceinline__ void dot4(float (&acc)[4], const float *a, const float (*b)[L4], int tn) {
 #pragma unroll 4
     for (int k = 0; k < kD; k += 4) {
         const float4 a4 = *reinterpret_cast<const float4 *>(a + k);
 #pragma unroll
-        for (int x = 0; x < 8; ++x) {
-            const float4 b4 = *reinterpret_cast<const float4 *>(&b[tn + (kD / 8) * x][k]);
+        for (int x = 0; x < 4; ++x) {
+            const float4 b4 = *reinterpret_cast<const float4 *>(&b[tn + 16 * x][k]);
             acc[x] = fmaf(a4.x, b4.x, fmaf(a4.y, b4.y, fmaf(a4.z, b4.z, fmaf(a4.w, b4.w, acc[x]))));
         }
     }
 }
-__device__ __forceinline__ void dot_rows2(float (&acc1)[8], float (&acc2)[8], const float *a1, const float *a2,
-                                          const float (*b)[L4], int tn) {
-#pragma unroll 2
+__device__ __forceinline__ void dot4x2(float (&acc1)[4], float (&acc2)[4], const float *a1, const float *a2,
+                                       const float (*b)[L4], int tn) {
+#pragma unroll 4
     for (int k = 0; k < kD; k += 4) {
         const float4 p = *reinterpret_cast<const float4 *>(a1 + k), q = *reinterpret_cast<const float4 *>(a2 + k);
 #pragma unroll
-        for (int x = 0; x < 8; ++x) {
-            const float4 b4 = *reinterpret_cast<const float4 *>(&b[tn + (kD / 8) * x][k]);
+        for (int x = 0; x < 4; ++x) {
+            const float4 b4 = *reinterpret_cast<const float4 *>(&b[tn + 16 * x][k]);
             acc1[x] = fmaf(p.x, b4.x, fmaf(p.y, b4.y, fmaf(p.z, b4.z, fmaf(p.w, b4.w, acc1[x]))));
             acc2[x] = fmaf(q.x, b4.x, fmaf(q.y, b4.y, fmaf(q.z, b4.z, fmaf(q.w, b4.w, acc2[x]))));
         }
     }
 }
 
-__global__ void __launch_bounds__(kThreads) cb_grad_kernel(const __grid_constant__ CbArgs A) {
+__global__ void __launch_bounds__(kThreads, 2) cb_grad_kernel(const __grid_constant__ CbArgs A) {
     extern __shared__ __align__(16) uint8_t dyn[];
     GradSmem &s = *reinterpret_cast<GradSmem *>(dyn);
     const int tid = threadIdx.x;
-    const int item = blockIdx.x, qc = item / A.H, h = item % A.H, H = A.H;
+    const int half = blockIdx.x & 1, item = blockIdx.x >> 1, qc = item / A.H, h = item % A.H, H = A.H;
     if (qc >= A.chunk_off[A.N]) return;
     const int t0 = A.ck_t0[qc], L = A.ck_len[qc];
+    const int cbase = half * kHC;
     // the sequence of this chunk: its chunk-start state slot is qc + n
     int n = 0;
     while (A.chunk_off[n + 1] <= qc) ++n;
     const size_t tile = (size_t)item * kC * kD, small = (size_t)item * kC * kC;
-    const float *St = A.St + ((size_t)(qc + n) * H + h) * kD * kD;
-    const float *dXg = A.dX + (size_t)item * kD * kD;
-    for (int e = tid; e < kD * (kD / 4); e += kThreads) {
+    const float *St = A.St + ((size_t)(qc + n) * H + h) * kD * kD + (size_t)cbase * kD;
+    const float *dXg = A.dX + (size_t)item * kD * kD + (size_t)cbase * kD;
+    for (int e = tid; e < kHC * (kD / 4); e += kThreads) {
         const int a = e / (kD / 4), p = e % (kD / 4);
         cp16(&s.S[a][p * 4], St + (size_t)a * kD + p * 4);
         cp16(&s.dX[a][p * 4], dXg + (size_t)a * kD + p * 4);
     }
     stage_tile(&s.Dl[0][0], L4, A.Dl + tile);
     stage_tile(&s.dR[0][0], L4, A.dR + tile);
-    stage_tile(&s.Qt[0][0], L4, A.Qt + tile);
-    stage_tile(&s.Kt[0][0], L4, A.Kt + tile);
-    stage_tile(&s.Kh[0][0], L4, A.Kh + tile);
+    for (int e = tid; e < kC * (kHC / 4); e += kThreads) {
+        const int i = e / (kHC / 4), p = e % (kHC / 4);
+        const size_t o = tile + (size_t)i * kD + cbase + p * 4;
+        cp16(&s.Qt[i][p * 4], A.Qt + o);
+        cp16(&s.Kt[i][p * 4], A.Kt + o);
+        cp16(&s.Kh[i][p * 4], A.Kh + o);
+    }
     for (int e = tid; e < kC * (kD / 4); e += kThreads) {
         const int i = e / (kD / 4), p = e % (kD / 4);
         const int ti = i < L ? t0 + i : t0;
@@ -511,8 +543,14 @@ __global__ void __launch_bounds__(kThreads) cb_grad_kernel(const __grid_constant
     }
     stage_vec(&s.Bm[0][0], A.Bm + small, kC * kC);
     cp_commit();
+    {
+        // the rows of the state after the chunk that the epilogue reads, into L2 meanwhile
+        const float *sn = A.St + ((size_t)(qc + 1 + n) * H + h) * kD * kD + (size_t)cbase * kD;
+        for (int e = tid; e < kHC * kD / 32; e += kThreads)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(sn + (size_t)e * 32));
+    }
     if (tid < kC) s.beta[tid] = tid < L ? A.beta[(size_t)(t0 + tid) * H + h] : 0.f;
-    if (tid < kD) s.er[tid] = expf(A.rr[(size_t)item * kD + tid]);
+    if (tid < kHC) s.er[tid] = expf(A.rr[(size_t)item * kD + cbase + tid]);
     cp_wait<0>();
     __syncthreads();
     const float scale = A.scale;
@@ -532,18 +570,18 @@ __global__ void __launch_bounds__(kThreads) cb_grad_kernel(const __grid_constant
         s.dAq[i][j] = j <= i ? scale * a2 : 0.f;
     }
     __syncthreads();
-    const int i = tid / (kD / 8), tn = tid % (kD / 8);    // row i, columns tn + 16 x
+    const int i = tid / 16, tn = tid % 16;            // row i, local columns tn + 16 x (x < 4)
     const float bi = s.beta[i];
-    float y[8], dqt[8], dkt[8], dkh[8];
+    float y[4], dqt[4], dkt[4], dkh[4];
 #pragma unroll
-    for (int x = 0; x < 8; ++x) y[x] = dqt[x] = dkt[x] = dkh[x] = 0.f;
+    for (int x = 0; x < 4; ++x) y[x] = dqt[x] = dkt[x] = dkh[x] = 0.f;
     // Y = dR S'^T and dO S'^T (S' = e^{r} S: the column factor is applied after the sums)
-    dot_rows2(y, dqt, s.dR[i], s.dO[i], s.S, tn);
+    dot4x2(y, dqt, s.dR[i], s.dO[i], s.S, tn);
     // dKh = Delta dX^T + ...
-    dot_rows(dkh, s.Dl[i], s.dX, tn);
+    dot4(dkh, s.Dl[i], s.dX, tn);
 #pragma unroll
-    for (int x = 0; x < 8; ++x) {
-        const float f = s.er[tn + (kD / 8) * x];
+    for (int x = 0; x < 4; ++x) {
+        const float f = s.er[tn + 16 * x];
         y[x] *= f;
         dqt[x] *= scale * f;
     }
@@ -552,30 +590,30 @@ __global__ void __launch_bounds__(kThreads) cb_grad_kernel(const __grid_constant
     for (int m = 0; m < kC; ++m) {
         const float aq = s.dAq[i][m], ad = s.dA[i][m], aqt = s.dAq[m][i], adt = s.dA[m][i] * s.beta[m];
 #pragma unroll
-        for (int x = 0; x < 8; ++x) {
-            const int c = tn + (kD / 8) * x;
+        for (int x = 0; x < 4; ++x) {
+            const int c = tn + 16 * x;
             const float kh = s.Kh[m][c];
             dqt[x] = fmaf(aq, kh, dqt[x]);
             dkt[x] = fmaf(ad, kh, dkt[x]);
             dkh[x] = fmaf(aqt, s.Qt[m][c], fmaf(adt, s.Kt[m][c], dkh[x]));
         }
     }
-    // dbeta: rowsum(v o dR) - rowsum(Kt o Y) + rowsum(dA o B); dv = beta dR
+    // dbeta share: rowsum(v o dR) - rowsum(Kt o Y) over this half (+ rowsum(dA o B) once); dv = beta dR
     float pb = 0.f;
     const size_t row = ((size_t)(t0 + i) * H + h) * kD;
-    float dgm[8];
+    float dgm[4];
 #pragma unroll
-    for (int x = 0; x < 8; ++x) {
-        const int c = tn + (kD / 8) * x;
-        const float dr = s.dR[i][c], kt = s.Kt[i][c];
-        const float vv = i < L ? ld_x(A.v, row + c, A.bf16) : 0.f;
+    for (int x = 0; x < 4; ++x) {
+        const int c = tn + 16 * x, cg = cbase + c;
+        const float dr = s.dR[i][cg], kt = s.Kt[i][c];
+        const float vv = i < L ? ld_x(A.v, row + cg, A.bf16) : 0.f;
         pb += vv * dr - kt * y[x];
         dkt[x] = bi * (dkt[x] - y[x]);
-        const float ex = A.E[tile + (size_t)i * kD + c];
+        const float ex = A.E[tile + (size_t)i * kD + cg];
         if (i < L) {
-            A.dv[row + c] = bi * dr;
-            A.dq[row + c] = dqt[x] * ex;
-            A.dk[row + c] = dkt[x] * ex + dkh[x] / ex;
+            A.dv[row + cg] = bi * dr;
+            A.dq[row + cg] = dqt[x] * ex;
+            A.dk[row + cg] = dkt[x] * ex + dkh[x] / ex;
         }
         dgm[x] = dqt[x] * s.Qt[i][c] + dkt[x] * kt - dkh[x] * s.Kh[i][c];
     }
@@ -585,21 +623,31 @@ __global__ void __launch_bounds__(kThreads) cb_grad_kernel(const __grid_constant
     __syncthreads();                                   // S free: dGamma goes there
     float (*dG)[L4] = s.S;
 #pragma unroll
-    for (int x = 0; x < 8; ++x) dG[i][tn + (kD / 8) * x] = dgm[x];
-    if (tn == 0) {
+    for (int x = 0; x < 4; ++x) dG[i][tn + 16 * x] = dgm[x];
+    if (tn == 0 && i < L) {
         float ab = 0.f;
-        for (int j = 0; j < i; ++j) ab = fmaf(s.dA[i][j], s.Bm[i][j], ab);
-        if (i < L) A.dbeta[(size_t)(t0 + i) * H + h] = pb + ab;
+        if (half == 0)
+            for (int j = 0; j < i; ++j) ab = fmaf(s.dA[i][j], s.Bm[i][j], ab);
+        atomicAdd(A.dbeta + (size_t)(t0 + i) * H + h, pb + ab);
     }
     __syncthreads();
-    if (tid < kD) {
+    if (tid < kHC) {
+        // the chunk's last row also moves the state it hands on: rowsum(S_next o Dout), with
+        // Dout = e^{-(Gamma_L - r)} dX
+        const int cg = cbase + tid;
+        const float *sn = A.St + ((size_t)(qc + 1 + n) * H + h) * kD * kD + (size_t)cg * kD;
         float gl = 0.f;
-        for (int b = 0; b < kNV; ++b) gl += A.dgl[((size_t)item * kNV + b) * kD + tid];
-        dG[L - 1][tid] += gl;
+#pragma unroll 4
+        for (int j = 0; j < kD; j += 4) {
+            const float4 a4 = *reinterpret_cast<const float4 *>(sn + j);
+            const float4 x4 = *reinterpret_cast<const float4 *>(&s.dX[tid][j]);
+            gl = fmaf(a4.x, x4.x, fmaf(a4.y, x4.y, fmaf(a4.z, x4.z, fmaf(a4.w, x4.w, gl))));
+        }
+        dG[L - 1][tid] += gl * expf(-A.glr[(size_t)item * kD + cg]);
         float run = 0.f;
         for (int ii = L - 1; ii >= 0; --ii) {
             run += dG[ii][tid];
-            A.dg[((size_t)(t0 + ii) * H + h) * kD + tid] = run;
+            A.dg[((size_t)(t0 + ii) * H + h) * kD + cg] = run;
         }
     }
 }
@@ -607,7 +655,7 @@ __global__ void __launch_bounds__(kThreads) cb_grad_kernel(const __grid_constant
 size_t r256(size_t b) { return (b + 255) & ~size_t(255); }
 
 struct Layout {
-    size_t off_chunk, ck_t0, ck_len, Qt, Kt, Kh, E, W, U, Tm, Aqk, Bm, rr, glr, Dl, dR, dX, dgl, St, total;
+    size_t off_chunk, ck_t0, ck_len, Qt, Kt, Kh, E, W, U, Tm, Aqk, Bm, rr, glr, Dl, dR, dX, St, total;
 };
 
 Layout layout(int N, int T, int H) {
@@ -625,13 +673,12 @@ Layout layout(int N, int T, int H) {
     l.rr = take(vb); l.glr = take(vb);
     l.Dl = take(tb); l.dR = take(tb);
     l.dX = take(NI * kD * kD * 4);
-    l.dgl = take(NI * kNV * kD * 4);
     l.St = take((Q + N) * (size_t)H * kD * kD * 4);
     l.total = o;
     return l;
 }
 
-std::atomic<uint64_t> g_grad_attr{0}, g_fwd_attr{0}, g_chain_attr{0};
+std::atomic<uint64_t> g_grad_attr{0}, g_chains_attr{0};
 
 }  // namespace
 
@@ -660,29 +707,28 @@ cudaError_t launch_backward_chunked(const void *q, const void *k, const void *v,
     auto f = [&](size_t off) { return reinterpret_cast<float *>(w + off); };
     A.Qt = f(l.Qt); A.Kt = f(l.Kt); A.Kh = f(l.Kh); A.E = f(l.E); A.W = f(l.W); A.U = f(l.U);
     A.Tm = f(l.Tm); A.Aqk = f(l.Aqk); A.Bm = f(l.Bm); A.rr = f(l.rr); A.glr = f(l.glr);
-    A.Dl = f(l.Dl); A.dR = f(l.dR); A.dX = f(l.dX); A.dgl = f(l.dgl); A.St = f(l.St);
+    A.Dl = f(l.Dl); A.dR = f(l.dR); A.dX = f(l.dX); A.St = f(l.St);
     A.dq = dq; A.dk = dk; A.dv = dv; A.dg = dg; A.dbeta = dbeta; A.dS0 = dS0;
     // chunk enumeration from the device cu_seqlens; the item grids cover the upper bound A.Q of
     // the chunk count and CTAs past the real chunks return at once
     cb_offsets_kernel<<<1, 32, 0, s>>>(A);
     count_launch();
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    const unsigned items = (unsigned)((size_t)A.Q * H), chains = (unsigned)((size_t)N * H * kNV);
+    const unsigned items = (unsigned)((size_t)A.Q * H), chains = (unsigned)((size_t)N * H * kNV),
+                   fchains = (unsigned)((size_t)N * H * kFN);
     cb_prep_kernel<<<items, kThreads, 0, s>>>(A);
     count_launch();
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if (chains) {
-        if ((e = smem_attr_once((const void *)cb_forward_kernel, (int)kFwdSmem, g_fwd_attr)) != cudaSuccess) return e;
-        if ((e = smem_attr_once((const void *)cb_chain_kernel, (int)kChainSmem, g_chain_attr)) != cudaSuccess) return e;
-        cb_forward_kernel<<<chains, kThreads, kFwdSmem, s>>>(A);
-        count_launch();
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
-        cb_chain_kernel<<<chains, kThreads, kChainSmem, s>>>(A);
+        if ((e = smem_attr_once((const void *)cb_chains_kernel, (int)kChainsSmem, g_chains_attr)) != cudaSuccess)
+            return e;
+        cb_chains_kernel<<<fchains + chains, kThreads, kChainsSmem, s>>>(A, (int)fchains);
         count_launch();
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     if ((e = smem_attr_once((const void *)cb_grad_kernel, (int)kGradSmem, g_grad_attr)) != cudaSuccess) return e;
-    cb_grad_kernel<<<items, kThreads, kGradSmem, s>>>(A);
+    if ((e = cudaMemsetAsync(dbeta, 0, (size_t)T * H * sizeof(float), s)) != cudaSuccess) return e;
+    cb_grad_kernel<<<2 * items, kThreads, kGradSmem, s>>>(A);
     count_launch();
     return cudaGetLastError();
 }
