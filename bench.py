@@ -85,7 +85,8 @@ def prefill_work(T, H, d, chunk, W, N=1):
 def backward_work(T, H, d):
     """Bytes: q, k, v (bf16), g, dO (fp32), beta in; dq, dk, dg, dv (fp32), dbeta out.
     Flops: one forward pass of the recurrence (5 d^2 per token and head) plus the reverse
-    sweep (18 d^2); the kernels also recompute the forward once more (5 d^2)."""
+    sweep (18 d^2), the minimal work of the method; the chunked kernels do more (the WY tiles and
+    the chunk products)."""
     per_tok_head = 3 * 2 * d + 4 * d + 4 * d + 4 + 4 * (3 * d + d) + 4
     return T * H * per_tok_head, T * H * 23 * d * d
 

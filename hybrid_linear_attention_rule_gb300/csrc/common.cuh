@@ -114,14 +114,7 @@ struct PrefillArgs {
 };
 
 cudaError_t launch_prefill_f32(const PrefillArgs &a, cudaStream_t s);
-// reverse-mode gradients of the recurrence (csrc/backward.cu); dk = dv = 128
-size_t backward_workspace(int N, int T, int H);
-cudaError_t launch_backward(const void *q, const void *k, const void *v, int bf16, const float *g, const float *beta,
-                            const float *S0, const int32_t *cu, int N, int T, int H, float scale, const float *dO,
-                            const float *dSfin, float *dq, float *dk, float *dv, float *dg, float *dbeta, float *dS0,
-                            void *ws, cudaStream_t s);
-
-// the same gradients in chunked form (csrc/backward_chunked.cu); dk = dv = 128
+// reverse-mode gradients of the recurrence in chunked form (csrc/backward_chunked.cu); dk = dv = 128
 size_t backward_chunked_workspace(int N, int T, int H);
 cudaError_t launch_backward_chunked(const void *q, const void *k, const void *v, int bf16, const float *g,
                                     const float *beta, const float *S0, const int32_t *cu, int N, int T, int H,

@@ -298,10 +298,11 @@ int k3kda_decode_step(const void *q, const void *k, const void *v, int in_dtype,
  *
  *   q, k [T, H, dk], v [T, H, dv]  in_dtype;  g [T, H, dk], beta [T, H], dO [T, H, dv] FP32
  *   cu_seqlens: int32 [N+1] device, cu_seqlens_host: optional host copy (validated when given)
- * Only dk = dv = 128 (UNSUPPORTED otherwise).  FP32 arithmetic on CUDA cores: a forward pass
- * keeps the state before every 16-token block in the workspace, a reverse pass recomputes each
- * block's states from its checkpoint and sweeps its tokens backwards; every (sequence, head)
- * is split over 8 CTAs by 16-column blocks of dv.  Asynchronous on `stream`; the workspace
+ * Only dk = dv = 128 (UNSUPPORTED otherwise).  FP32 arithmetic on CUDA cores, in chunked form:
+ * the chunk algebra of the recurrence (per 16-token chunk) differentiated, with one sequential
+ * pass over the chunks for the states and one for the gradients reaching each chunk boundary,
+ * and the per-token gradients of every chunk computed in parallel.  dbeta is zeroed and
+ * accumulated by the call.  Asynchronous on `stream`; the workspace
  * (k3kda_backward_workspace_size bytes, 256-byte aligned, caller-owned) is scratch only.
  * Errors: INVALID_ARG, UNSUPPORTED, ALIGNMENT (16 bytes for every array but beta, dbeta: 4),
  * WORKSPACE, CUDA. */

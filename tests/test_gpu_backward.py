@@ -2,9 +2,10 @@
 
 The gradients of the ungated recurrence with respect to q, k, v, g, beta and the initial
 state, for seeded output and final-state gradients, compared element by element per tensor:
-max |gpu - oracle| <= 5e-5 * RMS(oracle) + 1e-6 (FP32 arithmetic along the reverse sweep;
-measured errors stay below 1e-5 RMS; the oracle receives the exact values the GPU reads,
-bf16 inputs widened).  The full-size case is checked on the last tokens of sampled heads:
+max |gpu - oracle| <= 5e-5 * RMS(oracle) + 1e-6 (FP32 arithmetic on 16-token chunks, whose
+rescalings by e^(+-G') bound the cancellation in dg: a numpy restatement of the chunk formulas in
+fp32 stays under 1.7e-5 RMS at this chunk length; the oracle receives the exact values the GPU
+reads, bf16 inputs widened).  The full-size case is checked on the last tokens of sampled heads:
 the oracle runs the forward over the whole
 sequence without keeping states, then the reverse sweep over the window from the state it
 reached (gradients of tokens in the window depend on earlier tokens only through that state).
@@ -74,7 +75,7 @@ def test_backward_varlen_edges(bf16):
 
 
 def test_backward_long_sequence_zero_state():
-    """1000 tokens of one head (16 checkpointed chunks, a ragged tail), no initial state and
+    """1000 tokens of one head (62 full 16-token chunks and a ragged one), no initial state and
     no final-state gradient."""
     c, dO, _ = _case([1000], 1, seed=61, bf16=True, s0=False)
     got = _run_gpu(c, dO, None)
