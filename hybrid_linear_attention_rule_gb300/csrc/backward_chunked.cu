@@ -251,16 +251,17 @@ __device__ __forceinline__ void stage_fwd(const CbArgs &A, FwdStage &st, size_t 
     cp_commit();
 }
 
+constexpr int LF = kFV + 4;        // 16-byte aligned rows of Delta
 struct FwdSmem {
     FwdStage stg[kFS];
-    float sSp[kD][kFV + 1], sDl[kC][kFV + 1];
+    float sSp[kD][kFV + 1], sDl[kC][LF];
 };
 
 __device__ __forceinline__ void forward_chain(const CbArgs &A, uint8_t *dyn, int bid) {
     FwdSmem &fs = *reinterpret_cast<FwdSmem *>(dyn);
     FwdStage *stg = fs.stg;
     float (*sSp)[kFV + 1] = fs.sSp;
-    float (*sDl)[kFV + 1] = fs.sDl;
+    float (*sDl)[LF] = fs.sDl;
     // thread: row r, 16 columns; Delta elements (di, dj) and (di, dj + 1)
     const int tid = threadIdx.x, r = tid >> 1, c0 = (tid & 1) * 16;
     const int blk = bid % kFN, nh = bid / kFN, n = nh / A.H, h = nh % A.H, H = A.H;
@@ -316,7 +317,11 @@ __device__ __forceinline__ void forward_chain(const CbArgs &A, uint8_t *dyn, int
         for (int i = 0; i < kC; ++i) {
             const float khv = st.Kh[i][r];
 #pragma unroll
-            for (int u = 0; u < 16; ++u) acc[u] = fmaf(khv, sDl[i][c0 + u], acc[u]);
+            for (int u = 0; u < 16; u += 4) {
+                const float4 d4 = *reinterpret_cast<const float4 *>(&sDl[i][c0 + u]);
+                acc[u] = fmaf(khv, d4.x, acc[u]); acc[u + 1] = fmaf(khv, d4.y, acc[u + 1]);
+                acc[u + 2] = fmaf(khv, d4.z, acc[u + 2]); acc[u + 3] = fmaf(khv, d4.w, acc[u + 3]);
+            }
         }
         const float eg = expf(st.glr[r]);
 #pragma unroll
@@ -360,9 +365,10 @@ __device__ __forceinline__ void stage_chain(const CbArgs &A, ChainStage &st, siz
     cp_commit();
 }
 
+constexpr int LQ = kBV + 4;        // 16-byte aligned rows of beta dR
 struct ChainSmem {
     ChainStage stg[kCS];
-    float sdX[kD][LB], sdD[kC][LB], sbR[kC][LB];
+    float sdX[kD][LB], sdD[kC][LB], sbR[kC][LQ];
 };
 
 __device__ __forceinline__ void backward_chain(const CbArgs &A, uint8_t *dyn, int bid) {
@@ -370,7 +376,7 @@ __device__ __forceinline__ void backward_chain(const CbArgs &A, uint8_t *dyn, in
     ChainStage *stg = cs.stg;
     float (*sdX)[LB] = cs.sdX;
     float (*sdD)[LB] = cs.sdD;
-    float (*sbR)[LB] = cs.sbR;
+    float (*sbR)[LQ] = cs.sbR;
     const int tid = threadIdx.x, r = tid >> 1, c0 = (tid & 1) * 8;
     const int blk = bid % kNV, nh = bid / kNV, n = nh / A.H, h = nh % A.H, H = A.H;
     const int cb = blk * kBV;
@@ -440,9 +446,16 @@ __device__ __forceinline__ void backward_chain(const CbArgs &A, uint8_t *dyn, in
         for (int u = 0; u < 8; ++u) acc[u] = dX[u];
 #pragma unroll
         for (int i = 0; i < kC; ++i) {
-            const float qv = scale * st.Qt[i][r], kv = st.Kt[i][r];
+            const float qv = scale * st.Qt[i][r], kv = -st.Kt[i][r];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) acc[u] = fmaf(qv, st.dO[i][c0 + u], fmaf(-kv, sbR[i][c0 + u], acc[u]));
+            for (int u = 0; u < 8; u += 4) {
+                const float4 o4 = *reinterpret_cast<const float4 *>(&st.dO[i][c0 + u]);
+                const float4 b4 = *reinterpret_cast<const float4 *>(&sbR[i][c0 + u]);
+                acc[u] = fmaf(qv, o4.x, fmaf(kv, b4.x, acc[u]));
+                acc[u + 1] = fmaf(qv, o4.y, fmaf(kv, b4.y, acc[u + 1]));
+                acc[u + 2] = fmaf(qv, o4.z, fmaf(kv, b4.z, acc[u + 2]));
+                acc[u + 3] = fmaf(qv, o4.w, fmaf(kv, b4.w, acc[u + 3]));
+            }
         }
         const float er = expf(st.rr[r]);
 #pragma unroll
