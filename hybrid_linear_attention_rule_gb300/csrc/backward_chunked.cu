@@ -535,11 +535,6 @@ __global__ void __launch_bounds__(kThreads, 2) cb_grad_kernel(const __grid_const
     const size_t tile = (size_t)item * kC * kD, small = (size_t)item * kC * kC;
     const float *St = A.St + ((size_t)(qc + n) * H + h) * kD * kD + (size_t)cbase * kD;
     const float *dXg = A.dX + (size_t)item * kD * kD + (size_t)cbase * kD;
-    for (int e = tid; e < kHC * (kD / 4); e += kThreads) {
-        const int a = e / (kD / 4), p = e % (kD / 4);
-        cp16(&s.S[a][p * 4], St + (size_t)a * kD + p * 4);
-        cp16(&s.dX[a][p * 4], dXg + (size_t)a * kD + p * 4);
-    }
     stage_tile(&s.Dl[0][0], L4, A.Dl + tile);
     stage_tile(&s.dR[0][0], L4, A.dR + tile);
     for (int e = tid; e < kC * (kHC / 4); e += kThreads) {
@@ -556,6 +551,13 @@ __global__ void __launch_bounds__(kThreads, 2) cb_grad_kernel(const __grid_const
     }
     stage_vec(&s.Bm[0][0], A.Bm + small, kC * kC);
     cp_commit();
+    // the half's rows of S and dX in a second group, landing while dA and dAqk are formed
+    for (int e = tid; e < kHC * (kD / 4); e += kThreads) {
+        const int a = e / (kD / 4), p = e % (kD / 4);
+        cp16(&s.S[a][p * 4], St + (size_t)a * kD + p * 4);
+        cp16(&s.dX[a][p * 4], dXg + (size_t)a * kD + p * 4);
+    }
+    cp_commit();
     {
         // the rows of the state after the chunk that the epilogue reads, into L2 meanwhile
         const float *sn = A.St + ((size_t)(qc + 1 + n) * H + h) * kD * kD + (size_t)cbase * kD;
@@ -564,7 +566,7 @@ __global__ void __launch_bounds__(kThreads, 2) cb_grad_kernel(const __grid_const
     }
     if (tid < kC) s.beta[tid] = tid < L ? A.beta[(size_t)(t0 + tid) * H + h] : 0.f;
     if (tid < kHC) s.er[tid] = expf(A.rr[(size_t)item * kD + cbase + tid]);
-    cp_wait<0>();
+    cp_wait<1>();
     __syncthreads();
     const float scale = A.scale;
     {
@@ -582,6 +584,7 @@ __global__ void __launch_bounds__(kThreads, 2) cb_grad_kernel(const __grid_const
         s.dA[i][j] = j < i ? -a1 : 0.f;
         s.dAq[i][j] = j <= i ? scale * a2 : 0.f;
     }
+    cp_wait<0>();
     __syncthreads();
     const int i = tid / 16, tn = tid % 16;            // row i, local columns tn + 16 x (x < 4)
     const float bi = s.beta[i];
