@@ -64,9 +64,10 @@ def _compare(got, want, what):
 
 @pytest.mark.parametrize("bf16", [False, True])
 def test_backward_varlen_edges(bf16):
-    """Empty, one-token, chunk-1, chunk, chunk+1 and multi-chunk sequences, with initial and
-    final-state gradients; an empty sequence passes dS_final straight to dS0."""
-    c, dO, dSf = _case([0, 1, 63, 64, 65, 130], 2, seed=60, bf16=bf16)
+    """Empty, one-token, 16-token-chunk -1 / exact / +1, and multi-chunk sequences (with an empty
+    one between them), with initial and final-state gradients; an empty sequence passes dS_final
+    straight to dS0."""
+    c, dO, dSf = _case([0, 1, 15, 16, 17, 0, 63, 64, 65, 130], 2, seed=60, bf16=bf16)
     got = _run_gpu(c, dO, dSf)
     want = O.recurrent_backward(c.q, c.k, c.v, c.g, c.beta, dO, initial_state=c.S0, dS_final=dSf,
                                 cu_seqlens=c.cu_seqlens, scale=c.scale)
