@@ -252,15 +252,16 @@ __device__ __forceinline__ void stage_fwd(const CbArgs &A, FwdStage &st, size_t 
 }
 
 constexpr int LF = kFV + 4;        // 16-byte aligned rows of Delta
+constexpr int LT = kD + 4;         // 16-byte aligned rows of a transposed 128-row tile
 struct FwdSmem {
     FwdStage stg[kFS];
-    float sSp[kD][kFV + 1], sDl[kC][LF];
+    float sSpT[kFV][LT], sDl[kC][LF];              // S' transposed: column j of S' is row j
 };
 
 __device__ __forceinline__ void forward_chain(const CbArgs &A, uint8_t *dyn, int bid) {
     FwdSmem &fs = *reinterpret_cast<FwdSmem *>(dyn);
     FwdStage *stg = fs.stg;
-    float (*sSp)[kFV + 1] = fs.sSp;
+    float (*sSpT)[LT] = fs.sSpT;
     float (*sDl)[LF] = fs.sDl;
     // thread: row r, 16 columns; Delta elements (di, dj) and (di, dj + 1)
     const int tid = threadIdx.x, r = tid >> 1, c0 = (tid & 1) * 16;
@@ -270,7 +271,8 @@ __device__ __forceinline__ void forward_chain(const CbArgs &A, uint8_t *dyn, int
 #pragma unroll
     for (int u = 0; u < 16; ++u) S[u] = A.S0 ? A.S0[((size_t)nh * kD + r) * kD + cb + c0 + u] : 0.f;
     const int q0 = A.chunk_off[n], nq = A.chunk_off[n + 1] - q0;
-    const int di = tid / 16, dj = (tid % 16) * 2;
+    // Delta elements (di, dj) and (di, dj + 16)
+    const int di = tid / 16, dj = tid % 16;
     // one commit group per chunk (empty past the end), kFS - 1 chunks ahead
     for (int d = 0; d < kFS - 1; ++d) {
         if (d < nq) stage_fwd(A, stg[d], (size_t)(q0 + d) * H + h, cb);
@@ -291,23 +293,26 @@ __device__ __forceinline__ void forward_chain(const CbArgs &A, uint8_t *dyn, int
 #pragma unroll
         for (int u = 0; u < 16; ++u) {
             S[u] *= er;
-            sSp[r][c0 + u] = S[u];
+            sSpT[c0 + u][r] = S[u];
         }
         __syncthreads();
         {
-            const float *w = st.W[di];
+            const float *w = st.W[di], *x0 = sSpT[dj], *x1 = sSpT[dj + 16];
             float a0 = 0.f, a1 = 0.f;
+#pragma unroll 4
             for (int cc = 0; cc < kD; cc += 4) {
                 const float4 w4 = *reinterpret_cast<const float4 *>(w + cc);
-                a0 = fmaf(w4.x, sSp[cc][dj], a0);         a1 = fmaf(w4.x, sSp[cc][dj + 1], a1);
-                a0 = fmaf(w4.y, sSp[cc + 1][dj], a0);     a1 = fmaf(w4.y, sSp[cc + 1][dj + 1], a1);
-                a0 = fmaf(w4.z, sSp[cc + 2][dj], a0);     a1 = fmaf(w4.z, sSp[cc + 2][dj + 1], a1);
-                a0 = fmaf(w4.w, sSp[cc + 3][dj], a0);     a1 = fmaf(w4.w, sSp[cc + 3][dj + 1], a1);
+                const float4 p4 = *reinterpret_cast<const float4 *>(x0 + cc);
+                const float4 q4 = *reinterpret_cast<const float4 *>(x1 + cc);
+                a0 = fmaf(w4.x, p4.x, fmaf(w4.y, p4.y, fmaf(w4.z, p4.z, fmaf(w4.w, p4.w, a0))));
+                a1 = fmaf(w4.x, q4.x, fmaf(w4.y, q4.y, fmaf(w4.z, q4.z, fmaf(w4.w, q4.w, a1))));
             }
-            const float d0 = st.U[di][dj] - a0, d1 = st.U[di][dj + 1] - a1;
+            const float d0 = st.U[di][dj] - a0, d1 = st.U[di][dj + 16] - a1;
             sDl[di][dj] = d0;
-            sDl[di][dj + 1] = d1;
-            *reinterpret_cast<float2 *>(A.Dl + item * kC * kD + (size_t)di * kD + cb + dj) = make_float2(d0, d1);
+            sDl[di][dj + 16] = d1;
+            float *dlg = A.Dl + item * kC * kD + (size_t)di * kD + cb;
+            dlg[dj] = d0;
+            dlg[dj + 16] = d1;
         }
         __syncthreads();
         float acc[16];
@@ -368,13 +373,13 @@ __device__ __forceinline__ void stage_chain(const CbArgs &A, ChainStage &st, siz
 constexpr int LQ = kBV + 4;        // 16-byte aligned rows of beta dR
 struct ChainSmem {
     ChainStage stg[kCS];
-    float sdX[kD][LB], sdD[kC][LB], sbR[kC][LQ];
+    float sdXT[kBV][LT], sdD[kC][LB], sbR[kC][LQ];  // dX transposed: column j of dX is row j
 };
 
 __device__ __forceinline__ void backward_chain(const CbArgs &A, uint8_t *dyn, int bid) {
     ChainSmem &cs = *reinterpret_cast<ChainSmem *>(dyn);
     ChainStage *stg = cs.stg;
-    float (*sdX)[LB] = cs.sdX;
+    float (*sdXT)[LT] = cs.sdXT;
     float (*sdD)[LB] = cs.sdD;
     float (*sbR)[LQ] = cs.sbR;
     const int tid = threadIdx.x, r = tid >> 1, c0 = (tid & 1) * 8;
@@ -408,7 +413,7 @@ __device__ __forceinline__ void backward_chain(const CbArgs &A, uint8_t *dyn, in
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
             dX[u] = eg * Dout[u];
-            sdX[r][c0 + u] = dX[u];
+            sdXT[c0 + u][r] = dX[u];
         }
         {
             float *dxg = A.dX + item * kD * kD + (size_t)r * kD + cb + c0;
@@ -418,14 +423,13 @@ __device__ __forceinline__ void backward_chain(const CbArgs &A, uint8_t *dyn, in
         __syncthreads();
         // dDelta = Kh dX + Aqk^T dOs
         {
-            const float *kh = st.Kh[di];
+            const float *kh = st.Kh[di], *xt = sdXT[dj];
             float acc = 0.f;
+#pragma unroll 4
             for (int rr = 0; rr < kD; rr += 4) {
                 const float4 k4 = *reinterpret_cast<const float4 *>(kh + rr);
-                acc = fmaf(k4.x, sdX[rr][dj], acc);
-                acc = fmaf(k4.y, sdX[rr + 1][dj], acc);
-                acc = fmaf(k4.z, sdX[rr + 2][dj], acc);
-                acc = fmaf(k4.w, sdX[rr + 3][dj], acc);
+                const float4 x4 = *reinterpret_cast<const float4 *>(xt + rr);
+                acc = fmaf(k4.x, x4.x, fmaf(k4.y, x4.y, fmaf(k4.z, x4.z, fmaf(k4.w, x4.w, acc))));
             }
             float a2 = 0.f;
             for (int m = di; m < kC; ++m) a2 = fmaf(st.Aqk[m][di], st.dO[m][dj], a2);
