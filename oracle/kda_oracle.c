@@ -22,7 +22,7 @@
  *         o_t = scale * S_t^T q_t,      alpha_t = exp(g_t)   (per channel),
  *     and the mixer output is o_t * sigmoid(gate_t) when a gate is given.
  *
- * Readings where the pages are silent (each is listed in the design doc):
+ * Readings where the pages are silent:
  *   conv: depthwise, no bias, w[c, W-1] multiplies the current token, history
  *         before a sequence start comes from the conv state (oldest row first)
  *         or is zero; SiLU after the conv; the conv state keeps the last W-1

@@ -16,7 +16,7 @@
  *   - mlite-k3 README, "What this repository is": the 69 KDA + 24 gated-MLA
  *     layer schedule of the hybrid.
  *
- * Readings where the pages are silent (each is listed in the design doc):
+ * Readings where the pages are silent:
  *   heads: one key and one value row per query head (no sharing across heads),
  *         the decompressed form of the layer, since the token step receives
  *         projected q, k, v;
