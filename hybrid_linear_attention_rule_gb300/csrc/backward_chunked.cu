@@ -56,7 +56,7 @@ struct CbArgs {
     int N, T, H, Q;                // Q: chunks over all sequences
     float scale;
     int32_t *chunk_off;            // [N + 1]
-    int32_t *ck_t0, *ck_len;       // [Q]
+    int32_t *ck_t0, *ck_len, *ck_seq;   // [Q]: first token, length and sequence of each chunk
     // per (chunk, head) item, fp32
     float *Qt, *Kt, *Kh, *E, *W, *U;   // [item][kC][kD]
     float *Tm, *Aqk, *Bm;              // [item][kC][kC]
@@ -71,6 +71,7 @@ __device__ __forceinline__ float ld_x(const void *p, size_t i, int bf16) {
     return bf16 ? __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(p)[i]) : reinterpret_cast<const float *>(p)[i];
 }
 
+// chunk offsets of the sequences (a prefix over N, one thread)
 __global__ void __launch_bounds__(32) cb_offsets_kernel(CbArgs A) {
     if (threadIdx.x != 0) return;
     int acc = 0;
@@ -78,13 +79,27 @@ __global__ void __launch_bounds__(32) cb_offsets_kernel(CbArgs A) {
     for (int n = 0; n < A.N; ++n) {
         int b, e;
         seq_bounds(A.cu, n, A.T, b, e);
-        for (int t = b; t < e; t += kC) {
-            A.ck_t0[acc] = t;
-            A.ck_len[acc] = min(kC, e - t);
-            ++acc;
-        }
+        acc += (e - b + kC - 1) / kC;
         A.chunk_off[n + 1] = acc;
     }
+}
+
+// the chunk table, one thread per chunk: its sequence by binary search over the offsets
+__global__ void __launch_bounds__(256) cb_chunks_kernel(CbArgs A) {
+    const int q = blockIdx.x * blockDim.x + threadIdx.x;
+    if (q >= A.chunk_off[A.N]) return;
+    int lo = 0, hi = A.N - 1;                          // the last n with chunk_off[n] <= q
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (A.chunk_off[mid] <= q) lo = mid;
+        else hi = mid - 1;
+    }
+    int b, e;
+    seq_bounds(A.cu, lo, A.T, b, e);
+    const int t = b + (q - A.chunk_off[lo]) * kC;
+    A.ck_t0[q] = t;
+    A.ck_len[q] = min(kC, e - t);
+    A.ck_seq[q] = lo;
 }
 
 // C[m][n] over an M x N tile, thread tile TM x TN with rows m = tm + (M / TM) v and columns
@@ -534,8 +549,7 @@ __global__ void __launch_bounds__(kThreads, 2) cb_grad_kernel(const __grid_const
     const int t0 = A.ck_t0[qc], L = A.ck_len[qc];
     const int cbase = half * kHC;
     // the sequence of this chunk: its chunk-start state slot is qc + n
-    int n = 0;
-    while (A.chunk_off[n + 1] <= qc) ++n;
+    const int n = A.ck_seq[qc];
     const size_t tile = (size_t)item * kC * kD, small = (size_t)item * kC * kC;
     const float *St = A.St + ((size_t)(qc + n) * H + h) * kD * kD + (size_t)cbase * kD;
     const float *dXg = A.dX + (size_t)item * kD * kD + (size_t)cbase * kD;
@@ -675,7 +689,7 @@ __global__ void __launch_bounds__(kThreads, 2) cb_grad_kernel(const __grid_const
 size_t r256(size_t b) { return (b + 255) & ~size_t(255); }
 
 struct Layout {
-    size_t off_chunk, ck_t0, ck_len, Qt, Kt, Kh, E, W, U, Tm, Aqk, Bm, rr, glr, Dl, dR, dX, St, total;
+    size_t off_chunk, ck_t0, ck_len, ck_seq, Qt, Kt, Kh, E, W, U, Tm, Aqk, Bm, rr, glr, Dl, dR, dX, St, total;
 };
 
 Layout layout(int N, int T, int H) {
@@ -687,6 +701,7 @@ Layout layout(int N, int T, int H) {
     l.off_chunk = take((size_t)(N + 1) * 4);
     l.ck_t0 = take(Q * 4);
     l.ck_len = take(Q * 4);
+    l.ck_seq = take(Q * 4);
     const size_t tb = NI * kC * kD * 4, sb = NI * kC * kC * 4, vb = NI * kD * 4;
     l.Qt = take(tb); l.Kt = take(tb); l.Kh = take(tb); l.E = take(tb); l.W = take(tb); l.U = take(tb);
     l.Tm = take(sb); l.Aqk = take(sb); l.Bm = take(sb);
@@ -724,6 +739,7 @@ cudaError_t launch_backward_chunked(const void *q, const void *k, const void *v,
     A.chunk_off = reinterpret_cast<int32_t *>(w + l.off_chunk);
     A.ck_t0 = reinterpret_cast<int32_t *>(w + l.ck_t0);
     A.ck_len = reinterpret_cast<int32_t *>(w + l.ck_len);
+    A.ck_seq = reinterpret_cast<int32_t *>(w + l.ck_seq);
     auto f = [&](size_t off) { return reinterpret_cast<float *>(w + off); };
     A.Qt = f(l.Qt); A.Kt = f(l.Kt); A.Kh = f(l.Kh); A.E = f(l.E); A.W = f(l.W); A.U = f(l.U);
     A.Tm = f(l.Tm); A.Aqk = f(l.Aqk); A.Bm = f(l.Bm); A.rr = f(l.rr); A.glr = f(l.glr);
@@ -732,6 +748,9 @@ cudaError_t launch_backward_chunked(const void *q, const void *k, const void *v,
     // chunk enumeration from the device cu_seqlens; the item grids cover the upper bound A.Q of
     // the chunk count and CTAs past the real chunks return at once
     cb_offsets_kernel<<<1, 32, 0, s>>>(A);
+    count_launch();
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    cb_chunks_kernel<<<(unsigned)((A.Q + 255) / 256), 256, 0, s>>>(A);
     count_launch();
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     const unsigned items = (unsigned)((size_t)A.Q * H), chains = (unsigned)((size_t)N * H * kNV),
