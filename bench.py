@@ -331,11 +331,11 @@ def run_mla(args, K, torch, dev, rank, world):
     lens0 = torch.from_numpy(lens_np).to(dev)
     lens = lens0.clone()
     out = torch.empty(N, H, d, **bf)
-    ws = torch.empty(K.k3mla_decode_workspace_size(N, H, d, L), dtype=torch.uint8, device=dev)
+    ws = torch.empty(K.k3mla_decode_workspace_size(N, H, d, d, L), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 
     def call():
-        K.k3mla_decode_step(q, k, v, g, kc, vc, lens, N, H, d, L, 0, 10000.0, d ** -0.5, out, ws, stream)
+        K.k3mla_decode_step(q, k, v, g, kc, vc, lens, N, H, d, d, L, 0, 10000.0, d ** -0.5, out, ws, stream)
 
     for _ in range(args.warmup):
         lens.copy_(lens0)

@@ -94,9 +94,9 @@ def load_library(build_if_missing: bool = True):
         lib.k3kda_backward.argtypes = [P, P, P, I, P, P, P, P, P, I, I, I, I, I, F, P, P, P, P, P, P, P, P, P,
                                        ctypes.c_size_t, P]
         lib.k3kda_backward.restype = I
-        lib.k3mla_decode_workspace_size.argtypes = [I, I, I, I]
+        lib.k3mla_decode_workspace_size.argtypes = [I, I, I, I, I]
         lib.k3mla_decode_workspace_size.restype = Z
-        lib.k3mla_decode_step.argtypes = [P, P, P, I, P, P, P, I, P, I, I, I, I, I, F, F, P, I, P, Z, P]
+        lib.k3mla_decode_step.argtypes = [P, P, P, I, P, P, P, I, P, I, I, I, I, I, I, F, F, P, I, P, Z, P]
         lib.k3mla_decode_step.restype = I
         _lib = lib
         return lib
@@ -359,16 +359,17 @@ def short_conv(x, weight, conv_state=None, cu_seqlens=None, apply_silu=True, out
 
 # ---- the gated attention (MLA) layers' decode token ------------------------
 
-def k3mla_decode_workspace_size(N, H, d, L_max) -> int:
-    return int(load_library().k3mla_decode_workspace_size(int(N), int(H), int(d), int(L_max)))
+def k3mla_decode_workspace_size(N, H, dqk, dv, L_max) -> int:
+    return int(load_library().k3mla_decode_workspace_size(int(N), int(H), int(dqk), int(dv), int(L_max)))
 
 
-def k3mla_decode_step(q, k_new, v_new, gate, k_cache, v_cache, cache_len, N, H, d, L_max, rope_dim, rope_theta,
+def k3mla_decode_step(q, k_new, v_new, gate, k_cache, v_cache, cache_len, N, H, dqk, dv, L_max, rope_dim, rope_theta,
                       scale, out, workspace, stream=None):
     """One decode token of the gated attention layers (see include/k3kda.h): RoPE, append, attention, gate."""
     lib = load_library()
     st = lib.k3mla_decode_step(_ptr(q), _ptr(k_new), _ptr(v_new), _dtype(q), _ptr(gate), _ptr(k_cache),
-                               _ptr(v_cache), _dtype(k_cache), _ptr(cache_len), int(N), int(H), int(d), int(L_max),
+                               _ptr(v_cache), _dtype(k_cache), _ptr(cache_len), int(N), int(H), int(dqk), int(dv),
+                               int(L_max),
                                int(rope_dim), float(rope_theta), float(scale), _ptr(out), _dtype(out),
                                _ptr(workspace), int(workspace.numel() * workspace.element_size()), _stream(stream))
     _check("k3mla_decode_step", st)
@@ -376,15 +377,16 @@ def k3mla_decode_step(q, k_new, v_new, gate, k_cache, v_cache, cache_len, N, H, 
 
 def mla_decode_step(q, k_new, v_new, k_cache, v_cache, cache_len, gate=None, scale=None, rope_dim=0,
                     rope_theta=10000.0, out_dtype=None, workspace=None, stream=None):
-    """Decode one token for every sequence: q, k_new, v_new [N, H, d]; caches [N, H, L_max, d] and
-    cache_len int32 [N] are updated in place.  Returns the output [N, H, d] (allocated with torch, in
-    out_dtype, default q's type)."""
-    N, H, d = q.shape
+    """Decode one token for every sequence: q, k_new [N, H, dqk], v_new [N, H, dv]; caches
+    [N, H, L_max, dqk | dv] and cache_len int32 [N] are updated in place.  Returns the output
+    [N, H, dv] (allocated with torch, in out_dtype, default q's type)."""
+    N, H, dqk = q.shape
+    dv = v_new.shape[-1]
     L_max = k_cache.shape[2]
-    scale = float(d) ** -0.5 if scale is None else float(scale)
-    out = torch.empty(N, H, d, dtype=out_dtype or q.dtype, device=q.device)
+    scale = float(dqk) ** -0.5 if scale is None else float(scale)
+    out = torch.empty(N, H, dv, dtype=out_dtype or q.dtype, device=q.device)
     if workspace is None:
-        workspace = torch.empty(k3mla_decode_workspace_size(N, H, d, L_max), dtype=torch.uint8, device=q.device)
-    k3mla_decode_step(q, k_new, v_new, gate, k_cache, v_cache, cache_len, N, H, d, L_max, rope_dim, rope_theta,
+        workspace = torch.empty(k3mla_decode_workspace_size(N, H, dqk, dv, L_max), dtype=torch.uint8, device=q.device)
+    k3mla_decode_step(q, k_new, v_new, gate, k_cache, v_cache, cache_len, N, H, dqk, dv, L_max, rope_dim, rope_theta,
                       scale, out, workspace, stream)
     return out

@@ -328,20 +328,21 @@ int k3kda_decode_step_slots(const void *q, const void *k, const void *v, int in_
                        scale, use_qk_l2norm, out, out_dtype, stream, state_idx, num_slots);
 }
 
-size_t k3mla_decode_workspace_size(int N, int H, int d, int L_max) {
-    if (N < 0 || H < 1 || d < 1 || L_max < 1) return 0;
-    return mla_workspace(N, H, d, L_max);
+size_t k3mla_decode_workspace_size(int N, int H, int dqk, int dv, int L_max) {
+    if (N < 0 || H < 1 || dqk < 1 || dv < 1 || L_max < 1) return 0;
+    return mla_workspace(N, H, dqk, dv, L_max);
 }
 
 int k3mla_decode_step(const void *q, const void *k_new, const void *v_new, int in_dtype, const void *gate,
-                      void *k_cache, void *v_cache, int cache_dtype, int32_t *cache_len, int N, int H, int d,
-                      int L_max, int rope_dim, float rope_theta, float scale, void *out, int out_dtype,
+                      void *k_cache, void *v_cache, int cache_dtype, int32_t *cache_len, int N, int H, int dqk,
+                      int dv, int L_max, int rope_dim, float rope_theta, float scale, void *out, int out_dtype,
                       void *workspace, size_t workspace_bytes, void *stream) {
     if (N < 0 || H < 1 || L_max < 1) return K3KDA_ERR_INVALID_ARG;
     if (!dtype_ok(in_dtype) || !dtype_ok(cache_dtype) || !dtype_ok(out_dtype)) return K3KDA_ERR_INVALID_ARG;
-    if (rope_dim < 0 || (rope_dim & 1) || rope_dim > d) return K3KDA_ERR_INVALID_ARG;
+    if (rope_dim < 0 || (rope_dim & 1) || rope_dim > dqk) return K3KDA_ERR_INVALID_ARG;
     if (rope_dim > 0 && !(rope_theta > 0.f)) return K3KDA_ERR_INVALID_ARG;
-    if (d != 64 && d != 128 && d != 256) return K3KDA_ERR_UNSUPPORTED;
+    if ((dqk != 64 && dqk != 128 && dqk != 192 && dqk != 256) || (dv != 64 && dv != 128 && dv != 256))
+        return K3KDA_ERR_UNSUPPORTED;
     if ((long long)N * H * (long long)mla_splits(L_max) > 0x7fffffffLL) return K3KDA_ERR_UNSUPPORTED;
     if (N == 0) return K3KDA_OK;
     if (!q || !k_new || !v_new || !k_cache || !v_cache || !cache_len || !out) return K3KDA_ERR_INVALID_ARG;
@@ -349,10 +350,10 @@ int k3mla_decode_step(const void *q, const void *k_new, const void *v_new, int i
         if (!aligned16(p)) return K3KDA_ERR_ALIGNMENT;
     if (!aligned4(cache_len)) return K3KDA_ERR_ALIGNMENT;
     if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return K3KDA_ERR_WORKSPACE;
-    if (workspace_bytes < mla_workspace(N, H, d, L_max)) return K3KDA_ERR_WORKSPACE;
+    if (workspace_bytes < mla_workspace(N, H, dqk, dv, L_max)) return K3KDA_ERR_WORKSPACE;
     return cuda_status(launch_mla_decode(q, k_new, v_new, in_dtype == K3KDA_BF16, gate, k_cache, v_cache,
-                                         cache_dtype == K3KDA_BF16, cache_len, N, H, d, L_max, rope_dim, rope_theta,
-                                         scale, out, out_dtype == K3KDA_BF16, workspace,
+                                         cache_dtype == K3KDA_BF16, cache_len, N, H, dqk, dv, L_max, rope_dim,
+                                         rope_theta, scale, out, out_dtype == K3KDA_BF16, workspace,
                                          static_cast<cudaStream_t>(stream)));
 }
 

@@ -121,12 +121,13 @@ cudaError_t launch_backward_chunked(const void *q, const void *k, const void *v,
                                     float scale, const float *dO, const float *dSfin, float *dq, float *dk, float *dv,
                                     float *dg, float *dbeta, float *dS0, void *ws, cudaStream_t s);
 
-// one decode token of the gated attention layers (csrc/mla_decode.cu); d in {64, 128, 256}
+// one decode token of the gated attention layers (csrc/mla_decode.cu); dq in {64, 128, 192, 256},
+// dv in {64, 128, 256}
 size_t mla_splits(int L_max);
-size_t mla_workspace(int N, int H, int d, int L_max);
+size_t mla_workspace(int N, int H, int dq, int dv, int L_max);
 cudaError_t launch_mla_decode(const void *q, const void *k_new, const void *v_new, int in_bf16, const void *gate,
-                              void *k_cache, void *v_cache, int cache_bf16, int32_t *cache_len, int N, int H, int d,
-                              int L_max, int rope_dim, float theta, float scale, void *out, int out_bf16, void *ws,
-                              cudaStream_t st);
+                              void *k_cache, void *v_cache, int cache_bf16, int32_t *cache_len, int N, int H, int dq,
+                              int dv, int L_max, int rope_dim, float theta, float scale, void *out, int out_bf16,
+                              void *ws, cudaStream_t st);
 
 }  // namespace k3kda

@@ -328,22 +328,24 @@ int k3kda_backward(const void *q, const void *k, const void *v, int in_dtype,
  *   out[n,h] = softmax_j(scale * q' . k_cache[n,h,j], j = 0..pos) . v_cache[n,h,0..pos]
  *              (* sigmoid(gate[n,h]) when gate is given)
  *   cache_len[n] = pos + 1.
- * Layouts (row-major, contiguous): q, k_new, v_new, gate, out [N, H, d] (q, k_new, v_new and
- * gate in in_dtype, out in out_dtype); k_cache, v_cache [N, H, L_max, d] in cache_dtype (each
- * (sequence, head) owns L_max contiguous rows); cache_len int32 [N] in device memory, read and
- * advanced by the call.  d in {64, 128, 256} (UNSUPPORTED otherwise).
+ * Layouts (row-major, contiguous): q, k_new [N, H, dqk]; v_new, gate, out [N, H, dv] (q, k_new,
+ * v_new and gate in in_dtype, out in out_dtype); k_cache [N, H, L_max, dqk], v_cache
+ * [N, H, L_max, dv] in cache_dtype (each (sequence, head) owns L_max contiguous rows); cache_len
+ * int32 [N] in device memory, read and advanced by the call.  dqk in {64, 128, 192, 256}, dv in
+ * {64, 128, 256} (UNSUPPORTED otherwise): keys may be wider than values, e.g. 128 rotation-free
+ * dims and a 64-dim RoPE part.
  * A sequence whose cache is full (pos >= L_max) or whose length is negative gets NaN outputs;
  * its cache rows and length are left as they were (the length lives on the device, so this is
  * reported in the data, not in the status).
  * Ownership: every buffer is the caller's; the workspace (k3mla_decode_workspace_size bytes,
  * 256-byte aligned) is scratch.  Three kernel launches on `stream`, nothing synchronises.
  * Errors: INVALID_ARG (negative sizes, odd or too large rope_dim, rope_theta <= 0 with RoPE,
- * null pointers), UNSUPPORTED (d, or N*H*ceil(L_max/512) above 2^31-1), ALIGNMENT (16 bytes for
+ * null pointers), UNSUPPORTED (dqk, dv, or N*H*ceil(L_max/512) above 2^31-1), ALIGNMENT (16 bytes for
  * every array but cache_len: 4), WORKSPACE, CUDA.  N = 0 returns OK without a launch. */
-size_t k3mla_decode_workspace_size(int N, int H, int d, int L_max);
+size_t k3mla_decode_workspace_size(int N, int H, int dqk, int dv, int L_max);
 int k3mla_decode_step(const void *q, const void *k_new, const void *v_new, int in_dtype, const void *gate,
                       void *k_cache, void *v_cache, int cache_dtype, int32_t *cache_len,
-                      int N, int H, int d, int L_max, int rope_dim, float rope_theta, float scale,
+                      int N, int H, int dqk, int dv, int L_max, int rope_dim, float rope_theta, float scale,
                       void *out, int out_dtype, void *workspace, size_t workspace_bytes, void *stream);
 
 #ifdef __cplusplus

@@ -209,10 +209,10 @@ class MlaDecodeCase:
     in_dtype: str                      # storage type of q, k_new, v_new, gate
     cache_dtype: str                   # storage type of the caches
     q: np.ndarray                      # float32 [N, H, d]
-    k_new: np.ndarray
-    v_new: np.ndarray
+    k_new: np.ndarray                  # [N, H, d]
+    v_new: np.ndarray                  # [N, H, dv]
     k_cache: np.ndarray                # float32 [N, H, L_max, d]
-    v_cache: np.ndarray
+    v_cache: np.ndarray                # [N, H, L_max, dv]
     cache_len: np.ndarray              # int32 [N]
     scale: float
     rope_dim: int = 0
@@ -221,9 +221,11 @@ class MlaDecodeCase:
 
 
 def mla_decode_case(name, N, H, d, L_max, lengths, seed=0, in_dtype="bf16", cache_dtype="bf16",
-                    rope_dim=0, theta=10000.0, gate=True) -> MlaDecodeCase:
+                    rope_dim=0, theta=10000.0, gate=True, dv=None) -> MlaDecodeCase:
     """q, k_new, v_new, gate and the cached rows ~ N(0, 1) (bf16-exact for bf16 storage); lengths
-    given explicitly, or as (lo, hi) for uniform integers in [lo, hi]; scale = d^-1/2."""
+    given explicitly, or as (lo, hi) for uniform integers in [lo, hi]; d is the query/key width,
+    dv the value width (default d); scale = d^-1/2."""
+    dv = d if dv is None else dv
     bi, bc = in_dtype == "bf16", cache_dtype == "bf16"
     if isinstance(lengths, tuple):
         lens = _rng(seed, "mla_lengths").integers(lengths[0], lengths[1] + 1, size=N)
@@ -232,8 +234,8 @@ def mla_decode_case(name, N, H, d, L_max, lengths, seed=0, in_dtype="bf16", cach
     return MlaDecodeCase(
         name=name, N=N, H=H, d=d, L_max=L_max, in_dtype=in_dtype, cache_dtype=cache_dtype,
         q=normal((N, H, d), 1.0, seed, "mla_q", bi), k_new=normal((N, H, d), 1.0, seed, "mla_k", bi),
-        v_new=normal((N, H, d), 1.0, seed, "mla_v", bi),
+        v_new=normal((N, H, dv), 1.0, seed, "mla_v", bi),
         k_cache=normal((N, H, L_max, d), 1.0, seed, "mla_k_cache", bc),
-        v_cache=normal((N, H, L_max, d), 1.0, seed, "mla_v_cache", bc),
+        v_cache=normal((N, H, L_max, dv), 1.0, seed, "mla_v_cache", bc),
         cache_len=lens.astype(np.int32), scale=float(d) ** -0.5, rope_dim=rope_dim, theta=theta,
-        gate=normal((N, H, d), 1.0, seed, "mla_gate", bi) if gate else None)
+        gate=normal((N, H, dv), 1.0, seed, "mla_gate", bi) if gate else None)

@@ -209,8 +209,8 @@ def test_binding_refuses_cpu_tensors():
 
 
 def _mla(lib, **kw):
-    a = dict(q=A16, k=A16, v=A16, in_dtype=1, gate=None, kc=A16, vc=A16, cache_dtype=1, lens=A16, N=4, H=2, d=128,
-             L_max=1024, rope_dim=0, theta=10000.0, scale=1.0, out=A16, out_dtype=1, ws=None, ws_bytes=0, stream=None)
+    a = dict(q=A16, k=A16, v=A16, in_dtype=1, gate=None, kc=A16, vc=A16, cache_dtype=1, lens=A16, N=4, H=2, dq=128,
+             dv=128, L_max=1024, rope_dim=0, theta=10000.0, scale=1.0, out=A16, out_dtype=1, ws=None, ws_bytes=0, stream=None)
     a.update(kw)
     return lib.k3mla_decode_step(*a.values())
 
@@ -226,7 +226,9 @@ def test_mla_decode_rejects_bad_arguments(lib):
     assert _mla(lib, rope_dim=130) == -1                 # above d
     assert _mla(lib, rope_dim=64, theta=0.0) == -1
     assert _mla(lib, cache_dtype=7) == -1
-    assert _mla(lib, d=96) == -2
+    assert _mla(lib, dq=96) == -2
+    assert _mla(lib, dv=192) == -2                       # only the key width may be 192
+    assert _mla(lib, dq=192, dv=128, rope_dim=200) == -1
     assert _mla(lib, N=4096, H=64, L_max=big) == -2      # grid above 2^31 - 1 blocks
     assert _mla(lib, vc=MIS) == -3
     assert _mla(lib, ws=None) == -4
@@ -237,5 +239,5 @@ def test_mla_workspace_size(lib):
     r = lambda b: (b + 255) // 256 * 256
     N, H, d, L = 256, 32, 128, 8192
     S = L // 512
-    assert K.k3mla_decode_workspace_size(N, H, d, L) == r(N * 4) + r(N * H * d * 4) + r(N * H * S * 8) + r(N * H * S * d * 4)
-    assert K.k3mla_decode_workspace_size(3, 2, 64, 513) == r(12) + r(3 * 2 * 64 * 4) + r(3 * 2 * 2 * 8) + r(3 * 2 * 2 * 64 * 4)
+    assert K.k3mla_decode_workspace_size(N, H, d, d, L) == r(N * 4) + r(N * H * d * 4) + r(N * H * S * 8) + r(N * H * S * d * 4)
+    assert K.k3mla_decode_workspace_size(3, 2, 192, 64, 513) == r(12) + r(3 * 2 * 192 * 4) + r(3 * 2 * 2 * 8) + r(3 * 2 * 2 * 64 * 4)

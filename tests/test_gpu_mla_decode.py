@@ -72,27 +72,33 @@ def _check_rows(c, kc_dev, vc_dev, kc_ref, vc_ref, lens_before):
         assert np.all(np.abs(ka - kr) <= 1e-6 * (1 + np.abs(kr))), "appended key row (fp32)"
 
 
-CONFIGS = [  # d, in, cache, out, rope_dim, gate
-    (128, "bf16", "bf16", "f32", 0, True),
-    (128, "bf16", "bf16", "bf16", 64, True),
-    (128, "f32", "f32", "f32", 128, False),
-    (128, "bf16", "f32", "f32", 0, True),
-    (64, "bf16", "bf16", "f32", 0, True),
-    (64, "f32", "f32", "f32", 32, True),
-    (256, "bf16", "bf16", "f32", 0, False),
-    (256, "f32", "f32", "f32", 64, True),
+CONFIGS = [  # dqk, dv, in, cache, out, rope_dim, gate
+    (128, 128, "bf16", "bf16", "f32", 0, True),
+    (128, 128, "bf16", "bf16", "bf16", 64, True),
+    (128, 128, "f32", "f32", "f32", 128, False),
+    (128, 128, "bf16", "f32", "f32", 0, True),
+    (64, 64, "bf16", "bf16", "f32", 0, True),
+    (64, 64, "f32", "f32", "f32", 32, True),
+    (256, 256, "bf16", "bf16", "f32", 0, False),
+    (256, 256, "f32", "f32", "f32", 64, True),
+    (192, 128, "bf16", "bf16", "f32", 64, True),     # 128 rotation-free dims + a 64-dim RoPE part
+    (192, 128, "f32", "f32", "f32", 64, True),
+    (192, 256, "bf16", "bf16", "bf16", 0, True),
+    (128, 64, "f32", "bf16", "f32", 32, False),
+    (64, 256, "bf16", "f32", "f32", 0, True),
 ]
 
 
-@pytest.mark.parametrize("d,ind,cad,outd,rd,gate", CONFIGS,
+@pytest.mark.parametrize("d,dv,ind,cad,outd,rd,gate", CONFIGS,
                          ids=lambda x: str(x) if not isinstance(x, bool) else ("gate" if x else "nogate"))
-def test_mla_decode_small_parity(d, ind, cad, outd, rd, gate):
+def test_mla_decode_small_parity(d, dv, ind, cad, outd, rd, gate):
     """12 sequences x 3 heads, L_max = 1100 (three 512-key splits, the last ragged); cached lengths
-    0, 1, 15, 16, 17, 511, 512, 513, 1000, L_max - 1 (fills the cache), L_max (full: NaN) and -1."""
+    0, 1, 15, 16, 17, 511, 512, 513, 1000, L_max - 1 (fills the cache), L_max (full: NaN) and -1;
+    query/key width d, value width dv."""
     L = 1100
     lens = [0, 1, 15, 16, 17, 511, 512, 513, 1000, L - 1, L, -1]
-    c = KI.mla_decode_case("mla_small", len(lens), 3, d, L, lens, seed=d + rd, in_dtype=ind, cache_dtype=cad,
-                           rope_dim=rd, theta=10000.0 if rd != 32 else 500.0, gate=gate)
+    c = KI.mla_decode_case("mla_small", len(lens), 3, d, L, lens, seed=d + dv + rd, in_dtype=ind, cache_dtype=cad,
+                           rope_dim=rd, theta=10000.0 if rd != 32 else 500.0, gate=gate, dv=dv)
     t = _to_dev(c)
     out = K.mla_decode_step(t["q"], t["k"], t["v"], t["kc"], t["vc"], t["lens"], gate=t["gate"], scale=c.scale,
                             rope_dim=rd, rope_theta=c.theta, out_dtype=TORCH_DT[outd])
@@ -114,7 +120,7 @@ def test_mla_decode_consecutive_tokens():
     t = _to_dev(c)
     kc_o, vc_o, lens_o = c.k_cache.astype(np.float64), c.v_cache.astype(np.float64), c.cache_len.copy()
     rng = np.random.default_rng(17)
-    ws = torch.empty(K.k3mla_decode_workspace_size(4, H, d, L), dtype=torch.uint8, device="cuda")
+    ws = torch.empty(K.k3mla_decode_workspace_size(4, H, d, d, L), dtype=torch.uint8, device="cuda")
     worst = 0.0
     for step in range(40):
         q, k, v, g = (KI.round_bf16(rng.standard_normal((4, H, d)).astype(np.float32)) for _ in range(4))
