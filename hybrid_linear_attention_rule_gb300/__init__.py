@@ -25,7 +25,7 @@ __all__ = ["K3KDAError", "load_library", "library_path", "F32", "BF16", "L2_EPS"
            "k3kda_decode_step_slots", "k3kda_prefill_noalloc", "k3kda_workspace_status",
            "k3kda_backward_workspace_size", "k3kda_backward", "backward",
            "k3kda_decode_step", "prefill", "decode_step", "short_conv",
-           "k3mla_decode_workspace_size", "k3mla_decode_step", "mla_decode_step"]
+           "k3mla_decode_workspace_size", "k3mla_decode_step", "k3mla_decode_step_slots", "mla_decode_step"]
 
 F32, BF16 = 0, 1
 L2_EPS = 1e-6
@@ -98,6 +98,9 @@ def load_library(build_if_missing: bool = True):
         lib.k3mla_decode_workspace_size.restype = Z
         lib.k3mla_decode_step.argtypes = [P, P, P, I, P, P, P, I, P, I, I, I, I, I, I, F, F, P, I, P, Z, P]
         lib.k3mla_decode_step.restype = I
+        lib.k3mla_decode_step_slots.argtypes = [P, P, P, I, P, P, P, I, P, P, P, I, I, I, I, I, I, I, F, F, P, I, P,
+                                                Z, P]
+        lib.k3mla_decode_step_slots.restype = I
         _lib = lib
         return lib
 
@@ -373,6 +376,20 @@ def k3mla_decode_step(q, k_new, v_new, gate, k_cache, v_cache, cache_len, N, H, 
                                int(rope_dim), float(rope_theta), float(scale), _ptr(out), _dtype(out),
                                _ptr(workspace), int(workspace.numel() * workspace.element_size()), _stream(stream))
     _check("k3mla_decode_step", st)
+
+
+def k3mla_decode_step_slots(q, k_new, v_new, gate, k_cache_pool, v_cache_pool, cache_len_pool, cache_idx,
+                            cache_idx_host, num_slots, N, H, dqk, dv, L_max, rope_dim, rope_theta, scale, out,
+                            workspace, stream=None):
+    """One decode token over a slot-indexed cache pool (see include/k3kda.h)."""
+    lib = load_library()
+    st = lib.k3mla_decode_step_slots(_ptr(q), _ptr(k_new), _ptr(v_new), _dtype(q), _ptr(gate), _ptr(k_cache_pool),
+                                     _ptr(v_cache_pool), _dtype(k_cache_pool), _ptr(cache_len_pool), _ptr(cache_idx),
+                                     _host_i32(cache_idx_host, "cache_idx_host"), int(num_slots), int(N), int(H),
+                                     int(dqk), int(dv), int(L_max), int(rope_dim), float(rope_theta), float(scale),
+                                     _ptr(out), _dtype(out), _ptr(workspace),
+                                     int(workspace.numel() * workspace.element_size()), _stream(stream))
+    _check("k3mla_decode_step_slots", st)
 
 
 def mla_decode_step(q, k_new, v_new, k_cache, v_cache, cache_len, gate=None, scale=None, rope_dim=0,

@@ -333,10 +333,10 @@ size_t k3mla_decode_workspace_size(int N, int H, int dqk, int dv, int L_max) {
     return mla_workspace(N, H, dqk, dv, L_max);
 }
 
-int k3mla_decode_step(const void *q, const void *k_new, const void *v_new, int in_dtype, const void *gate,
-                      void *k_cache, void *v_cache, int cache_dtype, int32_t *cache_len, int N, int H, int dqk,
-                      int dv, int L_max, int rope_dim, float rope_theta, float scale, void *out, int out_dtype,
-                      void *workspace, size_t workspace_bytes, void *stream) {
+static int mla_impl(const void *q, const void *k_new, const void *v_new, int in_dtype, const void *gate,
+                    void *k_cache, void *v_cache, int cache_dtype, int32_t *cache_len, int N, int H, int dqk, int dv,
+                    int L_max, int rope_dim, float rope_theta, float scale, void *out, int out_dtype, void *workspace,
+                    size_t workspace_bytes, void *stream, const int32_t *slot, int num_slots) {
     if (N < 0 || H < 1 || L_max < 1) return K3KDA_ERR_INVALID_ARG;
     if (!dtype_ok(in_dtype) || !dtype_ok(cache_dtype) || !dtype_ok(out_dtype)) return K3KDA_ERR_INVALID_ARG;
     if (rope_dim < 0 || (rope_dim & 1) || rope_dim > dqk) return K3KDA_ERR_INVALID_ARG;
@@ -354,7 +354,29 @@ int k3mla_decode_step(const void *q, const void *k_new, const void *v_new, int i
     return cuda_status(launch_mla_decode(q, k_new, v_new, in_dtype == K3KDA_BF16, gate, k_cache, v_cache,
                                          cache_dtype == K3KDA_BF16, cache_len, N, H, dqk, dv, L_max, rope_dim,
                                          rope_theta, scale, out, out_dtype == K3KDA_BF16, workspace,
-                                         static_cast<cudaStream_t>(stream)));
+                                         static_cast<cudaStream_t>(stream), slot, num_slots));
+}
+
+int k3mla_decode_step(const void *q, const void *k_new, const void *v_new, int in_dtype, const void *gate,
+                      void *k_cache, void *v_cache, int cache_dtype, int32_t *cache_len, int N, int H, int dqk,
+                      int dv, int L_max, int rope_dim, float rope_theta, float scale, void *out, int out_dtype,
+                      void *workspace, size_t workspace_bytes, void *stream) {
+    return mla_impl(q, k_new, v_new, in_dtype, gate, k_cache, v_cache, cache_dtype, cache_len, N, H, dqk, dv, L_max,
+                    rope_dim, rope_theta, scale, out, out_dtype, workspace, workspace_bytes, stream, nullptr, 0);
+}
+
+int k3mla_decode_step_slots(const void *q, const void *k_new, const void *v_new, int in_dtype, const void *gate,
+                            void *k_cache_pool, void *v_cache_pool, int cache_dtype, int32_t *cache_len_pool,
+                            const int32_t *cache_idx, const int32_t *cache_idx_host, int num_slots, int N, int H,
+                            int dqk, int dv, int L_max, int rope_dim, float rope_theta, float scale, void *out,
+                            int out_dtype, void *workspace, size_t workspace_bytes, void *stream) {
+    if (N < 0 || num_slots < 1 || (N > 0 && !cache_idx)) return K3KDA_ERR_INVALID_ARG;
+    if ((long long)num_slots * H > 0x7fffffffLL) return K3KDA_ERR_UNSUPPORTED;
+    if (!aligned4(cache_idx)) return K3KDA_ERR_ALIGNMENT;
+    if (cache_idx_host && !slots_ok(cache_idx_host, N, num_slots)) return K3KDA_ERR_INVALID_ARG;
+    return mla_impl(q, k_new, v_new, in_dtype, gate, k_cache_pool, v_cache_pool, cache_dtype, cache_len_pool, N, H,
+                    dqk, dv, L_max, rope_dim, rope_theta, scale, out, out_dtype, workspace, workspace_bytes, stream,
+                    cache_idx, num_slots);
 }
 
 }  // extern "C"

@@ -128,6 +128,6 @@ size_t mla_workspace(int N, int H, int dq, int dv, int L_max);
 cudaError_t launch_mla_decode(const void *q, const void *k_new, const void *v_new, int in_bf16, const void *gate,
                               void *k_cache, void *v_cache, int cache_bf16, int32_t *cache_len, int N, int H, int dq,
                               int dv, int L_max, int rope_dim, float theta, float scale, void *out, int out_bf16,
-                              void *ws, cudaStream_t st);
+                              void *ws, cudaStream_t st, const int32_t *slot = nullptr, int num_slots = 0);
 
 }  // namespace k3kda

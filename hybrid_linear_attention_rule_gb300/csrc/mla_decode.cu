@@ -41,13 +41,16 @@ struct MlaArgs {
     const void *gate;                // [N, H, d] or null
     void *k_cache, *v_cache;         // [N, H, L_max, d]
     int cache_bf16;
-    int32_t *cache_len;              // [N]
+    int32_t *cache_len;              // [N] (or [num_slots] with a slot map)
+    const int32_t *slot;             // [N] cache slot of each sequence, or null (slot n)
+    int num_slots;
     int N, H, dq, dv, L_max, rope_dim;   // dq: query/key width, dv: value width
     float theta, scale;
     void *out;                       // [N, H, d]
     int out_bf16;
     int S;                           // splits per (sequence, head)
-    int32_t *vlen;                   // workspace [N]: keys to attend, 0 = cache full
+    int32_t *vlen;                   // workspace [N]: keys to attend, 0 = cache full or slot invalid
+    int32_t *vslot;                  // workspace [N]: the cache slot of each sequence
     float *qs;                       // workspace [N, H, dq]: rotated query * scale * log2(e)
     float2 *ml;                      // workspace [N, H, S]: (max, sum) of each split, base-2 scores
     float *po;                       // workspace [N, H, S, dv]: unnormalised weighted values
@@ -58,9 +61,13 @@ struct MlaArgs {
 __global__ void __launch_bounds__(256) mla_append_kernel(const __grid_constant__ MlaArgs A) {
     __shared__ float cs[128], sn[128];                  // rope_dim <= dq <= 256
     const int n = blockIdx.x;
-    const int pos = A.cache_len[n];
+    const int sl = seq_slot(A.slot, A.num_slots, n);
+    const int pos = sl >= 0 ? A.cache_len[sl] : -1;
     const bool valid = pos >= 0 && pos < A.L_max;
-    if (threadIdx.x == 0) A.vlen[n] = valid ? pos + 1 : 0;
+    if (threadIdx.x == 0) {
+        A.vlen[n] = valid ? pos + 1 : 0;
+        A.vslot[n] = sl;
+    }
     if (!valid) return;
     const int half = A.rope_dim / 2;
     for (int i = threadIdx.x; i < half; i += blockDim.x) {
@@ -90,11 +97,11 @@ __global__ void __launch_bounds__(256) mla_append_kernel(const __grid_constant__
             kv = kv * cs[i] + kp * sgn;
         }
         A.qs[src] = qv * qmul;
-        store_elt(A.k_cache, (((size_t)n * A.H + h) * A.L_max + pos) * dq + c, kv, A.cache_bf16);
+        store_elt(A.k_cache, (((size_t)sl * A.H + h) * A.L_max + pos) * dq + c, kv, A.cache_bf16);
     }
     for (size_t e = threadIdx.x; e < HV; e += blockDim.x) {
         const int h = (int)(e / dv), c = (int)(e - (size_t)h * dv);
-        store_elt(A.v_cache, (((size_t)n * A.H + h) * A.L_max + pos) * dv + c,
+        store_elt(A.v_cache, (((size_t)sl * A.H + h) * A.L_max + pos) * dv + c,
                   load_elt(A.v_new, (size_t)n * HV + e, A.in_bf16), A.cache_bf16);
     }
 }
@@ -166,8 +173,9 @@ __global__ void __launch_bounds__(kWarps * 32, 4) mla_attend_kernel(const __grid
             q[e] = x.x; q[e + 1] = x.y;
         }
     }
-    const T *Kc = reinterpret_cast<const T *>(A.k_cache) + nh * (size_t)A.L_max * DQ + lane * EQ;
-    const T *Vc = reinterpret_cast<const T *>(A.v_cache) + nh * (size_t)A.L_max * DV + lane * EV;
+    const size_t ch = (size_t)A.vslot[n] * A.H + (nh - (size_t)n * A.H);   // the cache's (slot, head)
+    const T *Kc = reinterpret_cast<const T *>(A.k_cache) + ch * (size_t)A.L_max * DQ + lane * EQ;
+    const T *Vc = reinterpret_cast<const T *>(A.v_cache) + ch * (size_t)A.L_max * DV + lane * EV;
 
     float m = -INFINITY, l = 0.f, o[EV];
 #pragma unroll
@@ -286,7 +294,7 @@ __global__ void __launch_bounds__(128) mla_combine_kernel(const __grid_constant_
         if (A.gate) r *= sigmoidf_(load_elt(A.gate, nh * D + c, A.in_bf16));
         store_elt(A.out, nh * D + c, r, A.out_bf16);
     }
-    if (h == 0 && threadIdx.x == 0) A.cache_len[n] = len;
+    if (h == 0 && threadIdx.x == 0) A.cache_len[A.vslot[n]] = len;
 }
 
 template <int EQ, int EV, bool BF> void *attend_fn() { return (void *)mla_attend_kernel<EQ, EV, BF>; }
@@ -306,13 +314,13 @@ size_t mla_splits(int L_max) { return ((size_t)L_max + kSplit - 1) / kSplit; }
 size_t mla_workspace(int N, int H, int dq, int dv, int L_max) {
     auto r256 = [](size_t b) { return (b + 255) & ~size_t(255); };
     const size_t S = mla_splits(L_max), NH = (size_t)N * H;
-    return r256((size_t)N * 4) + r256(NH * dq * 4) + r256(NH * S * 8) + r256(NH * S * dv * 4);
+    return 2 * r256((size_t)N * 4) + r256(NH * dq * 4) + r256(NH * S * 8) + r256(NH * S * dv * 4);
 }
 
 cudaError_t launch_mla_decode(const void *q, const void *k_new, const void *v_new, int in_bf16, const void *gate,
                               void *k_cache, void *v_cache, int cache_bf16, int32_t *cache_len, int N, int H, int dq,
                               int dv, int L_max, int rope_dim, float theta, float scale, void *out, int out_bf16,
-                              void *ws, cudaStream_t st) {
+                              void *ws, cudaStream_t st, const int32_t *slot, int num_slots) {
     if (N == 0) return cudaSuccess;
     auto r256 = [](size_t b) { return (b + 255) & ~size_t(255); };
     MlaArgs A;
@@ -320,10 +328,12 @@ cudaError_t launch_mla_decode(const void *q, const void *k_new, const void *v_ne
     A.k_cache = k_cache; A.v_cache = v_cache; A.cache_bf16 = cache_bf16; A.cache_len = cache_len;
     A.N = N; A.H = H; A.dq = dq; A.dv = dv; A.L_max = L_max; A.rope_dim = rope_dim; A.theta = theta; A.scale = scale;
     A.out = out; A.out_bf16 = out_bf16;
+    A.slot = slot; A.num_slots = num_slots;
     A.S = (int)mla_splits(L_max);
     const size_t NH = (size_t)N * H;
     char *p = static_cast<char *>(ws);
     A.vlen = reinterpret_cast<int32_t *>(p);  p += r256((size_t)N * 4);
+    A.vslot = reinterpret_cast<int32_t *>(p); p += r256((size_t)N * 4);
     A.qs = reinterpret_cast<float *>(p);      p += r256(NH * dq * 4);
     A.ml = reinterpret_cast<float2 *>(p);     p += r256(NH * A.S * 8);
     A.po = reinterpret_cast<float *>(p);

@@ -348,6 +348,20 @@ int k3mla_decode_step(const void *q, const void *k_new, const void *v_new, int i
                       int N, int H, int dqk, int dv, int L_max, int rope_dim, float rope_theta, float scale,
                       void *out, int out_dtype, void *workspace, size_t workspace_bytes, void *stream);
 
+/* The same token step over a slot-indexed cache pool (continuous batching: the hybrid cache's
+ * slot identity, as for the KDA state pools): sequence n reads and appends to slot cache_idx[n]
+ * of k_cache_pool [num_slots, H, L_max, dqk], v_cache_pool [num_slots, H, L_max, dv] and
+ * cache_len_pool int32 [num_slots]; q, k_new, v_new, gate and out stay indexed by n.  cache_idx is
+ * int32 [N] in device memory; a sequence whose entry is outside [0, num_slots) gets NaN outputs
+ * and writes nothing.  When cache_idx_host (a host copy) is given it is checked: every entry in
+ * range and none repeated (two sequences appending to one slot would race), else INVALID_ARG.
+ * The workspace is k3mla_decode_workspace_size(N, ...) bytes; errors as k3mla_decode_step. */
+int k3mla_decode_step_slots(const void *q, const void *k_new, const void *v_new, int in_dtype, const void *gate,
+                            void *k_cache_pool, void *v_cache_pool, int cache_dtype, int32_t *cache_len_pool,
+                            const int32_t *cache_idx, const int32_t *cache_idx_host, int num_slots,
+                            int N, int H, int dqk, int dv, int L_max, int rope_dim, float rope_theta, float scale,
+                            void *out, int out_dtype, void *workspace, size_t workspace_bytes, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

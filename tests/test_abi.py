@@ -239,5 +239,27 @@ def test_mla_workspace_size(lib):
     r = lambda b: (b + 255) // 256 * 256
     N, H, d, L = 256, 32, 128, 8192
     S = L // 512
-    assert K.k3mla_decode_workspace_size(N, H, d, d, L) == r(N * 4) + r(N * H * d * 4) + r(N * H * S * 8) + r(N * H * S * d * 4)
-    assert K.k3mla_decode_workspace_size(3, 2, 192, 64, 513) == r(12) + r(3 * 2 * 192 * 4) + r(3 * 2 * 2 * 8) + r(3 * 2 * 2 * 64 * 4)
+    # per sequence: keys to attend and cache slot; per (sequence, head): the query, and per split the
+    # (max, sum) pair and the weighted value row
+    assert K.k3mla_decode_workspace_size(N, H, d, d, L) == 2 * r(N * 4) + r(N * H * d * 4) + r(N * H * S * 8) + \
+        r(N * H * S * d * 4)
+    assert K.k3mla_decode_workspace_size(3, 2, 192, 64, 513) == 2 * r(12) + r(3 * 2 * 192 * 4) + r(3 * 2 * 2 * 8) + \
+        r(3 * 2 * 2 * 64 * 4)
+
+
+def test_mla_slot_call_validates_the_map(lib):
+    def call(**kw):
+        a = dict(q=A16, k=A16, v=A16, in_dtype=1, gate=None, kc=A16, vc=A16, cache_dtype=1, lens=A16, idx=A16,
+                 idx_h=None, slots=8, N=3, H=2, dq=128, dv=128, L_max=1024, rope_dim=0, theta=10000.0, scale=1.0,
+                 out=A16, out_dtype=1, ws=None, ws_bytes=0, stream=None)
+        a.update(kw)
+        return lib.k3mla_decode_step_slots(*a.values())
+    assert call(idx=None) == -1
+    assert call(slots=0) == -1
+    assert call(idx=ctypes.c_void_p(0x10002)) == -3      # int32 map off a 4-byte boundary
+    dup, dup_p = _i32(1, 1, 2)
+    assert call(idx_h=dup_p) == -1                       # a slot twice
+    far, far_p = _i32(1, 8, 2)
+    assert call(idx_h=far_p) == -1                       # outside the pool
+    ok, ok_p = _i32(7, 0, 2)
+    assert call(idx_h=ok_p) == -4                        # the map passes; the missing workspace does not

@@ -179,3 +179,37 @@ def test_mla_decode_full_size_sampled():
         assert np.array_equal(f64(kc[n, h, :p]), kh[:p]), "cached rows changed"
     del kc, vc
     torch.cuda.empty_cache()
+
+
+def test_mla_decode_slot_pool():
+    """Continuous batching: 4 sequences over a pool of 7 cache slots.  Mapped slots match the oracle
+    run on the gathered caches (outputs, appended rows, lengths); unmapped slots stay bit for bit;
+    entries outside the pool give NaN outputs and write nothing."""
+    P, H, d, dv, L = 7, 2, 192, 128, 700
+    pool = KI.mla_decode_case("mla_pool", P, H, d, L, (0, 650), seed=21, rope_dim=64, dv=dv)
+    tok = KI.mla_decode_case("mla_tok", 4, H, d, 8, [0, 0, 0, 0], seed=22, rope_dim=64, dv=dv)
+    t = _to_dev(pool)
+    q, k, v, g = (dev_tensor(x, True) for x in (tok.q, tok.k_new, tok.v_new, tok.gate))
+    for idx, checked in (([5, 0, 3, 6], True), ([5, 9, 3, -2], False)):
+        kc0, vc0, len0 = to_np(t["kc"]).copy(), to_np(t["vc"]).copy(), to_np(t["lens"]).copy()
+        cache_idx = torch.tensor(idx, dtype=torch.int32)
+        out = torch.empty(4, H, dv, dtype=torch.float32, device="cuda")
+        ws = torch.empty(K.k3mla_decode_workspace_size(4, H, d, dv, L), dtype=torch.uint8, device="cuda")
+        K.k3mla_decode_step_slots(q, k, v, g, t["kc"], t["vc"], t["lens"], cache_idx.cuda(),
+                                  cache_idx if checked else None, P, 4, H, d, dv, L, 64, pool.theta, d ** -0.5, out, ws)
+        torch.cuda.synchronize()
+        good = [j for j, sidx in enumerate(idx) if 0 <= sidx < P]
+        sl = [idx[j] for j in good]
+        ref, kr, vr, lr = OM.decode_step(tok.q[good], tok.k_new[good], tok.v_new[good], kc0[sl], vc0[sl], len0[sl],
+                                         d ** -0.5, gate=tok.gate[good], rope_dim=64, theta=pool.theta,
+                                         cache_bf16=True)
+        got = to_np(out).astype(np.float64)
+        _check_out(got[good], ref, False, False, "slots")
+        assert np.all(np.isnan(got[[j for j in range(4) if j not in good]]))
+        kc, vc, ln = to_np(t["kc"]), to_np(t["vc"]), to_np(t["lens"])
+        assert np.array_equal(ln[sl], lr)
+        assert np.array_equal(vc[sl].astype(np.float64), vr)
+        assert np.all(np.abs(kc[sl].astype(np.float64) - kr) <= 2.0 ** -8 * np.abs(kr) + 1e-30)
+        rest = [x for x in range(P) if x not in sl]
+        assert np.array_equal(kc[rest], kc0[rest]) and np.array_equal(vc[rest], vc0[rest])
+        assert np.array_equal(ln[rest], len0[rest])
