@@ -10,7 +10,10 @@ One step = one pass of the whole mixer hot path on synthetic inputs:
     gate.
 value = (prefill tokens + decode tokens) per step / step time, device-resident
 inputs; the "prefill" and "decode" objects give each part on its own with its
-roofline.  With --gpus N under torchrun every rank runs its own replica of the
+roofline.  Beside the step, not in value: "e2e" (the same step from pinned host
+buffers), "backward" (gradients of the recurrence, T=8192, H=32) and "mla_decode"
+(one decode token of the hybrid's attention layers, 256 sequences with bf16 caches
+of 8192 rows).  With --gpus N under torchrun every rank runs its own replica of the
 step (heads and sequences never interact, so there is no collective): weak
 scaling, max time over ranks.
 
