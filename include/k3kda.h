@@ -20,6 +20,11 @@
  *     o_t = scale * S_t^T q_t          (then o_t * sigmoid(gate_t) if gated)
  * with S in R^{dk x dv} kept in FP32.
  *
+ * Entry points: the causal short conv, the chunked prefill (plain, slot-pooled, without a
+ * workspace), the decode step (plain, slot-pooled), the gradients of the recurrence, and the
+ * decode token of the hybrid's other layer kind, gated attention (k3mla_*), each described where
+ * it is declared.
+ *
  * Conventions shared by every entry point
  *   - All tensor pointers are DEVICE pointers unless a name ends in _host.
  *     Every buffer is owned by the caller; the library allocates nothing and
@@ -31,8 +36,10 @@
  *   - Every entry point returns a k3kda_status.  Arguments are checked on the
  *     host before anything is launched; an invalid call launches nothing and
  *     returns a negative status.  Nothing aborts, throws or prints.
- *   - Supported head dims: dk, dv in {16, 32, ..., 128} (multiples of 16).
- *     Conv width W in {1, 2, 3, 4}.  Chunk in {16, 32, 64}.
+ *   - Supported head dims: dk, dv in {16, 32, ..., 128} (multiples of 16),
+ *     unless an entry point says otherwise (the backward takes 128, the
+ *     attention calls their own widths).  Conv width W in {1, 2, 3, 4}.
+ *     Chunk in {16, 32, 64}.
  *   - Element types: q, k, v and gate share one type (k3kda_dtype); g, beta,
  *     conv weights and all states are FP32.  Pointers must be 16-byte aligned,
  *     except beta, which needs 4-byte alignment (so token slices of it work).
