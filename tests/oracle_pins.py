@@ -382,12 +382,43 @@ def pin_backward_single_token_closed_form(lib):
     return err, 1e-13
 
 
+def pin_backward_autograd(lib):
+    """The reverse-mode gradients equal torch autograd (float64) through a plain token-by-token
+    forward of the gated delta rule, to rounding: an exact check, independent of the oracle's
+    hand-written reverse sweep (varlen, two heads, initial state, final-state gradient)."""
+    import torch
+    rng = np.random.default_rng(33)
+    cu = [0, 5, 5, 12]
+    T, H, dk, dv = 12, 2, 3, 4
+    arrs = dict(q=_rand(rng, T, H, dk), k=0.6 * _rand(rng, T, H, dk), v=_rand(rng, T, H, dv),
+                g=-0.4 * np.abs(_rand(rng, T, H, dk)), beta=rng.uniform(0.1, 0.9, (T, H)),
+                S0=0.3 * _rand(rng, 3, H, dk, dv))
+    dO, dSf, scale = _rand(rng, T, H, dv), _rand(rng, 3, H, dk, dv), 0.55
+    ts = {kk: torch.tensor(vv, dtype=torch.float64, requires_grad=True) for kk, vv in arrs.items()}
+    loss = torch.zeros((), dtype=torch.float64)
+    for n in range(3):
+        for h in range(H):
+            S = ts["S0"][n, h]
+            for t in range(cu[n], cu[n + 1]):
+                kt, vt, qt = ts["k"][t, h], ts["v"][t, h], ts["q"][t, h]
+                P = torch.exp(ts["g"][t, h])[:, None] * S
+                S = P + ts["beta"][t, h] * torch.outer(kt, vt - P.T @ kt)
+                loss = loss + (scale * (S.T @ qt) * torch.from_numpy(dO[t, h])).sum()
+            loss = loss + (S * torch.from_numpy(dSf[n, h])).sum()
+    loss.backward()
+    gr = O.recurrent_backward(arrs["q"], arrs["k"], arrs["v"], arrs["g"], arrs["beta"], dO, initial_state=arrs["S0"],
+                              dS_final=dSf, cu_seqlens=np.array(cu, dtype=np.int32), scale=scale, lib=lib)
+    names = dict(q="dq", k="dk", v="dv", g="dg", beta="dbeta", S0="dS0")
+    err = max(float(np.abs(ts[nm].grad.numpy() - gr[names[nm]]).max()) for nm in names)
+    return err, 1e-12
+
+
 ALL_PINS = [pin_single_token_closed_form, pin_pure_decay, pin_orthonormal_delta_rule,
             pin_repeated_key_overwrites, pin_linearity, pin_exact_rational, pin_bruteforce_agrees,
             pin_gate_is_sigmoid, pin_state_chaining, pin_varlen_is_independent,
             pin_chunked_equals_recurrent, pin_conv_matches_numpy, pin_conv_chaining, pin_l2norm,
             pin_decode_is_one_more_token, pin_mixer_composition, pin_backward_finite_differences,
-            pin_backward_single_token_closed_form]
+            pin_backward_single_token_closed_form, pin_backward_autograd]
 
 
 def failing_pins(lib):
