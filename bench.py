@@ -40,7 +40,7 @@ PREFILL = dict(T=65536, H=32, d=128, chunk=64, W=4)
 DECODE = dict(N=256, H=32, d=128, W=4)
 BACKWARD = dict(T=8192, H=32, d=128)      # gradients of the recurrence: the chunked-prefill shape
 MLA = dict(N=256, H=32, d=128, L_max=8192)   # the attention layers' decode token: the decode batch
-MLA_TRAFFIC_PER_KEY_HEAD = 1.388246e9 / ((84420 + 16) * 32)   # DRAM bytes per attended (key, head), measured
+MLA_TRAFFIC_PER_KEY_HEAD = 1.385983e9 / ((84420 + 16) * 32)   # DRAM bytes per attended (key, head), measured
 
 
 def parse():
@@ -357,7 +357,7 @@ def run_mla(args, K, torch, dev, rank, world):
     by, fl = mla_work(lens_np, H, d)
     pk = peaks()
     ach = by / (ms / 1e3) / 1e9
-    # DRAM bytes of the attention kernel from one ncu capture of the 16-sequence case (1.3882 GB for
+    # DRAM bytes of the attention kernel from one ncu capture of the 16-sequence case (1.3860 GB for
     # 84420 cached keys per head), scaled by the keys attended: traffic grows in proportion to them
     traffic = MLA_TRAFFIC_PER_KEY_HEAD * float(np.sum(lens_np.astype(np.int64) + 1)) * H
     del kc, vc
