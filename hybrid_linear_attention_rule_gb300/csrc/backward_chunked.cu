@@ -20,13 +20,15 @@
 //   dq = dQt e^{G'},  dk = dKt e^{G'} + dKh e^{-G'},
 //   dGamma = dQt o Qt + dKt o Kt - dKh o Kh  (+ rowsum(S_next o Dout) on the chunk's last row),
 //   dg = the in-chunk suffix sum of dGamma.
-// (r cancels from every output, so it is held constant.)  Four launches:
+// (r cancels from every output, so it is held constant.)  Launches, after the chunk table (its
+// offsets per sequence, then first token, length and sequence of each chunk):
 //   1. prep    one CTA per (chunk, head): the tiles above, Tm by forward substitution;
 //   2. forward one CTA per (sequence, head, 32-column block of dv): the states at chunk starts;
 //   3. chain   one CTA per (sequence, head, 16-column block), chunks in reverse: dX, dR and Din,
 //              with dS0 at the sequence start; it needs no forward state, so 2 and 3 are one
 //              launch whose CTAs run side by side;
-//   4. grads   one CTA per (chunk, head): dq, dk, dv, dg, dbeta.
+//   4. grads   two CTAs per (chunk, head), one per half of the dk columns: dq, dk, dv, dg and
+//              each half's share of dbeta.
 // Everything runs in fp32 on CUDA cores.  Chunks of 16 tokens keep e^{+-G'} small, so the
 // cancellations in dGamma stay at fp32 rounding level.
 #include <cuda_runtime.h>
