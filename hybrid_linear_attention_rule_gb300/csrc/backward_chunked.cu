@@ -3,34 +3,37 @@
 // The recurrence S_t = (I - beta_t k_t k_t^T) Diag(exp g_t) S_{t-1} + beta_t k_t v_t^T,
 // o_t = scale S_t^T q_t (the ungated core of the mixer, "Experimental Native Vulkan Backend for
 // Kimi K3", Hugging Face discussion #187, feature list) is written per chunk of kC tokens in the
-// WY form the forward uses: with Gamma the in-chunk cumulative log decay, r a per-channel centre
-// (half the chunk's first and last Gamma) and G' = Gamma - r,
-//   Qt = q e^{G'},  Kt = k e^{G'},  Kh = k e^{-G'},  B = strict_lower(Kt Kh^T),
-//   Aqk = lower(Qt Kh^T),  Tm = (I + diag(beta) B)^-1,  W = Tm diag(beta) Kt,  U = Tm diag(beta) V,
-//   S' = e^{r} S,  Delta = U - W S',  O = scale (Qt S' + Aqk Delta),
-//   S_next = e^{Gamma_L - r} (S' + Kh^T Delta).
+// WY form the forward uses.  With Gamma the in-chunk cumulative log decay (per channel), Gamma_L
+// its value at the chunk's last token, and
+//   Q0 = q e^{Gamma},  K0 = k e^{Gamma},  Kd = k e^{Gamma_L - Gamma}            (all factors <= 1)
+//   B_ij = sum_c k_ic k_jc e^{Gamma_ic - Gamma_jc} (j < i),  Aqk_ij = sum_c q_ic k_jc e^{...} (j <= i),
+//   Tm = (I + diag(beta) B)^-1,  W = Tm diag(beta) K0,  U = Tm diag(beta) V,
+//   Delta = U - W S,  O = scale (Q0 S + Aqk Delta),  S_next = e^{Gamma_L} S + Kd^T Delta.
 // Differentiating these products (the chain rule on the chunk algebra) gives, for the gradient
 // Dout reaching S_next and dO of the chunk's outputs (dOs = scale dO):
-//   dX = e^{Gamma_L - r} Dout,  dDelta = Kh dX + Aqk^T dOs,  dR = Tm^T dDelta,
-//   Din = e^{r} (dX + Qt^T dOs - Kt^T diag(beta) dR)        (the gradient reaching S),
-//   dA = -strict_lower(dR Delta^T),  dAqk = lower(dOs Delta^T),
-//   dQt = dOs S'^T + dAqk Kh,  dKt = diag(beta) (dA Kh - dR S'^T),
-//   dKh = Delta dX^T + dAqk^T Qt + dA^T diag(beta) Kt,  dv = diag(beta) dR,
-//   dbeta = rowsum((V - Kt S') o dR) + rowsum(dA o B),
-//   dq = dQt e^{G'},  dk = dKt e^{G'} + dKh e^{-G'},
-//   dGamma = dQt o Qt + dKt o Kt - dKh o Kh  (+ rowsum(S_next o Dout) on the chunk's last row),
+//   dDelta = Kd Dout + Aqk^T dOs,  dR = Tm^T dDelta,
+//   Din = e^{Gamma_L} Dout + Q0^T dOs - K0^T diag(beta) dR        (the gradient reaching S),
+//   dA = -strict_lower(dR Delta^T),  dAqk = lower(dOs Delta^T),  dv = diag(beta) dR,
+//   dq  = (dOs S^T) e^{Gamma} + P1,          P1_ic = sum_{j <= i} dAqk_ij k_jc e^{Gamma_ic - Gamma_jc}
+//   dkt = beta (P2 - (dR S^T) e^{Gamma}),    P2_ic = sum_{j < i}  dA_ij  k_jc e^{Gamma_ic - Gamma_jc}
+//   dkh = (Delta Dout^T) e^{Gamma_L - Gamma} + P3 + P4,
+//         P3_jc = sum_{i >= j} dAqk_ij q_ic e^{Gamma_ic - Gamma_jc},
+//         P4_jc = sum_{i > j} dA_ij beta_i k_ic e^{Gamma_ic - Gamma_jc},
+//   dk = dkt + dkh,  dbeta = rowsum((V - K0 S) o dR) + rowsum(dA o B),
+//   dGamma = q o dq + k o dkt - k o dkh  (+ rowsum(S_next o Dout) on the chunk's last row),
 //   dg = the in-chunk suffix sum of dGamma.
-// (r cancels from every output, so it is held constant.)  Launches, after the chunk table (its
-// offsets per sequence, then first token, length and sequence of each chunk):
+// Every exponential is of a non-positive argument (Gamma is non-increasing), so nothing overflows
+// whatever the decay: the pairwise products B, Aqk and P1..P4 take e^{-|Gamma_i - Gamma_j|}
+// element by element instead of factoring it through a reference.  Launches, after the chunk table
+// (its offsets per sequence, then first token, length and sequence of each chunk):
 //   1. prep    one CTA per (chunk, head): the tiles above, Tm by forward substitution;
 //   2. forward one CTA per (sequence, head, 32-column block of dv): the states at chunk starts;
-//   3. chain   one CTA per (sequence, head, 16-column block), chunks in reverse: dX, dR and Din,
+//   3. chain   one CTA per (sequence, head, 16-column block), chunks in reverse: Dout, dR and Din,
 //              with dS0 at the sequence start; it needs no forward state, so 2 and 3 are one
 //              launch whose CTAs run side by side;
 //   4. grads   two CTAs per (chunk, head), one per half of the dk columns: dq, dk, dv, dg and
 //              each half's share of dbeta.
-// Everything runs in fp32 on CUDA cores.  Chunks of 16 tokens keep e^{+-G'} small, so the
-// cancellations in dGamma stay at fp32 rounding level.
+// Everything runs in fp32 on CUDA cores; chunks of 16 tokens keep the products short.
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 
@@ -60,11 +63,11 @@ struct CbArgs {
     int32_t *chunk_off;            // [N + 1]
     int32_t *ck_t0, *ck_len, *ck_seq;   // [Q]: first token, length and sequence of each chunk
     // per (chunk, head) item, fp32
-    float *Qt, *Kt, *Kh, *E, *W, *U;   // [item][kC][kD]
+    float *Q0, *K0, *Kd, *Gm, *W, *U;  // [item][kC][kD]  (Gm: the in-chunk cumulative log decay)
     float *Tm, *Aqk, *Bm;              // [item][kC][kC]
-    float *rr, *glr;                   // [item][kD]
+    float *gl;                         // [item][kD]      Gamma_L
     float *Dl, *dR;                    // [item][kC][kD]
-    float *dX;                         // [item][kD][kD]
+    float *Dn;                         // [item][kD][kD]  Dout: the gradient reaching the chunk's S_next
     float *St;                         // [(Q + N) * H][kD][kD]: state at each chunk start, then the final
     float *dq, *dk, *dv, *dg, *dbeta, *dS0;
 };
@@ -135,48 +138,53 @@ __device__ __forceinline__ void zero(float (&acc)[TM][TN]) {
 // ---- 1. prep: one CTA per (chunk, head) ---------------------------------------------------------
 
 __global__ void __launch_bounds__(kThreads) cb_prep_kernel(const __grid_constant__ CbArgs A) {
-    __shared__ float sG[kC][LD], sQt[kC][LD], sKt[kC][LD], sKh[kC][LD];
+    __shared__ float sG[kC][LD], sQ[kC][LD], sK[kC][LD], sX[kC][LD];
     __shared__ float sB[kC][LC], sT[kC][LC];
-    __shared__ float sBeta[kC], sR[kD];
+    __shared__ float sBeta[kC];
     const int tid = threadIdx.x;
     const int item = blockIdx.x, qc = item / A.H, h = item % A.H, H = A.H;
     if (qc >= A.chunk_off[A.N]) return;                // the grid covers an upper bound of the chunks
     const int t0 = A.ck_t0[qc], L = A.ck_len[qc];
     for (int e = tid; e < kC * kD; e += kThreads) {
         const int i = e / kD, c = e % kD;
-        sG[i][c] = i < L ? A.g[((size_t)(t0 + i) * H + h) * kD + c] : 0.f;
+        const size_t src = ((size_t)(t0 + i) * H + h) * kD + c;
+        sG[i][c] = i < L ? A.g[src] : 0.f;
+        sQ[i][c] = i < L ? ld_x(A.q, src, A.bf16) : 0.f;
+        sK[i][c] = i < L ? ld_x(A.k, src, A.bf16) : 0.f;
     }
     if (tid < kC) sBeta[tid] = tid < L ? A.beta[(size_t)(t0 + tid) * H + h] : 0.f;
     __syncthreads();
     if (tid < kD) {
         float run = 0.f;
         for (int i = 0; i < kC; ++i) { run += sG[i][tid]; sG[i][tid] = run; }
-        const float r = 0.5f * (sG[0][tid] + sG[L - 1][tid]);
-        sR[tid] = r;
-        A.rr[(size_t)item * kD + tid] = r;
-        A.glr[(size_t)item * kD + tid] = sG[L - 1][tid] - r;
+        A.gl[(size_t)item * kD + tid] = sG[L - 1][tid];
     }
     __syncthreads();
     const size_t tile = (size_t)item * kC * kD;
     for (int e = tid; e < kC * kD; e += kThreads) {
         const int i = e / kD, c = e % kD;
-        const float gp = fminf(fmaxf(sG[i][c] - sR[c], -87.f), 87.f);
-        const float ex = expf(gp), exi = expf(-gp);
-        const size_t src = ((size_t)(t0 + i) * H + h) * kD + c;
-        const float qv = i < L ? ld_x(A.q, src, A.bf16) : 0.f, kv = i < L ? ld_x(A.k, src, A.bf16) : 0.f;
-        const float qt = qv * ex, kt = kv * ex, kh = kv * exi;
-        sQt[i][c] = qt; sKt[i][c] = kt; sKh[i][c] = kh;
-        A.Qt[tile + e] = qt; A.Kt[tile + e] = kt; A.Kh[tile + e] = kh; A.E[tile + e] = ex;
+        const float gm = sG[i][c], ea = expf(gm), ed = expf(sG[kC - 1][c] - gm);
+        const float k0 = sK[i][c] * ea;
+        A.Q0[tile + e] = sQ[i][c] * ea;
+        A.K0[tile + e] = k0;
+        A.Kd[tile + e] = sK[i][c] * ed;
+        A.Gm[tile + e] = gm;
+        sX[i][c] = sBeta[i] * k0;                      // beta K0, the right factor of W
     }
-    __syncthreads();
     {
-        // B = strict_lower(Kt Kh^T), Aqk = lower(Qt Kh^T): one element per thread
-        float b1[1][1], b2[1][1];
-        zero(b1); zero(b2);
-        mm<kC, kC, 1, 1>(b1, &sKt[0][0], LD, 1, &sKh[0][0], 1, LD, kD);
-        mm<kC, kC, 1, 1>(b2, &sQt[0][0], LD, 1, &sKh[0][0], 1, LD, kD);
+        // B = strict_lower, Aqk = lower of the decayed products, one element (i, j) per thread, each
+        // term with its own exponential e^{Gamma_ic - Gamma_jc} <= 1 (j <= i)
         const int i = tid / kC, j = tid % kC;
-        const float bv = j < i ? b1[0][0] : 0.f, av = j <= i ? b2[0][0] : 0.f;
+        float b1 = 0.f, b2 = 0.f;
+        if (j <= i) {
+#pragma unroll 4
+            for (int c = 0; c < kD; ++c) {
+                const float t = sK[j][c] * expf(sG[i][c] - sG[j][c]);
+                b1 = fmaf(sK[i][c], t, b1);
+                b2 = fmaf(sQ[i][c], t, b2);
+            }
+        }
+        const float bv = j < i ? b1 : 0.f, av = j <= i ? b2 : 0.f;
         sB[i][j] = bv;
         A.Bm[(size_t)item * kC * kC + tid] = bv;
         A.Aqk[(size_t)item * kC * kC + tid] = av;
@@ -197,17 +205,16 @@ __global__ void __launch_bounds__(kThreads) cb_prep_kernel(const __grid_constant
     }
     __syncthreads();
     A.Tm[(size_t)item * kC * kC + tid] = sT[tid / kC][tid % kC];
-    // W = Tm diag(beta) Kt, U = Tm diag(beta) V (V into sG, Kt scaled by beta in place)
+    // W = Tm diag(beta) K0, U = Tm diag(beta) V (beta V into sG, whose Gamma is no longer needed)
     for (int e = tid; e < kC * kD; e += kThreads) {
         const int i = e / kD, c = e % kD;
         sG[i][c] = i < L ? sBeta[i] * ld_x(A.v, ((size_t)(t0 + i) * H + h) * kD + c, A.bf16) : 0.f;
-        sKt[i][c] *= sBeta[i];
     }
     __syncthreads();
     {
         float w[1][8], u[1][8];
         zero(w); zero(u);
-        mm<kC, kD, 1, 8>(w, &sT[0][0], LC, 1, &sKt[0][0], LD, 1, kC);
+        mm<kC, kD, 1, 8>(w, &sT[0][0], LC, 1, &sX[0][0], LD, 1, kC);
         mm<kC, kD, 1, 8>(u, &sT[0][0], LC, 1, &sG[0][0], LD, 1, kC);
         const int i = tid / (kD / 8), tn = tid % (kD / 8);
 #pragma unroll
@@ -251,20 +258,19 @@ __device__ __forceinline__ void stage_vec(float *dst, const float *src, int n) {
 constexpr int kFV = 32;                                // dv columns of a forward-chain CTA
 constexpr int kFN = kD / kFV;
 struct FwdStage {
-    float W[kC][kD], Kh[kC][kD], U[kC][kFV], rr[kD], glr[kD];
+    float W[kC][kD], Kd[kC][kD], U[kC][kFV], gl[kD];
 };
 constexpr int kFS = 2;                                 // forward chain: stages in the ring
 
 __device__ __forceinline__ void stage_fwd(const CbArgs &A, FwdStage &st, size_t item, int cb) {
     const size_t tile = item * kC * kD;
     stage_tile(&st.W[0][0], kD, A.W + tile);
-    stage_tile(&st.Kh[0][0], kD, A.Kh + tile);
+    stage_tile(&st.Kd[0][0], kD, A.Kd + tile);
     for (int e = threadIdx.x; e < kC * (kFV / 4); e += kThreads) {
         const int i = e / (kFV / 4), p = e % (kFV / 4);
         cp16(&st.U[i][p * 4], A.U + tile + (size_t)i * kD + cb + p * 4);
     }
-    stage_vec(st.rr, A.rr + item * kD, kD);
-    stage_vec(st.glr, A.glr + item * kD, kD);
+    stage_vec(st.gl, A.gl + item * kD, kD);
     cp_commit();
 }
 
@@ -272,7 +278,7 @@ constexpr int LF = kFV + 4;        // 16-byte aligned rows of Delta
 constexpr int LT = kD + 4;         // 16-byte aligned rows of a transposed 128-row tile
 struct FwdSmem {
     FwdStage stg[kFS];
-    float sSpT[kFV][LT], sDl[kC][LF];              // S' transposed: column j of S' is row j
+    float sSpT[kFV][LT], sDl[kC][LF];              // S transposed: column j of S is row j
 };
 
 __device__ __forceinline__ void forward_chain(const CbArgs &A, uint8_t *dyn, int bid) {
@@ -306,12 +312,8 @@ __device__ __forceinline__ void forward_chain(const CbArgs &A, uint8_t *dyn, int
         cp_wait<kFS - 1>();
         const FwdStage &st = stg[c % kFS];
         __syncthreads();                               // chunk c's tiles are in
-        const float er = expf(st.rr[r]);
 #pragma unroll
-        for (int u = 0; u < 16; ++u) {
-            S[u] *= er;
-            sSpT[c0 + u][r] = S[u];
-        }
+        for (int u = 0; u < 16; ++u) sSpT[c0 + u][r] = S[u];
         __syncthreads();
         {
             const float *w = st.W[di], *x0 = sSpT[dj], *x1 = sSpT[dj + 16];
@@ -332,12 +334,14 @@ __device__ __forceinline__ void forward_chain(const CbArgs &A, uint8_t *dyn, int
             dlg[dj + 16] = d1;
         }
         __syncthreads();
+        // S_next = e^{Gamma_L} S + Kd^T Delta
+        const float eg = expf(st.gl[r]);
         float acc[16];
 #pragma unroll
-        for (int u = 0; u < 16; ++u) acc[u] = S[u];
+        for (int u = 0; u < 16; ++u) acc[u] = eg * S[u];
 #pragma unroll
         for (int i = 0; i < kC; ++i) {
-            const float khv = st.Kh[i][r];
+            const float khv = st.Kd[i][r];
 #pragma unroll
             for (int u = 0; u < 16; u += 4) {
                 const float4 d4 = *reinterpret_cast<const float4 *>(&sDl[i][c0 + u]);
@@ -345,9 +349,8 @@ __device__ __forceinline__ void forward_chain(const CbArgs &A, uint8_t *dyn, int
                 acc[u + 2] = fmaf(khv, d4.z, acc[u + 2]); acc[u + 3] = fmaf(khv, d4.w, acc[u + 3]);
             }
         }
-        const float eg = expf(st.glr[r]);
 #pragma unroll
-        for (int u = 0; u < 16; ++u) S[u] = eg * acc[u];
+        for (int u = 0; u < 16; ++u) S[u] = acc[u];
         __syncthreads();                               // buffer c % kFS is refilled for chunk c + kFS
     }
 }
@@ -355,18 +358,18 @@ __device__ __forceinline__ void forward_chain(const CbArgs &A, uint8_t *dyn, int
 // ---- 3. chain: gradients at chunk boundaries, chunks in reverse ----------------------------------
 
 struct ChainStage {
-    float Kh[kC][kD], Qt[kC][kD], Kt[kC][kD];
+    float Kd[kC][kD], Q0[kC][kD], K0[kC][kD];
     float Aqk[kC][kC], Tm[kC][kC], dO[kC][kBV];
-    float rr[kD], glr[kD], beta[kC];
+    float gl[kD], beta[kC];
 };
 constexpr int kCS = 2;                                 // backward chain: stages in the ring
 
 __device__ __forceinline__ void stage_chain(const CbArgs &A, ChainStage &st, size_t item, int qc, int h, int cb) {
     const size_t tile = item * kC * kD, small = item * kC * kC;
     const int t0 = A.ck_t0[qc], L = A.ck_len[qc], H = A.H;
-    stage_tile(&st.Kh[0][0], kD, A.Kh + tile);
-    stage_tile(&st.Qt[0][0], kD, A.Qt + tile);
-    stage_tile(&st.Kt[0][0], kD, A.Kt + tile);
+    stage_tile(&st.Kd[0][0], kD, A.Kd + tile);
+    stage_tile(&st.Q0[0][0], kD, A.Q0 + tile);
+    stage_tile(&st.K0[0][0], kD, A.K0 + tile);
     stage_vec(&st.Aqk[0][0], A.Aqk + small, kC * kC);
     stage_vec(&st.Tm[0][0], A.Tm + small, kC * kC);
     for (int e = threadIdx.x; e < kC * (kBV / 4); e += kThreads) {
@@ -374,8 +377,7 @@ __device__ __forceinline__ void stage_chain(const CbArgs &A, ChainStage &st, siz
         const int ti = i < L ? t0 + i : t0;            // rows past the chunk's end are zero-filled
         cp16z(&st.dO[i][p * 4], A.dO + ((size_t)ti * H + h) * kD + cb + p * 4, i < L ? 16 : 0);
     }
-    stage_vec(st.rr, A.rr + item * kD, kD);
-    stage_vec(st.glr, A.glr + item * kD, kD);
+    stage_vec(st.gl, A.gl + item * kD, kD);
     if (threadIdx.x < kC) {
         // beta is strided by H: 4-byte pieces
         const int i = threadIdx.x;
@@ -390,7 +392,7 @@ __device__ __forceinline__ void stage_chain(const CbArgs &A, ChainStage &st, siz
 constexpr int LQ = kBV + 4;        // 16-byte aligned rows of beta dR
 struct ChainSmem {
     ChainStage stg[kCS];
-    float sdXT[kBV][LT], sdD[kC][LB], sbR[kC][LQ];  // dX transposed: column j of dX is row j
+    float sdXT[kBV][LT], sdD[kC][LB], sbR[kC][LQ];  // Dout transposed: column j of Dout is row j
 };
 
 __device__ __forceinline__ void backward_chain(const CbArgs &A, uint8_t *dyn, int bid) {
@@ -425,22 +427,18 @@ __device__ __forceinline__ void backward_chain(const CbArgs &A, uint8_t *dyn, in
         cp_wait<kCS - 1>();
         const ChainStage &st = stg[j % kCS];
         __syncthreads();                               // chunk c's tiles are in
-        const float eg = expf(st.glr[r]);
-        float dX[8];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            dX[u] = eg * Dout[u];
-            sdXT[c0 + u][r] = dX[u];
-        }
+        for (int u = 0; u < 8; ++u) sdXT[c0 + u][r] = Dout[u];
         {
-            float *dxg = A.dX + item * kD * kD + (size_t)r * kD + cb + c0;
+            float *dng = A.Dn + item * kD * kD + (size_t)r * kD + cb + c0;
 #pragma unroll
-            for (int u = 0; u < 8; u += 4) *reinterpret_cast<float4 *>(dxg + u) = make_float4(dX[u], dX[u + 1], dX[u + 2], dX[u + 3]);
+            for (int u = 0; u < 8; u += 4)
+                *reinterpret_cast<float4 *>(dng + u) = make_float4(Dout[u], Dout[u + 1], Dout[u + 2], Dout[u + 3]);
         }
         __syncthreads();
-        // dDelta = Kh dX + Aqk^T dOs
+        // dDelta = Kd Dout + Aqk^T dOs
         {
-            const float *kh = st.Kh[di], *xt = sdXT[dj];
+            const float *kh = st.Kd[di], *xt = sdXT[dj];   // row di of Kd, column dj of Dout
             float acc = 0.f;
 #pragma unroll 4
             for (int rr = 0; rr < kD; rr += 4) {
@@ -461,13 +459,14 @@ __device__ __forceinline__ void backward_chain(const CbArgs &A, uint8_t *dyn, in
             sbR[di][dj] = st.beta[di] * acc;
         }
         __syncthreads();
-        // Din = e^{r} (dX + Qt^T dOs - Kt^T diag(beta) dR)
+        // Din = e^{Gamma_L} Dout + Q0^T dOs - K0^T diag(beta) dR
+        const float eg = expf(st.gl[r]);
         float acc[8];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) acc[u] = dX[u];
+        for (int u = 0; u < 8; ++u) acc[u] = eg * Dout[u];
 #pragma unroll
         for (int i = 0; i < kC; ++i) {
-            const float qv = scale * st.Qt[i][r], kv = -st.Kt[i][r];
+            const float qv = scale * st.Q0[i][r], kv = -st.K0[i][r];
 #pragma unroll
             for (int u = 0; u < 8; u += 4) {
                 const float4 o4 = *reinterpret_cast<const float4 *>(&st.dO[i][c0 + u]);
@@ -478,9 +477,8 @@ __device__ __forceinline__ void backward_chain(const CbArgs &A, uint8_t *dyn, in
                 acc[u + 3] = fmaf(qv, o4.w, fmaf(kv, b4.w, acc[u + 3]));
             }
         }
-        const float er = expf(st.rr[r]);
 #pragma unroll
-        for (int u = 0; u < 8; ++u) Dout[u] = er * acc[u];
+        for (int u = 0; u < 8; ++u) Dout[u] = acc[u];
         __syncthreads();                               // buffer j % kCS is refilled for chunk c - kCS
     }
     float *d0 = A.dS0 + ((size_t)nh * kD + r) * kD + cb + c0;
@@ -499,8 +497,8 @@ __global__ void __launch_bounds__(kThreads) cb_chains_kernel(const __grid_consta
 }
 
 // ---- 4. grads: two CTAs per (chunk, head), one per half of the dk columns --------------------------
-// Every product below that runs over dk (dQt, dKt, dKh and so dq, dk, dg) needs, for output
-// column c, only row c of S and of dX, so a CTA holds half of each and two CTAs share an SM.
+// Every product below that runs over dk (dq, dkt, dkh and so dk, dg) needs, for output column c,
+// only row c of S and of Dout, so a CTA holds half of each and two CTAs share an SM.
 // dbeta sums over dk: each half adds its share into the zeroed output.
 
 constexpr int kHC = kD / 2;        // dk columns of one grads CTA
@@ -508,11 +506,11 @@ constexpr int L4 = kD + 4;         // 16-byte aligned padded rows for float4 rea
 constexpr int LH = kHC + 4;
 
 struct GradSmem {
-    float S[kHC][L4], dX[kHC][L4];                 // rows c of this half
+    float S[kHC][L4], Dn[kHC][L4];                 // rows c of this half: the chunk-start state and Dout
     float Dl[kC][L4], dR[kC][L4], dO[kC][L4];
-    float Qt[kC][LH], Kt[kC][LH], Kh[kC][LH];      // this half's columns
+    float q[kC][LH], k[kC][LH], Gm[kC][LH];        // this half's columns
     float dA[kC][LC], dAq[kC][LC], Bm[kC][kC];
-    float beta[kC], er[kHC];
+    float beta[kC], gl[kHC];
 };
 constexpr size_t kGradSmem = sizeof(GradSmem);
 
@@ -554,15 +552,12 @@ __global__ void __launch_bounds__(kThreads, 2) cb_grad_kernel(const __grid_const
     const int n = A.ck_seq[qc];
     const size_t tile = (size_t)item * kC * kD, small = (size_t)item * kC * kC;
     const float *St = A.St + ((size_t)(qc + n) * H + h) * kD * kD + (size_t)cbase * kD;
-    const float *dXg = A.dX + (size_t)item * kD * kD + (size_t)cbase * kD;
+    const float *Dng = A.Dn + (size_t)item * kD * kD + (size_t)cbase * kD;
     stage_tile(&s.Dl[0][0], L4, A.Dl + tile);
     stage_tile(&s.dR[0][0], L4, A.dR + tile);
     for (int e = tid; e < kC * (kHC / 4); e += kThreads) {
         const int i = e / (kHC / 4), p = e % (kHC / 4);
-        const size_t o = tile + (size_t)i * kD + cbase + p * 4;
-        cp16(&s.Qt[i][p * 4], A.Qt + o);
-        cp16(&s.Kt[i][p * 4], A.Kt + o);
-        cp16(&s.Kh[i][p * 4], A.Kh + o);
+        cp16(&s.Gm[i][p * 4], A.Gm + tile + (size_t)i * kD + cbase + p * 4);
     }
     for (int e = tid; e < kC * (kD / 4); e += kThreads) {
         const int i = e / (kD / 4), p = e % (kD / 4);
@@ -570,12 +565,13 @@ __global__ void __launch_bounds__(kThreads, 2) cb_grad_kernel(const __grid_const
         cp16z(&s.dO[i][p * 4], A.dO + ((size_t)ti * H + h) * kD + p * 4, i < L ? 16 : 0);
     }
     stage_vec(&s.Bm[0][0], A.Bm + small, kC * kC);
+    stage_vec(s.gl, A.gl + (size_t)item * kD + cbase, kHC);
     cp_commit();
-    // the half's rows of S and dX in a second group, landing while dA and dAqk are formed
+    // the half's rows of S and Dout in a second group, landing while dA and dAqk are formed
     for (int e = tid; e < kHC * (kD / 4); e += kThreads) {
         const int a = e / (kD / 4), p = e % (kD / 4);
         cp16(&s.S[a][p * 4], St + (size_t)a * kD + p * 4);
-        cp16(&s.dX[a][p * 4], dXg + (size_t)a * kD + p * 4);
+        cp16(&s.Dn[a][p * 4], Dng + (size_t)a * kD + p * 4);
     }
     cp_commit();
     {
@@ -584,8 +580,14 @@ __global__ void __launch_bounds__(kThreads, 2) cb_grad_kernel(const __grid_const
         for (int e = tid; e < kHC * kD / 32; e += kThreads)
             asm volatile("prefetch.global.L2 [%0];" ::"l"(sn + (size_t)e * 32));
     }
+    // this half's columns of q and k, as given (bf16 or fp32)
+    for (int e = tid; e < kC * kHC; e += kThreads) {
+        const int i = e / kHC, c = e % kHC;
+        const size_t src = ((size_t)(t0 + i) * H + h) * kD + cbase + c;
+        s.q[i][c] = i < L ? ld_x(A.q, src, A.bf16) : 0.f;
+        s.k[i][c] = i < L ? ld_x(A.k, src, A.bf16) : 0.f;
+    }
     if (tid < kC) s.beta[tid] = tid < L ? A.beta[(size_t)(t0 + tid) * H + h] : 0.f;
-    if (tid < kHC) s.er[tid] = expf(A.rr[(size_t)item * kD + cbase + tid]);
     cp_wait<1>();
     __syncthreads();
     const float scale = A.scale;
@@ -608,50 +610,53 @@ __global__ void __launch_bounds__(kThreads, 2) cb_grad_kernel(const __grid_const
     __syncthreads();
     const int i = tid / 16, tn = tid % 16;            // row i, local columns tn + 16 x (x < 4)
     const float bi = s.beta[i];
-    float y[4], dqt[4], dkt[4], dkh[4];
+    float y[4], dos[4], dd[4];
 #pragma unroll
-    for (int x = 0; x < 4; ++x) y[x] = dqt[x] = dkt[x] = dkh[x] = 0.f;
-    // Y = dR S'^T and dO S'^T (S' = e^{r} S: the column factor is applied after the sums)
-    dot4x2(y, dqt, s.dR[i], s.dO[i], s.S, tn);
-    // dKh = Delta dX^T + ...
-    dot4(dkh, s.Dl[i], s.dX, tn);
+    for (int x = 0; x < 4; ++x) y[x] = dos[x] = dd[x] = 0.f;
+    // Y = dR S^T, dO S^T and Delta Dout^T over dv (rows c of S and Dout)
+    dot4x2(y, dos, s.dR[i], s.dO[i], s.S, tn);
+    dot4(dd, s.Dl[i], s.Dn, tn);
+    // the pairwise decayed sums P1 .. P4 (K = kC): for m <= i the factor is e^{Gamma_i - Gamma_m},
+    // for m >= i it is e^{Gamma_m - Gamma_i}; both are e^{-|Gamma_i - Gamma_m|}
+    float gi[4], p1[4], p2[4], p34[4];
 #pragma unroll
     for (int x = 0; x < 4; ++x) {
-        const float f = s.er[tn + 16 * x];
-        y[x] *= f;
-        dqt[x] *= scale * f;
+        gi[x] = s.Gm[i][tn + 16 * x];
+        p1[x] = p2[x] = p34[x] = 0.f;
     }
-    // + dAqk Kh, dA Kh, dAqk^T Qt, dA^T diag(beta) Kt  (K = kC)
-#pragma unroll
+#pragma unroll 4
     for (int m = 0; m < kC; ++m) {
         const float aq = s.dAq[i][m], ad = s.dA[i][m], aqt = s.dAq[m][i], adt = s.dA[m][i] * s.beta[m];
 #pragma unroll
         for (int x = 0; x < 4; ++x) {
             const int c = tn + 16 * x;
-            const float kh = s.Kh[m][c];
-            dqt[x] = fmaf(aq, kh, dqt[x]);
-            dkt[x] = fmaf(ad, kh, dkt[x]);
-            dkh[x] = fmaf(aqt, s.Qt[m][c], fmaf(adt, s.Kt[m][c], dkh[x]));
+            const float e = expf(-fabsf(gi[x] - s.Gm[m][c]));
+            const float km = s.k[m][c] * e;
+            p1[x] = fmaf(aq, km, p1[x]);
+            p2[x] = fmaf(ad, km, p2[x]);
+            p34[x] = fmaf(aqt, s.q[m][c] * e, fmaf(adt, km, p34[x]));
         }
     }
-    // dbeta share: rowsum(v o dR) - rowsum(Kt o Y) over this half (+ rowsum(dA o B) once); dv = beta dR
+    // dbeta share: rowsum(v o dR) - rowsum(K0 o Y) over this half (+ rowsum(dA o B) once); dv = beta dR
     float pb = 0.f;
     const size_t row = ((size_t)(t0 + i) * H + h) * kD;
     float dgm[4];
 #pragma unroll
     for (int x = 0; x < 4; ++x) {
         const int c = tn + 16 * x, cg = cbase + c;
-        const float dr = s.dR[i][cg], kt = s.Kt[i][c];
+        const float ea = expf(gi[x]), ed = expf(s.gl[c] - gi[x]);
+        const float dr = s.dR[i][cg], kv = s.k[i][c], qv = s.q[i][c];
         const float vv = i < L ? ld_x(A.v, row + cg, A.bf16) : 0.f;
-        pb += vv * dr - kt * y[x];
-        dkt[x] = bi * (dkt[x] - y[x]);
-        const float ex = A.E[tile + (size_t)i * kD + cg];
+        pb += vv * dr - kv * ea * y[x];
+        const float dq = fmaf(scale * dos[x], ea, p1[x]);
+        const float dkt = bi * (p2[x] - y[x] * ea);
+        const float dkh = fmaf(dd[x], ed, p34[x]);
         if (i < L) {
             A.dv[row + cg] = bi * dr;
-            A.dq[row + cg] = dqt[x] * ex;
-            A.dk[row + cg] = dkt[x] * ex + dkh[x] / ex;
+            A.dq[row + cg] = dq;
+            A.dk[row + cg] = dkt + dkh;
         }
-        dgm[x] = dqt[x] * s.Qt[i][c] + dkt[x] * kt - dkh[x] * s.Kh[i][c];
+        dgm[x] = qv * dq + kv * (dkt - dkh);
     }
     // sum pb over the row's 16 threads (consecutive lanes of one half-warp)
 #pragma unroll
@@ -668,18 +673,17 @@ __global__ void __launch_bounds__(kThreads, 2) cb_grad_kernel(const __grid_const
     }
     __syncthreads();
     if (tid < kHC) {
-        // the chunk's last row also moves the state it hands on: rowsum(S_next o Dout), with
-        // Dout = e^{-(Gamma_L - r)} dX
+        // the chunk's last row also moves the state it hands on: rowsum(S_next o Dout)
         const int cg = cbase + tid;
         const float *sn = A.St + ((size_t)(qc + 1 + n) * H + h) * kD * kD + (size_t)cg * kD;
         float gl = 0.f;
 #pragma unroll 4
         for (int j = 0; j < kD; j += 4) {
             const float4 a4 = *reinterpret_cast<const float4 *>(sn + j);
-            const float4 x4 = *reinterpret_cast<const float4 *>(&s.dX[tid][j]);
+            const float4 x4 = *reinterpret_cast<const float4 *>(&s.Dn[tid][j]);
             gl = fmaf(a4.x, x4.x, fmaf(a4.y, x4.y, fmaf(a4.z, x4.z, fmaf(a4.w, x4.w, gl))));
         }
-        dG[L - 1][tid] += gl * expf(-A.glr[(size_t)item * kD + cg]);
+        dG[L - 1][tid] += gl;
         float run = 0.f;
         for (int ii = L - 1; ii >= 0; --ii) {
             run += dG[ii][tid];
@@ -691,7 +695,7 @@ __global__ void __launch_bounds__(kThreads, 2) cb_grad_kernel(const __grid_const
 size_t r256(size_t b) { return (b + 255) & ~size_t(255); }
 
 struct Layout {
-    size_t off_chunk, ck_t0, ck_len, ck_seq, Qt, Kt, Kh, E, W, U, Tm, Aqk, Bm, rr, glr, Dl, dR, dX, St, total;
+    size_t off_chunk, ck_t0, ck_len, ck_seq, Q0, K0, Kd, Gm, W, U, Tm, Aqk, Bm, gl, Dl, dR, Dn, St, total;
 };
 
 Layout layout(int N, int T, int H) {
@@ -705,11 +709,11 @@ Layout layout(int N, int T, int H) {
     l.ck_len = take(Q * 4);
     l.ck_seq = take(Q * 4);
     const size_t tb = NI * kC * kD * 4, sb = NI * kC * kC * 4, vb = NI * kD * 4;
-    l.Qt = take(tb); l.Kt = take(tb); l.Kh = take(tb); l.E = take(tb); l.W = take(tb); l.U = take(tb);
+    l.Q0 = take(tb); l.K0 = take(tb); l.Kd = take(tb); l.Gm = take(tb); l.W = take(tb); l.U = take(tb);
     l.Tm = take(sb); l.Aqk = take(sb); l.Bm = take(sb);
-    l.rr = take(vb); l.glr = take(vb);
+    l.gl = take(vb);
     l.Dl = take(tb); l.dR = take(tb);
-    l.dX = take(NI * kD * kD * 4);
+    l.Dn = take(NI * kD * kD * 4);
     l.St = take((Q + N) * (size_t)H * kD * kD * 4);
     l.total = o;
     return l;
@@ -743,9 +747,9 @@ cudaError_t launch_backward_chunked(const void *q, const void *k, const void *v,
     A.ck_len = reinterpret_cast<int32_t *>(w + l.ck_len);
     A.ck_seq = reinterpret_cast<int32_t *>(w + l.ck_seq);
     auto f = [&](size_t off) { return reinterpret_cast<float *>(w + off); };
-    A.Qt = f(l.Qt); A.Kt = f(l.Kt); A.Kh = f(l.Kh); A.E = f(l.E); A.W = f(l.W); A.U = f(l.U);
-    A.Tm = f(l.Tm); A.Aqk = f(l.Aqk); A.Bm = f(l.Bm); A.rr = f(l.rr); A.glr = f(l.glr);
-    A.Dl = f(l.Dl); A.dR = f(l.dR); A.dX = f(l.dX); A.St = f(l.St);
+    A.Q0 = f(l.Q0); A.K0 = f(l.K0); A.Kd = f(l.Kd); A.Gm = f(l.Gm); A.W = f(l.W); A.U = f(l.U);
+    A.Tm = f(l.Tm); A.Aqk = f(l.Aqk); A.Bm = f(l.Bm); A.gl = f(l.gl);
+    A.Dl = f(l.Dl); A.dR = f(l.dR); A.Dn = f(l.Dn); A.St = f(l.St);
     A.dq = dq; A.dk = dk; A.dv = dv; A.dg = dg; A.dbeta = dbeta; A.dS0 = dS0;
     // chunk enumeration from the device cu_seqlens; the item grids cover the upper bound A.Q of
     // the chunk count and CTAs past the real chunks return at once

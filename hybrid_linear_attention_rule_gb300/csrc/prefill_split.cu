@@ -9,20 +9,24 @@
 // carried in from the previous chunk:
 //
 //   pass 1, chunk prep (one work item per (chunk, head), all SMs, persistent):
-//       conv, norm, decay -> Kh, Qh, Kb, v;  Akk, Aqk;  Tb = (I + Akk)^-1 diag(beta)
+//       conv, norm, decay -> Kh, Qh, Kb, Kd, v;  Akk, Aqk;  Tb = (I + Akk)^-1 diag(beta)
 //       W = Tb Kh,  U = Tb v                                   -> one record per item
 //   pass 2, chunk scan (one CTA per (sequence, head), chunks in order):
-//       S' = diag(exp(r)) S;  V' = U - W S';  O = scale (Qh S' + Aqk V') [* sigmoid(gate)]
-//       S_next = diag(exp(G_last - r)) (S' + Kb^T V')
+//       S' = diag(exp(rho)) S;  V' = U - W S';  O = scale (Qh S' + Aqk V') [* sigmoid(gate)]
+//       S_next = diag(exp(G_last)) S + Kd^T V'
+// (Kh = k exp(G - rho), Qh = q exp(G - rho) with rho a per-channel reference,
+// Kd = k exp(G_last - G): W S' and Qh S' carry exp(G) from the chunk start to
+// each token, Kd the decay from each token to the chunk end; every factor the
+// scan applies is <= 1, so the state needs no rescaling whatever the decay.)
 //
 // The record of an item (148,480 bytes, in the caller's workspace) holds the
-// split-bf16 tiles [W; Qh], Kb and Aqk^T in the exact 128B-swizzled shared-memory
+// split-bf16 tiles [W; Qh], Kd and Aqk^T in the exact 128B-swizzled shared-memory
 // layout in which the scan kernel's MMAs read them, U^T in fp32 and the
-// per-channel r and G_last; the scan kernel fetches the tiles with bulk copies
+// per-channel rho and G_last; the scan kernel fetches the tiles with bulk copies
 // that overlap its own MMAs.  It keeps the fp32 state in TMEM for the whole
 // sequence, like the single-pass kernel; per chunk it runs two MMA chains, both
 // with the A operand in TMEM: N = 128 against [W; Qh], then N = 192 against
-// [Aqk^T | Kb] (O += V'^T Aqk^T beside S += V'^T Kb in adjacent TMEM columns).
+// [Aqk^T | Kd] (O += V'^T Aqk^T beside S += V'^T Kd in adjacent TMEM columns).
 // The time of a tcgen05 MMA here is set by the instruction count far more than
 // by N, hence the wide chains.
 #include <cuda.h>
@@ -41,13 +45,13 @@ using namespace tcc;
 
 // ---- one chunk record (byte offsets; identical to the scan kernel's smem layout) ----
 constexpr uint32_t REC_X = 0;            // [W rows 0-63; Qh rows 64-127] x 128 K, per 64-wide K atom hi then lo (16 KB each)
-constexpr uint32_t REC_B = 65536;        // MN-major B of MMA O/S: 8 KB N-blocks Aqk^T hi, lo, then Kb hi, lo per K atom
+constexpr uint32_t REC_B = 65536;        // MN-major B of MMA O/S: 8 KB N-blocks Aqk^T hi, lo, then Kd hi, lo per K atom
 constexpr uint32_t REC_U = 114688;       // U^T fp32 as 16 blocks of 4 tokens: [tok / 4][128 dv][4 tok]
-constexpr uint32_t REC_VEC = 147456;     // r[128], G_last[128] fp32
+constexpr uint32_t REC_VEC = 147456;     // rho[128], G_last[128] fp32
 constexpr uint32_t REC_BYTES = 148480;
 static_assert(PlanPrep::X_LO == PlanPrep::X_HI + 16384 && PlanPrep::X_ATOM == 32768,
               "the record's [W; Qh] part is the prep plan's X tile: [hi 0 | lo 0 | hi 1 | lo 1]");
-static_assert(OFF_GL == OFF_REF + 512, "r and G_last must be adjacent (one bulk store)");
+static_assert(OFF_GL == OFF_REF + 512, "rho and G_last are adjacent");
 
 // byte offset of U^T element (dv j, token i) inside the U block: a warp's 32 consecutive dv
 // channels with the same 4 tokens fill 512 contiguous bytes (coalesced stores, conflict-free loads)
@@ -281,20 +285,20 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_prep_kernel(const __gri
         if (*sflag) break;
         clk.tick(0);
 
-        prep_qk<PlanPrep>(sm, a, x.cs, Lc, x.h, W, nullptr, nullptr);
+        float kd[kTok][4];
+        const bool strong = prep_qk<PlanPrep>(sm, a, x.cs, Lc, x.h, W, tl, kColA, kd);
         clk.tick(1);
         if (tid == 0) {
-            issue_mma_a<PlanPrep>(sbase, tbase + kColA, mbar_a);
+            issue_mma_a<PlanPrep>(sbase, tbase + kColA, mbar_a, strong);
             pend_a = true;
-            // Qh (rows 64..127 of each K atom, hi and lo) and Kb are final: out now.  The stacked Kb
-            // tile (per K atom the hi rows, then the lo rows) is the record's layout as it stands
+            // Qh (rows 64..127 of each K atom, hi and lo) is final: out now
 #pragma unroll
             for (int p = 0; p < 4; ++p)
                 bulk_s2g(rec + REC_X + p * 16384 + 8192, sbase + PlanPrep::X_HI + p * 16384 + 8192, 8192);
-            bulk_s2g(rec + REC_B + 16384, sbase + PlanPrep::KB_HI, 32768);
             bulk_commit();
         }
-        if (tid < kD) {                                  // r, G_last
+        put_kd(rec + REC_B + 16384, kd);                 // Kd straight from registers, in the record's layout
+        if (tid < kD) {                                  // rho, G_last
             reinterpret_cast<float *>(rec + REC_VEC)[tid] = reinterpret_cast<const float *>(sm + OFF_REF)[tid];
             reinterpret_cast<float *>(rec + REC_VEC)[kD + tid] = reinterpret_cast<const float *>(sm + OFF_GL)[tid];
         }
@@ -306,7 +310,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_prep_kernel(const __gri
         __syncthreads();                                 // this item's staged rows are consumed
         if (tid == 0) {
             if (has_next) stage_qkv(y);
-            bulk_wait_read_all();                        // Kb has left region R, which the extract reuses
+            bulk_wait_read_all();                        // the Qh rows have left (X is rewritten by the next prep)
         }
         if (!mma_wait()) break;
         clk.tick(3);
@@ -419,8 +423,7 @@ struct ScanArgs {
     const int32_t *chunk_off;
     const uint8_t *rec;       // records of this launch's chunks: [(q - q_lo) * H + h]
     int q_lo, q_hi;           // global chunk range of this launch
-    float *carry_S;           // [N*H][128 dv][128 dk] state in the last chunk's basis between launches
-    float *carry_logf;        // [N*H][128] log of that basis factor
+    float *carry_S;           // [N*H][128 dv][128 dk] state handed between launches
 };
 
 // scan kernel shared memory: [W; Qh] of even chunks and [Aqk^T | Kb] at their record offsets, then
@@ -429,9 +432,9 @@ constexpr uint32_t Q_X1 = REC_U;                    // [W; Qh] tile of odd chunk
 constexpr uint32_t Q_G0 = Q_X1 + 65536;             // gate logits bf16 [64 tok][128] of even / odd chunks
 constexpr uint32_t Q_G1 = Q_G0 + 16384;
 constexpr uint32_t Q_OST = Q_G1 + 16384;            // bf16 outputs [64 tok][128] of one chunk, stored by TMA
-constexpr uint32_t Q_LOGF = Q_OST + 16384;          // log of the basis factor carried in TMEM
-constexpr uint32_t Q_FCOL = Q_LOGF + 512;           // state column factors, two chunks (double buffer)
-constexpr uint32_t Q_MISC = Q_FCOL + 1024;          // 6 mbarriers, tmem slot, flag
+constexpr uint32_t Q_FA = Q_OST + 16384;            // exp(rho) per channel of the chunk whose state pass is next
+constexpr uint32_t Q_FS = Q_FA + 512;               // exp(G_last) per channel, same chunk
+constexpr uint32_t Q_MISC = Q_FS + 512;             // 6 mbarriers, tmem slot, flag
 constexpr uint32_t kScanSmemBytes = Q_MISC + 64 + 1024;
 static_assert(Q_X1 % 1024 == 0, "tile alignment");
 static_assert(kScanSmemBytes <= 232448, "scan kernel shared memory exceeds the per-CTA limit");
@@ -445,8 +448,8 @@ static_assert(kScanSmemBytes <= 232448, "scan kernel shared memory exceeds the p
 constexpr uint32_t kScanTmemCols = 512;
 constexpr uint32_t kColD = 0;       // D, 256 columns; V'^T split in [0, 64)
 constexpr uint32_t kColO = 192;     // O^T (fp32)
-constexpr uint32_t kColSs = 256;    // S'^T fp32, 128 columns
-static_assert(kColO + 64 == kColSs, "O^T and S'^T must be adjacent: one N = 192 chain accumulates into both");
+constexpr uint32_t kColSs = 256;    // S^T fp32 (the state), 128 columns
+static_assert(kColO + 64 == kColSs, "O^T and S^T must be adjacent: one N = 192 chain accumulates into both");
 constexpr uint32_t kColSh = 384;    // S'^T hi / lo, bf16 pairs: 64 columns each
 constexpr uint32_t kColSl = 448;
 
@@ -465,11 +468,11 @@ __device__ __forceinline__ void tmem_put_split16(uint32_t col_hi, uint32_t col_l
     tmem_st8(col_lo, lw);
 }
 
-// Per chunk: MMA [(W S')^T | (Qh S')^T]; V'^T = U^T - (W S')^T; MMA [O^T | S'^T] += V'^T [Aqk^T | Kb]
-// while the gate's sigmoid is taken; then one phase writes this chunk's outputs and moves the
-// state into the next chunk's basis.  [W; Qh] and the gate rows (both double-buffered, two chunks
-// ahead) and [Aqk^T | Kb] arrive by bulk copies issued as soon as their buffers are free; U^T, r
-// and G_last are read by the threads that use them, one chunk ahead, into registers.
+// Per chunk: MMA [(W S')^T | (Qh S')^T]; V'^T = U^T - (W S')^T; MMA [O^T | S^T] += V'^T [Aqk^T | Kd]
+// while the gate's sigmoid is taken; then one phase writes this chunk's outputs and runs the next
+// chunk's state pass.  [W; Qh] and the gate rows (both double-buffered, two chunks ahead) and
+// [Aqk^T | Kd] arrive by bulk copies issued as soon as their buffers are free; U^T, rho and
+// G_last are read by the threads that use them, one chunk ahead, into registers.
 __global__ void __launch_bounds__(kThreads, 1) kda_chunk_scan_kernel(const __grid_constant__ ScanArgs A) {
     extern __shared__ uint8_t smraw[];
     uint8_t *sm = smem_align1024(smraw);
@@ -478,8 +481,8 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_scan_kernel(const __gri
     const int nh = blockIdx.x, n = nh / a.H, h = nh % a.H;
     const int H = a.H;
     const uint32_t sbase = smem_u32(sm);
-    float *sLogf = reinterpret_cast<float *>(sm + Q_LOGF);
-    float *sFcol = reinterpret_cast<float *>(sm + Q_FCOL);
+    float *sFA = reinterpret_cast<float *>(sm + Q_FA);
+    float *sFS = reinterpret_cast<float *>(sm + Q_FS);
     uint64_t *mbar = reinterpret_cast<uint64_t *>(sm + Q_MISC);
     uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + Q_MISC + 48);
     volatile uint32_t *sflag = reinterpret_cast<volatile uint32_t *>(sm + Q_MISC + 52);
@@ -507,7 +510,6 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_scan_kernel(const __gri
         fence_mbar_init();
         *sflag = 0;
     }
-    if (tid < kD) sLogf[tid] = 0.f;
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -516,11 +518,10 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_scan_kernel(const __gri
     const uint32_t tl = tbase + (lrow << 16);
     const int quarter = warp >> 2;
     const int j = lrow + lane;                          // this thread's TMEM lane: dv channel
-    // S'^T <- S0^T (true state, basis factor 1) at the sequence start, else the carried state
-    // the per-channel basis factors are kept by the last four warps (vt >= 0), which have no
-    // copies or MMAs to issue, so that the issuing warp does not trail the others
+    // S^T <- S0^T at the sequence start, else the carried state.  The per-channel factors of the
+    // next state pass are formed by the last four warps (vt >= 0), which have no copies or MMAs to
+    // issue, so that the issuing warp does not trail the others
     const int vt = tid - (kThreads - kD);
-    float logf_cur = 0.f;         // vt >= 0: log of the basis factor of the current chunk
     {
         for (int cb = 0; cb < 32; cb += 16) {
             uint32_t r[16];
@@ -541,10 +542,6 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_scan_kernel(const __gri
             tmem_st16(tl + kColSs + quarter * 32 + cb, r);
         }
         tmem_wait_st();
-        if (!first && vt >= 0) {
-            logf_cur = A.carry_logf[(size_t)nh * kD + vt];
-            sLogf[vt] = logf_cur;
-        }
     }
 
     auto rec_of = [&](int c) { return A.rec + ((size_t)(q0 + c - A.q_lo) * H + h) * REC_BYTES; };
@@ -596,7 +593,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_scan_kernel(const __gri
 
     // register-resident operands, one chunk ahead
     float uR[16];                 // U^T row j, tokens 16*quarter .. +15
-    float rN = 0.f, glN = 0.f;    // vt >= 0: r and G_last of the chunk after the current one
+    float rN = 0.f, glN = 0.f;    // vt >= 0: rho and G_last of the chunk after the current one
     auto load_u = [&](int c) {
         const uint8_t *p = rec_of(c) + REC_U;
 #pragma unroll
@@ -610,8 +607,9 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_scan_kernel(const __gri
         rN = __ldg(p + vt);
         glN = __ldg(p + kD + vt);
     };
-    // S'^T = S^T diag(fcol) -> TMEM, fp32 and split bf16 (the A operand of MMA W/Qh)
-    auto to_basis = [&](const float *fcol) {
+    // the state pass of a chunk: S'^T = S^T diag(exp(rho)) as split bf16 (the A operand of MMA W/Qh),
+    // and the fp32 accumulator S^T <- S^T diag(exp(G_last)), onto which MMA O/S adds V'^T Kd
+    auto state_pass = [&]() {
         uint32_t r[2][16];
         tmem_ld16(tl + kColSs + quarter * 32, r[0]);
         tmem_ld16(tl + kColSs + quarter * 32 + 16, r[1]);
@@ -622,8 +620,9 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_scan_kernel(const __gri
             float v[16];
 #pragma unroll
             for (int u = 0; u < 16; ++u) {
-                v[u] = __uint_as_float(r[b][u]) * fcol[col + u];
-                r[b][u] = __float_as_uint(v[u]);
+                const float x = __uint_as_float(r[b][u]);
+                v[u] = x * sFA[col + u];
+                r[b][u] = __float_as_uint(x * sFS[col + u]);
             }
             tmem_st16(tl + kColSs + col, r[b]);
             tmem_put_split16(tl + kColSh + col / 2, tl + kColSl + col / 2, v);
@@ -638,7 +637,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_scan_kernel(const __gri
     };
 
     bool failed = false;
-    PhaseClock clk;   // phases: 0 MMA W, 1 V' tile, 2 MMA O/S, 3 epilogue + next basis
+    PhaseClock clk;   // phases: 0 MMA W, 1 V' tile, 2 MMA O/S, 3 epilogue + next state pass
     if (c_begin < c_end) {
         const int c = c_begin;
         if (tid == 0) {
@@ -654,13 +653,12 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_scan_kernel(const __gri
         load_u(c);
         if (vt >= 0) {
             load_vec(c);
-            sFcol[(c & 1) * kD + vt] = expf(logf_cur + rN);
-            logf_cur = glN - rN;
-            sLogf[vt] = logf_cur;
+            sFA[vt] = expf(rN);
+            sFS[vt] = expf(glN);
             if (c + 1 < c_end) load_vec(c + 1);
         }
         __syncthreads();
-        to_basis(sFcol + (c & 1) * kD);
+        state_pass();
         tc_fence_before();
         __syncthreads();
     }
@@ -668,7 +666,6 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_scan_kernel(const __gri
         const int cs = tb + c * kC;
         const int Lc = min(kC, te - cs);
         const bool more = c + 1 < c_end;
-        float *fnext = sFcol + ((c + 1) & 1) * kD;
         // ---- MMA: D = S'^T [W; Qh]^T, hi and lo parts in separate columns ----
         if (tid == 0 && wait_x(c)) {
             tc_fence_after();
@@ -687,11 +684,10 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_scan_kernel(const __gri
             mma_commit(mb_a);
             pend_a = true;
         }
-        // the next chunk's basis factor, while the MMAs run
+        // the next chunk's state-pass factors, while the MMAs run (this chunk's pass has read them)
         if (vt >= 0 && more) {
-            fnext[vt] = expf(logf_cur + rN);
-            logf_cur = glN - rN;
-            sLogf[vt] = logf_cur;
+            sFA[vt] = expf(rN);
+            sFS[vt] = expf(glN);
             if (c + 2 < c_end) load_vec(c + 2);
         }
         if (!mma_wait()) { failed = true; break; }
@@ -719,7 +715,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_scan_kernel(const __gri
         tc_fence_before();
         __syncthreads();
         clk.tick(1);
-        // ---- MMA: [O^T | S'^T] += V'^T [Aqk^T | Kb]  (N = 192: columns kColO .. kColSs + 127) ----
+        // ---- MMA: [O^T | S^T] += V'^T [Aqk^T | Kd]  (N = 192: columns kColO .. kColSs + 127) ----
         if (tid == 0 && wait_on(mb_k, kph, pend_k)) {
             tc_fence_after();
             const uint32_t id = idesc_bf16_f32(128, 192, false, false, /*b_mn=*/true);
@@ -760,7 +756,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_scan_kernel(const __gri
         // the record three chunks ahead into L2, queued behind the copies above
         if (tid == 0 && c + 3 < c_end) prefetch_chunk(c + 3);
         clk.tick(2);
-        // ---- this chunk's outputs, then the state into the next chunk's basis ----
+        // ---- this chunk's outputs, then the next chunk's state pass ----
         // bf16 outputs go through a shared tile and one TMA store that runs behind the next chunk,
         // unless the chunk is a ragged sequence end inside the tensor (the box would cross into
         // the next sequence's rows; TMA clips only at the tensor's end)
@@ -783,7 +779,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_scan_kernel(const __gri
                 }
             }
         }
-        if (more) to_basis(fnext);
+        if (more) state_pass();
         if (tma_out) fence_async_smem();
         tc_fence_before();
         __syncthreads();
@@ -796,7 +792,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_scan_kernel(const __gri
     clk.flush(reinterpret_cast<unsigned long long *>(a.status) + 8);
     if (!failed && !last) {
         tc_fence_after();
-        // ---- hand the state (and its basis) to the launch that continues the sequence ----
+        // ---- hand the state to the launch that continues the sequence ----
         float *carry = A.carry_S + ((size_t)nh * kD + j) * kD;
         for (int cb = 0; cb < 32; cb += 16) {
             uint32_t r[16];
@@ -806,11 +802,10 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_scan_kernel(const __gri
             for (int u = 0; u < 16; u += 4)
                 *reinterpret_cast<uint4 *>(carry + quarter * 32 + cb + u) = make_uint4(r[u], r[u + 1], r[u + 2], r[u + 3]);
         }
-        if (tid < kD) A.carry_logf[(size_t)nh * kD + tid] = sLogf[tid];
     }
     if (!failed && last) {
         tc_fence_after();
-        // ---- final state: S = S'^T diag(exp(logf)) ----
+        // ---- final state ----
         if (a.Sfin && sn >= 0) {
             for (int cb = 0; cb < 32; cb += 16) {
                 uint32_t r[16];
@@ -819,7 +814,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_scan_kernel(const __gri
 #pragma unroll
                 for (int u = 0; u < 16; ++u) {
                     const int c = quarter * 32 + cb + u;
-                    a.Sfin[(snh * kD + c) * kD + j] = __uint_as_float(r[u]) * expf(sLogf[c]);
+                    a.Sfin[(snh * kD + c) * kD + j] = __uint_as_float(r[u]);
                 }
             }
         }
@@ -877,7 +872,7 @@ constexpr int kMaxSegs = 64;
 constexpr int kRing = 3;
 constexpr int kMaxDevices = 64;
 bool use_segments(int N, int T, int H) { return (long long)N * H <= 64 && max_chunks(N, T) >= 2 * kSegChunks; }
-size_t carry_bytes(int N, int H) { return (size_t)N * H * (kD * kD + kD) * sizeof(float); }
+size_t carry_bytes(int N, int H) { return (size_t)N * H * kD * kD * sizeof(float); }
 // chunks one ring buffer holds: the longest segment the launcher may choose
 int ring_chunks(int N, int T) {
     const int qmax = (int)max_chunks(N, T);
@@ -936,10 +931,9 @@ cudaError_t launch_prefill_tc_split(const PrefillArgs &p, const float *conv_w, f
     int32_t *chunk_off = reinterpret_cast<int32_t *>(w);
     w += round256_((size_t)(p.N + 1) * sizeof(int32_t));
     const bool seg = use_segments(p.N, p.T, p.H);
-    float *carry_S = nullptr, *carry_logf = nullptr;
+    float *carry_S = nullptr;
     if (seg) {
         carry_S = reinterpret_cast<float *>(w);
-        carry_logf = carry_S + (size_t)p.N * p.H * kD * kD;
         w += round256_(carry_bytes(p.N, p.H));
     }
     uint8_t *rec = w;
@@ -988,7 +982,6 @@ cudaError_t launch_prefill_tc_split(const PrefillArgs &p, const float *conv_w, f
     S.chunk_off = chunk_off;
     S.rec = rec;
     S.carry_S = carry_S;
-    S.carry_logf = carry_logf;
     const unsigned scan_grid = (unsigned)(p.N * p.H);
 
     auto prep = [&](int q_lo, int q_hi, int max_ctas, cudaStream_t st) -> cudaError_t {

@@ -5,18 +5,20 @@
 // The recurrence ("recurrent KDA state", HF discussion #187 feature list; FP32
 // KdaState, metrale kimi_k3 docs) in its chunked (WY/UT) form.  For a chunk of
 // 64 tokens with chunk-local cumulative log-decay G (per channel) and a
-// per-channel reference r = (G_first + G_last) / 2:
-//   Kh = k E, Qh = q E, Kb = k / E          with E = exp(G - r)
+// per-channel reference rho (the mid-point of G, or G_first for a channel that
+// decays by more than kStrongDecay nats within the chunk):
+//   Kh = k E, Qh = q E, Kb = k / E, Kd = k exp(G_last - G),   E = exp(G - rho)
 //   Akk = diag(beta) tril(Kh Kb^T, -1),  Aqk = tril(Qh Kb^T)
+//       (a strong channel's share of both is formed exactly in tc_chunk.cuh)
 //   T  = (I + Akk)^-1,  Tb = T diag(beta)
-//   S' = diag(exp(r)) S                        (state in the chunk's basis)
+//   S' = diag(exp(rho)) S
 //   U  = Tb v,  Y = Kh S',  V' = U - Tb Y
 //   O  = scale (Qh S' + Aqk V')  [* sigmoid(gate)]
-//   S_next = diag(exp(G_last - r)) (S' + Kb^T V')
+//   S_next = diag(exp(G_last)) S + Kd^T V'
 // (V' = U - W S with W = Tb Kh written as U - Tb (Kh S') so that no transposed
-// copy of Kh or W is ever materialised.)  All exponents are of |G - r| <= half
-// the chunk's total decay, so nothing overflows for per-chunk decays below
-// ~170 nats per channel.
+// copy of Kh or W is ever materialised.)  Every factor applied to the state is
+// at most 1 and every E, 1/E stays within exp(+-kStrongDecay / 2), so nothing
+// overflows whatever the decay.
 //
 // Precision: every MMA operand that is not exactly bf16 is split into a bf16
 // high part and a bf16 low part (x = hi + lo to ~2^-17 relative) and each
@@ -30,7 +32,7 @@
 // shared-memory tiles and invert the 64x64 unit-triangular matrix in fp32; a
 // single elected thread issues the tcgen05.mma chains; the fp32 state lives in
 // TMEM for the whole sequence.  TMEM columns: [0,64) Akk|Aqk then O^T,
-// [64,128) Y^T, [128,192) U^T then V'^T, [192,320) S'^T.
+// [64,128) Y^T, [128,192) U^T then V'^T, [192,320) S^T (the state).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -66,8 +68,8 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
     const uint32_t sbase = smem_u32(sm);
     float *sRef = reinterpret_cast<float *>(sm + OFF_REF);
     float *sGL = reinterpret_cast<float *>(sm + OFF_GL);
-    float *sFcol = reinterpret_cast<float *>(sm + OFF_FCOL);
-    float *sLogf = reinterpret_cast<float *>(sm + OFF_LOGF);
+    float *sFA = reinterpret_cast<float *>(sm + OFF_FCOL);     // exp(rho) of the current chunk
+    float *sFS = reinterpret_cast<float *>(sm + OFF_LOGF);     // exp(G_last) of the current chunk
     float *sConvW = reinterpret_cast<float *>(sm + OFF_CONVW);
     float *sHist = reinterpret_cast<float *>(sm + OFF_HIST);
     uint64_t *mbar = reinterpret_cast<uint64_t *>(sm + OFF_MISC);
@@ -101,7 +103,6 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
             const int gch = (ch >> 7) * H * kD + h * kD + (ch & 127);
             sConvW[e] = t >= 4 - W ? A.conv_w[(size_t)gch * W + (t - (4 - W))] : 0.f;
         }
-    if (tid < kD) sLogf[tid] = 0.f;
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -109,7 +110,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
     const uint32_t lrow = 32u * (warp & 3);             // first TMEM lane of this warp
     const uint32_t tl = tbase + (lrow << 16);
     const int quarter = warp >> 2;                       // which column quarter this warp handles
-    {   // S'^T <- S0^T (true state; basis factor 1)
+    {   // S^T <- S0^T
         const int j = lrow + lane;
         for (int cb = 0; cb < 32; cb += 16) {
             uint32_t r[16];
@@ -182,7 +183,13 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
         sphase ^= 1u;
         __syncthreads();
         if (*sflag) { failed = true; break; }
-        prep_chunk<PlanFused>(sm, a, cs, Lc, h, W, sLogf, sFcol);
+        float kd[kTok][4];
+        const bool strong = prep_qk<PlanFused>(sm, a, cs, Lc, h, W, tl, kColA, kd);
+        if (tid < kD) {
+            sFA[tid] = expf(sRef[tid]);
+            sFS[tid] = expf(sGL[tid]);
+        }
+        prep_v<PlanFused>(sm, a, Lc, W);
         PHASE(0);
         // pre-conv rows 61..63 of this chunk are the conv history of the next one
         if (W > 0 && cs + kC < te)
@@ -192,8 +199,11 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
                 sHist[e] = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(sm + st + (kC - 3 + r) * (kD * 2) + c * 2));
             }
         // ================= MMA: [Kh; Qh] Kb^T  -> Akk | Aqk =================
-        if (tid == 0) issue_mma_a<PlanFused>(sbase, tbase + kColA, mbar_a);
+        if (tid == 0) issue_mma_a<PlanFused>(sbase, tbase + kColA, mbar_a, strong);
         if (!mma_wait()) { failed = true; break; }
+        // MMA A has read Kb: the Kb region takes Kd (stacked hi / lo tiles), the B operand of MMA S
+        put_kd(sm + OFF_KB_HI, kd);
+        fence_async_smem();
         PHASE(1);
         extract_a<PlanFused>(sm, tl, kColA);
         PHASE(2);
@@ -217,7 +227,8 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
         }
         if (!mma_wait()) { failed = true; break; }
         PHASE(4);
-        // ================= S'^T = S^T diag(fcol) -> TMEM and split A tile =================
+        // ================= state pass: S'^T = S^T diag(exp(rho)) -> split A tile;
+        //                   S^T <- S^T diag(exp(G_last)) in TMEM (MMA S adds V'^T Kd) =================
         {
             const int j = lrow + lane;
             for (int cb = 0; cb < 32; cb += 16) {
@@ -228,8 +239,9 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
                 float v[16];
 #pragma unroll
                 for (int u = 0; u < 16; ++u) {
-                    v[u] = __uint_as_float(r[u]) * sFcol[col + u];
-                    r[u] = __float_as_uint(v[u]);
+                    const float x = __uint_as_float(r[u]);
+                    v[u] = x * sFA[col + u];
+                    r[u] = __float_as_uint(x * sFS[col + u]);
                 }
                 tmem_st16(tl + kColS + col, r);
                 tile64_put16(sm, OFF_ST_HI + (col >> 6) * 16384, OFF_ST_LO + (col >> 6) * 16384, j, col & 63, v);
@@ -296,7 +308,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
             tma_load_3d(sbase + OFF_TB_HI, &A.tm_gate, 0, h, cs, mbar_g);
         }
         PHASE(7);
-        // ================= V'^T -> split tile;  MMA: O^T += V'^T Aqk^T,  S'^T += V'^T Kb =================
+        // ================= V'^T -> split tile;  MMA: O^T += V'^T Aqk^T,  S^T += V'^T Kd =================
         tmem_to_tile64(kColU, OFF_VPT_HI, OFF_VPT_LO);
         fence_async_smem();
         tc_fence_before();
@@ -307,7 +319,9 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
             const uint32_t id128 = idesc_bf16_f32(128, 128, false, false, /*b_mn=*/true);
             const uint64_t dVh = sdesc_kmajor_sw128(sbase + OFF_VPT_HI), dVl = sdesc_kmajor_sw128(sbase + OFF_VPT_LO);
             const uint64_t dAh = sdesc_mnmajor_sw128(sbase + OFF_AQK_HI, 8192), dAl = sdesc_mnmajor_sw128(sbase + OFF_AQK_LO, 8192);
-            const uint64_t dKh = sdesc_mnmajor_sw128(sbase + OFF_KB_HI, 8192), dKl = sdesc_mnmajor_sw128(sbase + OFF_KB_LO, 8192);
+            // Kd: per 64-wide K atom (16 KB apart) the hi tile, then the lo tile 8 KB after it
+            const uint64_t dKh = sdesc_mnmajor_sw128(sbase + OFF_KB_HI, 16384),
+                           dKl = sdesc_mnmajor_sw128(sbase + OFF_KB_HI + 8192, 16384);
 #pragma unroll
             for (int sp = 0; sp < 3; ++sp)
 #pragma unroll
@@ -328,7 +342,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
         if (!mma_wait()) { failed = true; break; }   // its barrier also publishes the gate tile
         if (cs + kC < te) stage_qk(cs + kC);          // V'^T region is free now
         PHASE(8);
-        // ================= epilogue: O^T -> gate -> out; carry the basis factor =================
+        // ================= epilogue: O^T -> gate -> out =================
         {
             const int j = lrow + lane;
             uint32_t r0[16];
@@ -347,7 +361,6 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
             }
         }
         PHASE(9);
-        if (tid < kD) sLogf[tid] = sGL[tid] - sRef[tid];
         tc_fence_before();
         __syncthreads();
         tc_fence_after();
@@ -360,7 +373,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
 #endif
 #undef PHASE
     if (!failed) {
-        // ---- final state: S = S'^T diag(exp(logf)) ----
+        // ---- final state ----
         if (a.Sfin && sn >= 0) {
             const int j = lrow + lane;
             for (int cb = 0; cb < 32; cb += 16) {
@@ -370,7 +383,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
 #pragma unroll
                 for (int u = 0; u < 16; ++u) {
                     const int c = quarter * 32 + cb + u;
-                    a.Sfin[(snh * kD + c) * kD + j] = __uint_as_float(r[u]) * expf(sLogf[c]);
+                    a.Sfin[(snh * kD + c) * kD + j] = __uint_as_float(r[u]);
                 }
             }
         }

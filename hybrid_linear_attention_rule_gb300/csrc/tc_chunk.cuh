@@ -3,15 +3,28 @@
 // prefill kernel and the chunk-prep kernel of the two-pass prefill.
 //
 // From a chunk's staged input rows it builds, in shared memory: the decayed
-// operands Kh = k E, Qh = q E, Kb = k / E (E = exp(G - r), r the per-channel
-// mid-point of the chunk-local cumulative log-decay G) as split-bf16 K-major
+// operands Kh = k E, Qh = q E, Kb = k / E (E = exp(G - rho), G the chunk-local
+// cumulative log-decay and rho a per-channel reference) as split-bf16 K-major
 // tiles, the v rows, Akk = diag(beta) tril(Kh Kb^T, -1) (fp32) and Aqk =
 // tril(Qh Kb^T) (split-bf16) from one tcgen05 MMA chain, and Tb = (I + Akk)^-1
-// diag(beta) (split-bf16) by a block-recursive fp32 triangular inverse.  The
-// WY/UT form of the delta rule this serves is the one of "recurrent KDA
-// state" (HF discussion #187 feature list; KdaState in the metrale kimi_k3
-// docs).  Every function but issue_mma_a is called by all threads of the CTA
-// (16 warps) and ends with a CTA barrier.
+// diag(beta) (split-bf16) by a block-recursive fp32 triangular inverse; and, in
+// registers, Kd = k exp(G_last - G), the operand of the state update.  The
+// WY/UT form of the delta rule this serves is the one of "recurrent KDA state"
+// (HF discussion #187 feature list; KdaState in the metrale kimi_k3 docs).
+//
+// Range.  The recurrence puts no bound on the decay, so no exponent here may
+// exceed the fp32 range whatever g is.  For a channel whose decay across the
+// chunk (G_first - G_last) is at most kStrongDecay nats, rho is the mid-point
+// of G and every factor E, 1/E lies within exp(+-kStrongDecay / 2).  A channel
+// that decays more ("strong") takes rho = G_first, so that E <= 1, and is left
+// out of the factorised product (its Kb column is zero); its share of Akk and
+// Aqk, sum_c x_ic k_jc exp(G_ic - G_jc) over the strong channels c, is formed
+// exactly on the CUDA cores and written into the MMA's TMEM accumulator before
+// the chain runs.  The state side never divides by a decay: the scan uses
+// exp(rho) <= 1, exp(G_last) <= 1 and Kd.
+//
+// Every function but issue_mma_a is called by all threads of the CTA (16 warps)
+// and ends with a CTA barrier.
 #pragma once
 
 #include <cuda.h>
@@ -32,6 +45,10 @@ constexpr int kTok = kC / kWarps;                // tokens per thread in the pre
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColA = 0, kColY = 64, kColU = 128, kColS = 192;
 constexpr uint32_t kWaitLimit = 1u << 26;
+// In-chunk decay (nats, G_first - G_last of one channel) above which a channel's share of Akk and
+// Aqk is computed exactly instead of through E and 1/E: below it every factor stays within
+// exp(+-80), far inside the fp32 range.
+constexpr float kStrongDecay = 160.f;
 
 // shared-memory plan (byte offsets from a 1024-aligned base).  Regions A and B
 // are reused phase by phase within a chunk; the input rows of the next chunk are
@@ -62,12 +79,13 @@ constexpr uint32_t OFF_VST = 196608;             // v rows bf16 [64][128] (stage
 constexpr uint32_t OFF_CONVW = 212992;           // fp32 [4 taps][384 channels]
 constexpr uint32_t OFF_HIST = OFF_CONVW + 384 * 4 * 4;   // fp32 [3 tensors][3 rows][128]: pre-conv rows before the chunk
 constexpr uint32_t OFF_BETA = OFF_HIST + 3 * 3 * 128 * 4;
-constexpr uint32_t OFF_REF = OFF_BETA + 256;          // r per channel
+constexpr uint32_t OFF_REF = OFF_BETA + 256;          // rho per channel
 constexpr uint32_t OFF_GL = OFF_REF + 512;            // G_last per channel
 constexpr uint32_t OFF_G0 = OFF_GL + 512;             // G_first per channel
-constexpr uint32_t OFF_FCOL = OFF_G0 + 512;           // state column factor for this chunk
-constexpr uint32_t OFF_LOGF = OFF_FCOL + 512;         // log of the basis factor carried in TMEM
-constexpr uint32_t OFF_MISC = OFF_LOGF + 512;         // mbarriers (2 x 8 B), tmem slot, flag
+constexpr uint32_t OFF_FCOL = OFF_G0 + 512;           // exp(rho) per channel (single-pass state pass)
+constexpr uint32_t OFF_LOGF = OFF_FCOL + 512;         // exp(G_last) per channel (single-pass state pass)
+constexpr uint32_t OFF_SMASK = 32;                    // (from OFF_MISC) 4 words: strong channels of the chunk
+constexpr uint32_t OFF_MISC = OFF_LOGF + 512;         // mbarriers (3 x 8 B), tmem slot, flag, strong masks
 constexpr uint32_t kSmemUsed = OFF_MISC + 64;
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;     // + alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory plan exceeds the per-CTA limit");
@@ -85,6 +103,9 @@ struct PlanFused {
     static constexpr uint32_t X_HI = OFF_X, X_LO = OFF_XL, X_ATOM = 16384;   // [Kh; Qh]: hi atoms, then lo atoms
     static constexpr bool KB_STACKED = false;    // Kb hi and lo as two 64-row tiles
     static constexpr bool CALLER_STAGES = false; // prep_qk loads beta and owns every tile it writes
+    // strong-channel correction: staged rows (GST/V region, free once G is in registers) and the
+    // fp32 correction (the Aqk and Tb tiles, free until the extract)
+    static constexpr uint32_t STRONG_STAGE = OFF_V_HI, STRONG_ACC = OFF_AQK_HI;
 };
 struct PlanPrep {
     static constexpr uint32_t V_HI = 65536, V_LO = 81920;                  // v rows      (prep_v .. MMA U)
@@ -104,8 +125,15 @@ struct PlanPrep {
     // the caller writes BETA before prep_qk, and the bulk stores still reading X rows 0-63 (issued
     // by thread 0) are waited for inside prep_qk, before those rows are rewritten
     static constexpr bool CALLER_STAGES = true;
+    // strong-channel correction: staged rows (the v tiles, written by prep_v afterwards) and the
+    // fp32 correction (the Aqk and Tb tiles, free until the extract)
+    static constexpr uint32_t STRONG_STAGE = V_HI, STRONG_ACC = AQK_HI;
 };
 static_assert(PlanPrep::TB_LO + 8192 <= OFF_CONVW, "prep plan runs into the small arrays");
+static_assert(PlanPrep::STRONG_ACC + 32768 == PlanPrep::TB_LO + 8192 && PlanFused::STRONG_ACC + 32768 == OFF_TB_LO + 8192,
+              "the strong-channel correction (32 KB) must span the Aqk and Tb tiles exactly");
+static_assert(PlanPrep::STRONG_STAGE + 24576 <= PlanPrep::QST && PlanFused::STRONG_STAGE + 24576 <= OFF_QST,
+              "the strong-channel staging (24 KB) must fit the v tiles");
 
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
     __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
@@ -224,12 +252,132 @@ __device__ __forceinline__ void put_row_split(uint8_t *sm, uint32_t off_hi, uint
     *reinterpret_cast<uint2 *>(sm + off_lo + o) = make_uint2(pack_bf16(lv[0], lv[1]), pack_bf16(lv[2], lv[3]));
 }
 
-// q and k: reads GST, QST, KST and the q, k rows of HIST; writes X/XL ([Kh; Qh] rows), KB, BETA,
-// G0, GL, REF, and FCOL = exp(LOGF + r) when fcol is given.  Reads of GST all precede the first
-// barrier, so GST may share its region with KB.
+// ---- strong channels (in-chunk decay above kStrongDecay) ----
+__device__ __forceinline__ const uint32_t *strong_mask(const uint8_t *sm) {
+    return reinterpret_cast<const uint32_t *>(sm + OFF_MISC + OFF_SMASK);
+}
+// 4 bits: whether channels c0 .. c0 + 3 (c0 a multiple of 4) are strong
+__device__ __forceinline__ uint32_t strong_bits4(const uint32_t *mask, int c0) { return (mask[c0 >> 5] >> (c0 & 31)) & 15u; }
+// rank of strong channel c among the strong channels
+__device__ __forceinline__ int strong_rank(const uint32_t *mask, int c) {
+    int p = __popc(mask[c >> 5] & ((1u << (c & 31)) - 1u));
+    for (int w = 0; w < (c >> 5); ++w) p += __popc(mask[w]);
+    return p;
+}
+
+// The strong channels' share of the MMA A result, exactly: for row i and column j of the chunk
+//   D[i][j] = sum_c k_ic k_jc exp(G_ic - G_jc),   D[64 + i][j] = sum_c q_ic k_jc exp(G_ic - G_jc)
+// over the strong channels c (j <= i; the extract masks the rest and applies beta), written into
+// TMEM columns [col, col + 64) of the MMA A accumulator (and zeros into [col + 64, col + 128) for a
+// stacked Kb, whose N = 128 chain accumulates there too).  The strong channels go in groups of 32
+// through a staging area ([k | q | G log2 e][32 channels][64 tokens] fp32); each of 272 threads
+// holds a block of 4 rows i x 2 columns j of the lower triangle, so that every exponential
+// serves both the k row and the q row; the blocks meet in an fp32 [128][64] array whose 16-byte
+// slots are swizzled by row.
 template <class P>
-__device__ __forceinline__ void prep_qk(uint8_t *sm, const PrefillArgs &a, int cs, int Lc, int h, int W,
-                                        const float *logf, float *fcol) {
+__device__ __forceinline__ void strong_correction(uint8_t *sm, const float (&yq)[kTok][4], const float (&yk)[kTok][4],
+                                                  const float (&G)[kTok][4], uint32_t tl, uint32_t col) {
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int i0 = warp * kTok, c0 = lane * 4;
+    const uint32_t *mask = strong_mask(sm);
+    float *stK = reinterpret_cast<float *>(sm + P::STRONG_STAGE);
+    float *stQ = stK + 32 * kC, *stG = stQ + 32 * kC;
+    float *acc = reinterpret_cast<float *>(sm + P::STRONG_ACC);
+    const int ns = __popc(mask[0]) + __popc(mask[1]) + __popc(mask[2]) + __popc(mask[3]);
+    const uint32_t mine = strong_bits4(mask, c0);
+    const int rank0 = mine ? strong_rank(mask, c0) : 0;
+    // this thread's block: rows 4 bi .. + 3, columns 2 bj .. + 1 (row block bi holds 2 bi + 2 blocks)
+    const bool unit = tid < 272;
+    int bi = 0;
+    while ((bi + 1) * (bi + 2) <= tid) ++bi;
+    const int bj = tid - bi * (bi + 1);
+    float akk[4][2], aqk[4][2];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) akk[u][0] = akk[u][1] = aqk[u][0] = aqk[u][1] = 0.f;
+    constexpr float kLog2e = 1.4426950408889634f;
+    for (int g0 = 0; g0 < ns; g0 += 32) {
+        int p = rank0;
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+            if ((mine >> m) & 1u) {
+                if (p >= g0 && p < g0 + 32) {
+                    const int s = p - g0;
+                    *reinterpret_cast<float4 *>(stK + s * kC + i0) = make_float4(yk[0][m], yk[1][m], yk[2][m], yk[3][m]);
+                    *reinterpret_cast<float4 *>(stQ + s * kC + i0) = make_float4(yq[0][m], yq[1][m], yq[2][m], yq[3][m]);
+                    *reinterpret_cast<float4 *>(stG + s * kC + i0) =
+                        make_float4(G[0][m] * kLog2e, G[1][m] * kLog2e, G[2][m] * kLog2e, G[3][m] * kLog2e);
+                }
+                ++p;
+            }
+        }
+        __syncthreads();
+        if (unit) {
+            const int ng = min(32, ns - g0);
+            for (int s = 0; s < ng; ++s) {
+                const float4 ki = *reinterpret_cast<const float4 *>(stK + s * kC + 4 * bi);
+                const float4 qi = *reinterpret_cast<const float4 *>(stQ + s * kC + 4 * bi);
+                const float4 gi = *reinterpret_cast<const float4 *>(stG + s * kC + 4 * bi);
+                const float2 kj = *reinterpret_cast<const float2 *>(stK + s * kC + 2 * bj);
+                const float2 gj = *reinterpret_cast<const float2 *>(stG + s * kC + 2 * bj);
+                const float kiv[4] = {ki.x, ki.y, ki.z, ki.w}, qiv[4] = {qi.x, qi.y, qi.z, qi.w};
+                const float giv[4] = {gi.x, gi.y, gi.z, gi.w};
+                const float kjv[2] = {kj.x, kj.y}, gjv[2] = {gj.x, gj.y};
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+#pragma unroll
+                    for (int v = 0; v < 2; ++v) {
+                        // G is non-increasing, so the exponent is <= 0 wherever j <= i; above the
+                        // diagonal (masked by the extract) it is capped at 0
+                        const float t = kjv[v] * exp2f(fminf(giv[u] - gjv[v], 0.f));
+                        akk[u][v] = fmaf(kiv[u], t, akk[u][v]);
+                        aqk[u][v] = fmaf(qiv[u], t, aqk[u][v]);
+                    }
+            }
+        }
+        __syncthreads();                                 // the staging area is rewritten by the next group
+    }
+    if (unit) {
+        const int slot = bj >> 1, half = (bj & 1) * 2;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int r = 4 * bi + u;
+            *reinterpret_cast<float2 *>(acc + r * 64 + ((slot ^ (r & 15)) << 2) + half) = make_float2(akk[u][0], akk[u][1]);
+            *reinterpret_cast<float2 *>(acc + (64 + r) * 64 + ((slot ^ (r & 15)) << 2) + half) =
+                make_float2(aqk[u][0], aqk[u][1]);
+        }
+    }
+    __syncthreads();
+    {
+        // TMEM lane row = this warp's lane base + lane; columns 16 * quarter .. + 15
+        const int row = 32 * (warp & 3) + lane, quarter = warp >> 2, rb = (row & 63) >> 2;
+        uint32_t v[16];
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            const int slot = quarter * 4 + t;
+            const float4 x = slot <= rb ? *reinterpret_cast<const float4 *>(acc + row * 64 + ((slot ^ (row & 15)) << 2))
+                                        : make_float4(0.f, 0.f, 0.f, 0.f);
+            v[4 * t] = __float_as_uint(x.x); v[4 * t + 1] = __float_as_uint(x.y);
+            v[4 * t + 2] = __float_as_uint(x.z); v[4 * t + 3] = __float_as_uint(x.w);
+        }
+        tmem_st16(tl + col + quarter * 16, v);
+        if (P::KB_STACKED) {
+#pragma unroll
+            for (int t = 0; t < 16; ++t) v[t] = 0u;
+            tmem_st16(tl + col + 64 + quarter * 16, v);
+        }
+        tmem_wait_st();
+    }
+}
+
+// q and k: reads GST, QST, KST and the q, k rows of HIST; writes X/XL ([Kh; Qh] rows), KB, BETA
+// (unless the caller stages it), G0, GL, REF (rho) and the strong-channel masks; returns Kd =
+// k exp(G_last - G) for this thread's 4 tokens x 4 channels in kd, and whether the chunk has a
+// strong channel, whose exact share of MMA A is then already in TMEM columns [col, col + 64) (the
+// chain must accumulate onto it).  Reads of GST all precede the first barrier, so GST may share
+// its region with KB and the strong-channel staging.
+template <class P>
+__device__ __forceinline__ bool prep_qk(uint8_t *sm, const PrefillArgs &a, int cs, int Lc, int h, int W, uint32_t tl,
+                                        uint32_t col, float (&kd)[kTok][4]) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int H = a.H;
     const int i0 = warp * kTok, c0 = lane * 4;
@@ -238,6 +386,7 @@ __device__ __forceinline__ void prep_qk(uint8_t *sm, const PrefillArgs &a, int c
     float *sGL = reinterpret_cast<float *>(sm + OFF_GL);
     float *sG0 = reinterpret_cast<float *>(sm + OFF_G0);
     float *sScan = reinterpret_cast<float *>(sm + P::SCAN);
+    uint32_t *sMask = reinterpret_cast<uint32_t *>(sm + OFF_MISC + OFF_SMASK);
     float G[kTok][4];
     {
         float run[4] = {0.f, 0.f, 0.f, 0.f};
@@ -271,50 +420,52 @@ __device__ __forceinline__ void prep_qk(uint8_t *sm, const PrefillArgs &a, int c
                 make_float4(G[kTok - 1][0], G[kTok - 1][1], G[kTok - 1][2], G[kTok - 1][3]);
     }
     __syncthreads();
+    bool strong = false;
     if (tid < kD) {
-        const float r = 0.5f * (sG0[tid] + sGL[tid]);
-        sRef[tid] = r;
-        if (fcol) fcol[tid] = expf(logf[tid] + r);     // TMEM basis -> this chunk's S' = exp(r) S
+        const float g0 = sG0[tid], gl = sGL[tid];
+        strong = g0 - gl > kStrongDecay;
+        sRef[tid] = strong ? g0 : 0.5f * (g0 + gl);
+    }
+    {
+        const uint32_t m = __ballot_sync(0xffffffffu, strong);
+        if (warp < 4 && lane == 0) sMask[warp] = m;
     }
     if (P::CALLER_STAGES && tid == 0) bulk_wait_read_all();   // X rows are rewritten below
-    __syncthreads();
-    float E[kTok][4], Eb[kTok][4];
+    const bool any_strong = __syncthreads_or(strong) != 0;
+    float yq[kTok][4], yk[kTok][4];
+    conv_rows(sm, a, 0, P::QST, Lc, W, yq);
+    conv_rows(sm, a, 1, P::KST, Lc, W, yk);
+    if (any_strong) strong_correction<P>(sm, yq, yk, G, tl, col);
     {
         const float4 r4 = *reinterpret_cast<const float4 *>(sRef + c0);
-        const float rr[4] = {r4.x, r4.y, r4.z, r4.w};
+        const float4 l4 = *reinterpret_cast<const float4 *>(sGL + c0);
+        const float rr[4] = {r4.x, r4.y, r4.z, r4.w}, gl[4] = {l4.x, l4.y, l4.z, l4.w};
+        const uint32_t sb = strong_bits4(sMask, c0);
 #pragma unroll
-        for (int m = 0; m < 4; ++m)
+        for (int ii = 0; ii < kTok; ++ii) {
+            float qh[4], kh[4], kb[4];
 #pragma unroll
-            for (int ii = 0; ii < kTok; ++ii) {
-                const float x = fminf(fmaxf(G[ii][m] - rr[m], -87.f), 87.f);
-                E[ii][m] = __expf(x);
-                Eb[ii][m] = __expf(-x);
+            for (int m = 0; m < 4; ++m) {
+                // |G - rho| <= kStrongDecay / 2 for the other channels; G - rho <= 0 for strong ones,
+                // whose factorised product is left out (Kb column zero)
+                const float x = G[ii][m] - rr[m];
+                const float e = __expf(x);
+                const float eb = ((sb >> m) & 1u) ? 0.f : __expf(-x);
+                qh[m] = yq[ii][m] * e;
+                kh[m] = yk[ii][m] * e;
+                kb[m] = yk[ii][m] * eb;
+                kd[ii][m] = yk[ii][m] * __expf(gl[m] - G[ii][m]);
             }
-    }
-    float y[kTok][4];
-    // q -> Qh = q E  (rows 64..127 of X / XL)
-    conv_rows(sm, a, 0, P::QST, Lc, W, y);
-#pragma unroll
-    for (int ii = 0; ii < kTok; ++ii) {
-        float t4[4];
-#pragma unroll
-        for (int m = 0; m < 4; ++m) t4[m] = y[ii][m] * E[ii][m];
-        put_row_split(sm, P::X_HI, P::X_LO, P::X_ATOM, 64 + i0 + ii, c0, t4);
-    }
-    // k -> Kh = k E (rows 0..63 of X / XL), Kb = k / E (rows; the state update reads them MN-major)
-    conv_rows(sm, a, 1, P::KST, Lc, W, y);
-#pragma unroll
-    for (int ii = 0; ii < kTok; ++ii) {
-        float t4[4], u4[4];
-#pragma unroll
-        for (int m = 0; m < 4; ++m) { t4[m] = y[ii][m] * E[ii][m]; u4[m] = y[ii][m] * Eb[ii][m]; }
-        put_row_split(sm, P::X_HI, P::X_LO, P::X_ATOM, i0 + ii, c0, t4);
-        if (P::KB_STACKED) put_row_split(sm, P::KB_HI, P::KB_HI + 8192, 16384, i0 + ii, c0, u4);
-        else put_row_split(sm, P::KB_HI, P::KB_LO, 8192, i0 + ii, c0, u4);
+            put_row_split(sm, P::X_HI, P::X_LO, P::X_ATOM, 64 + i0 + ii, c0, qh);   // Qh rows 64..127
+            put_row_split(sm, P::X_HI, P::X_LO, P::X_ATOM, i0 + ii, c0, kh);        // Kh rows 0..63
+            if (P::KB_STACKED) put_row_split(sm, P::KB_HI, P::KB_HI + 8192, 16384, i0 + ii, c0, kb);
+            else put_row_split(sm, P::KB_HI, P::KB_LO, 8192, i0 + ii, c0, kb);
+        }
     }
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
+    return any_strong;
 }
 
 // v: reads VST and the v rows of HIST; writes V_HI/LO (v rows, hi/lo; lo is zero unless the conv
@@ -332,17 +483,28 @@ __device__ __forceinline__ void prep_v(uint8_t *sm, const PrefillArgs &a, int Lc
     __syncthreads();
 }
 
-template <class P>
-__device__ __forceinline__ void prep_chunk(uint8_t *sm, const PrefillArgs &a, int cs, int Lc, int h, int W,
-                                           const float *logf, float *fcol) {
-    prep_qk<P>(sm, a, cs, Lc, h, W, logf, fcol);
-    prep_v<P>(sm, a, Lc, W);
+// Kd (4 tokens x 4 channels of this thread) as split-bf16 rows of a K = 128 tile whose two 64-wide
+// K atoms lie 16 KB apart, each the hi 64-row tile then the lo one: the layout of a stacked Kb tile
+// and of the record's Kd part, read MN-major by the state update.  dst is a shared or a global
+// (generic) address.
+__device__ __forceinline__ void put_kd(uint8_t *dst, const float (&kd)[kTok][4]) {
+    const int warp = threadIdx.x >> 5, c0 = (threadIdx.x & 31) * 4;
+#pragma unroll
+    for (int ii = 0; ii < kTok; ++ii) {
+        float hv[4], lv[4];
+#pragma unroll
+        for (int m = 0; m < 4; ++m) split_bf16(kd[ii][m], hv[m], lv[m]);
+        const uint32_t o = (c0 >> 6) * 16384u + sw128_offset(warp * kTok + ii, c0 & 63);
+        *reinterpret_cast<uint2 *>(dst + o) = make_uint2(pack_bf16(hv[0], hv[1]), pack_bf16(hv[2], hv[3]));
+        *reinterpret_cast<uint2 *>(dst + o + 8192) = make_uint2(pack_bf16(lv[0], lv[1]), pack_bf16(lv[2], lv[3]));
+    }
 }
 
 // ---- stage 2 (one thread): [Kh; Qh] Kb^T -> TMEM columns [col, col + 64) (with a stacked Kb tile:
-// [col, col + 128), the sum of the two halves), commit to mbar ----
+// [col, col + 128), the sum of the two halves), commit to mbar; with acc the chain adds onto what
+// the columns hold (the strong channels' share) ----
 template <class P>
-__device__ __forceinline__ void issue_mma_a(uint32_t sbase, uint32_t tmem_col_addr, uint32_t mbar) {
+__device__ __forceinline__ void issue_mma_a(uint32_t sbase, uint32_t tmem_col_addr, uint32_t mbar, bool acc) {
     tc_fence_after();
     const uint64_t dX = sdesc_kmajor_sw128(sbase + P::X_HI), dXL = sdesc_kmajor_sw128(sbase + P::X_LO);
     if (P::KB_STACKED) {
@@ -352,7 +514,7 @@ __device__ __forceinline__ void issue_mma_a(uint32_t sbase, uint32_t tmem_col_ad
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
             mma_bf16(tmem_col_addr, dadd(dX, (kk >> 2) * P::X_ATOM + (kk & 3) * 32),
-                     dadd(dK, (kk >> 2) * 16384 + (kk & 3) * 32), id128, kk != 0);
+                     dadd(dK, (kk >> 2) * 16384 + (kk & 3) * 32), id128, acc || kk != 0);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
             mma_bf16(tmem_col_addr, dadd(dXL, (kk >> 2) * P::X_ATOM + (kk & 3) * 32),
@@ -365,7 +527,7 @@ __device__ __forceinline__ void issue_mma_a(uint32_t sbase, uint32_t tmem_col_ad
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)
                 mma_bf16(tmem_col_addr, dadd(sp == 2 ? dXL : dX, (kk >> 2) * P::X_ATOM + (kk & 3) * 32),
-                         dadd(sp == 1 ? dKl : dKh, (kk >> 2) * 8192 + (kk & 3) * 32), id, (sp | kk) != 0);
+                         dadd(sp == 1 ? dKl : dKh, (kk >> 2) * 8192 + (kk & 3) * 32), id, acc || (sp | kk) != 0);
     }
     mma_commit(mbar);
 }

@@ -55,8 +55,8 @@ def test_workspace_size_is_aligned_and_grows_with_conv(lib):
     assert e == 256 + 256 + ((1000 + 63 * 3) // 64) * 2 * 148480
     # fp32 CUDA-core shapes stage the conv output in an fp32 [T, D] buffer
     # long sequences with few (sequence, head) pairs: a ring of three segments' records plus the
-    # scan's state carry (66,048 B per sequence and head), independent of T up to 64 segments
-    carry = -(-32 * 66048 // 256) * 256
+    # scan's state carry (65,536 B per sequence and head), independent of T up to 64 segments
+    carry = 32 * 65536
     ring = lambda chunks: min(chunks, 3 * max(80, -(-chunks // 64))) * 32 * 148480
     for T in (8192, 65536, 1 << 18):
         assert K.k3kda_prefill_workspace_size(1, T, 32, 128, 128, 64, K.BF16, True) == 256 + 256 + carry + ring(T // 64)
@@ -118,8 +118,8 @@ def test_backward_rejects_bad_arguments(lib):
 
 
 def test_backward_workspace_size(lib):
-    """The chunked backward's scratch: per (16-token chunk, head) item its fp32 tiles (Qt, Kt, Kh,
-    e^G', W, U, Delta, dR: 16 x 128 each; Tm, Aqk, B: 16 x 16; r, Gamma_L - r: 128; dX: 128 x 128),
+    """The chunked backward's scratch: per (16-token chunk, head) item its fp32 tiles (Q0, K0, Kd,
+    Gamma, W, U, Delta, dR: 16 x 128 each; Tm, Aqk, B: 16 x 16; Gamma_L: 128; Dout: 128 x 128),
     the state at every chunk start and each sequence's end, and the chunk tables (offsets; first
     token, length and sequence of each chunk); each array starts on a 256-byte boundary after a
     256-byte status word."""
@@ -128,7 +128,7 @@ def test_backward_workspace_size(lib):
         Q = (T + 15 * N) // 16 + 1
         NI = Q * H
         want = 256 + r(4 * (N + 1)) + 3 * r(4 * Q) + 8 * r(NI * 16 * 128 * 4) + 3 * r(NI * 256 * 4) + \
-            2 * r(NI * 128 * 4) + r(NI * 128 * 128 * 4) + r((Q + N) * H * 128 * 128 * 4)
+            r(NI * 128 * 4) + r(NI * 128 * 128 * 4) + r((Q + N) * H * 128 * 128 * 4)
         assert K.k3kda_backward_workspace_size(N, T, H, 128, 128) == want
     assert K.k3kda_backward_workspace_size(1, 8192, 32, 64, 64) == 256
 
