@@ -11,14 +11,20 @@ One step = one pass of the whole mixer hot path on synthetic inputs:
 value = (prefill tokens + decode tokens) per step / step time, device-resident
 inputs; the "prefill" and "decode" objects give each part on its own with its
 roofline.  Beside the step, not in value: "e2e" (the same step from pinned host
-buffers), "backward" (gradients of the recurrence, T=8192, H=32) and "mla_decode"
-(one decode token of the hybrid's attention layers, 256 sequences with bf16 caches
-of 8192 rows).  With --gpus N under torchrun every rank runs its own replica of the
+buffers), "configs" (the other synthetic workloads timed on their own: the fp32
+core's latency, the chunked prefill T=8192 and the packed varlen prefill with
+initial states, each with its roofline), "parity" (each workload's max-abs and
+RMS-relative error on one small seeded case against the oracle), "backward"
+(gradients of the recurrence, T=8192, H=32) and "mla_decode" (one decode token of
+the hybrid's attention layers, 256 sequences with bf16 caches of 8192 rows).  With --gpus N under torchrun every rank runs its own replica of the
 step (heads and sequences never interact, so there is no collective): weak
 scaling, max time over ranks.
 
 --impl reference times the CPU oracle (the reference arm for this method) on a
-bounded sample of the same workload on the host cores.
+bounded sample of the same workload on the host cores.  The CPU-baseline leg (rank 0,
+N=1, before any GPU work) times the FP64 oracle and the FP32 per-token loop on a
+sample of the step, and runs the oracle on the small parity cases whose GPU results
+are compared after the timed arm.
 """
 from __future__ import annotations
 
@@ -39,6 +45,9 @@ METRIC = "KDA prefill tokens/s & decode tokens/s at 1 GB300; % of tensor/HBM roo
 PREFILL = dict(T=65536, H=32, d=128, chunk=64, W=4)
 DECODE = dict(N=256, H=32, d=128, W=4)
 BACKWARD = dict(T=8192, H=32, d=128)      # gradients of the recurrence: the chunked-prefill shape
+CORE = dict(T=64, H=2, d=16, chunk=16)    # the fp32 core workload (latency)
+CHUNKED = dict(T=8192, H=32, d=128, chunk=64)                        # chunked prefill, bf16, S0 = 0
+VARLEN = dict(n_seqs=16, lo=256, hi=16384, H=32, d=128, chunk=64)    # packed, lengths from seed 0, S0 != 0
 MLA = dict(N=256, H=32, d=128, L_max=8192)   # the attention layers' decode token: the decode batch
 MLA_TRAFFIC_PER_KEY_HEAD = 1.385983e9 / ((84420 + 16) * 32)   # DRAM bytes per attended (key, head), measured
 
@@ -56,6 +65,7 @@ def parse():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-backward", action="store_true")
     p.add_argument("--no-mla", action="store_true")
+    p.add_argument("--no-configs", action="store_true", help="skip the other workloads' lines")
     p.add_argument("--mla-seqs", type=int, default=None,
                    help="override the attention decode batch (profiling captures on a smaller case)")
     p.add_argument("--prefill-tokens", type=int, default=None,
@@ -76,11 +86,15 @@ def peaks():
 
 # ---- algorithmic work (bytes that must cross HBM, flops of the chunked form) ----
 
-def prefill_work(T, H, d, chunk, W, N=1):
+def prefill_work(T, H, d, chunk, W, N=1, gate=True, initial_state=False):
+    """Bytes: q, k, v (bf16), g (fp32), beta, the gate (bf16) when gated, the bf16 output, the fp32
+    final state (and the initial state when given), the conv state in and out and the conv weights
+    when W > 0.  Flops: the chunked form, 10 C d + 6 d^2 per (token, head), plus the conv."""
     dk = dv = d
-    per_tok_head = 2 * (2 * dk + dv) + 4 * dk + 4 + 2 * dv + 2 * dv    # q,k,v bf16; g; beta; gate; out bf16
+    per_tok_head = 2 * (2 * dk + dv) + 4 * dk + 4 + (2 * dv if gate else 0) + 2 * dv
     D = 2 * H * dk + H * dv
-    bytes_ = T * H * per_tok_head + N * H * dk * dv * 4 + 2 * N * (W - 1) * D * 4 + D * W * 4
+    conv = 2 * N * (W - 1) * D * 4 + D * W * 4 if W > 0 else 0     # conv state in and out, weights
+    bytes_ = T * H * per_tok_head + N * H * dk * dv * 4 * (2 if initial_state else 1) + conv
     flops = T * H * (10 * chunk * d + 6 * d * d) + T * D * 2 * W
     return bytes_, flops
 
@@ -311,11 +325,156 @@ def run_ours(args, rank, world, dev, torch):
     }
     if not args.no_e2e:
         res["e2e"] = run_e2e(args, K, torch, dev, P, Dc, prefill_call, decode_call, out_p, fs, out_d, world, barrier)
+    if not args.no_configs:
+        res["configs"] = run_configs(args, K, torch, dev, rank, world)
     if not args.no_backward:
         res["backward"] = run_backward(args, K, torch, dev, rank, world, clk_mhz=res["clocks"].get("sm_mhz"))
     if not args.no_mla:
         res["mla_decode"] = run_mla(args, K, torch, dev, rank, world)
     return res
+
+
+def _time_calls(torch, call, steps, warmup, stream):
+    """Average CUDA-event time (ms) of `steps` calls after `warmup` untimed ones."""
+    for _ in range(warmup):
+        call()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        call()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / steps
+
+
+def _prefill_roofline(pk, by, fl, ms, traffic):
+    ach = by / (ms / 1e3) / 1e9
+    return {"bound": "hbm", "achieved": ach, "peak": pk["hbm"], "unit": "GB/s", "frac": ach / pk["hbm"],
+            "traffic": traffic,
+            "tensor": {"achieved_tflops": fl / (ms / 1e3) / 1e12, "peak": pk["bf16"],
+                       "frac": fl / (ms / 1e3) / 1e12 / pk["bf16"]}}
+
+
+def run_configs(args, K, torch, dev, rank, world):
+    """The other synthetic workloads, each timed on its own with CUDA events on the launching
+    stream (inputs drawn on the device with the workload recipe, larger than L2 except the fp32
+    core): the fp32 core (T=64, H=2, d=16, chunk 16; a latency), the chunked prefill (B=1, T=8192,
+    H=32, d=128, bf16 q/k/v, zero initial state, bf16 outputs, fp32 final state) and the packed
+    varlen prefill (16 sequences, lengths uniform in [256, 16384] from seed 0, initial states
+    ~ N(0, 0.02), bf16 outputs, fp32 final states)."""
+    import kda_inputs as KI
+    pk = peaks()
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(4000 + rank)
+    f32, bf16 = torch.float32, torch.bfloat16
+    stream = torch.cuda.current_stream()
+
+    def n(shape, std=1.0, dt=f32):
+        return (torch.randn(shape, generator=gen, device=dev, dtype=f32) * std).to(dt)
+
+    def prefill_inputs(T, H, d, dt):
+        return dict(q=n((T, H, d), dt=dt), k=n((T, H, d), dt=dt), v=n((T, H, d), dt=dt),
+                    g=-torch.nn.functional.softplus(n((T, H, d))), beta=torch.sigmoid(n((T, H))))
+
+    out = {}
+    steps = max(1, args.steps)
+    # ---- fp32 core: latency of one call ----
+    T, H, d, C = CORE["T"], CORE["H"], CORE["d"], CORE["chunk"]
+    x = prefill_inputs(T, H, d, f32)
+    cu_h = torch.tensor([0, T], dtype=torch.int32)
+    cu_d = cu_h.to(dev)
+    o = torch.empty((T, H, d), device=dev)
+    fs = torch.empty((1, H, d, d), device=dev)
+    ws = torch.zeros(K.k3kda_prefill_workspace_size(1, T, H, d, d, C, K.F32, False), dtype=torch.uint8, device=dev)
+    call = lambda: K.k3kda_prefill(x["q"], x["k"], x["v"], x["g"], x["beta"], None, cu_d, cu_h, 1, T, H, d, d, C,
+                                   d ** -0.5, True, None, None, 0, None, o, fs, ws, stream)
+    ms = _time_calls(torch, call, max(steps, 200), args.warmup, stream)
+    ms = max_over_ranks([ms], world, dev)[0]
+    out["core_fp32"] = {"workload": f"KDA core fp32, T={T} H={H} d={d} chunk {C}, no conv or gate", "us": ms * 1e3,
+                        "tokens_per_s": world * T / (ms / 1e3), "bound": "latency"}
+    # ---- chunked prefill ----
+    T, H, d, C = CHUNKED["T"], CHUNKED["H"], CHUNKED["d"], CHUNKED["chunk"]
+    x = prefill_inputs(T, H, d, bf16)
+    cu_h = torch.tensor([0, T], dtype=torch.int32)
+    cu_d = cu_h.to(dev)
+    o = torch.empty((T, H, d), dtype=bf16, device=dev)
+    fs = torch.empty((1, H, d, d), device=dev)
+    ws = torch.zeros(K.k3kda_prefill_workspace_size(1, T, H, d, d, C, K.BF16, False), dtype=torch.uint8, device=dev)
+    call = lambda: K.k3kda_prefill(x["q"], x["k"], x["v"], x["g"], x["beta"], None, cu_d, cu_h, 1, T, H, d, d, C,
+                                   d ** -0.5, True, None, None, 0, None, o, fs, ws, stream)
+    ms = _time_calls(torch, call, steps, args.warmup, stream)
+    ms = max_over_ranks([ms], world, dev)[0]
+    by, fl = prefill_work(T, H, d, C, 0, gate=False)
+    out["chunked_prefill"] = {"workload": f"chunked prefill B=1 T={T} H={H} d={d} chunk {C}, bf16 in/out, S0=0",
+                              "ms": ms, "tokens_per_s": world * T / (ms / 1e3), "algorithmic_bytes": by,
+                              "algorithmic_flops": fl, "workspace_bytes": ws.numel(),
+                              "roofline": _prefill_roofline(pk, by, fl, ms, CHUNKED_TRAFFIC_PER_LAUNCH)}
+    del x, o, ws
+    # ---- packed varlen prefill with initial states ----
+    lengths = KI.varlen_lengths(VARLEN["n_seqs"], VARLEN["lo"], VARLEN["hi"], 0)
+    N, H, d, C = len(lengths), VARLEN["H"], VARLEN["d"], VARLEN["chunk"]
+    cu_np = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)
+    T = int(cu_np[-1])
+    x = prefill_inputs(T, H, d, bf16)
+    S0 = n((N, H, d, d), 0.02)
+    cu_h = torch.from_numpy(cu_np)
+    cu_d = cu_h.to(dev)
+    o = torch.empty((T, H, d), dtype=bf16, device=dev)
+    fs = torch.empty((N, H, d, d), device=dev)
+    ws = torch.zeros(K.k3kda_prefill_workspace_size(N, T, H, d, d, C, K.BF16, False), dtype=torch.uint8, device=dev)
+    call = lambda: K.k3kda_prefill(x["q"], x["k"], x["v"], x["g"], x["beta"], S0, cu_d, cu_h, N, T, H, d, d, C,
+                                   d ** -0.5, True, None, None, 0, None, o, fs, ws, stream)
+    ms = _time_calls(torch, call, steps, args.warmup, stream)
+    ms = max_over_ranks([ms], world, dev)[0]
+    by, fl = prefill_work(T, H, d, C, 0, N=N, gate=False, initial_state=True)
+    out["varlen_prefill"] = {"workload": f"packed varlen prefill, {N} sequences (lengths uniform in "
+                                         f"[{VARLEN['lo']}, {VARLEN['hi']}] from seed 0: {T} tokens), H={H} d={d} "
+                                         f"chunk {C}, bf16 in/out, fp32 initial and final states",
+                             "ms": ms, "tokens_per_s": world * T / (ms / 1e3), "algorithmic_bytes": by,
+                             "algorithmic_flops": fl, "workspace_bytes": ws.numel(),
+                             "longest_sequence": int(lengths.max()),
+                             "roofline": _prefill_roofline(pk, by, fl, ms, VARLEN_TRAFFIC_PER_LAUNCH)}
+    del x, o, ws, fs, S0
+    torch.cuda.empty_cache()
+    return out
+
+
+def run_parity(K, torch, refs):
+    """Each workload's error on its small seeded case: the GPU through the public binding against
+    the oracle's outputs computed in the CPU-baseline leg (bf16-input workloads store fp32 outputs,
+    the comparison the 5e-3 x RMS bar is stated on)."""
+    out = {}
+    for name, r in refs.items():
+        c = r["case"]
+        dev = lambda a, bf=False: None if a is None else torch.from_numpy(np.ascontiguousarray(a)).to(
+            torch.bfloat16 if bf else torch.float32).cuda()
+        bf = c.in_dtype == "bf16"
+        if name == "decode":
+            st, cs = dev(c.state), dev(c.conv_state)
+            o = K.decode_step(dev(c.q, bf), dev(c.k, bf), dev(c.v, bf), dev(c.g), dev(c.beta), st,
+                              gate=dev(c.gate, bf), conv_weight=dev(c.conv_w), conv_state=cs,
+                              out_dtype=torch.float32)
+            got = [o, st]
+        else:
+            cs = None
+            if c.conv_w is not None:
+                cs = torch.zeros((c.N, c.W - 1, 2 * c.H * c.dk + c.H * c.dv), device="cuda")
+            o, fs = K.prefill(dev(c.q, bf), dev(c.k, bf), dev(c.v, bf), dev(c.g), dev(c.beta),
+                              initial_state=dev(c.S0), cu_seqlens=torch.from_numpy(c.cu_seqlens.copy()),
+                              chunk=c.chunk, scale=c.scale, use_qk_l2norm=c.use_qk_l2norm,
+                              conv_weight=dev(c.conv_w), conv_state=cs, gate=dev(c.gate, bf),
+                              out_dtype=torch.float32)
+            got = [o, fs]
+        torch.cuda.synchronize()
+        entry = {"case": r["desc"], "bar": r["bar"]}
+        for what, g, w in zip(("out", "final_state"), got, r["want"]):
+            gv = g.detach().double().cpu().numpy()
+            err = float(np.abs(gv - w).max())
+            rms = float(np.sqrt(np.mean(w * w)))
+            entry[what] = {"max_abs": err, "rms_rel": err / rms if rms > 0 else None}
+        out[name] = entry
+    return out
 
 
 def run_mla(args, K, torch, dev, rank, world):
@@ -487,7 +646,9 @@ def run_e2e(args, K, torch, dev, P, Dc, prefill_call, decode_call, out_p, fs, ou
 # Measured DRAM bytes per call (ncu dram__bytes_read.sum + dram__bytes_write.sum, summed over the
 # call's kernels) of the current kernel versions, or None when not yet captured for a kernel
 # version.  The prefill figure is a T=8192 capture scaled by the tokens processed to T=65536.
-PREFILL_TRAFFIC_PER_LAUNCH = 12.13e9     # two-pass call: prep + scan + offsets, 1.517 GB at T=8192 x 8
+PREFILL_TRAFFIC_PER_LAUNCH = None        # two-pass call (prep + scan + offsets): not yet captured for this version
+CHUNKED_TRAFFIC_PER_LAUNCH = None
+VARLEN_TRAFFIC_PER_LAUNCH = None
 DECODE_TRAFFIC_PER_LAUNCH = 1.0997e9
 
 
@@ -510,6 +671,46 @@ def cpu_oracle_sample(prefill_tokens, decode_seqs, seed=0):
                   conv_state=dc.conv_state)
     td = time.perf_counter() - t0
     return tp, td, O.num_threads()
+
+
+def cpu_f32_sample(prefill_tokens, seed=0):
+    """Time the FP32 per-token CPU baseline on the first `prefill_tokens` tokens of the fused-mixer
+    workload (all 32 heads); return the seconds and the threads used."""
+    import kda_inputs as KI
+    import oracle as O
+    O.load_cpu_f32()
+    c = KI.fused_mixer(seed=seed, T=prefill_tokens, H=PREFILL["H"], d=PREFILL["d"], W=PREFILL["W"])
+    t0 = time.perf_counter()
+    O.cpu_f32_mixer(c.q, c.k, c.v, c.g, c.beta, gate=c.gate, conv_w=c.conv_w)
+    return time.perf_counter() - t0, O.cpu_f32_threads()
+
+
+def parity_refs():
+    """The oracle's results on one small seeded case of each workload (run in the CPU leg)."""
+    import kda_inputs as KI
+    import oracle as O
+    cases = {
+        "core_fp32": (KI.core_fp32(seed=0), "T=64 H=2 d=16 chunk 16 fp32, q/k unit rows, seed 0", "1e-5 max-abs"),
+        "chunked_prefill": (KI.chunked_prefill(seed=0, T=1000, H=4), "T=1000 H=4 d=128 chunk 64 bf16, seed 0",
+                            "5e-3 x RMS"),
+        "varlen_prefill": (KI.prefill_case("varlen_parity", [300, 65, 1, 700], 4, 128, 128, 64, "bf16", seed=0,
+                                           s0_std=0.02),
+                           "4 sequences (300, 65, 1, 700 tokens) H=4 d=128 bf16, S0 ~ N(0, 0.02), seed 0",
+                           "5e-3 x RMS"),
+        "fused_mixer": (KI.fused_mixer(seed=0, T=777, H=4), "T=777 H=4 d=128 conv 4 gate bf16, seed 0", "5e-3 x RMS"),
+    }
+    refs = {}
+    for name, (c, desc, bar) in cases.items():
+        o, S, _ = O.mixer(c.q, c.k, c.v, c.g, c.beta, initial_state=c.S0, gate=c.gate, conv_w=c.conv_w,
+                          cu_seqlens=c.cu_seqlens, scale=c.scale, use_qk_l2norm=c.use_qk_l2norm)
+        refs[name] = {"case": c, "desc": desc, "bar": bar, "want": [o, S]}
+    d = KI.decode_case(seed=0, N=16, H=4, d=128)
+    o, S, _ = O.decode_step(d.q, d.k, d.v, d.g, d.beta, d.state, gate=d.gate, conv_w=d.conv_w,
+                            conv_state=d.conv_state)
+    d.in_dtype = "bf16"
+    refs["decode"] = {"case": d, "desc": "N=16 H=4 d=128 conv 4 gate bf16, fp32 state, seed 0", "bar": "5e-3 x RMS",
+                      "want": [o, S]}
+    return refs
 
 
 def cpu_value(tp, td, prefill_tokens, decode_seqs):
@@ -556,8 +757,10 @@ def main():
     dev = torch.device("cuda", local)
     if world > 1:
         torch.distributed.init_process_group("nccl", device_id=dev)
-    # the CPU baseline runs before any CUDA work of the timed arm, on rank 0 at N=1 only
-    cpu = None
+    # the CPU baseline leg runs before any CUDA work of the timed arm, on rank 0 at N=1 only: the
+    # oracle (FP64) and the FP32 per-token loop timed on a sample of the step, and the oracle's
+    # results on the small parity cases
+    cpu = cpu32 = refs = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         tok, seqs = args.cpu_sample_tokens, 64
         tp, td, th = cpu_oracle_sample(tok, seqs)
@@ -566,8 +769,18 @@ def main():
                "sample": f"oracle fused mixer on the first {tok} of {PREFILL['T']} tokens (all 32 heads, "
                          f"{tp:.1f} s) + decode on {seqs} of {DECODE['N']} sequences ({td:.1f} s), "
                          f"scaled to the full step"}
+        t32, th32 = cpu_f32_sample(tok)
+        cpu32 = {"value": PREFILL["T"] / (t32 * PREFILL["T"] / tok), "unit": "tokens/s", "cores": th32,
+                 "kind": "CPU baseline: FP32 per-token loop, the oracle's threading",
+                 "sample": f"fused mixer prefill on the first {tok} of {PREFILL['T']} tokens (all 32 heads, "
+                           f"{t32:.1f} s), scaled to the full prefill; prefill tokens/s"}
+        refs = parity_refs()
     res = run_ours(args, rank, world, dev, torch)
     res["cpu_baseline"] = cpu
+    res["cpu_baseline_f32"] = cpu32
+    if refs is not None:
+        import hybrid_linear_attention_rule_gb300 as K
+        res["parity"] = run_parity(K, torch, refs)
     if rank == 0:
         print(json.dumps(res))
     if world > 1:

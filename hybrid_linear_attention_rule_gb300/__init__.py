@@ -22,7 +22,8 @@ import torch
 __all__ = ["K3KDAError", "load_library", "library_path", "F32", "BF16", "L2_EPS",
            "k3kda_version", "k3kda_status_string", "k3kda_launch_count", "k3kda_short_conv",
            "k3kda_prefill_workspace_size", "k3kda_prefill_workspace_min", "k3kda_prefill", "k3kda_prefill_slots",
-           "k3kda_decode_step_slots", "k3kda_prefill_noalloc", "k3kda_workspace_status",
+           "k3kda_decode_step_slots", "k3kda_prefill_noalloc", "k3kda_prefill_noalloc_status",
+           "k3kda_decode_status", "k3kda_workspace_status",
            "k3kda_backward_workspace_size", "k3kda_backward", "backward",
            "k3kda_decode_step", "prefill", "decode_step", "short_conv",
            "k3mla_decode_workspace_size", "k3mla_decode_step", "k3mla_decode_step_slots", "mla_decode_step"]
@@ -81,6 +82,13 @@ def load_library(build_if_missing: bool = True):
         lib.k3kda_prefill_noalloc.restype = I
         lib.k3kda_workspace_status.argtypes = [P, P]
         lib.k3kda_workspace_status.restype = I
+        lib.k3kda_prefill_noalloc_status.argtypes = [P]
+        lib.k3kda_prefill_noalloc_status.restype = I
+        lib.k3kda_decode_status.argtypes = [P]
+        lib.k3kda_decode_status.restype = I
+        # internal test hook (not in the public header): see k3kda_test_arm_wait_timeout in api.cu
+        lib.k3kda_test_arm_wait_timeout.argtypes = [I, ctypes.c_uint]
+        lib.k3kda_test_arm_wait_timeout.restype = I
         lib.k3kda_decode_step.argtypes = [P, P, P, I, P, P, P, P, P, P, I, I, I, I, I, F, I, P, I, P]
         lib.k3kda_decode_step.restype = I
         lib.k3kda_prefill_slots.argtypes = [P, P, P, I, P, P, P, P, P, I, P, P, I, I, I, I, I, I, F, I, P, P,
@@ -293,6 +301,14 @@ def k3kda_prefill_noalloc(q, k, v, g, beta, initial_state, cu_seqlens, cu_seqlen
 
 def k3kda_workspace_status(workspace, stream=None) -> int:
     return int(load_library().k3kda_workspace_status(_ptr(workspace), _stream(stream)))
+
+
+def k3kda_prefill_noalloc_status(stream=None) -> int:
+    return int(load_library().k3kda_prefill_noalloc_status(_stream(stream)))
+
+
+def k3kda_decode_status(stream=None) -> int:
+    return int(load_library().k3kda_decode_status(_stream(stream)))
 
 
 def k3kda_decode_step(q, k, v, g, beta, gate, conv_weight, conv_state, state, N, H, dk, dv, W, scale,

@@ -71,9 +71,26 @@ size_t conv_buffer_bytes(int T, int H, int dk, int dv) {
 
 void k3kda::count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
+namespace {
+std::atomic<unsigned> g_test_timeout[kTestKinds];
+}  // namespace
+
+unsigned k3kda::take_test_timeout(int which) {
+    return which >= 0 && which < kTestKinds ? g_test_timeout[which].exchange(0u) : 0u;
+}
+
 extern "C" {
 
 long long k3kda_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+// Test hook (see TestTimeout in common.cuh): which = 0 the two-pass prefill's chunk scan, 1 the
+// single-pass prefill, 2 the decode step; tries = how many times the starved wait polls (0 disarms).
+// Only for tests on a working GPU: the armed call's outputs are invalid by design.
+int k3kda_test_arm_wait_timeout(int which, unsigned tries) {
+    if (which < 0 || which >= kTestKinds) return K3KDA_ERR_INVALID_ARG;
+    g_test_timeout[which].store(tries);
+    return K3KDA_OK;
+}
 
 
 const char *k3kda_status_string(int status) {
@@ -286,6 +303,13 @@ int k3kda_workspace_status(void *workspace, void *stream) {
     if (st != K3KDA_OK) return st;
     st = cuda_status(cudaStreamSynchronize(s));
     return st != K3KDA_OK ? st : K3KDA_ERR_TIMEOUT;
+}
+
+int k3kda_decode_status(void *stream) {
+    unsigned word = 0;
+    const int st = cuda_status(decode_status(static_cast<cudaStream_t>(stream), &word));
+    if (st != K3KDA_OK) return st;
+    return word == 0 ? K3KDA_OK : K3KDA_ERR_TIMEOUT;
 }
 
 static int decode_impl(const void *q, const void *k, const void *v, int in_dtype, const float *g,

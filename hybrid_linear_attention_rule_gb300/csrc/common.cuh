@@ -70,6 +70,14 @@ inline cudaError_t smem_attr_once(const void *func, int bytes, std::atomic<uint6
 // Counts every kernel this library launches (reported by k3kda_launch_count).
 void count_launch();
 
+// Test hook for the bounded in-kernel waits.  k3kda_test_arm_wait_timeout (exported for the tests,
+// not part of the public header) arms one of these; the next launch of that kernel takes the armed
+// count (and disarms it), and its CTA 0 then issues none of the copies its first bounded wait waits
+// for and gives up that wait after the armed number of tries, so the kernel's timeout path runs
+// (status recorded, nothing left in flight, TMEM freed) on a GPU that is working normally.
+enum TestTimeout { kTestScan = 0, kTestSinglePass = 1, kTestDecode = 2, kTestKinds = 3 };
+unsigned take_test_timeout(int which);
+
 // ---- launchers (defined in the kernel files, called by the C ABI layer) ----
 
 cudaError_t launch_short_conv(const void *x, int x_bf16, const float *w, const float *cs_in,
@@ -88,6 +96,9 @@ cudaError_t launch_conv_state_update_strided(const void *x, int64_t x_stride, in
                                              int Dc, int W, cudaStream_t s, const int32_t *slot = nullptr,
                                              int num_slots = 0);
 
+// Read and clear this device's decode status word (0, or nonzero after a decode kernel gave up a
+// bounded wait); synchronises s.
+cudaError_t decode_status(cudaStream_t s, unsigned *word);
 cudaError_t launch_decode(const void *q, const void *k, const void *v, int in_bf16, const float *g,
                           const float *beta, const void *gate, const float *conv_w, float *conv_state,
                           float *state, int N, int H, int dk, int dv, int W, float scale, int l2,
@@ -111,6 +122,7 @@ struct PrefillArgs {
     unsigned int *status;    // device status word (workspace offset 0)
     const int32_t *slot;     // [N] pool slot of each sequence for S0 / Sfin / conv state, or null (slot n)
     int num_slots;
+    unsigned test_limit;     // 0; else the armed test hook's tries (see TestTimeout)
 };
 
 cudaError_t launch_prefill_f32(const PrefillArgs &a, cudaStream_t s);

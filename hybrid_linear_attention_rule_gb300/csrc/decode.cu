@@ -66,10 +66,14 @@ struct DecodeArgs {
     int l2;
     void *out;
     int out_bf16;
-    unsigned int *status;   // may be null
     const int32_t *slot;    // [N] state / conv-state row of each sequence, or null (row n)
     int num_slots;
+    unsigned test_limit;    // 0; else the armed test hook's tries (see TestTimeout)
 };
+
+// This device's decode status word: a decode kernel that gives up a bounded wait ORs 2 into it
+// (its outputs are then invalid); k3kda_decode_status reads and clears it.
+__device__ unsigned int g_decode_status;
 
 __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(DecodeArgs a) {
     extern __shared__ uint8_t smraw[];
@@ -100,7 +104,8 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(DecodeArgs a) {
 
     if (warp == kConsumerWarps) {
         // ---------------- producer ----------------
-        if (lane == 0) {
+        // test hook: CTA 0 stages nothing, so its consumers' first wait runs out
+        if (lane == 0 && !(a.test_limit != 0 && blockIdx.x == 0)) {
             // m counts the items actually staged: an item whose slot is out of range is skipped by
             // the producer and the consumers alike, so both sides agree on stages and parities
             for (int kk = 0, m = 0;; ++kk) {
@@ -112,7 +117,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(DecodeArgs a) {
                 const int s = m & 1;
                 const uint32_t P = smem_u32(sm + s * kStageBytes);
                 if (m >= kStages && !mbar_wait_bounded(empty0 + 8 * s, ((m - kStages) >> 1) & 1, kWaitLimit)) {
-                    if (a.status) atomicOr(a.status, 2u);
+                    atomicOr(&g_decode_status, 2u);
                     break;
                 }
                 ++m;
@@ -147,6 +152,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(DecodeArgs a) {
 
     // ---------------- consumers (256 threads, named barrier 1) ----------------
     const bool colok = 4 * lane < dv;
+    uint32_t tlim = a.test_limit != 0 && blockIdx.x == 0 ? a.test_limit : kWaitLimit;
     for (int kk = 0, m = 0;; ++kk) {
         const int it = blockIdx.x + kk * gridDim.x;
         if (it >= NH) break;
@@ -160,10 +166,11 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(DecodeArgs a) {
         uint8_t *P = sm + s * kStageBytes;
         const size_t sit = (size_t)sn * H + h;
         const float bval = tid < dv ? __ldg(a.beta + it) : 0.f;   // in flight while the stage lands
-        if (tid == 0 && !mbar_wait_bounded(full0 + 8 * s, (m >> 1) & 1, kWaitLimit)) {
+        if (tid == 0 && !mbar_wait_bounded(full0 + 8 * s, (m >> 1) & 1, tlim)) {
             *sflag = 1;
-            if (a.status) atomicOr(a.status, 2u);
+            atomicOr(&g_decode_status, 2u);
         }
+        tlim = kWaitLimit;
         ++m;
         named_bar(1, kConsumers);
         if (*sflag) break;
@@ -305,12 +312,21 @@ cudaError_t launch_decode(const void *q, const void *k, const void *v, int in_bf
     if (e == cudaSuccess) e = smem_attr_once((const void *)decode_kernel, (int)kSmemBytes, g_decode_attr);
     if (e != cudaSuccess) return e;
     DecodeArgs a{q, k, v, in_bf16, g, beta, gate, conv_w, conv_state, state, N, H, dk, dv, conv_w ? W : 0, scale,
-                 l2, out, out_bf16, nullptr, slot, num_slots};
+                 l2, out, out_bf16, slot, num_slots, take_test_timeout(kTestDecode)};
     const long long items = (long long)N * H;
     const int grid = (int)(items < sms ? items : sms);
     decode_kernel<<<grid, kDecThreads, kSmemBytes, s>>>(a);
     count_launch();
     return cudaGetLastError();
+}
+
+cudaError_t decode_status(cudaStream_t s, unsigned *word) {
+    cudaError_t e = cudaMemcpyFromSymbolAsync(word, g_decode_status, sizeof(unsigned), 0, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess || *word == 0) return e;
+    const unsigned zero = 0;
+    e = cudaMemcpyToSymbolAsync(g_decode_status, &zero, sizeof(unsigned), 0, cudaMemcpyHostToDevice, s);
+    return e == cudaSuccess ? cudaStreamSynchronize(s) : e;
 }
 
 }  // namespace k3kda

@@ -9,8 +9,6 @@
 // conv staging buffer) lives in a fixed-size array that the library itself
 // reserves in device memory; every GPU that loads the library holds that
 // array until the process exits.
-#include <mutex>
-
 #include "common.cuh"
 
 namespace {
@@ -19,9 +17,15 @@ namespace {
 constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_noalloc_mu;
-void *g_noalloc_ptr[kMaxDevices] = {};
+// The device address of the array on the current device.  In host code the array's name is only a
+// host-side stand-in; the runtime resolves it per device and context.  Looked up on every call
+// (cheap, allocates nothing), so that a device reset or a new context never leaves a stale address.
+int scratch_address(void **out) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return K3KDA_ERR_CUDA;
+    *out = p;
+    return K3KDA_OK;
+}
 
 }  // namespace
 
@@ -42,24 +46,24 @@ int k3kda_prefill_noalloc(const void *q, const void *k, const void *v, int in_dt
     // Reject work whose scratch would not fit before touching the device.
     const size_t need = k3kda_prefill_workspace_min(N, T, H, dk, dv, chunk, in_dtype, conv != nullptr);
     if (need > kNoAllocScratchBytes) return K3KDA_ERR_WORKSPACE;
-    // Once per device, with that device current: find the device address of the array.
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return K3KDA_ERR_CUDA;
     void *scratch = nullptr;
-    {
-        std::lock_guard<std::mutex> lock(g_noalloc_mu);
-        if (g_noalloc_ptr[dev] == nullptr) {
-            void *p = nullptr;
-            if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return K3KDA_ERR_CUDA;
-            g_noalloc_ptr[dev] = p;
-        }
-        scratch = g_noalloc_ptr[dev];
-    }
+    if (int st = scratch_address(&scratch)) return st;
     // The status word must start at zero; the rest is written before it is read.
     if (cudaMemsetAsync(scratch, 0, 256, static_cast<cudaStream_t>(stream)) != cudaSuccess) return K3KDA_ERR_CUDA;
     return k3kda_prefill(q, k, v, in_dtype, g, beta, initial_state, cu_seqlens, cu_seqlens_host, N, T, H, dk, dv,
                          chunk, scale, use_qk_l2norm, conv, gate, out, out_dtype, final_state, scratch,
                          kNoAllocScratchBytes, stream);
+}
+
+// The status word of the library-held scratch on the current device: synchronise `stream`, read
+// and clear it (K3KDA_OK, or K3KDA_ERR_TIMEOUT when a kernel of the last k3kda_prefill_noalloc
+// call on this device gave up a bounded wait).
+int k3kda_workspace_status(void *workspace, void *stream);
+
+int k3kda_prefill_noalloc_status(void *stream) {
+    void *scratch = nullptr;
+    if (int st = scratch_address(&scratch)) return st;
+    return k3kda_workspace_status(scratch, stream);
 }
 
 }  // extern "C"

@@ -548,9 +548,12 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_scan_kernel(const __gri
     // thread 0's view of the outstanding asynchronous operations
     uint32_t aph = 0, kph = 0, xph0 = 0, xph1 = 0, gph0 = 0, gph1 = 0;
     bool pend_a = false, pend_k = false, pend_x0 = false, pend_x1 = false, pend_g0 = false, pend_g1 = false;
-    auto wait_on = [&](uint32_t bar, uint32_t &ph, bool &pend) -> bool {
+    // test hook: CTA 0 issues no copy of its first [W; Qh] tile and gives up that wait early
+    const bool tskip = a.test_limit != 0 && blockIdx.x == 0 && c_begin < c_end;
+    uint32_t xlim = tskip ? a.test_limit : kWaitLimit;
+    auto wait_on = [&](uint32_t bar, uint32_t &ph, bool &pend, uint32_t lim = kWaitLimit) -> bool {
         if (!pend) return true;
-        if (!mbar_wait_bounded(bar, ph, kWaitLimit)) {
+        if (!mbar_wait_bounded(bar, ph, lim)) {
             *sflag = 1;
             atomicOr(a.status, 1u);
             return false;
@@ -568,7 +571,11 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_scan_kernel(const __gri
         if (c & 1) load(mb_x1, Q_X1, REC_X, c, 65536, pend_x1);
         else load(mb_x0, REC_X, REC_X, c, 65536, pend_x0);
     };
-    auto wait_x = [&](int c) { return (c & 1) ? wait_on(mb_x1, xph1, pend_x1) : wait_on(mb_x0, xph0, pend_x0); };
+    auto wait_x = [&](int c) {
+        const uint32_t lim = xlim;
+        xlim = kWaitLimit;
+        return (c & 1) ? wait_on(mb_x1, xph1, pend_x1, lim) : wait_on(mb_x0, xph0, pend_x0, lim);
+    };
     auto load_gate = [&](int c) {                    // chunk c's gate rows -> buffer c & 1 (thread 0)
         const uint32_t bar = (c & 1) ? mb_g1 : mb_g0;
         mbar_arrive_expect_tx(bar, (uint32_t)A.box_rows * kD * 2);
@@ -641,7 +648,9 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_scan_kernel(const __gri
     if (c_begin < c_end) {
         const int c = c_begin;
         if (tid == 0) {
-            load_x(c);
+            if (!tskip) load_x(c);
+            else if (c & 1) pend_x1 = true;
+            else pend_x0 = true;
             load(mb_k, REC_B, REC_B, c, 49152, pend_k);     // [Aqk^T | Kb] hi, lo
             for (int d = 1; d <= 2 && c + d < c_end; ++d) prefetch_chunk(c + d);
             if (gated) load_gate(c);
@@ -845,6 +854,10 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_scan_kernel(const __gri
     }
     if (tid == 0) {
         bulk_wait_all();                                 // output tiles written
+        if (tskip) {                                     // the starved tile was never requested
+            if (c_begin & 1) pend_x1 = false;
+            else pend_x0 = false;
+        }
         // after a failure, let what is still in flight land before the CTA exits
         if (pend_a) mbar_wait_bounded(mb_a, aph, kWaitLimit);
         if (pend_x0) mbar_wait_bounded(mb_x0, xph0, kWaitLimit);
@@ -997,6 +1010,7 @@ cudaError_t launch_prefill_tc_split(const PrefillArgs &p, const float *conv_w, f
     auto scan = [&](int q_lo, int q_hi, cudaStream_t st) -> cudaError_t {
         S.q_lo = q_lo;
         S.q_hi = q_hi;
+        S.p.test_limit = q_lo == 0 ? take_test_timeout(kTestScan) : 0u;
         kda_chunk_scan_kernel<<<scan_grid, kThreads, kScanSmemBytes, st>>>(S);
         count_launch();
         return cudaGetLastError();

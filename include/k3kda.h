@@ -149,8 +149,9 @@ size_t k3kda_prefill_workspace_min(int N, int T, int H, int dk, int dv, int chun
  *
  *   q, k           [T, H, dk]      in_dtype   (pre-conv when conv != NULL)
  *   v              [T, H, dv]      in_dtype
- *   g              [T, H, dk]      FP32 log-decay (alpha = exp(g); g <= 0 is
- *                                  the supported range)
+ *   g              [T, H, dk]      FP32 log-decay (alpha = exp(g); any g <= 0,
+ *                                  however strong the decay: no exponent the
+ *                                  kernels form can leave the fp32 range)
  *   beta           [T, H]          FP32
  *   initial_state  [N, H, dk, dv]  FP32 or NULL (zeros)
  *   cu_seqlens     [N+1]           int32 device, cu[0] = 0, non-decreasing,
@@ -250,13 +251,15 @@ int k3kda_decode_step_slots(const void *q, const void *k, const void *v, int in_
  *     K3KDA_ERR_WORKSPACE before anything is enqueued.  Tensor-core shapes
  *     whose chunk records fit in the array run the two-pass path, larger ones
  *     the single-pass kernel.
- *   - The first call on each device looks up the array's device address with
- *     that device current; make that first call before any stream capture.
+ *   - Every call looks up the array's device address on the current device
+ *     (the runtime resolves it per device and context; nothing is cached, so
+ *     a device reset leaves no stale address).  Make the first call on a
+ *     device before any stream capture.
  *   - All calls on a device share the one array and it keeps the last call's
  *     contents.  Each call clears the status word on `stream` before its
  *     kernels; calls whose work overlaps on the GPU (different streams, no
  *     ordering between them) race on the array.  A timed-out in-kernel wait is
- *     recorded in the library's array and is not reported by this call.
+ *     recorded in the array's status word: k3kda_prefill_noalloc_status reads it.
  */
 #define K3KDA_NOALLOC_SCRATCH_BYTES (16u << 20)
 int k3kda_prefill_noalloc(const void *q, const void *k, const void *v, int in_dtype,
@@ -265,6 +268,13 @@ int k3kda_prefill_noalloc(const void *q, const void *k, const void *v, int in_dt
                           int N, int T, int H, int dk, int dv, int chunk, float scale,
                           int use_qk_l2norm, const k3kda_conv_args *conv, const void *gate,
                           void *out, int out_dtype, float *final_state, void *stream);
+
+/* The status of the last k3kda_prefill_noalloc call on the current device:
+ * synchronise `stream`, read and clear the status word of the library-held
+ * array.  K3KDA_OK, or K3KDA_ERR_TIMEOUT if one of its kernels gave up a
+ * bounded wait (its outputs are then invalid); K3KDA_ERR_CUDA on a runtime
+ * error.  Allocates nothing.  The pages have no counterpart. */
+int k3kda_prefill_noalloc_status(void *stream);
 
 /*
  * k3kda_decode_step -- one new token for each of N independent sequences
@@ -284,13 +294,22 @@ int k3kda_prefill_noalloc(const void *q, const void *k, const void *v, int in_dt
  *   conv_weight [2*H*dk + H*dv, W] FP32 or NULL;  conv_state [N, W-1, 2*H*dk + H*dv]
  *   state       [N, H, dk, dv] FP32, read-modify-write in place
  *   out         [N, H, dv] out_dtype
- * Errors: INVALID_ARG, UNSUPPORTED, ALIGNMENT, CUDA.
+ * Errors: INVALID_ARG, UNSUPPORTED, ALIGNMENT, CUDA.  The decode takes no
+ * workspace: a bounded in-kernel wait that gives up is recorded in a status
+ * word the library keeps per device, which k3kda_decode_status reads.
  */
 int k3kda_decode_step(const void *q, const void *k, const void *v, int in_dtype,
                       const float *g, const float *beta, const void *gate,
                       const float *conv_weight, float *conv_state, float *state,
                       int N, int H, int dk, int dv, int W, float scale, int use_qk_l2norm,
                       void *out, int out_dtype, void *stream);
+
+/* Synchronise `stream`, read and clear the current device's decode status word:
+ * K3KDA_OK, or K3KDA_ERR_TIMEOUT if a k3kda_decode_step / _slots kernel on
+ * this device gave up a bounded wait since the last read (its outputs are then
+ * invalid); K3KDA_ERR_CUDA on a runtime error.  Shared by every decode call on
+ * the device (failure detection, no counterpart on the pages). */
+int k3kda_decode_status(void *stream);
 
 /* ---- backward of the recurrence ----
  * Reverse-mode gradients of the ungated KDA recurrence (the one k3kda_prefill runs, without

@@ -276,3 +276,49 @@ def decode_step(q, k, v, g, beta, state, gate=None, conv_w=None, conv_state=None
                                       _ptr(conv_w), W, _ptr(cs), _ptr(st), N, H, dk, dv, float(scale),
                                       int(bool(use_qk_l2norm)), float(eps), _ptr(o)), "decode_step")
     return o, st, cs
+
+
+# ---- the FP32 CPU baseline (timed by the benchmark beside the oracle; never a reference) ----
+
+_F32_SRC = os.path.join(_HERE, "cpu_f32.c")
+_F32_PATH = os.path.join(_BUILD, "libkda_cpu_f32.so")
+_f32_lib = None
+
+
+def build_cpu_f32(force: bool = False) -> str:
+    """Compile the FP32 CPU baseline (cpu_f32.c) like the oracle; return the .so path."""
+    return build(force=force, out_path=_F32_PATH, src=_F32_SRC)
+
+
+def load_cpu_f32():
+    global _f32_lib
+    with _lock:
+        if _f32_lib is None:
+            lib = ctypes.CDLL(build_cpu_f32())
+            P, I, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+            lib.kda_cpu_f32_num_threads.restype = I
+            lib.kda_cpu_f32_mixer.argtypes = [P, P, P, P, P, P, P, I, I, I, I, F, F, P, P]
+            lib.kda_cpu_f32_mixer.restype = I
+            _f32_lib = lib
+    return _f32_lib
+
+
+def cpu_f32_threads() -> int:
+    return int(load_cpu_f32().kda_cpu_f32_num_threads())
+
+
+def cpu_f32_mixer(q, k, v, g, beta, gate=None, conv_w=None, scale=None, eps=KDA_L2_EPS):
+    """The mixer of one sequence in FP32 (conv width conv_w.shape[1] + SiLU, q/k L2 norm, the
+    per-token recurrence from a zero state, gate): q, k, v, g, gate [T, H, d], beta [T, H],
+    conv_w [3 H d, W].  Returns (o [T, H, d], final state [1, H, d, d]), float32."""
+    lib = load_cpu_f32()
+    f = lambda a: None if a is None else np.ascontiguousarray(np.asarray(a, dtype=np.float32))
+    q, k, v, g, beta, gate, conv_w = (f(x) for x in (q, k, v, g, beta, gate, conv_w))
+    T, H, d = q.shape
+    W = 0 if conv_w is None else conv_w.shape[1]
+    o = np.empty((T, H, d), np.float32)
+    Sf = np.empty((1, H, d, d), np.float32)
+    _check(lib.kda_cpu_f32_mixer(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(gate), _ptr(conv_w), W, T,
+                                 H, d, float(d ** -0.5 if scale is None else scale), float(eps), _ptr(o), _ptr(Sf)),
+           "cpu_f32_mixer")
+    return o, Sf

@@ -22,6 +22,16 @@ def test_prefill_bytes_and_flops_per_token_head():
     assert abs(by - 3.769e9) < 1e6                        # the 3.77 GB of the fused-mixer call
 
 
+def test_chunked_and_varlen_prefill_bytes():
+    """No conv, no gate: 1540 B per (token, head) and the fp32 states (406 MB for T=8192, H=32)."""
+    by, fl = bench.prefill_work(8192, 32, 128, 64, 0, gate=False)
+    assert by == 8192 * 32 * 1540 + 32 * 128 * 128 * 4
+    assert abs(by - 406e6) < 1e6
+    assert fl == 8192 * 32 * (10 * 64 * 128 + 6 * 128 * 128)
+    by3, _ = bench.prefill_work(135937, 32, 128, 64, 0, N=16, gate=False, initial_state=True)
+    assert by3 == 135937 * 32 * 1540 + 2 * 16 * 32 * 128 * 128 * 4
+
+
 def test_decode_bytes_per_sequence_head():
     N, H, d, W = 256, 32, 128, 4
     by, _ = bench.decode_work(N, H, d, W)

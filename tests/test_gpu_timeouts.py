@@ -1,0 +1,84 @@
+"""Failure detection on the GPU: a bounded in-kernel wait that runs out is reported, and the library
+keeps working afterwards.
+
+Every wait of the kernels on an mbarrier (a bulk copy or an MMA landing) polls a bounded number of
+times and, when that runs out, records K3KDA_ERR_TIMEOUT, lets whatever it issued land, frees its
+tensor memory and returns.  The internal hook k3kda_test_arm_wait_timeout (exported for these tests,
+not part of the public header) makes the next launch of one kernel starve its first wait on a
+working GPU: CTA 0 requests none of the copies that wait is for and gives up after a few hundred
+polls.  Nothing faults and nothing hangs: the other copies it issued land before it exits.  Each
+test checks that the status reader reports the timeout once, then that a normal call on the same
+workspace reports K3KDA_OK and matches the oracle.
+"""
+import numpy as np
+import pytest
+import torch
+
+import hybrid_linear_attention_rule_gb300 as K
+import kda_inputs as KI
+import oracle as O
+from parity_utils import assert_close, case_to_device, oracle_prefill, to_np
+
+pytestmark = pytest.mark.gpu
+
+SCAN, SINGLE_PASS, DECODE = 0, 1, 2
+TIMEOUT = -6
+TRIES = 256
+
+
+def _arm(which):
+    assert K.load_library().k3kda_test_arm_wait_timeout(which, TRIES) == 0
+
+
+def _prefill(c, d, ws, out):
+    T, H, dk, dv, N = c.T, c.H, c.dk, c.dv, c.N
+    fs = torch.empty((N, H, dk, dv), device="cuda")
+    K.k3kda_prefill(d["q"], d["k"], d["v"], d["g"], d["beta"], d["S0"], d["cu"].cuda(), d["cu"], N, T, H, dk, dv,
+                    c.chunk, c.scale, True, None, None, 0, d["gate"], out, fs, ws)
+    return fs
+
+
+@pytest.mark.parametrize("which", [SCAN, SINGLE_PASS], ids=["two_pass_scan", "single_pass"])
+def test_prefill_wait_runs_out_then_recovers(which):
+    c = KI.prefill_case("timeout", [200, 90], 2, 128, 128, 64, "bf16", seed=80, s0_std=0.02, gate=True)
+    d = case_to_device(c)
+    size = (K.k3kda_prefill_workspace_size if which == SCAN else K.k3kda_prefill_workspace_min)(
+        c.N, c.T, c.H, 128, 128, 64, K.BF16, False)
+    ws = torch.zeros(size, dtype=torch.uint8, device="cuda")
+    out = torch.zeros((c.T, c.H, 128), device="cuda")
+    _arm(which)
+    _prefill(c, d, ws, out)
+    assert K.k3kda_workspace_status(ws) == TIMEOUT
+    assert K.k3kda_workspace_status(ws) == 0                  # read once, then cleared
+    fs = _prefill(c, d, ws, out)
+    assert K.k3kda_workspace_status(ws) == 0
+    ro, rs, _ = oracle_prefill(c)
+    assert_close(to_np(out), ro, False, "out after a timed-out call")
+    assert_close(to_np(fs), rs, False, "final state after a timed-out call")
+
+
+def test_decode_wait_runs_out_then_recovers():
+    dc = KI.decode_case(seed=81, N=2, H=2, d=128)
+    dev = lambda x, bf=False: torch.from_numpy(np.ascontiguousarray(x)).to(torch.bfloat16 if bf else torch.float32).cuda()
+    args = lambda st, cs: (dev(dc.q, 1), dev(dc.k, 1), dev(dc.v, 1), dev(dc.g), dev(dc.beta), st)
+    assert K.k3kda_decode_status() == 0
+    _arm(DECODE)
+    st, cs = dev(dc.state), dev(dc.conv_state)
+    K.decode_step(*args(st, cs), gate=dev(dc.gate, 1), conv_weight=dev(dc.conv_w), conv_state=cs,
+                  out_dtype=torch.float32)
+    assert K.k3kda_decode_status() == TIMEOUT
+    assert K.k3kda_decode_status() == 0
+    st, cs = dev(dc.state), dev(dc.conv_state)
+    o = K.decode_step(*args(st, cs), gate=dev(dc.gate, 1), conv_weight=dev(dc.conv_w), conv_state=cs,
+                      out_dtype=torch.float32)
+    assert K.k3kda_decode_status() == 0
+    ro, rs, rcs = O.decode_step(dc.q, dc.k, dc.v, dc.g, dc.beta, dc.state, gate=dc.gate, conv_w=dc.conv_w,
+                                conv_state=dc.conv_state)
+    assert_close(to_np(o), ro, False, "decode out after a timed-out call")
+    assert_close(to_np(st), rs, False, "decode state after a timed-out call")
+    assert np.array_equal(to_np(cs), rcs)
+
+
+def test_disarmed_hook_changes_nothing():
+    assert K.load_library().k3kda_test_arm_wait_timeout(SCAN, 0) == 0
+    assert K.load_library().k3kda_test_arm_wait_timeout(7, 1) == -1
