@@ -186,6 +186,7 @@ static int prefill_impl(const void *q, const void *k, const void *v, int in_dtyp
     a.status = status;
     a.slot = slot;
     a.num_slots = num_slots;
+    a.cu_host = cu_seqlens_host;
 
     if (tc_prefill_supported(a.in_bf16, dk, dv, chunk)) {
         const float *cw = conv ? conv->weight : nullptr;

@@ -123,6 +123,7 @@ struct PrefillArgs {
     const int32_t *slot;     // [N] pool slot of each sequence for S0 / Sfin / conv state, or null (slot n)
     int num_slots;
     unsigned test_limit;     // 0; else the armed test hook's tries (see TestTimeout)
+    const int32_t *cu_host;  // host copy of cu (validated), or null: read on the host only, to plan segments
 };
 
 cudaError_t launch_prefill_f32(const PrefillArgs &a, cudaStream_t s);

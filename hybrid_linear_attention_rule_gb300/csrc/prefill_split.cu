@@ -59,15 +59,20 @@ __device__ __forceinline__ uint32_t u_off(uint32_t j, uint32_t i) {
     return (i >> 2) * 2048u + j * 16u + (i & 3u) * 4u;
 }
 
-// ============================ chunk offsets ============================
-// off[n] = number of 64-token chunks in sequences 0 .. n-1 (off[0] = 0, off[N] = total), capped
-// at qmax, the number of records the workspace holds: a malformed device cu_seqlens (overlapping
+// ============================ segment offsets ============================
+// A call runs in segments: segment k covers the local chunks [k per, (k + 1) per) of every
+// sequence (one segment of unbounded length when the call is not segmented).  Block k writes the
+// record table of segment k, off = tables + k (N + 1): off[n] = number of records (chunks) of
+// sequences 0 .. n-1 in the segment (off[0] = 0, off[N] = the segment's total), capped at qmax,
+// the number of records a segment's buffer holds: a malformed device cu_seqlens (overlapping
 // sequences) then loses chunks instead of sending either pass past the workspace.
-__global__ void __launch_bounds__(1024) kda_chunk_offsets_kernel(const int32_t *cu, int N, int T, int qmax,
-                                                                 int32_t *off) {
+__global__ void __launch_bounds__(1024) kda_segment_offsets_kernel(const int32_t *cu, int N, int T, int per, int qmax,
+                                                                   int32_t *tables) {
     __shared__ int32_t part[32];
     __shared__ int32_t carry;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const long long lo = (long long)blockIdx.x * per;
+    int32_t *off = tables + (size_t)blockIdx.x * (N + 1);
     if (tid == 0) { carry = 0; off[0] = 0; }
     __syncthreads();
     for (int base = 0; base < N; base += 1024) {
@@ -76,7 +81,8 @@ __global__ void __launch_bounds__(1024) kda_chunk_offsets_kernel(const int32_t *
         if (n < N) {
             int tb, te;
             seq_bounds(cu, n, T, tb, te);
-            x = (te - tb + kC - 1) / kC;
+            const long long nq = (te - tb + kC - 1) / kC;
+            x = (int)(nq <= lo ? 0 : (nq - lo < per ? nq - lo : per));
         }
 #pragma unroll
         for (int d = 1; d < 32; d <<= 1) {
@@ -111,9 +117,9 @@ struct PrepArgs {
     const float *conv_state;  // [N, W-1, 3*H*128] initial conv state or null (read only here)
     int W;
     int box_rows;
-    const int32_t *chunk_off; // [N + 1]
-    uint8_t *rec;             // records of this launch's chunks: [(q - q_lo) * H + h]
-    int q_lo, q_hi;           // global chunk range of this launch (items q * H + h)
+    const int32_t *seg_off;   // [N + 1] this segment's record table (record r of sequence n: seg_off[n] + r)
+    int seg_lo;               // first local chunk of the segment
+    uint8_t *rec;             // the segment's records: [record * H + h]
 };
 
 constexpr uint32_t kPrepTmemCols = 512;
@@ -173,24 +179,24 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_prep_kernel(const __gri
     // Items in head-major order (head, chunk), each CTA taking a contiguous run of them: a CTA's
     // consecutive items are then mostly consecutive chunks of one head, whose conv history is the
     // previous chunk's last staged rows and whose conv weights are already loaded.
-    const int nq = max(0, min(A.chunk_off[N], A.q_hi) - A.q_lo);   // chunks of this launch
+    const int nq = A.seg_off[N];                         // records (chunks) of this segment
     const long long total = (long long)nq * H;
     const int m_lo = (int)(total * blockIdx.x / gridDim.x);
     const int m_hi = (int)(total * (blockIdx.x + 1) / gridDim.x);
-    struct Item { int h, qc, n, tb, te, cs, qend; };   // qend: one past the sequence's last chunk
+    struct Item { int h, qc, n, tb, te, cs, qend; };   // qc: record; qend: one past the sequence's last record
     auto locate = [&](int m) {
         Item x;
         x.h = m / nq;
-        x.qc = A.q_lo + (m - x.h * nq);
+        x.qc = m - x.h * nq;
         int lo = 0, hi = N;                              // sequence n with off[n] <= qc < off[n + 1]
         while (hi - lo > 1) {
             const int mid = (lo + hi) >> 1;
-            if (A.chunk_off[mid] <= x.qc) lo = mid; else hi = mid;
+            if (A.seg_off[mid] <= x.qc) lo = mid; else hi = mid;
         }
         x.n = lo;
         seq_bounds(a.cu, x.n, a.T, x.tb, x.te);
-        x.cs = x.tb + (x.qc - A.chunk_off[x.n]) * kC;
-        x.qend = A.chunk_off[x.n + 1];
+        x.cs = x.tb + (A.seg_lo + x.qc - A.seg_off[x.n]) * kC;
+        x.qend = A.seg_off[x.n + 1];
         return x;
     };
     // item m + 1 after item x = item m: the next chunk of the same sequence and head without
@@ -204,7 +210,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_prep_kernel(const __gri
         }
         return locate(m + 1);
     };
-    auto rec_of = [&](const Item &x) { return A.rec + ((size_t)(x.qc - A.q_lo) * H + x.h) * REC_BYTES; };
+    auto rec_of = [&](const Item &x) { return A.rec + ((size_t)x.qc * H + x.h) * REC_BYTES; };
     // conv weights of the item's head and its conv history (pre-conv q, k, v rows of tokens
     // cs-3 .. cs-1 from the inputs, or from the right-aligned initial conv state before the
     // sequence start), by all threads; the prep stages are their only readers
@@ -274,7 +280,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_prep_kernel(const __gri
     }
     for (int m = m_lo; m < m_hi; ++m, x = y, y = m + 1 < m_hi ? advance(y, m) : y) {
         const bool has_next = m + 1 < m_hi;
-        const bool cont = has_next && y.h == x.h && y.qc == x.qc + 1 && y.cs > y.tb;
+        const bool cont = has_next && y.h == x.h && y.n == x.n && y.cs == x.cs + kC;
         const int Lc = min(kC, x.te - x.cs);
         uint8_t *rec = rec_of(x);
         if (tid == 0) {
@@ -420,9 +426,9 @@ struct ScanArgs {
     int box_rows;
     float *conv_state;        // [N, W-1, 3*H*128] advanced at the end, or null
     int W;
-    const int32_t *chunk_off;
-    const uint8_t *rec;       // records of this launch's chunks: [(q - q_lo) * H + h]
-    int q_lo, q_hi;           // global chunk range of this launch
+    const int32_t *seg_off;   // [N + 1] this segment's record table
+    int seg_lo;               // first local chunk of the segment
+    const uint8_t *rec;       // the segment's records: [record * H + h]
     float *carry_S;           // [N*H][128 dv][128 dk] state handed between launches
 };
 
@@ -491,11 +497,12 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_scan_kernel(const __gri
 
     int tb, te;
     seq_bounds(a.cu, n, a.T, tb, te);
-    const int q0 = A.chunk_off[n];
-    const int nq = A.chunk_off[n + 1] - q0;
-    // this launch's chunks of the sequence: [c_begin, c_end); an empty sequence belongs to the first launch
-    const int c_begin = max(0, A.q_lo - q0), c_end = min(nq, A.q_hi - q0);
-    if (c_begin >= c_end && !(nq == 0 && A.q_lo == 0)) return;
+    // this segment's chunks of the sequence: [c_begin, c_end) (local indices; records seg_off[n] ..);
+    // an empty sequence belongs to the first segment
+    const int q0 = A.seg_off[n];
+    const int nq = (te - tb + kC - 1) / kC;
+    const int c_begin = A.seg_lo, c_end = A.seg_lo + (A.seg_off[n + 1] - q0);
+    if (c_begin >= c_end && !(nq == 0 && A.seg_lo == 0)) return;
     const bool first = c_begin == 0, last = c_end == nq;
     const int sn = seq_slot(a.slot, a.num_slots, n);           // state / conv-state row (-1: none)
     const size_t snh = (size_t)(sn < 0 ? 0 : sn) * a.H + h;
@@ -544,7 +551,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_scan_kernel(const __gri
         tmem_wait_st();
     }
 
-    auto rec_of = [&](int c) { return A.rec + ((size_t)(q0 + c - A.q_lo) * H + h) * REC_BYTES; };
+    auto rec_of = [&](int c) { return A.rec + ((size_t)(q0 + c - A.seg_lo) * H + h) * REC_BYTES; };
     // thread 0's view of the outstanding asynchronous operations
     uint32_t aph = 0, kph = 0, xph0 = 0, xph1 = 0, gph0 = 0, gph1 = 0;
     bool pend_a = false, pend_k = false, pend_x0 = false, pend_x1 = false, pend_g0 = false, pend_g1 = false;
@@ -874,31 +881,70 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_scan_kernel(const __gri
 size_t max_chunks(int N, int T) { return ((size_t)T + 63u * (size_t)N) / kC; }
 size_t round256_(size_t b) { return (b + 255) & ~size_t(255); }
 
-// Segmented pipeline: the prep pass of chunk segment s + 1 (caller's stream) overlaps the scan of
-// segment s (a high-priority side stream of the library), ordered by events only; the scan hands
-// its state from one segment's launch to the next through the carry buffer.  Used when the
-// (sequence, head) pairs are few (the scan then leaves most SMs to the prep pass) and long.
-// Segments write their records into a ring of kRing buffers, so the workspace does not grow with
-// T: segment k's prep waits for the scan of segment k - kRing, the last reader of its buffer.
+// Segmented pipeline.  A call runs in segments of `per` local chunks of every sequence: the prep
+// pass of segment k + 1 (caller's stream) overlaps the scan of segment k (a high-priority side
+// stream of the library), ordered by events only, and the scan hands each chain's state from one
+// segment's launch to the next through the carry buffer.  Segments write their records into a ring
+// of buffers, so the workspace does not grow with T: segment k's prep waits for the scan of segment
+// k - ring, the last reader of its buffer.  Three shapes:
+//   one segment  few chunks in all: every record has its own place, prep then scan;
+//   overlap      few (sequence, head) chains (<= 64) with >= 128 chunks: the scan leaves most SMs
+//                to the prep, segments of ~64 chunks whose items fill whole waves of the prep grid,
+//                a ring of three;
+//   bounded      many chains whose records would exceed kRecordBudget: segments as long as a ring
+//                of two within the budget allows, all sequences advancing together (the longest
+//                sets the number of segments; with a host copy of cu_seqlens it is exact, else the
+//                bound ceil(T / 64) is used and the segments past the longest sequence are empty).
 constexpr int kSegChunks = 64;
-constexpr int kMaxSegs = 64;
-constexpr int kRing = 3;
+constexpr int kMaxSegsOverlap = 64;
+constexpr size_t kRecordBudget = size_t(5) << 28;       // 1.25 GiB of records in the bounded shape
+constexpr int kEvents = 8;                              // event ring (more than the record ring)
 constexpr int kMaxDevices = 64;
-bool use_segments(int N, int T, int H) { return (long long)N * H <= 64 && max_chunks(N, T) >= 2 * kSegChunks; }
 size_t carry_bytes(int N, int H) { return (size_t)N * H * kD * kD * sizeof(float); }
-// chunks one ring buffer holds: the longest segment the launcher may choose
-int ring_chunks(int N, int T) {
-    const int qmax = (int)max_chunks(N, T);
-    return std::max(kSegChunks * 5 / 4, (qmax + kMaxSegs - 1) / kMaxSegs);
+
+struct SegShape {
+    int mode;            // 0 one segment, 1 overlap, 2 bounded
+    int per_min, per_max;
+    int ring;
+    size_t slot_records; // records (chunk, head) one ring buffer holds
+    long long nseg_max;  // segments at most (record tables in the workspace)
+    bool linear;         // one sequence whose records all fit: segment k's records at chunk k * per
+};
+
+SegShape seg_shape(int N, int T, int H) {
+    const size_t maxq = max_chunks(N, T);
+    const long long longest = ((long long)T + kC - 1) / kC;
+    SegShape sh{0, 1 << 30, 1 << 30, 1, maxq * (size_t)H, 1, false};
+    if ((long long)N * H <= 64 && longest >= 2 * kSegChunks) {
+        sh.mode = 1;
+        sh.ring = 3;
+        sh.per_max = std::max(kSegChunks * 5 / 4, (int)((longest + kMaxSegsOverlap - 1) / kMaxSegsOverlap));
+        sh.per_min = std::min(kSegChunks * 3 / 4, sh.per_max);
+    } else if (maxq * H * REC_BYTES > kRecordBudget) {
+        sh.mode = 2;
+        sh.ring = 2;
+        sh.per_max = sh.per_min =
+            (int)std::max<size_t>(1, kRecordBudget / ((size_t)sh.ring * N * H * REC_BYTES));
+    }
+    if (sh.mode) {
+        sh.slot_records = std::min((size_t)N * sh.per_max, maxq) * H;
+        sh.nseg_max = (longest + sh.per_min - 1) / sh.per_min;
+        if (N == 1 && maxq <= (size_t)sh.ring * sh.per_max) {
+            // one sequence whose records take no more room than the ring: each at its own place
+            sh.linear = true;
+            sh.ring = 1;
+            sh.slot_records = maxq * H;
+        }
+    }
+    return sh;
 }
-// whether the records go through the ring (else every chunk's record has its own place)
-bool use_ring(int N, int T) { return max_chunks(N, T) > (size_t)kRing * ring_chunks(N, T); }
+size_t tables_bytes(const SegShape &sh, int N) { return round256_((size_t)sh.nseg_max * (N + 1) * sizeof(int32_t)); }
 
 struct SideStream {
     std::mutex enqueue;                  // one call's launches and event records at a time
     cudaStream_t stream = nullptr;
-    cudaEvent_t ev[kMaxSegs + 1] = {};   // prep of segment k done (scan k may start); [nseg]: all scans done
-    cudaEvent_t ev_scan[kMaxSegs] = {};  // scan of segment k done (its ring buffer may be rewritten)
+    cudaEvent_t ev[kEvents + 1] = {};    // prep of segment k done, by k mod kEvents; [kEvents]: all scans done
+    cudaEvent_t ev_scan[kEvents] = {};   // scan of segment k done (its ring buffer may be rewritten)
     bool ready = false;
 };
 std::mutex g_side_mu;
@@ -916,9 +962,9 @@ cudaError_t side_stream(SideStream **out) {
         if ((e = cudaDeviceGetStreamPriorityRange(&lo, &hi)) != cudaSuccess ||
             (e = cudaStreamCreateWithPriority(&ss.stream, cudaStreamNonBlocking, hi)) != cudaSuccess)
             return e;
-        for (int i = 0; i <= kMaxSegs; ++i)
+        for (int i = 0; i <= kEvents; ++i)
             if ((e = cudaEventCreateWithFlags(&ss.ev[i], cudaEventDisableTiming)) != cudaSuccess) return e;
-        for (int i = 0; i < kMaxSegs; ++i)
+        for (int i = 0; i < kEvents; ++i)
             if ((e = cudaEventCreateWithFlags(&ss.ev_scan[i], cudaEventDisableTiming)) != cudaSuccess) return e;
         ss.ready = true;
     }
@@ -928,30 +974,29 @@ cudaError_t side_stream(SideStream **out) {
 
 }  // namespace
 
-// Workspace of the two-pass path (after the status word): chunk offsets, then for the segmented
-// pipeline the scan's state carry and kRing record buffers, otherwise one record per (chunk, head).
+// Workspace of the two-pass path (after the status word): the segments' record tables, then for a
+// segmented call the scan's state carry, then the ring of record buffers (one buffer holding every
+// record when the call is one segment).
 size_t tc_split_workspace(int N, int T, int H) {
-    const size_t off = round256_((size_t)(N + 1) * sizeof(int32_t));
-    const size_t chunks = use_segments(N, T, H) && use_ring(N, T) ? (size_t)kRing * ring_chunks(N, T)
-                                                                   : max_chunks(N, T);
-    return off + (use_segments(N, T, H) ? round256_(carry_bytes(N, H)) : 0) + chunks * H * REC_BYTES;
+    const SegShape sh = seg_shape(N, T, H);
+    return tables_bytes(sh, N) + (sh.mode ? round256_(carry_bytes(N, H)) : 0) +
+           (size_t)sh.ring * sh.slot_records * REC_BYTES;
 }
 
 cudaError_t launch_prefill_tc_split(const PrefillArgs &p, const float *conv_w, float *conv_state, int W,
                                     void *ws, cudaStream_t s) {
     if ((long long)p.N * p.H == 0) return cudaSuccess;
+    const SegShape sh = seg_shape(p.N, p.T, p.H);
     uint8_t *w = static_cast<uint8_t *>(ws);
-    int32_t *chunk_off = reinterpret_cast<int32_t *>(w);
-    w += round256_((size_t)(p.N + 1) * sizeof(int32_t));
-    const bool seg = use_segments(p.N, p.T, p.H);
+    int32_t *tables = reinterpret_cast<int32_t *>(w);
+    w += tables_bytes(sh, p.N);
     float *carry_S = nullptr;
-    if (seg) {
+    if (sh.mode) {
         carry_S = reinterpret_cast<float *>(w);
         w += round256_(carry_bytes(p.N, p.H));
     }
     uint8_t *rec = w;
     const int box_rows = p.T < kC ? p.T : kC;
-    const int qmax = (int)max_chunks(p.N, p.T);
     cudaError_t e;
     static std::atomic<uint64_t> prep_attr{0}, scan_attr{0};
     if ((e = smem_attr_once((const void *)kda_chunk_prep_kernel, (int)kSmemBytes, prep_attr)) != cudaSuccess ||
@@ -962,9 +1007,40 @@ cudaError_t launch_prefill_tc_split(const PrefillArgs &p, const float *conv_w, f
         (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
         return e;
 
-    kda_chunk_offsets_kernel<<<1, 1024, 0, s>>>(p.cu, p.N, p.T, qmax, chunk_off);
+    // segment length and count: the longest sequence from the host copy when there is one
+    long long longest = ((long long)p.T + kC - 1) / kC;
+    if (p.cu_host) {
+        longest = 0;
+        for (int n = 0; n < p.N; ++n)
+            longest = std::max<long long>(longest, ((long long)p.cu_host[n + 1] - p.cu_host[n] + kC - 1) / kC);
+    }
+    const int reserve = (int)std::min<long long>((long long)p.N * p.H, sms);   // SMs left to a concurrent scan
+    const int prep_ctas = sh.mode == 1 ? std::max(1, sms - reserve) : sms;
+    int per = sh.per_max;
+    if (sh.mode == 1) {
+        // segment length near kSegChunks whose (chunk, head) items fill whole waves of the prep grid
+        const int n_chains = std::max(1, p.N);
+        per = kSegChunks;
+        double best = 0.0;
+        for (int c = sh.per_min; c <= kSegChunks * 5 / 4; ++c) {
+            const long long items = (long long)c * n_chains * p.H, waves = (items + prep_ctas - 1) / prep_ctas;
+            const double eff = (double)items / (double)(waves * prep_ctas);
+            if (eff > best + 1e-9 || (eff > best - 1e-9 && std::abs(c - kSegChunks) < std::abs(per - kSegChunks))) {
+                best = eff;
+                per = c;
+            }
+        }
+        per = std::max(per, (int)((longest + kMaxSegsOverlap - 1) / kMaxSegsOverlap));
+        per = std::min(per, sh.per_max);
+    }
+    const int nseg = sh.mode ? (int)std::max<long long>(1, (longest + per - 1) / per) : 1;
+    if (nseg > sh.nseg_max) return cudaErrorInvalidValue;        // cannot happen: per >= per_min
+    const int qcap = (int)(sh.slot_records / p.H);                  // records one buffer holds
+
+    kda_segment_offsets_kernel<<<nseg, 1024, 0, s>>>(p.cu, p.N, p.T, sh.mode ? per : (1 << 30), qcap, tables);
     count_launch();
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    const size_t qmax = max_chunks(p.N, p.T);
 
     PrepArgs P{};
     if (qmax > 0 &&
@@ -978,7 +1054,6 @@ cudaError_t launch_prefill_tc_split(const PrefillArgs &p, const float *conv_w, f
     P.conv_state = conv_state;
     P.W = conv_w ? W : 0;
     P.box_rows = box_rows;
-    P.chunk_off = chunk_off;
     P.rec = rec;
 
     ScanArgs S{};
@@ -992,69 +1067,53 @@ cudaError_t launch_prefill_tc_split(const PrefillArgs &p, const float *conv_w, f
     S.p = p;
     S.conv_state = conv_w ? conv_state : nullptr;
     S.W = conv_w ? W : 0;
-    S.chunk_off = chunk_off;
     S.rec = rec;
     S.carry_S = carry_S;
     const unsigned scan_grid = (unsigned)(p.N * p.H);
 
-    auto prep = [&](int q_lo, int q_hi, int max_ctas, cudaStream_t st) -> cudaError_t {
-        const size_t items = (size_t)(q_hi - q_lo) * p.H;
-        if (items == 0) return cudaSuccess;
-        P.q_lo = q_lo;
-        P.q_hi = q_hi;
-        const unsigned grid = (unsigned)(items < (size_t)max_ctas ? items : (size_t)max_ctas);
+    // segment k: its record table, first local chunk and ring buffer
+    auto set_segment = [&](int k) {
+        P.seg_off = S.seg_off = tables + (size_t)k * (p.N + 1);
+        P.seg_lo = S.seg_lo = k * per;
+        P.rec = rec + (sh.linear ? (size_t)k * per * p.H : (size_t)(k % sh.ring) * sh.slot_records) * REC_BYTES;
+        S.rec = P.rec;
+    };
+    auto prep = [&](int max_ctas, cudaStream_t st) -> cudaError_t {
+        const unsigned grid = (unsigned)std::min<size_t>(sh.slot_records, (size_t)max_ctas);
+        if (grid == 0) return cudaSuccess;
         kda_chunk_prep_kernel<<<grid, kThreads, kSmemBytes, st>>>(P);
         count_launch();
         return cudaGetLastError();
     };
-    auto scan = [&](int q_lo, int q_hi, cudaStream_t st) -> cudaError_t {
-        S.q_lo = q_lo;
-        S.q_hi = q_hi;
-        S.p.test_limit = q_lo == 0 ? take_test_timeout(kTestScan) : 0u;
+    auto scan = [&](int k, cudaStream_t st) -> cudaError_t {
+        S.p.test_limit = k == 0 ? take_test_timeout(kTestScan) : 0u;
         kda_chunk_scan_kernel<<<scan_grid, kThreads, kScanSmemBytes, st>>>(S);
         count_launch();
         return cudaGetLastError();
     };
-    if (!seg) {
-        if ((e = prep(0, qmax, sms, s)) != cudaSuccess) return e;
-        return scan(0, qmax, s);
+    if (sh.mode == 0) {
+        set_segment(0);
+        if (qmax > 0 && (e = prep(sms, s)) != cudaSuccess) return e;
+        return scan(0, s);
     }
     SideStream *side = nullptr;
     if ((e = side_stream(&side)) != cudaSuccess) return e;
     // The events are shared by every call on this device: a concurrent call recording them between
     // this call's record and wait would order this call's scans after the wrong prep launches.
     std::lock_guard<std::mutex> enqueue_lock(side->enqueue);
-    const int reserve = (int)scan_grid;                    // SMs left to the concurrent scan
-    const int prep_ctas = std::max(1, sms - reserve);
-    // segment length near kSegChunks whose (chunk, head) items fill whole waves of the prep grid
-    int per = kSegChunks;
-    double best = 0.0;
-    for (int c = kSegChunks * 3 / 4; c <= kSegChunks * 5 / 4; ++c) {
-        const long long items = (long long)c * p.H, waves = (items + prep_ctas - 1) / prep_ctas;
-        const double eff = (double)items / (double)(waves * prep_ctas);
-        if (eff > best + 1e-9 || (eff > best - 1e-9 && std::abs(c - kSegChunks) < std::abs(per - kSegChunks))) {
-            best = eff;
-            per = c;
-        }
-    }
-    if ((qmax + per - 1) / per > kMaxSegs) per = (qmax + kMaxSegs - 1) / kMaxSegs;
-    const int nseg = (qmax + per - 1) / per;
-    const bool ring = use_ring(p.N, p.T);
-    const int slot_chunks = ring_chunks(p.N, p.T);        // >= per by construction
     for (int k = 0; k < nseg; ++k) {
-        const int q_lo = k * per, q_hi = std::min(qmax, q_lo + per);
-        P.rec = rec + (ring ? (size_t)(k % kRing) * slot_chunks : (size_t)q_lo) * p.H * REC_BYTES;
-        S.rec = P.rec;
-        if ((ring && k >= kRing && (e = cudaStreamWaitEvent(s, side->ev_scan[k - kRing], 0)) != cudaSuccess) ||
-            (e = prep(q_lo, q_hi, k == 0 ? sms : prep_ctas, s)) != cudaSuccess ||
-            (e = cudaEventRecord(side->ev[k], s)) != cudaSuccess ||
-            (e = cudaStreamWaitEvent(side->stream, side->ev[k], 0)) != cudaSuccess ||
-            (e = scan(q_lo, q_hi, side->stream)) != cudaSuccess ||
-            (e = cudaEventRecord(side->ev_scan[k], side->stream)) != cudaSuccess)
+        set_segment(k);
+        if ((!sh.linear && k >= sh.ring &&
+             (e = cudaStreamWaitEvent(s, side->ev_scan[(k - sh.ring) % kEvents], 0)) != cudaSuccess) ||
+            (e = prep(k == 0 ? sms : prep_ctas, s)) != cudaSuccess ||
+            (e = cudaEventRecord(side->ev[k % kEvents], s)) != cudaSuccess ||
+            (e = cudaStreamWaitEvent(side->stream, side->ev[k % kEvents], 0)) != cudaSuccess ||
+            (e = scan(k, side->stream)) != cudaSuccess ||
+            (e = cudaEventRecord(side->ev_scan[k % kEvents], side->stream)) != cudaSuccess)
             return e;
     }
-    if ((e = cudaEventRecord(side->ev[nseg], side->stream)) != cudaSuccess) return e;
-    return cudaStreamWaitEvent(s, side->ev[nseg], 0);
+    if ((e = cudaEventRecord(side->ev[kEvents], side->stream)) != cudaSuccess) return e;
+    return cudaStreamWaitEvent(s, side->ev[kEvents], 0);
 }
 
 }  // namespace k3kda

@@ -139,10 +139,11 @@ def test_fused_mixer_varlen_with_conv_state(path):
 
 @pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
 def test_two_pass_segmented_varlen_with_states(out_dtype):
-    """Few (sequence, head) pairs and >= 128 chunks: the two passes run as a pipeline of chunk
-    segments, the scan handing its state between segment launches; the middle sequence (chunks
-    65 .. 130) crosses the segment boundary at chunk 67."""
-    c = KI.prefill_case("segmented_varlen", [4100, 4200, 70], 2, 128, 128, 64, "bf16", seed=40, s0_std=0.02,
+    """Few (sequence, head) pairs and a sequence of >= 128 chunks: the two passes run as a pipeline of
+    segments of local chunks, all sequences advancing together through a ring of record buffers, the
+    scan handing each chain's state between segment launches; the sequences end in different
+    segments (130, 66 and 2 chunks)."""
+    c = KI.prefill_case("segmented_varlen", [8300, 4200, 70], 2, 128, 128, 64, "bf16", seed=40, s0_std=0.02,
                         gate=True, conv_width=4, conv_state=True)
     _check(c, out_dtype=out_dtype)
 
@@ -192,6 +193,34 @@ def test_two_pass_segment_ring_wraps():
     """300 chunks of one head: four segments through a ring of three record buffers, so a
     prep launch rewrites the buffer of a segment whose scan has finished."""
     _check(KI.fused_mixer(seed=42, T=19200, H=1))
+
+
+@pytest.mark.parametrize("host_lengths", [True, False], ids=["host_cu_seqlens", "device_only"])
+def test_two_pass_bounded_segments_many_chains(host_lengths):
+    """Many (sequence, head) chains whose records would exceed the record budget (4 sequences x 32
+    heads, 322 chunks: 1.53 GB): the call runs in segments of 35 local chunks of every sequence, all
+    sequences advancing together through a ring of two record buffers; the scan hands each chain's
+    state from segment to segment.  Without a host copy of cu_seqlens the segments run to the bound
+    ceil(T / 64), the ones past the longest sequence empty.  Checked on sampled heads."""
+    c = KI.prefill_case("bounded_segments", [9000, 300, 64, 11000], 32, 128, 128, 64, "bf16", seed=43,
+                        s0_std=0.02, gate=True, conv_width=4, conv_state=True)
+    ws_bytes = K.k3kda_prefill_workspace_size(c.N, c.T, c.H, 128, 128, 64, K.BF16, True)
+    assert ws_bytes < 1.5e9                               # the ring, not 322 x 32 records
+    d = case_to_device(c)
+    out = torch.empty((c.T, c.H, 128), device="cuda")
+    fs = torch.empty((c.N, c.H, 128, 128), device="cuda")
+    ws = torch.zeros(ws_bytes, dtype=torch.uint8, device="cuda")
+    cs = d["conv_state"].clone()
+    K.k3kda_prefill(d["q"], d["k"], d["v"], d["g"], d["beta"], d["S0"], d["cu"].cuda(),
+                    d["cu"] if host_lengths else None, c.N, c.T, c.H, 128, 128, 64, c.scale, True, d["conv_w"], cs,
+                    4, d["gate"], out, fs, ws)
+    torch.cuda.synchronize()
+    assert K.k3kda_workspace_status(ws) == 0
+    heads = [3, 30]
+    sub = head_subset(c, heads)
+    ro, rs, _ = oracle_prefill(sub)
+    assert_close(to_np(out[:, heads]), ro, False, "bounded segments out")
+    assert_close(to_np(fs[:, heads]), rs, False, "bounded segments final state")
 
 
 @pytest.mark.parametrize("W", [1, 2, 3])
