@@ -49,7 +49,7 @@ CORE = dict(T=64, H=2, d=16, chunk=16)    # the fp32 core workload (latency)
 CHUNKED = dict(T=8192, H=32, d=128, chunk=64)                        # chunked prefill, bf16, S0 = 0
 VARLEN = dict(n_seqs=16, lo=256, hi=16384, H=32, d=128, chunk=64)    # packed, lengths from seed 0, S0 != 0
 MLA = dict(N=256, H=32, d=128, L_max=8192)   # the attention layers' decode token: the decode batch
-MLA_TRAFFIC_PER_KEY_HEAD = 1.385983e9 / ((84420 + 16) * 32)   # DRAM bytes per attended (key, head), measured
+MLA_TRAFFIC_PER_KEY_HEAD = 1.388077e9 / ((84420 + 16) * 32)   # DRAM bytes per attended (key, head), measured
 
 
 def parse():
@@ -68,6 +68,8 @@ def parse():
     p.add_argument("--no-configs", action="store_true", help="skip the other workloads' lines")
     p.add_argument("--mla-seqs", type=int, default=None,
                    help="override the attention decode batch (profiling captures on a smaller case)")
+    p.add_argument("--backward-tokens", type=int, default=None,
+                   help="override the backward's length (profiling captures on a smaller case)")
     p.add_argument("--prefill-tokens", type=int, default=None,
                    help="override the prefill length (profiling captures on a smaller case; "
                         "the JSON config records the length used)")
@@ -530,7 +532,7 @@ def run_mla(args, K, torch, dev, rank, world):
 def run_backward(args, K, torch, dev, rank, world, clk_mhz=None):
     """Gradients of the recurrence (k3kda_backward) on the chunked-prefill shape, timed with CUDA
     events over the same steps and warm-up as the main step; reported beside it, not in value."""
-    T, H, d = BACKWARD["T"], BACKWARD["H"], BACKWARD["d"]
+    T, H, d = args.backward_tokens or BACKWARD["T"], BACKWARD["H"], BACKWARD["d"]
     gen = torch.Generator(device=dev)
     gen.manual_seed(2000 + rank)
     n = lambda *s: torch.randn(s, generator=gen, device=dev)
@@ -646,10 +648,10 @@ def run_e2e(args, K, torch, dev, P, Dc, prefill_call, decode_call, out_p, fs, ou
 # Measured DRAM bytes per call (ncu dram__bytes_read.sum + dram__bytes_write.sum, summed over the
 # call's kernels) of the current kernel versions, or None when not yet captured for a kernel
 # version.  The prefill figure is a T=8192 capture scaled by the tokens processed to T=65536.
-PREFILL_TRAFFIC_PER_LAUNCH = None        # two-pass call (prep + scan + offsets): not yet captured for this version
+PREFILL_TRAFFIC_PER_LAUNCH = 12.18e9     # two-pass call: prep + scan + offsets, 1.522 GB at T=8192 x 8
 CHUNKED_TRAFFIC_PER_LAUNCH = None
 VARLEN_TRAFFIC_PER_LAUNCH = None
-DECODE_TRAFFIC_PER_LAUNCH = 1.0997e9
+DECODE_TRAFFIC_PER_LAUNCH = 1.1028e9
 
 
 # ---- the CPU oracle (baseline leg and the reference arm) ----
