@@ -320,9 +320,9 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_prep_kernel(const __gri
         }
         if (!mma_wait()) break;
         clk.tick(3);
-        extract_a<PlanPrep>(sm, tl, kColA);
+        extract_akk<PlanPrep>(sm, tl, kColA);
         clk.tick(4);
-        solve_tb<PlanPrep>(sm);
+        solve_tb<PlanPrep>(sm, tl, kColA);
         float beta_next = 0.f;                           // the next item's beta, written after MMA U/W
         if (has_next && tid < kC && tid < y.te - y.cs) beta_next = a.beta[(size_t)(y.cs + tid) * H + y.h];
         if (tid == 0) {
@@ -474,6 +474,9 @@ __device__ __forceinline__ void tmem_put_split16(uint32_t col_hi, uint32_t col_l
     tmem_st8(col_lo, lw);
 }
 
+// spare issuing lanes of the scan: lane 0 of warps 15 and 14
+constexpr int kIssueX = kThreads - 32, kIssueK = kThreads - 64;
+
 // Per chunk: MMA [(W S')^T | (Qh S')^T]; V'^T = U^T - (W S')^T; MMA [O^T | S^T] += V'^T [Aqk^T | Kd]
 // while the gate's sigmoid is taken; then one phase writes this chunk's outputs and runs the next
 // chunk's state pass.  [W; Qh] and the gate rows (both double-buffered, two chunks ahead) and
@@ -569,25 +572,40 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_scan_kernel(const __gri
         pend = false;
         return true;
     };
-    auto load = [&](uint32_t bar, uint32_t dst, uint32_t off, int c, uint32_t bytes, bool &pend) {
+    // Copies are issued by thread 0 before the loop and by the spare lanes kIssueX / kIssueK inside
+    // it (their warps have slack where they issue); thread 0 alone waits on every copy and keeps
+    // the pending flags and phases, setting a flag at the point where the copy is issued.
+    auto issue = [&](uint32_t bar, uint32_t dst, uint32_t off, int c, uint32_t bytes) {
         mbar_arrive_expect_tx(bar, bytes);
         bulk_g2s(sbase + dst, rec_of(c) + off, bytes, bar);
+    };
+    auto load = [&](uint32_t bar, uint32_t dst, uint32_t off, int c, uint32_t bytes, bool &pend) {
+        issue(bar, dst, off, c, bytes);
         pend = true;
     };
+    auto issue_x = [&](int c) {
+        if (c & 1) issue(mb_x1, Q_X1, REC_X, c, 65536);
+        else issue(mb_x0, REC_X, REC_X, c, 65536);
+    };
+    auto mark_x = [&](int c) { if (c & 1) pend_x1 = true; else pend_x0 = true; };
     auto load_x = [&](int c) {
-        if (c & 1) load(mb_x1, Q_X1, REC_X, c, 65536, pend_x1);
-        else load(mb_x0, REC_X, REC_X, c, 65536, pend_x0);
+        issue_x(c);
+        mark_x(c);
     };
     auto wait_x = [&](int c) {
         const uint32_t lim = xlim;
         xlim = kWaitLimit;
         return (c & 1) ? wait_on(mb_x1, xph1, pend_x1, lim) : wait_on(mb_x0, xph0, pend_x0, lim);
     };
-    auto load_gate = [&](int c) {                    // chunk c's gate rows -> buffer c & 1 (thread 0)
+    auto issue_gate = [&](int c) {                   // chunk c's gate rows -> buffer c & 1
         const uint32_t bar = (c & 1) ? mb_g1 : mb_g0;
         mbar_arrive_expect_tx(bar, (uint32_t)A.box_rows * kD * 2);
         tma_load_3d(sbase + ((c & 1) ? Q_G1 : Q_G0), &A.tm_gate, 0, h, tb + c * kC, bar);
-        if (c & 1) pend_g1 = true; else pend_g0 = true;
+    };
+    auto mark_gate = [&](int c) { if (c & 1) pend_g1 = true; else pend_g0 = true; };
+    auto load_gate = [&](int c) {
+        issue_gate(c);
+        mark_gate(c);
     };
     auto wait_gate = [&](int c) { return (c & 1) ? wait_on(mb_g1, gph1, pend_g1) : wait_on(mb_g0, gph0, pend_g0); };
     // the other threads wait for chunk c's gate rows themselves (no CTA barrier): the phase of
@@ -631,12 +649,17 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_scan_kernel(const __gri
 #pragma unroll
         for (int b = 0; b < 2; ++b) {
             const int col = quarter * 32 + 16 * b;
-            float v[16];
+            float v[16], fa[16], fs[16];
+#pragma unroll
+            for (int u = 0; u < 16; u += 4) {
+                *reinterpret_cast<float4 *>(fa + u) = *reinterpret_cast<const float4 *>(sFA + col + u);
+                *reinterpret_cast<float4 *>(fs + u) = *reinterpret_cast<const float4 *>(sFS + col + u);
+            }
 #pragma unroll
             for (int u = 0; u < 16; ++u) {
                 const float x = __uint_as_float(r[b][u]);
-                v[u] = x * sFA[col + u];
-                r[b][u] = __float_as_uint(x * sFS[col + u]);
+                v[u] = x * fa[u];
+                r[b][u] = __float_as_uint(x * fs[u]);
             }
             tmem_st16(tl + kColSs + col, r[b]);
             tmem_put_split16(tl + kColSh + col / 2, tl + kColSl + col / 2, v);
@@ -763,14 +786,23 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_scan_kernel(const __gri
 #pragma unroll
             for (int u = 0; u < 16; ++u) sg[u] = 1.f;
         }
-        if (!mma_wait()) { failed = true; break; }
-        if (tid == 0 && more) load(mb_k, REC_B, REC_B, c + 1, 49152, pend_k);   // [Aqk^T | Kb] of the next chunk
-        if (tid == 0 && c + 2 < c_end) {                 // this chunk's [W; Qh] and gate buffers are free
-            load_x(c + 2);
-            if (gated) load_gate(c + 2);
+        // this chunk's [W; Qh] buffer is free since MMA W: the tile two chunks ahead, and the record
+        // three chunks ahead into L2, while MMA O/S runs
+        if (c + 2 < c_end) {
+            if (tid == kIssueX) issue_x(c + 2);
+            if (tid == 0) mark_x(c + 2);
         }
-        // the record three chunks ahead into L2, queued behind the copies above
-        if (tid == 0 && c + 3 < c_end) prefetch_chunk(c + 3);
+        if (tid == kIssueX && c + 3 < c_end) prefetch_chunk(c + 3);
+        if (!mma_wait()) { failed = true; break; }
+        // the buffers read by MMA O/S and by the gate's sigmoid are free
+        if (more) {                                      // [Aqk^T | Kd] of the next chunk
+            if (tid == kIssueK) issue(mb_k, REC_B, REC_B, c + 1, 49152);
+            if (tid == 0) pend_k = true;
+        }
+        if (gated && c + 2 < c_end) {
+            if (tid == kIssueX) issue_gate(c + 2);
+            if (tid == 0) mark_gate(c + 2);
+        }
         clk.tick(2);
         // ---- this chunk's outputs, then the next chunk's state pass ----
         // bf16 outputs go through a shared tile and one TMA store that runs behind the next chunk,

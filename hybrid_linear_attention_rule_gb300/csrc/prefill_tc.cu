@@ -207,9 +207,9 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
         put_kd(sm + OFF_KB_HI, kd);
         fence_async_smem();
         PHASE(1);
-        extract_a<PlanFused>(sm, tl, kColA);
+        extract_akk<PlanFused>(sm, tl, kColA);
         PHASE(2);
-        solve_tb<PlanFused>(sm);
+        solve_tb<PlanFused>(sm, tl, kColA);
         PHASE(3);
         // ================= MMA: U^T = v^T Tb^T =================
         if (tid == 0) {

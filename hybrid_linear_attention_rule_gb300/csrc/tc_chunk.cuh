@@ -180,17 +180,17 @@ __device__ __forceinline__ void tile64_put16(uint8_t *sm, uint32_t off_hi, uint3
 // Thread (warp, lane) owns tokens 4*warp .. +3 and channels 4*lane .. +3 of the chunk.
 
 // Conv (+SiLU) and, for q and k with the L2 norm on, the norm of tensor `which` (0 q, 1 k, 2 v)
-// for this thread's 4 tokens x 4 channels: reads the staged rows at `st` and the pre-conv rows
-// before the chunk in HIST (tensor-major, three rows each).
+// for NT tokens from i0 x this lane's 4 channels: reads the staged rows at `st` and the pre-conv
+// rows before the chunk in HIST (tensor-major, three rows each).
+template <int NT>
 __device__ __forceinline__ void conv_rows(const uint8_t *sm, const PrefillArgs &a, int which, uint32_t st,
-                                          int Lc, int W, float (&y)[kTok][4]) {
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int i0 = warp * kTok, c0 = lane * 4;
+                                          int Lc, int W, int i0, float (&y)[NT][4]) {
+    const int c0 = (threadIdx.x & 31) * 4;
     const float *sConvW = reinterpret_cast<const float *>(sm + OFF_CONVW);
     const float *sHist = reinterpret_cast<const float *>(sm + OFF_HIST);
-    float x[kTok + 3][4];
+    float x[NT + 3][4];
 #pragma unroll
-    for (int t = 0; t < kTok + 3; ++t) {
+    for (int t = 0; t < NT + 3; ++t) {
         const int i = i0 - 3 + t;               // chunk-local token
         if (i < 0) {
             const float4 hv = *reinterpret_cast<const float4 *>(sHist + (which * 3 + 3 + i) * 128 + c0);
@@ -210,7 +210,7 @@ __device__ __forceinline__ void conv_rows(const uint8_t *sm, const PrefillArgs &
 #pragma unroll
         for (int t = 0; t < 4; ++t) w4[t] = *reinterpret_cast<const float4 *>(sConvW + t * 384 + which * kD + c0);
 #pragma unroll
-        for (int ii = 0; ii < kTok; ++ii) {
+        for (int ii = 0; ii < NT; ++ii) {
             float acc[4];
             acc[0] = w4[0].x * x[ii][0]; acc[1] = w4[0].y * x[ii][1];
             acc[2] = w4[0].z * x[ii][2]; acc[3] = w4[0].w * x[ii][3];
@@ -224,13 +224,13 @@ __device__ __forceinline__ void conv_rows(const uint8_t *sm, const PrefillArgs &
         }
     } else {
 #pragma unroll
-        for (int ii = 0; ii < kTok; ++ii)
+        for (int ii = 0; ii < NT; ++ii)
 #pragma unroll
             for (int m = 0; m < 4; ++m) y[ii][m] = x[ii + 3][m];
     }
     if (a.l2 && which < 2) {
 #pragma unroll
-        for (int ii = 0; ii < kTok; ++ii) {
+        for (int ii = 0; ii < NT; ++ii) {
             float ss = y[ii][0] * y[ii][0] + y[ii][1] * y[ii][1] + y[ii][2] * y[ii][2] + y[ii][3] * y[ii][3];
             ss = warp_sum(ss);
             const float inv = rsqrtf(ss + K3KDA_L2_EPS);
@@ -433,14 +433,19 @@ __device__ __forceinline__ bool prep_qk(uint8_t *sm, const PrefillArgs &a, int c
     if (P::CALLER_STAGES && tid == 0) bulk_wait_read_all();   // X rows are rewritten below
     const bool any_strong = __syncthreads_or(strong) != 0;
     float yq[kTok][4], yk[kTok][4];
-    conv_rows(sm, a, 0, P::QST, Lc, W, yq);
-    conv_rows(sm, a, 1, P::KST, Lc, W, yk);
+    conv_rows<kTok>(sm, a, 0, P::QST, Lc, W, i0, yq);
+    conv_rows<kTok>(sm, a, 1, P::KST, Lc, W, i0, yk);
     if (any_strong) strong_correction<P>(sm, yq, yk, G, tl, col);
     {
         const float4 r4 = *reinterpret_cast<const float4 *>(sRef + c0);
         const float4 l4 = *reinterpret_cast<const float4 *>(sGL + c0);
         const float rr[4] = {r4.x, r4.y, r4.z, r4.w}, gl[4] = {l4.x, l4.y, l4.z, l4.w};
         const uint32_t sb = strong_bits4(sMask, c0);
+        // exp(G_last - G) = exp(G_last - rho) exp(rho - G): two factors within exp(+-80) for the
+        // other channels; a strong channel (no 1/E) takes its own exponential
+        float cgl[4];
+#pragma unroll
+        for (int m = 0; m < 4; ++m) cgl[m] = __expf(gl[m] - rr[m]);
 #pragma unroll
         for (int ii = 0; ii < kTok; ++ii) {
             float qh[4], kh[4], kb[4];
@@ -454,7 +459,12 @@ __device__ __forceinline__ bool prep_qk(uint8_t *sm, const PrefillArgs &a, int c
                 qh[m] = yq[ii][m] * e;
                 kh[m] = yk[ii][m] * e;
                 kb[m] = yk[ii][m] * eb;
-                kd[ii][m] = yk[ii][m] * __expf(gl[m] - G[ii][m]);
+                kd[ii][m] = kb[m] * cgl[m];
+            }
+            if (sb != 0u) {
+#pragma unroll
+                for (int m = 0; m < 4; ++m)
+                    if ((sb >> m) & 1u) kd[ii][m] = yk[ii][m] * __expf(gl[m] - G[ii][m]);
             }
             put_row_split(sm, P::X_HI, P::X_LO, P::X_ATOM, 64 + i0 + ii, c0, qh);   // Qh rows 64..127
             put_row_split(sm, P::X_HI, P::X_LO, P::X_ATOM, i0 + ii, c0, kh);        // Kh rows 0..63
@@ -475,7 +485,7 @@ __device__ __forceinline__ void prep_v(uint8_t *sm, const PrefillArgs &a, int Lc
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int i0 = warp * kTok, c0 = lane * 4;
     float y[kTok][4];
-    conv_rows(sm, a, 2, P::VST, Lc, W, y);
+    conv_rows<kTok>(sm, a, 2, P::VST, Lc, W, i0, y);
 #pragma unroll
     for (int ii = 0; ii < kTok; ++ii) put_row_split(sm, P::V_HI, P::V_LO, 8192, i0 + ii, c0, y[ii]);
     fence_async_smem();
@@ -532,144 +542,192 @@ __device__ __forceinline__ void issue_mma_a(uint32_t sbase, uint32_t tmem_col_ad
     mma_commit(mbar);
 }
 
-// ---- stage 3: Akk (times beta, strictly lower) -> fp32 scratch A, Aqk (lower) -> split tile (transposed) ----
-// tl is this warp's TMEM lane base, col the first column of the MMA A result.
+// ---- stages 3 and 4: T = (I + Akk)^-1 (fp32, block recursive), Tb = T diag(beta) -> split tile,
+// and Aqk (lower) -> split tile (transposed), from the MMA A result in TMEM columns [col, col + 64)
+// (plus [col + 64, col + 128) for a stacked Kb).  The warps on TMEM lanes 0-63 (warp & 3 < 2) take
+// Akk and the substitution, those on lanes 64-127 take Aqk meanwhile.  tl is this warp's TMEM lane
+// base.
 template <class P>
-__device__ __forceinline__ void extract_a(uint8_t *sm, uint32_t tl, uint32_t col) {
+__device__ __forceinline__ void mma_a_row16(uint32_t tl, uint32_t col, uint32_t (&r0)[16]) {
+    tmem_ld16(tl + col, r0);
+    if (P::KB_STACKED) {
+        uint32_t r1[16];
+        tmem_ld16(tl + col + 64, r1);
+        tmem_wait_ld();
+#pragma unroll
+        for (int u = 0; u < 16; ++u) r0[u] = __float_as_uint(__uint_as_float(r0[u]) + __uint_as_float(r1[u]));
+    } else {
+        tmem_wait_ld();
+    }
+}
+
+// Akk (times beta, strictly lower) -> fp32 scratch A, by the warps on lanes 0-63; they also zero
+// the upper blocks (0,1) and (2,3) of T that the block products read.
+template <class P>
+__device__ __forceinline__ void extract_akk(uint8_t *sm, uint32_t tl, uint32_t col) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int quarter = warp >> 2, lrow = 32 * (warp & 3);
-    const float *sBeta = reinterpret_cast<const float *>(sm + OFF_BETA);
-    float *scrA = reinterpret_cast<float *>(sm + P::SCR_A);
-    // ================= Akk -> fp32 scratch, Aqk -> split tile =================
-    {
-        const int colbase = quarter * 16;
+    if ((warp & 3) < 2) {
+        const int quarter = warp >> 2, row = 32 * (warp & 3) + lane, colbase = quarter * 16;
+        const float b = reinterpret_cast<const float *>(sm + OFF_BETA)[row];
+        float *scrA = reinterpret_cast<float *>(sm + P::SCR_A);
+        float *scrT = reinterpret_cast<float *>(sm + P::SCR_T);
         uint32_t r0[16];
-        tmem_ld16(tl + col + colbase, r0);
-        if (P::KB_STACKED) {
-            uint32_t r1[16];
-            tmem_ld16(tl + col + 64 + colbase, r1);
-            tmem_wait_ld();
+        mma_a_row16<P>(tl, col + colbase, r0);
 #pragma unroll
-            for (int u = 0; u < 16; ++u) r0[u] = __float_as_uint(__uint_as_float(r0[u]) + __uint_as_float(r1[u]));
-        } else {
-            tmem_wait_ld();
+        for (int u = 0; u < 16; ++u) {
+            const int j = colbase + u;
+            scrA[sidx(row, j)] = j < row ? b * __uint_as_float(r0[u]) : 0.f;
         }
-        const int row = lrow + lane;
-        if (row < 64) {
-            const float b = sBeta[row];
+        const int e = (warp >> 2) * 64 + (warp & 1) * 32 + lane;    // 0 .. 255
 #pragma unroll
-            for (int u = 0; u < 16; ++u) {
-                const int j = colbase + u;
-                scrA[sidx(row, j)] = j < row ? b * __uint_as_float(r0[u]) : 0.f;
-            }
-        } else {
-            // Aqk stored transposed, [i'][i]: the MMAs read it as an MN-major B operand, so that
-            // it can sit beside the Kb rows in one N = 192 operand; a warp's 32 lanes (32
-            // consecutive i) fill 64 contiguous bytes of one row i'
-            const int i = row - 64;
-#pragma unroll
-            for (int u = 0; u < 16; ++u) {
-                const int ip = colbase + u;
-                float hv, lv;
-                split_bf16(ip > i ? 0.f : __uint_as_float(r0[u]), hv, lv);
-                const uint32_t o = sw128_offset(ip, i);
-                *reinterpret_cast<__nv_bfloat16 *>(sm + P::AQK_HI + o) = __float2bfloat16_rn(hv);
-                *reinterpret_cast<__nv_bfloat16 *>(sm + P::AQK_LO + o) = __float2bfloat16_rn(lv);
-            }
+        for (int k = 0; k < 2; ++k) {
+            const int f = e + 256 * k, blk = f >> 8, r = (f >> 4) & 15, c = f & 15;
+            scrT[sidx(blk * 32 + r, blk * 32 + 16 + c)] = 0.f;
         }
     }
     __syncthreads();
 }
 
-// ---- stage 4: T = (I + Akk)^-1 (fp32, block recursive), Tb = T diag(beta) -> split tile ----
 template <class P>
-__device__ __forceinline__ void solve_tb(uint8_t *sm) {
+__device__ __forceinline__ void solve_tb(uint8_t *sm, uint32_t tl, uint32_t col) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const float *sBeta = reinterpret_cast<const float *>(sm + OFF_BETA);
     const float *scrA = reinterpret_cast<const float *>(sm + P::SCR_A);
     float *scrT = reinterpret_cast<float *>(sm + P::SCR_T);
     // ================= T = (I + Akk)^-1 in fp32, Tb = T diag(beta) (hi/lo) =================
-    // diagonal 16x16 blocks by substitution (one column per thread); the upper blocks
-    // (0,1) and (2,3) that the block products read are zeroed at the same time
-    if (warp < 4 && lane < 16) {
-        const int b = warp, col = lane, ib = b * 16;
-        float x[16];
+    // Rows of the fp32 scratch are stored with their 16-byte slots permuted by the row (sidx): the
+    // four words from column c (a multiple of 4) of row r are the slot at r*64 + (c ^ (r & 28)),
+    // word w holding column c + (w ^ (r & 3)).
+    //
+    // Diagonal 16x16 blocks by substitution, x_i = -sum_{j<i} A_ij x_j down each column of the
+    // block inverse: warps 4b and 4b+1 take block b, four threads per column, each holding rows
+    // 4p .. 4p+3 of the column and summing over its own four of them (A is zero on and above the
+    // diagonal, so entries not yet final contribute nothing).  Meanwhile the warps on lanes 64-127
+    // store Aqk^T as split bf16 [i'][i]: the MMAs read it as an MN-major B operand, so that it can
+    // sit beside the Kd rows in one N = 192 operand; a warp's 32 lanes (32 consecutive i) fill 64
+    // contiguous bytes of one row i'.
+    if ((warp & 3) < 2) {
+        const int ib = (warp >> 2) * 16;
+        const int t = (warp & 1) * 32 + lane, col = t >> 2, p = t & 3;
+        float xr[4];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) x[i] = (i == col) ? 1.f : 0.f;
+        for (int u = 0; u < 4; ++u) xr[u] = (4 * p + u == col) ? 1.f : 0.f;
 #pragma unroll
         for (int i = 1; i < 16; ++i) {
-            float s0 = 0.f, s1 = 0.f;
-#pragma unroll
-            for (int j = 0; j < i; j += 2) {
-                s0 = fmaf(scrA[sidx(ib + i, ib + j)], x[j], s0);
-                if (j + 1 < i) s1 = fmaf(scrA[sidx(ib + i, ib + j + 1)], x[j + 1], s1);
-            }
-            if (i > col) x[i] = -(s0 + s1);
+            const int r = ib + i;
+            const float4 a4 = *reinterpret_cast<const float4 *>(scrA + r * 64 + ((ib + 4 * p) ^ (r & 28)));
+            const float av[4] = {a4.x, a4.y, a4.z, a4.w};
+            float s = fmaf(av[0 ^ (i & 3)], xr[0], av[1 ^ (i & 3)] * xr[1]);
+            s = fmaf(av[2 ^ (i & 3)], xr[2], s);
+            s = fmaf(av[3 ^ (i & 3)], xr[3], s);
+            s += __shfl_xor_sync(0xffffffffu, s, 1);
+            s += __shfl_xor_sync(0xffffffffu, s, 2);
+            if (i > col && p == (i >> 2)) xr[i & 3] = -s;
         }
 #pragma unroll
-        for (int i = 0; i < 16; ++i) scrT[sidx(ib + i, ib + col)] = x[i];
-    } else if (warp >= 4) {
-        for (int e = tid - 128; e < 512; e += kThreads - 128) {
-            const int blk = e >> 8, r = (e >> 4) & 15, c = e & 15;
-            scrT[sidx(blk * 32 + r, blk * 32 + 16 + c)] = 0.f;
+        for (int u = 0; u < 4; ++u) scrT[sidx(ib + 4 * p + u, ib + col)] = xr[u];
+    } else {
+        const int colbase = (warp >> 2) * 16, i = 32 * (warp & 3) + lane - 64;
+        uint32_t r0[16];
+        mma_a_row16<P>(tl, col + colbase, r0);
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+            const int ip = colbase + u;
+            float hv, lv;
+            split_bf16(ip > i ? 0.f : __uint_as_float(r0[u]), hv, lv);
+            const uint32_t o = sw128_offset(ip, i);
+            *reinterpret_cast<__nv_bfloat16 *>(sm + P::AQK_HI + o) = __float2bfloat16_rn(hv);
+            *reinterpret_cast<__nv_bfloat16 *>(sm + P::AQK_LO + o) = __float2bfloat16_rn(lv);
         }
     }
     __syncthreads();
-    // level 1: T[b+1,b] = -T[b+1,b+1] (A[b+1,b] T[b,b]) for b = 0, 2; P parked in block (0, 2 + b/2)
-    {
-        const int e = tid;                               // 512 elements, one per thread
-        const int pb = e >> 8, r = (e >> 4) & 15, c = e & 15, b = 2 * pb;
+    // sum_{m<16} L[R][c0 + m] R[r0 + m][rc] with L's row read as four 16-byte slots (c0 a multiple of 16)
+    auto dot16 = [&](const float *L, int R, int c0, int r0, int rc) {
+        const int xh = R & 28, xl = R & 3;
         float s0 = 0.f, s1 = 0.f;
 #pragma unroll
-        for (int m = 0; m < 16; m += 2) {
-            s0 = fmaf(scrA[sidx((b + 1) * 16 + r, b * 16 + m)], scrT[sidx(b * 16 + m, b * 16 + c)], s0);
-            s1 = fmaf(scrA[sidx((b + 1) * 16 + r, b * 16 + m + 1)], scrT[sidx(b * 16 + m + 1, b * 16 + c)], s1);
+        for (int q = 0; q < 4; ++q) {
+            const float4 a4 = *reinterpret_cast<const float4 *>(L + R * 64 + ((c0 + 4 * q) ^ xh));
+            s0 = fmaf(a4.x, scrT[sidx(r0 + 4 * q + (0 ^ xl), rc)], s0);
+            s1 = fmaf(a4.y, scrT[sidx(r0 + 4 * q + (1 ^ xl), rc)], s1);
+            s0 = fmaf(a4.z, scrT[sidx(r0 + 4 * q + (2 ^ xl), rc)], s0);
+            s1 = fmaf(a4.w, scrT[sidx(r0 + 4 * q + (3 ^ xl), rc)], s1);
         }
-        scrT[sidx(r, (2 + pb) * 16 + c)] = s0 + s1;
+        return s0 + s1;
+    };
+    // level 1: T[b+1,b] = -T[b+1,b+1] (A[b+1,b] T[b,b]) for b = 0, 2; P parked in block (0, 2 + b/2).
+    // One element per thread; the two half-warps take rows r and r + 4, so that both read the
+    // right factor's rows in the same order (one row of 16 words per step).
+    {
+        const int w = warp, pb = w >> 3, b = 2 * pb, c = lane & 15;
+        const int r = (w & 3) + 4 * ((lane >> 4) & 1) + 8 * ((w >> 2) & 1);
+        const float s = dot16(scrA, (b + 1) * 16 + r, b * 16, b * 16, b * 16 + c);
+        scrT[sidx(r, (2 + pb) * 16 + c)] = s;
         __syncthreads();
-        s0 = 0.f; s1 = 0.f;
-#pragma unroll
-        for (int m = 0; m < 16; m += 2) {
-            s0 = fmaf(scrT[sidx((b + 1) * 16 + r, (b + 1) * 16 + m)], scrT[sidx(m, (2 + pb) * 16 + c)], s0);
-            s1 = fmaf(scrT[sidx((b + 1) * 16 + r, (b + 1) * 16 + m + 1)], scrT[sidx(m + 1, (2 + pb) * 16 + c)], s1);
-        }
-        scrT[sidx((b + 1) * 16 + r, b * 16 + c)] = -(s0 + s1);
+        const float s2 = dot16(scrT, (b + 1) * 16 + r, (b + 1) * 16, 0, (2 + pb) * 16 + c);
+        scrT[sidx((b + 1) * 16 + r, b * 16 + c)] = -s2;
         __syncthreads();
     }
     // level 2: T[32:64, 0:32] = -T2 (A[32:64, 0:32] T1); P (32x32) parked in T[0:32, 32:64].
-    // 256 threads, each a 2x2 output tile (rows r0, r0+1; columns cc, cc+1; r0, cc even).  With
-    // the XOR swizzle, (row even, columns 2k, 2k+1) and (row m, columns cc, cc+1) are adjacent
-    // words, so every operand pair is one 8-byte load (for odd m the pair is stored swapped).
+    // Warps 0-7: 64 tiles of 4 x 4 outputs, four threads per tile each summing a quarter of the 32
+    // terms, so that every 16-byte load serves four products; both factors are read a slot at a
+    // time (rows r0 + rr with r0 a multiple of 4, so the word order within a slot is fixed).
     {
-        const int r0 = ((tid >> 4) & 15) * 2, cc = (tid & 15) * 2;
-        auto block_prod = [&](const float *Lm, int lrow, int lcol, int rcol, float (&p)[4]) {
-            p[0] = p[1] = p[2] = p[3] = 0.f;
+        const int hq = tid & 3, tile = (tid >> 2) & 63, tr = tile >> 3, tc = tile & 7;
+        auto block_prod = [&](const float *Lm, int lrow, int lcol, int rcol, float (&acc)[4][4]) {
 #pragma unroll
-            for (int m = 0; m < 32; m += 2) {
-                const float2 a0 = *reinterpret_cast<const float2 *>(Lm + sidx(lrow + r0, lcol + m));
-                const float2 a1 = *reinterpret_cast<const float2 *>(Lm + sidx(lrow + r0 + 1, lcol + m) - 1);
-                const float2 be = *reinterpret_cast<const float2 *>(scrT + sidx(m, rcol + cc));
-                const float2 bo = *reinterpret_cast<const float2 *>(scrT + sidx(m + 1, rcol + cc) - 1);
-                // row r0 + 1 is odd: its pair (m, m+1) sits swapped, like the odd-m row of the right factor
-                p[0] = fmaf(a0.x, be.x, p[0]); p[1] = fmaf(a0.x, be.y, p[1]);
-                p[2] = fmaf(a1.y, be.x, p[2]); p[3] = fmaf(a1.y, be.y, p[3]);
-                p[0] = fmaf(a0.y, bo.y, p[0]); p[1] = fmaf(a0.y, bo.x, p[1]);
-                p[2] = fmaf(a1.x, bo.y, p[2]); p[3] = fmaf(a1.x, bo.x, p[3]);
+            for (int rr = 0; rr < 4; ++rr)
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) acc[rr][cc] = 0.f;
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                const int m0 = 8 * hq + 4 * q;               // four consecutive terms
+                float av[4][4];
+#pragma unroll
+                for (int rr = 0; rr < 4; ++rr) {
+                    const int R = lrow + 4 * tr + rr;
+                    const float4 v = *reinterpret_cast<const float4 *>(Lm + R * 64 + ((lcol + m0) ^ (R & 28)));
+                    av[rr][0] = v.x; av[rr][1] = v.y; av[rr][2] = v.z; av[rr][3] = v.w;
+                }
+#pragma unroll
+                for (int mm = 0; mm < 4; ++mm) {
+                    const int M = m0 + mm;
+                    const float4 v = *reinterpret_cast<const float4 *>(scrT + M * 64 + ((rcol + 4 * tc) ^ (M & 28)));
+                    const float bv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                    for (int rr = 0; rr < 4; ++rr)
+#pragma unroll
+                        for (int cc = 0; cc < 4; ++cc)
+                            acc[rr][cc] = fmaf(av[rr][mm ^ rr], bv[cc ^ mm], acc[rr][cc]);
+                }
             }
+#pragma unroll
+            for (int rr = 0; rr < 4; ++rr)
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) {
+                    acc[rr][cc] += __shfl_xor_sync(0xffffffffu, acc[rr][cc], 1);
+                    acc[rr][cc] += __shfl_xor_sync(0xffffffffu, acc[rr][cc], 2);
+                }
         };
-        float p[4];
-        if (tid < 256) {
-            block_prod(scrA, 32, 0, 0, p);
-            // the park area is read by nobody in this pass
-            *reinterpret_cast<float2 *>(scrT + sidx(r0, 32 + cc)) = make_float2(p[0], p[1]);
-            *reinterpret_cast<float2 *>(scrT + sidx(r0 + 1, 32 + cc) - 1) = make_float2(p[3], p[2]);
+        // thread hq of a tile writes row hq of it (negated if neg) at rows orow.., columns ocol..
+        auto put_row = [&](const float (&acc)[4][4], int orow, int ocol, float sgn) {
+#pragma unroll
+            for (int rr = 0; rr < 4; ++rr)
+                if (rr == hq) {
+                    const int R = orow + 4 * tr + rr;
+                    *reinterpret_cast<float4 *>(scrT + R * 64 + ((ocol + 4 * tc) ^ (R & 28))) =
+                        make_float4(sgn * acc[rr][0 ^ rr], sgn * acc[rr][1 ^ rr], sgn * acc[rr][2 ^ rr], sgn * acc[rr][3 ^ rr]);
+                }
+        };
+        float acc[4][4];
+        if (warp < 8) {
+            block_prod(scrA, 32, 0, 0, acc);
+            put_row(acc, 0, 32, 1.f);                    // the park area is read by nobody in this pass
         }
         __syncthreads();
-        if (tid < 256) {
-            block_prod(scrT, 32, 32, 32, p);
-            // T21 lives in rows 32..63, columns 0..31: not read by this pass
-            *reinterpret_cast<float2 *>(scrT + sidx(32 + r0, cc)) = make_float2(-p[0], -p[1]);
-            *reinterpret_cast<float2 *>(scrT + sidx(33 + r0, cc) - 1) = make_float2(-p[3], -p[2]);
+        if (warp < 8) {
+            block_prod(scrT, 32, 32, 32, acc);
+            put_row(acc, 32, 0, -1.f);                   // T21: not read by this pass
         }
     }
     __syncthreads();
