@@ -163,7 +163,7 @@ __global__ void __launch_bounds__(kThreads) cb_prep_kernel(const __grid_constant
     const size_t tile = (size_t)item * kC * kD;
     for (int e = tid; e < kC * kD; e += kThreads) {
         const int i = e / kD, c = e % kD;
-        const float gm = sG[i][c], ea = expf(gm), ed = expf(sG[kC - 1][c] - gm);
+        const float gm = sG[i][c], ea = __expf(gm), ed = __expf(sG[kC - 1][c] - gm);
         const float k0 = sK[i][c] * ea;
         A.Q0[tile + e] = sQ[i][c] * ea;
         A.K0[tile + e] = k0;
@@ -179,7 +179,7 @@ __global__ void __launch_bounds__(kThreads) cb_prep_kernel(const __grid_constant
         if (j <= i) {
 #pragma unroll 4
             for (int c = 0; c < kD; ++c) {
-                const float t = sK[j][c] * expf(sG[i][c] - sG[j][c]);
+                const float t = sK[j][c] * __expf(sG[i][c] - sG[j][c]);
                 b1 = fmaf(sK[i][c], t, b1);
                 b2 = fmaf(sQ[i][c], t, b2);
             }
@@ -630,7 +630,7 @@ __global__ void __launch_bounds__(kThreads, 2) cb_grad_kernel(const __grid_const
 #pragma unroll
         for (int x = 0; x < 4; ++x) {
             const int c = tn + 16 * x;
-            const float e = expf(-fabsf(gi[x] - s.Gm[m][c]));
+            const float e = __expf(-fabsf(gi[x] - s.Gm[m][c]));
             const float km = s.k[m][c] * e;
             p1[x] = fmaf(aq, km, p1[x]);
             p2[x] = fmaf(ad, km, p2[x]);
@@ -644,7 +644,7 @@ __global__ void __launch_bounds__(kThreads, 2) cb_grad_kernel(const __grid_const
 #pragma unroll
     for (int x = 0; x < 4; ++x) {
         const int c = tn + 16 * x, cg = cbase + c;
-        const float ea = expf(gi[x]), ed = expf(s.gl[c] - gi[x]);
+        const float ea = __expf(gi[x]), ed = __expf(s.gl[c] - gi[x]);
         const float dr = s.dR[i][cg], kv = s.k[i][c], qv = s.q[i][c];
         const float vv = i < L ? ld_x(A.v, row + cg, A.bf16) : 0.f;
         pb += vv * dr - kv * ea * y[x];
