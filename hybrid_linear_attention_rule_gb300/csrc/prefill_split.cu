@@ -109,6 +109,55 @@ __global__ void __launch_bounds__(1024) kda_segment_offsets_kernel(const int32_t
     }
 }
 
+// ============================ one launch for every segment ============================
+// In the overlap shape one cooperative launch runs every segment: n_scan of its CTAs are the scan
+// chains, the rest the prep, all resident at once (the first segment is prepared beforehand by a
+// launch of the prep kernel on every SM, so that the chains start at once).  They meet through counters in the workspace:
+// a chain starts segment k once prep_done[k] = n_prep (every record of the segment written), and
+// the prep writes segment k's records into its ring buffer once scan_done[k - ring] = n_scan (the
+// previous reader of that buffer is through).  A CTA that gives up a wait, or whose own bounded
+// waits run out, raises abort, and every other CTA stops at its next wait.
+struct SegPlan {
+    const int32_t *tables;   // [nseg][N + 1] record tables
+    uint8_t *rec;            // record buffers
+    int nseg, per, ring, linear;
+    size_t slot_records;     // records one ring buffer holds
+    int *prep_done, *scan_done;   // [nseg]
+    int *abort;
+    int n_scan, n_prep;
+    int first_seg;           // segments before it were prepared by an earlier launch on all SMs
+};
+constexpr uint32_t kSpinLimit = 1u << 23;              // polls of a cross-CTA wait (each >= 0.2 us)
+
+__device__ __forceinline__ int ld_acquire_gpu(const int *p) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void red_release_add_gpu(int *p, int v) {
+    asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+// Orders this thread's generic-proxy accesses to global memory with its async-proxy (bulk copy)
+// accesses on either side of the fence.
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+// One thread waits until *ctr >= target; false (abort raised) when the wait runs out or another
+// CTA has aborted.
+__device__ __forceinline__ bool wait_counter(const SegPlan *pl, const int *ctr, int target) {
+    for (uint32_t i = 0; i < kSpinLimit; ++i) {
+        if (ld_acquire_gpu(ctr) >= target) return true;
+        if (*reinterpret_cast<volatile const int *>(pl->abort) != 0) return false;
+        __nanosleep(200);
+    }
+    atomicExch(pl->abort, 1);
+    return false;
+}
+// record buffer of segment k
+__device__ __forceinline__ uint8_t *seg_records(const SegPlan *pl, int k, int H) {
+    return pl->rec + (pl->linear ? (size_t)k * pl->per * H : (size_t)(k % pl->ring) * pl->slot_records) * REC_BYTES;
+}
+
 // ============================ pass 1: chunk prep ============================
 struct PrepArgs {
     CUtensorMap tm_q, tm_k, tm_v, tm_g;   // [T, H, 128] (bf16 q, k, v; fp32 g), box min(64, T) tokens of one head
@@ -126,7 +175,9 @@ constexpr uint32_t kPrepTmemCols = 512;
 // MMA A result in [0, 128) (two halves summed: hi*hi + lo*hi | hi*lo), U^T and W^T likewise
 constexpr uint32_t kColUp = 128, kColWp = 256;
 
-__global__ void __launch_bounds__(kThreads, 1) kda_chunk_prep_kernel(const __grid_constant__ PrepArgs A) {
+// The prep of one segment (pl null: A's segment, CTA cta of ncta) or of every segment of the plan.
+template <bool kPersist>
+__device__ __forceinline__ void prep_body(const PrepArgs &A, const SegPlan *pl, int cta, int ncta) {
     extern __shared__ uint8_t smraw[];
     uint8_t *sm = smem_align1024(smraw);
     const PrefillArgs &a = A.p;
@@ -176,13 +227,39 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_prep_kernel(const __gri
         return !bad;
     };
 
+    // the segment in hand: its record table, first local chunk and record buffer
+    const int32_t *seg_off = A.seg_off;
+    int seg_lo = A.seg_lo;
+    uint8_t *seg_rec = A.rec;
+    int nq = 0;
+    int cur_h = -1;                                      // head whose conv weights are loaded
+    PhaseClock clk;   // phases: 0 staging wait, 1 prep q/k, 2 prep v (MMA A), 3 history + MMA A wait, 4 extract, 5 solve, 6 MMA U/W, 7 records out
+    const int nseg = kPersist ? pl->nseg : 1;
+    for (int k = kPersist ? pl->first_seg : 0; k < nseg; ++k) {
+    if (kPersist) {
+        seg_off = pl->tables + (size_t)k * (N + 1);
+        seg_lo = k * pl->per;
+        seg_rec = seg_records(pl, k, H);
+        // the buffer's previous reader, the scan of segment k - ring, must be through
+        if (!pl->linear && k >= pl->ring) {
+            if (tid == 0) {
+                if (!wait_counter(pl, pl->scan_done + (k - pl->ring), pl->n_scan)) {
+                    *sflag = 1;
+                    atomicOr(a.status, 1u);
+                }
+                fence_proxy_async_global();              // the bulk stores below follow the reads
+            }
+            __syncthreads();
+            if (*sflag) break;
+        }
+    }
     // Items in head-major order (head, chunk), each CTA taking a contiguous run of them: a CTA's
     // consecutive items are then mostly consecutive chunks of one head, whose conv history is the
     // previous chunk's last staged rows and whose conv weights are already loaded.
-    const int nq = A.seg_off[N];                         // records (chunks) of this segment
+    nq = seg_off[N];                                     // records (chunks) of this segment
     const long long total = (long long)nq * H;
-    const int m_lo = (int)(total * blockIdx.x / gridDim.x);
-    const int m_hi = (int)(total * (blockIdx.x + 1) / gridDim.x);
+    const int m_lo = (int)(total * cta / ncta);
+    const int m_hi = (int)(total * (cta + 1) / ncta);
     struct Item { int h, qc, n, tb, te, cs, qend; };   // qc: record; qend: one past the sequence's last record
     auto locate = [&](int m) {
         Item x;
@@ -191,12 +268,12 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_prep_kernel(const __gri
         int lo = 0, hi = N;                              // sequence n with off[n] <= qc < off[n + 1]
         while (hi - lo > 1) {
             const int mid = (lo + hi) >> 1;
-            if (A.seg_off[mid] <= x.qc) lo = mid; else hi = mid;
+            if (seg_off[mid] <= x.qc) lo = mid; else hi = mid;
         }
         x.n = lo;
         seq_bounds(a.cu, x.n, a.T, x.tb, x.te);
-        x.cs = x.tb + (A.seg_lo + x.qc - A.seg_off[x.n]) * kC;
-        x.qend = A.seg_off[x.n + 1];
+        x.cs = x.tb + (seg_lo + x.qc - seg_off[x.n]) * kC;
+        x.qend = seg_off[x.n + 1];
         return x;
     };
     // item m + 1 after item x = item m: the next chunk of the same sequence and head without
@@ -210,11 +287,10 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_prep_kernel(const __gri
         }
         return locate(m + 1);
     };
-    auto rec_of = [&](const Item &x) { return A.rec + ((size_t)x.qc * H + x.h) * REC_BYTES; };
+    auto rec_of = [&](const Item &x) { return seg_rec + ((size_t)x.qc * H + x.h) * REC_BYTES; };
     // conv weights of the item's head and its conv history (pre-conv q, k, v rows of tokens
     // cs-3 .. cs-1 from the inputs, or from the right-aligned initial conv state before the
     // sequence start), by all threads; the prep stages are their only readers
-    int cur_h = -1;
     auto load_history = [&](const Item &x) {
         if (W == 0) return;
         if (x.h != cur_h) {
@@ -265,7 +341,6 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_prep_kernel(const __gri
     // item's solve); q, k and v are staged a whole item ahead and need no prefetch
     auto prefetch_rows = [&](const Item &x) { tma_prefetch_3d(&A.tm_g, 0, x.h, x.cs); };
 
-    PhaseClock clk;   // phases: 0 staging wait, 1 prep q/k, 2 prep v (MMA A), 3 history + MMA A wait, 4 extract, 5 solve, 6 MMA U/W, 7 records out
     Item x, y;                                           // this item and the next
     if (m_lo < m_hi) {
         x = locate(m_lo);
@@ -406,6 +481,20 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_prep_kernel(const __gri
         tc_fence_after();
         clk.tick(7);
     }
+    if (kPersist) {
+        // the segment's records are written (the bulk stores complete, everyone's stores before
+        // the barrier): publish them
+        __syncthreads();
+        if (tid == 0) {
+            bulk_wait_all();
+            fence_proxy_async_global();
+            __threadfence();
+            if (*sflag) atomicExch(pl->abort, 1);
+            else red_release_add_gpu(pl->prep_done + k, 1);
+        }
+    }
+    if (*sflag) break;
+    }   // segments
     clk.flush(reinterpret_cast<unsigned long long *>(a.status) + 16);
     if (tid == 0) {
         bulk_wait_all();
@@ -416,6 +505,10 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_prep_kernel(const __gri
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tbase, kPrepTmemCols);
+}
+
+__global__ void __launch_bounds__(kThreads, 1) kda_chunk_prep_kernel(const __grid_constant__ PrepArgs A) {
+    prep_body<false>(A, nullptr, blockIdx.x, gridDim.x);
 }
 
 // ============================ pass 2: chunk scan ============================
@@ -482,12 +575,15 @@ constexpr int kIssueX = kThreads - 32, kIssueK = kThreads - 64;
 // chunk's state pass.  [W; Qh] and the gate rows (both double-buffered, two chunks ahead) and
 // [Aqk^T | Kd] arrive by bulk copies issued as soon as their buffers are free; U^T, rho and
 // G_last are read by the threads that use them, one chunk ahead, into registers.
-__global__ void __launch_bounds__(kThreads, 1) kda_chunk_scan_kernel(const __grid_constant__ ScanArgs A) {
+// The scan of one segment (pl null: A's segment, with the state carried in and out through
+// A.carry_S) or of every segment of the plan (the state staying in TMEM), for chain nh.
+template <bool kPersist>
+__device__ __forceinline__ void scan_body(const ScanArgs &A, const SegPlan *pl, int nh) {
     extern __shared__ uint8_t smraw[];
     uint8_t *sm = smem_align1024(smraw);
     const PrefillArgs &a = A.p;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int nh = blockIdx.x, n = nh / a.H, h = nh % a.H;
+    const int n = nh / a.H, h = nh % a.H;
     const int H = a.H;
     const uint32_t sbase = smem_u32(sm);
     float *sFA = reinterpret_cast<float *>(sm + Q_FA);
@@ -500,13 +596,18 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_scan_kernel(const __gri
 
     int tb, te;
     seq_bounds(a.cu, n, a.T, tb, te);
-    // this segment's chunks of the sequence: [c_begin, c_end) (local indices; records seg_off[n] ..);
-    // an empty sequence belongs to the first segment
-    const int q0 = A.seg_off[n];
     const int nq = (te - tb + kC - 1) / kC;
-    const int c_begin = A.seg_lo, c_end = A.seg_lo + (A.seg_off[n + 1] - q0);
-    if (c_begin >= c_end && !(nq == 0 && A.seg_lo == 0)) return;
-    const bool first = c_begin == 0, last = c_end == nq;
+    // the segment in hand: its record table, first local chunk and record buffer; this sequence's
+    // chunks in it are [c_begin, c_end) (local indices; records seg_off[n] ..)
+    const int32_t *seg_off = kPersist ? pl->tables : A.seg_off;
+    int seg_lo = kPersist ? 0 : A.seg_lo;
+    const uint8_t *seg_rec = kPersist ? seg_records(pl, 0, a.H) : A.rec;
+    int q0 = seg_off[n], c_begin = seg_lo, c_end = seg_lo + (seg_off[n + 1] - q0);
+    const int c_begin0 = c_begin;                         // the first segment's
+    // one launch per segment: an empty sequence belongs to the first segment, and a chain with no
+    // chunks in the segment has nothing to do
+    if (!kPersist && c_begin >= c_end && !(nq == 0 && seg_lo == 0)) return;
+    const bool first = kPersist || c_begin == 0, last = kPersist || c_end == nq;
     const int sn = seq_slot(a.slot, a.num_slots, n);           // state / conv-state row (-1: none)
     const size_t snh = (size_t)(sn < 0 ? 0 : sn) * a.H + h;
     const int W = A.W;
@@ -554,12 +655,14 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_scan_kernel(const __gri
         tmem_wait_st();
     }
 
-    auto rec_of = [&](int c) { return A.rec + ((size_t)(q0 + c - A.seg_lo) * H + h) * REC_BYTES; };
+    // record of local chunk c: chain_rec + c H REC_BYTES, chain_rec set per segment
+    const uint8_t *chain_rec = seg_rec + ((ptrdiff_t)(q0 - seg_lo) * H + h) * (ptrdiff_t)REC_BYTES;
+    auto rec_of = [&](int c) { return chain_rec + (ptrdiff_t)c * H * (ptrdiff_t)REC_BYTES; };
     // thread 0's view of the outstanding asynchronous operations
     uint32_t aph = 0, kph = 0, xph0 = 0, xph1 = 0, gph0 = 0, gph1 = 0;
     bool pend_a = false, pend_k = false, pend_x0 = false, pend_x1 = false, pend_g0 = false, pend_g1 = false;
     // test hook: CTA 0 issues no copy of its first [W; Qh] tile and gives up that wait early
-    const bool tskip = a.test_limit != 0 && blockIdx.x == 0 && c_begin < c_end;
+    const bool tskip = a.test_limit != 0 && nh == 0 && c_begin < c_end;
     uint32_t xlim = tskip ? a.test_limit : kWaitLimit;
     auto wait_on = [&](uint32_t bar, uint32_t &ph, bool &pend, uint32_t lim = kWaitLimit) -> bool {
         if (!pend) return true;
@@ -612,7 +715,9 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_scan_kernel(const __gri
     // buffer c & 1 is the number of earlier loads into it, mod 2
     auto gate_ready = [&](int c) {
         const int b = c & 1;
-        const int first_b = c_begin + ((b - c_begin) & 1);
+        // every chunk from the first one of the launch loads its rows into buffer c & 1, in order
+        const int c0 = kPersist ? 0 : c_begin;
+        const int first_b = c0 + ((b - c0) & 1);
         mbar_wait_bounded(b ? mb_g1 : mb_g0, (uint32_t)(((c - first_b) >> 1) & 1), kWaitLimit);
     };
     auto mma_wait = [&]() -> bool {
@@ -630,14 +735,14 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_scan_kernel(const __gri
         const uint8_t *p = rec_of(c) + REC_U;
 #pragma unroll
         for (int t = 0; t < 4; ++t) {
-            const float4 v = __ldg(reinterpret_cast<const float4 *>(p + u_off(j, quarter * 16 + 4 * t)));
+            const float4 v = __ldcg(reinterpret_cast<const float4 *>(p + u_off(j, quarter * 16 + 4 * t)));
             uR[4 * t] = v.x; uR[4 * t + 1] = v.y; uR[4 * t + 2] = v.z; uR[4 * t + 3] = v.w;
         }
     };
     auto load_vec = [&](int c) {
         const float *p = reinterpret_cast<const float *>(rec_of(c) + REC_VEC);
-        rN = __ldg(p + vt);
-        glN = __ldg(p + kD + vt);
+        rN = __ldcg(p + vt);
+        glN = __ldcg(p + kD + vt);
     };
     // the state pass of a chunk: S'^T = S^T diag(exp(rho)) as split bf16 (the A operand of MMA W/Qh),
     // and the fp32 accumulator S^T <- S^T diag(exp(G_last)), onto which MMA O/S adds V'^T Kd
@@ -675,10 +780,34 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_scan_kernel(const __gri
 
     bool failed = false;
     PhaseClock clk;   // phases: 0 MMA W, 1 V' tile, 2 MMA O/S, 3 epilogue + next state pass
+    const int nseg = kPersist ? pl->nseg : 1;
+    for (int k = 0; k < nseg; ++k) {
+    if (kPersist) {
+        if (k > 0) {
+            const int32_t *off = pl->tables + (size_t)k * (a.N + 1);
+            c_begin = k * pl->per;
+            c_end = c_begin + (off[n + 1] - off[n]);
+            chain_rec = seg_records(pl, k, H) + ((ptrdiff_t)(off[n] - c_begin) * H + h) * (ptrdiff_t)REC_BYTES;
+        }
+        // every record of the segment is written (by this launch's prep CTAs, or before it); the
+        // bulk copies below read them
+        if (tid == 0) {
+            if (k >= pl->first_seg && !wait_counter(pl, pl->prep_done + k, pl->n_prep)) {
+                *sflag = 1;
+                atomicOr(a.status, 1u);
+            }
+            fence_proxy_async_global();
+        }
+        __syncthreads();
+        if (*sflag) {
+            failed = true;
+            break;
+        }
+    }
     if (c_begin < c_end) {
         const int c = c_begin;
         if (tid == 0) {
-            if (!tskip) load_x(c);
+            if (!(tskip && k == 0)) load_x(c);
             else if (c & 1) pend_x1 = true;
             else pend_x0 = true;
             load(mb_k, REC_B, REC_B, c, 49152, pend_k);     // [Aqk^T | Kb] hi, lo
@@ -837,6 +966,13 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_scan_kernel(const __gri
         }
         clk.tick(3);
     }
+    if (kPersist && tid == 0) {
+        // the segment's records have all been read (copies landed, U rows in registers and used)
+        if (failed) atomicExch(pl->abort, 1);
+        else red_release_add_gpu(pl->scan_done + k, 1);
+    }
+    if (failed) break;
+    }   // segments
     clk.flush(reinterpret_cast<unsigned long long *>(a.status) + 8);
     if (!failed && !last) {
         tc_fence_after();
@@ -894,7 +1030,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_scan_kernel(const __gri
     if (tid == 0) {
         bulk_wait_all();                                 // output tiles written
         if (tskip) {                                     // the starved tile was never requested
-            if (c_begin & 1) pend_x1 = false;
+            if (c_begin0 & 1) pend_x1 = false;
             else pend_x0 = false;
         }
         // after a failure, let what is still in flight land before the CTA exits
@@ -910,28 +1046,49 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_scan_kernel(const __gri
     if (warp == 0) tmem_dealloc(tbase, kScanTmemCols);
 }
 
+__global__ void __launch_bounds__(kThreads, 1) kda_chunk_scan_kernel(const __grid_constant__ ScanArgs A) {
+    // the prep of the next segment, launched as a programmatic dependent, may start beside this
+    // scan: it reads only inputs and writes the ring buffer that the scan before this one read
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    scan_body<false>(A, nullptr, blockIdx.x);
+}
+
+// The segments of an overlap-shape call in one cooperative launch: n_scan CTAs run the scan chains,
+// the rest the prep of segments first_seg.. (see SegPlan).
+struct SegmentsArgs {
+    PrepArgs P;
+    ScanArgs S;
+    SegPlan plan;
+};
+__global__ void __launch_bounds__(kThreads, 1) kda_prefill_segments_kernel(const __grid_constant__ SegmentsArgs A) {
+    // the chains are the last n_scan CTAs: with one CTA per SM these fill whole TPCs (SM pairs), so
+    // that no chain shares its TPC with a prep CTA (a chain beside a prep CTA slows both)
+    const int b = blockIdx.x;
+    if (b >= A.plan.n_prep) scan_body<true>(A.S, &A.plan, b - A.plan.n_prep);
+    else prep_body<true>(A.P, &A.plan, b, A.plan.n_prep);
+}
+
 size_t max_chunks(int N, int T) { return ((size_t)T + 63u * (size_t)N) / kC; }
 size_t round256_(size_t b) { return (b + 255) & ~size_t(255); }
 
-// Segmented pipeline.  A call runs in segments of `per` local chunks of every sequence: the prep
-// pass of segment k + 1 (caller's stream) overlaps the scan of segment k (a high-priority side
-// stream of the library), ordered by events only, and the scan hands each chain's state from one
-// segment's launch to the next through the carry buffer.  Segments write their records into a ring
-// of buffers, so the workspace does not grow with T: segment k's prep waits for the scan of segment
-// k - ring, the last reader of its buffer.  Three shapes:
+// Segmented calls.  A call runs in segments of `per` local chunks of every sequence, whose records
+// go to a ring of buffers, so the workspace does not grow with T.  Three shapes:
 //   one segment  few chunks in all: every record has its own place, prep then scan;
-//   overlap      few (sequence, head) chains (<= 64) with >= 128 chunks: the scan leaves most SMs
-//                to the prep, segments of ~64 chunks whose items fill whole waves of the prep grid,
-//                a ring of three;
+//   overlap      few (sequence, head) chains (<= 64) with >= 128 chunks: one cooperative launch in
+//                which the chains run beside the prep of the following segments (kda_prefill_
+//                segments_kernel), segments of ~64 chunks whose items fill whole waves of the prep
+//                CTAs, a ring of three, the chains' states staying in TMEM;
 //   bounded      many chains whose records would exceed kRecordBudget: segments as long as a ring
 //                of two within the budget allows, all sequences advancing together (the longest
 //                sets the number of segments; with a host copy of cu_seqlens it is exact, else the
-//                bound ceil(T / 64) is used and the segments past the longest sequence are empty).
+//                bound ceil(T / 64) is used and the segments past the longest sequence are empty),
+//                prep then scan per segment on the caller's stream, each prep a programmatic
+//                dependent of the scan before it so that the two overlap, the chains' states
+//                handed from one scan launch to the next through the carry buffer.
+// Everything runs on the caller's stream; the library keeps no stream or event of its own.
 constexpr int kSegChunks = 64;
 constexpr int kMaxSegsOverlap = 64;
 constexpr size_t kRecordBudget = size_t(5) << 28;       // 1.25 GiB of records in the bounded shape
-constexpr int kEvents = 8;                              // event ring (more than the record ring)
-constexpr int kMaxDevices = 64;
 size_t carry_bytes(int N, int H) { return (size_t)N * H * kD * kD * sizeof(float); }
 
 struct SegShape {
@@ -971,47 +1128,17 @@ SegShape seg_shape(int N, int T, int H) {
     return sh;
 }
 size_t tables_bytes(const SegShape &sh, int N) { return round256_((size_t)sh.nseg_max * (N + 1) * sizeof(int32_t)); }
-
-struct SideStream {
-    std::mutex enqueue;                  // one call's launches and event records at a time
-    cudaStream_t stream = nullptr;
-    cudaEvent_t ev[kEvents + 1] = {};    // prep of segment k done, by k mod kEvents; [kEvents]: all scans done
-    cudaEvent_t ev_scan[kEvents] = {};   // scan of segment k done (its ring buffer may be rewritten)
-    bool ready = false;
-};
-std::mutex g_side_mu;
-SideStream g_side[kMaxDevices];
-
-cudaError_t side_stream(SideStream **out) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-    std::lock_guard<std::mutex> lock(g_side_mu);
-    SideStream &ss = g_side[dev];
-    if (!ss.ready) {
-        int lo = 0, hi = 0;
-        if ((e = cudaDeviceGetStreamPriorityRange(&lo, &hi)) != cudaSuccess ||
-            (e = cudaStreamCreateWithPriority(&ss.stream, cudaStreamNonBlocking, hi)) != cudaSuccess)
-            return e;
-        for (int i = 0; i <= kEvents; ++i)
-            if ((e = cudaEventCreateWithFlags(&ss.ev[i], cudaEventDisableTiming)) != cudaSuccess) return e;
-        for (int i = 0; i < kEvents; ++i)
-            if ((e = cudaEventCreateWithFlags(&ss.ev_scan[i], cudaEventDisableTiming)) != cudaSuccess) return e;
-        ss.ready = true;
-    }
-    *out = &ss;
-    return cudaSuccess;
-}
+// prep_done[nseg_max], scan_done[nseg_max], abort
+size_t counters_bytes(const SegShape &sh) { return round256_(((size_t)2 * sh.nseg_max + 1) * sizeof(int)); }
 
 }  // namespace
 
 // Workspace of the two-pass path (after the status word): the segments' record tables, then for a
-// segmented call the scan's state carry, then the ring of record buffers (one buffer holding every
-// record when the call is one segment).
+// segmented call the segment counters and the scan's state carry, then the ring of record buffers
+// (one buffer holding every record when the call is one segment).
 size_t tc_split_workspace(int N, int T, int H) {
     const SegShape sh = seg_shape(N, T, H);
-    return tables_bytes(sh, N) + (sh.mode ? round256_(carry_bytes(N, H)) : 0) +
+    return tables_bytes(sh, N) + (sh.mode ? counters_bytes(sh) + round256_(carry_bytes(N, H)) : 0) +
            (size_t)sh.ring * sh.slot_records * REC_BYTES;
 }
 
@@ -1023,16 +1150,21 @@ cudaError_t launch_prefill_tc_split(const PrefillArgs &p, const float *conv_w, f
     int32_t *tables = reinterpret_cast<int32_t *>(w);
     w += tables_bytes(sh, p.N);
     float *carry_S = nullptr;
+    int *counters = nullptr;
     if (sh.mode) {
+        counters = reinterpret_cast<int *>(w);
+        w += counters_bytes(sh);
         carry_S = reinterpret_cast<float *>(w);
         w += round256_(carry_bytes(p.N, p.H));
     }
     uint8_t *rec = w;
     const int box_rows = p.T < kC ? p.T : kC;
     cudaError_t e;
-    static std::atomic<uint64_t> prep_attr{0}, scan_attr{0};
+    static std::atomic<uint64_t> prep_attr{0}, scan_attr{0}, seg_attr{0};
+    constexpr size_t kSegmentsSmem = kSmemBytes > kScanSmemBytes ? kSmemBytes : kScanSmemBytes;
     if ((e = smem_attr_once((const void *)kda_chunk_prep_kernel, (int)kSmemBytes, prep_attr)) != cudaSuccess ||
-        (e = smem_attr_once((const void *)kda_chunk_scan_kernel, (int)kScanSmemBytes, scan_attr)) != cudaSuccess)
+        (e = smem_attr_once((const void *)kda_chunk_scan_kernel, (int)kScanSmemBytes, scan_attr)) != cudaSuccess ||
+        (e = smem_attr_once((const void *)kda_prefill_segments_kernel, (int)kSegmentsSmem, seg_attr)) != cudaSuccess)
         return e;
     int dev = 0, sms = 0;
     if ((e = cudaGetDevice(&dev)) != cudaSuccess ||
@@ -1110,12 +1242,23 @@ cudaError_t launch_prefill_tc_split(const PrefillArgs &p, const float *conv_w, f
         P.rec = rec + (sh.linear ? (size_t)k * per * p.H : (size_t)(k % sh.ring) * sh.slot_records) * REC_BYTES;
         S.rec = P.rec;
     };
-    auto prep = [&](int max_ctas, cudaStream_t st) -> cudaError_t {
+    // overlap: launch as a programmatic dependent of the scan launched before it on the stream
+    auto prep = [&](int max_ctas, cudaStream_t st, bool overlap = false) -> cudaError_t {
         const unsigned grid = (unsigned)std::min<size_t>(sh.slot_records, (size_t)max_ctas);
         if (grid == 0) return cudaSuccess;
-        kda_chunk_prep_kernel<<<grid, kThreads, kSmemBytes, st>>>(P);
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(grid);
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = kSmemBytes;
+        cfg.stream = st;
+        cudaLaunchAttribute at[1];
+        at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        at[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = at;
+        cfg.numAttrs = overlap ? 1 : 0;
+        cudaError_t err = cudaLaunchKernelEx(&cfg, kda_chunk_prep_kernel, P);
         count_launch();
-        return cudaGetLastError();
+        return err != cudaSuccess ? err : cudaGetLastError();
     };
     auto scan = [&](int k, cudaStream_t st) -> cudaError_t {
         S.p.test_limit = k == 0 ? take_test_timeout(kTestScan) : 0u;
@@ -1128,24 +1271,51 @@ cudaError_t launch_prefill_tc_split(const PrefillArgs &p, const float *conv_w, f
         if (qmax > 0 && (e = prep(sms, s)) != cudaSuccess) return e;
         return scan(0, s);
     }
-    SideStream *side = nullptr;
-    if ((e = side_stream(&side)) != cudaSuccess) return e;
-    // The events are shared by every call on this device: a concurrent call recording them between
-    // this call's record and wait would order this call's scans after the wrong prep launches.
-    std::lock_guard<std::mutex> enqueue_lock(side->enqueue);
+    if (sh.mode == 1) {
+        // one cooperative launch, when every CTA of it can be resident at once
+        int coop = 0, per_sm = 0;
+        const int n_scan = p.N * p.H;
+        if ((e = cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev)) != cudaSuccess ||
+            (e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kda_prefill_segments_kernel, kThreads,
+                                                               kSegmentsSmem)) != cudaSuccess)
+            return e;
+        if (coop && per_sm >= 1 && n_scan < sms) {
+            if ((e = cudaMemsetAsync(counters, 0, counters_bytes(sh), s)) != cudaSuccess) return e;
+            set_segment(0);
+            if ((e = prep(sms, s)) != cudaSuccess) return e;
+            SegmentsArgs X;
+            X.P = P;
+            X.S = S;
+            X.S.p.test_limit = take_test_timeout(kTestScan);
+            X.plan.tables = tables;
+            X.plan.rec = rec;
+            X.plan.nseg = nseg;
+            X.plan.per = per;
+            X.plan.ring = sh.ring;
+            X.plan.linear = sh.linear ? 1 : 0;
+            X.plan.slot_records = sh.slot_records;
+            X.plan.prep_done = counters;
+            X.plan.scan_done = counters + sh.nseg_max;
+            X.plan.abort = counters + 2 * sh.nseg_max;
+            X.plan.n_scan = n_scan;
+            X.plan.n_prep = sms - n_scan;
+            X.plan.first_seg = 1;
+            void *args[] = {&X};
+            e = cudaLaunchCooperativeKernel((const void *)kda_prefill_segments_kernel, dim3((unsigned)sms),
+                                            dim3(kThreads), args, kSegmentsSmem, s);
+            count_launch();
+            return e;
+        }
+    }
+    // segment by segment on the caller's stream, the prep of segment k + 1 beside the scan of segment
+    // k: it is a programmatic dependent of that scan, and stream order still puts every scan after
+    // its own prep and after the scan before it, so a ring buffer (two or three) is rewritten only
+    // once the scan that read it has finished
     for (int k = 0; k < nseg; ++k) {
         set_segment(k);
-        if ((!sh.linear && k >= sh.ring &&
-             (e = cudaStreamWaitEvent(s, side->ev_scan[(k - sh.ring) % kEvents], 0)) != cudaSuccess) ||
-            (e = prep(k == 0 ? sms : prep_ctas, s)) != cudaSuccess ||
-            (e = cudaEventRecord(side->ev[k % kEvents], s)) != cudaSuccess ||
-            (e = cudaStreamWaitEvent(side->stream, side->ev[k % kEvents], 0)) != cudaSuccess ||
-            (e = scan(k, side->stream)) != cudaSuccess ||
-            (e = cudaEventRecord(side->ev_scan[k % kEvents], side->stream)) != cudaSuccess)
-            return e;
+        if ((e = prep(sms, s, k > 0)) != cudaSuccess || (e = scan(k, s)) != cudaSuccess) return e;
     }
-    if ((e = cudaEventRecord(side->ev[kEvents], side->stream)) != cudaSuccess) return e;
-    return cudaStreamWaitEvent(s, side->ev[kEvents], 0);
+    return cudaSuccess;
 }
 
 }  // namespace k3kda

@@ -177,11 +177,15 @@ size_t k3kda_prefill_workspace_min(int N, int T, int H, int dk, int dv, int chun
  * sequence and head that carries the state); with less, one single-pass kernel
  * per sequence and head.  Every other supported shape runs an FP32 CUDA-core
  * chunked kernel.  All compute the same chunked algebra.
- * With few (sequence, head) pairs (N*H <= 64) and at least 128 chunks the two
- * passes run as a pipeline of chunk segments: the scan launches go to one
- * high-priority stream per device that the library creates on first use and
- * joins back to `stream` with events (so stream capture sees one fork/join);
- * calls from several host threads are enqueued one after another there.
+ * Long inputs run the two passes as a pipeline of chunk segments whose records
+ * go to a ring of buffers in the workspace.  With few (sequence, head) pairs
+ * (N*H <= 64) and at least 128 chunks the whole pipeline is one cooperative
+ * launch that takes every SM: N*H of its CTAs carry the states while the others
+ * prepare the following segments, ordered by counters in the workspace (every
+ * wait bounded); with many pairs each segment's prep is a programmatic
+ * dependent of the previous segment's scan.  Everything runs on `stream`: the
+ * library creates no stream or event, and calls on different streams are
+ * independent (two cooperative launches run one after the other).
  * Errors: INVALID_ARG, UNSUPPORTED, ALIGNMENT, WORKSPACE, CUDA as above.
  * A bounded in-kernel wait that gives up records K3KDA_ERR_TIMEOUT in the
  * workspace status word (see k3kda_workspace_status) instead of hanging.

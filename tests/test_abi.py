@@ -54,23 +54,27 @@ def test_workspace_size_is_aligned_and_grows_with_conv(lib):
     e = K.k3kda_prefill_workspace_size(3, 1000, 2, 128, 128, 64, K.BF16, True)
     assert e == 256 + 256 + ((1000 + 63 * 3) // 64) * 2 * 148480
     # long sequences with few (sequence, head) pairs: the segments' record tables (int32 [N + 1] for
-    # each of at most ceil(chunks / 48) segments), the scan's state carry (65,536 B per sequence and
-    # head) and a ring of three segments' records (80 chunks, or chunks / 64 beyond 64 segments),
-    # independent of T; all records when they take less room than the ring
+    # each of at most ceil(chunks / 48) segments), the segment counters (int32: two per segment and
+    # an abort word), the scan's state carry (65,536 B per sequence and head) and a ring of three
+    # segments' records (80 chunks, or chunks / 64 beyond 64 segments), independent of T; all
+    # records when they take less room than the ring
     carry = 32 * 65536
     r256 = lambda b: (b + 255) // 256 * 256
     ring = lambda chunks: min(chunks, 3 * max(80, -(-chunks // 64))) * 32 * 148480
     for T in (8192, 65536, 1 << 18, 1 << 21):
         chunks = T // 64
-        tables = r256(-(-chunks // 48) * 2 * 4)
-        assert K.k3kda_prefill_workspace_size(1, T, 32, 128, 128, 64, K.BF16, True) == 256 + tables + carry + ring(chunks)
+        nseg = -(-chunks // 48)
+        tables, counters = r256(nseg * 2 * 4), r256((2 * nseg + 1) * 4)
+        want = 256 + tables + counters + carry + ring(chunks)
+        assert K.k3kda_prefill_workspace_size(1, T, 32, 128, 128, 64, K.BF16, True) == want
     # many (sequence, head) chains whose records would exceed 1.25 GiB: a ring of two buffers of
     # `per` local chunks of every sequence, per = 1.25 GiB / (2 N H 148480 B); the 16-sequence varlen
     # workload (135,937 tokens) fits in 1.3 GB instead of 10.2 GB
     N, T, H = 16, 135937, 32
     per = (5 << 28) // (2 * N * H * 148480)
-    tables = r256(-(-((T + 63) // 64) // per) * (N + 1) * 4)
-    want = 256 + tables + N * H * 65536 + 2 * min(N * per, (T + 63 * N) // 64) * H * 148480
+    nseg = -(-((T + 63) // 64) // per)
+    tables, counters = r256(nseg * (N + 1) * 4), r256((2 * nseg + 1) * 4)
+    want = 256 + tables + counters + N * H * 65536 + 2 * min(N * per, (T + 63 * N) // 64) * H * 148480
     got = K.k3kda_prefill_workspace_size(N, T, H, 128, 128, 64, K.BF16, True)
     assert got == want and got < 1.5e9
     c = K.k3kda_prefill_workspace_size(1, 1024, 4, 64, 128, 64, K.BF16, False)

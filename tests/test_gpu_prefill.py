@@ -153,9 +153,9 @@ def test_two_pass_segmented_single_long_sequence():
 
 
 def test_two_pass_pipeline_from_two_host_threads():
-    """Two host threads, each on its own stream, run the segmented pipeline (which shares the
-    library's side stream and events per device) repeatedly; every result must equal a run made
-    alone, bit for bit."""
+    """Two host threads, each on its own stream, run the segmented call (one cooperative launch
+    that takes every SM, so two of them run one after the other) repeatedly; every result must
+    equal a run made alone, bit for bit."""
     import threading
     cases = [KI.fused_mixer(seed=50 + i, T=8300, H=1) for i in range(2)]
     devs = [case_to_device(c) for c in cases]

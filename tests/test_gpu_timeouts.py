@@ -57,6 +57,28 @@ def test_prefill_wait_runs_out_then_recovers(which):
     assert_close(to_np(fs), rs, False, "final state after a timed-out call")
 
 
+def test_segmented_launch_wait_runs_out_then_recovers():
+    """One long sequence in segments (320 chunks: four segments of 80 in a ring of three), all in
+    one launch in which the scan chains and the prep CTAs wait on one another's counters.  The
+    chain's first tile is starved: it gives up, raises the abort word, and the prep CTAs waiting
+    for that chain to free a ring buffer stop too; the call reports the timeout once and the next
+    call is exact."""
+    c = KI.prefill_case("timeout_seg", [20480], 1, 128, 128, 64, "bf16", seed=82, s0_std=0.02, gate=True)
+    d = case_to_device(c)
+    size = K.k3kda_prefill_workspace_size(c.N, c.T, c.H, 128, 128, 64, K.BF16, False)
+    ws = torch.zeros(size, dtype=torch.uint8, device="cuda")
+    out = torch.zeros((c.T, c.H, 128), device="cuda")
+    _arm(SCAN)
+    _prefill(c, d, ws, out)
+    assert K.k3kda_workspace_status(ws) == TIMEOUT
+    assert K.k3kda_workspace_status(ws) == 0
+    fs = _prefill(c, d, ws, out)
+    assert K.k3kda_workspace_status(ws) == 0
+    ro, rs, _ = oracle_prefill(c)
+    assert_close(to_np(out), ro, False, "out after a timed-out segmented call")
+    assert_close(to_np(fs), rs, False, "final state after a timed-out segmented call")
+
+
 def test_decode_wait_runs_out_then_recovers():
     dc = KI.decode_case(seed=81, N=2, H=2, d=128)
     dev = lambda x, bf=False: torch.from_numpy(np.ascontiguousarray(x)).to(torch.bfloat16 if bf else torch.float32).cuda()
