@@ -296,25 +296,22 @@ __device__ __forceinline__ void forward_chain(const CbArgs &A, uint8_t *dyn, int
     const int q0 = A.chunk_off[n], nq = A.chunk_off[n + 1] - q0;
     // Delta elements (di, dj) and (di, dj + 16)
     const int di = tid / 16, dj = tid % 16;
-    // one commit group per chunk (empty past the end), kFS - 1 chunks ahead
-    for (int d = 0; d < kFS - 1; ++d) {
-        if (d < nq) stage_fwd(A, stg[d], (size_t)(q0 + d) * H + h, cb);
-        else cp_commit();
-    }
+    // one commit group per chunk, issued one chunk ahead; S transposed in sSpT for each chunk's Delta
+    if (nq > 0) stage_fwd(A, stg[0], (size_t)q0 * H + h, cb);
+#pragma unroll
+    for (int u = 0; u < 16; ++u) sSpT[c0 + u][r] = S[u];
     for (int c = 0; c <= nq; ++c) {
         float *stp = A.St + ((size_t)(q0 + c + n) * H + h) * kD * kD + (size_t)r * kD + cb + c0;
 #pragma unroll
         for (int u = 0; u < 16; u += 4) *reinterpret_cast<float4 *>(stp + u) = make_float4(S[u], S[u + 1], S[u + 2], S[u + 3]);
         if (c == nq) break;
         const size_t item = (size_t)(q0 + c) * H + h;
-        if (c + kFS - 1 < nq) stage_fwd(A, stg[(c + kFS - 1) % kFS], item + (size_t)(kFS - 1) * H, cb);
-        else cp_commit();
-        cp_wait<kFS - 1>();
+        cp_wait<0>();
         const FwdStage &st = stg[c % kFS];
-        __syncthreads();                               // chunk c's tiles are in
-#pragma unroll
-        for (int u = 0; u < 16; ++u) sSpT[c0 + u][r] = S[u];
+        // chunk c's tiles and S_c (sSpT) are in, and every thread is through chunk c - 1: its
+        // stage buffer may take chunk c + 1
         __syncthreads();
+        if (c + 1 < nq) stage_fwd(A, stg[(c + 1) % kFS], item + (size_t)H, cb);
         {
             const float *w = st.W[di], *x0 = sSpT[dj], *x1 = sSpT[dj + 16];
             float a0 = 0.f, a1 = 0.f;
@@ -350,8 +347,10 @@ __device__ __forceinline__ void forward_chain(const CbArgs &A, uint8_t *dyn, int
             }
         }
 #pragma unroll
-        for (int u = 0; u < 16; ++u) S[u] = acc[u];
-        __syncthreads();                               // buffer c % kFS is refilled for chunk c + kFS
+        for (int u = 0; u < 16; ++u) {
+            S[u] = acc[u];
+            sSpT[c0 + u][r] = acc[u];                  // S_{c+1} for the next chunk's Delta
+        }
     }
 }
 
@@ -410,32 +409,26 @@ __device__ __forceinline__ void backward_chain(const CbArgs &A, uint8_t *dyn, in
     for (int u = 0; u < 8; ++u) Dout[u] = A.dSfin ? A.dSfin[((size_t)nh * kD + r) * kD + cb + c0 + u] : 0.f;
     const int q0 = A.chunk_off[n], nq = A.chunk_off[n + 1] - q0;
     const int di = tid / kBV, dj = tid % kBV;
-    // chunk j of the sweep is c = nq - 1 - j; one commit group per chunk (empty past the end)
-    for (int d = 0; d < kCS - 1; ++d) {
-        const int cc = nq - 1 - d;
-        if (cc >= 0) stage_chain(A, stg[d], (size_t)(q0 + cc) * H + h, q0 + cc, h, cb);
-        else cp_commit();
-    }
+    // chunk j of the sweep is c = nq - 1 - j; one commit group per chunk, issued one chunk ahead;
+    // Dout transposed in sdXT for each chunk's dDelta
+    if (nq > 0) stage_chain(A, stg[0], (size_t)(q0 + nq - 1) * H + h, q0 + nq - 1, h, cb);
+#pragma unroll
+    for (int u = 0; u < 8; ++u) sdXT[c0 + u][r] = Dout[u];
     for (int j = 0; j < nq; ++j) {
         const int c = nq - 1 - j;
         const size_t item = (size_t)(q0 + c) * H + h, tile = item * kC * kD;
-        {
-            const int cc = c - (kCS - 1);
-            if (cc >= 0) stage_chain(A, stg[(j + kCS - 1) % kCS], (size_t)(q0 + cc) * H + h, q0 + cc, h, cb);
-            else cp_commit();
-        }
-        cp_wait<kCS - 1>();
-        const ChainStage &st = stg[j % kCS];
-        __syncthreads();                               // chunk c's tiles are in
-#pragma unroll
-        for (int u = 0; u < 8; ++u) sdXT[c0 + u][r] = Dout[u];
         {
             float *dng = A.Dn + item * kD * kD + (size_t)r * kD + cb + c0;
 #pragma unroll
             for (int u = 0; u < 8; u += 4)
                 *reinterpret_cast<float4 *>(dng + u) = make_float4(Dout[u], Dout[u + 1], Dout[u + 2], Dout[u + 3]);
         }
+        cp_wait<0>();
+        const ChainStage &st = stg[j % kCS];
+        // chunk c's tiles and its Dout (sdXT) are in, and every thread is through the chunk before:
+        // its stage buffer may take chunk c - 1
         __syncthreads();
+        if (c >= 1) stage_chain(A, stg[(j + 1) % kCS], (size_t)(q0 + c - 1) * H + h, q0 + c - 1, h, cb);
         // dDelta = Kd Dout + Aqk^T dOs
         {
             const float *kh = st.Kd[di], *xt = sdXT[dj];   // row di of Kd, column dj of Dout
@@ -478,8 +471,10 @@ __device__ __forceinline__ void backward_chain(const CbArgs &A, uint8_t *dyn, in
             }
         }
 #pragma unroll
-        for (int u = 0; u < 8; ++u) Dout[u] = acc[u];
-        __syncthreads();                               // buffer j % kCS is refilled for chunk c - kCS
+        for (int u = 0; u < 8; ++u) {
+            Dout[u] = acc[u];
+            sdXT[c0 + u][r] = acc[u];                  // the next chunk's Dout for its dDelta
+        }
     }
     float *d0 = A.dS0 + ((size_t)nh * kD + r) * kD + cb + c0;
 #pragma unroll
