@@ -195,6 +195,17 @@ def test_two_pass_segment_ring_wraps():
     _check(KI.fused_mixer(seed=42, T=19200, H=1))
 
 
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
+def test_one_launch_segments_many_chains_ring_wraps(out_dtype):
+    """Three sequences of 313, 141 and 3 chunks over 8 heads (24 chains, 458 chunks in all): the
+    segmented call is one cooperative launch whose 24 chains run beside the prep CTAs through
+    a ring of three segment buffers that wraps, the sequences ending in different segments, with
+    initial states, conv state and gate.  Checked on three heads (heads never interact)."""
+    c = KI.prefill_case("one_launch_ring", [20000, 9000, 130], 8, 128, 128, 64, "bf16", seed=43, s0_std=0.02,
+                        gate=True, conv_width=4, conv_state=True)
+    _check(c, out_dtype=out_dtype, heads=[0, 3, 7])
+
+
 @pytest.mark.parametrize("host_lengths", [True, False], ids=["host_cu_seqlens", "device_only"])
 def test_two_pass_bounded_segments_many_chains(host_lengths):
     """Many (sequence, head) chains whose records would exceed the record budget (4 sequences x 32

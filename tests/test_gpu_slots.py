@@ -126,6 +126,8 @@ CASES = {
     "tensor_core_two_pass": dict(lengths=[100, 7, 190], dk=128, min_ws=False),
     "tensor_core_single_pass": dict(lengths=[100, 7, 190], dk=128, min_ws=True),
     "tensor_core_segmented": dict(lengths=[4100, 4200, 70], dk=128, min_ws=False),
+    # 250, 66 and 2 chunks: the one-launch segmented path with its record ring wrapping
+    "tensor_core_one_launch": dict(lengths=[16000, 4200, 70], dk=128, min_ws=False),
     "fp32_path": dict(lengths=[77, 3, 123], dk=64, min_ws=False),
 }
 
