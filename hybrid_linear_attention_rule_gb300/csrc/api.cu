@@ -287,8 +287,8 @@ int k3kda_backward(const void *q, const void *k, const void *v, int in_dtype, co
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     char *ws = static_cast<char *>(workspace);
     return cuda_status(launch_backward_chunked(q, k, v, in_dtype == K3KDA_BF16, g, beta, initial_state, cu_seqlens, N, T, H,
-                                       scale, dO, dS_final, dq, dk_out, dv_out, dg, dbeta, dS0, ws + kStatusBytes,
-                                       s));
+                                       scale, dO, dS_final, dq, dk_out, dv_out, dg, dbeta, dS0,
+                                       reinterpret_cast<unsigned *>(ws), ws + kStatusBytes, s));
 }
 
 int k3kda_workspace_status(void *workspace, void *stream) {

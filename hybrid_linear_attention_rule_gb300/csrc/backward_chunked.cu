@@ -27,31 +27,30 @@
 // element by element instead of factoring it through a reference.  Launches, after the chunk table
 // (its offsets per sequence, then first token, length and sequence of each chunk):
 //   1. prep    one CTA per (chunk, head): the tiles above, Tm by forward substitution;
-//   2. forward one CTA per (sequence, head, 32-column block of dv): the states at chunk starts;
-//   3. chain   one CTA per (sequence, head, 16-column block), chunks in reverse: Dout, dR and Din,
-//              with dS0 at the sequence start; it needs no forward state, so 2 and 3 are one
-//              launch whose CTAs run side by side;
+//   2. forward one CTA per (sequence, head): the states at chunk starts and Delta;
+//   3. chain   one CTA per (sequence, head), chunks in reverse: Dout, dR and Din, with dS0 at the
+//              sequence start; it needs no forward state, so 2 and 3 are one launch whose CTAs
+//              run side by side;
 //   4. grads   two CTAs per (chunk, head), one per half of the dk columns: dq, dk, dv, dg and
 //              each half's share of dbeta.
-// Everything runs in fp32 on CUDA cores; chunks of 16 tokens keep the products short.
+// Prep and grads run in fp32 on CUDA cores; the two chains keep their carried matrix in tensor
+// memory and run their products on the tensor cores (kind::tf32, operands split in two parts).
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 
 #include <atomic>
 
 #include "common.cuh"
+#include "tc_ptx.cuh"
 
 namespace k3kda {
 namespace {
 
 constexpr int kD = 128;
 constexpr int kC = 16;             // tokens per chunk
-constexpr int kBV = 16;            // dv columns of a chain CTA
-constexpr int kNV = kD / kBV;      // chain CTAs per (sequence, head)
 constexpr int kThreads = 256;
 constexpr int LD = kD + 1;         // padded row of a 128-wide tile in shared memory
 constexpr int LC = kC + 1;         // padded row of a 16-wide tile
-constexpr int LB = kBV + 1;
 
 struct CbArgs {
     const void *q, *k, *v;
@@ -70,6 +69,7 @@ struct CbArgs {
     float *Dn;                         // [item][kD][kD]  Dout: the gradient reaching the chunk's S_next
     float *St;                         // [(Q + N) * H][kD][kD]: state at each chunk start, then the final
     float *dq, *dk, *dv, *dg, *dbeta, *dS0;
+    unsigned *status;              // the workspace's status word: set when a bounded wait gave up
 };
 
 __device__ __forceinline__ float ld_x(const void *p, size_t i, int bf16) {
@@ -253,242 +253,498 @@ __device__ __forceinline__ void stage_vec(float *dst, const float *src, int n) {
     for (int e = threadIdx.x; e < n / 4; e += kThreads) cp16(dst + e * 4, src + e * 4);
 }
 
-// ---- 2. forward: the states at chunk starts -------------------------------------------------------
+// ---- 2 + 3. the chains, on the tensor cores ----------------------------------------------------
+// One CTA per (sequence, head) for each chain.  The forward chain carries the state S over the
+// chunks (writing the state at every chunk start and Delta); the backward chain, chunks in
+// reverse, carries Dout, the gradient reaching a chunk's S_next (writing Dout and dR, and dS0 at the
+// sequence start); it needs no forward state, so the two run side by side in one launch.  The
+// carried matrix stays in tensor memory transposed (lane j = dv channel, column c = dk channel)
+// and every product runs as tcgen05 kind::tf32 MMAs on split operands x = hi + lo (hi rounded to
+// tf32, lo the fp32 remainder) summed as hi.hi + hi.lo + lo.hi, which keeps fp32 accuracy:
+//   forward   Delta^T = U^T - S^T W^T            (A = S^T from TMEM, K = dk)
+//             S^T <- e^{Gamma_L} S^T + Delta^T Kd (A = Delta^T from TMEM, K = the chunk's tokens)
+//   backward  dDelta^T = Dout^T Kd^T + dOs^T Aqk (A = Dout^T, then dOs^T, from TMEM)
+//             dR^T = dDelta^T Tm                 (CUDA cores: 16 x 16 per dv channel)
+//             Dout^T <- e^{Gamma_L} Dout^T + [dOs | -beta dR]^T [Q0; K0]
+// The B operands are built per chunk from the prep's fp32 tiles into 128-byte-swizzled K-major
+// shared tiles, one chunk ahead, while the MMAs run.
 
-constexpr int kFV = 32;                                // dv columns of a forward-chain CTA
-constexpr int kFN = kD / kFV;
-struct FwdStage {
-    float W[kC][kD], Kd[kC][kD], U[kC][kFV], gl[kD];
-};
-constexpr int kFS = 2;                                 // forward chain: stages in the ring
+constexpr int kTcData = 512;                           // threads that own TMEM rows (16 warps)
+constexpr int kTcThreads = kTcData + 32;               // and a warp whose lane 0 issues the MMAs
+constexpr int kIssuer = kTcData;
+constexpr uint32_t kTcCols = 512;
+// tensor-memory columns: the carried matrix (fp32), its hi and lo parts (the A operand of the
+// product over dk), and four 32-column accumulators that the product over dk cycles through (a
+// chain of small MMAs into one accumulator waits on each one's write-back)
+constexpr uint32_t TC_S = 0, TC_SH = 128, TC_SL = 256, TC_D = 384;
+constexpr int kAcc = 4;
+constexpr uint32_t kTcWait = 1u << 26;                 // polls of an MMA completion wait
 
-__device__ __forceinline__ void stage_fwd(const CbArgs &A, FwdStage &st, size_t item, int cb) {
-    const size_t tile = item * kC * kD;
-    stage_tile(&st.W[0][0], kD, A.W + tile);
-    stage_tile(&st.Kd[0][0], kD, A.Kd + tile);
-    for (int e = threadIdx.x; e < kC * (kFV / 4); e += kThreads) {
-        const int i = e / (kFV / 4), p = e % (kFV / 4);
-        cp16(&st.U[i][p * 4], A.U + tile + (size_t)i * kD + cb + p * 4);
-    }
-    stage_vec(st.gl, A.gl + item * kD, kD);
-    cp_commit();
+// shared memory (bytes from the 1024-aligned base)
+// forward: per stage, [W_hi; W_lo] (32 rows x 128 K, 4 atoms of 4 KB), Kd^T hi and lo (128 rows x
+// 16 K, one atom each), e^{Gamma_L}; raw fp32 W and Kd tiles and Gamma_L as copied; the A operand
+// over the chunk's tokens, Delta^T hi and lo (128 rows x 16 K)
+constexpr uint32_t F_XW = 0, F_KH = 32768, F_GL = 98304, F_RAW = 99328, F_RAW_BYTES = 16896, F_AT = 133120,
+                   F_MISC = 165888;
+// backward: per stage, [Kd_hi; Kd_lo] (32 x 128 K) then [Aqk_hi; Aqk_lo] as B(m, t) = Aqk[m][t]
+// (32 rows x 16 K), [Q0^T | K0^T] hi and lo (128 rows x 32 K); e^{Gamma_L}, beta, Tm; raw fp32 Kd,
+// Q0, K0, Aqk, Tm tiles, Gamma_L and beta as copied; the A operand over the chunk's tokens,
+// [dOs | -beta dR]^T hi and lo (128 rows x 32 K)
+constexpr uint32_t B_X1 = 0, B_X4 = 40960, B_SMALL = 106496, B_SMALL_BYTES = 1664, B_RAW = 109824,
+                   B_RAW_BYTES = 27200, B_AT = 164864, B_MISC = 197632;
+constexpr size_t kTcSmem = 1024 + 197632 + 64;
+static_assert(F_MISC <= B_MISC, "the backward layout is the larger one");
+static_assert(F_AT % 1024 == 0 && B_AT % 1024 == 0, "swizzled tiles start on 1024-byte boundaries");
+static_assert(F_RAW + 2 * F_RAW_BYTES <= F_AT && B_RAW + 2 * B_RAW_BYTES <= B_AT, "raw stages fit");
+
+// byte offsets inside a raw backward stage
+constexpr uint32_t BR_KD = 0, BR_Q0 = 8192, BR_K0 = 16384, BR_AQK = 24576, BR_TM = 25600, BR_GL = 26624,
+                   BR_BETA = 27136;
+// inside a small backward stage: e^{Gamma_L} [128], beta [16], Tm [16][16]
+constexpr uint32_t BS_EGL = 0, BS_BETA = 512, BS_TM = 576;
+
+// n_floats of fp32 at src into raw shared memory (16-byte pieces, this thread's commit group),
+// by the data threads
+__device__ __forceinline__ void tc_stage(uint8_t *dst, const float *src, int n_floats) {
+    for (int e = threadIdx.x; e < n_floats / 4; e += kTcData) cp16(dst + e * 16, src + e * 4);
+}
+// four fp32 values split into hi and lo, stored as one 16-byte chunk each at byte offset o of the
+// hi and lo tiles
+__device__ __forceinline__ void put_split4(uint8_t *hi_tile, uint8_t *lo_tile, uint32_t o, float a, float b, float c,
+                                           float d) {
+    uint4 h, l;
+    tc::split_tf32(a, h.x, l.x);
+    tc::split_tf32(b, h.y, l.y);
+    tc::split_tf32(c, h.z, l.z);
+    tc::split_tf32(d, h.w, l.w);
+    *reinterpret_cast<uint4 *>(hi_tile + o) = h;
+    *reinterpret_cast<uint4 *>(lo_tile + o) = l;
 }
 
-constexpr int LF = kFV + 4;        // 16-byte aligned rows of Delta
-constexpr int LT = kD + 4;         // 16-byte aligned rows of a transposed 128-row tile
-struct FwdSmem {
-    FwdStage stg[kFS];
-    float sSpT[kFV][LT], sDl[kC][LF];              // S transposed: column j of S is row j
-};
-
-__device__ __forceinline__ void forward_chain(const CbArgs &A, uint8_t *dyn, int bid) {
-    FwdSmem &fs = *reinterpret_cast<FwdSmem *>(dyn);
-    FwdStage *stg = fs.stg;
-    float (*sSpT)[LT] = fs.sSpT;
-    float (*sDl)[LF] = fs.sDl;
-    // thread: row r, 16 columns; Delta elements (di, dj) and (di, dj + 1)
-    const int tid = threadIdx.x, r = tid >> 1, c0 = (tid & 1) * 16;
-    const int blk = bid % kFN, nh = bid / kFN, n = nh / A.H, h = nh % A.H, H = A.H;
-    const int cb = blk * kFV;
-    float S[16];
-#pragma unroll
-    for (int u = 0; u < 16; ++u) S[u] = A.S0 ? A.S0[((size_t)nh * kD + r) * kD + cb + c0 + u] : 0.f;
-    const int q0 = A.chunk_off[n], nq = A.chunk_off[n + 1] - q0;
-    // Delta elements (di, dj) and (di, dj + 16)
-    const int di = tid / 16, dj = tid % 16;
-    // one commit group per chunk, issued one chunk ahead; S transposed in sSpT for each chunk's Delta
-    if (nq > 0) stage_fwd(A, stg[0], (size_t)q0 * H + h, cb);
-#pragma unroll
-    for (int u = 0; u < 16; ++u) sSpT[c0 + u][r] = S[u];
-    for (int c = 0; c <= nq; ++c) {
-        float *stp = A.St + ((size_t)(q0 + c + n) * H + h) * kD * kD + (size_t)r * kD + cb + c0;
-#pragma unroll
-        for (int u = 0; u < 16; u += 4) *reinterpret_cast<float4 *>(stp + u) = make_float4(S[u], S[u + 1], S[u + 2], S[u + 3]);
-        if (c == nq) break;
-        const size_t item = (size_t)(q0 + c) * H + h;
-        cp_wait<0>();
-        const FwdStage &st = stg[c % kFS];
-        // chunk c's tiles and S_c (sSpT) are in, and every thread is through chunk c - 1: its
-        // stage buffer may take chunk c + 1
-        __syncthreads();
-        if (c + 1 < nq) stage_fwd(A, stg[(c + 1) % kFS], item + (size_t)H, cb);
-        {
-            const float *w = st.W[di], *x0 = sSpT[dj], *x1 = sSpT[dj + 16];
-            float a0 = 0.f, a1 = 0.f;
-#pragma unroll 4
-            for (int cc = 0; cc < kD; cc += 4) {
-                const float4 w4 = *reinterpret_cast<const float4 *>(w + cc);
-                const float4 p4 = *reinterpret_cast<const float4 *>(x0 + cc);
-                const float4 q4 = *reinterpret_cast<const float4 *>(x1 + cc);
-                a0 = fmaf(w4.x, p4.x, fmaf(w4.y, p4.y, fmaf(w4.z, p4.z, fmaf(w4.w, p4.w, a0))));
-                a1 = fmaf(w4.x, q4.x, fmaf(w4.y, q4.y, fmaf(w4.z, q4.z, fmaf(w4.w, q4.w, a1))));
+__global__ void __launch_bounds__(kTcThreads, 1) cb_tc_chains_kernel(const __grid_constant__ CbArgs A) {
+    using namespace tc;
+    extern __shared__ uint8_t smraw[];
+    uint8_t *sm = smem_align1024(smraw);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const bool data = tid < kTcData, iss = tid == kIssuer;
+    const int lq = warp & 3, cg = warp >> 2;           // TMEM lane quarter; column / token group
+    const int j = 32 * lq + lane;                      // this thread's dv channel (TMEM lane)
+    const int NH = A.N * A.H, H = A.H;
+    const bool fwd = (int)blockIdx.x < NH;
+    const int nh = fwd ? blockIdx.x : blockIdx.x - NH, n = nh / H, h = nh % H;
+    const uint32_t misc = fwd ? F_MISC : B_MISC;
+    uint64_t *mbar = reinterpret_cast<uint64_t *>(sm + misc);
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + misc + 8);
+    volatile uint32_t *sflag = reinterpret_cast<volatile uint32_t *>(sm + misc + 12);
+    const uint32_t sbase = smem_u32(sm), mb = smem_u32(mbar);
+    if (warp == 0) { tmem_alloc(smem_u32(tslot), kTcCols); tmem_relinquish(); }
+    if (tid == 0) { mbar_init(mb, 1); fence_mbar_init(); *sflag = 0; }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = *tslot;
+    const uint32_t tl = tbase + ((uint32_t)(32 * lq) << 16);
+    uint32_t ph = 0;
+    bool pend = false, failed = false;
+    // the issuer waits for the MMAs it committed; everyone learns whether the wait ran out
+    auto mma_wait = [&]() -> bool {
+        if (iss && pend) {
+            if (mbar_wait_bounded(mb, ph, kTcWait)) {
+                ph ^= 1u;
+                pend = false;
+            } else {
+                *sflag = 1;
+                atomicOr(A.status, 1u);
             }
-            const float d0 = st.U[di][dj] - a0, d1 = st.U[di][dj + 16] - a1;
-            sDl[di][dj] = d0;
-            sDl[di][dj + 16] = d1;
-            float *dlg = A.Dl + item * kC * kD + (size_t)di * kD + cb;
-            dlg[dj] = d0;
-            dlg[dj + 16] = d1;
         }
         __syncthreads();
-        // S_next = e^{Gamma_L} S + Kd^T Delta
-        const float eg = expf(st.gl[r]);
-        float acc[16];
+        tc_fence_after();
+        return *sflag == 0;
+    };
+    // the carried matrix's row j, columns [32 cg, 32 cg + 32): into TMEM with its hi and lo parts
+    auto put_carried = [&](const float (&x)[32], bool with_fp32) {
 #pragma unroll
-        for (int u = 0; u < 16; ++u) acc[u] = eg * S[u];
+        for (int b = 0; b < 2; ++b) {
+            uint32_t r[16], hi[16], lo[16];
 #pragma unroll
-        for (int i = 0; i < kC; ++i) {
-            const float khv = st.Kd[i][r];
-#pragma unroll
-            for (int u = 0; u < 16; u += 4) {
-                const float4 d4 = *reinterpret_cast<const float4 *>(&sDl[i][c0 + u]);
-                acc[u] = fmaf(khv, d4.x, acc[u]); acc[u + 1] = fmaf(khv, d4.y, acc[u + 1]);
-                acc[u + 2] = fmaf(khv, d4.z, acc[u + 2]); acc[u + 3] = fmaf(khv, d4.w, acc[u + 3]);
+            for (int u = 0; u < 16; ++u) {
+                r[u] = __float_as_uint(x[16 * b + u]);
+                split_tf32(x[16 * b + u], hi[u], lo[u]);
             }
+            if (with_fp32) tmem_st16(tl + TC_S + 32 * cg + 16 * b, r);
+            tmem_st16(tl + TC_SH + 32 * cg + 16 * b, hi);
+            tmem_st16(tl + TC_SL + 32 * cg + 16 * b, lo);
         }
+    };
+    auto get_carried = [&](float (&x)[32]) {
+        uint32_t r[2][16];
+        tmem_ld16(tl + TC_S + 32 * cg, r[0]);
+        tmem_ld16(tl + TC_S + 32 * cg + 16, r[1]);
+        tmem_wait_ld();
 #pragma unroll
-        for (int u = 0; u < 16; ++u) {
-            S[u] = acc[u];
-            sSpT[c0 + u][r] = acc[u];                  // S_{c+1} for the next chunk's Delta
+        for (int u = 0; u < 32; ++u) x[u] = __uint_as_float(r[u >> 4][u & 15]);
+    };
+    // x written out, then x -> e^{Gamma_L} x (row j's columns) into the fp32 columns
+    auto scale_carried = [&](float (&x)[32], const float *egl, float *out) {
+#pragma unroll
+        for (int u = 0; u < 32; u += 4) {
+            const float4 e4 = *reinterpret_cast<const float4 *>(egl + 32 * cg + u);
+            out[(size_t)(32 * cg + u) * kD] = x[u];
+            out[(size_t)(32 * cg + u + 1) * kD] = x[u + 1];
+            out[(size_t)(32 * cg + u + 2) * kD] = x[u + 2];
+            out[(size_t)(32 * cg + u + 3) * kD] = x[u + 3];
+            x[u] *= e4.x; x[u + 1] *= e4.y; x[u + 2] *= e4.z; x[u + 3] *= e4.w;
         }
-    }
-}
-
-// ---- 3. chain: gradients at chunk boundaries, chunks in reverse ----------------------------------
-
-struct ChainStage {
-    float Kd[kC][kD], Q0[kC][kD], K0[kC][kD];
-    float Aqk[kC][kC], Tm[kC][kC], dO[kC][kBV];
-    float gl[kD], beta[kC];
-};
-constexpr int kCS = 2;                                 // backward chain: stages in the ring
-
-__device__ __forceinline__ void stage_chain(const CbArgs &A, ChainStage &st, size_t item, int qc, int h, int cb) {
-    const size_t tile = item * kC * kD, small = item * kC * kC;
-    const int t0 = A.ck_t0[qc], L = A.ck_len[qc], H = A.H;
-    stage_tile(&st.Kd[0][0], kD, A.Kd + tile);
-    stage_tile(&st.Q0[0][0], kD, A.Q0 + tile);
-    stage_tile(&st.K0[0][0], kD, A.K0 + tile);
-    stage_vec(&st.Aqk[0][0], A.Aqk + small, kC * kC);
-    stage_vec(&st.Tm[0][0], A.Tm + small, kC * kC);
-    for (int e = threadIdx.x; e < kC * (kBV / 4); e += kThreads) {
-        const int i = e / (kBV / 4), p = e % (kBV / 4);
-        const int ti = i < L ? t0 + i : t0;            // rows past the chunk's end are zero-filled
-        cp16z(&st.dO[i][p * 4], A.dO + ((size_t)ti * H + h) * kD + cb + p * 4, i < L ? 16 : 0);
-    }
-    stage_vec(st.gl, A.gl + item * kD, kD);
-    if (threadIdx.x < kC) {
-        // beta is strided by H: 4-byte pieces
-        const int i = threadIdx.x;
-        const int ti = i < L ? t0 + i : t0;
-        asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"((uint32_t)__cvta_generic_to_shared(&st.beta[i])),
-                     "l"(A.beta + (size_t)ti * H + h), "r"(i < L ? 4 : 0)
-                     : "memory");
-    }
-    cp_commit();
-}
-
-constexpr int LQ = kBV + 4;        // 16-byte aligned rows of beta dR
-struct ChainSmem {
-    ChainStage stg[kCS];
-    float sdXT[kBV][LT], sdD[kC][LB], sbR[kC][LQ];  // Dout transposed: column j of Dout is row j
-};
-
-__device__ __forceinline__ void backward_chain(const CbArgs &A, uint8_t *dyn, int bid) {
-    ChainSmem &cs = *reinterpret_cast<ChainSmem *>(dyn);
-    ChainStage *stg = cs.stg;
-    float (*sdXT)[LT] = cs.sdXT;
-    float (*sdD)[LB] = cs.sdD;
-    float (*sbR)[LQ] = cs.sbR;
-    const int tid = threadIdx.x, r = tid >> 1, c0 = (tid & 1) * 8;
-    const int blk = bid % kNV, nh = bid / kNV, n = nh / A.H, h = nh % A.H, H = A.H;
-    const int cb = blk * kBV;
-    const float scale = A.scale;
-    float Dout[8];
+        uint32_t r[16];
 #pragma unroll
-    for (int u = 0; u < 8; ++u) Dout[u] = A.dSfin ? A.dSfin[((size_t)nh * kD + r) * kD + cb + c0 + u] : 0.f;
-    const int q0 = A.chunk_off[n], nq = A.chunk_off[n + 1] - q0;
-    const int di = tid / kBV, dj = tid % kBV;
-    // chunk j of the sweep is c = nq - 1 - j; one commit group per chunk, issued one chunk ahead;
-    // Dout transposed in sdXT for each chunk's dDelta
-    if (nq > 0) stage_chain(A, stg[0], (size_t)(q0 + nq - 1) * H + h, q0 + nq - 1, h, cb);
+        for (int b = 0; b < 2; ++b) {
 #pragma unroll
-    for (int u = 0; u < 8; ++u) sdXT[c0 + u][r] = Dout[u];
-    for (int j = 0; j < nq; ++j) {
-        const int c = nq - 1 - j;
-        const size_t item = (size_t)(q0 + c) * H + h, tile = item * kC * kD;
-        {
-            float *dng = A.Dn + item * kD * kD + (size_t)r * kD + cb + c0;
-#pragma unroll
-            for (int u = 0; u < 8; u += 4)
-                *reinterpret_cast<float4 *>(dng + u) = make_float4(Dout[u], Dout[u + 1], Dout[u + 2], Dout[u + 3]);
+            for (int u = 0; u < 16; ++u) r[u] = __float_as_uint(x[16 * b + u]);
+            tmem_st16(tl + TC_S + 32 * cg + 16 * b, r);
         }
-        cp_wait<0>();
-        const ChainStage &st = stg[j % kCS];
-        // chunk c's tiles and its Dout (sdXT) are in, and every thread is through the chunk before:
-        // its stage buffer may take chunk c - 1
-        __syncthreads();
-        if (c >= 1) stage_chain(A, stg[(j + 1) % kCS], (size_t)(q0 + c - 1) * H + h, q0 + c - 1, h, cb);
-        // dDelta = Kd Dout + Aqk^T dOs
-        {
-            const float *kh = st.Kd[di], *xt = sdXT[dj];   // row di of Kd, column dj of Dout
+    };
+    // the accumulators' sum over this thread's four tokens [4 cg, 4 cg + 4) (and + 16: the lo rows)
+    auto sum_acc4 = [&](float (&d)[4]) {
+        uint32_t r[2 * kAcc][4];
+#pragma unroll
+        for (int a = 0; a < kAcc; ++a) {
+            tmem_ld4(tl + TC_D + 32 * a + 4 * cg, r[2 * a]);
+            tmem_ld4(tl + TC_D + 32 * a + 16 + 4 * cg, r[2 * a + 1]);
+        }
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
             float acc = 0.f;
-#pragma unroll 4
-            for (int rr = 0; rr < kD; rr += 4) {
-                const float4 k4 = *reinterpret_cast<const float4 *>(kh + rr);
-                const float4 x4 = *reinterpret_cast<const float4 *>(xt + rr);
-                acc = fmaf(k4.x, x4.x, fmaf(k4.y, x4.y, fmaf(k4.z, x4.z, fmaf(k4.w, x4.w, acc))));
+#pragma unroll
+            for (int a = 0; a < 2 * kAcc; ++a) acc += __uint_as_float(r[a][i]);
+            d[i] = acc;
+        }
+    };
+    const int q0 = A.chunk_off[n], nq = A.chunk_off[n + 1] - q0;
+    int tb, te;                                        // the sequence's tokens: chunk c starts at tb + 16 c
+    seq_bounds(A.cu, n, A.T, tb, te);
+    float X[32];                                       // the carried matrix, row j, this thread's columns
+    const uint32_t idN32 = idesc_tf32_f32(128, 32), idN16 = idesc_tf32_f32(128, 16), idN128 = idesc_tf32_f32(128, 128);
+    // MMAs over dk: A = the carried matrix's hi / lo columns, B = a 32-row tile (hi rows 0-15, lo
+    // rows 16-31) of 4 K atoms; K step kk goes to accumulator kk mod kAcc
+    auto issue_over_dk = [&](uint32_t btile) {
+        const uint64_t dB = sdesc_kmajor_sw128(sbase + btile);
+#pragma unroll
+        for (int kk = 0; kk < 16; ++kk)
+            mma_tf32_ta(tbase + TC_D + 32 * (kk % kAcc), tbase + TC_SH + 8 * kk, dadd(dB, (kk >> 2) * 4096 + (kk & 3) * 32),
+                        idN32, kk >= kAcc);
+#pragma unroll
+        for (int kk = 0; kk < 16; ++kk)
+            mma_tf32_ta(tbase + TC_D + 32 * (kk % kAcc), tbase + TC_SL + 8 * kk, dadd(dB, (kk >> 2) * 4096 + (kk & 3) * 32),
+                        idN16, 1);
+    };
+
+    if (fwd) {
+        // ================= forward chain: S at every chunk start, Delta =================
+        uint8_t *ath = sm + F_AT, *atl = sm + F_AT + 16384;
+        auto raw = [&](int s) { return sm + F_RAW + s * F_RAW_BYTES; };
+        auto stage_raw = [&](int c) {                // chunk c's W and Kd tiles into raw stage c & 1
+            const size_t tile = ((size_t)(q0 + c) * H + h) * kC * kD;
+            tc_stage(raw(c & 1), A.W + tile, kC * kD);
+            tc_stage(raw(c & 1) + 8192, A.Kd + tile, kC * kD);
+            tc_stage(raw(c & 1) + 16384, A.gl + ((size_t)(q0 + c) * H + h) * kD, kD);
+            cp_commit();
+        };
+        auto build = [&](int c) {                    // raw stage c & 1 -> operand stage c & 1
+            const int s = c & 1;
+            const float *rw = reinterpret_cast<const float *>(raw(s)), *rk = rw + kC * kD;
+            uint8_t *xw = sm + F_XW + s * 16384;
+            uint8_t *kh = sm + F_KH + s * 32768, *kl = kh + 16384;
+            {   // B(c, t) = W[t][c]: row t (hi), 16 + t (lo), four c per thread
+                const int t = tid >> 5, c4 = (tid & 31) * 4;
+                const float4 w = *reinterpret_cast<const float4 *>(rw + t * kD + c4);
+                uint4 hv, lv;
+                split_tf32(w.x, hv.x, lv.x); split_tf32(w.y, hv.y, lv.y);
+                split_tf32(w.z, hv.z, lv.z); split_tf32(w.w, hv.w, lv.w);
+                *reinterpret_cast<uint4 *>(xw + sw128_offset_f32(t, c4, 4096)) = hv;
+                *reinterpret_cast<uint4 *>(xw + sw128_offset_f32(16 + t, c4, 4096)) = lv;
             }
-            float a2 = 0.f;
-            for (int m = di; m < kC; ++m) a2 = fmaf(st.Aqk[m][di], st.dO[m][dj], a2);
-            sdD[di][dj] = fmaf(scale, a2, acc);
-        }
-        __syncthreads();
-        // dR = Tm^T dDelta
-        {
-            float acc = 0.f;
-            for (int m = di; m < kC; ++m) acc = fmaf(st.Tm[m][di], sdD[m][dj], acc);
-            A.dR[tile + (size_t)di * kD + cb + dj] = acc;
-            sbR[di][dj] = st.beta[di] * acc;
-        }
-        __syncthreads();
-        // Din = e^{Gamma_L} Dout + Q0^T dOs - K0^T diag(beta) dR
-        const float eg = expf(st.gl[r]);
-        float acc[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) acc[u] = eg * Dout[u];
-#pragma unroll
-        for (int i = 0; i < kC; ++i) {
-            const float qv = scale * st.Q0[i][r], kv = -st.K0[i][r];
-#pragma unroll
-            for (int u = 0; u < 8; u += 4) {
-                const float4 o4 = *reinterpret_cast<const float4 *>(&st.dO[i][c0 + u]);
-                const float4 b4 = *reinterpret_cast<const float4 *>(&sbR[i][c0 + u]);
-                acc[u] = fmaf(qv, o4.x, fmaf(kv, b4.x, acc[u]));
-                acc[u + 1] = fmaf(qv, o4.y, fmaf(kv, b4.y, acc[u + 1]));
-                acc[u + 2] = fmaf(qv, o4.z, fmaf(kv, b4.z, acc[u + 2]));
-                acc[u + 3] = fmaf(qv, o4.w, fmaf(kv, b4.w, acc[u + 3]));
+            {   // B(t, c) = Kd[t][c]: row c, four t per thread
+                const int c2 = tid & 127, t4 = (tid >> 7) * 4;
+                put_split4(kh, kl, sw128_offset_f32(c2, t4, 16384), rk[t4 * kD + c2], rk[(t4 + 1) * kD + c2],
+                           rk[(t4 + 2) * kD + c2], rk[(t4 + 3) * kD + c2]);
             }
-        }
+            if (tid < kD) reinterpret_cast<float *>(sm + F_GL + s * 512)[tid] = expf(rw[2 * kC * kD + tid]);
+        };
+        if (data) {
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            Dout[u] = acc[u];
-            sdXT[c0 + u][r] = acc[u];                  // the next chunk's Dout for its dDelta
+            for (int u = 0; u < 32; ++u) X[u] = A.S0 ? A.S0[((size_t)nh * kD + 32 * cg + u) * kD + j] : 0.f;
+            put_carried(X, true);
+            tmem_wait_st();
+            if (nq > 0) stage_raw(0);
+            if (nq > 1) stage_raw(1);
+            cp_wait<0>();
+            named_bar(1, kTcData);
+            if (nq > 0) build(0);
+            fence_async_smem();
+        }
+        tc_fence_before();
+        __syncthreads();
+        for (int c = 0; c < nq; ++c) {
+            const int s = c & 1;
+            const size_t tile = ((size_t)(q0 + c) * H + h) * kC * kD;
+            // ---- MMA: D = S^T [W_hi; W_lo]^T (N = 32) + S_lo^T W_hi^T (N = 16), over four accumulators ----
+            if (iss) {
+                tc_fence_after();
+                issue_over_dk(F_XW + s * 16384);
+                mma_commit(mb);
+                pend = true;
+            }
+            // while it runs: U of this chunk, S_c out, S <- e^{Gamma_L} S, the next chunk's operands
+            float u4[4];
+            if (data) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) u4[i] = A.U[tile + (size_t)(4 * cg + i) * kD + j];
+                scale_carried(X, reinterpret_cast<const float *>(sm + F_GL + s * 512),
+                              A.St + ((size_t)(q0 + c + n) * H + h) * kD * kD + j);
+                cp_wait<0>();
+                named_bar(1, kTcData);
+                if (c + 1 < nq) build(c + 1);
+                fence_async_smem();
+                if (c + 2 < nq) stage_raw(c + 2);
+                tmem_wait_st();
+            }
+            if (!mma_wait()) { failed = true; break; }
+            // ---- Delta^T = U^T - D, four tokens per thread: out, and split for the next MMA ----
+            if (data) {
+                float d[4];
+                sum_acc4(d);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    d[i] = u4[i] - d[i];
+                    A.Dl[tile + (size_t)(4 * cg + i) * kD + j] = d[i];
+                }
+                put_split4(ath, atl, sw128_offset_f32(j, 4 * cg, 16384), d[0], d[1], d[2], d[3]);
+                fence_async_smem();
+            }
+            tc_fence_before();
+            __syncthreads();
+            // ---- MMA: S^T += Delta^T Kd  (hi.hi + hi.lo + lo.hi, K = 16 tokens) ----
+            if (iss) {
+                tc_fence_after();
+                const uint64_t dAh = sdesc_kmajor_sw128(sbase + F_AT), dAl = sdesc_kmajor_sw128(sbase + F_AT + 16384);
+                const uint64_t dKh = sdesc_kmajor_sw128(sbase + F_KH + s * 32768),
+                               dKl = sdesc_kmajor_sw128(sbase + F_KH + s * 32768 + 16384);
+#pragma unroll
+                for (int sp = 0; sp < 3; ++sp)
+#pragma unroll
+                    for (int kk = 0; kk < 2; ++kk)
+                        mma_tf32(tbase + TC_S, dadd(sp == 2 ? dAl : dAh, kk * 32), dadd(sp == 1 ? dKl : dKh, kk * 32), idN128, 1);
+                mma_commit(mb);
+                pend = true;
+            }
+            if (!mma_wait()) { failed = true; break; }
+            if (data) {
+                get_carried(X);
+                put_carried(X, false);
+                tmem_wait_st();
+            }
+            tc_fence_before();
+            __syncthreads();
+        }
+        if (!failed && data) {
+            float *st = A.St + ((size_t)(q0 + nq + n) * H + h) * kD * kD + j;
+#pragma unroll
+            for (int u = 0; u < 32; ++u) st[(size_t)(32 * cg + u) * kD] = X[u];
+        }
+    } else {
+        // ================= backward chain: Dout, dR; dS0 =================
+        const float scale = A.scale;
+        uint8_t *ath = sm + B_AT, *atl = sm + B_AT + 16384;
+        auto raw = [&](int s) { return sm + B_RAW + s * B_RAW_BYTES; };
+        auto small = [&](int s) { return sm + B_SMALL + s * B_SMALL_BYTES; };
+        // iteration it handles chunk c = nq - 1 - it in stage it & 1 (the raw stage likewise)
+        auto stage_raw = [&](int c, int s) {
+            const size_t item = (size_t)(q0 + c) * H + h, tile = item * kC * kD, sml = item * kC * kC;
+            tc_stage(raw(s) + BR_KD, A.Kd + tile, kC * kD);
+            tc_stage(raw(s) + BR_Q0, A.Q0 + tile, kC * kD);
+            tc_stage(raw(s) + BR_K0, A.K0 + tile, kC * kD);
+            tc_stage(raw(s) + BR_AQK, A.Aqk + sml, kC * kC);
+            tc_stage(raw(s) + BR_TM, A.Tm + sml, kC * kC);
+            tc_stage(raw(s) + BR_GL, A.gl + item * kD, kD);
+            if (threadIdx.x < kC) {                      // beta is strided by H: 4-byte pieces, zero past the end
+                const int t = tb + c * kC + (int)threadIdx.x;
+                const float *src = A.beta + (size_t)(t < te ? t : tb + c * kC) * H + h;
+                asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_u32(raw(s) + BR_BETA + 4 * threadIdx.x)),
+                             "l"(src), "r"(t < te ? 4 : 0)
+                             : "memory");
+            }
+            cp_commit();
+        };
+        auto build = [&](int c, int s) {
+            const uint8_t *r = raw(s);
+            const float *rkd = reinterpret_cast<const float *>(r + BR_KD), *rq = reinterpret_cast<const float *>(r + BR_Q0),
+                        *rk = reinterpret_cast<const float *>(r + BR_K0);
+            uint8_t *x1 = sm + B_X1 + s * 20480, *xa = x1 + 16384;
+            uint8_t *x4h = sm + B_X4 + s * 32768, *x4l = x4h + 16384;
+            {   // B(c, t) = Kd[t][c]: row t (hi), 16 + t (lo), four c per thread
+                const int t = tid >> 5, c4 = (tid & 31) * 4;
+                const float4 w = *reinterpret_cast<const float4 *>(rkd + t * kD + c4);
+                uint4 hv, lv;
+                split_tf32(w.x, hv.x, lv.x); split_tf32(w.y, hv.y, lv.y);
+                split_tf32(w.z, hv.z, lv.z); split_tf32(w.w, hv.w, lv.w);
+                *reinterpret_cast<uint4 *>(x1 + sw128_offset_f32(t, c4, 4096)) = hv;
+                *reinterpret_cast<uint4 *>(x1 + sw128_offset_f32(16 + t, c4, 4096)) = lv;
+            }
+            {   // B(t, c) = Q0[t][c] and B(16 + t, c) = K0[t][c]: row c, four t per thread
+                const int c2 = tid & 127, t4 = (tid >> 7) * 4;
+                put_split4(x4h, x4l, sw128_offset_f32(c2, t4, 16384), rq[t4 * kD + c2], rq[(t4 + 1) * kD + c2],
+                           rq[(t4 + 2) * kD + c2], rq[(t4 + 3) * kD + c2]);
+                put_split4(x4h, x4l, sw128_offset_f32(c2, 16 + t4, 16384), rk[t4 * kD + c2], rk[(t4 + 1) * kD + c2],
+                           rk[(t4 + 2) * kD + c2], rk[(t4 + 3) * kD + c2]);
+            }
+            if (tid < kC * kC / 4) {                     // B(m, t) = Aqk[m][t]: row t, four m per thread
+                const int t = tid & 15, m4 = (tid >> 4) * 4;
+                const float *ra = reinterpret_cast<const float *>(r + BR_AQK);
+                uint4 hv, lv;
+                split_tf32(ra[m4 * kC + t], hv.x, lv.x);
+                split_tf32(ra[(m4 + 1) * kC + t], hv.y, lv.y);
+                split_tf32(ra[(m4 + 2) * kC + t], hv.z, lv.z);
+                split_tf32(ra[(m4 + 3) * kC + t], hv.w, lv.w);
+                *reinterpret_cast<uint4 *>(xa + sw128_offset_f32(t, m4, 4096)) = hv;
+                *reinterpret_cast<uint4 *>(xa + sw128_offset_f32(16 + t, m4, 4096)) = lv;
+            }
+            if (tid < kC * kC) reinterpret_cast<float *>(small(s) + BS_TM)[tid] = reinterpret_cast<const float *>(r + BR_TM)[tid];
+            if (tid < kD)
+                reinterpret_cast<float *>(small(s) + BS_EGL)[tid] = expf(reinterpret_cast<const float *>(r + BR_GL)[tid]);
+            if (tid < kC) reinterpret_cast<float *>(small(s) + BS_BETA)[tid] = reinterpret_cast<const float *>(r + BR_BETA)[tid];
+        };
+        // dO of chunk c at tokens [4 cg, 4 cg + 4) of channel j (zero past the sequence's end)
+        auto load_do = [&](int c, float (&o)[4]) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int t = tb + c * kC + 4 * cg + i;
+                o[i] = t < te ? A.dO[((size_t)t * H + h) * kD + j] : 0.f;
+            }
+        };
+        auto put_dos = [&](const float (&o)[4]) {
+            put_split4(ath, atl, sw128_offset_f32(j, 4 * cg, 16384), scale * o[0], scale * o[1], scale * o[2], scale * o[3]);
+        };
+        float dov[4];
+        if (data) {
+#pragma unroll
+            for (int u = 0; u < 32; ++u) X[u] = A.dSfin ? A.dSfin[((size_t)nh * kD + 32 * cg + u) * kD + j] : 0.f;
+            put_carried(X, true);
+            if (nq > 0) {
+                load_do(nq - 1, dov);
+                put_dos(dov);
+            }
+            tmem_wait_st();
+            if (nq > 0) stage_raw(nq - 1, 0);
+            if (nq > 1) stage_raw(nq - 2, 1);
+            cp_wait<0>();
+            named_bar(1, kTcData);
+            if (nq > 0) build(nq - 1, 0);
+            fence_async_smem();
+        }
+        tc_fence_before();
+        __syncthreads();
+        for (int it = 0; it < nq; ++it) {
+            const int c = nq - 1 - it, s = it & 1;
+            const size_t item = (size_t)(q0 + c) * H + h, tile = item * kC * kD;
+            // ---- MMA: D = Dout^T [Kd_hi; Kd_lo]^T + dOs^T [Aqk_hi; Aqk_lo] (N = 32), then the lo
+            // parts of the A operands against the hi rows (N = 16), over four accumulators ----
+            if (iss) {
+                tc_fence_after();
+                issue_over_dk(B_X1 + s * 20480);
+                const uint64_t dAh = sdesc_kmajor_sw128(sbase + B_AT), dAl = sdesc_kmajor_sw128(sbase + B_AT + 16384);
+                const uint64_t dQ = sdesc_kmajor_sw128(sbase + B_X1 + s * 20480 + 16384);
+#pragma unroll
+                for (int kk = 0; kk < 2; ++kk) mma_tf32(tbase + TC_D + 32 * kk, dadd(dAh, kk * 32), dadd(dQ, kk * 32), idN32, 1);
+#pragma unroll
+                for (int kk = 0; kk < 2; ++kk) mma_tf32(tbase + TC_D + 32 * (2 + kk), dadd(dAl, kk * 32), dadd(dQ, kk * 32), idN16, 1);
+                mma_commit(mb);
+                pend = true;
+            }
+            // while it runs: Dout of this chunk out, Dout <- e^{Gamma_L} Dout, dO of the next
+            // chunk, the next chunk's operands
+            if (data) {
+                scale_carried(X, reinterpret_cast<const float *>(small(s) + BS_EGL), A.Dn + item * kD * kD + j);
+                if (c >= 1) load_do(c - 1, dov);
+                cp_wait<0>();
+                named_bar(1, kTcData);
+                if (c >= 1) build(c - 1, s ^ 1);
+                fence_async_smem();
+                if (c >= 2) stage_raw(c - 2, s);
+                tmem_wait_st();
+            }
+            if (!mma_wait()) { failed = true; break; }
+            // ---- dDelta (all 16 tokens of channel j), dR = Tm^T dDelta for this thread's four ----
+            if (data) {
+                float dd[kC];                            // dDelta[m][j], summed over the accumulators
+#pragma unroll
+                for (int m = 0; m < kC; ++m) dd[m] = 0.f;
+#pragma unroll
+                for (int a = 0; a < kAcc; ++a) {
+                    uint32_t r0[16], r1[16];
+                    tmem_ld16(tl + TC_D + 32 * a, r0);
+                    tmem_ld16(tl + TC_D + 32 * a + 16, r1);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int m = 0; m < kC; ++m) dd[m] += __uint_as_float(r0[m]) + __uint_as_float(r1[m]);
+                }
+                const float *tm = reinterpret_cast<const float *>(small(s) + BS_TM);
+                const float4 be = *reinterpret_cast<const float4 *>(small(s) + BS_BETA + 16 * cg);
+                float dr[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int m = 0; m < kC; ++m) {
+                    const float4 t4 = *reinterpret_cast<const float4 *>(tm + m * kC + 4 * cg);
+                    dr[0] = fmaf(t4.x, dd[m], dr[0]); dr[1] = fmaf(t4.y, dd[m], dr[1]);
+                    dr[2] = fmaf(t4.z, dd[m], dr[2]); dr[3] = fmaf(t4.w, dd[m], dr[3]);
+                }
+#pragma unroll
+                for (int i = 0; i < 4; ++i) A.dR[tile + (size_t)(4 * cg + i) * kD + j] = dr[i];
+                put_split4(ath, atl, sw128_offset_f32(j, 16 + 4 * cg, 16384), -be.x * dr[0], -be.y * dr[1], -be.z * dr[2],
+                           -be.w * dr[3]);
+                fence_async_smem();
+            }
+            tc_fence_before();
+            __syncthreads();
+            // ---- MMA: Dout^T += [dOs | -beta dR]^T [Q0; K0]  (hi.hi + hi.lo + lo.hi, K = 32) ----
+            if (iss) {
+                tc_fence_after();
+                const uint64_t dAh = sdesc_kmajor_sw128(sbase + B_AT), dAl = sdesc_kmajor_sw128(sbase + B_AT + 16384);
+                const uint64_t dH = sdesc_kmajor_sw128(sbase + B_X4 + s * 32768),
+                               dL = sdesc_kmajor_sw128(sbase + B_X4 + s * 32768 + 16384);
+#pragma unroll
+                for (int sp = 0; sp < 3; ++sp)
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_tf32(tbase + TC_S, dadd(sp == 2 ? dAl : dAh, kk * 32), dadd(sp == 1 ? dL : dH, kk * 32), idN128, 1);
+                mma_commit(mb);
+                pend = true;
+            }
+            if (!mma_wait()) { failed = true; break; }
+            if (data) {
+                get_carried(X);
+                put_carried(X, false);
+                if (c >= 1) {
+                    put_dos(dov);
+                    fence_async_smem();
+                }
+                tmem_wait_st();
+            }
+            tc_fence_before();
+            __syncthreads();
+        }
+        if (!failed && data) {
+            float *d0 = A.dS0 + (size_t)nh * kD * kD + j;
+#pragma unroll
+            for (int u = 0; u < 32; ++u) d0[(size_t)(32 * cg + u) * kD] = X[u];
         }
     }
-    float *d0 = A.dS0 + ((size_t)nh * kD + r) * kD + cb + c0;
-#pragma unroll
-    for (int u = 0; u < 8; u += 4) *reinterpret_cast<float4 *>(d0 + u) = make_float4(Dout[u], Dout[u + 1], Dout[u + 2], Dout[u + 3]);
-}
-
-// Both chains in one launch: CTAs [0, N H kFN) run the forward chain, the rest the backward
-// chain.  The two share no data, and one grid lets them run side by side (three CTAs fit on an SM).
-constexpr size_t kChainsSmem = sizeof(FwdSmem) > sizeof(ChainSmem) ? sizeof(FwdSmem) : sizeof(ChainSmem);
-
-__global__ void __launch_bounds__(kThreads) cb_chains_kernel(const __grid_constant__ CbArgs A, int fchains) {
-    extern __shared__ __align__(16) uint8_t dyn[];
-    if ((int)blockIdx.x < fchains) forward_chain(A, dyn, blockIdx.x);
-    else backward_chain(A, dyn, blockIdx.x - fchains);
+    // after a failure, let the MMAs in flight land (bounded) before the columns are freed
+    if (iss && pend) mbar_wait_bounded(mb, ph, kTcWait);
+    cp_wait<0>();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0) tmem_dealloc(tbase, kTcCols);
 }
 
 // ---- 4. grads: two CTAs per (chunk, head), one per half of the dk columns --------------------------
@@ -723,7 +979,7 @@ size_t backward_chunked_workspace(int N, int T, int H) { return layout(N, T, H).
 cudaError_t launch_backward_chunked(const void *q, const void *k, const void *v, int bf16, const float *g,
                                     const float *beta, const float *S0, const int32_t *cu, int N, int T, int H,
                                     float scale, const float *dO, const float *dSfin, float *dq, float *dk, float *dv,
-                                    float *dg, float *dbeta, float *dS0, void *ws, cudaStream_t s) {
+                                    float *dg, float *dbeta, float *dS0, unsigned *status, void *ws, cudaStream_t s) {
     cudaError_t e;
     if (T == 0) {
         // no tokens: dS0 = dS_final (or zero)
@@ -745,7 +1001,7 @@ cudaError_t launch_backward_chunked(const void *q, const void *k, const void *v,
     A.Q0 = f(l.Q0); A.K0 = f(l.K0); A.Kd = f(l.Kd); A.Gm = f(l.Gm); A.W = f(l.W); A.U = f(l.U);
     A.Tm = f(l.Tm); A.Aqk = f(l.Aqk); A.Bm = f(l.Bm); A.gl = f(l.gl);
     A.Dl = f(l.Dl); A.dR = f(l.dR); A.Dn = f(l.Dn); A.St = f(l.St);
-    A.dq = dq; A.dk = dk; A.dv = dv; A.dg = dg; A.dbeta = dbeta; A.dS0 = dS0;
+    A.dq = dq; A.dk = dk; A.dv = dv; A.dg = dg; A.dbeta = dbeta; A.dS0 = dS0; A.status = status;
     // chunk enumeration from the device cu_seqlens; the item grids cover the upper bound A.Q of
     // the chunk count and CTAs past the real chunks return at once
     cb_offsets_kernel<<<1, 32, 0, s>>>(A);
@@ -754,15 +1010,14 @@ cudaError_t launch_backward_chunked(const void *q, const void *k, const void *v,
     cb_chunks_kernel<<<(unsigned)((A.Q + 255) / 256), 256, 0, s>>>(A);
     count_launch();
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    const unsigned items = (unsigned)((size_t)A.Q * H), chains = (unsigned)((size_t)N * H * kNV),
-                   fchains = (unsigned)((size_t)N * H * kFN);
+    const unsigned items = (unsigned)((size_t)A.Q * H), chains = (unsigned)((size_t)N * H);
     cb_prep_kernel<<<items, kThreads, 0, s>>>(A);
     count_launch();
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if (chains) {
-        if ((e = smem_attr_once((const void *)cb_chains_kernel, (int)kChainsSmem, g_chains_attr)) != cudaSuccess)
+        if ((e = smem_attr_once((const void *)cb_tc_chains_kernel, (int)kTcSmem, g_chains_attr)) != cudaSuccess)
             return e;
-        cb_chains_kernel<<<fchains + chains, kThreads, kChainsSmem, s>>>(A, (int)fchains);
+        cb_tc_chains_kernel<<<2 * chains, kTcThreads, kTcSmem, s>>>(A);
         count_launch();
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }

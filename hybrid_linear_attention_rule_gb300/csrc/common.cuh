@@ -132,7 +132,7 @@ size_t backward_chunked_workspace(int N, int T, int H);
 cudaError_t launch_backward_chunked(const void *q, const void *k, const void *v, int bf16, const float *g,
                                     const float *beta, const float *S0, const int32_t *cu, int N, int T, int H,
                                     float scale, const float *dO, const float *dSfin, float *dq, float *dk, float *dv,
-                                    float *dg, float *dbeta, float *dS0, void *ws, cudaStream_t s);
+                                    float *dg, float *dbeta, float *dS0, unsigned *status, void *ws, cudaStream_t s);
 
 // one decode token of the gated attention layers (csrc/mla_decode.cu); dq in {64, 128, 192, 256},
 // dv in {64, 128, 256}

@@ -148,10 +148,6 @@ __device__ __forceinline__ int sidx(int r, int c) { return r * 64 + (c ^ (r & 31
 __device__ __forceinline__ float silu_fast(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
 __device__ __forceinline__ float sigmoid_fast(float z) { return __fdividef(1.0f, 1.0f + __expf(-z)); }
 
-// Advance a shared-memory descriptor's start address by `bytes` (a multiple of 16, no carry
-// out of the 14-bit field for addresses below 256 KB).
-__device__ __forceinline__ uint64_t dadd(uint64_t desc, uint32_t bytes) { return desc + (bytes >> 4); }
-
 // Element (row, c) of a K-major tile whose K extent is 128 (two 64-wide atoms of rows*128 B each).
 __device__ __forceinline__ uint32_t kmaj128(uint32_t rows, uint32_t row, uint32_t c) {
     return (c >> 6) * rows * 128u + sw128_offset(row, c & 63u);

@@ -90,6 +90,10 @@ __device__ __forceinline__ uint64_t sdesc_mnmajor_sw128(uint32_t saddr, uint32_t
     return d;
 }
 
+// Advance a shared-memory descriptor's start address by `bytes` (a multiple of 16, no carry
+// out of the 14-bit field for addresses below 256 KB).
+__device__ __forceinline__ uint64_t dadd(uint64_t desc, uint32_t bytes) { return desc + (bytes >> 4); }
+
 // Instruction descriptor, kind::f16 with bf16 A and B, fp32 accumulator, both K-major
 // unless a_mn / b_mn select the MN-major layout for that operand.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool negate_a = false, bool a_mn = false,
@@ -100,6 +104,16 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool negate_
            | ((negate_a ? 1u : 0u) << 13)             // negate A
            | ((a_mn ? 1u : 0u) << 15)                 // A major: MN
            | ((b_mn ? 1u : 0u) << 16)                 // B major: MN
+           | ((uint32_t)(N >> 3) << 17)               // N / 8
+           | ((uint32_t)(M >> 4) << 24);              // M / 16
+}
+
+// Instruction descriptor, kind::tf32 (A and B fp32 words read as tf32), fp32 accumulator, both
+// operands K-major.
+__host__ __device__ constexpr uint32_t idesc_tf32_f32(int M, int N) {
+    return (1u << 4)                                  // D format: f32
+           | (2u << 7)                                // A format: tf32
+           | (2u << 10)                               // B format: tf32
            | ((uint32_t)(N >> 3) << 17)               // N / 8
            | ((uint32_t)(M >> 4) << 24);              // M / 16
 }
@@ -122,6 +136,26 @@ __device__ __forceinline__ void mma_bf16_ta(uint32_t d_tmem, uint32_t a_tmem, ui
         "{\n\t.reg .pred p;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+        ::"r"(d_tmem), "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// kind::tf32 MMA, both operands in shared memory (descriptors).
+__device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}"
+        ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// kind::tf32 MMA with A (M rows x 8 K, one fp32 word per column) read from tensor memory.
+__device__ __forceinline__ void mma_tf32_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                            uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n\t}"
         ::"r"(d_tmem), "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
@@ -153,9 +187,32 @@ __device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8])
         ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
         : "memory");
 }
+__device__ __forceinline__ void tmem_ld4(uint32_t taddr, uint32_t (&r)[4]) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_st4(uint32_t taddr, const uint32_t (&r)[4]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1,%2,%3,%4};"
+                 ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3])
+                 : "memory");
+}
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
+// x = hi + lo with hi rounded to the nearest tf32 value (low 13 mantissa bits zero) and lo the
+// exact fp32 remainder: a kind::tf32 product hi.hi + hi.lo + lo.hi then carries about 21 bits.
+__device__ __forceinline__ void split_tf32(float x, uint32_t &hi, uint32_t &lo) {
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(hi) : "f"(x));
+    lo = __float_as_uint(x - __uint_as_float(hi));
+}
+// Byte offset of fp32 element (row, k) in a K-major 128B-swizzled tile: 32 elements of K per
+// 128-byte row, 8-row groups of 1024 B, successive 32-element K atoms atom_bytes apart.
+__device__ __forceinline__ uint32_t sw128_offset_f32(uint32_t row, uint32_t k, uint32_t atom_bytes) {
+    const uint32_t byte = (k & 31u) * 4u;
+    return (k >> 5) * atom_bytes + (row >> 3) * 1024u + (row & 7u) * 128u +
+           ((((byte >> 4) ^ (row & 7u)) << 4) | (byte & 15u));
+}
 // Byte offset of element (row, col) in a K-major 128B-swizzled bf16 tile whose
 // rows hold 64 elements (one swizzle atom wide); col < 64.
 __device__ __forceinline__ uint32_t sw128_offset(uint32_t row, uint32_t col) {

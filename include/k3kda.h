@@ -328,11 +328,13 @@ int k3kda_decode_status(void *stream);
  *
  *   q, k [T, H, dk], v [T, H, dv]  in_dtype;  g [T, H, dk], beta [T, H], dO [T, H, dv] FP32
  *   cu_seqlens: int32 [N+1] device, cu_seqlens_host: optional host copy (validated when given)
- * Only dk = dv = 128 (UNSUPPORTED otherwise).  FP32 arithmetic on CUDA cores, in chunked form:
- * the chunk algebra of the recurrence (per 16-token chunk) differentiated, with one sequential
- * pass over the chunks for the states and one for the gradients reaching each chunk boundary,
- * and the per-token gradients of every chunk computed in parallel.  dbeta is zeroed and
- * accumulated by the call.  Asynchronous on `stream`; the workspace
+ * Only dk = dv = 128 (UNSUPPORTED otherwise).  FP32-accurate, in chunked form: the chunk algebra
+ * of the recurrence (per 16-token chunk) differentiated, with one sequential pass over the chunks
+ * for the states and one for the gradients reaching each chunk boundary (tensor-core MMAs on
+ * operands split into two tf32 parts, three products each), and the per-token gradients of every
+ * chunk computed in parallel on CUDA cores.  dbeta is zeroed and accumulated by the call.  A
+ * bounded wait for the tensor cores that runs out sets the workspace's status word (see
+ * k3kda_workspace_status).  Asynchronous on `stream`; the workspace
  * (k3kda_backward_workspace_size bytes, 256-byte aligned, caller-owned) is scratch only.
  * Errors: INVALID_ARG, UNSUPPORTED, ALIGNMENT (16 bytes for every array but beta, dbeta: 4),
  * WORKSPACE, CUDA. */
