@@ -84,7 +84,9 @@ extern "C" {
 long long k3kda_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
 // Test hook (see TestTimeout in common.cuh): which = 0 the two-pass prefill's chunk scan, 1 the
-// single-pass prefill, 2 the decode step; tries = how many times the starved wait polls (0 disarms).
+// single-pass prefill, 2 the decode step, 3 the backward's chains (the forward chain of the first
+// (sequence, head) issues no MMA for its first chunk); tries = how many times the starved wait
+// polls (0 disarms).
 // Only for tests on a working GPU: the armed call's outputs are invalid by design.
 int k3kda_test_arm_wait_timeout(int which, unsigned tries) {
     if (which < 0 || which >= kTestKinds) return K3KDA_ERR_INVALID_ARG;

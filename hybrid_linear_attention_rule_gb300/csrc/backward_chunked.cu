@@ -70,6 +70,7 @@ struct CbArgs {
     float *St;                         // [(Q + N) * H][kD][kD]: state at each chunk start, then the final
     float *dq, *dk, *dv, *dg, *dbeta, *dS0;
     unsigned *status;              // the workspace's status word: set when a bounded wait gave up
+    unsigned test_limit;           // 0; else the armed test hook's tries (see TestTimeout)
 };
 
 __device__ __forceinline__ float ld_x(const void *p, size_t i, int bf16) {
@@ -346,16 +347,21 @@ __global__ void __launch_bounds__(kTcThreads, 1) cb_tc_chains_kernel(const __gri
     const uint32_t tl = tbase + ((uint32_t)(32 * lq) << 16);
     uint32_t ph = 0;
     bool pend = false, failed = false;
+    // test hook: the first forward chain issues no MMA for its first chunk and gives up that wait
+    // after the armed number of tries
+    bool starve = A.test_limit != 0 && blockIdx.x == 0;
     // the issuer waits for the MMAs it committed; everyone learns whether the wait ran out
     auto mma_wait = [&]() -> bool {
         if (iss && pend) {
-            if (mbar_wait_bounded(mb, ph, kTcWait)) {
+            if (mbar_wait_bounded(mb, ph, starve ? A.test_limit : kTcWait)) {
                 ph ^= 1u;
                 pend = false;
             } else {
                 *sflag = 1;
                 atomicOr(A.status, 1u);
+                if (starve) pend = false;              // nothing was issued for it
             }
+            starve = false;
         }
         __syncthreads();
         tc_fence_after();
@@ -491,8 +497,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) cb_tc_chains_kernel(const __gri
             // ---- MMA: D = S^T [W_hi; W_lo]^T (N = 32) + S_lo^T W_hi^T (N = 16), over four accumulators ----
             if (iss) {
                 tc_fence_after();
-                issue_over_dk(F_XW + s * 16384);
-                mma_commit(mb);
+                if (!starve) {
+                    issue_over_dk(F_XW + s * 16384);
+                    mma_commit(mb);
+                }
                 pend = true;
             }
             // while it runs: U of this chunk, S_c out, S <- e^{Gamma_L} S, the next chunk's operands
@@ -1002,6 +1010,7 @@ cudaError_t launch_backward_chunked(const void *q, const void *k, const void *v,
     A.Tm = f(l.Tm); A.Aqk = f(l.Aqk); A.Bm = f(l.Bm); A.gl = f(l.gl);
     A.Dl = f(l.Dl); A.dR = f(l.dR); A.Dn = f(l.Dn); A.St = f(l.St);
     A.dq = dq; A.dk = dk; A.dv = dv; A.dg = dg; A.dbeta = dbeta; A.dS0 = dS0; A.status = status;
+    A.test_limit = take_test_timeout(kTestBackward);
     // chunk enumeration from the device cu_seqlens; the item grids cover the upper bound A.Q of
     // the chunk count and CTAs past the real chunks return at once
     cb_offsets_kernel<<<1, 32, 0, s>>>(A);

@@ -75,7 +75,7 @@ void count_launch();
 // count (and disarms it), and its CTA 0 then issues none of the copies its first bounded wait waits
 // for and gives up that wait after the armed number of tries, so the kernel's timeout path runs
 // (status recorded, nothing left in flight, TMEM freed) on a GPU that is working normally.
-enum TestTimeout { kTestScan = 0, kTestSinglePass = 1, kTestDecode = 2, kTestKinds = 3 };
+enum TestTimeout { kTestScan = 0, kTestSinglePass = 1, kTestDecode = 2, kTestBackward = 3, kTestKinds = 4 };
 unsigned take_test_timeout(int which);
 
 // ---- launchers (defined in the kernel files, called by the C ABI layer) ----

@@ -21,7 +21,7 @@ from parity_utils import assert_close, case_to_device, oracle_prefill, to_np
 
 pytestmark = pytest.mark.gpu
 
-SCAN, SINGLE_PASS, DECODE = 0, 1, 2
+SCAN, SINGLE_PASS, DECODE, BACKWARD = 0, 1, 2, 3
 TIMEOUT = -6
 TRIES = 256
 
@@ -99,6 +99,41 @@ def test_decode_wait_runs_out_then_recovers():
     assert_close(to_np(o), ro, False, "decode out after a timed-out call")
     assert_close(to_np(st), rs, False, "decode state after a timed-out call")
     assert np.array_equal(to_np(cs), rcs)
+
+
+def test_backward_chain_wait_runs_out_then_recovers():
+    """The backward's chains: the first forward chain issues no MMA for its first chunk, gives up
+    that wait, and stops; the call reports the timeout through the workspace's status word once,
+    and the next call on the same workspace matches the reverse-mode oracle."""
+    c = KI.prefill_case("timeout_bwd", [150, 40], 2, 128, 128, 64, "bf16", seed=83, s0_std=0.05)
+    unit = lambda x: KI.round_bf16(x / np.linalg.norm(x, axis=-1, keepdims=True))
+    c.q, c.k = unit(c.q), unit(c.k)
+    rng = np.random.default_rng(84)
+    dO = rng.standard_normal((c.T, c.H, 128))
+    dev = lambda x, low=False: torch.from_numpy(np.ascontiguousarray(x)).to(
+        torch.bfloat16 if low else torch.float32).cuda()
+    q, k, v, g, beta, S0, dOd = dev(c.q, 1), dev(c.k, 1), dev(c.v, 1), dev(c.g), dev(c.beta), dev(c.S0), dev(dO)
+    cu_h = torch.from_numpy(c.cu_seqlens.copy())
+    N, T, H = c.N, c.T, c.H
+    ws = torch.zeros(K.k3kda_backward_workspace_size(N, T, H, 128, 128), dtype=torch.uint8, device="cuda")
+    f32 = dict(dtype=torch.float32, device="cuda")
+    outs = [torch.empty(T, H, 128, **f32) for _ in range(4)] + [torch.empty(T, H, **f32), torch.empty(N, H, 128, 128, **f32)]
+
+    def call():
+        K.k3kda_backward(q, k, v, g, beta, S0, cu_h.cuda(), cu_h, N, T, H, 128, 128, c.scale, dOd, None, *outs, ws)
+
+    _arm(BACKWARD)
+    call()
+    assert K.k3kda_workspace_status(ws) == TIMEOUT
+    assert K.k3kda_workspace_status(ws) == 0
+    call()
+    assert K.k3kda_workspace_status(ws) == 0
+    want = O.recurrent_backward(c.q, c.k, c.v, c.g, c.beta, dO, initial_state=c.S0, scale=c.scale,
+                                cu_seqlens=c.cu_seqlens)
+    for name, got in zip(("dq", "dk", "dv", "dg", "dbeta", "dS0"), outs):
+        w = want[name]
+        err = float(np.abs(got.cpu().double().numpy() - w).max())
+        assert err <= 5e-5 * float(np.sqrt((w * w).mean())) + 1e-6, (name, err)
 
 
 def test_disarmed_hook_changes_nothing():
