@@ -773,32 +773,6 @@ struct GradSmem {
 };
 constexpr size_t kGradSmem = sizeof(GradSmem);
 
-// acc[x] += sum_k a1[k] b_x[k] (and a2), k < kD, b_x = row tn + 16 x of b (float4 reads)
-__device__ __forceinline__ void dot4(float (&acc)[4], const float *a, const float (*b)[L4], int tn) {
-#pragma unroll 4
-    for (int k = 0; k < kD; k += 4) {
-        const float4 a4 = *reinterpret_cast<const float4 *>(a + k);
-#pragma unroll
-        for (int x = 0; x < 4; ++x) {
-            const float4 b4 = *reinterpret_cast<const float4 *>(&b[tn + 16 * x][k]);
-            acc[x] = fmaf(a4.x, b4.x, fmaf(a4.y, b4.y, fmaf(a4.z, b4.z, fmaf(a4.w, b4.w, acc[x]))));
-        }
-    }
-}
-__device__ __forceinline__ void dot4x2(float (&acc1)[4], float (&acc2)[4], const float *a1, const float *a2,
-                                       const float (*b)[L4], int tn) {
-#pragma unroll 4
-    for (int k = 0; k < kD; k += 4) {
-        const float4 p = *reinterpret_cast<const float4 *>(a1 + k), q = *reinterpret_cast<const float4 *>(a2 + k);
-#pragma unroll
-        for (int x = 0; x < 4; ++x) {
-            const float4 b4 = *reinterpret_cast<const float4 *>(&b[tn + 16 * x][k]);
-            acc1[x] = fmaf(p.x, b4.x, fmaf(p.y, b4.y, fmaf(p.z, b4.z, fmaf(p.w, b4.w, acc1[x]))));
-            acc2[x] = fmaf(q.x, b4.x, fmaf(q.y, b4.y, fmaf(q.z, b4.z, fmaf(q.w, b4.w, acc2[x]))));
-        }
-    }
-}
-
 __global__ void __launch_bounds__(kThreads, 2) cb_grad_kernel(const __grid_constant__ CbArgs A) {
     extern __shared__ __align__(16) uint8_t dyn[];
     GradSmem &s = *reinterpret_cast<GradSmem *>(dyn);
@@ -870,11 +844,61 @@ __global__ void __launch_bounds__(kThreads, 2) cb_grad_kernel(const __grid_const
     const int i = tid / 16, tn = tid % 16;            // row i, local columns tn + 16 x (x < 4)
     const float bi = s.beta[i];
     float y[4], dos[4], dd[4];
+    {
+        // Y = dR S^T, dO S^T and Delta Dout^T over dv (rows c of S and Dout).  Each thread takes two
+        // rows (ig, ig + 8) and half of dv, so that every S and Dout element it loads feeds two
+        // rows; the two halves of dv meet through shared memory.
+        const int ig = (tid >> 4) & 7, kh = tid >> 7, i0 = ig, i1 = ig + 8;
+        float a[3][2][4];                              // [Y, dO S^T, Delta Dout^T][row][x]
 #pragma unroll
-    for (int x = 0; x < 4; ++x) y[x] = dos[x] = dd[x] = 0.f;
-    // Y = dR S^T, dO S^T and Delta Dout^T over dv (rows c of S and Dout)
-    dot4x2(y, dos, s.dR[i], s.dO[i], s.S, tn);
-    dot4(dd, s.Dl[i], s.Dn, tn);
+        for (int t = 0; t < 3; ++t)
+#pragma unroll
+            for (int r = 0; r < 2; ++r)
+#pragma unroll
+                for (int x = 0; x < 4; ++x) a[t][r][x] = 0.f;
+#pragma unroll 2
+        for (int k = kh * (kD / 2); k < (kh + 1) * (kD / 2); k += 4) {
+            const float4 r0 = *reinterpret_cast<const float4 *>(&s.dR[i0][k]), r1 = *reinterpret_cast<const float4 *>(&s.dR[i1][k]);
+            const float4 o0 = *reinterpret_cast<const float4 *>(&s.dO[i0][k]), o1 = *reinterpret_cast<const float4 *>(&s.dO[i1][k]);
+            const float4 l0 = *reinterpret_cast<const float4 *>(&s.Dl[i0][k]), l1 = *reinterpret_cast<const float4 *>(&s.Dl[i1][k]);
+#pragma unroll
+            for (int x = 0; x < 4; ++x) {
+                const float4 sv = *reinterpret_cast<const float4 *>(&s.S[tn + 16 * x][k]);
+                const float4 nv = *reinterpret_cast<const float4 *>(&s.Dn[tn + 16 * x][k]);
+                a[0][0][x] = fmaf(r0.x, sv.x, fmaf(r0.y, sv.y, fmaf(r0.z, sv.z, fmaf(r0.w, sv.w, a[0][0][x]))));
+                a[0][1][x] = fmaf(r1.x, sv.x, fmaf(r1.y, sv.y, fmaf(r1.z, sv.z, fmaf(r1.w, sv.w, a[0][1][x]))));
+                a[1][0][x] = fmaf(o0.x, sv.x, fmaf(o0.y, sv.y, fmaf(o0.z, sv.z, fmaf(o0.w, sv.w, a[1][0][x]))));
+                a[1][1][x] = fmaf(o1.x, sv.x, fmaf(o1.y, sv.y, fmaf(o1.z, sv.z, fmaf(o1.w, sv.w, a[1][1][x]))));
+                a[2][0][x] = fmaf(l0.x, nv.x, fmaf(l0.y, nv.y, fmaf(l0.z, nv.z, fmaf(l0.w, nv.w, a[2][0][x]))));
+                a[2][1][x] = fmaf(l1.x, nv.x, fmaf(l1.y, nv.y, fmaf(l1.z, nv.z, fmaf(l1.w, nv.w, a[2][1][x]))));
+            }
+        }
+        __syncthreads();                               // S is read: its rows take the sums
+        float (*acc)[kC][kHC] = reinterpret_cast<float (*)[kC][kHC]>(&s.S[0][0]);   // [3][row][column]
+        static_assert(3 * kC * kHC <= kHC * L4, "the sums fit in S");
+        if (kh == 1)
+#pragma unroll
+            for (int t = 0; t < 3; ++t)
+#pragma unroll
+                for (int r = 0; r < 2; ++r)
+#pragma unroll
+                    for (int x = 0; x < 4; ++x) acc[t][ig + 8 * r][tn + 16 * x] = a[t][r][x];
+        __syncthreads();
+        if (kh == 0)
+#pragma unroll
+            for (int t = 0; t < 3; ++t)
+#pragma unroll
+                for (int r = 0; r < 2; ++r)
+#pragma unroll
+                    for (int x = 0; x < 4; ++x) acc[t][ig + 8 * r][tn + 16 * x] += a[t][r][x];
+        __syncthreads();
+#pragma unroll
+        for (int x = 0; x < 4; ++x) {
+            y[x] = acc[0][i][tn + 16 * x];
+            dos[x] = acc[1][i][tn + 16 * x];
+            dd[x] = acc[2][i][tn + 16 * x];
+        }
+    }
     // the pairwise decayed sums P1 .. P4 (K = kC): for m <= i the factor is e^{Gamma_i - Gamma_m},
     // for m >= i it is e^{Gamma_m - Gamma_i}; both are e^{-|Gamma_i - Gamma_m|}
     float gi[4], p1[4], p2[4], p34[4];

@@ -84,6 +84,17 @@ def test_backward_long_sequence_zero_state():
     _compare(got, want, "long")
 
 
+def test_backward_many_chains_in_several_waves():
+    """60 sequences of mixed lengths x 4 heads: 240 (sequence, head) pairs, so the chains' launch
+    (one CTA per pair and chain, one CTA an SM) runs in several waves; bf16 inputs."""
+    lengths = [1 + (37 * i) % 90 for i in range(60)]
+    c, dO, dSf = _case(lengths, 4, seed=63, bf16=True, s0=True)
+    got = _run_gpu(c, dO, dSf)
+    want = O.recurrent_backward(c.q, c.k, c.v, c.g, c.beta, dO, initial_state=c.S0, dS_final=dSf,
+                                cu_seqlens=c.cu_seqlens, scale=c.scale)
+    _compare(got, want, "many chains")
+
+
 @pytest.mark.slow
 def test_backward_full_size_sampled_window():
     """B=1, T=8192, H=32, bf16 inputs: the last 384 tokens of three sampled heads."""
