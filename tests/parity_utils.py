@@ -117,7 +117,7 @@ def assert_close(gpu, ref, fp32, what, store_bf16=False):
     else:
         r = rms(ref)
         tol = BF16_REL * r
-        bad = err > (tol + (2.0 ** -8) * np.abs(ref) if store_bf16 else tol)
+        bad = err > (np.maximum(tol, (2.0 ** -8) * np.abs(ref)) if store_bf16 else tol)
     assert not bad.any(), (f"{what}: max err {err.max():.3e} (tol {tol:.3e}, rms {rms(ref):.3e}); "
                            f"{int(bad.sum())} of {err.size} elements out of tolerance")
     return float(err.max())

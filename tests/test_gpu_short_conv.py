@@ -36,4 +36,4 @@ def test_short_conv_no_state_no_silu_bf16_out():
     torch.cuda.synchronize()
     ry = O.short_conv(x, w, apply_silu=False)
     err = np.abs(to_np(out) - ry)
-    assert (err <= FP32_TOL + 2.0 ** -8 * np.abs(ry)).all()
+    assert (err <= np.maximum(FP32_TOL, 2.0 ** -8 * np.abs(ry))).all()   # one bf16 ulp of the value, if larger
