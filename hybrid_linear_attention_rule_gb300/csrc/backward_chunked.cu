@@ -409,6 +409,27 @@ __global__ void __launch_bounds__(kTcThreads, 1) cb_tc_chains_kernel(const __gri
             tmem_st16(tl + TC_S + 32 * cg + 16 * b, r);
         }
     };
+    // e^{Gamma_L} x (row j's columns) into the fp32 columns, x left as it is
+    auto scale_into_tmem = [&](const float (&x)[32], const float *egl) {
+        uint32_t r[16];
+#pragma unroll
+        for (int b = 0; b < 2; ++b) {
+#pragma unroll
+            for (int u = 0; u < 16; u += 4) {
+                const float4 e4 = *reinterpret_cast<const float4 *>(egl + 32 * cg + 16 * b + u);
+                r[u] = __float_as_uint(x[16 * b + u] * e4.x);
+                r[u + 1] = __float_as_uint(x[16 * b + u + 1] * e4.y);
+                r[u + 2] = __float_as_uint(x[16 * b + u + 2] * e4.z);
+                r[u + 3] = __float_as_uint(x[16 * b + u + 3] * e4.w);
+            }
+            tmem_st16(tl + TC_S + 32 * cg + 16 * b, r);
+        }
+    };
+    // half b of row j's columns of x out to [dk][dv] (the stores are spread over two MMA windows)
+    auto store_half = [&](const float (&x)[32], int b, float *out) {
+#pragma unroll
+        for (int u = 0; u < 16; ++u) out[(size_t)(32 * cg + 16 * b + u) * kD] = x[16 * b + u];
+    };
     // the accumulators' sum over this thread's four tokens [4 cg, 4 cg + 4) (and + 16: the lo rows)
     auto sum_acc4 = [&](float (&d)[4]) {
         uint32_t r[2 * kAcc][4];
@@ -672,7 +693,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) cb_tc_chains_kernel(const __gri
             // while it runs: Dout of this chunk out, Dout <- e^{Gamma_L} Dout, dO of the next
             // chunk, the next chunk's operands
             if (data) {
-                scale_carried(X, reinterpret_cast<const float *>(small(s) + BS_EGL), A.Dn + item * kD * kD + j);
+                scale_into_tmem(X, reinterpret_cast<const float *>(small(s) + BS_EGL));
+                store_half(X, 0, A.Dn + item * kD * kD + j);
                 if (c >= 1) load_do(c - 1, dov);
                 cp_wait<0>();
                 named_bar(1, kTcData);
@@ -727,6 +749,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) cb_tc_chains_kernel(const __gri
                 mma_commit(mb);
                 pend = true;
             }
+            if (data) store_half(X, 1, A.Dn + item * kD * kD + j);   // while it runs
             if (!mma_wait()) { failed = true; break; }
             if (data) {
                 get_carried(X);
