@@ -263,12 +263,13 @@ __device__ __forceinline__ void stage_vec(float *dst, const float *src, int n) {
 // and every product runs as tcgen05 kind::tf32 MMAs on split operands x = hi + lo (hi rounded to
 // tf32, lo the fp32 remainder) summed as hi.hi + hi.lo + lo.hi, which keeps fp32 accuracy:
 //   forward   Delta^T = U^T - S^T W^T            (A = S^T from TMEM, K = dk)
-//             S^T <- e^{Gamma_L} S^T + Delta^T Kd (A = Delta^T from TMEM, K = the chunk's tokens)
-//   backward  dDelta^T = Dout^T Kd^T + dOs^T Aqk (A = Dout^T, then dOs^T, from TMEM)
+//             S^T <- e^{Gamma_L} S^T + Delta^T Kd (A = Delta^T from shared memory, K = the chunk's tokens)
+//   backward  dDelta^T = Dout^T Kd^T + dOs^T Aqk (A = Dout^T from TMEM, then dOs^T from shared memory)
 //             dR^T = dDelta^T Tm                 (CUDA cores: 16 x 16 per dv channel)
-//             Dout^T <- e^{Gamma_L} Dout^T + [dOs | -beta dR]^T [Q0; K0]
+//             Dout^T <- e^{Gamma_L} Dout^T + [dOs | -beta dR]^T [Q0; K0]   (A from shared memory)
 // The B operands are built per chunk from the prep's fp32 tiles into 128-byte-swizzled K-major
-// shared tiles, one chunk ahead, while the MMAs run.
+// shared tiles, one chunk ahead, while the MMAs run; the A operands over the chunk's tokens are
+// written by the threads that own their rows.
 
 constexpr int kTcData = 512;                           // threads that own TMEM rows (16 warps)
 constexpr int kTcThreads = kTcData + 32;               // and a warp whose lane 0 issues the MMAs
