@@ -35,6 +35,16 @@ def test_every_declared_symbol_is_exported(lib):
     assert not missing, f"not exported: {missing}"
 
 
+def test_wait_timeout_hook_takes_the_four_kinds(lib):
+    """The internal test hook (exported for the GPU timeout tests, not in the public header) arms
+    the chunk scan, the single-pass prefill, the decode and the backward's chains, and rejects
+    any other kind; arming with zero tries disarms."""
+    for which in range(4):
+        assert lib.k3kda_test_arm_wait_timeout(which, 0) == 0
+    assert lib.k3kda_test_arm_wait_timeout(4, 1) == -1
+    assert lib.k3kda_test_arm_wait_timeout(-1, 1) == -1
+
+
 def test_version_and_status_strings(lib):
     assert K.k3kda_version() == 1
     assert K.k3kda_status_string(0) == "K3KDA_OK"
