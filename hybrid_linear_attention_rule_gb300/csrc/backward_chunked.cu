@@ -837,14 +837,26 @@ __global__ void __launch_bounds__(kThreads, 2) cb_grad_kernel(const __grid_const
         for (int e = tid; e < kHC * kD / 32; e += kThreads)
             asm volatile("prefetch.global.L2 [%0];" ::"l"(sn + (size_t)e * 32));
     }
-    // this half's columns of q and k, as given (bf16 or fp32)
-    for (int e = tid; e < kC * kHC; e += kThreads) {
-        const int i = e / kHC, c = e % kHC;
-        const size_t src = ((size_t)(t0 + i) * H + h) * kD + cbase + c;
-        s.q[i][c] = i < L ? ld_x(A.q, src, A.bf16) : 0.f;
-        s.k[i][c] = i < L ? ld_x(A.k, src, A.bf16) : 0.f;
+    // this half's columns of q and k, as given (bf16 or fp32): every load issued before the first
+    // store, so that they are in flight together
+    {
+        float qv[kC * kHC / kThreads], kv[kC * kHC / kThreads];
+        const float bv = tid < kC && tid < L ? A.beta[(size_t)(t0 + tid) * H + h] : 0.f;
+#pragma unroll
+        for (int u = 0; u < kC * kHC / kThreads; ++u) {
+            const int e = tid + u * kThreads, i = e / kHC, c = e % kHC;
+            const size_t src = ((size_t)(t0 + i) * H + h) * kD + cbase + c;
+            qv[u] = i < L ? ld_x(A.q, src, A.bf16) : 0.f;
+            kv[u] = i < L ? ld_x(A.k, src, A.bf16) : 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < kC * kHC / kThreads; ++u) {
+            const int e = tid + u * kThreads, i = e / kHC, c = e % kHC;
+            s.q[i][c] = qv[u];
+            s.k[i][c] = kv[u];
+        }
+        if (tid < kC) s.beta[tid] = bv;
     }
-    if (tid < kC) s.beta[tid] = tid < L ? A.beta[(size_t)(t0 + tid) * H + h] : 0.f;
     cp_wait<1>();
     __syncthreads();
     const float scale = A.scale;
@@ -923,6 +935,11 @@ __global__ void __launch_bounds__(kThreads, 2) cb_grad_kernel(const __grid_const
             dd[x] = acc[2][i][tn + 16 * x];
         }
     }
+    // the epilogue's v values, in flight during the pairwise sums
+    const size_t row = ((size_t)(t0 + i) * H + h) * kD;
+    float vv[4];
+#pragma unroll
+    for (int x = 0; x < 4; ++x) vv[x] = i < L ? ld_x(A.v, row + cbase + tn + 16 * x, A.bf16) : 0.f;
     // the pairwise decayed sums P1 .. P4 (K = kC): for m <= i the factor is e^{Gamma_i - Gamma_m},
     // for m >= i it is e^{Gamma_m - Gamma_i}; both are e^{-|Gamma_i - Gamma_m|}
     float gi[4], p1[4], p2[4], p34[4];
@@ -946,15 +963,13 @@ __global__ void __launch_bounds__(kThreads, 2) cb_grad_kernel(const __grid_const
     }
     // dbeta share: rowsum(v o dR) - rowsum(K0 o Y) over this half (+ rowsum(dA o B) once); dv = beta dR
     float pb = 0.f;
-    const size_t row = ((size_t)(t0 + i) * H + h) * kD;
     float dgm[4];
 #pragma unroll
     for (int x = 0; x < 4; ++x) {
         const int c = tn + 16 * x, cg = cbase + c;
         const float ea = __expf(gi[x]), ed = __expf(s.gl[c] - gi[x]);
         const float dr = s.dR[i][cg], kv = s.k[i][c], qv = s.q[i][c];
-        const float vv = i < L ? ld_x(A.v, row + cg, A.bf16) : 0.f;
-        pb += vv * dr - kv * ea * y[x];
+        pb += vv[x] * dr - kv * ea * y[x];
         const float dq = fmaf(scale * dos[x], ea, p1[x]);
         const float dkt = bi * (p2[x] - y[x] * ea);
         const float dkh = fmaf(dd[x], ed, p34[x]);
