@@ -144,8 +144,10 @@ __global__ void __launch_bounds__(kThreads) cb_prep_kernel(const __grid_constant
     __shared__ float sBeta[kC];
     const int tid = threadIdx.x;
     const int item = blockIdx.x, qc = item / A.H, h = item % A.H, H = A.H;
-    if (qc >= A.chunk_off[A.N]) return;                // the grid covers an upper bound of the chunks
-    const int t0 = A.ck_t0[qc], L = A.ck_len[qc];
+    // the grid covers an upper bound of the chunks (the tables have that many entries): the table
+    // reads go out together, before the bound is known
+    const int nq = A.chunk_off[A.N], t0 = A.ck_t0[qc], L = A.ck_len[qc];
+    if (qc >= nq) return;
     for (int e = tid; e < kC * kD; e += kThreads) {
         const int i = e / kD, c = e % kD;
         const size_t src = ((size_t)(t0 + i) * H + h) * kD + c;
@@ -794,6 +796,7 @@ struct GradSmem {
     float q[kC][LH], k[kC][LH], Gm[kC][LH];        // this half's columns
     float dA[kC][LC], dAq[kC][LC], Bm[kC][kC];
     float beta[kC], gl[kHC];
+    float glrow[kHC];                              // rowsum(S_next o Dout) per column of the half
 };
 constexpr size_t kGradSmem = sizeof(GradSmem);
 
@@ -802,11 +805,11 @@ __global__ void __launch_bounds__(kThreads, 2) cb_grad_kernel(const __grid_const
     GradSmem &s = *reinterpret_cast<GradSmem *>(dyn);
     const int tid = threadIdx.x;
     const int half = blockIdx.x & 1, item = blockIdx.x >> 1, qc = item / A.H, h = item % A.H, H = A.H;
-    if (qc >= A.chunk_off[A.N]) return;
-    const int t0 = A.ck_t0[qc], L = A.ck_len[qc];
+    // the table reads go out together, before the bound on the chunks is known (see the prep);
+    // n is the chunk's sequence: its chunk-start state slot is qc + n
+    const int nq = A.chunk_off[A.N], t0 = A.ck_t0[qc], L = A.ck_len[qc], n = A.ck_seq[qc];
+    if (qc >= nq) return;
     const int cbase = half * kHC;
-    // the sequence of this chunk: its chunk-start state slot is qc + n
-    const int n = A.ck_seq[qc];
     const size_t tile = (size_t)item * kC * kD, small = (size_t)item * kC * kC;
     const float *St = A.St + ((size_t)(qc + n) * H + h) * kD * kD + (size_t)cbase * kD;
     const float *Dng = A.Dn + (size_t)item * kD * kD + (size_t)cbase * kD;
@@ -935,6 +938,19 @@ __global__ void __launch_bounds__(kThreads, 2) cb_grad_kernel(const __grid_const
             dd[x] = acc[2][i][tn + 16 * x];
         }
     }
+    if (tid < kHC) {
+        // the chunk's last row also moves the state it hands on: rowsum(S_next o Dout); two warps
+        // form it while the others start on the pairwise sums
+        const float *sn = A.St + ((size_t)(qc + 1 + n) * H + h) * kD * kD + (size_t)(cbase + tid) * kD;
+        float gsum = 0.f;
+#pragma unroll 8
+        for (int j = 0; j < kD; j += 4) {
+            const float4 a4 = *reinterpret_cast<const float4 *>(sn + j);
+            const float4 x4 = *reinterpret_cast<const float4 *>(&s.Dn[tid][j]);
+            gsum = fmaf(a4.x, x4.x, fmaf(a4.y, x4.y, fmaf(a4.z, x4.z, fmaf(a4.w, x4.w, gsum))));
+        }
+        s.glrow[tid] = gsum;
+    }
     // the epilogue's v values, in flight during the pairwise sums
     const size_t row = ((size_t)(t0 + i) * H + h) * kD;
     float vv[4];
@@ -995,17 +1011,8 @@ __global__ void __launch_bounds__(kThreads, 2) cb_grad_kernel(const __grid_const
     }
     __syncthreads();
     if (tid < kHC) {
-        // the chunk's last row also moves the state it hands on: rowsum(S_next o Dout)
         const int cg = cbase + tid;
-        const float *sn = A.St + ((size_t)(qc + 1 + n) * H + h) * kD * kD + (size_t)cg * kD;
-        float gl = 0.f;
-#pragma unroll 4
-        for (int j = 0; j < kD; j += 4) {
-            const float4 a4 = *reinterpret_cast<const float4 *>(sn + j);
-            const float4 x4 = *reinterpret_cast<const float4 *>(&s.Dn[tid][j]);
-            gl = fmaf(a4.x, x4.x, fmaf(a4.y, x4.y, fmaf(a4.z, x4.z, fmaf(a4.w, x4.w, gl))));
-        }
-        dG[L - 1][tid] += gl;
+        dG[L - 1][tid] += s.glrow[tid];
         float run = 0.f;
         for (int ii = L - 1; ii >= 0; --ii) {
             run += dG[ii][tid];
