@@ -71,6 +71,8 @@ struct CbArgs {
     float *dq, *dk, *dv, *dg, *dbeta, *dS0;
     unsigned *status;              // the workspace's status word: set when a bounded wait gave up
     unsigned test_limit;           // 0; else the armed test hook's tries (see TestTimeout)
+    int *ready;                    // [item]: the chains that have written the item's rows (2: both)
+    int *abort;                    // set by a chain that gave up: the grads stop waiting
 };
 
 __device__ __forceinline__ float ld_x(const void *p, size_t i, int bf16) {
@@ -325,8 +327,17 @@ __device__ __forceinline__ void put_split4(uint8_t *hi_tile, uint8_t *lo_tile, u
     *reinterpret_cast<uint4 *>(lo_tile + o) = l;
 }
 
+// One thread marks an item's rows as written by this chain (release: every thread's stores came
+// before the barrier that precedes the call).
+__device__ __forceinline__ void publish_item(int *ready) {
+    __threadfence();
+    asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(ready) : "memory");
+}
+
 __global__ void __launch_bounds__(kTcThreads, 1) cb_tc_chains_kernel(const __grid_constant__ CbArgs A) {
     using namespace tc;
+    // the grads (a programmatic dependent launch) may start on the SMs this grid leaves free
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     extern __shared__ uint8_t smraw[];
     uint8_t *sm = smem_align1024(smraw);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -362,6 +373,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) cb_tc_chains_kernel(const __gri
             } else {
                 *sflag = 1;
                 atomicOr(A.status, 1u);
+                atomicExch(A.abort, 1);                // the grads waiting for this chain's items stop
                 if (starve) pend = false;              // nothing was issued for it
             }
             starve = false;
@@ -578,12 +590,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) cb_tc_chains_kernel(const __gri
             }
             tc_fence_before();
             __syncthreads();
+            // chunk c - 1's rows are all written (its state, its Delta, and the state after it)
+            if (tid == 0 && c >= 1) publish_item(A.ready + (tile / (kC * kD) - H));
         }
         if (!failed && data) {
             float *st = A.St + ((size_t)(q0 + nq + n) * H + h) * kD * kD + j;
 #pragma unroll
             for (int u = 0; u < 32; ++u) st[(size_t)(32 * cg + u) * kD] = X[u];
         }
+        __syncthreads();
+        if (tid == 0 && !failed && nq >= 1) publish_item(A.ready + (size_t)(q0 + nq - 1) * H + h);
     } else {
         // ================= backward chain: Dout, dR; dS0 =================
         const float scale = A.scale;
@@ -765,6 +781,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) cb_tc_chains_kernel(const __gri
             }
             tc_fence_before();
             __syncthreads();
+            if (tid == 0) publish_item(A.ready + item);    // chunk c's Dout and dR rows are written
         }
         if (!failed && data) {
             float *d0 = A.dS0 + (size_t)nh * kD * kD + j;
@@ -799,17 +816,39 @@ struct GradSmem {
     float glrow[kHC];                              // rowsum(S_next o Dout) per column of the half
 };
 constexpr size_t kGradSmem = sizeof(GradSmem);
+constexpr uint32_t kGradWait = 1u << 22;          // polls (each >= 0.25 us) of an item's readiness
 
 __global__ void __launch_bounds__(kThreads, 2) cb_grad_kernel(const __grid_constant__ CbArgs A) {
     extern __shared__ __align__(16) uint8_t dyn[];
     GradSmem &s = *reinterpret_cast<GradSmem *>(dyn);
     const int tid = threadIdx.x;
-    const int half = blockIdx.x & 1, item = blockIdx.x >> 1, qc = item / A.H, h = item % A.H, H = A.H;
-    // the table reads go out together, before the bound on the chunks is known (see the prep);
+    const int half = blockIdx.x & 1, H = A.H, nq = A.chunk_off[A.N];
+    // CTA pairs take the chunks middle-out (rank r: the middle chunk, then one below, one above,
+    // ...): both chains reach the middle first, so the items become ready in about this order
+    const int m = blockIdx.x >> 1, r = m / H, h = m % H;
+    if (r >= nq) return;
+    const int mid = nq >> 1, qc = (r & 1) ? mid - ((r + 1) >> 1) : mid + (r >> 1), item = qc * H + h;
     // n is the chunk's sequence: its chunk-start state slot is qc + n
-    const int nq = A.chunk_off[A.N], t0 = A.ck_t0[qc], L = A.ck_len[qc], n = A.ck_seq[qc];
-    if (qc >= nq) return;
+    const int t0 = A.ck_t0[qc], L = A.ck_len[qc], n = A.ck_seq[qc];
     const int cbase = half * kHC;
+    {
+        // both chains have written the item's rows (bounded wait; a chain that gave up raises abort)
+        __shared__ int go;
+        if (tid == 0) {
+            int ok = 0;
+            for (uint32_t k = 0; k < kGradWait; ++k) {
+                int v;
+                asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(A.ready + item) : "memory");
+                if (v >= 2) { ok = 1; break; }
+                if (*reinterpret_cast<volatile const int *>(A.abort) != 0) break;
+                __nanosleep(256);
+            }
+            if (!ok) atomicOr(A.status, 1u);
+            go = ok;
+        }
+        __syncthreads();
+        if (!go) return;
+    }
     const size_t tile = (size_t)item * kC * kD, small = (size_t)item * kC * kC;
     const float *St = A.St + ((size_t)(qc + n) * H + h) * kD * kD + (size_t)cbase * kD;
     const float *Dng = A.Dn + (size_t)item * kD * kD + (size_t)cbase * kD;
@@ -1024,7 +1063,7 @@ __global__ void __launch_bounds__(kThreads, 2) cb_grad_kernel(const __grid_const
 size_t r256(size_t b) { return (b + 255) & ~size_t(255); }
 
 struct Layout {
-    size_t off_chunk, ck_t0, ck_len, ck_seq, Q0, K0, Kd, Gm, W, U, Tm, Aqk, Bm, gl, Dl, dR, Dn, St, total;
+    size_t off_chunk, ck_t0, ck_len, ck_seq, ready, Q0, K0, Kd, Gm, W, U, Tm, Aqk, Bm, gl, Dl, dR, Dn, St, total;
 };
 
 Layout layout(int N, int T, int H) {
@@ -1037,6 +1076,7 @@ Layout layout(int N, int T, int H) {
     l.ck_t0 = take(Q * 4);
     l.ck_len = take(Q * 4);
     l.ck_seq = take(Q * 4);
+    l.ready = take((NI + 1) * 4);                      // per item, then the abort word
     const size_t tb = NI * kC * kD * 4, sb = NI * kC * kC * 4, vb = NI * kD * 4;
     l.Q0 = take(tb); l.K0 = take(tb); l.Kd = take(tb); l.Gm = take(tb); l.W = take(tb); l.U = take(tb);
     l.Tm = take(sb); l.Aqk = take(sb); l.Bm = take(sb);
@@ -1075,6 +1115,8 @@ cudaError_t launch_backward_chunked(const void *q, const void *k, const void *v,
     A.ck_t0 = reinterpret_cast<int32_t *>(w + l.ck_t0);
     A.ck_len = reinterpret_cast<int32_t *>(w + l.ck_len);
     A.ck_seq = reinterpret_cast<int32_t *>(w + l.ck_seq);
+    A.ready = reinterpret_cast<int *>(w + l.ready);
+    A.abort = A.ready + (size_t)A.Q * H + H;           // past every item of the chunk bound
     auto f = [&](size_t off) { return reinterpret_cast<float *>(w + off); };
     A.Q0 = f(l.Q0); A.K0 = f(l.K0); A.Kd = f(l.Kd); A.Gm = f(l.Gm); A.W = f(l.W); A.U = f(l.U);
     A.Tm = f(l.Tm); A.Aqk = f(l.Aqk); A.Bm = f(l.Bm); A.gl = f(l.gl);
@@ -1093,6 +1135,9 @@ cudaError_t launch_backward_chunked(const void *q, const void *k, const void *v,
     cb_prep_kernel<<<items, kThreads, 0, s>>>(A);
     count_launch();
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    // the readiness flags, the abort word and dbeta (accumulated by the grads) start at zero
+    if ((e = cudaMemsetAsync(A.ready, 0, ((size_t)A.Q * H + H + 1) * sizeof(int), s)) != cudaSuccess) return e;
+    if ((e = cudaMemsetAsync(dbeta, 0, (size_t)T * H * sizeof(float), s)) != cudaSuccess) return e;
     if (chains) {
         if ((e = smem_attr_once((const void *)cb_tc_chains_kernel, (int)kTcSmem, g_chains_attr)) != cudaSuccess)
             return e;
@@ -1101,10 +1146,22 @@ cudaError_t launch_backward_chunked(const void *q, const void *k, const void *v,
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     if ((e = smem_attr_once((const void *)cb_grad_kernel, (int)kGradSmem, g_grad_attr)) != cudaSuccess) return e;
-    if ((e = cudaMemsetAsync(dbeta, 0, (size_t)T * H * sizeof(float), s)) != cudaSuccess) return e;
-    cb_grad_kernel<<<2 * items, kThreads, kGradSmem, s>>>(A);
+    // a programmatic dependent launch: the grads start on the SMs the chains leave free and take
+    // each item as soon as both chains have published it (their flags, not the launch order, carry
+    // the dependency)
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * items);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kGradSmem;
+    cfg.stream = s;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = chains ? 1 : 0;
+    e = cudaLaunchKernelEx(&cfg, cb_grad_kernel, A);
     count_launch();
-    return cudaGetLastError();
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace k3kda

@@ -145,15 +145,15 @@ def test_backward_rejects_bad_arguments(lib):
 def test_backward_workspace_size(lib):
     """The chunked backward's scratch: per (16-token chunk, head) item its fp32 tiles (Q0, K0, Kd,
     Gamma, W, U, Delta, dR: 16 x 128 each; Tm, Aqk, B: 16 x 16; Gamma_L: 128; Dout: 128 x 128),
-    the state at every chunk start and each sequence's end, and the chunk tables (offsets; first
-    token, length and sequence of each chunk); each array starts on a 256-byte boundary after a
-    256-byte status word."""
+    the state at every chunk start and each sequence's end, the chunk tables (offsets; first
+    token, length and sequence of each chunk) and a readiness flag per item plus an abort word;
+    each array starts on a 256-byte boundary after a 256-byte status word."""
     r = lambda b: (b + 255) // 256 * 256
     for N, T, H in ((1, 8192, 32), (3, 1000, 4)):
         Q = (T + 15 * N) // 16 + 1
         NI = Q * H
-        want = 256 + r(4 * (N + 1)) + 3 * r(4 * Q) + 8 * r(NI * 16 * 128 * 4) + 3 * r(NI * 256 * 4) + \
-            r(NI * 128 * 4) + r(NI * 128 * 128 * 4) + r((Q + N) * H * 128 * 128 * 4)
+        want = 256 + r(4 * (N + 1)) + 3 * r(4 * Q) + r(4 * (NI + 1)) + 8 * r(NI * 16 * 128 * 4) + \
+            3 * r(NI * 256 * 4) + r(NI * 128 * 4) + r(NI * 128 * 128 * 4) + r((Q + N) * H * 128 * 128 * 4)
         assert K.k3kda_backward_workspace_size(N, T, H, 128, 128) == want
     assert K.k3kda_backward_workspace_size(1, 8192, 32, 64, 64) == 256
 
