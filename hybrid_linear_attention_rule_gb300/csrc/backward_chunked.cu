@@ -78,6 +78,28 @@ struct CbArgs {
 __device__ __forceinline__ float ld_x(const void *p, size_t i, int bf16) {
     return bf16 ? __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(p)[i]) : reinterpret_cast<const float *>(p)[i];
 }
+// Elements i .. i + 7 of an input (i a multiple of 8; the inputs are 16-byte aligned) in 16-byte
+// pieces, or zeros when !ok.
+__device__ __forceinline__ void ld_x8(const void *p, size_t i, int bf16, bool ok, float (&o)[8]) {
+    if (!ok) {
+#pragma unroll
+        for (int x = 0; x < 8; ++x) o[x] = 0.f;
+    } else if (bf16) {
+        const uint4 r = __ldg(reinterpret_cast<const uint4 *>(reinterpret_cast<const __nv_bfloat16 *>(p) + i));
+        const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+        for (int x = 0; x < 4; ++x) {
+            const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w[x]));
+            o[2 * x] = f.x;
+            o[2 * x + 1] = f.y;
+        }
+    } else {
+        const float4 a = __ldg(reinterpret_cast<const float4 *>(reinterpret_cast<const float *>(p) + i));
+        const float4 b = __ldg(reinterpret_cast<const float4 *>(reinterpret_cast<const float *>(p) + i) + 1);
+        o[0] = a.x; o[1] = a.y; o[2] = a.z; o[3] = a.w;
+        o[4] = b.x; o[5] = b.y; o[6] = b.z; o[7] = b.w;
+    }
+}
 
 // chunk offsets of the sequences (a prefix over N, one thread)
 __global__ void __launch_bounds__(32) cb_offsets_kernel(CbArgs A) {
@@ -140,7 +162,7 @@ __device__ __forceinline__ void zero(float (&acc)[TM][TN]) {
 
 // ---- 1. prep: one CTA per (chunk, head) ---------------------------------------------------------
 
-__global__ void __launch_bounds__(kThreads) cb_prep_kernel(const __grid_constant__ CbArgs A) {
+__global__ void __launch_bounds__(kThreads, 6) cb_prep_kernel(const __grid_constant__ CbArgs A) {
     __shared__ float sG[kC][LD], sQ[kC][LD], sK[kC][LD], sX[kC][LD];
     __shared__ float sB[kC][LC], sT[kC][LC];
     __shared__ float sBeta[kC];
@@ -150,14 +172,34 @@ __global__ void __launch_bounds__(kThreads) cb_prep_kernel(const __grid_constant
     // reads go out together, before the bound is known
     const int nq = A.chunk_off[A.N], t0 = A.ck_t0[qc], L = A.ck_len[qc];
     if (qc >= nq) return;
-    for (int e = tid; e < kC * kD; e += kThreads) {
-        const int i = e / kD, c = e % kD;
-        const size_t src = ((size_t)(t0 + i) * H + h) * kD + c;
-        sG[i][c] = i < L ? A.g[src] : 0.f;
-        sQ[i][c] = i < L ? ld_x(A.q, src, A.bf16) : 0.f;
-        sK[i][c] = i < L ? ld_x(A.k, src, A.bf16) : 0.f;
+    // every load of the chunk's g, q and k rows goes out before the first store (one round trip
+    // instead of one per element): 16-byte pieces, thread tid taking row i8 and channels c8 .. c8 + 7
+    // of q and k (and later v) and two 4-channel pieces of g
+    static_assert(kC * kD == 8 * kThreads, "one 8-channel piece of each row tensor per thread");
+    const int i8 = tid >> 4, c8 = (tid & 15) * 8;
+    const size_t src8 = ((size_t)(t0 + i8) * H + h) * kD + c8;
+    float qv[8], kv[8];
+    ld_x8(A.q, src8, A.bf16, i8 < L, qv);
+    ld_x8(A.k, src8, A.bf16, i8 < L, kv);
+    float4 gv[2];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+        const int e = tid + u * kThreads, i = e >> 5, c = (e & 31) * 4;
+        gv[u] = i < L ? __ldg(reinterpret_cast<const float4 *>(A.g + ((size_t)(t0 + i) * H + h) * kD + c))
+                      : make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    if (tid < kC) sBeta[tid] = tid < L ? A.beta[(size_t)(t0 + tid) * H + h] : 0.f;
+    const float bv = tid < kC && tid < L ? A.beta[(size_t)(t0 + tid) * H + h] : 0.f;
+#pragma unroll
+    for (int x = 0; x < 8; ++x) {
+        sQ[i8][c8 + x] = qv[x];
+        sK[i8][c8 + x] = kv[x];
+    }
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+        const int e = tid + u * kThreads, i = e >> 5, c = (e & 31) * 4;
+        sG[i][c] = gv[u].x; sG[i][c + 1] = gv[u].y; sG[i][c + 2] = gv[u].z; sG[i][c + 3] = gv[u].w;
+    }
+    if (tid < kC) sBeta[tid] = bv;
     __syncthreads();
     if (tid < kD) {
         float run = 0.f;
@@ -211,9 +253,11 @@ __global__ void __launch_bounds__(kThreads) cb_prep_kernel(const __grid_constant
     __syncthreads();
     A.Tm[(size_t)item * kC * kC + tid] = sT[tid / kC][tid % kC];
     // W = Tm diag(beta) K0, U = Tm diag(beta) V (beta V into sG, whose Gamma is no longer needed)
-    for (int e = tid; e < kC * kD; e += kThreads) {
-        const int i = e / kD, c = e % kD;
-        sG[i][c] = i < L ? sBeta[i] * ld_x(A.v, ((size_t)(t0 + i) * H + h) * kD + c, A.bf16) : 0.f;
+    {
+        float vv[8];
+        ld_x8(A.v, src8, A.bf16, i8 < L, vv);
+#pragma unroll
+        for (int x = 0; x < 8; ++x) sG[i8][c8 + x] = sBeta[i8] * vv[x];
     }
     __syncthreads();
     {
