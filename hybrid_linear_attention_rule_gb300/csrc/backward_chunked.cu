@@ -894,6 +894,33 @@ __global__ void __launch_bounds__(kThreads, 2) cb_grad_kernel(const __grid_const
         if (!go) return;
     }
     const size_t tile = (size_t)item * kC * kD, small = (size_t)item * kC * kC;
+    // this half's columns of q and k, as given (bf16 or fp32), 4 channels a thread: loaded first, so
+    // that they do not queue behind the staging copies below, and stored once those are issued
+    static_assert(kC * kHC == 4 * kThreads, "one 4-channel piece of q and of k per thread");
+    const int iq = tid >> 4, cq = (tid & 15) * 4;
+    float qv[4], kv[4];
+    {
+        const size_t src = ((size_t)(t0 + iq) * H + h) * kD + cbase + cq;
+        if (iq >= L) {
+#pragma unroll
+            for (int x = 0; x < 4; ++x) qv[x] = kv[x] = 0.f;
+        } else if (A.bf16) {
+            const uint2 rq = __ldg(reinterpret_cast<const uint2 *>(reinterpret_cast<const __nv_bfloat16 *>(A.q) + src));
+            const uint2 rk = __ldg(reinterpret_cast<const uint2 *>(reinterpret_cast<const __nv_bfloat16 *>(A.k) + src));
+            const float2 q0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&rq.x));
+            const float2 q1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&rq.y));
+            const float2 k0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&rk.x));
+            const float2 k1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&rk.y));
+            qv[0] = q0.x; qv[1] = q0.y; qv[2] = q1.x; qv[3] = q1.y;
+            kv[0] = k0.x; kv[1] = k0.y; kv[2] = k1.x; kv[3] = k1.y;
+        } else {
+            const float4 q4 = __ldg(reinterpret_cast<const float4 *>(reinterpret_cast<const float *>(A.q) + src));
+            const float4 k4 = __ldg(reinterpret_cast<const float4 *>(reinterpret_cast<const float *>(A.k) + src));
+            qv[0] = q4.x; qv[1] = q4.y; qv[2] = q4.z; qv[3] = q4.w;
+            kv[0] = k4.x; kv[1] = k4.y; kv[2] = k4.z; kv[3] = k4.w;
+        }
+    }
+    const float bv = tid < kC && tid < L ? A.beta[(size_t)(t0 + tid) * H + h] : 0.f;
     const float *St = A.St + ((size_t)(qc + n) * H + h) * kD * kD + (size_t)cbase * kD;
     const float *Dng = A.Dn + (size_t)item * kD * kD + (size_t)cbase * kD;
     stage_tile(&s.Dl[0][0], L4, A.Dl + tile);
@@ -923,26 +950,9 @@ __global__ void __launch_bounds__(kThreads, 2) cb_grad_kernel(const __grid_const
         for (int e = tid; e < kHC * kD / 32; e += kThreads)
             asm volatile("prefetch.global.L2 [%0];" ::"l"(sn + (size_t)e * 32));
     }
-    // this half's columns of q and k, as given (bf16 or fp32): every load issued before the first
-    // store, so that they are in flight together
-    {
-        float qv[kC * kHC / kThreads], kv[kC * kHC / kThreads];
-        const float bv = tid < kC && tid < L ? A.beta[(size_t)(t0 + tid) * H + h] : 0.f;
-#pragma unroll
-        for (int u = 0; u < kC * kHC / kThreads; ++u) {
-            const int e = tid + u * kThreads, i = e / kHC, c = e % kHC;
-            const size_t src = ((size_t)(t0 + i) * H + h) * kD + cbase + c;
-            qv[u] = i < L ? ld_x(A.q, src, A.bf16) : 0.f;
-            kv[u] = i < L ? ld_x(A.k, src, A.bf16) : 0.f;
-        }
-#pragma unroll
-        for (int u = 0; u < kC * kHC / kThreads; ++u) {
-            const int e = tid + u * kThreads, i = e / kHC, c = e % kHC;
-            s.q[i][c] = qv[u];
-            s.k[i][c] = kv[u];
-        }
-        if (tid < kC) s.beta[tid] = bv;
-    }
+    *reinterpret_cast<float4 *>(&s.q[iq][cq]) = make_float4(qv[0], qv[1], qv[2], qv[3]);
+    *reinterpret_cast<float4 *>(&s.k[iq][cq]) = make_float4(kv[0], kv[1], kv[2], kv[3]);
+    if (tid < kC) s.beta[tid] = bv;
     cp_wait<1>();
     __syncthreads();
     const float scale = A.scale;
