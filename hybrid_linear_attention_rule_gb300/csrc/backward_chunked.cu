@@ -1031,19 +1031,6 @@ __global__ void __launch_bounds__(kThreads, 2) cb_grad_kernel(const __grid_const
             dd[x] = acc[2][i][tn + 16 * x];
         }
     }
-    if (tid < kHC) {
-        // the chunk's last row also moves the state it hands on: rowsum(S_next o Dout); two warps
-        // form it while the others start on the pairwise sums
-        const float *sn = A.St + ((size_t)(qc + 1 + n) * H + h) * kD * kD + (size_t)(cbase + tid) * kD;
-        float gsum = 0.f;
-#pragma unroll 8
-        for (int j = 0; j < kD; j += 4) {
-            const float4 a4 = *reinterpret_cast<const float4 *>(sn + j);
-            const float4 x4 = *reinterpret_cast<const float4 *>(&s.Dn[tid][j]);
-            gsum = fmaf(a4.x, x4.x, fmaf(a4.y, x4.y, fmaf(a4.z, x4.z, fmaf(a4.w, x4.w, gsum))));
-        }
-        s.glrow[tid] = gsum;
-    }
     // the epilogue's v values, in flight during the pairwise sums
     const size_t row = ((size_t)(t0 + i) * H + h) * kD;
     float vv[4];
@@ -1070,6 +1057,17 @@ __global__ void __launch_bounds__(kThreads, 2) cb_grad_kernel(const __grid_const
             p34[x] = fmaf(aqt, s.q[m][c] * e, fmaf(adt, km, p34[x]));
         }
     }
+    // the chunk's last row also moves the state it hands on: rowsum(S_next o Dout), thread (column
+    // cr, quarter pr of dv) taking 32 products, its rows of S_next loaded here and used after the
+    // epilogue; the quarters start at rotated pieces so that the four threads of a column read
+    // different banks of Dout
+    const int cr = tid >> 2, pr = tid & 3;
+    float4 snv[8];
+    {
+        const float *sn = A.St + ((size_t)(qc + 1 + n) * H + h) * kD * kD + (size_t)(cbase + cr) * kD + 32 * pr;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) snv[u] = __ldg(reinterpret_cast<const float4 *>(sn) + ((u + pr) & 7));
+    }
     // dbeta share: rowsum(v o dR) - rowsum(K0 o Y) over this half (+ rowsum(dA o B) once); dv = beta dR
     float pb = 0.f;
     float dgm[4];
@@ -1092,6 +1090,17 @@ __global__ void __launch_bounds__(kThreads, 2) cb_grad_kernel(const __grid_const
     // sum pb over the row's 16 threads (consecutive lanes of one half-warp)
 #pragma unroll
     for (int o = 8; o > 0; o >>= 1) pb += __shfl_xor_sync(0xffffffffu, pb, o);
+    {
+        float gsum = 0.f;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const float4 x4 = *reinterpret_cast<const float4 *>(&s.Dn[cr][32 * pr + 4 * ((u + pr) & 7)]);
+            gsum = fmaf(snv[u].x, x4.x, fmaf(snv[u].y, x4.y, fmaf(snv[u].z, x4.z, fmaf(snv[u].w, x4.w, gsum))));
+        }
+        gsum += __shfl_xor_sync(0xffffffffu, gsum, 1);
+        gsum += __shfl_xor_sync(0xffffffffu, gsum, 2);
+        if (pr == 0) s.glrow[cr] = gsum;
+    }
     __syncthreads();                                   // S free: dGamma goes there
     float (*dG)[L4] = s.S;
 #pragma unroll
