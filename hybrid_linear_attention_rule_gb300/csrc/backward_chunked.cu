@@ -219,11 +219,28 @@ __global__ void __launch_bounds__(kThreads, 6) cb_prep_kernel(const __grid_const
         sX[i][c] = sBeta[i] * k0;                      // beta K0, the right factor of W
     }
     {
-        // B = strict_lower, Aqk = lower of the decayed products, one element (i, j) per thread, each
-        // term with its own exponential e^{Gamma_ic - Gamma_jc} <= 1 (j <= i)
-        const int i = tid / kC, j = tid % kC;
+        // B = strict_lower, Aqk = lower of the decayed products, each term with its own exponential
+        // e^{Gamma_ic - Gamma_jc} <= 1 (j <= i).  The 136 elements with j <= i go to the first 136
+        // threads (element p of the lower triangle in row order), so that whole warps of the others,
+        // which write the zeros above the diagonal, do not run the loop
+        constexpr int kLow = kC * (kC + 1) / 2;
+        static_assert(kC * kC == kThreads, "one element of the 16 x 16 tiles per thread");
+        int i, j;
+        if (tid < kLow) {                              // p = i (i + 1) / 2 + j, j <= i
+            i = (int)((sqrtf(8.f * tid + 1.f) - 1.f) * 0.5f);
+            if ((i + 1) * (i + 2) / 2 <= tid) ++i;
+            if (i * (i + 1) / 2 > tid) --i;
+            j = tid - i * (i + 1) / 2;
+        } else {                                       // q = a (a - 1) / 2 + b, b < a; element (b, a)
+            const int q = tid - kLow;
+            int a = (int)((sqrtf(8.f * q + 1.f) + 1.f) * 0.5f);
+            if (a * (a - 1) / 2 > q) --a;
+            if ((a + 1) * a / 2 <= q) ++a;
+            i = q - a * (a - 1) / 2;
+            j = a;
+        }
         float b1 = 0.f, b2 = 0.f;
-        if (j <= i) {
+        if (tid < kLow) {
 #pragma unroll 4
             for (int c = 0; c < kD; ++c) {
                 const float t = sK[j][c] * __expf(sG[i][c] - sG[j][c]);
@@ -233,8 +250,8 @@ __global__ void __launch_bounds__(kThreads, 6) cb_prep_kernel(const __grid_const
         }
         const float bv = j < i ? b1 : 0.f, av = j <= i ? b2 : 0.f;
         sB[i][j] = bv;
-        A.Bm[(size_t)item * kC * kC + tid] = bv;
-        A.Aqk[(size_t)item * kC * kC + tid] = av;
+        A.Bm[(size_t)item * kC * kC + i * kC + j] = bv;
+        A.Aqk[(size_t)item * kC * kC + i * kC + j] = av;
     }
     __syncthreads();
     if (tid < kC) {
