@@ -160,6 +160,27 @@ __device__ __forceinline__ void zero(float (&acc)[TM][TN]) {
         for (int u = 0; u < TN; ++u) acc[v][u] = 0.f;
 }
 
+// Element (i, j) of a 16 x 16 tile for thread t: t < 136 takes element t of the lower triangle
+// (j <= i) in row order, the other 120 threads the elements above the diagonal, so that the work on
+// the lower triangle fills whole warps.
+constexpr int kLow = kC * (kC + 1) / 2;
+static_assert(kC * kC == kThreads, "one element of a 16 x 16 tile per thread");
+__device__ __forceinline__ void tri_pair(int t, int &i, int &j) {
+    if (t < kLow) {                                    // t = i (i + 1) / 2 + j, j <= i
+        i = (int)((sqrtf(8.f * t + 1.f) - 1.f) * 0.5f);
+        if ((i + 1) * (i + 2) / 2 <= t) ++i;
+        if (i * (i + 1) / 2 > t) --i;
+        j = t - i * (i + 1) / 2;
+    } else {                                           // q = a (a - 1) / 2 + b, b < a: element (b, a)
+        const int q = t - kLow;
+        int a = (int)((sqrtf(8.f * q + 1.f) + 1.f) * 0.5f);
+        if (a * (a - 1) / 2 > q) --a;
+        if ((a + 1) * a / 2 <= q) ++a;
+        i = q - a * (a - 1) / 2;
+        j = a;
+    }
+}
+
 // ---- 1. prep: one CTA per (chunk, head) ---------------------------------------------------------
 
 __global__ void __launch_bounds__(kThreads, 6) cb_prep_kernel(const __grid_constant__ CbArgs A) {
@@ -220,25 +241,9 @@ __global__ void __launch_bounds__(kThreads, 6) cb_prep_kernel(const __grid_const
     }
     {
         // B = strict_lower, Aqk = lower of the decayed products, each term with its own exponential
-        // e^{Gamma_ic - Gamma_jc} <= 1 (j <= i).  The 136 elements with j <= i go to the first 136
-        // threads (element p of the lower triangle in row order), so that whole warps of the others,
-        // which write the zeros above the diagonal, do not run the loop
-        constexpr int kLow = kC * (kC + 1) / 2;
-        static_assert(kC * kC == kThreads, "one element of the 16 x 16 tiles per thread");
+        // e^{Gamma_ic - Gamma_jc} <= 1 (j <= i): the loop on the lower triangle's threads only
         int i, j;
-        if (tid < kLow) {                              // p = i (i + 1) / 2 + j, j <= i
-            i = (int)((sqrtf(8.f * tid + 1.f) - 1.f) * 0.5f);
-            if ((i + 1) * (i + 2) / 2 <= tid) ++i;
-            if (i * (i + 1) / 2 > tid) --i;
-            j = tid - i * (i + 1) / 2;
-        } else {                                       // q = a (a - 1) / 2 + b, b < a; element (b, a)
-            const int q = tid - kLow;
-            int a = (int)((sqrtf(8.f * q + 1.f) + 1.f) * 0.5f);
-            if (a * (a - 1) / 2 > q) --a;
-            if ((a + 1) * a / 2 <= q) ++a;
-            i = q - a * (a - 1) / 2;
-            j = a;
-        }
+        tri_pair(tid, i, j);
         float b1 = 0.f, b2 = 0.f;
         if (tid < kLow) {
 #pragma unroll 4
@@ -974,11 +979,13 @@ __global__ void __launch_bounds__(kThreads, 2) cb_grad_kernel(const __grid_const
     __syncthreads();
     const float scale = A.scale;
     {
-        // dA = -strict_lower(dR Delta^T), dAqk = lower(dOs Delta^T): one element per thread
-        const int i = tid / kC, j = tid % kC;
+        // dA = -strict_lower(dR Delta^T), dAqk = lower(dOs Delta^T): one element per thread, the
+        // products on the lower triangle's threads only
+        int i, j;
+        tri_pair(tid, i, j);
         float a1 = 0.f, a2 = 0.f;
 #pragma unroll 4
-        for (int k = 0; k < kD; k += 4) {
+        for (int k = 0; k < (tid < kLow ? kD : 0); k += 4) {
             const float4 d4 = *reinterpret_cast<const float4 *>(&s.Dl[j][k]);
             const float4 r4 = *reinterpret_cast<const float4 *>(&s.dR[i][k]);
             const float4 o4 = *reinterpret_cast<const float4 *>(&s.dO[i][k]);
@@ -1061,17 +1068,36 @@ __global__ void __launch_bounds__(kThreads, 2) cb_grad_kernel(const __grid_const
         gi[x] = s.Gm[i][tn + 16 * x];
         p1[x] = p2[x] = p34[x] = 0.f;
     }
-#pragma unroll 4
-    for (int m = 0; m < kC; ++m) {
-        const float aq = s.dAq[i][m], ad = s.dA[i][m], aqt = s.dAq[m][i], adt = s.dA[m][i] * s.beta[m];
+    // dAqk is lower and dA strictly lower, so m < i feeds P1 and P2 only, m > i P3 and P4 only, and
+    // m = i (factor 1) P1 and P3 through dAqk[i][i]
+#pragma unroll 2
+    for (int m = 0; m < i; ++m) {
+        const float aq = s.dAq[i][m], ad = s.dA[i][m];
 #pragma unroll
         for (int x = 0; x < 4; ++x) {
             const int c = tn + 16 * x;
-            const float e = __expf(-fabsf(gi[x] - s.Gm[m][c]));
-            const float km = s.k[m][c] * e;
+            const float km = s.k[m][c] * __expf(gi[x] - s.Gm[m][c]);     // Gamma_i <= Gamma_m: <= 0
             p1[x] = fmaf(aq, km, p1[x]);
             p2[x] = fmaf(ad, km, p2[x]);
-            p34[x] = fmaf(aqt, s.q[m][c] * e, fmaf(adt, km, p34[x]));
+        }
+    }
+    {
+        const float aii = s.dAq[i][i];
+#pragma unroll
+        for (int x = 0; x < 4; ++x) {
+            const int c = tn + 16 * x;
+            p1[x] = fmaf(aii, s.k[i][c], p1[x]);
+            p34[x] = fmaf(aii, s.q[i][c], p34[x]);
+        }
+    }
+#pragma unroll 2
+    for (int m = i + 1; m < kC; ++m) {
+        const float aqt = s.dAq[m][i], adt = s.dA[m][i] * s.beta[m];
+#pragma unroll
+        for (int x = 0; x < 4; ++x) {
+            const int c = tn + 16 * x;
+            const float e = __expf(s.Gm[m][c] - gi[x]);                  // Gamma_m <= Gamma_i: <= 0
+            p34[x] = fmaf(aqt, s.q[m][c] * e, fmaf(adt, s.k[m][c] * e, p34[x]));
         }
     }
     // the chunk's last row also moves the state it hands on: rowsum(S_next o Dout), thread (column
