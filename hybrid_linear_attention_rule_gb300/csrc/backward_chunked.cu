@@ -132,25 +132,6 @@ __global__ void __launch_bounds__(256) cb_chunks_kernel(CbArgs A) {
     A.ck_seq[q] = lo;
 }
 
-// C[m][n] over an M x N tile, thread tile TM x TN with rows m = tm + (M / TM) v and columns
-// n = tn + (N / TN) u; A(m, kk) = a[m * sam + kk * sak], B(kk, n) = b[kk * sbk + n * sbn].
-template <int M, int N, int TM, int TN>
-__device__ __forceinline__ void mm(float (&acc)[TM][TN], const float *a, int sam, int sak, const float *b, int sbk,
-                                   int sbn, int K) {
-    static_assert((M / TM) * (N / TN) == kThreads, "tile shape");
-    const int tn = threadIdx.x % (N / TN), tm = threadIdx.x / (N / TN);
-    for (int kk = 0; kk < K; ++kk) {
-        float av[TM], bv[TN];
-#pragma unroll
-        for (int v = 0; v < TM; ++v) av[v] = a[(tm + (M / TM) * v) * sam + kk * sak];
-#pragma unroll
-        for (int u = 0; u < TN; ++u) bv[u] = b[kk * sbk + (tn + (N / TN) * u) * sbn];
-#pragma unroll
-        for (int v = 0; v < TM; ++v)
-#pragma unroll
-            for (int u = 0; u < TN; ++u) acc[v][u] = fmaf(av[v], bv[u], acc[v][u]);
-    }
-}
 
 template <int TM, int TN>
 __device__ __forceinline__ void zero(float (&acc)[TM][TN]) {
@@ -259,18 +240,21 @@ __global__ void __launch_bounds__(kThreads, 6) cb_prep_kernel(const __grid_const
         A.Aqk[(size_t)item * kC * kC + i * kC + j] = av;
     }
     __syncthreads();
-    if (tid < kC) {
-        // column tid of Tm = (I + diag(beta) B)^-1 by forward substitution
-        float x[kC];
+    {
+        // Tm = (I + diag(beta) B)^-1 by forward substitution, x_i = -beta_i sum_{j<i} B_ij x_j down
+        // column col (x_col = 1, zero above): thread (col, r) holds x_r, and the sum for row i runs
+        // over the column's 16 threads (a half-warp) by shuffles
+        static_assert(kC * kC == kThreads && kC == 16, "one thread per element, a column per half-warp");
+        const int col = tid >> 4, r = tid & 15;
+        float xr = r == col ? 1.f : 0.f;
 #pragma unroll
-        for (int i = 0; i < kC; ++i) {
-            float s = 0.f;
+        for (int i = 1; i < kC; ++i) {
+            float p = r < i ? sB[i][r] * xr : 0.f;
 #pragma unroll
-            for (int j = 0; j < i; ++j) s = fmaf(sB[i][j], x[j], s);
-            x[i] = (i == tid) ? 1.f : (i < tid ? 0.f : -sBeta[i] * s);
+            for (int o = 1; o < 16; o <<= 1) p += __shfl_xor_sync(0xffffffffu, p, o, 16);
+            if (r == i && i > col) xr = -sBeta[i] * p;
         }
-#pragma unroll
-        for (int i = 0; i < kC; ++i) sT[i][tid] = x[i];
+        sT[r][col] = xr;
     }
     __syncthreads();
     A.Tm[(size_t)item * kC * kC + tid] = sT[tid / kC][tid % kC];
@@ -283,11 +267,18 @@ __global__ void __launch_bounds__(kThreads, 6) cb_prep_kernel(const __grid_const
     }
     __syncthreads();
     {
+        // row i of W and U over columns tn + 16 x: Tm is lower triangular, so the sums stop at kk = i
+        const int i = tid / (kD / 8), tn = tid % (kD / 8);
         float w[1][8], u[1][8];
         zero(w); zero(u);
-        mm<kC, kD, 1, 8>(w, &sT[0][0], LC, 1, &sX[0][0], LD, 1, kC);
-        mm<kC, kD, 1, 8>(u, &sT[0][0], LC, 1, &sG[0][0], LD, 1, kC);
-        const int i = tid / (kD / 8), tn = tid % (kD / 8);
+        for (int kk = 0; kk <= i; ++kk) {
+            const float t = sT[i][kk];
+#pragma unroll
+            for (int x = 0; x < 8; ++x) {
+                w[0][x] = fmaf(t, sX[kk][tn + (kD / 8) * x], w[0][x]);
+                u[0][x] = fmaf(t, sG[kk][tn + (kD / 8) * x], u[0][x]);
+            }
+        }
 #pragma unroll
         for (int x = 0; x < 8; ++x) {
             const int c = tn + (kD / 8) * x;
