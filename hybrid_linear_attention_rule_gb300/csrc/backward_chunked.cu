@@ -1100,7 +1100,7 @@ __global__ void __launch_bounds__(kThreads, 2) cb_grad_kernel(const __grid_const
     {
         const float *sn = A.St + ((size_t)(qc + 1 + n) * H + h) * kD * kD + (size_t)(cbase + cr) * kD + 32 * pr;
 #pragma unroll
-        for (int u = 0; u < 8; ++u) snv[u] = __ldg(reinterpret_cast<const float4 *>(sn) + ((u + pr) & 7));
+        for (int u = 0; u < 8; ++u) snv[u] = reinterpret_cast<const float4 *>(sn)[(u + pr) & 7];   // written by the chains: plain loads
     }
     // dbeta share: rowsum(v o dR) - rowsum(K0 o Y) over this half (+ rowsum(dA o B) once); dv = beta dR
     float pb = 0.f;
