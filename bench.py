@@ -632,6 +632,13 @@ def run_e2e(args, K, torch, dev, P, Dc, prefill_call, decode_call, out_p, fs, ou
 
     run(2)
     torch.cuda.synchronize()
+    # the host link's rate on this machine: one step's uploads alone, timed on the copy stream
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(up)
+    upload(0)
+    e1.record(up)
+    torch.cuda.synchronize()
+    h2d_gbs = h2d / (e0.elapsed_time(e1) * 1e-3) / 1e9
     n = max(1, args.e2e_steps)
     barrier()
     t0 = time.perf_counter()
@@ -641,6 +648,7 @@ def run_e2e(args, K, torch, dev, P, Dc, prefill_call, decode_call, out_p, fs, ou
     dt = max_over_ranks([dt], world, dev)[0]
     return {"value": job_value(PREFILL["T"] + DECODE["N"], world, dt), "unit": "tokens/s", "ms_per_step": dt * 1e3,
             "steps": n, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "h2d_gbs": h2d_gbs, "h2d_floor_ms": h2d / h2d_gbs / 1e6,
             "pipelining": "inputs double-buffered: step i+1 uploads during step i's compute and read-back",
             "resident": "conv weights; the decode's recurrent state and conv window (its cache)"}
 
