@@ -852,6 +852,23 @@ __device__ __forceinline__ void scan_body(const ScanArgs &A, const SegPlan *pl, 
             mma_commit(mb_a);
             pend_a = true;
         }
+        // the sigmoid of this chunk's gate logits, while MMA W runs
+        float sg[16];
+        if (gated) {
+            if (tid == 0) {
+                if (!*sflag) wait_gate(c);
+            } else {
+                gate_ready(c);
+            }
+            const uint8_t *gt = sm + ((c & 1) ? Q_G1 : Q_G0);
+#pragma unroll
+            for (int u = 0; u < 16; ++u)
+                sg[u] = sigmoid_fast(__bfloat162float(
+                    *reinterpret_cast<const __nv_bfloat16 *>(gt + (quarter * 16 + u) * (kD * 2) + j * 2)));
+        } else {
+#pragma unroll
+            for (int u = 0; u < 16; ++u) sg[u] = 1.f;
+        }
         // the next chunk's state-pass factors, while the MMAs run (this chunk's pass has read them)
         if (vt >= 0 && more) {
             sFA[vt] = expf(rN);
@@ -898,22 +915,6 @@ __device__ __forceinline__ void scan_body(const ScanArgs &A, const SegPlan *pl, 
                                 dadd(sp == 1 ? dBl : dBh, kk * 2048), id, 1);
             mma_commit(mb_a);
             pend_a = true;
-        }
-        float sg[16];                                    // sigmoid of the gate logits, while the MMAs run
-        if (gated) {
-            if (tid == 0) {
-                if (!*sflag) wait_gate(c);
-            } else {
-                gate_ready(c);
-            }
-            const uint8_t *gt = sm + ((c & 1) ? Q_G1 : Q_G0);
-#pragma unroll
-            for (int u = 0; u < 16; ++u)
-                sg[u] = sigmoid_fast(__bfloat162float(
-                    *reinterpret_cast<const __nv_bfloat16 *>(gt + (quarter * 16 + u) * (kD * 2) + j * 2)));
-        } else {
-#pragma unroll
-            for (int u = 0; u < 16; ++u) sg[u] = 1.f;
         }
         // this chunk's [W; Qh] buffer is free since MMA W: the tile two chunks ahead, and the record
         // three chunks ahead into L2, while MMA O/S runs
