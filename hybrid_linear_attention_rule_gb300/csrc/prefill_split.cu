@@ -570,8 +570,8 @@ __device__ __forceinline__ void tmem_put_split16(uint32_t col_hi, uint32_t col_l
 // spare issuing lanes of the scan: lane 0 of warps 15 and 14
 constexpr int kIssueX = kThreads - 32, kIssueK = kThreads - 64;
 
-// Per chunk: MMA [(W S')^T | (Qh S')^T]; V'^T = U^T - (W S')^T; MMA [O^T | S^T] += V'^T [Aqk^T | Kd]
-// while the gate's sigmoid is taken; then one phase writes this chunk's outputs and runs the next
+// Per chunk: MMA [(W S')^T | (Qh S')^T], while the gate's sigmoid is taken; V'^T = U^T - (W S')^T;
+// MMA [O^T | S^T] += V'^T [Aqk^T | Kd]; then one phase writes this chunk's outputs and runs the next
 // chunk's state pass.  [W; Qh] and the gate rows (both double-buffered, two chunks ahead) and
 // [Aqk^T | Kd] arrive by bulk copies issued as soon as their buffers are free; U^T, rho and
 // G_last are read by the threads that use them, one chunk ahead, into registers.
