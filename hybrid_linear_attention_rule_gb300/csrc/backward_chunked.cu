@@ -880,11 +880,22 @@ __global__ void __launch_bounds__(kThreads, 2) cb_grad_kernel(const __grid_const
     GradSmem &s = *reinterpret_cast<GradSmem *>(dyn);
     const int tid = threadIdx.x;
     const int half = blockIdx.x & 1, H = A.H, nq = A.chunk_off[A.N];
-    // CTA pairs take the chunks middle-out (rank r: the middle chunk, then one below, one above,
-    // ...): both chains reach the middle first, so the items become ready in about this order
+    // CTA pairs take the chunks outwards from where the two chains meet (rank r: that chunk, then one
+    // below, one above, ...), so the items become ready in about this order.  A forward-chain step
+    // is the shorter (about 0.77 of a backward one), so they meet past the middle, near 9/16 of the
+    // chunks; ranks past either end continue on the other side.
     const int m = blockIdx.x >> 1, r = m / H, h = m % H;
     if (r >= nq) return;
-    const int mid = nq >> 1, qc = (r & 1) ? mid - ((r + 1) >> 1) : mid + (r >> 1), item = qc * H + h;
+    const int mid = (int)(((long long)nq * 9) >> 4);
+    int qc = (r & 1) ? mid - ((r + 1) >> 1) : mid + (r >> 1);
+    {
+        // the two sides hold mid (below) and nq - mid (above) chunks: once one side is used up the
+        // remaining ranks go to the other, in order
+        const int lo_n = mid, hi_n = nq - mid;
+        const int two = 2 * (lo_n < hi_n ? lo_n : hi_n);        // ranks that alternate
+        if (r >= two) qc = lo_n < hi_n ? mid + (r - lo_n) : mid - 1 - (r - hi_n);
+    }
+    const int item = qc * H + h;
     // n is the chunk's sequence: its chunk-start state slot is qc + n
     const int t0 = A.ck_t0[qc], L = A.ck_len[qc], n = A.ck_seq[qc];
     const int cbase = half * kHC;
