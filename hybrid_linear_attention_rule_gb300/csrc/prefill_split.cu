@@ -883,16 +883,18 @@ __device__ __forceinline__ void scan_body(const ScanArgs &A, const SegPlan *pl, 
             tmem_ld16(tl + kColD + quarter * 16, r);
             tmem_ld16(tl + kColD + 128 + quarter * 16, r2);
             tmem_wait_ld();
+            // (Qh S')^T's two parts go out at once, read while V' is formed (other columns)
+            uint32_t r3[16], r4[16];
+            tmem_ld16(tl + kColD + 64 + quarter * 16, r3);
+            tmem_ld16(tl + kColO + quarter * 16, r4);
             float v[16];
 #pragma unroll
             for (int u = 0; u < 16; ++u) v[u] = uR[u] - (__uint_as_float(r[u]) + __uint_as_float(r2[u]));
             tmem_put_split16(tl + kColD + quarter * 16, tl + kColD + quarter * 16 + 8, v);
-            tmem_ld16(tl + kColD + 64 + quarter * 16, r);
-            tmem_ld16(tl + kColO + quarter * 16, r2);
             tmem_wait_ld();
 #pragma unroll
-            for (int u = 0; u < 16; ++u) r[u] = __float_as_uint(__uint_as_float(r[u]) + __uint_as_float(r2[u]));
-            tmem_st16(tl + kColO + quarter * 16, r);
+            for (int u = 0; u < 16; ++u) r3[u] = __float_as_uint(__uint_as_float(r3[u]) + __uint_as_float(r4[u]));
+            tmem_st16(tl + kColO + quarter * 16, r3);
             tmem_wait_st();
         }
         if (more) load_u(c + 1);
