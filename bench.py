@@ -656,7 +656,7 @@ def run_e2e(args, K, torch, dev, P, Dc, prefill_call, decode_call, out_p, fs, ou
 # Measured DRAM bytes per call (ncu dram__bytes_read.sum + dram__bytes_write.sum, summed over the
 # call's kernels) of the current kernel versions, or None when not yet captured for a kernel
 # version.  The prefill figure is a T=8192 capture scaled by the tokens processed to T=65536.
-PREFILL_TRAFFIC_PER_LAUNCH = 13.05e9     # segment 0 prep + the cooperative segments launch, 1.631 GB at T=8192 x 8
+PREFILL_TRAFFIC_PER_LAUNCH = 13.02e9     # segment 0 prep + the cooperative segments launch, 1.628 GB at T=8192 x 8
 CHUNKED_TRAFFIC_PER_LAUNCH = None
 VARLEN_TRAFFIC_PER_LAUNCH = None
 DECODE_TRAFFIC_PER_LAUNCH = 1.1028e9
